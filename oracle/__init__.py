@@ -1,0 +1,159 @@
+"""fp64 CPU oracle for the selective scan — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may
+import this package.  The product path (the CUDA library and its Python binding)
+never imports it, and it imports nothing from the product.
+
+The arithmetic lives in ``selscan_oracle.c`` (plain sequential fp64 loops); this
+module only marshals numpy arrays into it.  See that file's header for the passages
+each function follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _configure(lib):
+    """Declare the C signatures on a loaded oracle library."""
+    f32p = ctypes.POINTER(ctypes.c_float)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    i64 = ctypes.c_int64
+    lib.oracle_softplus.argtypes = [ctypes.c_double]
+    lib.oracle_softplus.restype = ctypes.c_double
+    lib.oracle_silu.argtypes = [ctypes.c_double]
+    lib.oracle_silu.restype = ctypes.c_double
+    lib.oracle_ss_fwd_rows.argtypes = [f32p] * 8 + [i64p, i64, f64p, f64p, f64p, i64, i64, i64, i64]
+    lib.oracle_ss_fwd_rows.restype = ctypes.c_int
+    lib.oracle_ss_fwd_chunked.argtypes = [f32p] * 8 + [f64p, f64p, i64, i64, i64, i64, i64]
+    lib.oracle_ss_fwd_chunked.restype = ctypes.c_int
+    lib.oracle_ss_step.argtypes = [f64p] + [f32p] * 8 + [f64p, f64p, i64, i64, i64]
+    lib.oracle_ss_step.restype = ctypes.c_int
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = _configure(ctypes.CDLL(_build.build()))
+    return _lib
+
+
+def _f32(a, shape=None, name="array"):
+    """Return a C-contiguous float32 view/copy (None stays None)."""
+    if a is None:
+        return None
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    if shape is not None and a.shape != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {a.shape}")
+    return a
+
+
+def _ptr(a, ctype):
+    if a is None:
+        return ctypes.POINTER(ctype)()
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def softplus(x: float) -> float:
+    return float(_load().oracle_softplus(float(x)))
+
+
+def silu(x: float) -> float:
+    return float(_load().oracle_silu(float(x)))
+
+
+def ss_fwd(u, delta_raw, delta_bias, A_log, B, C, D, z, rows=None):
+    """Sequential fp64 forward scan.
+
+    Shapes: u, delta_raw, z [batch, L, Dm]; B, C [batch, L, N]; A_log [Dm, N];
+    D, delta_bias [Dm] (or None).  Inputs are taken as float32 values.
+
+    rows=None  -> returns (y [batch, L, Dm], last_state [batch, Dm, N], mag [batch, L, Dm])
+    rows=array -> flat indices b*Dm+d; returns (y [nrows, L], last [nrows, N], mag [nrows, L])
+    """
+    u = _f32(u, name="u")
+    if u.ndim != 3:
+        raise ValueError("u must be [batch, L, Dm]")
+    batch, L, Dm = u.shape
+    A_log = _f32(A_log, name="A_log")
+    N = A_log.shape[1]
+    delta_raw = _f32(delta_raw, (batch, L, Dm), "delta_raw")
+    z = _f32(z, (batch, L, Dm), "z")
+    B = _f32(B, (batch, L, N), "B")
+    C = _f32(C, (batch, L, N), "C")
+    D = _f32(D, (Dm,), "D")
+    delta_bias = _f32(delta_bias, (Dm,), "delta_bias")
+    if rows is None:
+        nrows = batch * Dm
+        rows_arr = None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = rows_arr.size
+    y = np.empty((nrows, L), np.float64)
+    mag = np.empty((nrows, L), np.float64)
+    last = np.empty((nrows, N), np.float64)
+    st = _load().oracle_ss_fwd_rows(
+        _ptr(u, ctypes.c_float), _ptr(delta_raw, ctypes.c_float), _ptr(delta_bias, ctypes.c_float),
+        _ptr(A_log, ctypes.c_float), _ptr(B, ctypes.c_float), _ptr(C, ctypes.c_float),
+        _ptr(D, ctypes.c_float), _ptr(z, ctypes.c_float), _ptr(rows_arr, ctypes.c_int64), nrows,
+        _ptr(y, ctypes.c_double), _ptr(mag, ctypes.c_double), _ptr(last, ctypes.c_double),
+        batch, L, Dm, N)
+    if st != 0:
+        raise RuntimeError(f"oracle_ss_fwd_rows failed with status {st}")
+    if rows is not None:
+        return y, last, mag
+    y = y.reshape(batch, Dm, L).transpose(0, 2, 1)
+    mag = mag.reshape(batch, Dm, L).transpose(0, 2, 1)
+    return np.ascontiguousarray(y), last.reshape(batch, Dm, N), np.ascontiguousarray(mag)
+
+
+def ss_fwd_chunked(u, delta_raw, delta_bias, A_log, B, C, D, z, chunk):
+    """fp64 chunked evaluation with the pair operator and a carry; same returns as
+    ss_fwd(rows=None) minus mag."""
+    u = _f32(u, name="u")
+    batch, L, Dm = u.shape
+    A_log = _f32(A_log, name="A_log")
+    N = A_log.shape[1]
+    args = [u, _f32(delta_raw, (batch, L, Dm)), _f32(delta_bias, (Dm,)), A_log,
+            _f32(B, (batch, L, N)), _f32(C, (batch, L, N)), _f32(D, (Dm,)), _f32(z, (batch, L, Dm))]
+    y = np.empty((batch * Dm, L), np.float64)
+    last = np.empty((batch * Dm, N), np.float64)
+    st = _load().oracle_ss_fwd_chunked(*[_ptr(a, ctypes.c_float) for a in args],
+                                       _ptr(y, ctypes.c_double), _ptr(last, ctypes.c_double),
+                                       batch, L, Dm, N, int(chunk))
+    if st != 0:
+        raise RuntimeError(f"oracle_ss_fwd_chunked failed with status {st}")
+    y = np.ascontiguousarray(y.reshape(batch, Dm, L).transpose(0, 2, 1))
+    return y, last.reshape(batch, Dm, N)
+
+
+def ss_step(state, x, delta_raw, delta_bias, A_log, B, C, D, z):
+    """One decode step in fp64.  state [batch, Dm, N] (any float dtype, not modified);
+    x, delta_raw, z [batch, Dm]; B, C [batch, N].  Returns (y [batch, Dm], new_state, mag)."""
+    st64 = np.array(state, dtype=np.float64, copy=True, order="C")
+    batch, Dm, N = st64.shape
+    x = _f32(x, (batch, Dm), "x")
+    args = [x, _f32(delta_raw, (batch, Dm), "delta_raw"), _f32(delta_bias, (Dm,), "delta_bias"),
+            _f32(A_log, (Dm, N), "A_log"), _f32(B, (batch, N), "B"), _f32(C, (batch, N), "C"),
+            _f32(D, (Dm,), "D"), _f32(z, (batch, Dm), "z")]
+    y = np.empty((batch, Dm), np.float64)
+    mag = np.empty((batch, Dm), np.float64)
+    st = _load().oracle_ss_step(_ptr(st64, ctypes.c_double), *[_ptr(a, ctypes.c_float) for a in args],
+                                _ptr(y, ctypes.c_double), _ptr(mag, ctypes.c_double), batch, Dm, N)
+    if st != 0:
+        raise RuntimeError(f"oracle_ss_step failed with status {st}")
+    return y, st64, mag

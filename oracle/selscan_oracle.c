@@ -1,0 +1,234 @@
+/*
+ * Selective-scan oracle: a plain, slow, sequential fp64 CPU evaluation of the
+ * Mamba selective state-space recurrence and of its single-token decode update.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or call
+ * this file: only the test suite, the smoke check and the CPU-baseline leg of the
+ * benchmark use it.  It shares no code, header, table or helper with the CUDA
+ * library.
+ *
+ * Sources (the web pages this build is specified from):
+ *   [M]  "mamba-metal: Apple Silicon で Mamba を動かす" (createcentury blog #4),
+ *        section "Selective scan の本質" (h_t = Ā_t h_{t-1} + B̄_t u_t, y_t = C_tᵀ h_t,
+ *        Ā_t = exp(Δ_t A)), section "チャンク間 running prefix" (carry combined from
+ *        the left), section "O(L) インクリメンタルデコード" (the per-token update
+ *        h_new = exp(Δ A_s) h + Δ x B_s, y = Σ_s h_new C_s + D x, then the z gate).
+ *   [K]  the same blog's walkthrough of the official CUDA forward kernel (title lost
+ *        in the feed extraction), section "なぜ「scan」か" (the pair a_i = exp(Δ A),
+ *        b_i = Δ B u, and the associative operator), section "1チャンク内の処理フロー"
+ *        (softplus on Δ, out = D·u, out += h·C per state, out *= z·sigmoid(z)).
+ *   [S]  SpeechLens docs/kernel-optimization.md, MetalSelectiveScan section (tensor
+ *        contract: A_log [D,N], B,C [B,L,N], delta_raw,u,z [B,L,D], D [D]; the kernel
+ *        takes raw A_log and applies -exp(A_log); softplus log(1+exp(x)) on delta_raw).
+ *
+ * Readings where the pages are silent (each is listed in the design doc):
+ *   - B̄ is the Euler form b = Δ·B·u ([K] writes the pair's second element as Δ B u).
+ *   - delta_bias (per channel, NULL = 0) is added to delta_raw before softplus.
+ *   - softplus(x) = max(x,0) + log1p(exp(-|x|)), the exact overflow-free form.
+ *   - h_{-1} = 0; the D skip is added before the gate; silu(z) = z / (1 + exp(-z)).
+ *   - B and C are shared by all channels of a batch row: [B,L,N]; last_state is [B,D,N].
+ *
+ * Layouts (all contiguous, row-major): u, delta_raw, z : [batch, L, Dm];
+ * B, C : [batch, L, N]; A_log : [Dm, N]; D, delta_bias : [Dm].
+ * Inputs arrive as float (the exact values the GPU path consumes); every
+ * arithmetic step is done in double.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL 1
+#define ORACLE_ENOMEM 2
+
+/* softplus: the stable closed form of log(1 + exp(x)) ([S] MetalSelectiveScan; [K] step 2). */
+double oracle_softplus(double x) { return fmax(x, 0.0) + log1p(exp(-fabs(x))); }
+
+/* silu(z) = z * sigmoid(z) ([K] step 6: out *= z * sigmoid(z)). */
+double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
+
+/*
+ * Sequential forward recurrence for a list of (batch, channel) rows.
+ *   rows[r] = b * Dm + d  (NULL: every row, in that order)
+ * Outputs (any may be NULL):
+ *   y_rows    [nrows, L]  y[b, t, d]
+ *   mag_rows  [nrows, L]  |silu(z)| * (sum_n |C_n h_t[n]| + |D u_t|): the size of the
+ *                          terms that make up y, used as the denominator of the
+ *                          condition-aware relative error
+ *   last_rows [nrows, N]  h_{L-1}[n]
+ * Per row, for t = 0..L-1 ([M] "Selective scan の本質", [K] "1チャンク内の処理フロー"):
+ *   Δ_t     = softplus(delta_raw[b,t,d] + bias[d])
+ *   h_t[n]  = exp(Δ_t · A_n) · h_{t-1}[n] + Δ_t · B[b,t,n] · u[b,t,d],  A_n = -exp(A_log[d,n])
+ *   ŷ_t     = Σ_n C[b,t,n] · h_t[n] + D[d] · u[b,t,d]
+ *   y[b,t,d]= ŷ_t · silu(z[b,t,d])   (ŷ_t when z is NULL)
+ */
+int oracle_ss_fwd_rows(const float* u, const float* delta_raw, const float* delta_bias,
+                       const float* A_log, const float* B, const float* C, const float* D,
+                       const float* z, const int64_t* rows, int64_t nrows,
+                       double* y_rows, double* mag_rows, double* last_rows,
+                       int64_t batch, int64_t L, int64_t Dm, int64_t N)
+{
+    if (batch < 0 || L < 0 || Dm < 0 || N < 1) return ORACLE_EINVAL;
+    if (!u || !delta_raw || !A_log || !B || !C) return ORACLE_EINVAL;
+    if (rows == NULL) nrows = batch * Dm;
+    int status = ORACLE_OK;
+
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t row = rows ? rows[r] : r;
+        if (row < 0 || row >= batch * Dm) {
+#pragma omp atomic write
+            status = ORACLE_EINVAL;
+            continue;
+        }
+        const int64_t b = row / Dm, d = row % Dm;
+        double* h = (double*)calloc((size_t)N, sizeof(double));
+        double* A = (double*)malloc((size_t)N * sizeof(double));
+        if (!h || !A) {
+            free(h);
+            free(A);
+#pragma omp atomic write
+            status = ORACLE_ENOMEM;
+            continue;
+        }
+        for (int64_t n = 0; n < N; ++n) A[n] = -exp((double)A_log[d * N + n]);
+        const double bias = delta_bias ? (double)delta_bias[d] : 0.0;
+        const double Dd = D ? (double)D[d] : 0.0;
+
+        for (int64_t t = 0; t < L; ++t) {
+            const int64_t io = (b * L + t) * Dm + d;   /* [b, t, d] */
+            const int64_t ib = (b * L + t) * N;        /* [b, t, 0] */
+            const double ut = (double)u[io];
+            const double delta = oracle_softplus((double)delta_raw[io] + bias);
+            double acc = 0.0, acc_abs = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                h[n] = exp(delta * A[n]) * h[n] + delta * (double)B[ib + n] * ut;
+                const double ch = (double)C[ib + n] * h[n];
+                acc += ch;
+                acc_abs += fabs(ch);
+            }
+            const double skip = Dd * ut;
+            const double gate = z ? oracle_silu((double)z[io]) : 1.0;
+            if (y_rows) y_rows[r * L + t] = (acc + skip) * gate;
+            if (mag_rows) mag_rows[r * L + t] = fabs(gate) * (acc_abs + fabs(skip));
+        }
+        if (last_rows)
+            for (int64_t n = 0; n < N; ++n) last_rows[r * N + n] = h[n];
+        free(h);
+        free(A);
+    }
+    return status;
+}
+
+/*
+ * The same forward result reached the way the scan method reaches it, in fp64:
+ * per (row, state) the sequence is cut into chunks of `chunk` steps; inside a chunk
+ * the pairs (a_t, b_t) = (exp(Δ_t A_n), Δ_t B_t,n u_t) are combined left to right with
+ * the associative operator (a2,b2)∘(a1,b1) = (a2 a1, a2 b1 + b2) ([M] "Selective scan
+ * の本質"; [K] "なぜ「scan」か"), and each chunk's running pair is applied to the carry
+ * from the previous chunk, the carry being the state at the chunk's end ([M]
+ * "チャンク間 running prefix").  It exists to check the oracle against itself:
+ * any chunk length must give the sequential result up to rounding.
+ * Output layout as oracle_ss_fwd_rows (all rows, natural order).
+ */
+int oracle_ss_fwd_chunked(const float* u, const float* delta_raw, const float* delta_bias,
+                          const float* A_log, const float* B, const float* C, const float* D,
+                          const float* z, double* y_rows, double* last_rows,
+                          int64_t batch, int64_t L, int64_t Dm, int64_t N, int64_t chunk)
+{
+    if (batch < 0 || L < 0 || Dm < 0 || N < 1 || chunk < 1) return ORACLE_EINVAL;
+    const int64_t nrows = batch * Dm;
+    int status = ORACLE_OK;
+
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t row = 0; row < nrows; ++row) {
+        const int64_t b = row / Dm, d = row % Dm;
+        const double bias = delta_bias ? (double)delta_bias[d] : 0.0;
+        const double Dd = D ? (double)D[d] : 0.0;
+        double* pre = (double*)calloc((size_t)(L > 0 ? L : 1), sizeof(double));
+        if (!pre) {
+#pragma omp atomic write
+            status = ORACLE_ENOMEM;
+            continue;
+        }
+        for (int64_t n = 0; n < N; ++n) {
+            const double An = -exp((double)A_log[d * N + n]);
+            double carry = 0.0;                       /* state before the chunk */
+            for (int64_t t0 = 0; t0 < L; t0 += chunk) {
+                const int64_t t1 = (t0 + chunk < L) ? t0 + chunk : L;
+                double run_a = 1.0, run_b = 0.0;      /* identity pair */
+                for (int64_t t = t0; t < t1; ++t) {
+                    const int64_t io = (b * L + t) * Dm + d;
+                    const double delta = oracle_softplus((double)delta_raw[io] + bias);
+                    const double a = exp(delta * An);
+                    const double bb = delta * (double)B[(b * L + t) * N + n] * (double)u[io];
+                    /* (a, bb) ∘ (run_a, run_b) */
+                    run_b = a * run_b + bb;
+                    run_a = a * run_a;
+                    /* (run_a, run_b) ∘ (1, carry): the state at t */
+                    const double h = run_a * carry + run_b;
+                    pre[t] += (double)C[(b * L + t) * N + n] * h;
+                }
+                carry = run_a * carry + run_b;
+            }
+            if (last_rows) last_rows[row * N + n] = carry;
+        }
+        for (int64_t t = 0; t < L; ++t) {
+            const int64_t io = (b * L + t) * Dm + d;
+            const double gate = z ? oracle_silu((double)z[io]) : 1.0;
+            if (y_rows) y_rows[row * L + t] = (pre[t] + Dd * (double)u[io]) * gate;
+        }
+        free(pre);
+    }
+    return status;
+}
+
+/*
+ * Single-token decode update ([M] "O(L) インクリメンタルデコード"):
+ *   Δ        = softplus(delta_raw[b,d] + bias[d])
+ *   h[b,d,n] ← exp(Δ · A_n) · h[b,d,n] + Δ · x[b,d] · B[b,n]
+ *   y[b,d]   = (Σ_n C[b,n] · h[b,d,n] + D[d] · x[b,d]) · silu(z[b,d])
+ * state [batch, Dm, N] is read and overwritten in place (double).
+ * x, delta_raw, z : [batch, Dm];  B, C : [batch, N].
+ */
+int oracle_ss_step(double* state, const float* x, const float* delta_raw,
+                   const float* delta_bias, const float* A_log, const float* B,
+                   const float* C, const float* D, const float* z,
+                   double* y, double* mag, int64_t batch, int64_t Dm, int64_t N)
+{
+    if (batch < 0 || Dm < 0 || N < 1) return ORACLE_EINVAL;
+    if (!state || !x || !delta_raw || !A_log || !B || !C) return ORACLE_EINVAL;
+
+#pragma omp parallel for schedule(static)
+    for (int64_t row = 0; row < batch * Dm; ++row) {
+        const int64_t b = row / Dm, d = row % Dm;
+        const double xt = (double)x[row];
+        const double delta =
+            oracle_softplus((double)delta_raw[row] + (delta_bias ? (double)delta_bias[d] : 0.0));
+        double acc = 0.0, acc_abs = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            const double An = -exp((double)A_log[d * N + n]);
+            double* h = &state[row * N + n];
+            *h = exp(delta * An) * (*h) + delta * xt * (double)B[b * N + n];
+            const double ch = (double)C[b * N + n] * (*h);
+            acc += ch;
+            acc_abs += fabs(ch);
+        }
+        const double skip = (D ? (double)D[d] : 0.0) * xt;
+        const double gate = z ? oracle_silu((double)z[row]) : 1.0;
+        if (y) y[row] = (acc + skip) * gate;
+        if (mag) mag[row] = fabs(gate) * (acc_abs + fabs(skip));
+    }
+    return ORACLE_OK;
+}
+
+/* Threads the OpenMP runtime will use (1 when built without OpenMP). */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,104 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check that the
+pins in test_oracle_pins.py reject every one of them.  The real oracle source is
+never modified: each mutant is compiled from a patched copy in a temporary folder."""
+import ctypes
+import importlib.util
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "selscan_oracle.c")
+
+# (name, original text, replacement): each original must occur in the source.
+MUTANTS = [
+    ("drop_D_skip", "const double skip = Dd * ut;", "const double skip = 0.0 * ut;"),
+    ("A_sign_flipped", "A[n] = -exp((double)A_log[d * N + n]);", "A[n] = exp((double)A_log[d * N + n]);"),
+    ("A_log_transposed", "A[n] = -exp((double)A_log[d * N + n]);",
+     "A[n] = -exp((double)A_log[(n % Dm) * N + (d % N)]);"),
+    ("b_without_delta", "h[n] = exp(delta * A[n]) * h[n] + delta * (double)B[ib + n] * ut;",
+     "h[n] = exp(delta * A[n]) * h[n] + (double)B[ib + n] * ut;"),
+    ("decay_without_delta", "h[n] = exp(delta * A[n]) * h[n] + delta * (double)B[ib + n] * ut;",
+     "h[n] = exp(A[n]) * h[n] + delta * (double)B[ib + n] * ut;"),
+    ("state_not_carried", "h[n] = exp(delta * A[n]) * h[n] + delta * (double)B[ib + n] * ut;",
+     "h[n] = exp(delta * A[n]) * 0.0 + delta * (double)B[ib + n] * ut;"),
+    ("bias_after_softplus", "oracle_softplus((double)delta_raw[io] + bias)",
+     "(oracle_softplus((double)delta_raw[io]) + bias)"),
+    ("skip_after_gate", "y_rows[r * L + t] = (acc + skip) * gate;", "y_rows[r * L + t] = acc * gate + skip;"),
+    ("gate_is_sigmoid", "return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
+    ("softplus_without_log", "return fmax(x, 0.0) + log1p(exp(-fabs(x)));",
+     "return fmax(x, 0.0) + exp(-fabs(x));"),
+    ("B_from_previous_step", "const int64_t ib = (b * L + t) * N;",
+     "const int64_t ib = (b * L + (t > 0 ? t - 1 : t)) * N;"),
+    ("C_replaced_by_B", "const double ch = (double)C[ib + n] * h[n];",
+     "const double ch = (double)B[ib + n] * h[n];"),
+    ("u_wrong_channel", "const double ut = (double)u[io];",
+     "const double ut = (double)u[(b * L + t) * Dm + (Dm - 1 - d)];"),
+    ("step_without_decay", "*h = exp(delta * An) * (*h) + delta * xt * (double)B[b * N + n];",
+     "*h = (*h) + delta * xt * (double)B[b * N + n];"),
+    ("step_bias_dropped",
+     "oracle_softplus((double)delta_raw[row] + (delta_bias ? (double)delta_bias[d] : 0.0))",
+     "oracle_softplus((double)delta_raw[row])"),
+]
+
+
+def _load_by_path(name, path, search=None):
+    spec = importlib.util.spec_from_file_location(name, path, submodule_search_locations=search)
+    mod = importlib.util.module_from_spec(spec)
+    sys.modules[name] = mod
+    spec.loader.exec_module(mod)
+    return mod
+
+
+@pytest.fixture(scope="module")
+def harness():
+    pins = _load_by_path("_oracle_pins_for_mutants", os.path.join(ROOT, "tests", "test_oracle_pins.py"))
+    mod = _load_by_path("_oracle_mutant_pkg", os.path.join(ROOT, "oracle", "__init__.py"),
+                        [os.path.join(ROOT, "oracle")])
+    battery = [
+        pins.test_A_to_zero_is_cumulative_sum,
+        pins.test_constant_inputs_geometric_series,
+        pins.test_unrolled_sum_form,
+        pins.test_skip_only_when_B_or_C_is_zero,
+        pins.test_hand_worked_example,
+        pins.test_single_step_by_hand,
+        pins.test_decode_iterated_equals_forward,
+        pins.test_prefix_then_decode_equals_forward,
+        pins.test_channel_permutation_and_batch_independence,
+        pins.test_linear_in_u_without_gate,
+        lambda m: pins.test_chunked_scan_equals_sequential(m, 3),
+        pins.test_softplus_textbook,
+        pins.test_silu_textbook,
+    ]
+    return mod, battery
+
+
+def test_unmutated_copy_passes(harness, tmp_path):
+    mod, battery = harness
+    lib = tmp_path / "orig.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", SRC, "-o", str(lib), "-lm"], check=True)
+    mod._lib = mod._configure(ctypes.CDLL(str(lib)))
+    for pin in battery:
+        pin(mod)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(harness, tmp_path, name, old, new):
+    mod, battery = harness
+    text = open(SRC).read()
+    assert old in text, f"mutation site for {name} not found"
+    src = tmp_path / f"{name}.c"
+    src.write_text(text.replace(old, new, 1))
+    lib = tmp_path / f"{name}.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", str(src), "-o", str(lib), "-lm"],
+                   check=True)
+    mod._lib = mod._configure(ctypes.CDLL(str(lib)))
+    failures = 0
+    for pin in battery:
+        try:
+            pin(mod)
+        except AssertionError:
+            failures += 1
+    assert failures > 0, f"no pin rejects the planted mistake {name}"

@@ -1,0 +1,314 @@
+"""Pins for the fp64 oracle: each test checks it against something other than itself
+(closed forms, textbook routines, a hand-derived example, exact-rational brute force,
+high-precision arithmetic, invariants).  CPU only."""
+import itertools
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+from scipy.special import expit
+
+from selective_state_space_scan_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _softplus_np(x):
+    return np.logaddexp(0.0, x)  # library routine: log(exp(0) + exp(x))
+
+
+def _rand_inputs(seed, batch, L, Dm, N, dist="mamba", **kw):
+    w = synth.fwd_inputs(batch, L, Dm, N, seed=seed, dist=dist, **kw)
+    return w.arrays
+
+
+def _call(oracle_mod, a, **kw):
+    return oracle_mod.ss_fwd(a["u"], a["delta_raw"], a["delta_bias"], a["A_log"], a["B"], a["C"],
+                             a["D"], a["z"], **kw)
+
+
+# ---------------------------------------------------------------- textbook functions
+
+def test_softplus_textbook(oracle_mod):
+    assert oracle_mod.softplus(0.0) == pytest.approx(math.log(2.0), rel=0, abs=1e-16)
+    xs = np.concatenate([np.linspace(-60, 60, 2401), [-745.0, -200.0, 200.0, 1000.0]])
+    got = np.array([oracle_mod.softplus(x) for x in xs])
+    np.testing.assert_allclose(got, _softplus_np(xs), rtol=2e-16 * 8, atol=0)
+    assert oracle_mod.softplus(1000.0) == 1000.0
+    assert oracle_mod.softplus(-1000.0) == 0.0
+
+
+def test_silu_textbook(oracle_mod):
+    xs = np.linspace(-40, 40, 1601)
+    got = np.array([oracle_mod.silu(x) for x in xs])
+    np.testing.assert_allclose(got, xs * expit(xs), rtol=1e-15, atol=1e-300)
+    assert oracle_mod.silu(0.0) == 0.0
+
+
+# ---------------------------------------------------------------- closed forms
+
+def test_A_to_zero_is_cumulative_sum(oracle_mod):
+    """A_log = -40 makes A = -exp(-40); exp(Δ·A) rounds to 1 in fp64, so the state is the
+    running sum of Δ_s B_s u_s and y_t = silu(z_t)(Σ_n C_tn Σ_{s<=t} Δ_s B_sn u_s + D u_t)."""
+    a = _rand_inputs(11, batch=2, L=37, Dm=5, N=3)
+    a["A_log"] = np.full_like(a["A_log"], -40.0)
+    y, last, _ = _call(oracle_mod, a)
+    u = a["u"].astype(np.float64)
+    dlt = _softplus_np(a["delta_raw"].astype(np.float64) + a["delta_bias"][None, None, :])
+    Bm = a["B"].astype(np.float64)
+    Cm = a["C"].astype(np.float64)
+    # h[b,t,d,n] = cumsum over t of Δ[b,t,d] * B[b,t,n] * u[b,t,d]
+    incr = (dlt * u)[..., None] * Bm[:, :, None, :]
+    h = np.cumsum(incr, axis=1)
+    pre = np.einsum("btn,btdn->btd", Cm, h) + a["D"][None, None, :] * u
+    z = a["z"].astype(np.float64)
+    y_ref = pre * z * expit(z)
+    np.testing.assert_allclose(y, y_ref, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(last, h[:, -1], rtol=1e-12, atol=1e-13)
+
+
+def test_constant_inputs_geometric_series(oracle_mod):
+    """Constant Δ, B, u, C and no gate: h_t[n] = ΔBu(1 - a_n^{t+1})/(1 - a_n), a_n = exp(Δ A_n)."""
+    batch, L, Dm, N = 1, 300, 2, 4
+    u = np.full((batch, L, Dm), 0.75, np.float32)
+    dr = np.full((batch, L, Dm), -1.5, np.float32)
+    Bm = np.full((batch, L, N), 1.25, np.float32)
+    Cm = np.full((batch, L, N), -0.5, np.float32)
+    A_log = np.tile(np.log(np.arange(1, N + 1)).astype(np.float32), (Dm, 1))
+    y, last, _ = oracle_mod.ss_fwd(u, dr, None, A_log, Bm, Cm, None, None)
+    dlt = float(_softplus_np(-1.5))
+    A = -np.exp(A_log[0].astype(np.float64))
+    a = np.exp(dlt * A)
+    t = np.arange(L)[:, None]
+    h = dlt * 1.25 * 0.75 * (1 - a[None, :] ** (t + 1)) / (1 - a[None, :])
+    y_ref = (-0.5 * h).sum(axis=1)
+    for d in range(Dm):
+        np.testing.assert_allclose(y[0, :, d], y_ref, rtol=1e-13, atol=0)
+        np.testing.assert_allclose(last[0, d], h[-1], rtol=1e-13, atol=0)
+
+
+def test_unrolled_sum_form(oracle_mod):
+    """The recurrence unrolled: h_t[n] = Σ_{s<=t} exp(A_n (S_t - S_s)) Δ_s B_sn u_s with
+    S_t = Σ_{r<=t} Δ_r.  Written as an O(L^2) double sum, independent of the loop order."""
+    a = _rand_inputs(5, batch=2, L=23, Dm=3, N=5, dist="tiny")
+    a["A_log"] = (a["A_log"] + np.linspace(-1.0, 0.5, 3, dtype=np.float32)[:, None]).astype(np.float32)
+    y, last, _ = _call(oracle_mod, a)
+    u = a["u"].astype(np.float64)
+    dlt = _softplus_np(a["delta_raw"].astype(np.float64) + a["delta_bias"][None, None, :])
+    A = -np.exp(a["A_log"].astype(np.float64))          # [Dm, N]
+    S = np.cumsum(dlt, axis=1)                           # [b, t, d]
+    L = u.shape[1]
+    h = np.zeros(u.shape + (A.shape[1],))
+    for t in range(L):
+        for s in range(t + 1):
+            decay = np.exp(A[None, :, :] * (S[:, t, :] - S[:, s, :])[:, :, None])
+            h[:, t] += decay * (dlt[:, s, :] * u[:, s, :])[:, :, None] * a["B"][:, s, None, :]
+    pre = np.einsum("btn,btdn->btd", a["C"].astype(np.float64), h) + a["D"] * u
+    z = a["z"].astype(np.float64)
+    np.testing.assert_allclose(y, pre * z * expit(z), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(last, h[:, -1], rtol=1e-11, atol=1e-12)
+
+
+def test_skip_only_when_B_or_C_is_zero(oracle_mod):
+    a = _rand_inputs(3, batch=2, L=17, Dm=4, N=4)
+    z = a["z"].astype(np.float64)
+    expect = a["D"] * a["u"].astype(np.float64) * z * expit(z)
+    for key in ("B", "C"):
+        b = dict(a)
+        b[key] = np.zeros_like(a[key])
+        y, last, _ = _call(oracle_mod, b)
+        np.testing.assert_allclose(y, expect, rtol=1e-15, atol=0)
+        if key == "B":
+            assert np.all(last == 0.0)
+        else:
+            assert np.any(last != 0.0)
+
+
+def test_hand_worked_example(oracle_mod):
+    g = json.load(open(os.path.join(GOLDEN, "hand_n1_l4.json")))
+    sh3 = (g["batch"], g["L"], g["Dm"])
+    shn = (g["batch"], g["L"], g["N"])
+    y, last, _ = oracle_mod.ss_fwd(
+        np.array(g["u"], np.float32).reshape(sh3), np.array(g["delta_raw"], np.float32).reshape(sh3),
+        None, np.array(g["A_log"], np.float32), np.array(g["B"], np.float32).reshape(shn),
+        np.array(g["C"], np.float32).reshape(shn), np.array(g["D"], np.float32),
+        np.array(g["z"], np.float32).reshape(sh3))
+    ln2 = math.log(2.0)
+    expect = (np.array(g["y_ln2_coeff"]) * ln2 + np.array(g["y_const"])) * np.array(g["gate"])
+    np.testing.assert_allclose(y.ravel(), expect, rtol=1e-15, atol=1e-15)
+    assert last.ravel()[0] == pytest.approx(g["h_ln2_coeff"][-1] * ln2, rel=1e-15)
+
+
+def test_single_step_by_hand(oracle_mod):
+    """N = 1, L = 1: y = (C Δ B u + D u) silu(z), h = Δ B u."""
+    u, dr, bias, al, Bv, Cv, Dv, zv = 0.7, -0.3, 0.2, 0.4, 1.5, -2.0, 0.9, 1.1
+    y, last, _ = oracle_mod.ss_fwd(
+        np.full((1, 1, 1), u, np.float32), np.full((1, 1, 1), dr, np.float32),
+        np.full(1, bias, np.float32), np.full((1, 1), al, np.float32),
+        np.full((1, 1, 1), Bv, np.float32), np.full((1, 1, 1), Cv, np.float32),
+        np.full(1, Dv, np.float32), np.full((1, 1, 1), zv, np.float32))
+    f = lambda v: float(np.float32(v))
+    dlt = math.log1p(math.exp(f(dr) + f(bias)))
+    h = dlt * f(Bv) * f(u)
+    expect = (f(Cv) * h + f(Dv) * f(u)) * f(zv) / (1 + math.exp(-f(zv)))
+    assert y.ravel()[0] == pytest.approx(expect, rel=1e-15)
+    assert last.ravel()[0] == pytest.approx(h, rel=1e-15)
+
+
+# ---------------------------------------------------------------- the operator
+
+def _combine(p2, p1):
+    """(a2,b2)∘(a1,b1) = (a2 a1, a2 b1 + b2): p1 is the earlier element."""
+    return (p2[0] * p1[0], p2[0] * p1[1] + p2[1])
+
+
+def _all_bracketings(seq):
+    if len(seq) == 1:
+        yield seq[0]
+        return
+    for k in range(1, len(seq)):
+        for left in _all_bracketings(seq[:k]):
+            for right in _all_bracketings(seq[k:]):
+                yield _combine(right, left)
+
+
+@pytest.mark.parametrize("L", [2, 3, 4, 5, 6])
+def test_operator_associative_bruteforce(L):
+    """Every bracketing of the pair product over exact rationals equals the left fold, whose
+    second component is the sequential recurrence h_t = a_t h_{t-1} + b_t from h_{-1} = 0."""
+    rng = np.random.default_rng(L)
+    pairs = [(Fraction(int(rng.integers(1, 9)), int(rng.integers(1, 9))),
+              Fraction(int(rng.integers(-9, 10)), int(rng.integers(1, 9)))) for _ in range(L)]
+    h = Fraction(0)
+    for a, b in pairs:
+        h = a * h + b
+    fold = pairs[0]
+    for p in pairs[1:]:
+        fold = _combine(p, fold)
+    assert fold[1] == h
+    results = set(_all_bracketings(pairs))
+    assert results == {fold}
+    # The in-place update order matters: updating a before b (a *= a_prev; b = a*b_prev + b)
+    # is a different operator; check it disagrees here, so the order is pinned.
+    wrong = pairs[0]
+    for a2, b2 in pairs[1:]:
+        na = a2 * wrong[0]
+        wrong = (na, na * wrong[1] + b2)
+    assert L == 1 or wrong[1] != h or all(p[0] == 1 for p in pairs)
+
+
+@pytest.mark.parametrize("chunk", [1, 3, 16, 64, 1000])
+def test_chunked_scan_equals_sequential(oracle_mod, chunk):
+    """The pair scan with a per-chunk carry gives the sequential result for any chunk length."""
+    a = _rand_inputs(7, batch=2, L=100, Dm=3, N=6)
+    y, last, _ = _call(oracle_mod, a)
+    yc, lastc = oracle_mod.ss_fwd_chunked(a["u"], a["delta_raw"], a["delta_bias"], a["A_log"],
+                                          a["B"], a["C"], a["D"], a["z"], chunk)
+    np.testing.assert_allclose(yc, y, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lastc, last, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- decode vs scan
+
+def test_decode_iterated_equals_forward(oracle_mod):
+    a = _rand_inputs(9, batch=3, L=40, Dm=6, N=5)
+    y, last, _ = _call(oracle_mod, a)
+    state = np.zeros((3, 6, 5))
+    for t in range(40):
+        yt, state, _ = oracle_mod.ss_step(state, a["u"][:, t], a["delta_raw"][:, t], a["delta_bias"],
+                                          a["A_log"], a["B"][:, t], a["C"][:, t], a["D"], a["z"][:, t])
+        np.testing.assert_allclose(yt, y[:, t], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(state, last, rtol=1e-13, atol=1e-15)
+
+
+def test_prefix_then_decode_equals_forward(oracle_mod):
+    a = _rand_inputs(10, batch=1, L=30, Dm=4, N=4)
+    y, last, _ = _call(oracle_mod, a)
+    k = 19
+    pre = {key: (v[:, :k] if key in ("u", "delta_raw", "z", "B", "C") else v) for key, v in a.items()}
+    _, state, _ = _call(oracle_mod, pre)
+    for t in range(k, 30):
+        yt, state, _ = oracle_mod.ss_step(state, a["u"][:, t], a["delta_raw"][:, t], a["delta_bias"],
+                                          a["A_log"], a["B"][:, t], a["C"][:, t], a["D"], a["z"][:, t])
+        np.testing.assert_allclose(yt, y[:, t], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(state, last, rtol=1e-13, atol=1e-15)
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_channel_permutation_and_batch_independence(oracle_mod):
+    a = _rand_inputs(12, batch=3, L=25, Dm=7, N=4)
+    a["A_log"] = (a["A_log"] * np.linspace(0.5, 1.5, 7, dtype=np.float32)[:, None]).astype(np.float32)
+    y, last, _ = _call(oracle_mod, a)
+    perm = np.random.default_rng(0).permutation(7)
+    b = dict(a)
+    for key in ("u", "delta_raw", "z"):
+        b[key] = np.ascontiguousarray(a[key][:, :, perm])
+    for key in ("delta_bias", "D"):
+        b[key] = np.ascontiguousarray(a[key][perm])
+    b["A_log"] = np.ascontiguousarray(a["A_log"][perm])
+    yp, lastp, _ = _call(oracle_mod, b)
+    np.testing.assert_array_equal(yp, y[:, :, perm])
+    np.testing.assert_array_equal(lastp, last[:, perm])
+    for bi in range(3):
+        c = {key: (np.ascontiguousarray(v[bi:bi + 1]) if key in ("u", "delta_raw", "z", "B", "C") else v)
+             for key, v in a.items()}
+        yb, lastb, _ = _call(oracle_mod, c)
+        np.testing.assert_array_equal(yb[0], y[bi])
+        np.testing.assert_array_equal(lastb[0], last[bi])
+
+
+def test_linear_in_u_without_gate(oracle_mod):
+    a = _rand_inputs(13, batch=2, L=31, Dm=3, N=4)
+    a["z"] = None
+    y1, l1, _ = _call(oracle_mod, a)
+    b = dict(a)
+    b["u"] = (a["u"] * np.float32(2.0)).astype(np.float32)   # exact scaling by 2
+    y2, l2, _ = _call(oracle_mod, b)
+    np.testing.assert_allclose(y2, 2 * y1, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(l2, 2 * l1, rtol=1e-14, atol=1e-15)
+
+
+def test_rows_subset_matches_full(oracle_mod):
+    a = _rand_inputs(14, batch=2, L=20, Dm=5, N=3)
+    y, last, mag = _call(oracle_mod, a)
+    rows = np.array([7, 0, 9, 3])
+    yr, lr, mr = _call(oracle_mod, a, rows=rows)
+    for i, r in enumerate(rows):
+        b, d = divmod(int(r), 5)
+        np.testing.assert_array_equal(yr[i], y[b, :, d])
+        np.testing.assert_array_equal(lr[i], last[b, d])
+        np.testing.assert_array_equal(mr[i], mag[b, :, d])
+    assert np.all(mag >= np.abs(y) * (1 - 1e-15))
+
+
+# ---------------------------------------------------------------- high precision
+
+def test_tiny_config_against_high_precision(oracle_mod):
+    """Re-run the tiny workload with 40-digit arithmetic: the fp64 oracle agrees to ~1e-13
+    of each output's magnitude."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 40
+    w = synth.config("tiny")
+    a = w.arrays
+    y, last, mag = _call(oracle_mod, a)
+    mp = mpmath.mpf
+    for d in range(w.Dm):
+        A = [-mpmath.exp(mp(float(a["A_log"][d, n]))) for n in range(w.N)]
+        h = [mp(0)] * w.N
+        for t in range(w.L):
+            x = mp(float(a["delta_raw"][0, t, d])) + mp(float(a["delta_bias"][d]))
+            dlt = mpmath.log1p(mpmath.exp(x))
+            ut = mp(float(a["u"][0, t, d]))
+            acc = mp(0)
+            for n in range(w.N):
+                h[n] = mpmath.exp(dlt * A[n]) * h[n] + dlt * mp(float(a["B"][0, t, n])) * ut
+                acc += mp(float(a["C"][0, t, n])) * h[n]
+            zt = mp(float(a["z"][0, t, d]))
+            yt = (acc + mp(float(a["D"][d])) * ut) * zt / (1 + mpmath.exp(-zt))
+            assert abs(float(yt) - y[0, t, d]) <= 1e-13 * mag[0, t, d] + 1e-300
+        for n in range(w.N):
+            assert abs(float(h[n]) - last[0, d, n]) <= 1e-13 * abs(float(h[n])) + 1e-300
