@@ -1,0 +1,372 @@
+"""Benchmark: selective-scan forward (or decode) throughput on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  forward workloads: one ss_fwd over the whole [batch, L, Dm] problem (softplus, the scan,
+                     D skip, z gate and last_state, all in one kernel launch);
+  decode workload:   ss_step for each of 48 layers' distinct states, replayed as one CUDA graph.
+Prints one JSON line.  Inputs live in HBM before the timed region; every workload's working
+set is larger than the 129 MB L2, so no flush is needed between steps.  Under torchrun each
+rank runs its own copy of the workload (independent problems, no collective): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selective-scan state-updates/s (B·L·D·N) & HBM GB/s vs roofline, 1×GB300"
+UNIT = "state-updates/s"
+DECODE_LAYERS = 48
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mamba130m",
+                    choices=["mamba130m", "long32k", "mamba2p8b_bf16", "decode1p4b", "tiny"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def alg_bytes(w) -> int:
+    """Bytes the method must move: read u, delta_raw, z and write y ([B,L,Dm] io dtype); read
+    B, C ([B,L,N]); params A_log [Dm,N], D, bias [Dm] fp32; write last_state [B,Dm,N] fp32."""
+    s = w.io_bytes()
+    if w.name.startswith("decode"):
+        # per layer: x, delta_raw, z read + y write [B,Dm]; B, C [B,N]; A_log, D; state r+w
+        per = (4 * w.batch * w.Dm + 2 * w.batch * w.N) * s + (w.Dm * w.N + w.Dm) * 4 \
+            + 2 * w.batch * w.Dm * w.N * 4
+        return per * DECODE_LAYERS
+    return w.batch * w.L * (4 * w.Dm + 2 * w.N) * s + w.Dm * (w.N + 2) * 4 + w.batch * w.Dm * w.N * 4
+
+
+def updates_per_step(w) -> int:
+    if w.name.startswith("decode"):
+        return w.batch * w.Dm * w.N * DECODE_LAYERS
+    return w.state_updates
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        finally:
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [v for v in sm if mx and v >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def make_fwd_call(w, torch, ss, dev):
+    a = w.arrays
+    io = w.io
+
+    def up(x):
+        if x is None:
+            return None
+        t = torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(dev)
+        return t.to(torch.bfloat16) if io == "bf16" else t
+
+    def upf(x):
+        return None if x is None else torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(dev)
+
+    t = dict(u=up(a["u"]), delta_raw=up(a["delta_raw"]), z=up(a["z"]), B=up(a["B"]), C=up(a["C"]),
+             A_log=upf(a["A_log"]), D=upf(a["D"]), delta_bias=upf(a["delta_bias"]))
+    y = torch.empty_like(t["u"])
+    last = torch.empty((w.batch, w.Dm, w.N), device=dev)
+
+    def step():
+        ss.ss_fwd(t["u"], t["delta_raw"], t["delta_bias"], t["A_log"], t["B"], t["C"], t["D"], t["z"],
+                  y=y, last_state=last)
+    return step, t, y, last
+
+
+def make_decode_call(w0, torch, ss, dev):
+    from selective_state_space_scan_gb300 import synth
+    layers = []
+    for layer in range(DECODE_LAYERS):
+        w = synth.step_inputs(w0.batch, w0.Dm, w0.N, io=w0.io, seed=w0.seed, layer=layer)
+        a = w.arrays
+        layers.append({k: (None if v is None else torch.from_numpy(v).to(dev)) for k, v in a.items()})
+    ys = [torch.empty((w0.batch, w0.Dm), device=dev) for _ in layers]
+
+    def eager():
+        for L, y in zip(layers, ys):
+            ss.ss_step(L["state"], L["x"], L["delta_raw"], L["delta_bias"], L["A_log"], L["B"], L["C"],
+                       L["D"], L["z"], y=y)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        eager()                      # warm the library on this stream before capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        eager()
+
+    def step():
+        g.replay()
+    return step, layers, ys
+
+
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    import selective_state_space_scan_gb300 as ss
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    decode = w.name.startswith("decode")
+    if decode:
+        step, tensors, outs = make_decode_call(w, torch, ss, dev)
+    else:
+        step, tensors, y, last = make_fwd_call(w, torch, ss, dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    barrier()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        end.record(stream)
+        barrier()
+    total_ms = start.elapsed_time(end)
+    per_launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if dist is not None:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    err = ss.device_error(clear=True)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} after the timed region")
+
+    # end-to-end through the public API: pinned host inputs -> device -> ss_fwd -> host output
+    e2e = None
+    if not args.no_e2e and not decode:
+        e2e = run_e2e(args, w, torch, ss, dev, tensors, y, last, barrier)
+    return dict(total_ms=total_ms, per_launch_ms=per_launch_ms, clocks=clk.summary(), e2e=e2e)
+
+
+def run_e2e(args, w, torch, ss, dev, t, y, last, barrier):
+    keys = [k for k in ("u", "delta_raw", "z", "B", "C", "A_log", "D", "delta_bias") if t[k] is not None]
+    host = {k: t[k].cpu().pin_memory() for k in keys}
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    last_host = torch.empty(last.shape, dtype=last.dtype).pin_memory()
+    h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
+    d2h = y_host.numel() * y_host.element_size() + last_host.numel() * last_host.element_size()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for k in keys:
+            t[k].copy_(host[k], non_blocking=True)
+        ss.ss_fwd(t["u"], t["delta_raw"], t["delta_bias"], t["A_log"], t["B"], t["C"], t["D"], t["z"],
+                  y=y, last_state=last)
+        y_host.copy_(y, non_blocking=True)
+        last_host.copy_(last, non_blocking=True)
+
+    steps = max(3, min(args.steps, 10))
+    for _ in range(3):
+        step()
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    barrier()
+    ms = a.elapsed_time(b) / steps
+    return dict(ms=ms, h2d=h2d, d2h=d2h)
+
+
+# ---------------------------------------------------------------------------- oracle arm
+
+def oracle_time(w, min_seconds=10.0, max_passes=50):
+    """Time the fp64 oracle on the workload's full set of rows, repeated until min_seconds."""
+    import oracle
+    a = w.arrays
+    passes, elapsed = 0, 0.0
+    while passes < 1 or (elapsed < min_seconds and passes < max_passes):
+        t0 = time.perf_counter()
+        if w.name.startswith("decode"):
+            oracle.ss_step(a["state"], a["x"], a["delta_raw"], a["delta_bias"], a["A_log"], a["B"],
+                           a["C"], a["D"], a["z"])
+        else:
+            oracle.ss_fwd(a["u"], a["delta_raw"], a["delta_bias"], a["A_log"], a["B"], a["C"], a["D"],
+                          a["z"])
+        elapsed += time.perf_counter() - t0
+        passes += 1
+    units = (w.batch * w.Dm * w.N if w.name.startswith("decode") else w.state_updates) * passes
+    return units / elapsed, passes, elapsed, oracle.num_threads()
+
+
+def workload_config(w, extra=None):
+    c = {"workload": f"{w.name}: batch={w.batch} L={w.L} Dm={w.Dm} N={w.N} io={w.io}",
+         "batch": w.batch, "L": w.L, "Dm": w.Dm, "N": w.N, "io": w.io, "seed": w.seed,
+         "l2": "no flush: working set {:.0f} MB > 129 MB L2".format(alg_bytes(w) / 1e6)}
+    if w.name.startswith("decode"):
+        c["layers"] = DECODE_LAYERS
+        c["graph"] = "48 ss_step launches captured in one CUDA graph per step"
+    if extra:
+        c.update(extra)
+    return c
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    from selective_state_space_scan_gb300 import synth
+    w = synth.config(args.workload)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        rates = []
+        for _ in range(args.warmup):
+            oracle_time(w, min_seconds=0.0, max_passes=1)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            rate, _, _, cores = oracle_time(w, min_seconds=0.0, max_passes=1)
+            rates.append(rate)
+        total = time.perf_counter() - t0
+        value = updates_per_step(w) * args.steps / total if not w.name.startswith("decode") \
+            else w.batch * w.Dm * w.N * args.steps / total
+        sample = f"one full pass of the {w.name} workload per step (fp64 oracle, OpenMP over rows)"
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return 0
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    res = run_ours(args, w, rank, world, local_rank)
+    units = updates_per_step(w)
+    ms_step = res["total_ms"] / args.steps
+    value = units * world / (res["total_ms"] / 1e3 / args.steps)
+    launch_ms = statistics.mean(res["per_launch_ms"])
+    if w.name.startswith("decode"):
+        launch_ms = launch_ms / DECODE_LAYERS    # per ss_step kernel
+        bytes_launch = alg_bytes(w) / DECODE_LAYERS
+    else:
+        bytes_launch = alg_bytes(w)
+    hbm_peak, peak_kind = peaks()
+    achieved = bytes_launch / (launch_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+            "frac": achieved / hbm_peak, "traffic": None, "peak_source": peak_kind,
+            "kernel": "ss_step_kernel" if w.name.startswith("decode") else "ss_fwd_kernel",
+            "launch_ms": launch_ms}
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w), "hbm_gbs": alg_bytes(w) / (ms_step / 1e3) / 1e9,
+        "gpu_launches": args.steps * (DECODE_LAYERS if w.name.startswith("decode") else 1),
+        "clocks": res["clocks"], "roofline": roof,
+    }
+    if res["e2e"] is not None:
+        e = res["e2e"]
+        out["e2e"] = {"value": units * world / (e["ms"] / 1e3), "unit": UNIT,
+                      "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"], "ms_per_step": e["ms"]}
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, passes, elapsed, cores = oracle_time(w)
+        out["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": f"{passes} full pass(es) of the {w.name} workload, "
+                                         f"{elapsed:.1f} s of fp64 oracle time"}
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

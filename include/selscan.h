@@ -1,0 +1,136 @@
+/*
+ * libselscan — Mamba selective-scan forward pass and single-token decode update on
+ * NVIDIA GB300 (sm_103a).  Plain C ABI: device pointers, sizes, a CUDA stream handle.
+ *
+ * The operation (sources: "mamba-metal: Apple Silicon で Mamba を動かす", sections
+ * "Selective scan の本質", "チャンク間 running prefix" and "O(L) インクリメンタルデコード";
+ * the same blog's walkthrough of the official CUDA forward kernel, section
+ * "1チャンク内の処理フロー"; SpeechLens docs/kernel-optimization.md, MetalSelectiveScan
+ * tensor contract).  For every batch row b, channel d and state n, with h_{-1} = 0:
+ *
+ *   Δ_t      = softplus(delta_raw[b,t,d] + delta_bias[d])
+ *   h_t[n]   = exp(Δ_t · A[d,n]) · h_{t-1}[n] + Δ_t · B[b,t,n] · u[b,t,d],
+ *              A[d,n] = -exp(A_log[d,n])
+ *   y[b,t,d] = (Σ_n C[b,t,n] · h_t[n] + D[d] · u[b,t,d]) · silu(z[b,t,d])
+ *
+ * with silu(z) = z · sigmoid(z).  It is evaluated as a chunked associative scan over the
+ * pairs (a,b) = (exp(Δ A), Δ B u) with (a2,b2)∘(a1,b1) = (a2 a1, a2 b1 + b2) and a
+ * per-state carry across chunks, so any L runs in one launch.
+ *
+ * Conventions for every call:
+ *   - Ownership: the caller owns every buffer.  The library allocates no device or
+ *     host memory and never synchronises; work is enqueued on `stream` (a
+ *     cudaStream_t; NULL = the legacy default stream) and runs asynchronously.
+ *   - Errors: arguments are validated on the host before anything is enqueued; a
+ *     failed check returns an SS_ERR_* code and enqueues nothing.  There is no CPU or
+ *     alternative fallback.  A failed launch returns SS_ERR_CUDA.  Faults detected on
+ *     the device (a wait that timed out) set bits in a per-device error word, read
+ *     with ss_device_error().
+ *   - Pointers: every pointer argument must be device-accessible memory of the current
+ *     device (cudaMalloc or managed); host pointers are rejected with SS_ERR_INVALID_ARG.
+ *   - Types: u, delta_raw, z, B, C and y are `io_dtype` (fp32 or bf16); A_log, D,
+ *     delta_bias, last_state and the decode state are always fp32.  Arithmetic and
+ *     the recurrent state are fp32 in both cases.
+ *   - Thread safety: calls are reentrant; the only process-wide state is the cached
+ *     driver entry point used to build TMA descriptors.
+ */
+#ifndef SELSCAN_H
+#define SELSCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SS_OK = 0,
+    SS_ERR_INVALID_ARG = 1,   /* null required pointer, bad size, host pointer, aliasing */
+    SS_ERR_UNSUPPORTED = 2,   /* N outside 1..16, size beyond the 32-bit grid limits */
+    SS_ERR_MISALIGNED = 3,    /* a pointer not aligned to its element size */
+    SS_ERR_CUDA = 4           /* a CUDA runtime/driver call or a kernel launch failed */
+} ss_status;
+
+typedef enum { SS_F32 = 0, SS_BF16 = 1 } ss_dtype;
+
+/*
+ * Element strides (not bytes) of the forward tensors.  The channel axis of u,
+ * delta_raw, z, y and the state axis of B, C have stride 1.  A NULL strides pointer
+ * means: io_dtype = SS_F32 and every tensor contiguous
+ * (x_b = L·Dm, x_l = Dm for [batch, L, Dm]; B_b = L·N, B_l = N for [batch, L, N]).
+ */
+typedef struct {
+    int32_t io_dtype;                       /* ss_dtype */
+    int64_t u_b, u_l;                       /* u        [batch, L, Dm] */
+    int64_t delta_b, delta_l;               /* delta_raw[batch, L, Dm] */
+    int64_t z_b, z_l;                       /* z        [batch, L, Dm] (ignored if z NULL) */
+    int64_t y_b, y_l;                       /* y        [batch, L, Dm] */
+    int64_t B_b, B_l;                       /* B        [batch, L, N]  */
+    int64_t C_b, C_l;                       /* C        [batch, L, N]  */
+} ss_fwd_strides;
+
+/*
+ * Selective-scan forward pass (prefill / layer scan).
+ *   u, delta_raw  [batch, L, Dm] io_dtype   input activation, pre-softplus time step
+ *   delta_bias    [Dm] fp32 or NULL (= 0)   added to delta_raw before softplus
+ *   A_log         [Dm, N] fp32 contiguous    A = -exp(A_log), computed in-kernel
+ *   B, C          [batch, L, N] io_dtype    input / output state coefficients, shared
+ *                                           by all channels of a batch row
+ *   D             [Dm] fp32 or NULL (= 0)   skip weight
+ *   z             [batch, L, Dm] io_dtype or NULL (no gate)
+ *   y             [batch, L, Dm] io_dtype   output; must not overlap any input
+ *   last_state    [batch, Dm, N] fp32 contiguous or NULL: h_{L-1}, the state that a
+ *                                           following ss_step continues from
+ *   batch, L, Dm  >= 0; batch == 0 or Dm == 0 is a no-op; L == 0 writes zeros to
+ *                 last_state (if given) and nothing else
+ *   N             1..16
+ * Returns SS_OK once the work is enqueued.
+ */
+ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias,
+                 const float* A_log, const void* B, const void* C, const float* D,
+                 const void* z, void* y, float* last_state, int64_t batch, int64_t L,
+                 int64_t Dm, int64_t N, const ss_fwd_strides* strides, void* stream);
+
+/*
+ * Element strides of the decode tensors.  x, delta_raw, z, y are [batch, Dm] with channel
+ * stride 1; B, C are [batch, N] with state stride 1; the state is [batch, Dm, N] with
+ * state stride 1.  NULL means io_dtype = SS_F32 and all contiguous.
+ */
+typedef struct {
+    int32_t io_dtype;
+    int64_t x_b, delta_b, z_b, y_b, B_b, C_b;
+    int64_t state_b, state_d;
+} ss_step_strides;
+
+/*
+ * Single-token decode update (the O(1)-per-token step):
+ *   Δ = softplus(delta_raw[b,d] + delta_bias[d]);
+ *   state[b,d,n] <- exp(Δ·A[d,n])·state[b,d,n] + Δ·x[b,d]·B[b,n]   (in place, fp32)
+ *   y[b,d] = (Σ_n C[b,n]·state[b,d,n] + D[d]·x[b,d]) · silu(z[b,d])
+ * Arguments as for ss_fwd with L = 1 and the initial state given; y must not overlap any
+ * input or the state.  batch == 0 or Dm == 0 is a no-op.
+ */
+ss_status ss_step(float* state, const void* x, const void* delta_raw, const float* delta_bias,
+                  const float* A_log, const void* B, const void* C, const float* D,
+                  const void* z, void* y, int64_t batch, int64_t Dm, int64_t N,
+                  const ss_step_strides* strides, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* ss_status_string(ss_status status);
+
+/*
+ * Read (and, if `clear` is non-zero, reset) the device error word of the current
+ * device: bit 0 = a kernel gave up waiting for a TMA tile (its outputs are invalid).
+ * Synchronises with the device.  Returns SS_ERR_CUDA if the word cannot be read.
+ */
+ss_status ss_device_error(uint32_t* bits, int clear);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int ss_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SELSCAN_H */

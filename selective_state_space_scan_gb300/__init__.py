@@ -1,1 +1,151 @@
-"""GB300-native selective scan (placeholder; binding added with the CUDA library)."""
+"""GB300-native Mamba selective scan: Python binding of libselscan's C ABI.
+
+Argument marshalling only: every step of the scan runs in the CUDA library
+(``include/selscan.h``).  PyTorch supplies device memory and the current stream.
+There is no CPU path: if the library cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import _build
+
+__all__ = ["ss_fwd", "ss_step", "SelscanError", "lib", "device_error", "version",
+           "status_string", "SS_F32", "SS_BF16", "FwdStrides", "StepStrides"]
+
+SS_F32, SS_BF16 = 0, 1
+_STATUS = {0: "SS_OK", 1: "SS_ERR_INVALID_ARG", 2: "SS_ERR_UNSUPPORTED", 3: "SS_ERR_MISALIGNED",
+           4: "SS_ERR_CUDA"}
+
+
+class SelscanError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+class FwdStrides(ctypes.Structure):
+    _fields_ = [("io_dtype", ctypes.c_int32)] + [(n, ctypes.c_int64) for n in (
+        "u_b", "u_l", "delta_b", "delta_l", "z_b", "z_l", "y_b", "y_l", "B_b", "B_l", "C_b", "C_l")]
+
+
+class StepStrides(ctypes.Structure):
+    _fields_ = [("io_dtype", ctypes.c_int32)] + [(n, ctypes.c_int64) for n in (
+        "x_b", "delta_b", "z_b", "y_b", "B_b", "C_b", "state_b", "state_d")]
+
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libselscan (built in-tree first if missing or stale)."""
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        L.ss_fwd.argtypes = [vp] * 10 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp]
+        L.ss_fwd.restype = ctypes.c_int
+        L.ss_step.argtypes = [vp] * 10 + [i64] * 3 + [ctypes.POINTER(StepStrides), vp]
+        L.ss_step.restype = ctypes.c_int
+        L.ss_status_string.argtypes = [ctypes.c_int]
+        L.ss_status_string.restype = ctypes.c_char_p
+        L.ss_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+        L.ss_device_error.restype = ctypes.c_int
+        L.ss_version.argtypes = []
+        L.ss_version.restype = ctypes.c_int
+        _LIB = L
+    return _LIB
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().ss_status_string(int(status)).decode()
+    except OSError:
+        return _STATUS.get(int(status), f"status {status}")
+
+
+def version() -> int:
+    return int(lib().ss_version())
+
+
+def device_error(clear: bool = False) -> int:
+    bits = ctypes.c_uint32(0)
+    st = lib().ss_device_error(ctypes.byref(bits), int(bool(clear)))
+    if st != 0:
+        raise SelscanError(st, "ss_device_error")
+    return int(bits.value)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _io_code(dtype) -> int:
+    import torch
+    if dtype == torch.float32:
+        return SS_F32
+    if dtype == torch.bfloat16:
+        return SS_BF16
+    raise TypeError(f"io tensors must be float32 or bfloat16, got {dtype}")
+
+
+def _check_inner(t, name):
+    if t is not None and t.dim() > 0 and t.stride(-1) != 1 and t.shape[-1] > 1:
+        raise ValueError(f"{name}: the last axis must have stride 1")
+
+
+def ss_fwd(u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, last_state=None,
+           stream=None):
+    """Selective-scan forward pass through the C ABI.
+
+    u, delta_raw, z: [batch, L, Dm]; B, C: [batch, L, N] (same dtype, float32 or bfloat16);
+    A_log [Dm, N], D and delta_bias [Dm]: float32.  ``y`` (allocated like u when None) and
+    ``last_state`` ([batch, Dm, N] float32, optional) are written.  Returns y.
+    """
+    import torch
+    batch, L, Dm = u.shape
+    N = A_log.shape[1]
+    io = _io_code(u.dtype)
+    if y is None:
+        y = torch.empty((batch, L, Dm), dtype=u.dtype, device=u.device)
+    for name, t in (("u", u), ("delta_raw", delta_raw), ("z", z), ("y", y), ("B", B), ("C", C)):
+        _check_inner(t, name)
+    s = FwdStrides(io, u.stride(0), u.stride(1), delta_raw.stride(0), delta_raw.stride(1),
+                   z.stride(0) if z is not None else 0, z.stride(1) if z is not None else 0,
+                   y.stride(0), y.stride(1), B.stride(0), B.stride(1), C.stride(0), C.stride(1))
+    st = lib().ss_fwd(_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C),
+                      _ptr(D), _ptr(z), _ptr(y), _ptr(last_state), batch, L, Dm, N,
+                      ctypes.byref(s), _stream_handle(stream))
+    if st != 0:
+        raise SelscanError(st, "ss_fwd")
+    return y
+
+
+def ss_step(state, x, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, stream=None):
+    """One decode step through the C ABI: updates ``state`` [batch, Dm, N] (float32) in place
+    and returns y [batch, Dm] (allocated like x when None)."""
+    import torch
+    batch, Dm, N = state.shape
+    io = _io_code(x.dtype)
+    if y is None:
+        y = torch.empty((batch, Dm), dtype=x.dtype, device=x.device)
+    for name, t in (("x", x), ("delta_raw", delta_raw), ("z", z), ("y", y), ("B", B), ("C", C),
+                    ("state", state)):
+        _check_inner(t, name)
+    s = StepStrides(io, x.stride(0), delta_raw.stride(0), z.stride(0) if z is not None else 0,
+                    y.stride(0), B.stride(0), C.stride(0), state.stride(0), state.stride(1))
+    st = lib().ss_step(_ptr(state), _ptr(x), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log),
+                       _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(y), batch, Dm, N, ctypes.byref(s),
+                       _stream_handle(stream))
+    if st != 0:
+        raise SelscanError(st, "ss_step")
+    return y

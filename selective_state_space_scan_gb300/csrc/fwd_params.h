@@ -1,0 +1,49 @@
+// Kernel argument blocks shared by the host dispatcher and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+namespace selscan {
+
+// Forward scan: element strides (channel / state stride is 1), sizes and pointers.
+struct FwdParams {
+    const void* u;
+    const void* delta;
+    const void* z;       // nullptr: no gate
+    const void* Bm;
+    const void* Cm;
+    const float* bias;   // nullptr: 0
+    const float* A_log;  // [Dm, N]
+    const float* Dv;     // nullptr: 0
+    void* y;
+    float* last_state;   // nullptr: not written; else [batch, Dm, N] contiguous
+    int64_t u_b, u_l, d_b, d_l, z_b, z_l, y_b, y_l, B_b, B_l, C_b, C_l;
+    int batch, L, Dm, N;
+    int nchunks;
+    int tiles_per_batch;
+    unsigned int* err;   // device error word
+};
+
+// TMA descriptors for the five streamed tensors (unused by the plain-load variant).
+struct FwdMaps {
+    CUtensorMap u, delta, z, B, C;
+};
+
+// Decode step.
+struct StepParams {
+    float* state;        // [batch, Dm, N] with strides state_b, state_d (state stride 1)
+    const void* x;
+    const void* delta;
+    const void* z;       // nullptr: no gate
+    const void* Bm;      // [batch, N]
+    const void* Cm;
+    const float* bias;
+    const float* A_log;
+    const float* Dv;
+    void* y;             // [batch, Dm]
+    int64_t x_b, d_b, z_b, y_b, B_b, C_b, s_b, s_d;
+    int batch, Dm, N;
+};
+
+}  // namespace selscan

@@ -1,0 +1,347 @@
+// libselscan C ABI: host-side validation, TMA descriptor construction and kernel dispatch.
+// Declarations and the full contract are in include/selscan.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/selscan.h"
+#include "internal.h"
+
+namespace selscan {
+
+__device__ unsigned int g_device_error;
+
+namespace {
+
+constexpr int kVersion = 100;   // 0.1.0
+
+// Test hook: 0 = automatic choice, 1 = force the plain-load forward kernel,
+// 2 = force the TMA kernel (rejected with SS_ERR_UNSUPPORTED when not eligible).
+std::atomic<int> g_force_fwd_path{0};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+unsigned int* device_error_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    static std::atomic<unsigned int*> cache[64] = {};
+    if (dev < 0 || dev >= 64) return nullptr;
+    unsigned int* p = cache[dev].load();
+    if (!p) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_device_error) != cudaSuccess) return nullptr;
+        p = static_cast<unsigned int*>(a);
+        cache[dev].store(p);
+    }
+    return p;
+}
+
+bool is_device_pointer(const void* p, int dev) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeManaged) return true;
+    return a.type == cudaMemoryTypeDevice && a.device == dev;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Byte range touched by a [n0, n1, n2] tensor with element strides (s0, s1, 1).
+struct Span {
+    uintptr_t lo = 0, hi = 0;
+    bool empty() const { return hi <= lo; }
+};
+Span span3(const void* p, int64_t n0, int64_t n1, int64_t n2, int64_t s0, int64_t s1, int64_t es) {
+    Span s;
+    if (!p || n0 <= 0 || n1 <= 0 || n2 <= 0) return s;
+    s.lo = reinterpret_cast<uintptr_t>(p);
+    s.hi = s.lo + static_cast<uintptr_t>(((n0 - 1) * s0 + (n1 - 1) * s1 + n2) * es);
+    return s;
+}
+bool overlap(const Span& a, const Span& b) {
+    return !a.empty() && !b.empty() && a.lo < b.hi && b.lo < a.hi;
+}
+
+ss_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SS_OK : SS_ERR_CUDA; }
+
+// 3-D tiled descriptor over a [batch, rows, cols] tensor (cols contiguous) with a box of
+// [1, box_rows, box_cols]; rows/channels past the end read as zero.
+bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t cols, int64_t rows,
+              int64_t batch, int64_t row_stride, int64_t batch_stride, int box_cols, int box_rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const int64_t es = bf16 ? 2 : 4;
+    const int row_bytes = box_cols * static_cast<int>(es);
+    CUtensorMapSwizzle sw = row_bytes >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : row_bytes == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
+                          : row_bytes == 32  ? CU_TENSOR_MAP_SWIZZLE_32B
+                                             : CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (batch <= 1) batch_stride = rows * row_stride;   // any valid stride; never stepped
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_stride * es),
+                             static_cast<cuuint64_t>(batch_stride * es)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                     const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool tma_stride_ok(int64_t stride_elems, int64_t es) {
+    return stride_elems > 0 && (stride_elems * es) % 16 == 0 && stride_elems * es < (int64_t(1) << 40);
+}
+
+}  // namespace
+}  // namespace selscan
+
+using namespace selscan;
+
+extern "C" {
+
+const char* ss_status_string(ss_status s) {
+    switch (s) {
+        case SS_OK: return "SS_OK";
+        case SS_ERR_INVALID_ARG: return "SS_ERR_INVALID_ARG: invalid argument";
+        case SS_ERR_UNSUPPORTED: return "SS_ERR_UNSUPPORTED: unsupported size or configuration";
+        case SS_ERR_MISALIGNED: return "SS_ERR_MISALIGNED: pointer not aligned to its element type";
+        case SS_ERR_CUDA: return "SS_ERR_CUDA: CUDA call or kernel launch failed";
+    }
+    return "unknown ss_status";
+}
+
+int ss_version(void) { return kVersion; }
+
+ss_status ss_device_error(uint32_t* bits, int clear) {
+    if (!bits) return SS_ERR_INVALID_ARG;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return SS_ERR_CUDA;
+    *bits = v;
+    if (clear) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return SS_ERR_CUDA;
+    }
+    return SS_OK;
+}
+
+// Internal test hook (not part of the public header).
+int ss__force_fwd_path(int mode) {
+    if (mode < 0 || mode > 2) return -1;
+    return g_force_fwd_path.exchange(mode);
+}
+
+ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
+                 const void* B, const void* C, const float* D, const void* z, void* y,
+                 float* last_state, int64_t batch, int64_t L, int64_t Dm, int64_t N,
+                 const ss_fwd_strides* strides, void* stream_ptr) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    if (batch < 0 || L < 0 || Dm < 0) return SS_ERR_INVALID_ARG;
+    if (N < 1 || N > 16) return SS_ERR_UNSUPPORTED;
+    ss_fwd_strides s;
+    if (strides) {
+        s = *strides;
+    } else {
+        std::memset(&s, 0, sizeof(s));
+        s.io_dtype = SS_F32;
+        s.u_b = s.delta_b = s.z_b = s.y_b = L * Dm;
+        s.u_l = s.delta_l = s.z_l = s.y_l = Dm;
+        s.B_b = s.C_b = L * N;
+        s.B_l = s.C_l = N;
+    }
+    if (s.io_dtype != SS_F32 && s.io_dtype != SS_BF16) return SS_ERR_INVALID_ARG;
+    const bool bf16 = s.io_dtype == SS_BF16;
+    const int64_t es = bf16 ? 2 : 4;
+    if (batch == 0 || Dm == 0) return SS_OK;
+    if (!A_log) return SS_ERR_INVALID_ARG;
+    if (L == 0) {
+        if (!last_state) return SS_OK;
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+        if (!is_device_pointer(last_state, dev)) return SS_ERR_INVALID_ARG;
+        return cuda_status(cudaMemsetAsync(last_state, 0, sizeof(float) * batch * Dm * N, stream));
+    }
+    if (!u || !delta_raw || !B || !C || !y) return SS_ERR_INVALID_ARG;
+    // strides: non-negative; the batch stride may only be anything when batch == 1
+    const int64_t st[] = {s.u_b, s.u_l, s.delta_b, s.delta_l, s.y_b, s.y_l, s.B_b, s.B_l, s.C_b, s.C_l,
+                          z ? s.z_b : 0, z ? s.z_l : 0};
+    for (int64_t v : st)
+        if (v < 0) return SS_ERR_INVALID_ARG;
+    if (s.u_l < Dm || s.delta_l < Dm || s.y_l < Dm || (z && s.z_l < Dm)) {
+        if (L > 1) return SS_ERR_INVALID_ARG;
+    }
+    if ((s.B_l < N || s.C_l < N) && L > 1) return SS_ERR_INVALID_ARG;
+    // grid limits of this kernel family
+    const int tile_w = fwd_tile_channels();
+    const int64_t tiles = (Dm + tile_w - 1) / tile_w;
+    if (L > INT32_MAX || Dm > INT32_MAX || batch * tiles > INT32_MAX) return SS_ERR_UNSUPPORTED;
+    // alignment to the element type
+    const void* io_ptrs[] = {u, delta_raw, B, C, y, z};
+    for (const void* p : io_ptrs)
+        if (p && !aligned(p, es)) return SS_ERR_MISALIGNED;
+    const void* f_ptrs[] = {A_log, D, delta_bias, last_state};
+    for (const void* p : f_ptrs)
+        if (p && !aligned(p, 4)) return SS_ERR_MISALIGNED;
+    // device memory of the current device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+    const void* all_ptrs[] = {u, delta_raw, B, C, y, z, A_log, D, delta_bias, last_state};
+    for (const void* p : all_ptrs)
+        if (p && !is_device_pointer(p, dev)) return SS_ERR_INVALID_ARG;
+    // outputs must not overlap inputs
+    const Span sy = span3(y, batch, L, Dm, s.y_b, s.y_l, es);
+    const Span sl = span3(last_state, batch, Dm, N, Dm * N, N, 4);
+    const Span ins[] = {span3(u, batch, L, Dm, s.u_b, s.u_l, es),
+                        span3(delta_raw, batch, L, Dm, s.delta_b, s.delta_l, es),
+                        span3(z, batch, L, Dm, s.z_b, s.z_l, es),
+                        span3(B, batch, L, N, s.B_b, s.B_l, es),
+                        span3(C, batch, L, N, s.C_b, s.C_l, es),
+                        span3(A_log, 1, Dm, N, 0, N, 4),
+                        span3(D, 1, 1, Dm, 0, 0, 4),
+                        span3(delta_bias, 1, 1, Dm, 0, 0, 4)};
+    for (const Span& in : ins)
+        if (overlap(sy, in) || overlap(sl, in)) return SS_ERR_INVALID_ARG;
+    if (overlap(sy, sl)) return SS_ERR_INVALID_ARG;
+
+    FwdParams p;
+    p.u = u; p.delta = delta_raw; p.z = z; p.Bm = B; p.Cm = C;
+    p.bias = delta_bias; p.A_log = A_log; p.Dv = D; p.y = y; p.last_state = last_state;
+    p.u_b = s.u_b; p.u_l = s.u_l; p.d_b = s.delta_b; p.d_l = s.delta_l;
+    p.z_b = s.z_b; p.z_l = s.z_l; p.y_b = s.y_b; p.y_l = s.y_l;
+    p.B_b = s.B_b; p.B_l = s.B_l; p.C_b = s.C_b; p.C_l = s.C_l;
+    p.batch = static_cast<int>(batch);
+    p.L = static_cast<int>(L);
+    p.Dm = static_cast<int>(Dm);
+    p.N = static_cast<int>(N);
+    const int T = fwd_chunk_steps();
+    p.nchunks = static_cast<int>((L + T - 1) / T);
+    p.tiles_per_batch = static_cast<int>(tiles);
+    p.err = device_error_ptr();
+    if (!p.err) return SS_ERR_CUDA;
+
+    FwdVariant v;
+    v.ns = N <= 4 ? 4 : N <= 8 ? 8 : 16;
+    // TMA path: B/C rows exactly ns wide and a multiple of 16 bytes, 16-byte aligned
+    // bases and row/batch strides.
+    bool tma = (N == v.ns) && (N * es) % 16 == 0;
+    const void* tma_ptrs[] = {u, delta_raw, B, C, z};
+    for (const void* q : tma_ptrs)
+        if (q && !aligned(q, 16)) tma = false;
+    const int64_t tma_strides[] = {s.u_l, s.delta_l, s.B_l, s.C_l, z ? s.z_l : s.u_l};
+    for (int64_t v2 : tma_strides)
+        if (!tma_stride_ok(v2, es)) tma = false;
+    if (batch > 1) {
+        const int64_t bstr[] = {s.u_b, s.delta_b, s.B_b, s.C_b, z ? s.z_b : s.u_b};
+        for (int64_t v2 : bstr)
+            if (!tma_stride_ok(v2, es)) tma = false;
+    }
+    const int force = g_force_fwd_path.load();
+    if (force == 1) tma = false;
+
+    FwdMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    if (tma) {
+        // A shape the descriptor encoder rejects is served by the plain-load kernel.
+        tma = make_map(&maps.u, u, bf16, Dm, L, batch, s.u_l, s.u_b, tile_w, T) &&
+              make_map(&maps.delta, delta_raw, bf16, Dm, L, batch, s.delta_l, s.delta_b, tile_w, T) &&
+              (!z || make_map(&maps.z, z, bf16, Dm, L, batch, s.z_l, s.z_b, tile_w, T)) &&
+              make_map(&maps.B, B, bf16, N, L, batch, s.B_l, s.B_b, v.ns, T) &&
+              make_map(&maps.C, C, bf16, N, L, batch, s.C_l, s.C_b, v.ns, T);
+    }
+    if (force == 2 && !tma) return SS_ERR_UNSUPPORTED;
+    v.tma = tma;
+    const cudaError_t e = bf16 ? launch_fwd_bf16(v, p, maps, stream) : launch_fwd_f32(v, p, maps, stream);
+    return cuda_status(e);
+}
+
+ss_status ss_step(float* state, const void* x, const void* delta_raw, const float* delta_bias,
+                  const float* A_log, const void* B, const void* C, const float* D, const void* z,
+                  void* y, int64_t batch, int64_t Dm, int64_t N, const ss_step_strides* strides,
+                  void* stream_ptr) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    if (batch < 0 || Dm < 0) return SS_ERR_INVALID_ARG;
+    if (N < 1 || N > 16) return SS_ERR_UNSUPPORTED;
+    ss_step_strides s;
+    if (strides) {
+        s = *strides;
+    } else {
+        std::memset(&s, 0, sizeof(s));
+        s.io_dtype = SS_F32;
+        s.x_b = s.delta_b = s.z_b = s.y_b = Dm;
+        s.B_b = s.C_b = N;
+        s.state_b = Dm * N;
+        s.state_d = N;
+    }
+    if (s.io_dtype != SS_F32 && s.io_dtype != SS_BF16) return SS_ERR_INVALID_ARG;
+    const bool bf16 = s.io_dtype == SS_BF16;
+    const int64_t es = bf16 ? 2 : 4;
+    if (batch == 0 || Dm == 0) return SS_OK;
+    if (!state || !x || !delta_raw || !A_log || !B || !C || !y) return SS_ERR_INVALID_ARG;
+    const int64_t st[] = {s.x_b, s.delta_b, s.y_b, s.B_b, s.C_b, s.state_b, s.state_d, z ? s.z_b : 0};
+    for (int64_t v : st)
+        if (v < 0) return SS_ERR_INVALID_ARG;
+    if (batch > 1 && (s.x_b < Dm || s.delta_b < Dm || s.y_b < Dm || (z && s.z_b < Dm) || s.B_b < N ||
+                      s.C_b < N))
+        return SS_ERR_INVALID_ARG;
+    if (Dm > 1 && s.state_d < N) return SS_ERR_INVALID_ARG;
+    if (batch * Dm * 4 > (int64_t(1) << 40) || Dm > INT32_MAX || batch > INT32_MAX)
+        return SS_ERR_UNSUPPORTED;
+    const void* io_ptrs[] = {x, delta_raw, B, C, y, z};
+    for (const void* p : io_ptrs)
+        if (p && !aligned(p, es)) return SS_ERR_MISALIGNED;
+    const void* f_ptrs[] = {state, A_log, D, delta_bias};
+    for (const void* p : f_ptrs)
+        if (p && !aligned(p, 4)) return SS_ERR_MISALIGNED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+    const void* all_ptrs[] = {state, x, delta_raw, B, C, y, z, A_log, D, delta_bias};
+    for (const void* p : all_ptrs)
+        if (p && !is_device_pointer(p, dev)) return SS_ERR_INVALID_ARG;
+    const Span sy = span3(y, 1, batch, Dm, 0, s.y_b, es);
+    const Span sst = span3(state, batch, Dm, N, s.state_b, s.state_d, 4);
+    const Span ins[] = {span3(x, 1, batch, Dm, 0, s.x_b, es),
+                        span3(delta_raw, 1, batch, Dm, 0, s.delta_b, es),
+                        span3(z, 1, batch, Dm, 0, s.z_b, es),
+                        span3(B, 1, batch, N, 0, s.B_b, es),
+                        span3(C, 1, batch, N, 0, s.C_b, es),
+                        span3(A_log, 1, Dm, N, 0, N, 4),
+                        span3(D, 1, 1, Dm, 0, 0, 4),
+                        span3(delta_bias, 1, 1, Dm, 0, 0, 4)};
+    for (const Span& in : ins)
+        if (overlap(sy, in) || overlap(sst, in)) return SS_ERR_INVALID_ARG;
+    if (overlap(sy, sst)) return SS_ERR_INVALID_ARG;
+
+    StepParams p;
+    p.state = state; p.x = x; p.delta = delta_raw; p.z = z; p.Bm = B; p.Cm = C;
+    p.bias = delta_bias; p.A_log = A_log; p.Dv = D; p.y = y;
+    p.x_b = s.x_b; p.d_b = s.delta_b; p.z_b = s.z_b; p.y_b = s.y_b;
+    p.B_b = s.B_b; p.C_b = s.C_b; p.s_b = s.state_b; p.s_d = s.state_d;
+    p.batch = static_cast<int>(batch);
+    p.Dm = static_cast<int>(Dm);
+    p.N = static_cast<int>(N);
+    const bool vec = (N % 4 == 0) && aligned(state, 16) && aligned(A_log, 16) &&
+                     (s.state_d % 4 == 0 || Dm == 1) && (s.state_b % 4 == 0 || batch == 1);
+    return cuda_status(launch_step(p, bf16, vec, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,81 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every
+function include/selscan.h declares, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import selective_state_space_scan_gb300 as ss
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(ss_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ss.lib()
+    names = _declared_functions()
+    assert {"ss_fwd", "ss_step", "ss_status_string", "ss_device_error", "ss_version"} <= names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_version_and_status_strings():
+    assert ss.version() >= 100
+    for code in range(5):
+        assert ss.status_string(code).startswith("SS_")
+
+
+def _fwd(**kw):
+    args = dict(u=None, delta_raw=None, delta_bias=None, A_log=None, B=None, C=None, D=None, z=None,
+                y=None, last=None, batch=1, L=8, Dm=8, N=16, strides=None)
+    args.update(kw)
+    lib = ss.lib()
+    return lib.ss_fwd(args["u"], args["delta_raw"], args["delta_bias"], args["A_log"], args["B"],
+                      args["C"], args["D"], args["z"], args["y"], args["last"], args["batch"],
+                      args["L"], args["Dm"], args["N"], args["strides"], None)
+
+
+FAKE = 0x10000   # never dereferenced: these calls fail validation before any device access
+
+
+def test_fwd_rejects_bad_sizes_on_host():
+    assert _fwd(N=0) == 2 and _fwd(N=17) == 2           # SS_ERR_UNSUPPORTED
+    assert _fwd(batch=-1) == 1 and _fwd(L=-1) == 1 and _fwd(Dm=-5) == 1
+    assert _fwd(batch=0) == 0 and _fwd(Dm=0) == 0         # no-ops
+
+
+def test_fwd_rejects_null_and_misaligned_on_host():
+    full = dict(u=FAKE, delta_raw=FAKE, A_log=FAKE, B=FAKE, C=FAKE, y=FAKE)
+    assert _fwd(**{**full, "u": None}) == 1
+    assert _fwd(**{**full, "A_log": None}) == 1
+    assert _fwd(**{**full, "y": None}) == 1
+    assert _fwd(**{**full, "u": FAKE + 2}) == 3            # fp32 pointer not 4-byte aligned
+    assert _fwd(**{**full, "A_log": FAKE + 1}) == 3
+    s = ss.FwdStrides(7, 64, 8, 64, 8, 0, 0, 64, 8, 128, 16, 128, 16)
+    assert _fwd(**full, strides=ctypes.byref(s)) == 1     # unknown io dtype
+    s = ss.FwdStrides(ss.SS_BF16, 64, 8, 64, 8, 0, 0, 64, 8, 128, 16, 128, 16)
+    assert _fwd(**{**full, "u": FAKE + 1}, strides=ctypes.byref(s)) == 3
+    s = ss.FwdStrides(ss.SS_F32, 64, -8, 64, 8, 0, 0, 64, 8, 128, 16, 128, 16)
+    assert _fwd(**full, strides=ctypes.byref(s)) == 1     # negative stride
+
+
+def test_step_rejects_bad_arguments_on_host():
+    lib = ss.lib()
+    call = lambda **kw: lib.ss_step(kw.get("state", FAKE), kw.get("x", FAKE), FAKE, None, FAKE,
+                                    FAKE, FAKE, None, None, kw.get("y", FAKE), kw.get("batch", 2),
+                                    kw.get("Dm", 8), kw.get("N", 16), None, None)
+    assert call(N=0) == 2 and call(N=20) == 2
+    assert call(batch=-1) == 1
+    assert call(batch=0) == 0
+    assert call(state=None) == 1 and call(y=None) == 1
+    assert call(state=FAKE + 2) == 3

@@ -1,0 +1,213 @@
+"""Parity of the CUDA forward scan (through the C ABI) with the fp64 oracle."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import selective_state_space_scan_gb300 as ss
+from selective_state_space_scan_gb300 import synth
+
+from helpers import assert_fwd_close, f32dev, rel_l2, to_dev, to_host
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    torch.cuda.synchronize()
+    assert ss.device_error(clear=True) == 0
+
+
+class _ForcePath:
+    """Select the forward kernel's tile-load path (0 auto, 1 plain loads, 2 TMA)."""
+    def __init__(self, mode):
+        self.mode = mode
+
+    def __enter__(self):
+        f = ss.lib().ss__force_fwd_path
+        f.argtypes = [ctypes.c_int]
+        self.prev = f(self.mode)
+
+    def __exit__(self, *exc):
+        ss.lib().ss__force_fwd_path(self.prev)
+
+
+def run_gpu(w, with_last=True, path=0):
+    a = w.arrays
+    u, dr, z = to_dev(a["u"], w.io), to_dev(a["delta_raw"], w.io), to_dev(a["z"], w.io)
+    Bm, Cm = to_dev(a["B"], w.io), to_dev(a["C"], w.io)
+    last = torch.full((w.batch, w.Dm, w.N), float("nan"), device="cuda") if with_last else None
+    with _ForcePath(path):
+        y = ss.ss_fwd(u, dr, f32dev(a["delta_bias"]), f32dev(a["A_log"]), Bm, Cm, f32dev(a["D"]), z,
+                      last_state=last)
+    torch.cuda.synchronize()
+    return to_host(y), (to_host(last) if with_last else None)
+
+
+def run_oracle(w):
+    a = w.arrays
+    return oracle.ss_fwd(a["u"], a["delta_raw"], a["delta_bias"], a["A_log"], a["B"], a["C"], a["D"], a["z"])
+
+
+def check(w, path=0, with_last=True):
+    y, last = run_gpu(w, with_last, path)
+    ry, rlast, mag = run_oracle(w)
+    assert_fwd_close(w.io, y, ry, mag, last, rlast if with_last else None,
+                     what=f"{w.name} b={w.batch} L={w.L} Dm={w.Dm} N={w.N} {w.io} path={path}")
+    return y, last
+
+
+# ------------------------------------------------------------------ the named workloads
+
+def test_tiny_workload():
+    check(synth.config("tiny"))
+
+
+@pytest.mark.parametrize("name", ["mamba130m", "long32k", "mamba2p8b_bf16"])
+def test_full_size_workloads(name):
+    """Full-size forward on every output element against the fp64 oracle."""
+    check(synth.config(name))
+
+
+# ------------------------------------------------------------------ shapes and paths
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("L", [1, 5, 47, 48, 49, 95, 97, 1000, 2049])
+def test_ragged_lengths(io, L):
+    check(synth.fwd_inputs(2, L, 40, 16, io=io, seed=100 + L))
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 7, 8, 9, 12, 15, 16])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_state_counts(N, io):
+    check(synth.fwd_inputs(2, 131, 72, N, io=io, seed=200 + N))
+
+
+@pytest.mark.parametrize("Dm", [1, 7, 8, 31, 32, 33, 100, 257])
+def test_channel_counts(Dm):
+    check(synth.fwd_inputs(3, 77, Dm, 16, seed=300 + Dm))
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("path", [1, 2])
+def test_tma_and_plain_paths_agree(io, path):
+    w = synth.fwd_inputs(2, 500, 96, 16, io=io, seed=7)
+    check(w, path=path)
+
+
+def test_paths_identical_to_each_other():
+    """Both tile-load paths feed the same arithmetic in the same order: bitwise equal."""
+    w = synth.fwd_inputs(2, 300, 64, 16, seed=8)
+    y1, l1 = run_gpu(w, path=1)
+    y2, l2 = run_gpu(w, path=2)
+    np.testing.assert_array_equal(y1, y2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("flags", ["no_z", "no_D", "no_bias", "none", "no_last"])
+def test_optional_inputs(flags):
+    kw = dict(with_z=flags not in ("no_z", "none"), with_D=flags not in ("no_D", "none"),
+              with_bias=flags not in ("no_bias", "none"))
+    w = synth.fwd_inputs(2, 150, 48, 16, seed=9, **kw)
+    check(w, with_last=flags != "no_last")
+
+
+# ------------------------------------------------------------------ strides
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("pad", [0, 8, 3])
+def test_strided_inputs(io, pad):
+    """Inputs and output as views into wider buffers (row stride Dm + pad); pad 3 makes the
+    row stride unusable for TMA and exercises the plain-load path."""
+    w = synth.fwd_inputs(2, 130, 64, 16, io=io, seed=11)
+    a = w.arrays
+    def widen(x):
+        t = to_dev(x, io)
+        big = torch.zeros(t.shape[:-1] + (t.shape[-1] + pad,), dtype=t.dtype, device="cuda")
+        big[..., :t.shape[-1]] = t
+        return big[..., :t.shape[-1]]
+    u, dr, z = widen(a["u"]), widen(a["delta_raw"]), widen(a["z"])
+    Bm, Cm = widen(a["B"]), widen(a["C"])
+    ybig = torch.full((2, 130, 64 + pad), 7.0, dtype=u.dtype, device="cuda")
+    y = ybig[..., :64]
+    last = torch.empty((2, 64, 16), device="cuda")
+    ss.ss_fwd(u, dr, f32dev(a["delta_bias"]), f32dev(a["A_log"]), Bm, Cm, f32dev(a["D"]), z, y=y,
+              last_state=last)
+    torch.cuda.synchronize()
+    ry, rlast, mag = run_oracle(w)
+    assert_fwd_close(io, to_host(y), ry, mag, to_host(last), rlast, what=f"strided pad={pad}")
+    if pad:
+        assert torch.all(ybig[..., 64:].float() == 7.0), "wrote outside y"
+
+
+def test_batch_rows_are_independent():
+    w = synth.fwd_inputs(3, 200, 48, 16, seed=12)
+    y, last = run_gpu(w)
+    for b in range(3):
+        sub = synth.Workload("row", 1, 200, 48, 16, "f32", 12,
+                             {k: (v[b:b + 1] if k in ("u", "delta_raw", "z", "B", "C") else v)
+                              for k, v in w.arrays.items()})
+        yb, lb = run_gpu(sub)
+        np.testing.assert_array_equal(yb[0], y[b])
+        np.testing.assert_array_equal(lb[0], last[b])
+
+
+# ------------------------------------------------------------------ closed forms on the GPU
+
+def test_gpu_A_to_zero_is_cumulative_sum():
+    w = synth.fwd_inputs(1, 3000, 32, 16, seed=13)
+    w.arrays["A_log"] = np.full_like(w.arrays["A_log"], -40.0)
+    check(w)
+
+
+def test_gpu_skip_only_when_C_zero():
+    w = synth.fwd_inputs(2, 100, 32, 16, seed=14)
+    w.arrays["C"] = np.zeros_like(w.arrays["C"])
+    y, _ = run_gpu(w, with_last=False)
+    a = w.arrays
+    zz = a["z"].astype(np.float64)
+    expect = a["D"] * a["u"].astype(np.float64) * zz / (1 + np.exp(-zz))
+    assert rel_l2(y, expect) < 1e-6
+
+
+# ------------------------------------------------------------------ degenerate and errors
+
+def test_L_zero_writes_zero_state():
+    last = torch.full((2, 16, 16), 5.0, device="cuda")
+    dummy = torch.zeros(1, device="cuda")
+    st = ss.lib().ss_fwd(dummy.data_ptr(), dummy.data_ptr(), None,
+                         torch.zeros(16, 16, device="cuda").data_ptr(), dummy.data_ptr(),
+                         dummy.data_ptr(), None, None, dummy.data_ptr(), last.data_ptr(), 2, 0, 16,
+                         16, None, None)
+    torch.cuda.synchronize()
+    assert st == 0
+    assert torch.all(last == 0)
+
+
+def test_empty_batch_is_noop():
+    y = torch.full((0, 10, 16), 1.0, device="cuda")
+    w = synth.fwd_inputs(1, 10, 16, 4, seed=1)
+    a = w.arrays
+    u = to_dev(a["u"], "f32")[:0]
+    ss.ss_fwd(u, u, None, f32dev(a["A_log"]), to_dev(a["B"], "f32")[:0], to_dev(a["C"], "f32")[:0],
+              None, None, y=y)
+
+
+def test_rejects_host_pointer_and_aliasing():
+    w = synth.fwd_inputs(1, 64, 32, 16, seed=2)
+    a = w.arrays
+    u, dr = to_dev(a["u"], "f32"), to_dev(a["delta_raw"], "f32")
+    Bm, Cm, Al = to_dev(a["B"], "f32"), to_dev(a["C"], "f32"), f32dev(a["A_log"])
+    with pytest.raises(ss.SelscanError) as e:
+        ss.ss_fwd(u, dr, None, Al, Bm, Cm, y=u)               # y aliases u
+    assert e.value.status == 1
+    host_u = torch.from_numpy(a["u"])
+    st = ss.lib().ss_fwd(host_u.data_ptr(), dr.data_ptr(), None, Al.data_ptr(), Bm.data_ptr(),
+                         Cm.data_ptr(), None, None, torch.empty_like(u).data_ptr(), None, 1, 64, 32,
+                         16, None, None)
+    assert st == 1

@@ -1,0 +1,129 @@
+"""Parity of the CUDA decode step (through the C ABI) with the fp64 oracle, and the
+decode == scan identities between the two entry points."""
+import numpy as np
+import pytest
+
+import oracle
+import selective_state_space_scan_gb300 as ss
+from selective_state_space_scan_gb300 import synth
+
+from helpers import assert_fwd_close, f32dev, rel_l2, to_dev, to_host
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    torch.cuda.synchronize()
+    assert ss.device_error(clear=True) == 0
+
+
+def gpu_step(w, state_dev=None):
+    a = w.arrays
+    io = w.io
+    st = f32dev(a["state"]) if state_dev is None else state_dev
+    y = ss.ss_step(st, to_dev(a["x"], io), to_dev(a["delta_raw"], io), f32dev(a["delta_bias"]),
+                   f32dev(a["A_log"]), to_dev(a["B"], io), to_dev(a["C"], io), f32dev(a["D"]),
+                   to_dev(a["z"], io))
+    torch.cuda.synchronize()
+    return to_host(y), st
+
+
+def oracle_step(w):
+    a = w.arrays
+    return oracle.ss_step(a["state"], a["x"], a["delta_raw"], a["delta_bias"], a["A_log"], a["B"],
+                          a["C"], a["D"], a["z"])
+
+
+def check_step(w):
+    y, st = gpu_step(w)
+    ry, rst, mag = oracle_step(w)
+    assert_fwd_close(w.io, y, ry, mag, to_host(st), rst, what=f"step {w.name} {w.io} N={w.N}")
+
+
+def test_decode_workload_one_layer():
+    check_step(synth.config("decode1p4b"))
+
+
+def test_decode_workload_48_layers():
+    """Every one of the 48 layers' distinct states and inputs, stepped once in order."""
+    for layer in range(48):
+        check_step(synth.step_inputs(64, 4096, 16, seed=4, layer=layer))
+
+
+@pytest.mark.parametrize("N", [1, 3, 4, 5, 8, 11, 16])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_step_state_counts(N, io):
+    check_step(synth.step_inputs(5, 77, N, io=io, seed=40 + N, with_bias=True))
+
+
+def test_step_without_gate_and_skip():
+    w = synth.step_inputs(4, 64, 16, seed=41)
+    w.arrays["z"] = None
+    w.arrays["D"] = None
+    check_step(w)
+
+
+def test_step_strided_state():
+    """State as a view with padded per-channel and per-batch strides."""
+    w = synth.step_inputs(3, 40, 16, seed=42)
+    big = torch.zeros((3, 41, 20), device="cuda")
+    big[:, :40, :16] = f32dev(w.arrays["state"])
+    view = big[:, :40, :16]
+    y, _ = gpu_step(w, state_dev=view)
+    ry, rst, mag = oracle_step(w)
+    assert_fwd_close("f32", y, ry, mag, to_host(view), rst, what="strided state")
+    assert torch.all(big[:, 40, :] == 0) and torch.all(big[:, :, 16:] == 0)
+
+
+def _fwd_dev(w):
+    a = w.arrays
+    io = w.io
+    return dict(u=to_dev(a["u"], io), delta_raw=to_dev(a["delta_raw"], io), z=to_dev(a["z"], io),
+                B=to_dev(a["B"], io), C=to_dev(a["C"], io), A_log=f32dev(a["A_log"]),
+                D=f32dev(a["D"]), delta_bias=f32dev(a["delta_bias"]))
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_iterated_step_equals_forward(io):
+    """ss_step run L times from h = 0 reproduces ss_fwd's y and last_state."""
+    w = synth.fwd_inputs(2, 120, 48, 16, io=io, seed=43)
+    t = _fwd_dev(w)
+    last = torch.empty((2, 48, 16), device="cuda")
+    y_fwd = ss.ss_fwd(t["u"], t["delta_raw"], t["delta_bias"], t["A_log"], t["B"], t["C"], t["D"],
+                      t["z"], last_state=last)
+    state = torch.zeros((2, 48, 16), device="cuda")
+    ys = []
+    for k in range(120):
+        ys.append(ss.ss_step(state, t["u"][:, k], t["delta_raw"][:, k], t["delta_bias"], t["A_log"],
+                             t["B"][:, k], t["C"][:, k], t["D"], t["z"][:, k]))
+    torch.cuda.synchronize()
+    y_step = torch.stack(ys, dim=1)
+    ry, rlast, mag = oracle.ss_fwd(*(w.arrays[k] for k in ("u", "delta_raw", "delta_bias", "A_log",
+                                                            "B", "C", "D", "z")))
+    assert_fwd_close(io, to_host(y_step), ry, mag, to_host(state), rlast, what="iterated step")
+    tol = 1e-5 if io == "f32" else 2e-2
+    assert rel_l2(to_host(y_step), to_host(y_fwd)) < tol
+    assert rel_l2(to_host(state), to_host(last)) < 1e-5
+
+
+def test_prefill_then_decode_equals_forward():
+    """ss_fwd over a prefix, its last_state handed to ss_step for the rest, equals ss_fwd over
+    the whole sequence."""
+    w = synth.fwd_inputs(2, 300, 64, 16, seed=44)
+    t = _fwd_dev(w)
+    k = 211
+    state = torch.empty((2, 64, 16), device="cuda")
+    ss.ss_fwd(t["u"][:, :k], t["delta_raw"][:, :k], t["delta_bias"], t["A_log"], t["B"][:, :k],
+              t["C"][:, :k], t["D"], t["z"][:, :k], last_state=state)
+    ys = [ss.ss_step(state, t["u"][:, j], t["delta_raw"][:, j], t["delta_bias"], t["A_log"],
+                     t["B"][:, j], t["C"][:, j], t["D"], t["z"][:, j]) for j in range(k, 300)]
+    torch.cuda.synchronize()
+    ry, rlast, mag = oracle.ss_fwd(*(w.arrays[n] for n in ("u", "delta_raw", "delta_bias", "A_log",
+                                                            "B", "C", "D", "z")))
+    assert_fwd_close("f32", to_host(torch.stack(ys, 1)), ry[:, k:], mag[:, k:], to_host(state), rlast,
+                     what="prefill+decode")
