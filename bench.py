@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--variant", default=None,
+                    help="pin the forward kernel as family,q,tma (family 0 channel-lane / 1 segment-lane; "
+                         "q warps per CTA 1|2|4 or 0 auto; tma 1|0|-1 auto); default: the library's choice")
     return ap.parse_args()
 
 
@@ -177,10 +180,17 @@ def make_decode_call(w0, torch, ss, dev):
 
 
 def run_ours(args, w, rank, world, local_rank):
+    import ctypes
     import torch
     import selective_state_space_scan_gb300 as ss
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    if args.variant:
+        fam, q, tma = (int(x) for x in args.variant.split(","))
+        hook = ss.lib().ss__force_fwd_variant
+        hook.argtypes = [ctypes.c_int] * 3
+        if hook(fam, q, tma) != 0:
+            raise ValueError(f"bad --variant {args.variant}")
     decode = w.name.startswith("decode")
     if decode:
         step, tensors, outs = make_decode_call(w, torch, ss, dev)
@@ -280,13 +290,15 @@ def oracle_time(w, min_seconds=10.0, max_passes=50):
     return units / elapsed, passes, elapsed, oracle.num_threads()
 
 
-def workload_config(w, extra=None):
+def workload_config(w, extra=None, variant=None):
     c = {"workload": f"{w.name}: batch={w.batch} L={w.L} Dm={w.Dm} N={w.N} io={w.io}",
          "batch": w.batch, "L": w.L, "Dm": w.Dm, "N": w.N, "io": w.io, "seed": w.seed,
          "l2": "no flush: working set {:.0f} MB > 129 MB L2".format(alg_bytes(w) / 1e6)}
     if w.name.startswith("decode"):
         c["layers"] = DECODE_LAYERS
         c["graph"] = "48 ss_step launches captured in one CUDA graph per step"
+    if variant:
+        c["kernel_variant"] = variant
     if extra:
         c.update(extra)
     return c
@@ -347,7 +359,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_config(w), "hbm_gbs": alg_bytes(w) / (ms_step / 1e3) / 1e9,
+        "config": workload_config(w, variant=args.variant), "hbm_gbs": alg_bytes(w) / (ms_step / 1e3) / 1e9,
         "gpu_launches": args.steps * (DECODE_LAYERS if w.name.startswith("decode") else 1),
         "clocks": res["clocks"], "roofline": roof,
     }

@@ -121,7 +121,9 @@ const char* ss_status_string(ss_status status);
 
 /*
  * Read (and, if `clear` is non-zero, reset) the device error word of the current
- * device: bit 0 = a kernel gave up waiting for a TMA tile (its outputs are invalid).
+ * device: bit 0 = a kernel gave up waiting for a TMA tile; bit 1 = a kernel was launched
+ * with a tile geometry other than its own and did nothing.  Either way that call's outputs
+ * are invalid.
  * Synchronises with the device.  Returns SS_ERR_CUDA if the word cannot be read.
  */
 ss_status ss_device_error(uint32_t* bits, int clear);

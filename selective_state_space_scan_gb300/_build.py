@@ -51,15 +51,19 @@ def is_stale() -> bool:
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and not is_stale():
+def build(force: bool = False, verbose: bool = False, extra_flags=None, out: str = None) -> str:
+    """Compile and link.  `out` (with `extra_flags`, e.g. -D overrides of the tile table)
+    builds a separate library at that path in its own object folder."""
+    lib_path = out or LIB
+    if out is None and not force and not is_stale():
         return LIB
     nvcc = nvcc_path()
-    os.makedirs(BUILD, exist_ok=True)
+    objdir = BUILD if out is None else out + ".objs"
+    os.makedirs(objdir, exist_ok=True)
     flags = ARCH + NVCC_FLAGS + list(extra_flags or [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc] + flags + ["-c", src, "-o", obj]
         proc = subprocess.run(cmd, capture_output=True, text=True)
         if proc.returncode != 0:
@@ -71,13 +75,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     srcs = _sources()
     with ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
     proc = subprocess.run(cmd, capture_output=True, text=True)
     if proc.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{proc.stdout}\n{proc.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -14,6 +14,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Error bits written to the library's device error word.
 enum : unsigned int {
     kErrWaitTimeout = 1u,   // an mbarrier wait for a TMA tile exceeded its limit
+    kErrGeometry = 2u,      // launch geometry disagrees with the kernel's tile shape
 };
 
 // 2^x on the SFU (ex2.approx.ftz: inputs below -126 flush to 0).
@@ -23,16 +24,47 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// softplus(x) = log(1 + exp(x)); the identity above x = 20 avoids exp overflow and is
-// exact to fp32 precision there (log1p(e^-20) < 2^-24 · 20).
-__device__ __forceinline__ float softplus(float x) {
-    return x <= 20.f ? log1pf(expf(x)) : x;
+// 1/x on the SFU (rcp.approx.ftz).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-// silu(z) = z · sigmoid(z) = z / (1 + e^{-z}).
-__device__ __forceinline__ float silu(float z) {
-    return __fdividef(z, 1.f + __expf(-z));
+// Coefficients of P(w) ~ 2·atanh(sqrt(w))/sqrt(w) on w in [0, 1/9], degree 4: fitted by
+// iteratively reweighted least squares on the relative error (approaching the minimax fit);
+// the approximation error is below 4e-9 relative, far under fp32 rounding.
+constexpr float kLog1pP0 = 2.0f;
+constexpr float kLog1pP1 = 0.6666631698608398f;
+constexpr float kLog1pP2 = 0.40024885535240173f;
+constexpr float kLog1pP3 = 0.27960675954818726f;
+constexpr float kLog1pP4 = 0.28178852796554565f;
+
+// softplus(x) = log(1 + e^x) = max(x, 0) + log1p(e), e = e^{-|x|} in (0, 1].
+// log1p(e) = 2·atanh(m) with m = e / (2 + e) in (0, 1/3] (the identity
+// ln((1+m)/(1-m)) = 2·atanh(m) at (1+m)/(1-m) = 1+e), evaluated as m·P(m²).
+// No branch and no overflow for any finite x; 13 instructions, 2 of them on the SFU.
+// Relative error about 3e-7 at x ~ -5 (dominated by rounding x·log2(e)).
+__device__ __forceinline__ float softplus(float x) {
+    const float e = ex2(-fabsf(x) * kLog2e);
+    const float m = e * rcp_approx(2.f + e);
+    const float w = m * m;
+    float p = fmaf(w, kLog1pP4, kLog1pP3);
+    p = fmaf(w, p, kLog1pP2);
+    p = fmaf(w, p, kLog1pP1);
+    p = fmaf(w, p, kLog1pP0);
+    return fmaf(m, p, fmaxf(x, 0.f));
 }
+
+// silu(z) = z · sigmoid(z) = z / (1 + e^{-z}); e^{-z} -> inf gives z · 0.
+__device__ __forceinline__ float silu(float z) {
+    return z * rcp_approx(1.f + ex2(-z * kLog2e));
+}
+
+// Packed fp32 pairs (one instruction for two lanes of arithmetic on sm_100+).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 ex2x2(float2 v) { return make_float2(ex2(v.x), ex2(v.y)); }
 
 template <typename T> __device__ __forceinline__ float to_f32(T v);
 template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }

@@ -1,0 +1,31 @@
+// Tile geometry of the forward-scan kernel instantiations, shared by the host dispatcher
+// (grid sizing, TMA boxes) and the kernel translation units.
+#pragma once
+
+namespace selscan {
+
+// State-split lane family: 32 channels per CTA; a channel's states are split over LPC lanes
+// (1, 2 or 4), so a CTA is LPC warps of 32/LPC channels each; T steps per chunk.
+#ifndef SS_LANE_T
+#define SS_LANE_T 64
+#endif
+#ifndef SS_LANE_STAGES
+#define SS_LANE_STAGES 2
+#endif
+#ifndef SS_LANE_UNROLL
+#define SS_LANE_UNROLL 2
+#endif
+constexpr int kLaneT = SS_LANE_T;
+constexpr int kLaneUnroll = SS_LANE_UNROLL;   // step groups unrolled together
+constexpr int kLaneStages = SS_LANE_STAGES;
+#ifndef SS_LANE_MINB4
+#define SS_LANE_MINB4 3
+#endif
+constexpr int lane_minb(int lpc) { return lpc == 4 ? SS_LANE_MINB4 : lpc == 2 ? 6 : 8; }
+
+// Segment-lane family (time-parallel; few channels, long sequences): 8 channels per CTA,
+// each warp holds 4 time segments of those 8 channels, 8 warps.  K = 7 steps per thread
+// keeps the swizzled tile reads free of bank conflicts for 8-channel rows.
+constexpr int kSegG = 1, kSegQ = 8, kSegK = 7, kSegStages = 3;
+
+}  // namespace selscan

@@ -22,6 +22,8 @@ struct FwdParams {
     int batch, L, Dm, N;
     int nchunks;
     int tiles_per_batch;
+    int chunk_steps;     // steps per chunk the host sized the grid and TMA boxes for
+    int tile_channels;   // channels per CTA the host sized them for
     unsigned int* err;   // device error word
 };
 

@@ -3,26 +3,41 @@
 
 #include <cuda_runtime.h>
 
+#include "fwd_configs.h"
 #include "fwd_params.h"
 
 namespace selscan {
 
-// Forward-scan kernel variants.  `ns` is the state count the kernel is built for (4, 8
-// or 16, N <= ns); `tma` selects the TMA-fed variant (which needs N == ns and 16-byte
-// aligned bases and row strides) over the plain-load variant.
+enum FwdFamily { kFamLane = 0, kFamSeg = 1 };
+
+// One forward-scan kernel instantiation.  `ns` is the state count it is built for (4, 8
+// or 16, with N <= ns); `lpc` the lane family's lanes per channel (1, 2 or 4, at most
+// ns/4); `tma` selects TMA-fed tiles (needs N == ns, 16-byte aligned bases and row strides)
+// over the plain-load fill.
 struct FwdVariant {
+    int family;
     int ns;
+    int lpc;
     bool tma;
 };
 
-// Channels per CTA and steps per chunk of the forward kernels (for grid sizing).
-int fwd_tile_channels();
-int fwd_chunk_steps();
+struct FwdGeom {
+    int tile_channels;   // channels per CTA
+    int box_channels;    // width of one u/Δ/z TMA box
+    int chunk_steps;     // steps per chunk (TMA box height)
+};
 
-cudaError_t launch_fwd_f32(const FwdVariant& v, const FwdParams& p, const FwdMaps& m,
+inline FwdGeom fwd_geometry(const FwdVariant& v) {
+    if (v.family == kFamSeg) return FwdGeom{8 * kSegG, 8 * kSegG, 4 * kSegQ * kSegK};
+    return FwdGeom{32, 32 / v.lpc, kLaneT};
+}
+
+cudaError_t launch_fwd_lane_f32(const FwdVariant& v, const FwdParams& p, const FwdMaps& m,
+                                cudaStream_t stream);
+cudaError_t launch_fwd_lane_bf16(const FwdVariant& v, const FwdParams& p, const FwdMaps& m,
+                                 cudaStream_t stream);
+cudaError_t launch_fwd_seg(const FwdVariant& v, bool bf16, const FwdParams& p, const FwdMaps& m,
                            cudaStream_t stream);
-cudaError_t launch_fwd_bf16(const FwdVariant& v, const FwdParams& p, const FwdMaps& m,
-                            cudaStream_t stream);
 cudaError_t launch_step(const StepParams& p, bool bf16, bool vec, cudaStream_t stream);
 
 }  // namespace selscan

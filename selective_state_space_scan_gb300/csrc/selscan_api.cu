@@ -20,9 +20,11 @@ namespace {
 
 constexpr int kVersion = 100;   // 0.1.0
 
-// Test hook: 0 = automatic choice, 1 = force the plain-load forward kernel,
-// 2 = force the TMA kernel (rejected with SS_ERR_UNSUPPORTED when not eligible).
-std::atomic<int> g_force_fwd_path{0};
+// Test hook overriding the automatic choice of forward kernel: family (-1 auto, 0 state-split
+// lane, 1 segment-lane), lanes per channel of the lane family (0 auto, 1, 2 or 4) and tile fill
+// (-1 auto, 0 plain loads, 1 TMA; a forced choice the arguments cannot use is
+// SS_ERR_UNSUPPORTED).
+std::atomic<int> g_force_family{-1}, g_force_lpc{0}, g_force_tma{-1};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -86,12 +88,14 @@ ss_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SS_OK : SS_ERR_
 // 3-D tiled descriptor over a [batch, rows, cols] tensor (cols contiguous) with a box of
 // [1, box_rows, box_cols]; rows/channels past the end read as zero.
 bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t cols, int64_t rows,
-              int64_t batch, int64_t row_stride, int64_t batch_stride, int box_cols, int box_rows) {
+              int64_t batch, int64_t row_stride, int64_t batch_stride, int box_cols, int box_rows,
+              bool swizzle) {
     auto enc = encode_fn();
     if (!enc) return false;
     const int64_t es = bf16 ? 2 : 4;
     const int row_bytes = box_cols * static_cast<int>(es);
-    CUtensorMapSwizzle sw = row_bytes >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+    CUtensorMapSwizzle sw = !swizzle         ? CU_TENSOR_MAP_SWIZZLE_NONE
+                          : row_bytes >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                           : row_bytes == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
                           : row_bytes == 32  ? CU_TENSOR_MAP_SWIZZLE_32B
                                              : CU_TENSOR_MAP_SWIZZLE_NONE;
@@ -145,10 +149,14 @@ ss_status ss_device_error(uint32_t* bits, int clear) {
     return SS_OK;
 }
 
-// Internal test hook (not part of the public header).
-int ss__force_fwd_path(int mode) {
-    if (mode < 0 || mode > 2) return -1;
-    return g_force_fwd_path.exchange(mode);
+// Internal test hook (not part of the public header); see g_force_family.
+int ss__force_fwd_variant(int family, int lpc, int tma) {
+    if (family < -1 || family > 1 || (lpc != 0 && lpc != 1 && lpc != 2 && lpc != 4) || tma < -1 || tma > 1)
+        return -1;
+    g_force_family.store(family);
+    g_force_lpc.store(lpc);
+    g_force_tma.store(tma);
+    return 0;
 }
 
 ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
@@ -191,10 +199,7 @@ ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias, 
         if (L > 1) return SS_ERR_INVALID_ARG;
     }
     if ((s.B_l < N || s.C_l < N) && L > 1) return SS_ERR_INVALID_ARG;
-    // grid limits of this kernel family
-    const int tile_w = fwd_tile_channels();
-    const int64_t tiles = (Dm + tile_w - 1) / tile_w;
-    if (L > INT32_MAX || Dm > INT32_MAX || batch * tiles > INT32_MAX) return SS_ERR_UNSUPPORTED;
+    if (L > INT32_MAX || Dm > INT32_MAX || batch > INT32_MAX) return SS_ERR_UNSUPPORTED;
     // alignment to the element type
     const void* io_ptrs[] = {u, delta_raw, B, C, y, z};
     for (const void* p : io_ptrs)
@@ -223,6 +228,29 @@ ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias, 
         if (overlap(sy, in) || overlap(sl, in)) return SS_ERR_INVALID_ARG;
     if (overlap(sy, sl)) return SS_ERR_INVALID_ARG;
 
+    // Kernel choice.  The lane family folds each (channel, state) chain sequentially, its
+    // parallelism being channels x LPC lanes; LPC grows until there are enough warps to fill
+    // the GPU.  With few rows even LPC = 4 is not enough (a long sequence at batch 1) and the
+    // segment-lane family, which runs time segments in parallel through the scan, takes over.
+    const int64_t tiles32 = batch * ((Dm + 31) / 32);
+    const int64_t want_warps = 1216;   // ~8 warps on each of GB300's 152 SMs
+    FwdVariant v;
+    v.ns = N <= 4 ? 4 : N <= 8 ? 8 : 16;
+    const int max_lpc = v.ns / 4;
+    v.lpc = 1;
+    while (v.lpc < max_lpc && tiles32 * v.lpc < want_warps) v.lpc *= 2;
+    v.family = tiles32 * v.lpc >= want_warps / 2 ? kFamLane : kFamSeg;
+    v.tma = true;
+    const int ff = g_force_family.load(), fl = g_force_lpc.load(), ft = g_force_tma.load();
+    if (ff >= 0) v.family = ff;
+    if (fl > 0) {
+        if (fl > max_lpc) return SS_ERR_UNSUPPORTED;
+        v.lpc = fl;
+    }
+    const FwdGeom geo = fwd_geometry(v);
+    const int64_t tiles = (Dm + geo.tile_channels - 1) / geo.tile_channels;
+    if (batch * tiles > INT32_MAX) return SS_ERR_UNSUPPORTED;
+
     FwdParams p;
     p.u = u; p.delta = delta_raw; p.z = z; p.Bm = B; p.Cm = C;
     p.bias = delta_bias; p.A_log = A_log; p.Dv = D; p.y = y; p.last_state = last_state;
@@ -233,16 +261,15 @@ ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias, 
     p.L = static_cast<int>(L);
     p.Dm = static_cast<int>(Dm);
     p.N = static_cast<int>(N);
-    const int T = fwd_chunk_steps();
-    p.nchunks = static_cast<int>((L + T - 1) / T);
+    p.nchunks = static_cast<int>((L + geo.chunk_steps - 1) / geo.chunk_steps);
     p.tiles_per_batch = static_cast<int>(tiles);
+    p.chunk_steps = geo.chunk_steps;
+    p.tile_channels = geo.tile_channels;
     p.err = device_error_ptr();
     if (!p.err) return SS_ERR_CUDA;
 
-    FwdVariant v;
-    v.ns = N <= 4 ? 4 : N <= 8 ? 8 : 16;
-    // TMA path: B/C rows exactly ns wide and a multiple of 16 bytes, 16-byte aligned
-    // bases and row/batch strides.
+    // TMA fill: B/C rows exactly ns wide and a multiple of 16 bytes, 16-byte aligned bases
+    // and row/batch strides.
     bool tma = (N == v.ns) && (N * es) % 16 == 0;
     const void* tma_ptrs[] = {u, delta_raw, B, C, z};
     for (const void* q : tma_ptrs)
@@ -255,22 +282,29 @@ ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias, 
         for (int64_t v2 : bstr)
             if (!tma_stride_ok(v2, es)) tma = false;
     }
-    const int force = g_force_fwd_path.load();
-    if (force == 1) tma = false;
+    if (ft == 0) tma = false;
 
     FwdMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     if (tma) {
-        // A shape the descriptor encoder rejects is served by the plain-load kernel.
-        tma = make_map(&maps.u, u, bf16, Dm, L, batch, s.u_l, s.u_b, tile_w, T) &&
-              make_map(&maps.delta, delta_raw, bf16, Dm, L, batch, s.delta_l, s.delta_b, tile_w, T) &&
-              (!z || make_map(&maps.z, z, bf16, Dm, L, batch, s.z_l, s.z_b, tile_w, T)) &&
-              make_map(&maps.B, B, bf16, N, L, batch, s.B_l, s.B_b, v.ns, T) &&
-              make_map(&maps.C, C, bf16, N, L, batch, s.C_l, s.C_b, v.ns, T);
+        // The segment-lane kernel reads its tiles through the hardware swizzle; the lane
+        // kernel reads whole rows of its own sub-tiles and needs none.  A shape the
+        // descriptor encoder rejects is served by the plain-load fill.
+        const bool sw = v.family == kFamSeg;
+        const int bw = geo.box_channels, bh = geo.chunk_steps;
+        tma = make_map(&maps.u, u, bf16, Dm, L, batch, s.u_l, s.u_b, bw, bh, sw) &&
+              make_map(&maps.delta, delta_raw, bf16, Dm, L, batch, s.delta_l, s.delta_b, bw, bh, sw) &&
+              (!z || make_map(&maps.z, z, bf16, Dm, L, batch, s.z_l, s.z_b, bw, bh, sw)) &&
+              make_map(&maps.B, B, bf16, N, L, batch, s.B_l, s.B_b, v.ns, bh, sw) &&
+              make_map(&maps.C, C, bf16, N, L, batch, s.C_l, s.C_b, v.ns, bh, sw);
     }
-    if (force == 2 && !tma) return SS_ERR_UNSUPPORTED;
+    if (ft == 1 && !tma) return SS_ERR_UNSUPPORTED;
     v.tma = tma;
-    const cudaError_t e = bf16 ? launch_fwd_bf16(v, p, maps, stream) : launch_fwd_f32(v, p, maps, stream);
+    cudaError_t e;
+    if (v.family == kFamSeg)
+        e = launch_fwd_seg(v, bf16, p, maps, stream);
+    else
+        e = bf16 ? launch_fwd_lane_bf16(v, p, maps, stream) : launch_fwd_lane_f32(v, p, maps, stream);
     return cuda_status(e);
 }
 

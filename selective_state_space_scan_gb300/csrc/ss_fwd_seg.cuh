@@ -1,4 +1,4 @@
-// Selective-scan forward kernel for sm_103a.
+// Selective-scan forward kernel, segment-lane layout (time-parallel inside a warp), for sm_103a.
 //
 // What it computes (per batch row b, channel d, state n, step t; h_{-1} = 0):
 //   Δ_t   = softplus(delta_raw[b,t,d] + delta_bias[d])
@@ -174,14 +174,15 @@ __device__ __forceinline__ void issue_stage_tma(uint8_t* st, uint64_t* bar, cons
 
 template <class Cfg, bool USE_TMA>
 __global__ void __launch_bounds__(Cfg::THREADS)
-ss_fwd_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
+ss_fwd_seg_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     using TIO = typename Cfg::TIO;
     constexpr int W = Cfg::W, K = Cfg::K, Q = Cfg::Q, NS = Cfg::NS, NQ = Cfg::NQ, T = Cfg::T;
     constexpr int STAGES = USE_TMA ? Cfg::STAGES : 1;
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // Round up to 1024 bytes (the swizzle period) by pointer arithmetic on the shared array,
+    // keeping every pointer visibly in the shared window.
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     float* aux = reinterpret_cast<float*>(smem + STAGES * Cfg::STAGE_BYTES);
     float* sA = aux + Cfg::AUX_A;
     float* carry = aux + Cfg::AUX_CARRY;
@@ -190,6 +191,12 @@ ss_fwd_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     volatile int* abort_flag = reinterpret_cast<volatile int*>(aux + Cfg::AUX_FLOATS);
     uint64_t* full = reinterpret_cast<uint64_t*>(aux + Cfg::AUX_FLOATS + 16);
 
+    // A grid or TMA box sized for another tile shape would never complete the stage
+    // barriers: refuse to run, and say so.
+    if (p.chunk_steps != Cfg::T || p.tile_channels != Cfg::W) {
+        if (threadIdx.x == 0 && p.err) atomicOr(p.err, kErrGeometry);
+        return;
+    }
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int w_lo = lane & 7, s_lo = lane >> 3;

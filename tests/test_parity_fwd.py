@@ -23,26 +23,33 @@ def _need_gpu():
     assert ss.device_error(clear=True) == 0
 
 
-class _ForcePath:
-    """Select the forward kernel's tile-load path (0 auto, 1 plain loads, 2 TMA)."""
-    def __init__(self, mode):
-        self.mode = mode
+class ForceVariant:
+    """Pin the forward kernel: family (-1 auto, 0 state-split lane, 1 segment-lane), lanes per
+    channel of the lane family (0 auto, 1, 2, 4), tile fill (-1 auto, 0 plain, 1 TMA)."""
+    def __init__(self, family=-1, lpc=0, tma=-1):
+        self.args = (family, lpc, tma)
 
     def __enter__(self):
-        f = ss.lib().ss__force_fwd_path
-        f.argtypes = [ctypes.c_int]
-        self.prev = f(self.mode)
+        f = ss.lib().ss__force_fwd_variant
+        f.argtypes = [ctypes.c_int] * 3
+        assert f(*self.args) == 0
 
     def __exit__(self, *exc):
-        ss.lib().ss__force_fwd_path(self.prev)
+        ss.lib().ss__force_fwd_variant(-1, 0, -1)
 
 
-def run_gpu(w, with_last=True, path=0):
+# every kernel instantiation family x warps x fill
+VARIANTS = [(0, 1, 1), (0, 2, 1), (0, 4, 1), (1, 0, 1), (0, 1, 0), (0, 2, 0), (0, 4, 0), (1, 0, 0)]
+VARIANT_IDS = ["lane1-tma", "lane2-tma", "lane4-tma", "seg-tma", "lane1-plain", "lane2-plain",
+               "lane4-plain", "seg-plain"]
+
+
+def run_gpu(w, with_last=True, variant=(-1, 0, -1)):
     a = w.arrays
     u, dr, z = to_dev(a["u"], w.io), to_dev(a["delta_raw"], w.io), to_dev(a["z"], w.io)
     Bm, Cm = to_dev(a["B"], w.io), to_dev(a["C"], w.io)
     last = torch.full((w.batch, w.Dm, w.N), float("nan"), device="cuda") if with_last else None
-    with _ForcePath(path):
+    with ForceVariant(*variant):
         y = ss.ss_fwd(u, dr, f32dev(a["delta_bias"]), f32dev(a["A_log"]), Bm, Cm, f32dev(a["D"]), z,
                       last_state=last)
     torch.cuda.synchronize()
@@ -54,11 +61,11 @@ def run_oracle(w):
     return oracle.ss_fwd(a["u"], a["delta_raw"], a["delta_bias"], a["A_log"], a["B"], a["C"], a["D"], a["z"])
 
 
-def check(w, path=0, with_last=True):
-    y, last = run_gpu(w, with_last, path)
+def check(w, variant=(-1, 0, -1), with_last=True):
+    y, last = run_gpu(w, with_last, variant)
     ry, rlast, mag = run_oracle(w)
     assert_fwd_close(w.io, y, ry, mag, last, rlast if with_last else None,
-                     what=f"{w.name} b={w.batch} L={w.L} Dm={w.Dm} N={w.N} {w.io} path={path}")
+                     what=f"{w.name} b={w.batch} L={w.L} Dm={w.Dm} N={w.N} {w.io} variant={variant}")
     return y, last
 
 
@@ -94,19 +101,40 @@ def test_channel_counts(Dm):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("path", [1, 2])
-def test_tma_and_plain_paths_agree(io, path):
-    w = synth.fwd_inputs(2, 500, 96, 16, io=io, seed=7)
-    check(w, path=path)
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+def test_every_kernel_variant(io, variant):
+    """Each instantiation on a ragged shape (L and Dm not multiples of any tile)."""
+    check(synth.fwd_inputs(2, 531, 72, 16, io=io, seed=7), variant=variant)
 
 
-def test_paths_identical_to_each_other():
-    """Both tile-load paths feed the same arithmetic in the same order: bitwise equal."""
+@pytest.mark.parametrize("N", [3, 4, 8, 12])
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+def test_every_kernel_variant_small_state(N, variant):
+    ns = 4 if N <= 4 else 8 if N <= 8 else 16
+    if variant[0] == 0 and variant[1] > ns // 4:
+        pytest.skip("a channel's states split over more lanes than it has state quads")
+    if N not in (4, 8, 16) and variant[2] == 1:
+        variant = (variant[0], variant[1], -1)   # TMA needs N in {4, 8, 16}: plain fill
+    w = synth.fwd_inputs(1, 203, 40, N, seed=70 + N)
+    y, last = run_gpu(w, variant=variant)
+    ry, rlast, mag = run_oracle(w)
+    assert_fwd_close("f32", y, ry, mag, last, rlast, what=f"N={N} variant={variant}")
+
+
+@pytest.mark.parametrize("family,q", [(0, 1), (0, 2), (0, 4), (1, 0)])
+def test_fills_identical(family, q):
+    """TMA and plain-load fills feed the same arithmetic in the same order: bitwise equal."""
     w = synth.fwd_inputs(2, 300, 64, 16, seed=8)
-    y1, l1 = run_gpu(w, path=1)
-    y2, l2 = run_gpu(w, path=2)
+    y1, l1 = run_gpu(w, variant=(family, q, 0))
+    y2, l2 = run_gpu(w, variant=(family, q, 1))
     np.testing.assert_array_equal(y1, y2)
     np.testing.assert_array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("name", ["mamba130m", "long32k"])
+@pytest.mark.parametrize("variant", [(0, 4, 1), (0, 1, 1), (1, 0, 1)], ids=["lane4", "lane1", "seg"])
+def test_full_size_both_families(name, variant):
+    check(synth.config(name), variant=variant)
 
 
 @pytest.mark.parametrize("flags", ["no_z", "no_D", "no_bias", "none", "no_last"])
@@ -145,14 +173,15 @@ def test_strided_inputs(io, pad):
         assert torch.all(ybig[..., 64:].float() == 7.0), "wrote outside y"
 
 
-def test_batch_rows_are_independent():
+@pytest.mark.parametrize("variant", [(0, 4, 1), (1, 0, 1)], ids=["lane4", "seg"])
+def test_batch_rows_are_independent(variant):
     w = synth.fwd_inputs(3, 200, 48, 16, seed=12)
-    y, last = run_gpu(w)
+    y, last = run_gpu(w, variant=variant)
     for b in range(3):
         sub = synth.Workload("row", 1, 200, 48, 16, "f32", 12,
                              {k: (v[b:b + 1] if k in ("u", "delta_raw", "z", "B", "C") else v)
                               for k, v in w.arrays.items()})
-        yb, lb = run_gpu(sub)
+        yb, lb = run_gpu(sub, variant=variant)
         np.testing.assert_array_equal(yb[0], y[b])
         np.testing.assert_array_equal(lb[0], last[b])
 
