@@ -68,6 +68,58 @@ def alg_bytes(w) -> int:
     return w.batch * w.L * (4 * w.Dm + 2 * w.N) * s + w.Dm * (w.N + 2) * 4 + w.batch * w.Dm * w.N * 4
 
 
+SFU_EX2_PER_CLK_PER_SM = 32      # MUFU ex2 results per SM per clock on GB300 (measured 31.6)
+GB300_SMS = 152
+GB300_MAX_SM_MHZ = 2070.0
+
+
+def decay_ex2_per_step(w) -> int:
+    """One exp2 per state update: the decay exp(Δ·A) of every (b, t, d, n)."""
+    return updates_per_step(w)
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources: a traffic figure measured on other sources is stale."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "selective_state_space_scan_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
+                    glob.glob(os.path.join(csrc, "*.h"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, kernel: str):
+    """DRAM bytes (read + write) per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(workload)
+    if not rec or rec.get("kernel") != kernel or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The largest value over all ranks (the timed region of the slowest rank)."""
+    if dist is None or not dist.is_available() or not dist.is_initialized():
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, world: int, total_ms: float, steps: int) -> float:
+    """Whole-job units per second: every rank's units over the slowest rank's time per step."""
+    return units_per_rank * world / (total_ms / 1e3 / steps)
+
+
 def updates_per_step(w) -> int:
     if w.name.startswith("decode"):
         return w.batch * w.Dm * w.N * DECODE_LAYERS
@@ -221,21 +273,25 @@ def run_ours(args, w, rank, world, local_rank):
             ev[i][1].record(stream)
         end.record(stream)
         barrier()
-    total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(start.elapsed_time(end), dist, dev)
     per_launch_ms = [a.elapsed_time(b) for a, b in ev]
-    if dist is not None:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
     err = ss.device_error(clear=True)
     if err:
         raise RuntimeError(f"device error word {err:#x} after the timed region")
+    if decode:
+        kernel = "ss_step_kernel"
+    else:
+        namef = ss.lib().ss__fwd_kernel_name
+        namef.restype = ctypes.c_char_p
+        namef.argtypes = [ctypes.c_int64] * 3
+        kernel = namef(w.batch, w.Dm, w.N).decode()
 
     # end-to-end through the public API: pinned host inputs -> device -> ss_fwd -> host output
     e2e = None
     if not args.no_e2e and not decode:
         e2e = run_e2e(args, w, torch, ss, dev, tensors, y, last, barrier)
-    return dict(total_ms=total_ms, per_launch_ms=per_launch_ms, clocks=clk.summary(), e2e=e2e)
+    return dict(total_ms=total_ms, per_launch_ms=per_launch_ms, clocks=clk.summary(), e2e=e2e,
+                kernel=kernel)
 
 
 def run_e2e(args, w, torch, ss, dev, t, y, last, barrier):
@@ -342,7 +398,7 @@ def main():
     res = run_ours(args, w, rank, world, local_rank)
     units = updates_per_step(w)
     ms_step = res["total_ms"] / args.steps
-    value = units * world / (res["total_ms"] / 1e3 / args.steps)
+    value = job_throughput(units, world, res["total_ms"], args.steps)
     launch_ms = statistics.mean(res["per_launch_ms"])
     if w.name.startswith("decode"):
         launch_ms = launch_ms / DECODE_LAYERS    # per ss_step kernel
@@ -350,11 +406,24 @@ def main():
     else:
         bytes_launch = alg_bytes(w)
     hbm_peak, peak_kind = peaks()
-    achieved = bytes_launch / (launch_ms / 1e3) / 1e9
-    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-            "frac": achieved / hbm_peak, "traffic": None, "peak_source": peak_kind,
-            "kernel": "ss_step_kernel" if w.name.startswith("decode") else "ss_fwd_kernel",
-            "launch_ms": launch_ms}
+    # Roofline of the dominant kernel: the slower of moving the algorithmic bytes at the
+    # measured HBM copy bandwidth and issuing one exp2 per state update at the SFU rate.
+    sfu_peak = GB300_SMS * SFU_EX2_PER_CLK_PER_SM * GB300_MAX_SM_MHZ * 1e6     # ex2 / s
+    ex2_launch = decay_ex2_per_step(w) / (DECODE_LAYERS if w.name.startswith("decode") else 1)
+    t_hbm = bytes_launch / (hbm_peak * 1e9)
+    t_sfu = ex2_launch / sfu_peak
+    if t_hbm >= t_sfu:
+        achieved = bytes_launch / (launch_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"}
+    else:
+        achieved = ex2_launch / (launch_ms / 1e3) / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": sfu_peak / 1e12, "unit": "Tex2/s",
+                "frac": achieved * 1e12 / sfu_peak,
+                "peak_source": "152 SMs x 32 MUFU ex2/clk x 2070 MHz (ex2 rate measured at 31.6/clk/SM)"}
+    roof.update({"traffic": measured_traffic(w.name, res["kernel"]), "kernel": res["kernel"],
+                 "launch_ms": launch_ms, "alg_bytes_per_launch": bytes_launch,
+                 "decay_ex2_per_launch": ex2_launch, "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6})
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,

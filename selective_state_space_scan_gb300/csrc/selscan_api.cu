@@ -113,6 +113,20 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t cols, int64_t
     return r == CUDA_SUCCESS;
 }
 
+// Automatic forward-kernel choice (see ss_fwd).
+FwdVariant choose_fwd_variant(int64_t batch, int64_t Dm, int64_t N) {
+    const int64_t tiles32 = batch * ((Dm + 31) / 32);
+    const int64_t want_warps = 1216;   // ~8 warps on each of GB300's 152 SMs
+    FwdVariant v;
+    v.ns = N <= 4 ? 4 : N <= 8 ? 8 : 16;
+    const int max_lpc = v.ns / 4;
+    v.lpc = 1;
+    while (v.lpc < max_lpc && tiles32 * v.lpc < want_warps) v.lpc *= 2;
+    v.family = tiles32 * v.lpc >= want_warps / 2 ? kFamLane : kFamSeg;
+    v.tma = true;
+    return v;
+}
+
 bool tma_stride_ok(int64_t stride_elems, int64_t es) {
     return stride_elems > 0 && (stride_elems * es) % 16 == 0 && stride_elems * es < (int64_t(1) << 40);
 }
@@ -147,6 +161,18 @@ ss_status ss_device_error(uint32_t* bits, int clear) {
         if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return SS_ERR_CUDA;
     }
     return SS_OK;
+}
+
+// Internal reporting hook (not part of the public header): the forward kernel ss_fwd would
+// launch for these sizes, as "<family>-<lanes>" ("lane-4", "seg-0"), forced choices included.
+const char* ss__fwd_kernel_name(int64_t batch, int64_t Dm, int64_t N) {
+    if (N < 1 || N > 16) return "unsupported";
+    FwdVariant v = choose_fwd_variant(batch, Dm, N);
+    if (g_force_family.load() >= 0) v.family = g_force_family.load();
+    if (g_force_lpc.load() > 0) v.lpc = g_force_lpc.load();
+    if (v.family == kFamSeg) return "ss_fwd_seg_kernel";
+    return v.lpc == 1 ? "ss_fwd_lane_kernel(lpc=1)" : v.lpc == 2 ? "ss_fwd_lane_kernel(lpc=2)"
+                                                               : "ss_fwd_lane_kernel(lpc=4)";
 }
 
 // Internal test hook (not part of the public header); see g_force_family.
@@ -232,15 +258,8 @@ ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias, 
     // parallelism being channels x LPC lanes; LPC grows until there are enough warps to fill
     // the GPU.  With few rows even LPC = 4 is not enough (a long sequence at batch 1) and the
     // segment-lane family, which runs time segments in parallel through the scan, takes over.
-    const int64_t tiles32 = batch * ((Dm + 31) / 32);
-    const int64_t want_warps = 1216;   // ~8 warps on each of GB300's 152 SMs
-    FwdVariant v;
-    v.ns = N <= 4 ? 4 : N <= 8 ? 8 : 16;
+    FwdVariant v = choose_fwd_variant(batch, Dm, N);
     const int max_lpc = v.ns / 4;
-    v.lpc = 1;
-    while (v.lpc < max_lpc && tiles32 * v.lpc < want_warps) v.lpc *= 2;
-    v.family = tiles32 * v.lpc >= want_warps / 2 ? kFamLane : kFamSeg;
-    v.tma = true;
     const int ff = g_force_family.load(), fl = g_force_lpc.load(), ft = g_force_tma.load();
     if (ff >= 0) v.family = ff;
     if (fl > 0) {

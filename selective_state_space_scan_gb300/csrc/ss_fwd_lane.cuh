@@ -231,92 +231,98 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
         const int64_t tbase = static_cast<int64_t>(ch) * T;
         const int64_t left = L - tbase;                     // steps of this chunk before L
         const bool whole = left >= T;
-        constexpr int G = T / LPC;                          // step groups in the chunk
+        constexpr int GT = T / LPC;                         // step groups in the chunk
+        constexpr int G = GT > 16 ? 16 : GT;                // groups per sub-block (register budget)
+        static_assert(GT % G == 0, "chunk must be whole sub-blocks");
+#pragma unroll 1
+        for (int g0 = 0; g0 < GT; g0 += G) {
 
-        // Phase 1: Δ and Δ·u of the steps this lane prepares (step g·LPC + j of each group;
-        // zero past L, i.e. identity pairs).  G independent softplus chains.
-        float dd[G], du[G];
+            // Phase 1: Δ and Δ·u of the steps this lane prepares (step g·LPC + j of each group;
+            // zero past L, i.e. identity pairs).  G independent softplus chains.
+            float dd[G], du[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const int r = g * LPC + j;
-            const float x = softplus(to_f32<TIO>(td[r * CPW + c]) + bias_w);
-            dd[g] = x;
-            du[g] = x * to_f32<TIO>(tu[r * CPW + c]);
-        }
-        if (!whole) {
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-                if (g * LPC + j >= left) dd[g] = du[g] = 0.f;
-        }
-        // Phase 2: the sequential fold.  Step g·LPC + k takes its Δ, Δ·u from lane (c, k);
-        // the C·h partial sums of the channel's LPC lanes are reduce-scattered so that lane
-        // (c, j) ends with the sum of step g·LPC + j.
-        float yv[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float dk[LPC], uk[LPC];
-#pragma unroll
-            for (int k = 0; k < LPC; ++k) {
-                dk[k] = LPC == 1 ? dd[g] : __shfl_sync(0xffffffffu, dd[g], k * CPW + c);
-                uk[k] = LPC == 1 ? du[g] : __shfl_sync(0xffffffffu, du[g], k * CPW + c);
+            for (int g = 0; g < G; ++g) {
+                const int r = (g0 + g) * LPC + j;
+                const float x = softplus(to_f32<TIO>(td[r * CPW + c]) + bias_w);
+                dd[g] = x;
+                du[g] = x * to_f32<TIO>(tu[r * CPW + c]);
             }
-            float yp[LPC];
+            if (!whole) {
 #pragma unroll
-            for (int k = 0; k < LPC; ++k) {
-                const float2 dl2 = make_float2(dk[k], dk[k]), du2 = make_float2(uk[k], uk[k]);
-                const int row = g * LPC + k;
-                float2 acc = make_float2(0.f, 0.f);
+                for (int g = 0; g < G; ++g)
+                    if ((g0 + g) * LPC + j >= left) dd[g] = du[g] = 0.f;
+            }
+            // Phase 2: the sequential fold.  Step g·LPC + k takes its Δ, Δ·u from lane (c, k);
+            // the C·h partial sums of the channel's LPC lanes are reduce-scattered so that lane
+            // (c, j) ends with the sum of step g·LPC + j.
+            float yv[G];
 #pragma unroll
-                for (int qq = 0; qq < QPL; ++qq) {
-                    const float4 B4 = *reinterpret_cast<const float4*>(tB + row * NS + n0 + 4 * qq);
-                    const float4 C4 = *reinterpret_cast<const float4*>(tC + row * NS + n0 + 4 * qq);
-                    const float2 a01 = ex2x2(mul2(dl2, A2[qq][0]));
-                    const float2 a23 = ex2x2(mul2(dl2, A2[qq][1]));
-                    h[qq][0] = fma2(a01, h[qq][0], mul2(du2, make_float2(B4.x, B4.y)));
-                    h[qq][1] = fma2(a23, h[qq][1], mul2(du2, make_float2(B4.z, B4.w)));
-                    acc = fma2(make_float2(C4.x, C4.y), h[qq][0], acc);
-                    acc = fma2(make_float2(C4.z, C4.w), h[qq][1], acc);
+            for (int g = 0; g < G; ++g) {
+                float dk[LPC], uk[LPC];
+#pragma unroll
+                for (int k = 0; k < LPC; ++k) {
+                    dk[k] = LPC == 1 ? dd[g] : __shfl_sync(0xffffffffu, dd[g], k * CPW + c);
+                    uk[k] = LPC == 1 ? du[g] : __shfl_sync(0xffffffffu, du[g], k * CPW + c);
                 }
-                yp[k] = acc.x + acc.y;
-            }
-            if constexpr (LPC == 1) {
-                yv[g] = yp[0];
-            } else if constexpr (LPC == 2) {
-                const bool hi = j & 1;
-                const float send = hi ? yp[0] : yp[1];
-                const float keep = hi ? yp[1] : yp[0];
-                yv[g] = keep + __shfl_xor_sync(0xffffffffu, send, CPW);
-            } else {
-                // transpose through this warp's shared scratch: lane (c, j) stores its four
-                // partials, then reads the four slices' partials of step j
-                *reinterpret_cast<float4*>(xbuf + lane * 4) = make_float4(yp[0], yp[1], yp[2], yp[3]);
-                __syncwarp();
-                float sum = 0.f;
+                float yp[LPC];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) sum += xbuf[(k * CPW + c) * 4 + j];
-                yv[g] = sum;
-                __syncwarp();
-            }
-        }
-        // Phase 3: D skip, z gate, store (G independent chains).
-        if (d_ok) {
-            char* yrow = reinterpret_cast<char*>(static_cast<TIO*>(p.y) + b * p.y_b + (tbase + j) * p.y_l + d);
-            const int nst = whole ? G : static_cast<int>((left - j + LPC - 1) / LPC);   // steps to store
-            if (has_z && nst == G) {
+                for (int k = 0; k < LPC; ++k) {
+                    const float2 dl2 = make_float2(dk[k], dk[k]), du2 = make_float2(uk[k], uk[k]);
+                    const int row = (g0 + g) * LPC + k;
+                    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const int r = g * LPC + j;
-                    const float v = fmaf(D_w, to_f32<TIO>(tu[r * CPW + c]), yv[g]) * silu(to_f32<TIO>(tz[r * CPW + c]));
-                    *reinterpret_cast<TIO*>(yrow + g * LPC * ystride) = from_f32<TIO>(v);
+                    for (int qq = 0; qq < QPL; ++qq) {
+                        const float4 B4 = *reinterpret_cast<const float4*>(tB + row * NS + n0 + 4 * qq);
+                        const float4 C4 = *reinterpret_cast<const float4*>(tC + row * NS + n0 + 4 * qq);
+                        const float2 a01 = ex2x2(mul2(dl2, A2[qq][0]));
+                        const float2 a23 = ex2x2(mul2(dl2, A2[qq][1]));
+                        h[qq][0] = fma2(a01, h[qq][0], mul2(du2, make_float2(B4.x, B4.y)));
+                        h[qq][1] = fma2(a23, h[qq][1], mul2(du2, make_float2(B4.z, B4.w)));
+                        acc = fma2(make_float2(C4.x, C4.y), h[qq][0], acc);
+                        acc = fma2(make_float2(C4.z, C4.w), h[qq][1], acc);
+                    }
+                    yp[k] = acc.x + acc.y;
                 }
-            } else {
+                if constexpr (LPC == 1) {
+                    yv[g] = yp[0];
+                } else if constexpr (LPC == 2) {
+                    const bool hi = j & 1;
+                    const float send = hi ? yp[0] : yp[1];
+                    const float keep = hi ? yp[1] : yp[0];
+                    yv[g] = keep + __shfl_xor_sync(0xffffffffu, send, CPW);
+                } else {
+                    // transpose through this warp's shared scratch: lane (c, j) stores its four
+                    // partials, then reads the four slices' partials of step j
+                    *reinterpret_cast<float4*>(xbuf + lane * 4) = make_float4(yp[0], yp[1], yp[2], yp[3]);
+                    __syncwarp();
+                    float sum = 0.f;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    if (g < nst) {
-                        const int r = g * LPC + j;
-                        float v = fmaf(D_w, to_f32<TIO>(tu[r * CPW + c]), yv[g]);
-                        if (has_z) v *= silu(to_f32<TIO>(tz[r * CPW + c]));
+                    for (int k = 0; k < 4; ++k) sum += xbuf[(k * CPW + c) * 4 + j];
+                    yv[g] = sum;
+                    __syncwarp();
+                }
+            }
+            // Phase 3: D skip, z gate, store (G independent chains).
+            if (d_ok) {
+                char* yrow = reinterpret_cast<char*>(static_cast<TIO*>(p.y) + b * p.y_b + (tbase + g0 * LPC + j) * p.y_l + d);
+                const int64_t rem = left - g0 * LPC - j;          // steps of this lane's column before L
+                const int nst = whole ? G : (rem <= 0 ? 0 : rem >= int64_t(G) * LPC ? G : static_cast<int>((rem + LPC - 1) / LPC));
+                if (has_z && nst == G) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const int r = (g0 + g) * LPC + j;
+                        const float v = fmaf(D_w, to_f32<TIO>(tu[r * CPW + c]), yv[g]) * silu(to_f32<TIO>(tz[r * CPW + c]));
                         *reinterpret_cast<TIO*>(yrow + g * LPC * ystride) = from_f32<TIO>(v);
+                    }
+                } else {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        if (g < nst) {
+                            const int r = (g0 + g) * LPC + j;
+                            float v = fmaf(D_w, to_f32<TIO>(tu[r * CPW + c]), yv[g]);
+                            if (has_z) v *= silu(to_f32<TIO>(tz[r * CPW + c]));
+                            *reinterpret_cast<TIO*>(yrow + g * LPC * ystride) = from_f32<TIO>(v);
+                        }
                     }
                 }
             }

@@ -1,0 +1,63 @@
+"""Host-side pieces of bench.py that need no GPU: the multi-rank timing aggregation over a
+2-rank gloo group, the whole-job throughput and the algorithmic byte counts."""
+import os
+import socket
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from selective_state_space_scan_gb300 import synth  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    slowest = bench.max_over_ranks(10.0 + rank, dist)          # rank 1 is the slower one
+    value = bench.job_throughput(1000, world, slowest, steps=4)
+    out.put((rank, slowest, value))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_aggregation_gloo():
+    torch = pytest.importorskip("torch")
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, slowest, value in res:
+        assert slowest == 11.0                                  # max over ranks, on every rank
+        assert value == pytest.approx(1000 * 2 / (11.0e-3 / 4))
+
+
+def test_single_process_aggregation_is_identity():
+    assert bench.max_over_ranks(3.5) == 3.5
+
+
+def test_algorithmic_bytes_match_the_formula():
+    w = synth.Workload("mamba130m", 8, 2048, 1536, 16, "f32", 1)
+    assert bench.alg_bytes(w) == 405_647_360
+    w = synth.Workload("long32k", 1, 32768, 1536, 16, "f32", 2)
+    assert bench.alg_bytes(w) == 809_709_568
+    w = synth.Workload("mamba2p8b_bf16", 4, 8192, 5120, 16, "bf16", 3)
+    assert bench.alg_bytes(w) == 1_345_953_792
+    w = synth.Workload("decode1p4b", 64, 1, 4096, 16, "f32", 4)
+    assert bench.alg_bytes(w) == 48 * 38_035_456
