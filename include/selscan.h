@@ -31,8 +31,9 @@
  *   - Types: u, delta_raw, z, B, C and y are `io_dtype` (fp32 or bf16); A_log, D,
  *     delta_bias, last_state and the decode state are always fp32.  Arithmetic and
  *     the recurrent state are fp32 in both cases.
- *   - Thread safety: calls are reentrant; the only process-wide state is the cached
- *     driver entry point used to build TMA descriptors.
+ *   - Thread safety: calls are reentrant.  Process-wide state: the cached driver entry
+ *     point used to build TMA descriptors, the per-device error word, and a call counter that
+ *     tags ss_fwd_ws hand-overs.
  */
 #ifndef SELSCAN_H
 #define SELSCAN_H
@@ -91,6 +92,37 @@ ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias,
                  const float* A_log, const void* B, const void* C, const float* D,
                  const void* z, void* y, float* last_state, int64_t batch, int64_t L,
                  int64_t Dm, int64_t N, const ss_fwd_strides* strides, void* stream);
+
+/*
+ * Forward pass with a caller-provided workspace; same arguments and result as ss_fwd.
+ *
+ * ss_fwd runs one CTA per tile of channels over the whole sequence.  ss_fwd_ws instead
+ * splits the (tile, chunk) work into equal contiguous ranges, one per CTA the device can hold
+ * at once (a cooperative launch), so every SM gets the same amount of work; a range that starts
+ * inside a tile takes the state at its start from the CTA before it.  That hand-over needs
+ * the workspace: one flag and one tile state per CTA.  This is the same carry-across-chunks
+ * scan ("mamba-metal: Apple Silicon で Mamba を動かす", section "チャンク間 running prefix")
+ * with the carry passed between CTAs instead of kept in one CTA; results are bitwise equal to
+ * ss_fwd's.
+ *   workspace        device memory, 256-byte aligned, at least workspace_bytes =
+ *                    ss_fwd_workspace_size(...) bytes, zero-filled before its first use (the
+ *                    library never needs it cleared again).  Calls that share a workspace must
+ *                    not run concurrently on the device.
+ *   workspace NULL   behaves exactly like ss_fwd.
+ * Too small a workspace returns SS_ERR_INVALID_ARG; a misaligned one SS_ERR_MISALIGNED.  When
+ * the arguments cannot use TMA-fed tiles (see ss_fwd_strides) the workspace is not used.
+ */
+ss_status ss_fwd_ws(const void* u, const void* delta_raw, const float* delta_bias,
+                    const float* A_log, const void* B, const void* C, const float* D,
+                    const void* z, void* y, float* last_state, int64_t batch, int64_t L,
+                    int64_t Dm, int64_t N, const ss_fwd_strides* strides, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes ss_fwd_ws needs for these sizes on the current device (0: it needs none,
+ * or the sizes are invalid).  Depends on the device's SM count and the kernel's occupancy.
+ */
+size_t ss_fwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dtype);
 
 /*
  * Element strides of the decode tensors.  x, delta_raw, z, y are [batch, Dm] with channel

@@ -12,7 +12,7 @@ from typing import Optional
 
 from . import _build
 
-__all__ = ["ss_fwd", "ss_step", "SelscanError", "lib", "device_error", "version",
+__all__ = ["ss_fwd", "ss_step", "ss_fwd_workspace_size", "SelscanError", "lib", "device_error", "version",
            "status_string", "SS_F32", "SS_BF16", "FwdStrides", "StepStrides"]
 
 SS_F32, SS_BF16 = 0, 1
@@ -48,6 +48,10 @@ def lib() -> ctypes.CDLL:
         vp, i64 = ctypes.c_void_p, ctypes.c_int64
         L.ss_fwd.argtypes = [vp] * 10 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp]
         L.ss_fwd.restype = ctypes.c_int
+        L.ss_fwd_ws.argtypes = [vp] * 10 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp, ctypes.c_size_t, vp]
+        L.ss_fwd_ws.restype = ctypes.c_int
+        L.ss_fwd_workspace_size.argtypes = [i64] * 4 + [ctypes.c_int32]
+        L.ss_fwd_workspace_size.restype = ctypes.c_size_t
         L.ss_step.argtypes = [vp] * 10 + [i64] * 3 + [ctypes.POINTER(StepStrides), vp]
         L.ss_step.restype = ctypes.c_int
         L.ss_status_string.argtypes = [ctypes.c_int]
@@ -103,13 +107,41 @@ def _check_inner(t, name):
         raise ValueError(f"{name}: the last axis must have stride 1")
 
 
+_WORKSPACES = {}
+_WS_SIZES = {}
+
+
+def workspace_for(device, stream_handle, nbytes: int):
+    """A zero-filled, 256-byte aligned device buffer of at least nbytes, cached per (device,
+    stream) and grown when needed; calls on one stream are ordered, so they never overlap on
+    the GPU while sharing it."""
+    import torch
+    key = (str(device), stream_handle)
+    ws = _WORKSPACES.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 1), dtype=torch.uint8, device=device)
+        _WORKSPACES[key] = ws
+    return ws
+
+
+def ss_fwd_workspace_size(batch, L, Dm, N, io_dtype=SS_F32) -> int:
+    """Bytes of workspace ss_fwd_ws needs on the current device (0: none)."""
+    import torch
+    key = (torch.cuda.current_device() if torch.cuda.is_available() else -1, batch, L, Dm, N, io_dtype)
+    if key not in _WS_SIZES:
+        _WS_SIZES[key] = int(lib().ss_fwd_workspace_size(batch, L, Dm, N, io_dtype))
+    return _WS_SIZES[key]
+
+
 def ss_fwd(u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, last_state=None,
-           stream=None):
+           stream=None, balanced=False):
     """Selective-scan forward pass through the C ABI.
 
     u, delta_raw, z: [batch, L, Dm]; B, C: [batch, L, N] (same dtype, float32 or bfloat16);
     A_log [Dm, N], D and delta_bias [Dm]: float32.  ``y`` (allocated like u when None) and
     ``last_state`` ([batch, Dm, N] float32, optional) are written.  Returns y.
+    balanced=False (default) calls ss_fwd: one CTA per tile, no workspace.  balanced=True calls
+    ss_fwd_ws with a workspace cached per (device, stream): equal (tile, chunk) work per CTA.
     """
     import torch
     batch, L, Dm = u.shape
@@ -122,11 +154,19 @@ def ss_fwd(u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, last_s
     s = FwdStrides(io, u.stride(0), u.stride(1), delta_raw.stride(0), delta_raw.stride(1),
                    z.stride(0) if z is not None else 0, z.stride(1) if z is not None else 0,
                    y.stride(0), y.stride(1), B.stride(0), B.stride(1), C.stride(0), C.stride(1))
-    st = lib().ss_fwd(_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C),
-                      _ptr(D), _ptr(z), _ptr(y), _ptr(last_state), batch, L, Dm, N,
-                      ctypes.byref(s), _stream_handle(stream))
+    args = (_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C),
+            _ptr(D), _ptr(z), _ptr(y), _ptr(last_state), batch, L, Dm, N, ctypes.byref(s))
+    nbytes = ss_fwd_workspace_size(batch, L, Dm, N, io) if balanced and batch * L * Dm > 0 else 0
+    if nbytes:
+        sh = _stream_handle(stream)
+        ws = workspace_for(u.device, sh, nbytes)
+        st = lib().ss_fwd_ws(*args, ws.data_ptr(), ws.numel(), sh)
+        where = "ss_fwd_ws"
+    else:
+        st = lib().ss_fwd(*args, _stream_handle(stream))
+        where = "ss_fwd"
     if st != 0:
-        raise SelscanError(st, "ss_fwd")
+        raise SelscanError(st, where)
     return y
 
 

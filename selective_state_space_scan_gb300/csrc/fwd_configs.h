@@ -22,6 +22,9 @@ constexpr int kLaneStages = SS_LANE_STAGES;
 #define SS_LANE_MINB4 3
 #endif
 constexpr int lane_minb(int lpc) { return lpc == 4 ? SS_LANE_MINB4 : lpc == 2 ? 6 : 8; }
+// Tile width: 32 channels for one CTA per tile; 16 for the balanced schedule, which needs at
+// least as many tiles as resident CTAs (a lane family tile is whole warps of 32/lpc channels).
+constexpr int lane_w(int lpc, bool balanced) { return balanced && lpc > 1 ? 16 : 32; }
 
 // Segment-lane family (time-parallel; few channels, long sequences): 8 channels per CTA,
 // each warp holds 4 time segments of those 8 channels, 8 warps.  K = 7 steps per thread

@@ -6,30 +6,35 @@
 
 namespace selscan {
 
-template <typename TIO, int NS, int LPC, bool TMA>
-cudaError_t launch_lane_cfg(const FwdParams& p, const FwdMaps& m, cudaStream_t stream) {
-    using Cfg = LaneCfg<TIO, NS, LPC, kLaneT, kLaneStages, lane_minb(LPC)>;
+template <typename TIO, int NS, int LPC, bool BAL, bool TMA>
+cudaError_t launch_lane_cfg(const FwdParams& p, const FwdMaps& m, cudaStream_t stream, int* max_grid) {
+    using Cfg = LaneCfg<TIO, NS, LPC, lane_w(LPC, BAL), kLaneT, kLaneStages, lane_minb(LPC)>;
     constexpr int smem = TMA ? Cfg::SMEM_BYTES : Cfg::SMEM_BYTES - (Cfg::STAGES - 1) * Cfg::STAGE_BYTES;
     static_assert(smem <= 227 * 1024, "shared memory budget exceeded");
-    return launch_with_smem<Cfg, TMA>(ss_fwd_lane_kernel<Cfg, TMA>, p, m, stream, smem);
+    return launch_with_smem<Cfg, TMA>(ss_fwd_lane_kernel<Cfg, TMA>, p, m, stream, smem, BAL, max_grid);
 }
 
 template <typename TIO, int NS, int LPC>
-cudaError_t launch_lane_tma(const FwdVariant& v, const FwdParams& p, const FwdMaps& m, cudaStream_t s) {
-    return v.tma ? launch_lane_cfg<TIO, NS, LPC, true>(p, m, s) : launch_lane_cfg<TIO, NS, LPC, false>(p, m, s);
+cudaError_t launch_lane_v(const FwdVariant& v, const FwdParams& p, const FwdMaps& m, cudaStream_t s, int* mg) {
+    if (v.balanced) {
+        if (!v.tma) return cudaErrorInvalidValue;   // the balanced schedule is TMA-fed only
+        return launch_lane_cfg<TIO, NS, LPC, true, true>(p, m, s, mg);
+    }
+    return v.tma ? launch_lane_cfg<TIO, NS, LPC, false, true>(p, m, s, mg)
+                 : launch_lane_cfg<TIO, NS, LPC, false, false>(p, m, s, mg);
 }
 
 template <typename TIO>
-cudaError_t launch_lane_dtype(const FwdVariant& v, const FwdParams& p, const FwdMaps& m, cudaStream_t s) {
+cudaError_t launch_lane_dtype(const FwdVariant& v, const FwdParams& p, const FwdMaps& m, cudaStream_t s, int* mg) {
     if (v.ns == 16) {
-        if (v.lpc == 1) return launch_lane_tma<TIO, 16, 1>(v, p, m, s);
-        if (v.lpc == 2) return launch_lane_tma<TIO, 16, 2>(v, p, m, s);
-        if (v.lpc == 4) return launch_lane_tma<TIO, 16, 4>(v, p, m, s);
+        if (v.lpc == 1) return launch_lane_v<TIO, 16, 1>(v, p, m, s, mg);
+        if (v.lpc == 2) return launch_lane_v<TIO, 16, 2>(v, p, m, s, mg);
+        if (v.lpc == 4) return launch_lane_v<TIO, 16, 4>(v, p, m, s, mg);
     } else if (v.ns == 8) {
-        if (v.lpc == 1) return launch_lane_tma<TIO, 8, 1>(v, p, m, s);
-        if (v.lpc == 2) return launch_lane_tma<TIO, 8, 2>(v, p, m, s);
+        if (v.lpc == 1) return launch_lane_v<TIO, 8, 1>(v, p, m, s, mg);
+        if (v.lpc == 2) return launch_lane_v<TIO, 8, 2>(v, p, m, s, mg);
     } else if (v.ns == 4) {
-        if (v.lpc == 1) return launch_lane_tma<TIO, 4, 1>(v, p, m, s);
+        if (v.lpc == 1) return launch_lane_v<TIO, 4, 1>(v, p, m, s, mg);
     }
     return cudaErrorInvalidValue;
 }

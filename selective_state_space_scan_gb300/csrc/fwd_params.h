@@ -25,6 +25,14 @@ struct FwdParams {
     int chunk_steps;     // steps per chunk the host sized the grid and TMA boxes for
     int tile_channels;   // channels per CTA the host sized them for
     unsigned int* err;   // device error word
+    // Balanced schedule (ws_flag != nullptr): the grid's CTAs split the batch·tiles·nchunks
+    // (tile, chunk) units into equal contiguous ranges; a range that starts inside a tile takes
+    // the state at its start from the previous CTA, which publishes it (ws_state, then ws_flag
+    // set to epoch) as soon as it has folded the head of that tile.
+    float* ws_state;     // [grid][tile_channels][ns] fp32
+    unsigned int* ws_flag;   // [grid]
+    unsigned int epoch;  // this call's nonzero tag
+    int grid;            // CTAs in the launch
 };
 
 // TMA descriptors for the five streamed tensors (unused by the plain-load variant).

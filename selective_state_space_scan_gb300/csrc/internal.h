@@ -19,6 +19,7 @@ struct FwdVariant {
     int ns;
     int lpc;
     bool tma;
+    bool balanced;   // lane family: equal (tile, chunk) ranges per CTA (needs a workspace, TMA)
 };
 
 struct FwdGeom {
@@ -29,13 +30,15 @@ struct FwdGeom {
 
 inline FwdGeom fwd_geometry(const FwdVariant& v) {
     if (v.family == kFamSeg) return FwdGeom{8 * kSegG, 8 * kSegG, 4 * kSegQ * kSegK};
-    return FwdGeom{32, 32 / v.lpc, kLaneT};
+    return FwdGeom{lane_w(v.lpc, v.balanced), 32 / v.lpc, kLaneT};
 }
 
+// Launch (grid = p.grid CTAs; cooperative when v.balanced).  With `max_grid` non-null, launch
+// nothing and return in it the number of CTAs of this kernel that fit on the current device.
 cudaError_t launch_fwd_lane_f32(const FwdVariant& v, const FwdParams& p, const FwdMaps& m,
-                                cudaStream_t stream);
+                                cudaStream_t stream, int* max_grid = nullptr);
 cudaError_t launch_fwd_lane_bf16(const FwdVariant& v, const FwdParams& p, const FwdMaps& m,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, int* max_grid = nullptr);
 cudaError_t launch_fwd_seg(const FwdVariant& v, bool bf16, const FwdParams& p, const FwdMaps& m,
                            cudaStream_t stream);
 cudaError_t launch_step(const StepParams& p, bool bf16, bool vec, cudaStream_t stream);

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -25,6 +26,8 @@ constexpr int kVersion = 100;   // 0.1.0
 // (-1 auto, 0 plain loads, 1 TMA; a forced choice the arguments cannot use is
 // SS_ERR_UNSUPPORTED).
 std::atomic<int> g_force_family{-1}, g_force_lpc{0}, g_force_tma{-1};
+// Test hook: 0 runs ss_fwd_ws with the one-CTA-per-tile schedule (workspace unused).
+std::atomic<int> g_force_balanced{1};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -175,6 +178,10 @@ const char* ss__fwd_kernel_name(int64_t batch, int64_t Dm, int64_t N) {
                                                                : "ss_fwd_lane_kernel(lpc=4)";
 }
 
+// Internal test hook: 0 keeps ss_fwd_ws on the one-CTA-per-tile schedule; 1 (default) lets it
+// use the balanced schedule.
+int ss__force_balanced(int on) { return g_force_balanced.exchange(on ? 1 : 0); }
+
 // Internal test hook (not part of the public header); see g_force_family.
 int ss__force_fwd_variant(int family, int lpc, int tma) {
     if (family < -1 || family > 1 || (lpc != 0 && lpc != 1 && lpc != 2 && lpc != 4) || tma < -1 || tma > 1)
@@ -185,10 +192,41 @@ int ss__force_fwd_variant(int family, int lpc, int tma) {
     return 0;
 }
 
-ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
-                 const void* B, const void* C, const float* D, const void* z, void* y,
-                 float* last_state, int64_t batch, int64_t L, int64_t Dm, int64_t N,
-                 const ss_fwd_strides* strides, void* stream_ptr) {
+}  // extern "C"
+
+namespace selscan {
+namespace {
+
+std::atomic<unsigned int> g_epoch{0};
+
+unsigned int next_epoch() {
+    unsigned int e;
+    do {
+        e = g_epoch.fetch_add(1) + 1;
+    } while (e == 0);
+    return e;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace bytes of the balanced schedule for `grid` CTAs of tile width w and ns states.
+size_t balanced_ws_bytes(int grid, int w, int ns) {
+    return align_up(static_cast<size_t>(grid) * 4, 256) + static_cast<size_t>(grid) * w * ns * 4;
+}
+
+cudaError_t lane_max_grid(const FwdVariant& v, bool bf16, int* out) {
+    FwdParams dummy;
+    std::memset(&dummy, 0, sizeof(dummy));
+    FwdMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    return bf16 ? launch_fwd_lane_bf16(v, dummy, maps, nullptr, out)
+                : launch_fwd_lane_f32(v, dummy, maps, nullptr, out);
+}
+
+ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
+                   const void* B, const void* C, const float* D, const void* z, void* y,
+                   float* last_state, int64_t batch, int64_t L, int64_t Dm, int64_t N,
+                   const ss_fwd_strides* strides, void* workspace, size_t ws_bytes, void* stream_ptr) {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     if (batch < 0 || L < 0 || Dm < 0) return SS_ERR_INVALID_ARG;
     if (N < 1 || N > 16) return SS_ERR_UNSUPPORTED;
@@ -266,27 +304,6 @@ ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias, 
         if (fl > max_lpc) return SS_ERR_UNSUPPORTED;
         v.lpc = fl;
     }
-    const FwdGeom geo = fwd_geometry(v);
-    const int64_t tiles = (Dm + geo.tile_channels - 1) / geo.tile_channels;
-    if (batch * tiles > INT32_MAX) return SS_ERR_UNSUPPORTED;
-
-    FwdParams p;
-    p.u = u; p.delta = delta_raw; p.z = z; p.Bm = B; p.Cm = C;
-    p.bias = delta_bias; p.A_log = A_log; p.Dv = D; p.y = y; p.last_state = last_state;
-    p.u_b = s.u_b; p.u_l = s.u_l; p.d_b = s.delta_b; p.d_l = s.delta_l;
-    p.z_b = s.z_b; p.z_l = s.z_l; p.y_b = s.y_b; p.y_l = s.y_l;
-    p.B_b = s.B_b; p.B_l = s.B_l; p.C_b = s.C_b; p.C_l = s.C_l;
-    p.batch = static_cast<int>(batch);
-    p.L = static_cast<int>(L);
-    p.Dm = static_cast<int>(Dm);
-    p.N = static_cast<int>(N);
-    p.nchunks = static_cast<int>((L + geo.chunk_steps - 1) / geo.chunk_steps);
-    p.tiles_per_batch = static_cast<int>(tiles);
-    p.chunk_steps = geo.chunk_steps;
-    p.tile_channels = geo.tile_channels;
-    p.err = device_error_ptr();
-    if (!p.err) return SS_ERR_CUDA;
-
     // TMA fill: B/C rows exactly ns wide and a multiple of 16 bytes, 16-byte aligned bases
     // and row/batch strides.
     bool tma = (N == v.ns) && (N * es) % 16 == 0;
@@ -303,14 +320,16 @@ ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias, 
     }
     if (ft == 0) tma = false;
 
+    // TMA descriptors (their boxes do not depend on the schedule).  The segment-lane kernel
+    // reads its tiles through the hardware swizzle; the lane kernel reads whole rows of its
+    // own sub-tiles and needs none.  A shape the descriptor encoder rejects is served by the
+    // plain-load fill.
     FwdMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     if (tma) {
-        // The segment-lane kernel reads its tiles through the hardware swizzle; the lane
-        // kernel reads whole rows of its own sub-tiles and needs none.  A shape the
-        // descriptor encoder rejects is served by the plain-load fill.
+        const FwdGeom g0 = fwd_geometry(v);
         const bool sw = v.family == kFamSeg;
-        const int bw = geo.box_channels, bh = geo.chunk_steps;
+        const int bw = g0.box_channels, bh = g0.chunk_steps;
         tma = make_map(&maps.u, u, bf16, Dm, L, batch, s.u_l, s.u_b, bw, bh, sw) &&
               make_map(&maps.delta, delta_raw, bf16, Dm, L, batch, s.delta_l, s.delta_b, bw, bh, sw) &&
               (!z || make_map(&maps.z, z, bf16, Dm, L, batch, s.z_l, s.z_b, bw, bh, sw)) &&
@@ -319,12 +338,88 @@ ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias, 
     }
     if (ft == 1 && !tma) return SS_ERR_UNSUPPORTED;
     v.tma = tma;
+    // With a workspace, TMA-fed lane kernels run the balanced schedule.
+    v.balanced = workspace != nullptr && v.family == kFamLane && tma && g_force_balanced.load() != 0;
+
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.u = u; p.delta = delta_raw; p.z = z; p.Bm = B; p.Cm = C;
+    p.bias = delta_bias; p.A_log = A_log; p.Dv = D; p.y = y; p.last_state = last_state;
+    p.u_b = s.u_b; p.u_l = s.u_l; p.d_b = s.delta_b; p.d_l = s.delta_l;
+    p.z_b = s.z_b; p.z_l = s.z_l; p.y_b = s.y_b; p.y_l = s.y_l;
+    p.B_b = s.B_b; p.B_l = s.B_l; p.C_b = s.C_b; p.C_l = s.C_l;
+    const FwdGeom geo = fwd_geometry(v);
+    const int64_t tiles = (Dm + geo.tile_channels - 1) / geo.tile_channels;
+    if (batch * tiles > INT32_MAX) return SS_ERR_UNSUPPORTED;
+    p.batch = static_cast<int>(batch);
+    p.L = static_cast<int>(L);
+    p.Dm = static_cast<int>(Dm);
+    p.N = static_cast<int>(N);
+    p.nchunks = static_cast<int>((L + geo.chunk_steps - 1) / geo.chunk_steps);
+    p.tiles_per_batch = static_cast<int>(tiles);
+    p.chunk_steps = geo.chunk_steps;
+    p.tile_channels = geo.tile_channels;
+    p.err = device_error_ptr();
+    if (!p.err) return SS_ERR_CUDA;
+    if (v.balanced) {
+        // grid: every CTA resident at once (cooperative launch), never more CTAs than tiles
+        int max_grid = 0;
+        if (lane_max_grid(v, bf16, &max_grid) != cudaSuccess || max_grid <= 0) return SS_ERR_CUDA;
+        const int64_t grid = std::min<int64_t>(batch * tiles, max_grid);
+        if (balanced_ws_bytes(static_cast<int>(grid), geo.tile_channels, v.ns) > ws_bytes)
+            return SS_ERR_INVALID_ARG;
+        if (!aligned(workspace, 256)) return SS_ERR_MISALIGNED;
+        if (!is_device_pointer(workspace, dev)) return SS_ERR_INVALID_ARG;
+        p.grid = static_cast<int>(grid);
+        p.ws_flag = static_cast<unsigned int*>(workspace);
+        p.ws_state = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                              align_up(static_cast<size_t>(grid) * 4, 256));
+        p.epoch = next_epoch();
+    }
     cudaError_t e;
     if (v.family == kFamSeg)
         e = launch_fwd_seg(v, bf16, p, maps, stream);
     else
         e = bf16 ? launch_fwd_lane_bf16(v, p, maps, stream) : launch_fwd_lane_f32(v, p, maps, stream);
     return cuda_status(e);
+}
+
+}  // namespace
+}  // namespace selscan
+
+extern "C" {
+
+ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
+                 const void* B, const void* C, const float* D, const void* z, void* y,
+                 float* last_state, int64_t batch, int64_t L, int64_t Dm, int64_t N,
+                 const ss_fwd_strides* strides, void* stream) {
+    return fwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, y, last_state, batch, L, Dm, N,
+                    strides, nullptr, 0, stream);
+}
+
+ss_status ss_fwd_ws(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
+                    const void* B, const void* C, const float* D, const void* z, void* y,
+                    float* last_state, int64_t batch, int64_t L, int64_t Dm, int64_t N,
+                    const ss_fwd_strides* strides, void* workspace, size_t workspace_bytes, void* stream) {
+    return fwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, y, last_state, batch, L, Dm, N,
+                    strides, workspace, workspace_bytes, stream);
+}
+
+size_t ss_fwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dtype) {
+    if (batch <= 0 || L <= 0 || Dm <= 0 || N < 1 || N > 16) return 0;
+    if (io_dtype != SS_F32 && io_dtype != SS_BF16) return 0;
+    FwdVariant v = choose_fwd_variant(batch, Dm, N);
+    if (g_force_family.load() >= 0) v.family = g_force_family.load();
+    if (g_force_lpc.load() > 0 && g_force_lpc.load() <= v.ns / 4) v.lpc = g_force_lpc.load();
+    if (v.family != kFamLane) return 0;
+    v.balanced = true;
+    v.tma = true;
+    const FwdGeom geo = fwd_geometry(v);
+    const int64_t tiles = batch * ((Dm + geo.tile_channels - 1) / geo.tile_channels);
+    int max_grid = 0;
+    if (lane_max_grid(v, io_dtype == SS_BF16, &max_grid) != cudaSuccess || max_grid <= 0) return 0;
+    const int64_t grid = std::min<int64_t>(tiles, max_grid);
+    return balanced_ws_bytes(static_cast<int>(grid), geo.tile_channels, v.ns);
 }
 
 ss_status ss_step(float* state, const void* x, const void* delta_raw, const float* delta_bias,

@@ -17,17 +17,24 @@
 // the cheapest evaluation there is (no second pass, no aggregates).  To give the GPU enough
 // independent warps when there are fewer than ~40k channels, a channel's NS states are split
 // over LPC lanes (LPC = 1, 2 or 4), each lane folding NS/LPC states with its slice of the state
-// in registers across the whole sequence.  A warp covers CPW = 32/LPC channels; a CTA is LPC
-// warps covering 32 channels, which share one B/C tile.
-//   * per group of LPC steps, lane (c, j) computes Δ, Δ·u for step j of the group and channel
-//     c (one warp instruction covers 32 (step, channel) pairs, as when a lane owns a whole
-//     channel), and the LPC lanes of a channel exchange them by shuffles;
-//   * each lane folds its states over the LPC steps; B, C are read as 16-byte broadcasts;
-//   * the C·h partial sums of the LPC lanes of a channel are combined by a shuffle
-//     reduce-scatter, after which lane (c, j) owns step j's output: D·u skip, z gate, store.
-// u/Δ/z arrive by TMA as one [T × CPW] tile per warp (rows of CPW channels), B/C as one
-// [T × NS] tile per CTA, in a STAGES-deep ring of mbarrier-completed stages.  Packed fp32x2
-// instructions carry pairs of states.  Steps past L are identity pairs (Δ = 0).
+// in registers.  A warp covers CPW = 32/LPC channels; a CTA covers a tile of W channels
+// (W/CPW warps), which share one B/C tile.  Each chunk of T steps runs in three phases per warp:
+//   1. lane (c, j) computes Δ, Δ·u for step j of every group of LPC steps (one warp
+//      instruction covers 32 (step, channel) pairs; independent softplus chains);
+//   2. the fold: step g·LPC + k takes Δ, Δ·u from lane (c, k) by shuffle, B and C are 16-byte
+//      shared-memory broadcasts, packed fp32x2 instructions carry pairs of states; the C·h
+//      partial sums of a channel's LPC lanes are reduce-scattered so that lane (c, j) owns
+//      step j's sum;
+//   3. D·u skip, z gate, store (one row of the warp's channels per step).
+// u/Δ/z arrive by TMA as one [T × CPW] tile per warp, B/C as one [T × NS] tile per CTA, in a
+// STAGES-deep ring of mbarrier-completed stages.  Steps past L are identity pairs (Δ = 0).
+//
+// Schedules.  Without a workspace each CTA owns one tile and walks its whole sequence.  With
+// one (FwdParams::ws_flag), the grid is the number of CTAs that fit on the GPU at once and each
+// CTA takes an equal contiguous range of the (tile, chunk) units, so every SM gets the same
+// work.  A range may start inside a tile: the previous CTA folds that tile's head first and
+// publishes the state where it stops; this CTA folds that piece last, after waiting (with a
+// time limit) for the publication.
 #pragma once
 
 #include "device_common.cuh"
@@ -35,17 +42,17 @@
 
 namespace selscan {
 
-template <typename TIO_, int NS_, int LPC_, int T_, int STAGES_, int MINB_>
+template <typename TIO_, int NS_, int LPC_, int W_, int T_, int STAGES_, int MINB_>
 struct LaneCfg {
     using TIO = TIO_;
     static constexpr int NS = NS_;            // states handled (4, 8 or 16; N <= NS)
     static constexpr int LPC = LPC_;          // lanes per channel
+    static constexpr int W = W_;              // channels per CTA (tile)
     static constexpr int T = T_;              // steps per chunk
     static constexpr int STAGES = STAGES_;
     static constexpr int MINB = MINB_;
     static constexpr int CPW = 32 / LPC;      // channels per warp
-    static constexpr int WARPS = LPC;         // warps per CTA
-    static constexpr int W = CPW * WARPS;     // channels per CTA (32)
+    static constexpr int WARPS = W / CPW;     // warps per CTA
     static constexpr int THREADS = 32 * WARPS;
     static constexpr int SPL = NS / LPC;      // states per lane
     static constexpr int QPL = SPL / 4;       // state quads per lane
@@ -69,8 +76,57 @@ struct LaneCfg {
     static constexpr int AUX_BYTES = AUX_BAR + STAGES * 8;
     static constexpr int SMEM_BYTES = 128 + STAGES * STAGE_BYTES + AUX_BYTES;
     static_assert(NS % (4 * LPC) == 0, "each lane must hold whole state quads");
+    static_assert(W % CPW == 0 && WARPS >= 1, "a tile is whole warps");
     static_assert(T % LPC == 0 && T <= 256, "chunk must be whole groups and one TMA box");
 };
+
+// A CTA's work in processing order: up to three runs of (tile, chunk) units.
+//   run 0: the head (chunks [0, c_end)) of the last tile of the range, if the range ends
+//          inside it; its final state is published for the next CTA;
+//   run 1: whole tiles;
+//   run 2: the tail (chunks [c_start, nchunks)) of the first tile of the range, if the range
+//          starts inside it; its initial state comes from the previous CTA.
+struct LaneWork {
+    int t0, n0;          // run 0: tile, chunk count (chunks 0 .. n0-1)
+    int t1, n1;          // run 1: first whole tile, unit count (whole tiles × nchunks)
+    int t2, c2, n2;      // run 2: tile, first chunk, count
+    __device__ __forceinline__ int total() const { return n0 + n1 + n2; }
+    __device__ __forceinline__ void unit(int k, int nchunks, int& tile, int& chunk) const {
+        if (k < n0) { tile = t0; chunk = k; return; }
+        k -= n0;
+        if (k < n1) { tile = t1 + k / nchunks; chunk = k % nchunks; return; }
+        k -= n1;
+        tile = t2;
+        chunk = c2 + k;
+    }
+};
+
+__device__ __forceinline__ LaneWork lane_work(const FwdParams& p, int tiles_total) {
+    LaneWork w{0, 0, 0, 0, 0, 0, 0};
+    const int nch = p.nchunks;
+    if (p.ws_flag == nullptr) {               // one whole tile per CTA
+        w.t1 = blockIdx.x;
+        w.n1 = nch;
+        return w;
+    }
+    const int64_t U = static_cast<int64_t>(tiles_total) * nch;
+    const int64_t u0 = U * blockIdx.x / p.grid, u1 = U * (blockIdx.x + 1) / p.grid;
+    if (u1 <= u0) return w;
+    const int tf = static_cast<int>(u0 / nch), cf = static_cast<int>(u0 % nch);
+    const int tl = static_cast<int>((u1 - 1) / nch), ce = static_cast<int>((u1 - 1) % nch) + 1;
+    if (tf == tl) {                           // the whole of one tile (the grid is <= tiles)
+        w.t1 = tf;
+        w.n1 = nch;
+        return w;
+    }
+    if (ce < nch) { w.t0 = tl; w.n0 = ce; }
+    if (cf > 0) { w.t2 = tf; w.c2 = cf; w.n2 = nch - cf; }
+    const int first_whole = cf > 0 ? tf + 1 : tf;
+    const int last_whole = ce < nch ? tl - 1 : tl;
+    w.t1 = first_whole;
+    w.n1 = last_whole >= first_whole ? (last_whole - first_whole + 1) * nch : 0;
+    return w;
+}
 
 // Plain-load fill of one stage with the TMA layout (per-warp sub-tiles, zeros outside).
 template <class Cfg>
@@ -122,6 +178,25 @@ __device__ __forceinline__ void lane_issue_tma(uint8_t* st, uint64_t* bar, const
     tma_load_3d(st + Cfg::OFF_C, &m.C, bar, 0, t0, b);
 }
 
+// Wait (thread 0 only) until another CTA has published with this call's epoch; gives up
+// after ~2^31 SM cycles, recording kErrWaitTimeout.
+__device__ __forceinline__ void wait_published(const unsigned int* flag, unsigned int epoch,
+                                               unsigned int* err) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v == epoch) return;
+    const long long t0 = clock64();
+    while (true) {
+        __nanosleep(64);
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v == epoch) return;
+        if (clock64() - t0 > (1ll << 31)) {
+            if (err) atomicOr(err, kErrWaitTimeout);
+            return;
+        }
+    }
+}
+
 template <class Cfg, bool USE_TMA>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
 ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
@@ -148,15 +223,13 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     const int lane = tid & 31, warp = tid >> 5;
     const int j = lane / CPW;            // state slice of this lane / step within a group
     const int c = lane % CPW;            // channel within the warp
-    const int tile = blockIdx.x;
-    const int b = tile / p.tiles_per_batch;
-    const int d0 = (tile % p.tiles_per_batch) * Cfg::W;
-    const int d = d0 + warp * CPW + c;
-    const bool d_ok = d < p.Dm;
     const int nchunks = p.nchunks;
     const bool has_z = p.z != nullptr;
     const int64_t L = p.L;
     const int n0 = j * Cfg::SPL;         // first state of this lane's slice
+    const int64_t ystride = p.y_l * static_cast<int64_t>(sizeof(TIO));   // bytes between steps of y
+    const LaneWork work = lane_work(p, p.batch * p.tiles_per_batch);
+    const int total = work.total();
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -172,40 +245,72 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
         }
     }
     __syncthreads();
+    auto issue = [&](int k, uint8_t* st, uint64_t* bar) {
+        int tl, chk;
+        work.unit(k, nchunks, tl, chk);
+        lane_issue_tma<Cfg>(st, bar, maps, has_z, tl / p.tiles_per_batch,
+                            (tl % p.tiles_per_batch) * Cfg::W, chk);
+    };
     if (USE_TMA && tid == 0) {
-        const int pre = nchunks < STAGES ? nchunks : STAGES;
-        for (int ch = 0; ch < pre; ++ch)
-            lane_issue_tma<Cfg>(smem + ch * Cfg::STAGE_BYTES, &full[ch], maps, has_z, b, d0, ch);
+        const int pre = total < STAGES ? total : STAGES;
+        for (int k = 0; k < pre; ++k) issue(k, smem + k * Cfg::STAGE_BYTES, &full[k]);
     }
 
-    // A'[n] = -exp(A_log[d,n]) · log2(e) for this lane's states, hoisted out of the scan.
-    float2 A2[QPL][2];
+    // per-tile state of this lane (set when the unit loop enters a tile)
+    int cur_tile = -1, b = 0, d = 0;
+    bool d_ok = false;
+    float bias_w = 0.f, D_w = 0.f;
+    float2 A2[QPL][2];                   // A'[n] = -exp(A_log[d,n])·log2(e), hoisted out of the scan
+    float2 h[QPL][2];                    // this lane's slice of the state
 #pragma unroll
     for (int qq = 0; qq < QPL; ++qq) {
-        float v[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int n = n0 + 4 * qq + k;
-            v[k] = (d_ok && n < p.N) ? -expf(p.A_log[static_cast<int64_t>(d) * p.N + n]) * kLog2e : 0.f;
-        }
-        A2[qq][0] = make_float2(v[0], v[1]);
-        A2[qq][1] = make_float2(v[2], v[3]);
+        A2[qq][0] = A2[qq][1] = make_float2(0.f, 0.f);
+        h[qq][0] = h[qq][1] = make_float2(0.f, 0.f);
     }
-    const float bias_w = (p.bias && d_ok) ? p.bias[d] : 0.f;
-    const float D_w = (p.Dv && d_ok) ? p.Dv[d] : 0.f;
-    const int64_t ystride = p.y_l * static_cast<int64_t>(sizeof(TIO));   // bytes between steps of y
 
-    float2 h[QPL][2];                    // this lane's slice of the state, kept across chunks
+    for (int k = 0; k < total; ++k) {
+        int tile, ch;
+        work.unit(k, nchunks, tile, ch);
+        if (tile != cur_tile) {
+            cur_tile = tile;
+            b = tile / p.tiles_per_batch;
+            d = (tile % p.tiles_per_batch) * Cfg::W + warp * CPW + c;
+            d_ok = d < p.Dm;
+            bias_w = (p.bias && d_ok) ? p.bias[d] : 0.f;
+            D_w = (p.Dv && d_ok) ? p.Dv[d] : 0.f;
 #pragma unroll
-    for (int qq = 0; qq < QPL; ++qq) h[qq][0] = h[qq][1] = make_float2(0.f, 0.f);
+            for (int qq = 0; qq < QPL; ++qq) {
+                float v[4];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int n = n0 + 4 * qq + q4;
+                    v[q4] = (d_ok && n < p.N) ? -expf(p.A_log[static_cast<int64_t>(d) * p.N + n]) * kLog2e : 0.f;
+                }
+                A2[qq][0] = make_float2(v[0], v[1]);
+                A2[qq][1] = make_float2(v[2], v[3]);
+                h[qq][0] = h[qq][1] = make_float2(0.f, 0.f);
+            }
+            if (ch > 0) {
+                // the tail of a tile whose head the previous CTA folded: take its state
+                if (tid == 0) wait_published(p.ws_flag + blockIdx.x - 1, p.epoch, p.err);
+                __syncthreads();
+                const float* src = p.ws_state + (static_cast<int64_t>(blockIdx.x - 1) * Cfg::W +
+                                                  warp * CPW + c) * NS + n0;
+#pragma unroll
+                for (int qq = 0; qq < QPL; ++qq) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(src + 4 * qq));
+                    h[qq][0] = make_float2(v.x, v.y);
+                    h[qq][1] = make_float2(v.z, v.w);
+                }
+            }
+        }
 
-    for (int ch = 0; ch < nchunks; ++ch) {
-        const int stage = ch % STAGES;
+        const int stage = k % STAGES;
         uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
         if (USE_TMA) {
-            mbar_wait_bounded(&full[stage], static_cast<uint32_t>((ch / STAGES) & 1), abort_flag, p.err);
+            mbar_wait_bounded(&full[stage], static_cast<uint32_t>((k / STAGES) & 1), abort_flag, p.err);
         } else {
-            lane_fill_generic<Cfg>(st, p, b, d0, ch);
+            lane_fill_generic<Cfg>(st, p, b, (tile % p.tiles_per_batch) * Cfg::W, ch);
             __syncthreads();
         }
         const int sub = warp * Cfg::up128(Cfg::SUB) / Cfg::ES;   // element offset of this warp's sub-tile
@@ -236,7 +341,6 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
         static_assert(GT % G == 0, "chunk must be whole sub-blocks");
 #pragma unroll 1
         for (int g0 = 0; g0 < GT; g0 += G) {
-
             // Phase 1: Δ and Δ·u of the steps this lane prepares (step g·LPC + j of each group;
             // zero past L, i.e. identity pairs).  G independent softplus chains.
             float dd[G], du[G];
@@ -260,15 +364,15 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             for (int g = 0; g < G; ++g) {
                 float dk[LPC], uk[LPC];
 #pragma unroll
-                for (int k = 0; k < LPC; ++k) {
-                    dk[k] = LPC == 1 ? dd[g] : __shfl_sync(0xffffffffu, dd[g], k * CPW + c);
-                    uk[k] = LPC == 1 ? du[g] : __shfl_sync(0xffffffffu, du[g], k * CPW + c);
+                for (int kk = 0; kk < LPC; ++kk) {
+                    dk[kk] = LPC == 1 ? dd[g] : __shfl_sync(0xffffffffu, dd[g], kk * CPW + c);
+                    uk[kk] = LPC == 1 ? du[g] : __shfl_sync(0xffffffffu, du[g], kk * CPW + c);
                 }
                 float yp[LPC];
 #pragma unroll
-                for (int k = 0; k < LPC; ++k) {
-                    const float2 dl2 = make_float2(dk[k], dk[k]), du2 = make_float2(uk[k], uk[k]);
-                    const int row = (g0 + g) * LPC + k;
+                for (int kk = 0; kk < LPC; ++kk) {
+                    const float2 dl2 = make_float2(dk[kk], dk[kk]), du2 = make_float2(uk[kk], uk[kk]);
+                    const int row = (g0 + g) * LPC + kk;
                     float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int qq = 0; qq < QPL; ++qq) {
@@ -281,7 +385,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                         acc = fma2(make_float2(C4.x, C4.y), h[qq][0], acc);
                         acc = fma2(make_float2(C4.z, C4.w), h[qq][1], acc);
                     }
-                    yp[k] = acc.x + acc.y;
+                    yp[kk] = acc.x + acc.y;
                 }
                 if constexpr (LPC == 1) {
                     yv[g] = yp[0];
@@ -297,7 +401,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                     __syncwarp();
                     float sum = 0.f;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) sum += xbuf[(k * CPW + c) * 4 + j];
+                    for (int kk = 0; kk < 4; ++kk) sum += xbuf[(kk * CPW + c) * 4 + j];
                     yv[g] = sum;
                     __syncwarp();
                 }
@@ -335,25 +439,39 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                 __threadfence_block();
                 if (atomicAdd(&done[stage], 1) == Cfg::WARPS - 1) {
                     done[stage] = 0;
-                    if (ch + STAGES < nchunks && !*abort_flag)
-                        lane_issue_tma<Cfg>(st, &full[stage], maps, has_z, b, d0, ch + STAGES);
+                    if (k + STAGES < total && !*abort_flag) issue(k + STAGES, st, &full[stage]);
                 }
             }
         } else {
             __syncthreads();   // stage (and the widened B/C) consumed by every warp
-            if (USE_TMA && tid == 0 && ch + STAGES < nchunks && !*abort_flag)
-                lane_issue_tma<Cfg>(st, &full[stage], maps, has_z, b, d0, ch + STAGES);
+            if (USE_TMA && tid == 0 && k + STAGES < total && !*abort_flag) issue(k + STAGES, st, &full[stage]);
         }
-    }
 
-    if (p.last_state && d_ok) {
-        float* out = p.last_state + (static_cast<int64_t>(b) * p.Dm + d) * p.N;
+        // End of a tile piece: the sequence's final state, or (head of a tile another CTA
+        // finishes) the state to hand over.
+        if (ch == nchunks - 1) {
+            if (p.last_state && d_ok) {
+                float* out = p.last_state + (static_cast<int64_t>(b) * p.Dm + d) * p.N;
 #pragma unroll
-        for (int qq = 0; qq < QPL; ++qq) {
-            const float v[4] = {h[qq][0].x, h[qq][0].y, h[qq][1].x, h[qq][1].y};
+                for (int qq = 0; qq < QPL; ++qq) {
+                    const float v[4] = {h[qq][0].x, h[qq][0].y, h[qq][1].x, h[qq][1].y};
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (n0 + 4 * qq + k < p.N) out[n0 + 4 * qq + k] = v[k];
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        if (n0 + 4 * qq + q4 < p.N) out[n0 + 4 * qq + q4] = v[q4];
+                }
+            }
+        } else if (k == work.n0 - 1) {
+            float* dst = p.ws_state + (static_cast<int64_t>(blockIdx.x) * Cfg::W + warp * CPW + c) * NS + n0;
+#pragma unroll
+            for (int qq = 0; qq < QPL; ++qq)
+                __stcg(reinterpret_cast<float4*>(dst + 4 * qq),
+                       make_float4(h[qq][0].x, h[qq][0].y, h[qq][1].x, h[qq][1].y));
+            __syncthreads();
+            if (tid == 0) {
+                __threadfence();
+                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.ws_flag + blockIdx.x), "r"(p.epoch)
+                             : "memory");
+            }
         }
     }
 }

@@ -44,14 +44,14 @@ VARIANT_IDS = ["lane1-tma", "lane2-tma", "lane4-tma", "seg-tma", "lane1-plain", 
                "lane4-plain", "seg-plain"]
 
 
-def run_gpu(w, with_last=True, variant=(-1, 0, -1)):
+def run_gpu(w, with_last=True, variant=(-1, 0, -1), balanced=True):
     a = w.arrays
     u, dr, z = to_dev(a["u"], w.io), to_dev(a["delta_raw"], w.io), to_dev(a["z"], w.io)
     Bm, Cm = to_dev(a["B"], w.io), to_dev(a["C"], w.io)
     last = torch.full((w.batch, w.Dm, w.N), float("nan"), device="cuda") if with_last else None
     with ForceVariant(*variant):
         y = ss.ss_fwd(u, dr, f32dev(a["delta_bias"]), f32dev(a["A_log"]), Bm, Cm, f32dev(a["D"]), z,
-                      last_state=last)
+                      last_state=last, balanced=balanced)
     torch.cuda.synchronize()
     return to_host(y), (to_host(last) if with_last else None)
 
@@ -240,3 +240,57 @@ def test_rejects_host_pointer_and_aliasing():
                          Cm.data_ptr(), None, None, torch.empty_like(u).data_ptr(), None, 1, 64, 32,
                          16, None, None)
     assert st == 1
+
+
+# ------------------------------------------------------------------ balanced schedule (ss_fwd_ws)
+
+@pytest.mark.parametrize("shape", [
+    ("mamba130m", None), ("mamba2p8b_bf16", None),
+    ("custom", (6, 1000, 4096, 16, "f32")),      # ~2 tiles per CTA, ranges split tiles mid-way
+    ("custom", (3, 515, 2000, 16, "bf16")),      # ragged L and Dm, bf16
+    ("custom", (16, 333, 1536, 8, "f32")),       # N = 8 (2 lanes per channel)
+    ("custom", (16, 200, 512, 16, "f32")),       # fewer tiles than CTAs: one tile per CTA
+], ids=["130m", "2.8b", "split", "ragged-bf16", "n8", "few-tiles"])
+def test_balanced_equals_per_tile(shape):
+    """The balanced schedule hands the state between CTAs exactly: bitwise equal results."""
+    name, dims = shape
+    w = synth.config(name) if dims is None else synth.fwd_inputs(*dims[:4], io=dims[4], seed=21)
+    if dims is not None:
+        assert ss.ss_fwd_workspace_size(*dims[:4], ss.SS_BF16 if dims[4] == "bf16" else ss.SS_F32) > 0
+    y1, l1 = run_gpu(w, balanced=False)
+    y2, l2 = run_gpu(w, balanced=True)
+    np.testing.assert_array_equal(y1, y2)
+    np.testing.assert_array_equal(l1, l2)
+    if dims is not None and dims[0] * dims[1] * dims[2] < 3e6:
+        ry, rlast, mag = run_oracle(w)
+        assert_fwd_close(w.io, y2, ry, mag, l2, rlast, what="balanced")
+
+
+def test_balanced_repeated_calls_reuse_workspace():
+    """Consecutive calls reuse one workspace: each call's epoch keeps stale hand-overs out."""
+    w = synth.fwd_inputs(6, 1000, 4096, 16, seed=22)
+    y1, l1 = run_gpu(w, balanced=True)
+    for _ in range(3):
+        y2, l2 = run_gpu(w, balanced=True)
+        np.testing.assert_array_equal(y1, y2)
+        np.testing.assert_array_equal(l1, l2)
+
+
+def test_balanced_rejects_small_or_misaligned_workspace():
+    w = synth.fwd_inputs(4, 300, 4096, 16, seed=23)
+    a = w.arrays
+    t = {k: (to_dev(v, "f32") if v is not None else None) for k, v in a.items()}
+    y = torch.empty_like(t["u"])
+    need = ss.ss_fwd_workspace_size(4, 300, 4096, 16)
+    assert need > 0
+    ws = torch.zeros(need + 512, dtype=torch.uint8, device="cuda")
+    s = ss.FwdStrides(ss.SS_F32, 300 * 4096, 4096, 300 * 4096, 4096, 300 * 4096, 4096, 300 * 4096, 4096,
+                      300 * 16, 16, 300 * 16, 16)
+    call = lambda ptr, nb: ss.lib().ss_fwd_ws(
+        t["u"].data_ptr(), t["delta_raw"].data_ptr(), t["delta_bias"].data_ptr(), t["A_log"].data_ptr(),
+        t["B"].data_ptr(), t["C"].data_ptr(), t["D"].data_ptr(), t["z"].data_ptr(), y.data_ptr(), None,
+        4, 300, 4096, 16, ctypes.byref(s), ptr, nb, None)
+    assert call(ws.data_ptr(), need - 4) == 1          # too small
+    assert call(ws.data_ptr() + 16, need) == 3         # not 256-byte aligned
+    assert call(ws.data_ptr(), need) == 0
+    torch.cuda.synchronize()
