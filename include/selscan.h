@@ -124,6 +124,33 @@ ss_status ss_fwd_ws(const void* u, const void* delta_raw, const float* delta_bia
  */
 size_t ss_fwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dtype);
 
+/* Size of the fixed device array ss_fwd_static uses as its workspace (1 MiB). */
+#define SS_STATIC_WORKSPACE_BYTES ((size_t)1 << 20)
+
+/*
+ * ss_fwd_ws without a caller-provided workspace, for callers that cannot allocate device
+ * memory: a host whose own allocator already owns all device memory and lends none to
+ * libraries, a runtime that forbids allocation once it has started (fixed-footprint serving),
+ * or a plugin interface that passes the library tensors and a stream but no allocation hook.
+ * The pages this library follows have no counterpart of this call; it is a packaging of
+ * ss_fwd_ws.
+ *   Arguments and results are those of ss_fwd (bitwise equal to it).
+ *   Workspace: a fixed SS_STATIC_WORKSPACE_BYTES array built into the library's device code;
+ *   each device that loads the library holds it until the process exits.  The call allocates
+ *   nothing (no cudaMalloc/cudaFree, no allocating library routine).
+ *   Sizes whose ss_fwd_workspace_size exceeds SS_STATIC_WORKSPACE_BYTES return
+ *   SS_ERR_UNSUPPORTED (use ss_fwd_ws with your own workspace).  Sizes that need no workspace
+ *   run as ss_fwd.
+ *   The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *   with that device current) and caches it; make that first call before any stream capture.
+ *   Every call on a device shares the array: calls that overlap on the GPU (e.g. on two
+ *   streams) race and give wrong results.  Nothing in it needs clearing between calls.
+ */
+ss_status ss_fwd_static(const void* u, const void* delta_raw, const float* delta_bias,
+                        const float* A_log, const void* B, const void* C, const float* D,
+                        const void* z, void* y, float* last_state, int64_t batch, int64_t L,
+                        int64_t Dm, int64_t N, const ss_fwd_strides* strides, void* stream);
+
 /*
  * Element strides of the decode tensors.  x, delta_raw, z, y are [batch, Dm] with channel
  * stride 1; B, C are [batch, N] with state stride 1; the state is [batch, Dm, N] with

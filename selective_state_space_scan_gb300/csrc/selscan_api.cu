@@ -17,6 +17,13 @@ namespace selscan {
 
 __device__ unsigned int g_device_error;
 
+// Workspace of ss_fwd_static: a fixed array in the library's device image, so that callers
+// that cannot allocate device memory can still run the balanced schedule.  Every device that
+// loads the library holds these SS_STATIC_WORKSPACE_BYTES until the process exits.  It needs
+// no clearing: each call tags its hand-overs with a fresh call number, so flags left by
+// earlier calls never match.  All calls on a device share it.
+static __device__ __align__(256) unsigned char g_static_ws[SS_STATIC_WORKSPACE_BYTES];
+
 namespace {
 
 constexpr int kVersion = 100;   // 0.1.0
@@ -53,6 +60,25 @@ unsigned int* device_error_ptr() {
         void* a = nullptr;
         if (cudaGetSymbolAddress(&a, g_device_error) != cudaSuccess) return nullptr;
         p = static_cast<unsigned int*>(a);
+        cache[dev].store(p);
+    }
+    return p;
+}
+
+// Device address of g_static_ws on the current device.  In host code the symbol's name is only
+// a host-side handle, so the address is looked up once per device (with that device current)
+// and cached; a failed lookup returns nullptr.
+void* static_workspace_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    static std::atomic<void*> cache[64] = {};
+    if (dev < 0 || dev >= 64) return nullptr;
+    void* p = cache[dev].load();
+    if (!p) {
+        if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
         cache[dev].store(p);
     }
     return p;
@@ -420,6 +446,22 @@ size_t ss_fwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N, in
     if (lane_max_grid(v, io_dtype == SS_BF16, &max_grid) != cudaSuccess || max_grid <= 0) return 0;
     const int64_t grid = std::min<int64_t>(tiles, max_grid);
     return balanced_ws_bytes(static_cast<int>(grid), geo.tile_channels, v.ns);
+}
+
+ss_status ss_fwd_static(const void* u, const void* delta_raw, const float* delta_bias,
+                        const float* A_log, const void* B, const void* C, const float* D,
+                        const void* z, void* y, float* last_state, int64_t batch, int64_t L,
+                        int64_t Dm, int64_t N, const ss_fwd_strides* strides, void* stream) {
+    const int32_t io = strides ? strides->io_dtype : SS_F32;
+    const size_t need = (batch > 0 && L > 0 && Dm > 0) ? ss_fwd_workspace_size(batch, L, Dm, N, io) : 0;
+    if (need > SS_STATIC_WORKSPACE_BYTES) return SS_ERR_UNSUPPORTED;   // beyond the fixed array
+    void* ws = nullptr;
+    if (need > 0) {
+        ws = static_workspace_ptr();
+        if (!ws) return SS_ERR_CUDA;
+    }
+    return fwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, y, last_state, batch, L, Dm, N,
+                    strides, ws, ws ? SS_STATIC_WORKSPACE_BYTES : 0, stream);
 }
 
 ss_status ss_step(float* state, const void* x, const void* delta_raw, const float* delta_bias,
