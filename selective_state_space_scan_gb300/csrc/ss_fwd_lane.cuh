@@ -23,8 +23,8 @@
 //      instruction covers 32 (step, channel) pairs; independent softplus chains);
 //   2. the fold: step g·LPC + k takes Δ, Δ·u from lane (c, k) by shuffle, B and C are 16-byte
 //      shared-memory broadcasts, packed fp32x2 instructions carry pairs of states; the C·h
-//      partial sums of a channel's LPC lanes are reduce-scattered so that lane (c, j) owns
-//      step j's sum;
+//      partial sums of a channel's LPC lanes are reduce-scattered by shuffles so that lane
+//      (c, j) owns step j's sum;
 //   3. D·u skip, z gate, store (one row of the warp's channels per step).
 // u/Δ/z arrive by TMA as one [T × CPW] tile per warp, B/C as one [T × NS] tile per CTA, in a
 // STAGES-deep ring of mbarrier-completed stages.  Steps past L are identity pairs (Δ = 0).
@@ -69,8 +69,7 @@ struct LaneCfg {
     static constexpr int OFF_C = OFF_B + up128(TILE_N);
     static constexpr int STAGE_BYTES = OFF_C + up128(TILE_N);
     static constexpr int AUX_BC = 0;                                       // fp32 B,C [2][T][NS]
-    static constexpr int AUX_XBUF = AUX_BC + (CONVERT_BC ? 2 * T * NS * 4 : 0);  // [WARPS][32][4] floats
-    static constexpr int AUX_FLAG = AUX_XBUF + WARPS * 32 * 16;
+    static constexpr int AUX_FLAG = AUX_BC + (CONVERT_BC ? 2 * T * NS * 4 : 0);
     static constexpr int AUX_DONE = AUX_FLAG + 16;                        // per-stage warp counters
     static constexpr int AUX_BAR = AUX_DONE + ((STAGES * 4 + 15) / 16) * 16;
     static constexpr int AUX_BYTES = AUX_BAR + STAGES * 8;
@@ -210,7 +209,6 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     float* bcf = reinterpret_cast<float*>(aux + Cfg::AUX_BC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(aux + Cfg::AUX_FLAG);
     int* done = reinterpret_cast<int*>(aux + Cfg::AUX_DONE);
-    float* xbuf = reinterpret_cast<float*>(aux + Cfg::AUX_XBUF) + (threadIdx.x >> 5) * 32 * 4;
     uint64_t* full = reinterpret_cast<uint64_t*>(aux + Cfg::AUX_BAR);
 
     // A grid or TMA box sized for another tile shape would never complete the stage
@@ -395,15 +393,17 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                     const float keep = hi ? yp[1] : yp[0];
                     yv[g] = keep + __shfl_xor_sync(0xffffffffu, send, CPW);
                 } else {
-                    // transpose through this warp's shared scratch: lane (c, j) stores its four
-                    // partials, then reads the four slices' partials of step j
-                    *reinterpret_cast<float4*>(xbuf + lane * 4) = make_float4(yp[0], yp[1], yp[2], yp[3]);
-                    __syncwarp();
-                    float sum = 0.f;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) sum += xbuf[(kk * CPW + c) * 4 + j];
-                    yv[g] = sum;
-                    __syncwarp();
+                    // butterfly reduce-scatter over the four slices (lanes c + CPW·s): first
+                    // across slice bit 1 (each side keeps two steps), then across bit 0.  Only
+                    // shuffles, no shared-memory round trip or warp barrier, so the next
+                    // group's loads are free to start early.
+                    const bool b1 = (j & 2) != 0, b0 = (j & 1) != 0;
+                    const float s0 = b1 ? yp[0] : yp[2], s1 = b1 ? yp[1] : yp[3];
+                    const float k0 = b1 ? yp[2] : yp[0], k1 = b1 ? yp[3] : yp[1];
+                    const float t0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 2 * CPW);   // step 2·b1
+                    const float t1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 2 * CPW);   // step 2·b1 + 1
+                    const float sd = b0 ? t0 : t1, kp = b0 ? t1 : t0;
+                    yv[g] = kp + __shfl_xor_sync(0xffffffffu, sd, CPW);                 // step j
                 }
             }
             // Phase 3: D skip, z gate, store (G independent chains).
