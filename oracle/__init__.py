@@ -30,9 +30,9 @@ def _configure(lib):
     lib.oracle_softplus.restype = ctypes.c_double
     lib.oracle_silu.argtypes = [ctypes.c_double]
     lib.oracle_silu.restype = ctypes.c_double
-    lib.oracle_ss_fwd_rows.argtypes = [f32p] * 8 + [i64p, i64, f64p, f64p, f64p, i64, i64, i64, i64]
+    lib.oracle_ss_fwd_rows.argtypes = [f32p] * 8 + [f64p, i64p, i64, f64p, f64p, f64p, i64, i64, i64, i64]
     lib.oracle_ss_fwd_rows.restype = ctypes.c_int
-    lib.oracle_ss_fwd_chunked.argtypes = [f32p] * 8 + [f64p, f64p, i64, i64, i64, i64, i64]
+    lib.oracle_ss_fwd_chunked.argtypes = [f32p] * 8 + [f64p, f64p, f64p, i64, i64, i64, i64, i64]
     lib.oracle_ss_fwd_chunked.restype = ctypes.c_int
     lib.oracle_ss_step.argtypes = [f64p] + [f32p] * 8 + [f64p, f64p, i64, i64, i64]
     lib.oracle_ss_step.restype = ctypes.c_int
@@ -76,11 +76,21 @@ def silu(x: float) -> float:
     return float(_load().oracle_silu(float(x)))
 
 
-def ss_fwd(u, delta_raw, delta_bias, A_log, B, C, D, z, rows=None):
+def _h0(h0, batch, Dm, N):
+    if h0 is None:
+        return None
+    h = np.ascontiguousarray(np.asarray(h0, dtype=np.float64))
+    if h.shape != (batch, Dm, N):
+        raise ValueError(f"h0: expected shape {(batch, Dm, N)}, got {h.shape}")
+    return h
+
+
+def ss_fwd(u, delta_raw, delta_bias, A_log, B, C, D, z, rows=None, h0=None):
     """Sequential fp64 forward scan.
 
     Shapes: u, delta_raw, z [batch, L, Dm]; B, C [batch, L, N]; A_log [Dm, N];
-    D, delta_bias [Dm] (or None).  Inputs are taken as float32 values.
+    D, delta_bias [Dm] (or None).  Inputs are taken as float32 values.  h0 [batch, Dm, N]
+    (or None for zeros) is the state before step 0, taken in float64.
 
     rows=None  -> returns (y [batch, L, Dm], last_state [batch, Dm, N], mag [batch, L, Dm])
     rows=array -> flat indices b*Dm+d; returns (y [nrows, L], last [nrows, N], mag [nrows, L])
@@ -97,6 +107,7 @@ def ss_fwd(u, delta_raw, delta_bias, A_log, B, C, D, z, rows=None):
     C = _f32(C, (batch, L, N), "C")
     D = _f32(D, (Dm,), "D")
     delta_bias = _f32(delta_bias, (Dm,), "delta_bias")
+    h0 = _h0(h0, batch, Dm, N)
     if rows is None:
         nrows = batch * Dm
         rows_arr = None
@@ -109,7 +120,8 @@ def ss_fwd(u, delta_raw, delta_bias, A_log, B, C, D, z, rows=None):
     st = _load().oracle_ss_fwd_rows(
         _ptr(u, ctypes.c_float), _ptr(delta_raw, ctypes.c_float), _ptr(delta_bias, ctypes.c_float),
         _ptr(A_log, ctypes.c_float), _ptr(B, ctypes.c_float), _ptr(C, ctypes.c_float),
-        _ptr(D, ctypes.c_float), _ptr(z, ctypes.c_float), _ptr(rows_arr, ctypes.c_int64), nrows,
+        _ptr(D, ctypes.c_float), _ptr(z, ctypes.c_float), _ptr(h0, ctypes.c_double),
+        _ptr(rows_arr, ctypes.c_int64), nrows,
         _ptr(y, ctypes.c_double), _ptr(mag, ctypes.c_double), _ptr(last, ctypes.c_double),
         batch, L, Dm, N)
     if st != 0:
@@ -121,9 +133,9 @@ def ss_fwd(u, delta_raw, delta_bias, A_log, B, C, D, z, rows=None):
     return np.ascontiguousarray(y), last.reshape(batch, Dm, N), np.ascontiguousarray(mag)
 
 
-def ss_fwd_chunked(u, delta_raw, delta_bias, A_log, B, C, D, z, chunk):
-    """fp64 chunked evaluation with the pair operator and a carry; same returns as
-    ss_fwd(rows=None) minus mag."""
+def ss_fwd_chunked(u, delta_raw, delta_bias, A_log, B, C, D, z, chunk, h0=None):
+    """fp64 chunked evaluation with the pair operator and a carry (starting from h0, or
+    zeros); same returns as ss_fwd(rows=None) minus mag."""
     u = _f32(u, name="u")
     batch, L, Dm = u.shape
     A_log = _f32(A_log, name="A_log")
@@ -132,7 +144,8 @@ def ss_fwd_chunked(u, delta_raw, delta_bias, A_log, B, C, D, z, chunk):
             _f32(B, (batch, L, N)), _f32(C, (batch, L, N)), _f32(D, (Dm,)), _f32(z, (batch, L, Dm))]
     y = np.empty((batch * Dm, L), np.float64)
     last = np.empty((batch * Dm, N), np.float64)
-    st = _load().oracle_ss_fwd_chunked(*[_ptr(a, ctypes.c_float) for a in args],
+    h0 = _h0(h0, batch, Dm, N)
+    st = _load().oracle_ss_fwd_chunked(*[_ptr(a, ctypes.c_float) for a in args], _ptr(h0, ctypes.c_double),
                                        _ptr(y, ctypes.c_double), _ptr(last, ctypes.c_double),
                                        batch, L, Dm, N, int(chunk))
     if st != 0:

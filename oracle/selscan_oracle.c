@@ -25,7 +25,11 @@
  *   - B̄ is the Euler form b = Δ·B·u ([K] writes the pair's second element as Δ B u).
  *   - delta_bias (per channel, NULL = 0) is added to delta_raw before softplus.
  *   - softplus(x) = max(x,0) + log1p(exp(-|x|)), the exact overflow-free form.
- *   - h_{-1} = 0; the D skip is added before the gate; silu(z) = z / (1 + exp(-z)).
+ *   - h_{-1} = 0 unless an initial state h0 is given; the D skip is added before the
+ *     gate; silu(z) = z / (1 + exp(-z)).
+ *   - h0 (the initial-state input) is the state a previous call left behind: the carry
+ *     of [M] "チャンク間 running prefix" handed across calls instead of across chunks, the
+ *     prefill state that [M] "O(L) インクリメンタルデコード" continues from.
  *   - B and C are shared by all channels of a batch row: [B,L,N]; last_state is [B,D,N].
  *
  * Layouts (all contiguous, row-major): u, delta_raw, z : [batch, L, Dm];
@@ -50,6 +54,7 @@ double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
 /*
  * Sequential forward recurrence for a list of (batch, channel) rows.
  *   rows[r] = b * Dm + d  (NULL: every row, in that order)
+ *   h0 [batch, Dm, N] (NULL: zeros) is the state before step 0: h_{-1}[n] = h0[b, d, n].
  * Outputs (any may be NULL):
  *   y_rows    [nrows, L]  y[b, t, d]
  *   mag_rows  [nrows, L]  |silu(z)| * (sum_n |C_n h_t[n]| + |D u_t|): the size of the
@@ -64,7 +69,7 @@ double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
  */
 int oracle_ss_fwd_rows(const float* u, const float* delta_raw, const float* delta_bias,
                        const float* A_log, const float* B, const float* C, const float* D,
-                       const float* z, const int64_t* rows, int64_t nrows,
+                       const float* z, const double* h0, const int64_t* rows, int64_t nrows,
                        double* y_rows, double* mag_rows, double* last_rows,
                        int64_t batch, int64_t L, int64_t Dm, int64_t N)
 {
@@ -92,6 +97,8 @@ int oracle_ss_fwd_rows(const float* u, const float* delta_raw, const float* delt
             continue;
         }
         for (int64_t n = 0; n < N; ++n) A[n] = -exp((double)A_log[d * N + n]);
+        if (h0)
+            for (int64_t n = 0; n < N; ++n) h[n] = h0[row * N + n];
         const double bias = delta_bias ? (double)delta_bias[d] : 0.0;
         const double Dd = D ? (double)D[d] : 0.0;
 
@@ -128,12 +135,13 @@ int oracle_ss_fwd_rows(const float* u, const float* delta_raw, const float* delt
  * の本質"; [K] "なぜ「scan」か"), and each chunk's running pair is applied to the carry
  * from the previous chunk, the carry being the state at the chunk's end ([M]
  * "チャンク間 running prefix").  It exists to check the oracle against itself:
- * any chunk length must give the sequential result up to rounding.
+ * any chunk length must give the sequential result up to rounding.  h0 (NULL: zeros) is
+ * the carry before the first chunk.
  * Output layout as oracle_ss_fwd_rows (all rows, natural order).
  */
 int oracle_ss_fwd_chunked(const float* u, const float* delta_raw, const float* delta_bias,
                           const float* A_log, const float* B, const float* C, const float* D,
-                          const float* z, double* y_rows, double* last_rows,
+                          const float* z, const double* h0, double* y_rows, double* last_rows,
                           int64_t batch, int64_t L, int64_t Dm, int64_t N, int64_t chunk)
 {
     if (batch < 0 || L < 0 || Dm < 0 || N < 1 || chunk < 1) return ORACLE_EINVAL;
@@ -153,7 +161,7 @@ int oracle_ss_fwd_chunked(const float* u, const float* delta_raw, const float* d
         }
         for (int64_t n = 0; n < N; ++n) {
             const double An = -exp((double)A_log[d * N + n]);
-            double carry = 0.0;                       /* state before the chunk */
+            double carry = h0 ? h0[row * N + n] : 0.0;  /* state before the chunk */
             for (int64_t t0 = 0; t0 < L; t0 += chunk) {
                 const int64_t t1 = (t0 + chunk < L) ? t0 + chunk : L;
                 double run_a = 1.0, run_b = 0.0;      /* identity pair */

@@ -38,6 +38,13 @@ MUTANTS = [
      "const double ut = (double)u[(b * L + t) * Dm + (Dm - 1 - d)];"),
     ("step_without_decay", "*h = exp(delta * An) * (*h) + delta * xt * (double)B[b * N + n];",
      "*h = (*h) + delta * xt * (double)B[b * N + n];"),
+    ("h0_ignored", "for (int64_t n = 0; n < N; ++n) h[n] = h0[row * N + n];",
+     "for (int64_t n = 0; n < N; ++n) h[n] = 0.0 * h0[row * N + n];"),
+    ("h0_wrong_row", "for (int64_t n = 0; n < N; ++n) h[n] = h0[row * N + n];",
+     "for (int64_t n = 0; n < N; ++n) h[n] = h0[((row + 1) % (batch * Dm)) * N + n];"),
+    ("h0_scaled", "for (int64_t n = 0; n < N; ++n) h[n] = h0[row * N + n];",
+     "for (int64_t n = 0; n < N; ++n) h[n] = 0.5 * h0[row * N + n];"),
+    ("h0_not_in_chunked_carry", "double carry = h0 ? h0[row * N + n] : 0.0;", "double carry = 0.0;"),
     ("step_bias_dropped",
      "oracle_softplus((double)delta_raw[row] + (delta_bias ? (double)delta_bias[d] : 0.0))",
      "oracle_softplus((double)delta_raw[row])"),
@@ -71,6 +78,11 @@ def harness():
         lambda m: pins.test_chunked_scan_equals_sequential(m, 3),
         pins.test_softplus_textbook,
         pins.test_silu_textbook,
+        pins.test_h0_zero_input_is_pure_decay,
+        pins.test_h0_with_A_to_zero_adds_to_the_running_sum,
+        lambda m: pins.test_h0_split_composition(m, 17),
+        pins.test_h0_chunked_equals_sequential,
+        pins.test_h0_decode_iterated_equals_forward,
     ]
     return mod, battery
 

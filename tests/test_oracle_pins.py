@@ -211,6 +211,83 @@ def test_chunked_scan_equals_sequential(oracle_mod, chunk):
     np.testing.assert_allclose(lastc, last, rtol=1e-12, atol=1e-14)
 
 
+# ---------------------------------------------------------------- initial state h0
+
+def _h0_for(seed, batch, Dm, N):
+    return np.random.default_rng(seed).normal(0.0, 0.7, (batch, Dm, N))
+
+
+def test_h0_zero_input_is_pure_decay(oracle_mod):
+    """With u = 0 every b_t is 0 and only the initial state decays:
+    h_t[n] = exp(A_n S_t) h0[n], S_t = Σ_{r<=t} Δ_r, y_t = silu(z_t) Σ_n C_tn h_t[n]."""
+    a = _rand_inputs(21, batch=2, L=41, Dm=3, N=4)
+    a["u"] = np.zeros_like(a["u"])
+    h0 = _h0_for(1, 2, 3, 4)
+    y, last, _ = _call(oracle_mod, a, h0=h0)
+    dlt = _softplus_np(a["delta_raw"].astype(np.float64) + a["delta_bias"][None, None, :])
+    S = np.cumsum(dlt, axis=1)                                     # [b, t, d]
+    A = -np.exp(a["A_log"].astype(np.float64))                     # [d, n]
+    h = np.exp(S[..., None] * A[None, None]) * h0[:, None]         # [b, t, d, n]
+    z = a["z"].astype(np.float64)
+    y_ref = np.einsum("btn,btdn->btd", a["C"].astype(np.float64), h) * z * expit(z)
+    np.testing.assert_allclose(y, y_ref, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(last, h[:, -1], rtol=1e-12, atol=1e-14)
+
+
+def test_h0_with_A_to_zero_adds_to_the_running_sum(oracle_mod):
+    """A -> 0 keeps the state undecayed: h_t = h0 + Σ_{s<=t} Δ_s B_s u_s."""
+    a = _rand_inputs(22, batch=2, L=29, Dm=4, N=3)
+    a["A_log"] = np.full_like(a["A_log"], -40.0)
+    h0 = _h0_for(2, 2, 4, 3)
+    y, last, _ = _call(oracle_mod, a, h0=h0)
+    u = a["u"].astype(np.float64)
+    dlt = _softplus_np(a["delta_raw"].astype(np.float64) + a["delta_bias"][None, None, :])
+    h = h0[:, None] + np.cumsum((dlt * u)[..., None] * a["B"].astype(np.float64)[:, :, None, :], axis=1)
+    pre = np.einsum("btn,btdn->btd", a["C"].astype(np.float64), h) + a["D"][None, None, :] * u
+    z = a["z"].astype(np.float64)
+    np.testing.assert_allclose(y, pre * z * expit(z), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(last, h[:, -1], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("k", [1, 17, 39])
+def test_h0_split_composition(oracle_mod, k):
+    """Running steps [0, k) and then [k, L) from the state the first part left behind gives
+    the one-call result: the carry handed across calls."""
+    a = _rand_inputs(23, batch=2, L=40, Dm=5, N=6)
+    h0 = _h0_for(3, 2, 5, 6)
+    y, last, _ = _call(oracle_mod, a, h0=h0)
+    seq = ("u", "delta_raw", "z", "B", "C")
+    p1 = {key: (v[:, :k] if key in seq else v) for key, v in a.items()}
+    p2 = {key: (v[:, k:] if key in seq else v) for key, v in a.items()}
+    y1, l1, _ = _call(oracle_mod, p1, h0=h0)
+    y2, l2, _ = _call(oracle_mod, p2, h0=l1)
+    np.testing.assert_allclose(np.concatenate([y1, y2], axis=1), y, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(l2, last, rtol=1e-13, atol=1e-15)
+
+
+def test_h0_chunked_equals_sequential(oracle_mod):
+    a = _rand_inputs(24, batch=2, L=70, Dm=3, N=5)
+    h0 = _h0_for(4, 2, 3, 5)
+    y, last, _ = _call(oracle_mod, a, h0=h0)
+    yc, lastc = oracle_mod.ss_fwd_chunked(a["u"], a["delta_raw"], a["delta_bias"], a["A_log"],
+                                          a["B"], a["C"], a["D"], a["z"], 8, h0=h0)
+    np.testing.assert_allclose(yc, y, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lastc, last, rtol=1e-12, atol=1e-14)
+
+
+def test_h0_decode_iterated_equals_forward(oracle_mod):
+    """The decode update stepped from h0 reproduces the forward pass started at h0."""
+    a = _rand_inputs(25, batch=2, L=12, Dm=4, N=3)
+    h0 = _h0_for(5, 2, 4, 3)
+    y, last, _ = _call(oracle_mod, a, h0=h0)
+    state = h0.copy()
+    for t in range(12):
+        yt, state, _ = oracle_mod.ss_step(state, a["u"][:, t], a["delta_raw"][:, t], a["delta_bias"],
+                                          a["A_log"], a["B"][:, t], a["C"][:, t], a["D"], a["z"][:, t])
+        np.testing.assert_allclose(yt, y[:, t], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(state, last, rtol=1e-13, atol=1e-15)
+
+
 # ---------------------------------------------------------------- decode vs scan
 
 def test_decode_iterated_equals_forward(oracle_mod):
