@@ -84,7 +84,7 @@ typedef struct {
  *   last_state    [batch, Dm, N] fp32 contiguous or NULL: h_{L-1}, the state that a
  *                                           following ss_step continues from
  *   batch, L, Dm  >= 0; batch == 0 or Dm == 0 is a no-op; L == 0 writes zeros to
- *                 last_state (if given) and nothing else
+ *                 last_state (if given) and nothing else (ss_fwd_h0: copies h0 there)
  *   N             1..16
  * Returns SS_OK once the work is enqueued.
  */
@@ -96,21 +96,30 @@ ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias,
 /*
  * Forward pass with a caller-provided workspace; same arguments and result as ss_fwd.
  *
- * ss_fwd runs one CTA per tile of channels over the whole sequence.  ss_fwd_ws instead
- * splits the (tile, chunk) work into equal contiguous ranges, one per CTA the device can hold
- * at once (a cooperative launch), so every SM gets the same amount of work; a range that starts
- * inside a tile takes the state at its start from the CTA before it.  That hand-over needs
- * the workspace: one flag and one tile state per CTA.  This is the same carry-across-chunks
- * scan ("mamba-metal: Apple Silicon で Mamba を動かす", section "チャンク間 running prefix")
- * with the carry passed between CTAs instead of kept in one CTA; results are bitwise equal to
- * ss_fwd's.
+ * ss_fwd runs one CTA per tile of channels over the whole sequence.  With a workspace, one of
+ * two schedules of the same carry-across-chunks scan ("mamba-metal: Apple Silicon で Mamba を
+ * 動かす", section "チャンク間 running prefix") runs instead:
+ *   - balanced (enough channel tiles to fill the GPU): the (tile, chunk) work is split into
+ *     equal contiguous ranges, one per CTA the device can hold at once (a cooperative launch),
+ *     so every SM gets the same amount of work; a range that starts inside a tile takes the
+ *     state at its start from the CTA before it (the workspace holds one flag and one tile
+ *     state per CTA).  Results are bitwise equal to ss_fwd's.
+ *   - time-split (too few channel tiles, e.g. one long sequence): each sequence is cut into
+ *     segments that run side by side.  A first pass folds every segment but the last from a
+ *     zero state; a carry pass combines those end states left to right (the decay over a
+ *     segment is exp(A · Σ Δ)); a last pass folds every segment from its carried start.  The
+ *     workspace holds one state per (segment, row, state) and one Σ Δ per (segment, row).
+ *     Results equal ss_fwd's up to rounding (the carry is composed in another order).
  *   workspace        device memory, 256-byte aligned, at least workspace_bytes =
  *                    ss_fwd_workspace_size(...) bytes, zero-filled before its first use (the
  *                    library never needs it cleared again).  Calls that share a workspace must
- *                    not run concurrently on the device.
+ *                    not run concurrently on the device.  A workspace smaller than the size
+ *                    query asks for gives the time-split schedule fewer segments (none, i.e.
+ *                    ss_fwd's schedule, below two); for the balanced schedule it returns
+ *                    SS_ERR_INVALID_ARG.
  *   workspace NULL   behaves exactly like ss_fwd.
- * Too small a workspace returns SS_ERR_INVALID_ARG; a misaligned one SS_ERR_MISALIGNED.  When
- * the arguments cannot use TMA-fed tiles (see ss_fwd_strides) the workspace is not used.
+ * A misaligned workspace returns SS_ERR_MISALIGNED.  When the arguments cannot use TMA-fed
+ * tiles (see ss_fwd_strides) the workspace is not used.
  */
 ss_status ss_fwd_ws(const void* u, const void* delta_raw, const float* delta_bias,
                     const float* A_log, const void* B, const void* C, const float* D,
@@ -119,10 +128,29 @@ ss_status ss_fwd_ws(const void* u, const void* delta_raw, const float* delta_bia
                     size_t workspace_bytes, void* stream);
 
 /*
- * Workspace bytes ss_fwd_ws needs for these sizes on the current device (0: it needs none,
+ * Workspace bytes ss_fwd_ws (and ss_fwd_h0) need for these sizes on the current device (0: none,
  * or the sizes are invalid).  Depends on the device's SM count and the kernel's occupancy.
  */
 size_t ss_fwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dtype);
+
+/*
+ * Forward pass from a given initial state: ss_fwd_ws with h_{-1} = h0 instead of 0.
+ * The recurrence continues from a state an earlier call left behind: the carry of
+ * "mamba-metal: Apple Silicon で Mamba を動かす" (section "チャンク間 running prefix") handed
+ * across calls, so a long sequence can be processed in pieces (chunked prefill: pass the
+ * previous piece's last_state as h0) with the same result as one call, up to rounding.
+ *   h0               [batch, Dm, N] fp32 contiguous, or NULL (= zeros, i.e. ss_fwd_ws).
+ *                    It may be last_state itself (the state is then updated in place); it must
+ *                    not overlap last_state otherwise, nor y.  4-byte aligned.
+ *   L == 0           last_state (if given) receives a copy of h0 (zeros without one).
+ *   workspace        as for ss_fwd_ws, NULL allowed.
+ * Other arguments, errors and results as ss_fwd_ws.
+ */
+ss_status ss_fwd_h0(const void* u, const void* delta_raw, const float* delta_bias,
+                    const float* A_log, const void* B, const void* C, const float* D,
+                    const void* z, void* y, float* last_state, const float* h0, int64_t batch,
+                    int64_t L, int64_t Dm, int64_t N, const ss_fwd_strides* strides,
+                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* Size of the fixed device array ss_fwd_static uses as its workspace (1 MiB). */
 #define SS_STATIC_WORKSPACE_BYTES ((size_t)1 << 20)
@@ -134,7 +162,8 @@ size_t ss_fwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N, in
  * or a plugin interface that passes the library tensors and a stream but no allocation hook.
  * The pages this library follows have no counterpart of this call; it is a packaging of
  * ss_fwd_ws.
- *   Arguments and results are those of ss_fwd (bitwise equal to it).
+ *   Arguments and results are those of ss_fwd: bitwise equal to it on the balanced schedule,
+ *   equal up to rounding on the time-split one (see ss_fwd_ws).
  *   Workspace: a fixed SS_STATIC_WORKSPACE_BYTES array built into the library's device code;
  *   each device that loads the library holds it until the process exits.  The call allocates
  *   nothing (no cudaMalloc/cudaFree, no allocating library routine).

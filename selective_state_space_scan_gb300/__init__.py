@@ -50,6 +50,8 @@ def lib() -> ctypes.CDLL:
         L.ss_fwd.restype = ctypes.c_int
         L.ss_fwd_ws.argtypes = [vp] * 10 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp, ctypes.c_size_t, vp]
         L.ss_fwd_ws.restype = ctypes.c_int
+        L.ss_fwd_h0.argtypes = [vp] * 11 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp, ctypes.c_size_t, vp]
+        L.ss_fwd_h0.restype = ctypes.c_int
         L.ss_fwd_workspace_size.argtypes = [i64] * 4 + [ctypes.c_int32]
         L.ss_fwd_workspace_size.restype = ctypes.c_size_t
         L.ss_step.argtypes = [vp] * 10 + [i64] * 3 + [ctypes.POINTER(StepStrides), vp]
@@ -125,7 +127,7 @@ def workspace_for(device, stream_handle, nbytes: int):
 
 
 def ss_fwd_workspace_size(batch, L, Dm, N, io_dtype=SS_F32) -> int:
-    """Bytes of workspace ss_fwd_ws needs on the current device (0: none)."""
+    """Bytes of workspace ss_fwd_ws / ss_fwd_h0 need on the current device (0: none)."""
     import torch
     key = (torch.cuda.current_device() if torch.cuda.is_available() else -1, batch, L, Dm, N, io_dtype)
     if key not in _WS_SIZES:
@@ -134,14 +136,17 @@ def ss_fwd_workspace_size(batch, L, Dm, N, io_dtype=SS_F32) -> int:
 
 
 def ss_fwd(u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, last_state=None,
-           stream=None, balanced=False):
+           stream=None, workspace=False, h0=None):
     """Selective-scan forward pass through the C ABI.
 
     u, delta_raw, z: [batch, L, Dm]; B, C: [batch, L, N] (same dtype, float32 or bfloat16);
     A_log [Dm, N], D and delta_bias [Dm]: float32.  ``y`` (allocated like u when None) and
     ``last_state`` ([batch, Dm, N] float32, optional) are written.  Returns y.
-    balanced=False (default) calls ss_fwd: one CTA per tile, no workspace.  balanced=True calls
-    ss_fwd_ws with a workspace cached per (device, stream): equal (tile, chunk) work per CTA.
+    h0 ([batch, Dm, N] float32, optional) is the state before step 0 (ss_fwd_h0); it may be
+    last_state itself.
+    workspace=False (default) runs one CTA per channel tile over the whole sequence (ss_fwd).
+    workspace=True passes a workspace cached per (device, stream), which enables the balanced
+    schedule (equal work per CTA) or, for few channel tiles, the time-split one (ss_fwd_ws).
     """
     import torch
     batch, L, Dm = u.shape
@@ -151,19 +156,29 @@ def ss_fwd(u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, last_s
         y = torch.empty((batch, L, Dm), dtype=u.dtype, device=u.device)
     for name, t in (("u", u), ("delta_raw", delta_raw), ("z", z), ("y", y), ("B", B), ("C", C)):
         _check_inner(t, name)
+    if h0 is not None and (h0.dtype != torch.float32 or not h0.is_contiguous() or
+                           tuple(h0.shape) != (batch, Dm, N)):
+        raise ValueError("h0 must be a contiguous float32 [batch, Dm, N] tensor")
     s = FwdStrides(io, u.stride(0), u.stride(1), delta_raw.stride(0), delta_raw.stride(1),
                    z.stride(0) if z is not None else 0, z.stride(1) if z is not None else 0,
                    y.stride(0), y.stride(1), B.stride(0), B.stride(1), C.stride(0), C.stride(1))
-    args = (_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C),
-            _ptr(D), _ptr(z), _ptr(y), _ptr(last_state), batch, L, Dm, N, ctypes.byref(s))
-    nbytes = ss_fwd_workspace_size(batch, L, Dm, N, io) if balanced and batch * L * Dm > 0 else 0
+    head = (_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C),
+            _ptr(D), _ptr(z), _ptr(y), _ptr(last_state))
+    dims = (batch, L, Dm, N, ctypes.byref(s))
+    nbytes = ss_fwd_workspace_size(batch, L, Dm, N, io) if workspace and batch * L * Dm > 0 else 0
+    sh = _stream_handle(stream)
+    ws_ptr, ws_len = None, 0
     if nbytes:
-        sh = _stream_handle(stream)
         ws = workspace_for(u.device, sh, nbytes)
-        st = lib().ss_fwd_ws(*args, ws.data_ptr(), ws.numel(), sh)
+        ws_ptr, ws_len = ws.data_ptr(), ws.numel()
+    if h0 is not None:
+        st = lib().ss_fwd_h0(*head, _ptr(h0), *dims, ws_ptr, ws_len, sh)
+        where = "ss_fwd_h0"
+    elif nbytes:
+        st = lib().ss_fwd_ws(*head, *dims, ws_ptr, ws_len, sh)
         where = "ss_fwd_ws"
     else:
-        st = lib().ss_fwd(*args, _stream_handle(stream))
+        st = lib().ss_fwd(*head, *dims, sh)
         where = "ss_fwd"
     if st != 0:
         raise SelscanError(st, where)

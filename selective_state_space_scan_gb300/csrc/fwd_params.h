@@ -32,7 +32,19 @@ struct FwdParams {
     float* ws_state;     // [grid][tile_channels][ns] fp32
     unsigned int* ws_flag;   // [grid]
     unsigned int epoch;  // this call's nonzero tag
-    int grid;            // CTAs in the launch
+    int grid;            // CTAs in the launch (0: batch·tiles_per_batch)
+    // Initial state h_{-1} [batch, Dm, N] contiguous (nullptr: zeros).
+    const float* h0;
+    // Time-split schedule (seg_launch > 0): the sequence is cut into segments of seg_chunks
+    // chunks; CTA x takes segment x % seg_launch of tile x / seg_launch.  Pass A (state-only
+    // kernel) folds segments 0 .. nseg-2 from zero and writes each end state to slot s + 1
+    // of seg_slots and its Σ Δ to seg_dsum; the carry kernel turns the slots into the state at
+    // every segment's start (slot 0 = h0); pass C folds every segment from its slot.
+    int seg_launch;      // segments per tile in this launch
+    int seg_chunks;      // chunks per segment
+    int nseg;            // segments per tile in the schedule
+    float* seg_slots;    // [nseg][batch·Dm·N]
+    float* seg_dsum;     // [nseg - 1][batch·Dm]
 };
 
 // TMA descriptors for the five streamed tensors (unused by the plain-load variant).

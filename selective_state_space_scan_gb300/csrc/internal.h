@@ -20,6 +20,7 @@ struct FwdVariant {
     int lpc;
     bool tma;
     bool balanced;   // lane family: equal (tile, chunk) ranges per CTA (needs a workspace, TMA)
+    bool state_only; // lane family, TMA: pass A of the time-split schedule (end states only)
 };
 
 struct FwdGeom {
@@ -42,5 +43,8 @@ cudaError_t launch_fwd_lane_bf16(const FwdVariant& v, const FwdParams& p, const 
 cudaError_t launch_fwd_seg(const FwdVariant& v, bool bf16, const FwdParams& p, const FwdMaps& m,
                            cudaStream_t stream);
 cudaError_t launch_step(const StepParams& p, bool bf16, bool vec, cudaStream_t stream);
+// Time-split carry pass: slot 0 of p.seg_slots = h0 (or zeros); slot s = exp(A·ΣΔ of segment
+// s-1)·slot s-1 + the end state pass A left in slot s, for s = 1 .. p.nseg - 1.
+cudaError_t launch_fwd_carry(const FwdParams& p, cudaStream_t stream);
 
 }  // namespace selscan

@@ -35,6 +35,9 @@ constexpr int kVersion = 100;   // 0.1.0
 std::atomic<int> g_force_family{-1}, g_force_lpc{0}, g_force_tma{-1};
 // Test hook: 0 runs ss_fwd_ws with the one-CTA-per-tile schedule (workspace unused).
 std::atomic<int> g_force_balanced{1};
+// Test hook on the time-split schedule: -1 automatic (with a workspace, for shapes with too
+// few channel tiles to fill the GPU), 0 never, n >= 2 always with up to n segments.
+std::atomic<int> g_force_nseg{-1};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -153,6 +156,8 @@ FwdVariant choose_fwd_variant(int64_t batch, int64_t Dm, int64_t N) {
     while (v.lpc < max_lpc && tiles32 * v.lpc < want_warps) v.lpc *= 2;
     v.family = tiles32 * v.lpc >= want_warps / 2 ? kFamLane : kFamSeg;
     v.tma = true;
+    v.balanced = false;
+    v.state_only = false;
     return v;
 }
 
@@ -208,6 +213,9 @@ const char* ss__fwd_kernel_name(int64_t batch, int64_t Dm, int64_t N) {
 // use the balanced schedule.
 int ss__force_balanced(int on) { return g_force_balanced.exchange(on ? 1 : 0); }
 
+// Internal test hook (see g_force_nseg); returns the previous setting.
+int ss__force_nseg(int n) { return g_force_nseg.exchange(n < 0 ? -1 : n == 1 ? 0 : n); }
+
 // Internal test hook (not part of the public header); see g_force_family.
 int ss__force_fwd_variant(int family, int lpc, int tma) {
     if (family < -1 || family > 1 || (lpc != 0 && lpc != 1 && lpc != 2 && lpc != 4) || tma < -1 || tma > 1)
@@ -240,6 +248,41 @@ size_t balanced_ws_bytes(int grid, int w, int ns) {
     return align_up(static_cast<size_t>(grid) * 4, 256) + static_cast<size_t>(grid) * w * ns * 4;
 }
 
+// Time-split schedule sizes.  Workspace: the per-segment state slots [nseg][rows·N] fp32,
+// then the per-segment Σ Δ [nseg - 1][rows] fp32.
+struct SplitPlan {
+    int nseg = 0;        // 0: the schedule does not apply
+    int seg_chunks = 0;
+    size_t bytes = 0;
+    size_t off_dsum = 0;
+};
+
+size_t split_slot_bytes(int nseg, int64_t rows, int64_t N) {
+    return align_up(static_cast<size_t>(nseg) * rows * N * 4, 256);
+}
+
+// As many segments as fill the GPU once (tiles × segments <= the CTAs resident together),
+// or the forced count; at most one per chunk and 64; fewer if ws_bytes cannot hold them.
+SplitPlan split_plan(int64_t tiles_total, int nchunks, int64_t rows, int64_t N, int max_grid,
+                     size_t ws_bytes, int forced) {
+    SplitPlan pl;
+    int64_t want = forced >= 2 ? forced : (tiles_total > 0 ? max_grid / tiles_total : 0);
+    want = std::min<int64_t>(std::min<int64_t>(want, nchunks), 64);
+    auto bytes = [&](int64_t ns) {
+        return split_slot_bytes(static_cast<int>(ns), rows, N) + static_cast<size_t>(ns - 1) * rows * 4;
+    };
+    while (want >= 2 && bytes(want) > ws_bytes) --want;
+    if (want < 2) return pl;
+    const int seg_chunks = static_cast<int>((nchunks + want - 1) / want);
+    const int nseg = (nchunks + seg_chunks - 1) / seg_chunks;
+    if (nseg < 2) return pl;
+    pl.nseg = nseg;
+    pl.seg_chunks = seg_chunks;
+    pl.bytes = bytes(nseg);
+    pl.off_dsum = split_slot_bytes(nseg, rows, N);
+    return pl;
+}
+
 cudaError_t lane_max_grid(const FwdVariant& v, bool bf16, int* out) {
     FwdParams dummy;
     std::memset(&dummy, 0, sizeof(dummy));
@@ -251,7 +294,7 @@ cudaError_t lane_max_grid(const FwdVariant& v, bool bf16, int* out) {
 
 ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
                    const void* B, const void* C, const float* D, const void* z, void* y,
-                   float* last_state, int64_t batch, int64_t L, int64_t Dm, int64_t N,
+                   float* last_state, const float* h0, int64_t batch, int64_t L, int64_t Dm, int64_t N,
                    const ss_fwd_strides* strides, void* workspace, size_t ws_bytes, void* stream_ptr) {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     if (batch < 0 || L < 0 || Dm < 0) return SS_ERR_INVALID_ARG;
@@ -272,12 +315,23 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     const int64_t es = bf16 ? 2 : 4;
     if (batch == 0 || Dm == 0) return SS_OK;
     if (!A_log) return SS_ERR_INVALID_ARG;
+    if (h0 && !aligned(h0, 4)) return SS_ERR_MISALIGNED;
+    const Span sh = span3(h0, batch, Dm, N, Dm * N, N, 4);
+    const Span sl = span3(last_state, batch, Dm, N, Dm * N, N, 4);
+    // h0 may be last_state itself (continue in place) but not overlap it otherwise
+    if (h0 && static_cast<const void*>(h0) != static_cast<const void*>(last_state) && overlap(sh, sl))
+        return SS_ERR_INVALID_ARG;
     if (L == 0) {
+        // no steps: the final state is the initial one
         if (!last_state) return SS_OK;
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
         if (!is_device_pointer(last_state, dev)) return SS_ERR_INVALID_ARG;
-        return cuda_status(cudaMemsetAsync(last_state, 0, sizeof(float) * batch * Dm * N, stream));
+        const size_t bytes = sizeof(float) * batch * Dm * N;
+        if (!h0) return cuda_status(cudaMemsetAsync(last_state, 0, bytes, stream));
+        if (!is_device_pointer(h0, dev)) return SS_ERR_INVALID_ARG;
+        if (static_cast<const void*>(h0) == static_cast<const void*>(last_state)) return SS_OK;
+        return cuda_status(cudaMemcpyAsync(last_state, h0, bytes, cudaMemcpyDeviceToDevice, stream));
     }
     if (!u || !delta_raw || !B || !C || !y) return SS_ERR_INVALID_ARG;
     // strides: non-negative; the batch stride may only be anything when batch == 1
@@ -294,18 +348,18 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     const void* io_ptrs[] = {u, delta_raw, B, C, y, z};
     for (const void* p : io_ptrs)
         if (p && !aligned(p, es)) return SS_ERR_MISALIGNED;
-    const void* f_ptrs[] = {A_log, D, delta_bias, last_state};
+    const void* f_ptrs[] = {A_log, D, delta_bias, last_state, h0};
     for (const void* p : f_ptrs)
         if (p && !aligned(p, 4)) return SS_ERR_MISALIGNED;
     // device memory of the current device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
-    const void* all_ptrs[] = {u, delta_raw, B, C, y, z, A_log, D, delta_bias, last_state};
+    const void* all_ptrs[] = {u, delta_raw, B, C, y, z, A_log, D, delta_bias, last_state, h0};
     for (const void* p : all_ptrs)
         if (p && !is_device_pointer(p, dev)) return SS_ERR_INVALID_ARG;
     // outputs must not overlap inputs
     const Span sy = span3(y, batch, L, Dm, s.y_b, s.y_l, es);
-    const Span sl = span3(last_state, batch, Dm, N, Dm * N, N, 4);
+    if (overlap(sy, sh)) return SS_ERR_INVALID_ARG;
     const Span ins[] = {span3(u, batch, L, Dm, s.u_b, s.u_l, es),
                         span3(delta_raw, batch, L, Dm, s.delta_b, s.delta_l, es),
                         span3(z, batch, L, Dm, s.z_b, s.z_l, es),
@@ -346,6 +400,28 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     }
     if (ft == 0) tma = false;
 
+    // Time-split schedule (needs a workspace and TMA): when the channel tiles alone cannot
+    // fill the GPU, cut the sequence into segments that run side by side (pass A: end states
+    // from zero; carry pass; pass C: the fold from each segment's carried start).
+    const int fs = g_force_nseg.load();
+    SplitPlan plan;
+    if (workspace && tma && fs != 0 && (fs >= 2 || (v.family == kFamSeg && ff < 0))) {
+        FwdVariant vs = v;
+        vs.family = kFamLane;
+        if (fl <= 0) vs.lpc = vs.ns / 4;
+        vs.tma = true;
+        vs.balanced = false;
+        vs.state_only = false;
+        int max_grid = 0;
+        if (lane_max_grid(vs, bf16, &max_grid) != cudaSuccess || max_grid <= 0) return SS_ERR_CUDA;
+        const int64_t tiles_ts = batch * ((Dm + lane_w(vs.lpc, false) - 1) / lane_w(vs.lpc, false));
+        const int64_t nch = (L + kLaneT - 1) / kLaneT;
+        if (nch <= INT32_MAX && tiles_ts * 64 <= INT32_MAX) {
+            plan = split_plan(tiles_ts, static_cast<int>(nch), batch * Dm, N, max_grid, ws_bytes, fs);
+            if (plan.nseg >= 2) v = vs;
+        }
+    }
+
     // TMA descriptors (their boxes do not depend on the schedule).  The segment-lane kernel
     // reads its tiles through the hardware swizzle; the lane kernel reads whole rows of its
     // own sub-tiles and needs none.  A shape the descriptor encoder rejects is served by the
@@ -364,13 +440,15 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     }
     if (ft == 1 && !tma) return SS_ERR_UNSUPPORTED;
     v.tma = tma;
-    // With a workspace, TMA-fed lane kernels run the balanced schedule.
-    v.balanced = workspace != nullptr && v.family == kFamLane && tma && g_force_balanced.load() != 0;
+    if (!tma) plan = SplitPlan();   // descriptors refused: the plain-load fill, no time split
+    const bool split = plan.nseg >= 2;
+    // Otherwise, with a workspace, TMA-fed lane kernels run the balanced schedule.
+    v.balanced = !split && workspace != nullptr && v.family == kFamLane && tma && g_force_balanced.load() != 0;
 
     FwdParams p;
     std::memset(&p, 0, sizeof(p));
     p.u = u; p.delta = delta_raw; p.z = z; p.Bm = B; p.Cm = C;
-    p.bias = delta_bias; p.A_log = A_log; p.Dv = D; p.y = y; p.last_state = last_state;
+    p.bias = delta_bias; p.A_log = A_log; p.Dv = D; p.y = y; p.last_state = last_state; p.h0 = h0;
     p.u_b = s.u_b; p.u_l = s.u_l; p.d_b = s.delta_b; p.d_l = s.delta_l;
     p.z_b = s.z_b; p.z_l = s.z_l; p.y_b = s.y_b; p.y_l = s.y_l;
     p.B_b = s.B_b; p.B_l = s.B_l; p.C_b = s.C_b; p.C_l = s.C_l;
@@ -402,6 +480,33 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
                                               align_up(static_cast<size_t>(grid) * 4, 256));
         p.epoch = next_epoch();
     }
+    if (split) {
+        if (plan.bytes > ws_bytes) return SS_ERR_INVALID_ARG;
+        if (!aligned(workspace, 256)) return SS_ERR_MISALIGNED;
+        if (!is_device_pointer(workspace, dev)) return SS_ERR_INVALID_ARG;
+        const int64_t tiles_total = batch * tiles;
+        p.nseg = plan.nseg;
+        p.seg_chunks = plan.seg_chunks;
+        p.seg_slots = static_cast<float*>(workspace);
+        p.seg_dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.off_dsum);
+        auto lane = [&](const FwdVariant& vv, const FwdParams& pp) {
+            return bf16 ? launch_fwd_lane_bf16(vv, pp, maps, stream) : launch_fwd_lane_f32(vv, pp, maps, stream);
+        };
+        FwdParams pa = p;                 // pass A: segments 0 .. nseg-2 from zero
+        pa.seg_launch = plan.nseg - 1;
+        pa.grid = static_cast<int>(tiles_total * pa.seg_launch);
+        pa.h0 = nullptr;
+        pa.last_state = nullptr;
+        FwdVariant va = v;
+        va.state_only = true;
+        cudaError_t e = lane(va, pa);
+        if (e != cudaSuccess) return cuda_status(e);
+        if ((e = launch_fwd_carry(p, stream)) != cudaSuccess) return cuda_status(e);
+        FwdParams pc = p;                 // pass C: every segment from its carried start
+        pc.seg_launch = plan.nseg;
+        pc.grid = static_cast<int>(tiles_total * plan.nseg);
+        return cuda_status(lane(v, pc));
+    }
     cudaError_t e;
     if (v.family == kFamSeg)
         e = launch_fwd_seg(v, bf16, p, maps, stream);
@@ -419,7 +524,7 @@ ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias, 
                  const void* B, const void* C, const float* D, const void* z, void* y,
                  float* last_state, int64_t batch, int64_t L, int64_t Dm, int64_t N,
                  const ss_fwd_strides* strides, void* stream) {
-    return fwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, y, last_state, batch, L, Dm, N,
+    return fwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, y, last_state, nullptr, batch, L, Dm, N,
                     strides, nullptr, 0, stream);
 }
 
@@ -427,7 +532,15 @@ ss_status ss_fwd_ws(const void* u, const void* delta_raw, const float* delta_bia
                     const void* B, const void* C, const float* D, const void* z, void* y,
                     float* last_state, int64_t batch, int64_t L, int64_t Dm, int64_t N,
                     const ss_fwd_strides* strides, void* workspace, size_t workspace_bytes, void* stream) {
-    return fwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, y, last_state, batch, L, Dm, N,
+    return fwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, y, last_state, nullptr, batch, L, Dm, N,
+                    strides, workspace, workspace_bytes, stream);
+}
+
+ss_status ss_fwd_h0(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
+                    const void* B, const void* C, const float* D, const void* z, void* y,
+                    float* last_state, const float* h0, int64_t batch, int64_t L, int64_t Dm, int64_t N,
+                    const ss_fwd_strides* strides, void* workspace, size_t workspace_bytes, void* stream) {
+    return fwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, y, last_state, h0, batch, L, Dm, N,
                     strides, workspace, workspace_bytes, stream);
 }
 
@@ -435,8 +548,24 @@ size_t ss_fwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N, in
     if (batch <= 0 || L <= 0 || Dm <= 0 || N < 1 || N > 16) return 0;
     if (io_dtype != SS_F32 && io_dtype != SS_BF16) return 0;
     FwdVariant v = choose_fwd_variant(batch, Dm, N);
-    if (g_force_family.load() >= 0) v.family = g_force_family.load();
-    if (g_force_lpc.load() > 0 && g_force_lpc.load() <= v.ns / 4) v.lpc = g_force_lpc.load();
+    const int ff = g_force_family.load(), fs = g_force_nseg.load();
+    if (ff >= 0) v.family = ff;
+    const int fl = g_force_lpc.load() > 0 && g_force_lpc.load() <= v.ns / 4 ? g_force_lpc.load() : 0;
+    if (fl) v.lpc = fl;
+    if (fs != 0 && (fs >= 2 || (v.family == kFamSeg && ff < 0))) {
+        // the time-split schedule
+        v.family = kFamLane;
+        if (!fl) v.lpc = v.ns / 4;
+        v.tma = true;
+        int max_grid = 0;
+        if (lane_max_grid(v, io_dtype == SS_BF16, &max_grid) != cudaSuccess || max_grid <= 0) return 0;
+        const int64_t tiles_ts = batch * ((Dm + lane_w(v.lpc, false) - 1) / lane_w(v.lpc, false));
+        const int64_t nch = (L + kLaneT - 1) / kLaneT;
+        if (nch > INT32_MAX) return 0;
+        const SplitPlan pl = split_plan(tiles_ts, static_cast<int>(nch), batch * Dm, N, max_grid,
+                                        static_cast<size_t>(-1), fs);
+        return pl.nseg >= 2 ? pl.bytes : 0;
+    }
     if (v.family != kFamLane) return 0;
     v.balanced = true;
     v.tma = true;
@@ -460,7 +589,7 @@ ss_status ss_fwd_static(const void* u, const void* delta_raw, const float* delta
         ws = static_workspace_ptr();
         if (!ws) return SS_ERR_CUDA;
     }
-    return fwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, y, last_state, batch, L, Dm, N,
+    return fwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, y, last_state, nullptr, batch, L, Dm, N,
                     strides, ws, ws ? SS_STATIC_WORKSPACE_BYTES : 0, stream);
 }
 

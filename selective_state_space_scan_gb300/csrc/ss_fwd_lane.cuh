@@ -1,7 +1,7 @@
 // Selective-scan forward kernel, state-split lane layout, for sm_103a.
 //
 // Computes exactly what ss_fwd specifies (include/selscan.h): per batch row b, channel d,
-// state n and step t, with h_{-1} = 0,
+// state n and step t, with h_{-1} = h0 (zeros when none is given),
 //   Δ_t = softplus(delta_raw + bias),  h_t = exp(Δ_t A_n) h_{t-1} + Δ_t B_t,n u_t,
 //   y_t = (Σ_n C_t,n h_t[n] + D u_t) · silu(z_t),   last_state = h_{L-1},
 // i.e. the recurrence of "mamba-metal: Apple Silicon で Mamba を動かす" (section "Selective
@@ -34,7 +34,9 @@
 // CTA takes an equal contiguous range of the (tile, chunk) units, so every SM gets the same
 // work.  A range may start inside a tile: the previous CTA folds that tile's head first and
 // publishes the state where it stops; this CTA folds that piece last, after waiting (with a
-// time limit) for the publication.
+// time limit) for the publication.  In the time-split schedule (FwdParams::seg_launch) CTA x
+// folds one segment of one tile: pass A (STATE_ONLY) from a zero state, keeping only the end
+// state and Σ Δ; pass C from the segment's start state that the carry kernel composed.
 #pragma once
 
 #include "device_common.cuh"
@@ -103,6 +105,15 @@ struct LaneWork {
 __device__ __forceinline__ LaneWork lane_work(const FwdParams& p, int tiles_total) {
     LaneWork w{0, 0, 0, 0, 0, 0, 0};
     const int nch = p.nchunks;
+    if (p.seg_launch > 0) {                   // time-split: one segment of one tile
+        const int s = static_cast<int>(blockIdx.x) % p.seg_launch;
+        const int c0 = s * p.seg_chunks;
+        const int cnt = nch - c0 < p.seg_chunks ? nch - c0 : p.seg_chunks;
+        w.t2 = static_cast<int>(blockIdx.x) / p.seg_launch;
+        w.c2 = c0;
+        w.n2 = cnt > 0 ? cnt : 0;
+        return w;
+    }
     if (p.ws_flag == nullptr) {               // one whole tile per CTA
         w.t1 = blockIdx.x;
         w.n1 = nch;
@@ -196,7 +207,9 @@ __device__ __forceinline__ void wait_published(const unsigned int* flag, unsigne
     }
 }
 
-template <class Cfg, bool USE_TMA>
+// STATE_ONLY: pass A of the time-split schedule.  The same fold from a zero state, without
+// C, y or the z gate: it writes the segment's end state and its Σ Δ.
+template <class Cfg, bool USE_TMA, bool STATE_ONLY = false>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
 ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     using TIO = typename Cfg::TIO;
@@ -260,6 +273,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     float bias_w = 0.f, D_w = 0.f;
     float2 A2[QPL][2];                   // A'[n] = -exp(A_log[d,n])·log2(e), hoisted out of the scan
     float2 h[QPL][2];                    // this lane's slice of the state
+    float dsum = 0.f;                    // STATE_ONLY: Σ Δ over this lane's steps
 #pragma unroll
     for (int qq = 0; qq < QPL; ++qq) {
         A2[qq][0] = A2[qq][1] = make_float2(0.f, 0.f);
@@ -288,17 +302,40 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                 A2[qq][1] = make_float2(v[2], v[3]);
                 h[qq][0] = h[qq][1] = make_float2(0.f, 0.f);
             }
-            if (ch > 0) {
-                // the tail of a tile whose head the previous CTA folded: take its state
-                if (tid == 0) wait_published(p.ws_flag + blockIdx.x - 1, p.epoch, p.err);
-                __syncthreads();
-                const float* src = p.ws_state + (static_cast<int64_t>(blockIdx.x - 1) * Cfg::W +
-                                                  warp * CPW + c) * NS + n0;
+            dsum = 0.f;
+            if constexpr (!STATE_ONLY) {
+                const float* src = nullptr;    // the state before this unit's first chunk
+                if (p.seg_launch > 0) {
+                    // time-split pass C: the carry the carry kernel left for this segment
+                    src = p.seg_slots +
+                          ((static_cast<int64_t>(ch / p.seg_chunks) * p.batch + b) * p.Dm + d) * p.N;
+                } else if (ch == 0) {
+                    if (p.h0) src = p.h0 + (static_cast<int64_t>(b) * p.Dm + d) * p.N;
+                } else {
+                    // balanced: the tail of a tile whose head the previous CTA folded
+                    if (tid == 0) wait_published(p.ws_flag + blockIdx.x - 1, p.epoch, p.err);
+                    __syncthreads();
+                    const float* ws = p.ws_state + (static_cast<int64_t>(blockIdx.x - 1) * Cfg::W +
+                                                     warp * CPW + c) * NS + n0;
 #pragma unroll
-                for (int qq = 0; qq < QPL; ++qq) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(src + 4 * qq));
-                    h[qq][0] = make_float2(v.x, v.y);
-                    h[qq][1] = make_float2(v.z, v.w);
+                    for (int qq = 0; qq < QPL; ++qq) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4*>(ws + 4 * qq));
+                        h[qq][0] = make_float2(v.x, v.y);
+                        h[qq][1] = make_float2(v.z, v.w);
+                    }
+                }
+                if (src && d_ok) {
+#pragma unroll
+                    for (int qq = 0; qq < QPL; ++qq) {
+                        float v[4];
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const int n = n0 + 4 * qq + q4;
+                            v[q4] = n < p.N ? __ldcg(src + n) : 0.f;
+                        }
+                        h[qq][0] = make_float2(v[0], v[1]);
+                        h[qq][1] = make_float2(v[2], v[3]);
+                    }
                 }
             }
         }
@@ -354,6 +391,10 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                 for (int g = 0; g < G; ++g)
                     if ((g0 + g) * LPC + j >= left) dd[g] = du[g] = 0.f;
             }
+            if constexpr (STATE_ONLY) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) dsum += dd[g];
+            }
             // Phase 2: the sequential fold.  Step g·LPC + k takes its Δ, Δ·u from lane (c, k);
             // the C·h partial sums of the channel's LPC lanes are reduce-scattered so that lane
             // (c, j) ends with the sum of step g·LPC + j.
@@ -375,17 +416,21 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
 #pragma unroll
                     for (int qq = 0; qq < QPL; ++qq) {
                         const float4 B4 = *reinterpret_cast<const float4*>(tB + row * NS + n0 + 4 * qq);
-                        const float4 C4 = *reinterpret_cast<const float4*>(tC + row * NS + n0 + 4 * qq);
                         const float2 a01 = ex2x2(mul2(dl2, A2[qq][0]));
                         const float2 a23 = ex2x2(mul2(dl2, A2[qq][1]));
                         h[qq][0] = fma2(a01, h[qq][0], mul2(du2, make_float2(B4.x, B4.y)));
                         h[qq][1] = fma2(a23, h[qq][1], mul2(du2, make_float2(B4.z, B4.w)));
-                        acc = fma2(make_float2(C4.x, C4.y), h[qq][0], acc);
-                        acc = fma2(make_float2(C4.z, C4.w), h[qq][1], acc);
+                        if constexpr (!STATE_ONLY) {
+                            const float4 C4 = *reinterpret_cast<const float4*>(tC + row * NS + n0 + 4 * qq);
+                            acc = fma2(make_float2(C4.x, C4.y), h[qq][0], acc);
+                            acc = fma2(make_float2(C4.z, C4.w), h[qq][1], acc);
+                        }
                     }
                     yp[kk] = acc.x + acc.y;
                 }
-                if constexpr (LPC == 1) {
+                if constexpr (STATE_ONLY) {
+                    (void)yp;
+                } else if constexpr (LPC == 1) {
                     yv[g] = yp[0];
                 } else if constexpr (LPC == 2) {
                     const bool hi = j & 1;
@@ -407,7 +452,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                 }
             }
             // Phase 3: D skip, z gate, store (G independent chains).
-            if (d_ok) {
+            if (!STATE_ONLY && d_ok) {
                 char* yrow = reinterpret_cast<char*>(static_cast<TIO*>(p.y) + b * p.y_b + (tbase + g0 * LPC + j) * p.y_l + d);
                 const int64_t rem = left - g0 * LPC - j;          // steps of this lane's column before L
                 const int nst = whole ? G : (rem <= 0 ? 0 : rem >= int64_t(G) * LPC ? G : static_cast<int>((rem + LPC - 1) / LPC));
@@ -448,8 +493,26 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
         }
 
         // End of a tile piece: the sequence's final state, or (head of a tile another CTA
-        // finishes) the state to hand over.
-        if (ch == nchunks - 1) {
+        // finishes) the state to hand over; for pass A, the segment's end state and Σ Δ.
+        if constexpr (STATE_ONLY) {
+            if (k == total - 1) {
+                const int sg = ch / p.seg_chunks;
+                if (d_ok) {
+                    float* dst = p.seg_slots + ((static_cast<int64_t>(sg + 1) * p.batch + b) * p.Dm + d) * p.N;
+#pragma unroll
+                    for (int qq = 0; qq < QPL; ++qq) {
+                        const float v[4] = {h[qq][0].x, h[qq][0].y, h[qq][1].x, h[qq][1].y};
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            if (n0 + 4 * qq + q4 < p.N) dst[n0 + 4 * qq + q4] = v[q4];
+                    }
+                }
+                float x = dsum;                 // Σ over the channel's LPC lanes
+                if constexpr (LPC >= 2) x += __shfl_xor_sync(0xffffffffu, x, CPW);
+                if constexpr (LPC >= 4) x += __shfl_xor_sync(0xffffffffu, x, 2 * CPW);
+                if (j == 0 && d_ok) p.seg_dsum[(static_cast<int64_t>(sg) * p.batch + b) * p.Dm + d] = x;
+            }
+        } else if (ch == nchunks - 1) {
             if (p.last_state && d_ok) {
                 float* out = p.last_state + (static_cast<int64_t>(b) * p.Dm + d) * p.N;
 #pragma unroll

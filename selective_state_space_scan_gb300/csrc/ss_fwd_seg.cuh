@@ -1,6 +1,6 @@
 // Selective-scan forward kernel, segment-lane layout (time-parallel inside a warp), for sm_103a.
 //
-// What it computes (per batch row b, channel d, state n, step t; h_{-1} = 0):
+// What it computes (per batch row b, channel d, state n, step t; h_{-1} = h0, or 0):
 //   Δ_t   = softplus(delta_raw[b,t,d] + delta_bias[d])
 //   h_t   = exp(Δ_t A_n) h_{t-1} + Δ_t B[b,t,n] u[b,t,d],   A_n = -exp(A_log[d,n])
 //   y_t   = (Σ_n C[b,t,n] h_t[n] + D[d] u[b,t,d]) · silu(z[b,t,d])
@@ -230,7 +230,9 @@ ss_fwd_seg_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
         const int dd = d0 + ww;
         sA[i] = (dd < p.Dm && n < p.N) ? -expf(p.A_log[static_cast<int64_t>(dd) * p.N + n]) * kLog2e
                                        : 0.f;
-        carry[i] = 0.f;
+        // the state before the first chunk: h0, or zeros
+        carry[i] = (p.h0 && dd < p.Dm && n < p.N)
+                       ? p.h0[(static_cast<int64_t>(b) * p.Dm + dd) * p.N + n] : 0.f;
     }
     __syncthreads();
     if (USE_TMA && tid == 0) {

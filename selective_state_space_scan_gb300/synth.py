@@ -142,6 +142,14 @@ def step_inputs(batch: int, Dm: int, N: int, io: str = "f32", seed: int = 4, lay
     return Workload(name, batch, 1, Dm, N, io, seed, arrays)
 
 
+def initial_state(batch: int, Dm: int, N: int, seed: int = 0) -> np.ndarray:
+    """A forward pass's initial state h0 [batch, Dm, N] fp32 ~ N(0, 0.5) (sd 0.5), the
+    distribution of the decode workload's states (its own generator stream)."""
+    g = rng_for(seed, 3)
+    f = np.float32
+    return (f(0.5) * g.standard_normal((batch, Dm, N), dtype=f)).astype(f)
+
+
 def config(name: str, **overrides) -> Workload:
     """The named workload (see CONFIGS); decode returns layer 0."""
     c = dict(CONFIGS[name])

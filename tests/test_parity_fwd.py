@@ -44,14 +44,14 @@ VARIANT_IDS = ["lane1-tma", "lane2-tma", "lane4-tma", "seg-tma", "lane1-plain", 
                "lane4-plain", "seg-plain"]
 
 
-def run_gpu(w, with_last=True, variant=(-1, 0, -1), balanced=True):
+def run_gpu(w, with_last=True, variant=(-1, 0, -1), workspace=True):
     a = w.arrays
     u, dr, z = to_dev(a["u"], w.io), to_dev(a["delta_raw"], w.io), to_dev(a["z"], w.io)
     Bm, Cm = to_dev(a["B"], w.io), to_dev(a["C"], w.io)
     last = torch.full((w.batch, w.Dm, w.N), float("nan"), device="cuda") if with_last else None
     with ForceVariant(*variant):
         y = ss.ss_fwd(u, dr, f32dev(a["delta_bias"]), f32dev(a["A_log"]), Bm, Cm, f32dev(a["D"]), z,
-                      last_state=last, balanced=balanced)
+                      last_state=last, workspace=workspace)
     torch.cuda.synchronize()
     return to_host(y), (to_host(last) if with_last else None)
 
@@ -257,8 +257,8 @@ def test_balanced_equals_per_tile(shape):
     w = synth.config(name) if dims is None else synth.fwd_inputs(*dims[:4], io=dims[4], seed=21)
     if dims is not None:
         assert ss.ss_fwd_workspace_size(*dims[:4], ss.SS_BF16 if dims[4] == "bf16" else ss.SS_F32) > 0
-    y1, l1 = run_gpu(w, balanced=False)
-    y2, l2 = run_gpu(w, balanced=True)
+    y1, l1 = run_gpu(w, workspace=False)
+    y2, l2 = run_gpu(w, workspace=True)
     np.testing.assert_array_equal(y1, y2)
     np.testing.assert_array_equal(l1, l2)
     if dims is not None and dims[0] * dims[1] * dims[2] < 3e6:
@@ -269,9 +269,9 @@ def test_balanced_equals_per_tile(shape):
 def test_balanced_repeated_calls_reuse_workspace():
     """Consecutive calls reuse one workspace: each call's epoch keeps stale hand-overs out."""
     w = synth.fwd_inputs(6, 1000, 4096, 16, seed=22)
-    y1, l1 = run_gpu(w, balanced=True)
+    y1, l1 = run_gpu(w, workspace=True)
     for _ in range(3):
-        y2, l2 = run_gpu(w, balanced=True)
+        y2, l2 = run_gpu(w, workspace=True)
         np.testing.assert_array_equal(y1, y2)
         np.testing.assert_array_equal(l1, l2)
 
