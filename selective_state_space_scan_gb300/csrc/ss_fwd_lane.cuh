@@ -267,8 +267,8 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
         for (int k = 0; k < pre; ++k) issue(k, smem + k * Cfg::STAGE_BYTES, &full[k]);
     }
 
-    // per-tile state of this lane (set when the unit loop enters a tile)
-    int cur_tile = -1, b = 0, d = 0;
+    // per-tile state of this lane (set when a piece enters a tile)
+    int b = 0, d = 0;
     bool d_ok = false;
     float bias_w = 0.f, D_w = 0.f;
     float2 A2[QPL][2];                   // A'[n] = -exp(A_log[d,n])·log2(e), hoisted out of the scan
@@ -280,239 +280,254 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
         h[qq][0] = h[qq][1] = make_float2(0.f, 0.f);
     }
 
-    for (int k = 0; k < total; ++k) {
-        int tile, ch;
-        work.unit(k, nchunks, tile, ch);
-        if (tile != cur_tile) {
-            cur_tile = tile;
-            b = tile / p.tiles_per_batch;
-            d = (tile % p.tiles_per_batch) * Cfg::W + warp * CPW + c;
-            d_ok = d < p.Dm;
-            bias_w = (p.bias && d_ok) ? p.bias[d] : 0.f;
-            D_w = (p.Dv && d_ok) ? p.Dv[d] : 0.f;
+    // The work is a list of pieces, each chunks [c0, c0 + cnt) of one tile, in the order the
+    // unit index k (the stage ring position) runs through them.  Entering a piece (tile
+    // constants, initial state) and leaving it (final or handed-over state) stay outside the
+    // chunk loop, which keeps that loop's body the fold alone.
+    const int whole_tiles = work.n1 / nchunks;
+    const int npieces = (work.n0 > 0 ? 1 : 0) + whole_tiles + (work.n2 > 0 ? 1 : 0);
+    int k = 0;
+    for (int piece = 0; piece < npieces; ++piece) {
+        int tile, c0, cnt;
+        const int q = piece - (work.n0 > 0 ? 1 : 0);
+        if (q < 0) {
+            tile = work.t0; c0 = 0; cnt = work.n0;            // head, handed over at its end
+        } else if (q < whole_tiles) {
+            tile = work.t1 + q; c0 = 0; cnt = nchunks;        // whole tile
+        } else {
+            tile = work.t2; c0 = work.c2; cnt = work.n2;      // tail, or a time-split segment
+        }
+        b = tile / p.tiles_per_batch;
+        d = (tile % p.tiles_per_batch) * Cfg::W + warp * CPW + c;
+        d_ok = d < p.Dm;
+        bias_w = (p.bias && d_ok) ? p.bias[d] : 0.f;
+        D_w = (p.Dv && d_ok) ? p.Dv[d] : 0.f;
 #pragma unroll
-            for (int qq = 0; qq < QPL; ++qq) {
-                float v[4];
+        for (int qq = 0; qq < QPL; ++qq) {
+            float v[4];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int n = n0 + 4 * qq + q4;
-                    v[q4] = (d_ok && n < p.N) ? -expf(p.A_log[static_cast<int64_t>(d) * p.N + n]) * kLog2e : 0.f;
-                }
-                A2[qq][0] = make_float2(v[0], v[1]);
-                A2[qq][1] = make_float2(v[2], v[3]);
-                h[qq][0] = h[qq][1] = make_float2(0.f, 0.f);
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const int n = n0 + 4 * qq + q4;
+                v[q4] = (d_ok && n < p.N) ? -expf(p.A_log[static_cast<int64_t>(d) * p.N + n]) * kLog2e : 0.f;
             }
-            dsum = 0.f;
-            if constexpr (!STATE_ONLY) {
-                const float* src = nullptr;    // the state before this unit's first chunk
-                if (p.seg_launch > 0) {
-                    // time-split pass C: the carry the carry kernel left for this segment
-                    src = p.seg_slots +
-                          ((static_cast<int64_t>(ch / p.seg_chunks) * p.batch + b) * p.Dm + d) * p.N;
-                } else if (ch == 0) {
-                    if (p.h0) src = p.h0 + (static_cast<int64_t>(b) * p.Dm + d) * p.N;
-                } else {
-                    // balanced: the tail of a tile whose head the previous CTA folded
-                    if (tid == 0) wait_published(p.ws_flag + blockIdx.x - 1, p.epoch, p.err);
-                    __syncthreads();
-                    const float* ws = p.ws_state + (static_cast<int64_t>(blockIdx.x - 1) * Cfg::W +
-                                                     warp * CPW + c) * NS + n0;
+            A2[qq][0] = make_float2(v[0], v[1]);
+            A2[qq][1] = make_float2(v[2], v[3]);
+            h[qq][0] = h[qq][1] = make_float2(0.f, 0.f);
+        }
+        dsum = 0.f;
+        if constexpr (!STATE_ONLY) {
+            const float* src = nullptr;    // the state before this unit's first chunk
+            if (p.seg_launch > 0) {
+                // time-split pass C: the carry the carry kernel left for this segment
+                src = p.seg_slots +
+                      ((static_cast<int64_t>(c0 / p.seg_chunks) * p.batch + b) * p.Dm + d) * p.N;
+            } else if (c0 == 0) {
+                if (p.h0) src = p.h0 + (static_cast<int64_t>(b) * p.Dm + d) * p.N;
+            } else {
+                // balanced: the tail of a tile whose head the previous CTA folded
+                if (tid == 0) wait_published(p.ws_flag + blockIdx.x - 1, p.epoch, p.err);
+                __syncthreads();
+                const float* ws = p.ws_state + (static_cast<int64_t>(blockIdx.x - 1) * Cfg::W +
+                                                 warp * CPW + c) * NS + n0;
 #pragma unroll
-                    for (int qq = 0; qq < QPL; ++qq) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4*>(ws + 4 * qq));
-                        h[qq][0] = make_float2(v.x, v.y);
-                        h[qq][1] = make_float2(v.z, v.w);
-                    }
+                for (int qq = 0; qq < QPL; ++qq) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(ws + 4 * qq));
+                    h[qq][0] = make_float2(v.x, v.y);
+                    h[qq][1] = make_float2(v.z, v.w);
                 }
-                if (src && d_ok) {
+            }
+            if (src && d_ok) {
 #pragma unroll
-                    for (int qq = 0; qq < QPL; ++qq) {
-                        float v[4];
+                for (int qq = 0; qq < QPL; ++qq) {
+                    float v[4];
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const int n = n0 + 4 * qq + q4;
-                            v[q4] = n < p.N ? __ldcg(src + n) : 0.f;
-                        }
-                        h[qq][0] = make_float2(v[0], v[1]);
-                        h[qq][1] = make_float2(v[2], v[3]);
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int n = n0 + 4 * qq + q4;
+                        v[q4] = n < p.N ? __ldcg(src + n) : 0.f;
                     }
+                    h[qq][0] = make_float2(v[0], v[1]);
+                    h[qq][1] = make_float2(v[2], v[3]);
                 }
             }
         }
 
-        const int stage = k % STAGES;
-        uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
-        if (USE_TMA) {
-            mbar_wait_bounded(&full[stage], static_cast<uint32_t>((k / STAGES) & 1), abort_flag, p.err);
-        } else {
-            lane_fill_generic<Cfg>(st, p, b, (tile % p.tiles_per_batch) * Cfg::W, ch);
-            __syncthreads();
-        }
-        const int sub = warp * Cfg::up128(Cfg::SUB) / Cfg::ES;   // element offset of this warp's sub-tile
-        const TIO* tu = reinterpret_cast<const TIO*>(st + Cfg::OFF_U) + sub;
-        const TIO* td = reinterpret_cast<const TIO*>(st + Cfg::OFF_D) + sub;
-        const TIO* tz = reinterpret_cast<const TIO*>(st + Cfg::OFF_Z) + sub;
-        const float* tB;
-        const float* tC;
-        if constexpr (Cfg::CONVERT_BC) {
-            const TIO* rb = reinterpret_cast<const TIO*>(st + Cfg::OFF_B);
-            const TIO* rc = reinterpret_cast<const TIO*>(st + Cfg::OFF_C);
-            for (int i = tid; i < T * NS; i += Cfg::THREADS) {
-                bcf[i] = to_f32<TIO>(rb[i]);
-                bcf[T * NS + i] = to_f32<TIO>(rc[i]);
+        for (int i = 0; i < cnt; ++i, ++k) {
+            const int ch = c0 + i;
+            const int stage = k % STAGES;
+            uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
+            if (USE_TMA) {
+                mbar_wait_bounded(&full[stage], static_cast<uint32_t>((k / STAGES) & 1), abort_flag, p.err);
+            } else {
+                lane_fill_generic<Cfg>(st, p, b, (tile % p.tiles_per_batch) * Cfg::W, ch);
+                __syncthreads();
             }
-            __syncthreads();
-            tB = bcf;
-            tC = bcf + T * NS;
-        } else {
-            tB = reinterpret_cast<const float*>(st + Cfg::OFF_B);
-            tC = reinterpret_cast<const float*>(st + Cfg::OFF_C);
-        }
-        const int64_t tbase = static_cast<int64_t>(ch) * T;
-        const int64_t left = L - tbase;                     // steps of this chunk before L
-        const bool whole = left >= T;
-        constexpr int GT = T / LPC;                         // step groups in the chunk
-        constexpr int G = GT > 16 ? 16 : GT;                // groups per sub-block (register budget)
-        static_assert(GT % G == 0, "chunk must be whole sub-blocks");
-#pragma unroll 1
-        for (int g0 = 0; g0 < GT; g0 += G) {
-            // Phase 1: Δ and Δ·u of the steps this lane prepares (step g·LPC + j of each group;
-            // zero past L, i.e. identity pairs).  G independent softplus chains.
-            float dd[G], du[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const int r = (g0 + g) * LPC + j;
-                const float x = softplus(to_f32<TIO>(td[r * CPW + c]) + bias_w);
-                dd[g] = x;
-                du[g] = x * to_f32<TIO>(tu[r * CPW + c]);
-            }
-            if (!whole) {
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-                    if ((g0 + g) * LPC + j >= left) dd[g] = du[g] = 0.f;
-            }
-            if constexpr (STATE_ONLY) {
-#pragma unroll
-                for (int g = 0; g < G; ++g) dsum += dd[g];
-            }
-            // Phase 2: the sequential fold.  Step g·LPC + k takes its Δ, Δ·u from lane (c, k);
-            // the C·h partial sums of the channel's LPC lanes are reduce-scattered so that lane
-            // (c, j) ends with the sum of step g·LPC + j.
-            float yv[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float dk[LPC], uk[LPC];
-#pragma unroll
-                for (int kk = 0; kk < LPC; ++kk) {
-                    dk[kk] = LPC == 1 ? dd[g] : __shfl_sync(0xffffffffu, dd[g], kk * CPW + c);
-                    uk[kk] = LPC == 1 ? du[g] : __shfl_sync(0xffffffffu, du[g], kk * CPW + c);
+            const int sub = warp * Cfg::up128(Cfg::SUB) / Cfg::ES;   // element offset of this warp's sub-tile
+            const TIO* tu = reinterpret_cast<const TIO*>(st + Cfg::OFF_U) + sub;
+            const TIO* td = reinterpret_cast<const TIO*>(st + Cfg::OFF_D) + sub;
+            const TIO* tz = reinterpret_cast<const TIO*>(st + Cfg::OFF_Z) + sub;
+            const float* tB;
+            const float* tC;
+            if constexpr (Cfg::CONVERT_BC) {
+                const TIO* rb = reinterpret_cast<const TIO*>(st + Cfg::OFF_B);
+                const TIO* rc = reinterpret_cast<const TIO*>(st + Cfg::OFF_C);
+                for (int i = tid; i < T * NS; i += Cfg::THREADS) {
+                    bcf[i] = to_f32<TIO>(rb[i]);
+                    bcf[T * NS + i] = to_f32<TIO>(rc[i]);
                 }
-                float yp[LPC];
-#pragma unroll
-                for (int kk = 0; kk < LPC; ++kk) {
-                    const float2 dl2 = make_float2(dk[kk], dk[kk]), du2 = make_float2(uk[kk], uk[kk]);
-                    const int row = (g0 + g) * LPC + kk;
-                    float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int qq = 0; qq < QPL; ++qq) {
-                        const float4 B4 = *reinterpret_cast<const float4*>(tB + row * NS + n0 + 4 * qq);
-                        const float2 a01 = ex2x2(mul2(dl2, A2[qq][0]));
-                        const float2 a23 = ex2x2(mul2(dl2, A2[qq][1]));
-                        h[qq][0] = fma2(a01, h[qq][0], mul2(du2, make_float2(B4.x, B4.y)));
-                        h[qq][1] = fma2(a23, h[qq][1], mul2(du2, make_float2(B4.z, B4.w)));
-                        if constexpr (!STATE_ONLY) {
-                            const float4 C4 = *reinterpret_cast<const float4*>(tC + row * NS + n0 + 4 * qq);
-                            acc = fma2(make_float2(C4.x, C4.y), h[qq][0], acc);
-                            acc = fma2(make_float2(C4.z, C4.w), h[qq][1], acc);
-                        }
-                    }
-                    yp[kk] = acc.x + acc.y;
+                __syncthreads();
+                tB = bcf;
+                tC = bcf + T * NS;
+            } else {
+                tB = reinterpret_cast<const float*>(st + Cfg::OFF_B);
+                tC = reinterpret_cast<const float*>(st + Cfg::OFF_C);
+            }
+            const int64_t tbase = static_cast<int64_t>(ch) * T;
+            const int64_t left = L - tbase;                     // steps of this chunk before L
+            const bool whole = left >= T;
+            constexpr int GT = T / LPC;                         // step groups in the chunk
+            constexpr int G = GT > 16 ? 16 : GT;                // groups per sub-block (register budget)
+            static_assert(GT % G == 0, "chunk must be whole sub-blocks");
+    #pragma unroll 1
+            for (int g0 = 0; g0 < GT; g0 += G) {
+                // Phase 1: Δ and Δ·u of the steps this lane prepares (step g·LPC + j of each group;
+                // zero past L, i.e. identity pairs).  G independent softplus chains.
+                float dd[G], du[G];
+    #pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const int r = (g0 + g) * LPC + j;
+                    const float x = softplus(to_f32<TIO>(td[r * CPW + c]) + bias_w);
+                    dd[g] = x;
+                    du[g] = x * to_f32<TIO>(tu[r * CPW + c]);
+                }
+                if (!whole) {
+    #pragma unroll
+                    for (int g = 0; g < G; ++g)
+                        if ((g0 + g) * LPC + j >= left) dd[g] = du[g] = 0.f;
                 }
                 if constexpr (STATE_ONLY) {
-                    (void)yp;
-                } else if constexpr (LPC == 1) {
-                    yv[g] = yp[0];
-                } else if constexpr (LPC == 2) {
-                    const bool hi = j & 1;
-                    const float send = hi ? yp[0] : yp[1];
-                    const float keep = hi ? yp[1] : yp[0];
-                    yv[g] = keep + __shfl_xor_sync(0xffffffffu, send, CPW);
-                } else {
-                    // butterfly reduce-scatter over the four slices (lanes c + CPW·s): first
-                    // across slice bit 1 (each side keeps two steps), then across bit 0.  Only
-                    // shuffles, no shared-memory round trip or warp barrier, so the next
-                    // group's loads are free to start early.
-                    const bool b1 = (j & 2) != 0, b0 = (j & 1) != 0;
-                    const float s0 = b1 ? yp[0] : yp[2], s1 = b1 ? yp[1] : yp[3];
-                    const float k0 = b1 ? yp[2] : yp[0], k1 = b1 ? yp[3] : yp[1];
-                    const float t0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 2 * CPW);   // step 2·b1
-                    const float t1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 2 * CPW);   // step 2·b1 + 1
-                    const float sd = b0 ? t0 : t1, kp = b0 ? t1 : t0;
-                    yv[g] = kp + __shfl_xor_sync(0xffffffffu, sd, CPW);                 // step j
+    #pragma unroll
+                    for (int g = 0; g < G; ++g) dsum += dd[g];
                 }
-            }
-            // Phase 3: D skip, z gate, store (G independent chains).
-            if (!STATE_ONLY && d_ok) {
-                char* yrow = reinterpret_cast<char*>(static_cast<TIO*>(p.y) + b * p.y_b + (tbase + g0 * LPC + j) * p.y_l + d);
-                const int64_t rem = left - g0 * LPC - j;          // steps of this lane's column before L
-                const int nst = whole ? G : (rem <= 0 ? 0 : rem >= int64_t(G) * LPC ? G : static_cast<int>((rem + LPC - 1) / LPC));
-                if (has_z && nst == G) {
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const int r = (g0 + g) * LPC + j;
-                        const float v = fmaf(D_w, to_f32<TIO>(tu[r * CPW + c]), yv[g]) * silu(to_f32<TIO>(tz[r * CPW + c]));
-                        *reinterpret_cast<TIO*>(yrow + g * LPC * ystride) = from_f32<TIO>(v);
+                // Phase 2: the sequential fold.  Step g·LPC + k takes its Δ, Δ·u from lane (c, k);
+                // the C·h partial sums of the channel's LPC lanes are reduce-scattered so that lane
+                // (c, j) ends with the sum of step g·LPC + j.
+                float yv[G];
+    #pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float dk[LPC], uk[LPC];
+    #pragma unroll
+                    for (int kk = 0; kk < LPC; ++kk) {
+                        dk[kk] = LPC == 1 ? dd[g] : __shfl_sync(0xffffffffu, dd[g], kk * CPW + c);
+                        uk[kk] = LPC == 1 ? du[g] : __shfl_sync(0xffffffffu, du[g], kk * CPW + c);
                     }
-                } else {
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        if (g < nst) {
+                    float yp[LPC];
+    #pragma unroll
+                    for (int kk = 0; kk < LPC; ++kk) {
+                        const float2 dl2 = make_float2(dk[kk], dk[kk]), du2 = make_float2(uk[kk], uk[kk]);
+                        const int row = (g0 + g) * LPC + kk;
+                        float2 acc = make_float2(0.f, 0.f);
+    #pragma unroll
+                        for (int qq = 0; qq < QPL; ++qq) {
+                            // B and C are loaded together, ahead of the decay (their latency overlaps it)
+                            const float4 B4 = *reinterpret_cast<const float4*>(tB + row * NS + n0 + 4 * qq);
+                            float4 C4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if constexpr (!STATE_ONLY)
+                                C4 = *reinterpret_cast<const float4*>(tC + row * NS + n0 + 4 * qq);
+                            const float2 a01 = ex2x2(mul2(dl2, A2[qq][0]));
+                            const float2 a23 = ex2x2(mul2(dl2, A2[qq][1]));
+                            h[qq][0] = fma2(a01, h[qq][0], mul2(du2, make_float2(B4.x, B4.y)));
+                            h[qq][1] = fma2(a23, h[qq][1], mul2(du2, make_float2(B4.z, B4.w)));
+                            if constexpr (!STATE_ONLY) {
+                                acc = fma2(make_float2(C4.x, C4.y), h[qq][0], acc);
+                                acc = fma2(make_float2(C4.z, C4.w), h[qq][1], acc);
+                            }
+                        }
+                        yp[kk] = acc.x + acc.y;
+                    }
+                    if constexpr (STATE_ONLY) {
+                        (void)yp;
+                    } else if constexpr (LPC == 1) {
+                        yv[g] = yp[0];
+                    } else if constexpr (LPC == 2) {
+                        const bool hi = j & 1;
+                        const float send = hi ? yp[0] : yp[1];
+                        const float keep = hi ? yp[1] : yp[0];
+                        yv[g] = keep + __shfl_xor_sync(0xffffffffu, send, CPW);
+                    } else {
+                        // butterfly reduce-scatter over the four slices (lanes c + CPW·s): first
+                        // across slice bit 1 (each side keeps two steps), then across bit 0.  Only
+                        // shuffles, no shared-memory round trip or warp barrier, so the next
+                        // group's loads are free to start early.
+                        const bool b1 = (j & 2) != 0, b0 = (j & 1) != 0;
+                        const float s0 = b1 ? yp[0] : yp[2], s1 = b1 ? yp[1] : yp[3];
+                        const float k0 = b1 ? yp[2] : yp[0], k1 = b1 ? yp[3] : yp[1];
+                        const float t0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 2 * CPW);   // step 2·b1
+                        const float t1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 2 * CPW);   // step 2·b1 + 1
+                        const float sd = b0 ? t0 : t1, kp = b0 ? t1 : t0;
+                        yv[g] = kp + __shfl_xor_sync(0xffffffffu, sd, CPW);                 // step j
+                    }
+                }
+                // Phase 3: D skip, z gate, store (G independent chains).
+                if (!STATE_ONLY && d_ok) {
+                    char* yrow = reinterpret_cast<char*>(static_cast<TIO*>(p.y) + b * p.y_b + (tbase + g0 * LPC + j) * p.y_l + d);
+                    const int64_t rem = left - g0 * LPC - j;          // steps of this lane's column before L
+                    const int nst = whole ? G : (rem <= 0 ? 0 : rem >= int64_t(G) * LPC ? G : static_cast<int>((rem + LPC - 1) / LPC));
+                    if (has_z && nst == G) {
+    #pragma unroll
+                        for (int g = 0; g < G; ++g) {
                             const int r = (g0 + g) * LPC + j;
-                            float v = fmaf(D_w, to_f32<TIO>(tu[r * CPW + c]), yv[g]);
-                            if (has_z) v *= silu(to_f32<TIO>(tz[r * CPW + c]));
+                            const float v = fmaf(D_w, to_f32<TIO>(tu[r * CPW + c]), yv[g]) * silu(to_f32<TIO>(tz[r * CPW + c]));
                             *reinterpret_cast<TIO*>(yrow + g * LPC * ystride) = from_f32<TIO>(v);
+                        }
+                    } else {
+    #pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            if (g < nst) {
+                                const int r = (g0 + g) * LPC + j;
+                                float v = fmaf(D_w, to_f32<TIO>(tu[r * CPW + c]), yv[g]);
+                                if (has_z) v *= silu(to_f32<TIO>(tz[r * CPW + c]));
+                                *reinterpret_cast<TIO*>(yrow + g * LPC * ystride) = from_f32<TIO>(v);
+                            }
                         }
                     }
                 }
             }
-        }
-        if (USE_TMA && !Cfg::CONVERT_BC) {
-            // Release the stage without a block-wide barrier: the warp that finishes it last
-            // refills it, so warps that are ahead run on into the stages already loaded.
-            __syncwarp();
-            if (lane == 0) {
-                __threadfence_block();
-                if (atomicAdd(&done[stage], 1) == Cfg::WARPS - 1) {
-                    done[stage] = 0;
-                    if (k + STAGES < total && !*abort_flag) issue(k + STAGES, st, &full[stage]);
-                }
-            }
-        } else {
-            __syncthreads();   // stage (and the widened B/C) consumed by every warp
-            if (USE_TMA && tid == 0 && k + STAGES < total && !*abort_flag) issue(k + STAGES, st, &full[stage]);
-        }
-
-        // End of a tile piece: the sequence's final state, or (head of a tile another CTA
-        // finishes) the state to hand over; for pass A, the segment's end state and Σ Δ.
-        if constexpr (STATE_ONLY) {
-            if (k == total - 1) {
-                const int sg = ch / p.seg_chunks;
-                if (d_ok) {
-                    float* dst = p.seg_slots + ((static_cast<int64_t>(sg + 1) * p.batch + b) * p.Dm + d) * p.N;
-#pragma unroll
-                    for (int qq = 0; qq < QPL; ++qq) {
-                        const float v[4] = {h[qq][0].x, h[qq][0].y, h[qq][1].x, h[qq][1].y};
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4)
-                            if (n0 + 4 * qq + q4 < p.N) dst[n0 + 4 * qq + q4] = v[q4];
+            if (USE_TMA && !Cfg::CONVERT_BC) {
+                // Release the stage without a block-wide barrier: the warp that finishes it last
+                // refills it, so warps that are ahead run on into the stages already loaded.
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence_block();
+                    if (atomicAdd(&done[stage], 1) == Cfg::WARPS - 1) {
+                        done[stage] = 0;
+                        if (k + STAGES < total && !*abort_flag) issue(k + STAGES, st, &full[stage]);
                     }
                 }
-                float x = dsum;                 // Σ over the channel's LPC lanes
-                if constexpr (LPC >= 2) x += __shfl_xor_sync(0xffffffffu, x, CPW);
-                if constexpr (LPC >= 4) x += __shfl_xor_sync(0xffffffffu, x, 2 * CPW);
-                if (j == 0 && d_ok) p.seg_dsum[(static_cast<int64_t>(sg) * p.batch + b) * p.Dm + d] = x;
+            } else {
+                __syncthreads();   // stage (and the widened B/C) consumed by every warp
+                if (USE_TMA && tid == 0 && k + STAGES < total && !*abort_flag) issue(k + STAGES, st, &full[stage]);
             }
-        } else if (ch == nchunks - 1) {
+        }
+
+        // End of the piece: the sequence's final state, or (head of a tile another CTA
+        // finishes) the state to hand over; for pass A, the segment's end state and Σ Δ.
+        if constexpr (STATE_ONLY) {
+            const int sg = c0 / p.seg_chunks;
+            if (d_ok) {
+                float* dst = p.seg_slots + ((static_cast<int64_t>(sg + 1) * p.batch + b) * p.Dm + d) * p.N;
+#pragma unroll
+                for (int qq = 0; qq < QPL; ++qq) {
+                    const float v[4] = {h[qq][0].x, h[qq][0].y, h[qq][1].x, h[qq][1].y};
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        if (n0 + 4 * qq + q4 < p.N) dst[n0 + 4 * qq + q4] = v[q4];
+                }
+            }
+            float x = dsum;                 // Σ over the channel's LPC lanes
+            if constexpr (LPC >= 2) x += __shfl_xor_sync(0xffffffffu, x, CPW);
+            if constexpr (LPC >= 4) x += __shfl_xor_sync(0xffffffffu, x, 2 * CPW);
+            if (j == 0 && d_ok) p.seg_dsum[(static_cast<int64_t>(sg) * p.batch + b) * p.Dm + d] = x;
+        } else if (c0 + cnt == nchunks) {
             if (p.last_state && d_ok) {
                 float* out = p.last_state + (static_cast<int64_t>(b) * p.Dm + d) * p.N;
 #pragma unroll
@@ -523,7 +538,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                         if (n0 + 4 * qq + q4 < p.N) out[n0 + 4 * qq + q4] = v[q4];
                 }
             }
-        } else if (k == work.n0 - 1) {
+        } else if (work.n0 > 0 && piece == 0) {
             float* dst = p.ws_state + (static_cast<int64_t>(blockIdx.x) * Cfg::W + warp * CPW + c) * NS + n0;
 #pragma unroll
             for (int qq = 0; qq < QPL; ++qq)
