@@ -24,6 +24,7 @@ struct FwdParams {
     int tiles_per_batch;
     int chunk_steps;     // steps per chunk the host sized the grid and TMA boxes for
     int tile_channels;   // channels per CTA the host sized them for
+    int box_channels;    // width of the u/Δ/z TMA boxes the host encoded (0: no TMA)
     unsigned int* err;   // device error word
     // Balanced schedule (ws_flag != nullptr): the grid's CTAs split the batch·tiles·nchunks
     // (tile, chunk) units into equal contiguous ranges; a range that starts inside a tile takes

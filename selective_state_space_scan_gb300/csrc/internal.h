@@ -31,7 +31,7 @@ struct FwdGeom {
 
 inline FwdGeom fwd_geometry(const FwdVariant& v) {
     if (v.family == kFamSeg) return FwdGeom{8 * kSegG, 8 * kSegG, 4 * kSegQ * kSegK};
-    return FwdGeom{lane_w(v.lpc, v.balanced), 32 / v.lpc, kLaneT};
+    return FwdGeom{lane_w(v.lpc, v.balanced), lane_w(v.lpc, v.balanced), kLaneT};
 }
 
 // Launch (grid = p.grid CTAs; cooperative when v.balanced).  With `max_grid` non-null, launch

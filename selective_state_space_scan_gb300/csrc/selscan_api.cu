@@ -422,28 +422,33 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         }
     }
 
-    // TMA descriptors (their boxes do not depend on the schedule).  The segment-lane kernel
-    // reads its tiles through the hardware swizzle; the lane kernel reads whole rows of its
-    // own sub-tiles and needs none.  A shape the descriptor encoder rejects is served by the
-    // plain-load fill.
+    // TMA descriptors.  Both kernels read the u/Δ/z tiles through the hardware swizzle (one
+    // box per stream, rows of a whole tile's channels); the segment-lane kernel also reads its
+    // B/C tiles swizzled, the lane kernel reads them linearly.  A shape the descriptor encoder
+    // rejects is served by the plain-load fill.
+    // The schedule fixes the tile width (and so the box width): decide it first.  With a
+    // workspace, TMA-fed lane kernels that do not take the time split run the balanced one.
+    v.balanced = plan.nseg < 2 && workspace != nullptr && v.family == kFamLane && tma &&
+                 g_force_balanced.load() != 0;
     FwdMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     if (tma) {
         const FwdGeom g0 = fwd_geometry(v);
-        const bool sw = v.family == kFamSeg;
+        const bool swbc = v.family == kFamSeg;
         const int bw = g0.box_channels, bh = g0.chunk_steps;
-        tma = make_map(&maps.u, u, bf16, Dm, L, batch, s.u_l, s.u_b, bw, bh, sw) &&
-              make_map(&maps.delta, delta_raw, bf16, Dm, L, batch, s.delta_l, s.delta_b, bw, bh, sw) &&
-              (!z || make_map(&maps.z, z, bf16, Dm, L, batch, s.z_l, s.z_b, bw, bh, sw)) &&
-              make_map(&maps.B, B, bf16, N, L, batch, s.B_l, s.B_b, v.ns, bh, sw) &&
-              make_map(&maps.C, C, bf16, N, L, batch, s.C_l, s.C_b, v.ns, bh, sw);
+        tma = make_map(&maps.u, u, bf16, Dm, L, batch, s.u_l, s.u_b, bw, bh, true) &&
+              make_map(&maps.delta, delta_raw, bf16, Dm, L, batch, s.delta_l, s.delta_b, bw, bh, true) &&
+              (!z || make_map(&maps.z, z, bf16, Dm, L, batch, s.z_l, s.z_b, bw, bh, true)) &&
+              make_map(&maps.B, B, bf16, N, L, batch, s.B_l, s.B_b, v.ns, bh, swbc) &&
+              make_map(&maps.C, C, bf16, N, L, batch, s.C_l, s.C_b, v.ns, bh, swbc);
     }
     if (ft == 1 && !tma) return SS_ERR_UNSUPPORTED;
     v.tma = tma;
-    if (!tma) plan = SplitPlan();   // descriptors refused: the plain-load fill, no time split
+    if (!tma) {                     // descriptors refused: the plain-load fill, per-tile schedule
+        plan = SplitPlan();
+        v.balanced = false;
+    }
     const bool split = plan.nseg >= 2;
-    // Otherwise, with a workspace, TMA-fed lane kernels run the balanced schedule.
-    v.balanced = !split && workspace != nullptr && v.family == kFamLane && tma && g_force_balanced.load() != 0;
 
     FwdParams p;
     std::memset(&p, 0, sizeof(p));
@@ -463,6 +468,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     p.tiles_per_batch = static_cast<int>(tiles);
     p.chunk_steps = geo.chunk_steps;
     p.tile_channels = geo.tile_channels;
+    p.box_channels = tma ? geo.box_channels : 0;
     p.err = device_error_ptr();
     if (!p.err) return SS_ERR_CUDA;
     if (v.balanced) {

@@ -26,7 +26,8 @@
 //      partial sums of a channel's LPC lanes are reduce-scattered by shuffles so that lane
 //      (c, j) owns step j's sum;
 //   3. D·u skip, z gate, store (one row of the warp's channels per step).
-// u/Δ/z arrive by TMA as one [T × CPW] tile per warp, B/C as one [T × NS] tile per CTA, in a
+// u/Δ/z arrive by TMA as one [T × W] tile per stream (rows of W channels, hardware swizzle:
+// few, long rows keep the TMA engine's row count low), B/C as one [T × NS] tile, in a
 // STAGES-deep ring of mbarrier-completed stages.  Steps past L are identity pairs (Δ = 0).
 //
 // Schedules.  Without a workspace each CTA owns one tile and walks its whole sequence.  With
@@ -61,21 +62,23 @@ struct LaneCfg {
     static constexpr int ES = sizeof(TIO);
     static constexpr bool CONVERT_BC = ES == 2;
     static constexpr int up128(int x) { return (x + 127) / 128 * 128; }
-    static constexpr int SUB = T * CPW * ES;                  // one warp's u/Δ/z sub-tile
-    static constexpr int TILE_X = WARPS * up128(SUB);          // one tensor, all warps
+    static constexpr int up1024(int x) { return (x + 1023) / 1024 * 1024; }
+    static constexpr int RB = W * ES;                         // bytes of one tile row (W channels)
+    static constexpr int TILE_X = T * RB;                     // one tensor's [T][W] tile, swizzled
     static constexpr int TILE_N = T * NS * ES;
     static constexpr int OFF_U = 0;
     static constexpr int OFF_D = TILE_X;
     static constexpr int OFF_Z = 2 * TILE_X;
     static constexpr int OFF_B = 3 * TILE_X;
     static constexpr int OFF_C = OFF_B + up128(TILE_N);
-    static constexpr int STAGE_BYTES = OFF_C + up128(TILE_N);
+    static constexpr int STAGE_BYTES = up1024(OFF_C + up128(TILE_N));   // keeps every tile 1 KB aligned
     static constexpr int AUX_BC = 0;                                       // fp32 B,C [2][T][NS]
     static constexpr int AUX_FLAG = AUX_BC + (CONVERT_BC ? 2 * T * NS * 4 : 0);
     static constexpr int AUX_DONE = AUX_FLAG + 16;                        // per-stage warp counters
     static constexpr int AUX_BAR = AUX_DONE + ((STAGES * 4 + 15) / 16) * 16;
     static constexpr int AUX_BYTES = AUX_BAR + STAGES * 8;
-    static constexpr int SMEM_BYTES = 128 + STAGES * STAGE_BYTES + AUX_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + AUX_BYTES;
+    static_assert(RB == 128 || RB == 64 || RB == 32, "a tile row must be one TMA swizzle span");
     static_assert(NS % (4 * LPC) == 0, "each lane must hold whole state quads");
     static_assert(W % CPW == 0 && WARPS >= 1, "a tile is whole warps");
     static_assert(T % LPC == 0 && T <= 256, "chunk must be whole groups and one TMA box");
@@ -138,7 +141,7 @@ __device__ __forceinline__ LaneWork lane_work(const FwdParams& p, int tiles_tota
     return w;
 }
 
-// Plain-load fill of one stage with the TMA layout (per-warp sub-tiles, zeros outside).
+// Plain-load fill of one stage with the TMA layout (swizzled [T][W] tiles, zeros outside).
 template <class Cfg>
 __device__ void lane_fill_generic(uint8_t* st, const FwdParams& p, int b, int d0, int chunk) {
     using TIO = typename Cfg::TIO;
@@ -154,10 +157,10 @@ __device__ void lane_fill_generic(uint8_t* st, const FwdParams& p, int b, int d0
         const int64_t t = t0 + r;
         const int d = d0 + w * Cfg::CPW + c;
         const bool in = t < p.L && d < p.Dm;
-        const int o = w * Cfg::up128(Cfg::SUB) / Cfg::ES + rem;
-        reinterpret_cast<TIO*>(st + Cfg::OFF_U)[o] = in ? u[b * p.u_b + t * p.u_l + d] : zero;
-        reinterpret_cast<TIO*>(st + Cfg::OFF_D)[o] = in ? dl[b * p.d_b + t * p.d_l + d] : zero;
-        if (z) reinterpret_cast<TIO*>(st + Cfg::OFF_Z)[o] = in ? z[b * p.z_b + t * p.z_l + d] : zero;
+        const uint32_t o = swz<Cfg::RB>(static_cast<uint32_t>(r * Cfg::RB + (w * Cfg::CPW + c) * Cfg::ES));
+        *reinterpret_cast<TIO*>(st + Cfg::OFF_U + o) = in ? u[b * p.u_b + t * p.u_l + d] : zero;
+        *reinterpret_cast<TIO*>(st + Cfg::OFF_D + o) = in ? dl[b * p.d_b + t * p.d_l + d] : zero;
+        if (z) *reinterpret_cast<TIO*>(st + Cfg::OFF_Z + o) = in ? z[b * p.z_b + t * p.z_l + d] : zero;
     }
     const TIO* Bm = static_cast<const TIO*>(p.Bm);
     const TIO* Cm = static_cast<const TIO*>(p.Cm);
@@ -173,17 +176,13 @@ __device__ void lane_fill_generic(uint8_t* st, const FwdParams& p, int b, int d0
 template <class Cfg>
 __device__ __forceinline__ void lane_issue_tma(uint8_t* st, uint64_t* bar, const FwdMaps& m,
                                                bool has_z, int b, int d0, int chunk) {
-    const uint32_t bytes = (has_z ? 3u : 2u) * Cfg::WARPS * Cfg::SUB + 2u * Cfg::TILE_N;
+    const uint32_t bytes = (has_z ? 3u : 2u) * Cfg::TILE_X + 2u * Cfg::TILE_N;
     mbar_expect_tx(bar, bytes);
     const int t0 = chunk * Cfg::T;
-#pragma unroll
-    for (int w = 0; w < Cfg::WARPS; ++w) {
-        const int o = w * Cfg::up128(Cfg::SUB);
-        const int dw = d0 + w * Cfg::CPW;
-        tma_load_3d(st + Cfg::OFF_U + o, &m.u, bar, dw, t0, b);
-        tma_load_3d(st + Cfg::OFF_D + o, &m.delta, bar, dw, t0, b);
-        if (has_z) tma_load_3d(st + Cfg::OFF_Z + o, &m.z, bar, dw, t0, b);
-    }
+    // one [T][W] box per stream (rows of W channels, hardware swizzle), one [T][NS] box for B, C
+    tma_load_3d(st + Cfg::OFF_U, &m.u, bar, d0, t0, b);
+    tma_load_3d(st + Cfg::OFF_D, &m.delta, bar, d0, t0, b);
+    if (has_z) tma_load_3d(st + Cfg::OFF_Z, &m.z, bar, d0, t0, b);
     tma_load_3d(st + Cfg::OFF_B, &m.B, bar, 0, t0, b);
     tma_load_3d(st + Cfg::OFF_C, &m.C, bar, 0, t0, b);
 }
@@ -216,8 +215,9 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     constexpr int LPC = Cfg::LPC, CPW = Cfg::CPW, NS = Cfg::NS, QPL = Cfg::QPL, T = Cfg::T;
     constexpr int STAGES = USE_TMA ? Cfg::STAGES : 1;
 
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    uint8_t* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1 KB alignment (the 128-byte swizzle's period) by pointer arithmetic on the shared array
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t* aux = smem + STAGES * Cfg::STAGE_BYTES;
     float* bcf = reinterpret_cast<float*>(aux + Cfg::AUX_BC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(aux + Cfg::AUX_FLAG);
@@ -226,7 +226,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
 
     // A grid or TMA box sized for another tile shape would never complete the stage
     // barriers: refuse to run, and say so.
-    if (p.chunk_steps != T || p.tile_channels != Cfg::W) {
+    if (p.chunk_steps != T || p.tile_channels != Cfg::W || (USE_TMA && p.box_channels != Cfg::W)) {
         if (threadIdx.x == 0 && p.err) atomicOr(p.err, kErrGeometry);
         return;
     }
@@ -241,6 +241,14 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     const int64_t ystride = p.y_l * static_cast<int64_t>(sizeof(TIO));   // bytes between steps of y
     const LaneWork work = lane_work(p, p.batch * p.tiles_per_batch);
     const int total = work.total();
+    // Byte offset of this lane's element in a swizzled [T][W] tile, for rows j + q·LPC (row
+    // offset included).  A sub-block's rows g·LPC + j fall in NCX classes mod 8, and the
+    // swizzle depends on the row only mod 8.
+    constexpr int NCX = LPC == 4 ? 2 : LPC == 2 ? 4 : 8;
+    uint32_t cx[NCX];
+#pragma unroll
+    for (int q = 0; q < NCX; ++q)
+        cx[q] = swz<Cfg::RB>(static_cast<uint32_t>((q * LPC + j) * Cfg::RB + (warp * CPW + c) * Cfg::ES));
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -361,10 +369,14 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                 lane_fill_generic<Cfg>(st, p, b, (tile % p.tiles_per_batch) * Cfg::W, ch);
                 __syncthreads();
             }
-            const int sub = warp * Cfg::up128(Cfg::SUB) / Cfg::ES;   // element offset of this warp's sub-tile
-            const TIO* tu = reinterpret_cast<const TIO*>(st + Cfg::OFF_U) + sub;
-            const TIO* td = reinterpret_cast<const TIO*>(st + Cfg::OFF_D) + sub;
-            const TIO* tz = reinterpret_cast<const TIO*>(st + Cfg::OFF_Z) + sub;
+            const uint8_t* tu = st + Cfg::OFF_U;
+            const uint8_t* td = st + Cfg::OFF_D;
+            const uint8_t* tz = st + Cfg::OFF_Z;
+            // this lane's element of row (g0 + g)·LPC + j (g0 a multiple of G, hence of NCX)
+            auto at = [&](const uint8_t* tile, int g0, int g) -> float {
+                return to_f32<TIO>(*reinterpret_cast<const TIO*>(tile + (g0 + g - g % NCX) * LPC * Cfg::RB +
+                                                                 cx[g % NCX]));
+            };
             const float* tB;
             const float* tC;
             if constexpr (Cfg::CONVERT_BC) {
@@ -387,6 +399,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             constexpr int GT = T / LPC;                         // step groups in the chunk
             constexpr int G = GT > 16 ? 16 : GT;                // groups per sub-block (register budget)
             static_assert(GT % G == 0, "chunk must be whole sub-blocks");
+            static_assert(G % NCX == 0, "sub-blocks start on a swizzle row class");
     #pragma unroll 1
             for (int g0 = 0; g0 < GT; g0 += G) {
                 // Phase 1: Δ and Δ·u of the steps this lane prepares (step g·LPC + j of each group;
@@ -394,10 +407,9 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                 float dd[G], du[G];
     #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const int r = (g0 + g) * LPC + j;
-                    const float x = softplus(to_f32<TIO>(td[r * CPW + c]) + bias_w);
+                    const float x = softplus(at(td, g0, g) + bias_w);
                     dd[g] = x;
-                    du[g] = x * to_f32<TIO>(tu[r * CPW + c]);
+                    du[g] = x * at(tu, g0, g);
                 }
                 if (!whole) {
     #pragma unroll
@@ -475,17 +487,15 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                     if (has_z && nst == G) {
     #pragma unroll
                         for (int g = 0; g < G; ++g) {
-                            const int r = (g0 + g) * LPC + j;
-                            const float v = fmaf(D_w, to_f32<TIO>(tu[r * CPW + c]), yv[g]) * silu(to_f32<TIO>(tz[r * CPW + c]));
+                            const float v = fmaf(D_w, at(tu, g0, g), yv[g]) * silu(at(tz, g0, g));
                             *reinterpret_cast<TIO*>(yrow + g * LPC * ystride) = from_f32<TIO>(v);
                         }
                     } else {
     #pragma unroll
                         for (int g = 0; g < G; ++g) {
                             if (g < nst) {
-                                const int r = (g0 + g) * LPC + j;
-                                float v = fmaf(D_w, to_f32<TIO>(tu[r * CPW + c]), yv[g]);
-                                if (has_z) v *= silu(to_f32<TIO>(tz[r * CPW + c]));
+                                float v = fmaf(D_w, at(tu, g0, g), yv[g]);
+                                if (has_z) v *= silu(at(tz, g0, g));
                                 *reinterpret_cast<TIO*>(yrow + g * LPC * ystride) = from_f32<TIO>(v);
                             }
                         }
