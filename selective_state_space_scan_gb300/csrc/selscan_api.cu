@@ -664,8 +664,11 @@ ss_status ss_step(float* state, const void* x, const void* delta_raw, const floa
     p.batch = static_cast<int>(batch);
     p.Dm = static_cast<int>(Dm);
     p.N = static_cast<int>(N);
+    // vector path: whole state quads, 16-byte aligned state and A_log rows, B/C quads aligned
     const bool vec = (N % 4 == 0) && aligned(state, 16) && aligned(A_log, 16) &&
-                     (s.state_d % 4 == 0 || Dm == 1) && (s.state_b % 4 == 0 || batch == 1);
+                     (s.state_d % 4 == 0 || Dm == 1) && (s.state_b % 4 == 0 || batch == 1) &&
+                     aligned(B, 4 * es) && aligned(C, 4 * es) && (s.B_b % 4 == 0 || batch == 1) &&
+                     (s.C_b % 4 == 0 || batch == 1);
     return cuda_status(launch_step(p, bf16, vec, stream));
 }
 

@@ -397,7 +397,8 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             const int64_t left = L - tbase;                     // steps of this chunk before L
             const bool whole = left >= T;
             constexpr int GT = T / LPC;                         // step groups in the chunk
-            constexpr int G = GT > 16 ? 16 : GT;                // groups per sub-block (register budget)
+            // groups per sub-block (register budget): at most 16, a divisor of GT
+            constexpr int G = GT <= 16 ? GT : GT % 16 == 0 ? 16 : GT % 12 == 0 ? 12 : 8;
             static_assert(GT % G == 0, "chunk must be whole sub-blocks");
             static_assert(G % NCX == 0, "sub-blocks start on a swizzle row class");
     #pragma unroll 1

@@ -4,79 +4,155 @@
 //   h[b,d,n]  <- exp(Δ A_n) h[b,d,n] + Δ x[b,d] B[b,n],    A_n = -exp(A_log[d,n])
 //   y[b,d]     = (Σ_n C[b,n] h[b,d,n] + D[d] x[b,d]) · silu(z[b,d])
 // The state is updated in place.  The step is elementwise over (b,d) and HBM-bound on the
-// state read + write, so the mapping is: LPR lanes per (b,d) row, each lane owning four
-// consecutive states (one 16-byte load and store of h), the partial C·h sums reduced across
-// the row's lanes by shuffles.
+// state read + write (16 states x 8 bytes per row against 16 bytes of x, Δ, z, y), so the
+// kernel is a stream: LPR lanes per (b,d) row, each lane owning four consecutive states (one
+// 16-byte load and store of h), RPT rows per thread with every load of all of them issued
+// before any arithmetic (bytes in flight hide HBM latency), the partial C·h sums reduced
+// across the row's lanes by shuffles.  Block x covers rows of batch row x / blocks_per_b: one
+// 32-bit division per block, none per element.
+// exp(A_log) is taken on the SFU (2^(A_log·log2 e)); its relative error (~1e-7) moves the
+// decay exponent by as much, far below the fp32 tolerance.
 #include "device_common.cuh"
 #include "fwd_params.h"
 #include "internal.h"
 
 namespace selscan {
 
-template <typename TIO, int LPR, bool VEC>
-__global__ void __launch_bounds__(256) ss_step_kernel(const StepParams p) {
-    const int64_t gt = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t row = gt / LPR;
-    const int qd = static_cast<int>(gt % LPR);
-    const int64_t rows = static_cast<int64_t>(p.batch) * p.Dm;
-    const bool row_ok = row < rows;
-    const int64_t b = row_ok ? row / p.Dm : 0;
-    const int64_t d = row_ok ? row % p.Dm : 0;
+template <typename TIO> struct Vec4;
+template <> struct Vec4<float> {
+    using T = float4;
+    static __device__ __forceinline__ float4 get(const T& v) { return v; }
+};
+template <> struct Vec4<__nv_bfloat16> {
+    using T = uint2;   // four bf16
+    static __device__ __forceinline__ float4 get(const T& v) {
+        const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+        const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+        return make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+};
 
-    float partial = 0.f, xv = 0.f, zv = 0.f;
-    if (row_ok) {
-        const TIO* x = static_cast<const TIO*>(p.x);
-        const TIO* dr = static_cast<const TIO*>(p.delta);
-        xv = to_f32<TIO>(x[b * p.x_b + d]);
-        const float bias = p.bias ? p.bias[d] : 0.f;
-        const float dlt = softplus(to_f32<TIO>(dr[b * p.d_b + d]) + bias);
-        const float dx = dlt * xv;
-        if (p.z) zv = to_f32<TIO>(static_cast<const TIO*>(p.z)[b * p.z_b + d]);
-        float* h = p.state + b * p.s_b + d * p.s_d;
-        const float* al = p.A_log + d * p.N;
-        const TIO* Bm = static_cast<const TIO*>(p.Bm) + b * p.B_b;
-        const TIO* Cm = static_cast<const TIO*>(p.Cm) + b * p.C_b;
-        for (int n0 = qd * 4; n0 < p.N; n0 += LPR * 4) {
-            if (VEC) {
-                float4 hv = *reinterpret_cast<const float4*>(h + n0);
-                const float4 av = *reinterpret_cast<const float4*>(al + n0);
-                float hs[4] = {hv.x, hv.y, hv.z, hv.w};
-                const float as[4] = {av.x, av.y, av.z, av.w};
+// One row's decode update with the state already loaded (VEC path): returns this lane's C·h
+// partial sum and writes the new state back.
+__device__ __forceinline__ float step_quad(float4& hv, const float4& av, const float4& Bv,
+                                           const float4& Cv, float dlt, float dx) {
+    const float k = -dlt * kLog2e;
+    const float h0 = fmaf(ex2(k * ex2(av.x * kLog2e)), hv.x, dx * Bv.x);
+    const float h1 = fmaf(ex2(k * ex2(av.y * kLog2e)), hv.y, dx * Bv.y);
+    const float h2 = fmaf(ex2(k * ex2(av.z * kLog2e)), hv.z, dx * Bv.z);
+    const float h3 = fmaf(ex2(k * ex2(av.w * kLog2e)), hv.w, dx * Bv.w);
+    hv = make_float4(h0, h1, h2, h3);
+    return fmaf(Cv.x, h0, fmaf(Cv.y, h1, fmaf(Cv.z, h2, Cv.w * h3)));
+}
+
+template <typename TIO, int LPR, int RPT, bool VEC>
+__global__ void __launch_bounds__(256) ss_step_kernel(const StepParams p) {
+    constexpr int ROWS_PASS = 256 / LPR;             // rows one pass of the block covers
+    const int blocks_per_b = static_cast<int>((static_cast<int64_t>(p.Dm) + ROWS_PASS * RPT - 1) / (ROWS_PASS * RPT));
+    const int b = static_cast<int>(blockIdx.x) / blocks_per_b;
+    const int blk = static_cast<int>(blockIdx.x) - b * blocks_per_b;
+    const int qd = threadIdx.x % LPR;
+    const int d0 = blk * (ROWS_PASS * RPT) + threadIdx.x / LPR;
+    const TIO* x = static_cast<const TIO*>(p.x) + static_cast<int64_t>(b) * p.x_b;
+    const TIO* dr = static_cast<const TIO*>(p.delta) + static_cast<int64_t>(b) * p.d_b;
+    const TIO* zz = p.z ? static_cast<const TIO*>(p.z) + static_cast<int64_t>(b) * p.z_b : nullptr;
+    const TIO* Bm = static_cast<const TIO*>(p.Bm) + static_cast<int64_t>(b) * p.B_b;
+    const TIO* Cm = static_cast<const TIO*>(p.Cm) + static_cast<int64_t>(b) * p.C_b;
+    float* hb = p.state + static_cast<int64_t>(b) * p.s_b;
+
+    if constexpr (VEC) {
+        // B and C of this batch row, this lane's quad (shared by every row of the block)
+        const int n0 = qd * 4;
+        const bool q_ok = n0 < p.N;
+        float4 Bv = make_float4(0.f, 0.f, 0.f, 0.f), Cv = Bv;
+        if (q_ok) {
+            Bv = Vec4<TIO>::get(*reinterpret_cast<const typename Vec4<TIO>::T*>(Bm + n0));
+            Cv = Vec4<TIO>::get(*reinterpret_cast<const typename Vec4<TIO>::T*>(Cm + n0));
+        }
+        // issue every load of the RPT rows first
+        float4 hv[RPT], av[RPT];
+        float xv[RPT], dv[RPT], zv[RPT];
+        bool ok[RPT];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float A2 = -expf(as[j]) * kLog2e;
-                    hs[j] = fmaf(ex2(dlt * A2), hs[j], dx * to_f32<TIO>(Bm[n0 + j]));
-                    partial = fmaf(to_f32<TIO>(Cm[n0 + j]), hs[j], partial);
-                }
-                *reinterpret_cast<float4*>(h + n0) = make_float4(hs[0], hs[1], hs[2], hs[3]);
-            } else {
-                for (int j = 0; j < 4 && n0 + j < p.N; ++j) {
-                    const int n = n0 + j;
-                    const float A2 = -expf(al[n]) * kLog2e;
-                    const float hn = fmaf(ex2(dlt * A2), h[n], dx * to_f32<TIO>(Bm[n]));
-                    h[n] = hn;
-                    partial = fmaf(to_f32<TIO>(Cm[n]), hn, partial);
+        for (int i = 0; i < RPT; ++i) {
+            const int d = d0 + i * ROWS_PASS;
+            ok[i] = d < p.Dm;
+            hv[i] = av[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            xv[i] = dv[i] = zv[i] = 0.f;
+            if (ok[i]) {
+                xv[i] = to_f32<TIO>(x[d]);
+                dv[i] = to_f32<TIO>(dr[d]) + (p.bias ? p.bias[d] : 0.f);
+                if (zz) zv[i] = to_f32<TIO>(zz[d]);
+                if (q_ok) {
+                    hv[i] = *reinterpret_cast<const float4*>(hb + static_cast<int64_t>(d) * p.s_d + n0);
+                    av[i] = *reinterpret_cast<const float4*>(p.A_log + static_cast<int64_t>(d) * p.N + n0);
                 }
             }
         }
-    }
 #pragma unroll
-    for (int off = 1; off < LPR; off <<= 1) partial += __shfl_xor_sync(0xffffffffu, partial, off);
-    if (row_ok && qd == 0) {
-        float v = fmaf(p.Dv ? p.Dv[d] : 0.f, xv, partial);
-        if (p.z) v *= silu(zv);
-        static_cast<TIO*>(p.y)[b * p.y_b + d] = from_f32<TIO>(v);
+        for (int i = 0; i < RPT; ++i) {
+            const int d = d0 + i * ROWS_PASS;
+            const float dlt = softplus(dv[i]);
+            float partial = 0.f;
+            if (ok[i] && q_ok) {
+                partial = step_quad(hv[i], av[i], Bv, Cv, dlt, dlt * xv[i]);
+                *reinterpret_cast<float4*>(hb + static_cast<int64_t>(d) * p.s_d + n0) = hv[i];
+            }
+#pragma unroll
+            for (int off = 1; off < LPR; off <<= 1) partial += __shfl_xor_sync(0xffffffffu, partial, off);
+            if (ok[i] && qd == 0) {
+                float v = fmaf(p.Dv ? p.Dv[d] : 0.f, xv[i], partial);
+                if (zz) v *= silu(zv[i]);
+                static_cast<TIO*>(p.y)[static_cast<int64_t>(b) * p.y_b + d] = from_f32<TIO>(v);
+            }
+        }
+    } else {
+        // any N, strides or alignment: scalar states
+#pragma unroll 1
+        for (int i = 0; i < RPT; ++i) {
+            const int d = d0 + i * ROWS_PASS;
+            const bool row_ok = d < p.Dm;
+            float partial = 0.f, xv = 0.f, zv = 0.f;
+            if (row_ok) {
+                xv = to_f32<TIO>(x[d]);
+                const float dlt = softplus(to_f32<TIO>(dr[d]) + (p.bias ? p.bias[d] : 0.f));
+                const float dx = dlt * xv;
+                if (zz) zv = to_f32<TIO>(zz[d]);
+                float* h = hb + static_cast<int64_t>(d) * p.s_d;
+                const float* al = p.A_log + static_cast<int64_t>(d) * p.N;
+                for (int n0 = qd * 4; n0 < p.N; n0 += LPR * 4) {
+                    for (int jj = 0; jj < 4 && n0 + jj < p.N; ++jj) {
+                        const int n = n0 + jj;
+                        const float a = ex2(-dlt * kLog2e * ex2(al[n] * kLog2e));
+                        const float hn = fmaf(a, h[n], dx * to_f32<TIO>(Bm[n]));
+                        h[n] = hn;
+                        partial = fmaf(to_f32<TIO>(Cm[n]), hn, partial);
+                    }
+                }
+            }
+#pragma unroll
+            for (int off = 1; off < LPR; off <<= 1) partial += __shfl_xor_sync(0xffffffffu, partial, off);
+            if (row_ok && qd == 0) {
+                float v = fmaf(p.Dv ? p.Dv[d] : 0.f, xv, partial);
+                if (zz) v *= silu(zv);
+                static_cast<TIO*>(p.y)[static_cast<int64_t>(b) * p.y_b + d] = from_f32<TIO>(v);
+            }
+        }
     }
 }
 
 template <typename TIO, int LPR>
 static cudaError_t launch_step_t(const StepParams& p, bool vec, cudaStream_t stream) {
-    const int64_t threads = static_cast<int64_t>(p.batch) * p.Dm * LPR;
-    const int64_t blocks = (threads + 255) / 256;
+    constexpr int RPT = 2;
+    constexpr int rows_block = (256 / LPR) * RPT;
+    const int64_t blocks = (static_cast<int64_t>(p.Dm) + rows_block - 1) / rows_block * p.batch;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
+    const dim3 grid(static_cast<unsigned>(blocks));
     if (vec)
-        ss_step_kernel<TIO, LPR, true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+        ss_step_kernel<TIO, LPR, RPT, true><<<grid, 256, 0, stream>>>(p);
     else
-        ss_step_kernel<TIO, LPR, false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+        ss_step_kernel<TIO, LPR, RPT, false><<<grid, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
