@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--variant", default=None,
                     help="pin the forward kernel as family,q,tma (family 0 channel-lane / 1 segment-lane; "
                          "q warps per CTA 1|2|4 or 0 auto; tma 1|0|-1 auto); default: the library's choice")
+    ap.add_argument("--no-workspace", action="store_true",
+                    help="call the forward pass without a workspace (ss_fwd: one CTA per channel tile); "
+                         "default: with one (ss_fwd_ws: the balanced or the time-split schedule)")
     return ap.parse_args()
 
 
@@ -78,14 +81,30 @@ def decay_ex2_per_step(w) -> int:
     return updates_per_step(w)
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources: a traffic figure measured on other sources is stale."""
+# Sources each timed kernel's code and launch configuration come from: a traffic figure
+# measured on other sources is stale.
+_COMMON_SOURCES = ("device_common.cuh", "fwd_params.h", "internal.h", "fwd_configs.h", "selscan_api.cu")
+KERNEL_SOURCES = {
+    "ss_fwd_lane_kernel": _COMMON_SOURCES + ("ss_fwd_lane.cuh", "fwd_lane_impl.cuh", "fwd_launch_common.cuh",
+                                             "fwd_lane_f32.cu", "fwd_lane_bf16.cu"),
+    "ss_fwd_seg_kernel": _COMMON_SOURCES + ("ss_fwd_seg.cuh", "fwd_seg.cu", "fwd_launch_common.cuh"),
+    "ss_step_kernel": _COMMON_SOURCES + ("ss_step.cu",),
+}
+
+
+def kernel_source_hash(kernel: str = "") -> str:
+    """Hash of the CUDA sources a kernel is built and launched from (all of csrc for "")."""
     import glob
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "selective_state_space_scan_gb300", "csrc")
-    for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
-                    glob.glob(os.path.join(csrc, "*.h"))):
+    base = kernel.split("(")[0]
+    if base in KERNEL_SOURCES:
+        files = [os.path.join(csrc, f) for f in KERNEL_SOURCES[base]]
+    else:
+        files = glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) + \
+            glob.glob(os.path.join(csrc, "*.h"))
+    for f in sorted(set(files)):
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode())
             h.update(fh.read())
@@ -94,13 +113,13 @@ def kernel_source_hash() -> str:
 
 def measured_traffic(workload: str, kernel: str):
     """DRAM bytes (read + write) per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    on the current sources of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f).get(workload)
-    if not rec or rec.get("kernel") != kernel or rec.get("source_hash") != kernel_source_hash():
+    if not rec or rec.get("kernel") != kernel or rec.get("source_hash") != kernel_source_hash(kernel):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -180,7 +199,7 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------- our arm
 
-def make_fwd_call(w, torch, ss, dev):
+def make_fwd_call(w, torch, ss, dev, workspace=False):
     a = w.arrays
     io = w.io
 
@@ -200,7 +219,7 @@ def make_fwd_call(w, torch, ss, dev):
 
     def step():
         ss.ss_fwd(t["u"], t["delta_raw"], t["delta_bias"], t["A_log"], t["B"], t["C"], t["D"], t["z"],
-                  y=y, last_state=last)
+                  y=y, last_state=last, workspace=workspace)
     return step, t, y, last
 
 
@@ -247,7 +266,7 @@ def run_ours(args, w, rank, world, local_rank):
     if decode:
         step, tensors, outs = make_decode_call(w, torch, ss, dev)
     else:
-        step, tensors, y, last = make_fwd_call(w, torch, ss, dev)
+        step, tensors, y, last = make_fwd_call(w, torch, ss, dev, workspace=not args.no_workspace)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -279,19 +298,22 @@ def run_ours(args, w, rank, world, local_rank):
     if err:
         raise RuntimeError(f"device error word {err:#x} after the timed region")
     if decode:
-        kernel = "ss_step_kernel"
+        kernel, launches = "ss_step_kernel", DECODE_LAYERS
     else:
-        namef = ss.lib().ss__fwd_kernel_name
-        namef.restype = ctypes.c_char_p
-        namef.argtypes = [ctypes.c_int64] * 3
-        kernel = namef(w.batch, w.Dm, w.N).decode()
+        plan = ss.lib().ss__fwd_plan
+        plan.restype = ctypes.c_int
+        plan.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int32, ctypes.c_int, ctypes.c_char_p, ctypes.c_int]
+        buf = ctypes.create_string_buffer(128)
+        launches = plan(w.batch, w.L, w.Dm, w.N, ss.SS_BF16 if w.io == "bf16" else ss.SS_F32,
+                        0 if args.no_workspace else 1, buf, 128)
+        kernel = buf.value.decode()
 
     # end-to-end through the public API: pinned host inputs -> device -> ss_fwd -> host output
     e2e = None
     if not args.no_e2e and not decode:
         e2e = run_e2e(args, w, torch, ss, dev, tensors, y, last, barrier)
     return dict(total_ms=total_ms, per_launch_ms=per_launch_ms, clocks=clk.summary(), e2e=e2e,
-                kernel=kernel)
+                kernel=kernel, launches=launches)
 
 
 def run_e2e(args, w, torch, ss, dev, t, y, last, barrier):
@@ -307,7 +329,7 @@ def run_e2e(args, w, torch, ss, dev, t, y, last, barrier):
         for k in keys:
             t[k].copy_(host[k], non_blocking=True)
         ss.ss_fwd(t["u"], t["delta_raw"], t["delta_bias"], t["A_log"], t["B"], t["C"], t["D"], t["z"],
-                  y=y, last_state=last)
+                  y=y, last_state=last, workspace=not args.no_workspace)
         y_host.copy_(y, non_blocking=True)
         last_host.copy_(last, non_blocking=True)
 
@@ -429,7 +451,7 @@ def main():
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config(w, variant=args.variant), "hbm_gbs": alg_bytes(w) / (ms_step / 1e3) / 1e9,
-        "gpu_launches": args.steps * (DECODE_LAYERS if w.name.startswith("decode") else 1),
+        "gpu_launches": args.steps * res["launches"],
         "clocks": res["clocks"], "roofline": roof,
     }
     if res["e2e"] is not None:

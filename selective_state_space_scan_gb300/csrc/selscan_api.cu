@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -503,6 +504,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         pa.grid = static_cast<int>(tiles_total * pa.seg_launch);
         pa.h0 = nullptr;
         pa.last_state = nullptr;
+        pa.z = nullptr;                   // pass A reads neither z nor C
         FwdVariant va = v;
         va.state_only = true;
         cudaError_t e = lane(va, pa);
@@ -581,6 +583,57 @@ size_t ss_fwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N, in
     if (lane_max_grid(v, io_dtype == SS_BF16, &max_grid) != cudaSuccess || max_grid <= 0) return 0;
     const int64_t grid = std::min<int64_t>(tiles, max_grid);
     return balanced_ws_bytes(static_cast<int>(grid), geo.tile_channels, v.ns);
+}
+
+// Internal reporting hook (not part of the public header): the schedule a forward call with
+// (with_ws != 0) or without a workspace of ss_fwd_workspace_size bytes makes for these sizes,
+// assuming TMA-eligible arguments.  Writes its name into `name` (cap bytes) and returns the
+// number of kernel launches per call (0: sizes invalid).
+int ss__fwd_plan(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dtype, int with_ws,
+                 char* name, int cap) {
+    auto put = [&](const char* txt) {
+        if (name && cap > 0) {
+            std::strncpy(name, txt, static_cast<size_t>(cap) - 1);
+            name[cap - 1] = '\0';
+        }
+    };
+    if (batch <= 0 || L <= 0 || Dm <= 0 || N < 1 || N > 16) {
+        put("none");
+        return 0;
+    }
+    FwdVariant v = choose_fwd_variant(batch, Dm, N);
+    const int ff = g_force_family.load(), fs = g_force_nseg.load();
+    if (ff >= 0) v.family = ff;
+    const int fl = g_force_lpc.load() > 0 && g_force_lpc.load() <= v.ns / 4 ? g_force_lpc.load() : 0;
+    if (fl) v.lpc = fl;
+    char buf[96];
+    if (with_ws && fs != 0 && (fs >= 2 || (v.family == kFamSeg && ff < 0))) {
+        FwdVariant vs = v;
+        vs.family = kFamLane;
+        if (!fl) vs.lpc = vs.ns / 4;
+        int max_grid = 0;
+        if (lane_max_grid(vs, io_dtype == SS_BF16, &max_grid) == cudaSuccess && max_grid > 0) {
+            const int64_t tiles = batch * ((Dm + lane_w(vs.lpc, false) - 1) / lane_w(vs.lpc, false));
+            const int64_t nch = (L + kLaneT - 1) / kLaneT;
+            if (nch <= INT32_MAX) {
+                const SplitPlan pl = split_plan(tiles, static_cast<int>(nch), batch * Dm, N, max_grid,
+                                                static_cast<size_t>(-1), fs);
+                if (pl.nseg >= 2) {
+                    std::snprintf(buf, sizeof(buf), "ss_fwd_lane_kernel(lpc=%d,time-split,nseg=%d)", vs.lpc, pl.nseg);
+                    put(buf);
+                    return 3;
+                }
+            }
+        }
+    }
+    if (v.family == kFamSeg) {
+        put("ss_fwd_seg_kernel");
+        return 1;
+    }
+    const bool bal = with_ws && g_force_balanced.load() != 0;
+    std::snprintf(buf, sizeof(buf), "ss_fwd_lane_kernel(lpc=%d%s)", v.lpc, bal ? ",balanced" : "");
+    put(buf);
+    return 1;
 }
 
 ss_status ss_fwd_static(const void* u, const void* delta_raw, const float* delta_bias,

@@ -173,18 +173,21 @@ __device__ void lane_fill_generic(uint8_t* st, const FwdParams& p, int b, int d0
     }
 }
 
-template <class Cfg>
+// WITH_C = false (pass A of the time split) skips the C tile; has_z = false the z tile.
+template <class Cfg, bool WITH_C>
 __device__ __forceinline__ void lane_issue_tma(uint8_t* st, uint64_t* bar, const FwdMaps& m,
                                                bool has_z, int b, int d0, int chunk) {
-    const uint32_t bytes = (has_z ? 3u : 2u) * Cfg::TILE_X + 2u * Cfg::TILE_N;
+    const uint32_t bytes = (has_z ? 3u : 2u) * Cfg::TILE_X + (WITH_C ? 2u : 1u) * Cfg::TILE_N;
     mbar_expect_tx(bar, bytes);
     const int t0 = chunk * Cfg::T;
-    // one [T][W] box per stream (rows of W channels, hardware swizzle), one [T][NS] box for B, C
-    tma_load_3d(st + Cfg::OFF_U, &m.u, bar, d0, t0, b);
-    tma_load_3d(st + Cfg::OFF_D, &m.delta, bar, d0, t0, b);
-    if (has_z) tma_load_3d(st + Cfg::OFF_Z, &m.z, bar, d0, t0, b);
-    tma_load_3d(st + Cfg::OFF_B, &m.B, bar, 0, t0, b);
-    tma_load_3d(st + Cfg::OFF_C, &m.C, bar, 0, t0, b);
+    // one [T][W] box per stream (rows of W channels, hardware swizzle), read once: evict first;
+    // one [T][NS] box for B and C, which every channel tile of the batch row reads: keep in L2
+    const uint64_t once = l2_evict_first(), kept = l2_evict_last();
+    tma_load_3d_hint(st + Cfg::OFF_U, &m.u, bar, d0, t0, b, once);
+    tma_load_3d_hint(st + Cfg::OFF_D, &m.delta, bar, d0, t0, b, once);
+    if (has_z) tma_load_3d_hint(st + Cfg::OFF_Z, &m.z, bar, d0, t0, b, once);
+    tma_load_3d_hint(st + Cfg::OFF_B, &m.B, bar, 0, t0, b, kept);
+    if (WITH_C) tma_load_3d_hint(st + Cfg::OFF_C, &m.C, bar, 0, t0, b, kept);
 }
 
 // Wait (thread 0 only) until another CTA has published with this call's epoch; gives up
@@ -267,7 +270,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     auto issue = [&](int k, uint8_t* st, uint64_t* bar) {
         int tl, chk;
         work.unit(k, nchunks, tl, chk);
-        lane_issue_tma<Cfg>(st, bar, maps, has_z, tl / p.tiles_per_batch,
+        lane_issue_tma<Cfg, !STATE_ONLY>(st, bar, maps, has_z, tl / p.tiles_per_batch,
                             (tl % p.tiles_per_batch) * Cfg::W, chk);
     };
     if (USE_TMA && tid == 0) {
@@ -384,7 +387,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                 const TIO* rc = reinterpret_cast<const TIO*>(st + Cfg::OFF_C);
                 for (int i = tid; i < T * NS; i += Cfg::THREADS) {
                     bcf[i] = to_f32<TIO>(rb[i]);
-                    bcf[T * NS + i] = to_f32<TIO>(rc[i]);
+                    if constexpr (!STATE_ONLY) bcf[T * NS + i] = to_f32<TIO>(rc[i]);
                 }
                 __syncthreads();
                 tB = bcf;
@@ -401,83 +404,104 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             constexpr int G = GT <= 16 ? GT : GT % 16 == 0 ? 16 : GT % 12 == 0 ? 12 : 8;
             static_assert(GT % G == 0, "chunk must be whole sub-blocks");
             static_assert(G % NCX == 0, "sub-blocks start on a swizzle row class");
-    #pragma unroll 1
+#pragma unroll 1
             for (int g0 = 0; g0 < GT; g0 += G) {
                 // Phase 1: Δ and Δ·u of the steps this lane prepares (step g·LPC + j of each group;
                 // zero past L, i.e. identity pairs).  G independent softplus chains.
                 float dd[G], du[G];
-    #pragma unroll
+#pragma unroll
                 for (int g = 0; g < G; ++g) {
                     const float x = softplus(at(td, g0, g) + bias_w);
                     dd[g] = x;
                     du[g] = x * at(tu, g0, g);
                 }
                 if (!whole) {
-    #pragma unroll
+#pragma unroll
                     for (int g = 0; g < G; ++g)
                         if ((g0 + g) * LPC + j >= left) dd[g] = du[g] = 0.f;
                 }
                 if constexpr (STATE_ONLY) {
-    #pragma unroll
+#pragma unroll
                     for (int g = 0; g < G; ++g) dsum += dd[g];
                 }
                 // Phase 2: the sequential fold.  Step g·LPC + k takes its Δ, Δ·u from lane (c, k);
                 // the C·h partial sums of the channel's LPC lanes are reduce-scattered so that lane
                 // (c, j) ends with the sum of step g·LPC + j.
                 float yv[G];
-    #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float dk[LPC], uk[LPC];
-    #pragma unroll
-                    for (int kk = 0; kk < LPC; ++kk) {
-                        dk[kk] = LPC == 1 ? dd[g] : __shfl_sync(0xffffffffu, dd[g], kk * CPW + c);
-                        uk[kk] = LPC == 1 ? du[g] : __shfl_sync(0xffffffffu, du[g], kk * CPW + c);
-                    }
-                    float yp[LPC];
-    #pragma unroll
-                    for (int kk = 0; kk < LPC; ++kk) {
-                        const float2 dl2 = make_float2(dk[kk], dk[kk]), du2 = make_float2(uk[kk], uk[kk]);
-                        const int row = (g0 + g) * LPC + kk;
-                        float2 acc = make_float2(0.f, 0.f);
-    #pragma unroll
-                        for (int qq = 0; qq < QPL; ++qq) {
-                            // B and C are loaded together, ahead of the decay (their latency overlaps it)
-                            const float4 B4 = *reinterpret_cast<const float4*>(tB + row * NS + n0 + 4 * qq);
-                            float4 C4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if constexpr (!STATE_ONLY)
-                                C4 = *reinterpret_cast<const float4*>(tC + row * NS + n0 + 4 * qq);
-                            const float2 a01 = ex2x2(mul2(dl2, A2[qq][0]));
-                            const float2 a23 = ex2x2(mul2(dl2, A2[qq][1]));
-                            h[qq][0] = fma2(a01, h[qq][0], mul2(du2, make_float2(B4.x, B4.y)));
-                            h[qq][1] = fma2(a23, h[qq][1], mul2(du2, make_float2(B4.z, B4.w)));
-                            if constexpr (!STATE_ONLY) {
-                                acc = fma2(make_float2(C4.x, C4.y), h[qq][0], acc);
-                                acc = fma2(make_float2(C4.z, C4.w), h[qq][1], acc);
+                {
+                    // The decays a = 2^(Δ·A') and inputs b = Δu·B of group g + 1 are formed (shuffle,
+                    // B load, SFU) before group g's recurrence runs, so their latency overlaps it.
+                    float2 an[LPC][QPL][2], bn[LPC][QPL][2];
+                    auto prep = [&](int g, float2 (&a)[LPC][QPL][2], float2 (&bb)[LPC][QPL][2]) {
+#pragma unroll
+                        for (int kk = 0; kk < LPC; ++kk) {
+                            const float dk = LPC == 1 ? dd[g] : __shfl_sync(0xffffffffu, dd[g], kk * CPW + c);
+                            const float uk = LPC == 1 ? du[g] : __shfl_sync(0xffffffffu, du[g], kk * CPW + c);
+                            const float2 dl2 = make_float2(dk, dk), du2 = make_float2(uk, uk);
+                            const int row = (g0 + g) * LPC + kk;
+#pragma unroll
+                            for (int qq = 0; qq < QPL; ++qq) {
+                                const float4 B4 = *reinterpret_cast<const float4*>(tB + row * NS + n0 + 4 * qq);
+                                a[kk][qq][0] = ex2x2(mul2(dl2, A2[qq][0]));
+                                a[kk][qq][1] = ex2x2(mul2(dl2, A2[qq][1]));
+                                bb[kk][qq][0] = mul2(du2, make_float2(B4.x, B4.y));
+                                bb[kk][qq][1] = mul2(du2, make_float2(B4.z, B4.w));
                             }
                         }
-                        yp[kk] = acc.x + acc.y;
-                    }
-                    if constexpr (STATE_ONLY) {
-                        (void)yp;
-                    } else if constexpr (LPC == 1) {
-                        yv[g] = yp[0];
-                    } else if constexpr (LPC == 2) {
-                        const bool hi = j & 1;
-                        const float send = hi ? yp[0] : yp[1];
-                        const float keep = hi ? yp[1] : yp[0];
-                        yv[g] = keep + __shfl_xor_sync(0xffffffffu, send, CPW);
-                    } else {
-                        // butterfly reduce-scatter over the four slices (lanes c + CPW·s): first
-                        // across slice bit 1 (each side keeps two steps), then across bit 0.  Only
-                        // shuffles, no shared-memory round trip or warp barrier, so the next
-                        // group's loads are free to start early.
-                        const bool b1 = (j & 2) != 0, b0 = (j & 1) != 0;
-                        const float s0 = b1 ? yp[0] : yp[2], s1 = b1 ? yp[1] : yp[3];
-                        const float k0 = b1 ? yp[2] : yp[0], k1 = b1 ? yp[3] : yp[1];
-                        const float t0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 2 * CPW);   // step 2·b1
-                        const float t1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 2 * CPW);   // step 2·b1 + 1
-                        const float sd = b0 ? t0 : t1, kp = b0 ? t1 : t0;
-                        yv[g] = kp + __shfl_xor_sync(0xffffffffu, sd, CPW);                 // step j
+                    };
+                    prep(0, an, bn);
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        float2 ac[LPC][QPL][2], bc[LPC][QPL][2];
+#pragma unroll
+                        for (int kk = 0; kk < LPC; ++kk)
+#pragma unroll
+                            for (int qq = 0; qq < QPL; ++qq) {
+                                ac[kk][qq][0] = an[kk][qq][0]; ac[kk][qq][1] = an[kk][qq][1];
+                                bc[kk][qq][0] = bn[kk][qq][0]; bc[kk][qq][1] = bn[kk][qq][1];
+                            }
+                        if (g + 1 < G) prep(g + 1, an, bn);
+                        float yp[LPC];
+#pragma unroll
+                        for (int kk = 0; kk < LPC; ++kk) {
+                            const int row = (g0 + g) * LPC + kk;
+                            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int qq = 0; qq < QPL; ++qq) {
+                                float4 C4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                                if constexpr (!STATE_ONLY)
+                                    C4 = *reinterpret_cast<const float4*>(tC + row * NS + n0 + 4 * qq);
+                                h[qq][0] = fma2(ac[kk][qq][0], h[qq][0], bc[kk][qq][0]);
+                                h[qq][1] = fma2(ac[kk][qq][1], h[qq][1], bc[kk][qq][1]);
+                                if constexpr (!STATE_ONLY) {
+                                    acc = fma2(make_float2(C4.x, C4.y), h[qq][0], acc);
+                                    acc = fma2(make_float2(C4.z, C4.w), h[qq][1], acc);
+                                }
+                            }
+                            yp[kk] = acc.x + acc.y;
+                        }
+                        if constexpr (STATE_ONLY) {
+                            (void)yp;
+                        } else if constexpr (LPC == 1) {
+                            yv[g] = yp[0];
+                        } else if constexpr (LPC == 2) {
+                            const bool hi = j & 1;
+                            const float send = hi ? yp[0] : yp[1];
+                            const float keep = hi ? yp[1] : yp[0];
+                            yv[g] = keep + __shfl_xor_sync(0xffffffffu, send, CPW);
+                        } else {
+                            // butterfly reduce-scatter over the four slices (lanes c + CPW·s): first
+                            // across slice bit 1 (each side keeps two steps), then across bit 0.  Only
+                            // shuffles, no shared-memory round trip or warp barrier, so the next
+                            // group's loads are free to start early.
+                            const bool b1 = (j & 2) != 0, b0 = (j & 1) != 0;
+                            const float s0 = b1 ? yp[0] : yp[2], s1 = b1 ? yp[1] : yp[3];
+                            const float k0 = b1 ? yp[2] : yp[0], k1 = b1 ? yp[3] : yp[1];
+                            const float t0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 2 * CPW);
+                            const float t1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 2 * CPW);
+                            const float sd = b0 ? t0 : t1, kp = b0 ? t1 : t0;
+                            yv[g] = kp + __shfl_xor_sync(0xffffffffu, sd, CPW);
+                        }
                     }
                 }
                 // Phase 3: D skip, z gate, store (G independent chains).
@@ -486,13 +510,13 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                     const int64_t rem = left - g0 * LPC - j;          // steps of this lane's column before L
                     const int nst = whole ? G : (rem <= 0 ? 0 : rem >= int64_t(G) * LPC ? G : static_cast<int>((rem + LPC - 1) / LPC));
                     if (has_z && nst == G) {
-    #pragma unroll
+#pragma unroll
                         for (int g = 0; g < G; ++g) {
                             const float v = fmaf(D_w, at(tu, g0, g), yv[g]) * silu(at(tz, g0, g));
                             *reinterpret_cast<TIO*>(yrow + g * LPC * ystride) = from_f32<TIO>(v);
                         }
                     } else {
-    #pragma unroll
+#pragma unroll
                         for (int g = 0; g < G; ++g) {
                             if (g < nst) {
                                 float v = fmaf(D_w, at(tu, g0, g), yv[g]);
