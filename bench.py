@@ -44,9 +44,9 @@ def parse():
     ap.add_argument("--variant", default=None,
                     help="pin the forward kernel as family,q,tma (family 0 channel-lane / 1 segment-lane; "
                          "q warps per CTA 1|2|4 or 0 auto; tma 1|0|-1 auto); default: the library's choice")
-    ap.add_argument("--no-workspace", action="store_true",
-                    help="call the forward pass without a workspace (ss_fwd: one CTA per channel tile); "
-                         "default: with one (ss_fwd_ws: the balanced or the time-split schedule)")
+    ap.add_argument("--workspace", action="store_true",
+                    help="call the forward pass with a workspace (ss_fwd_ws: the balanced or the time-split "
+                         "schedule); default: ss_fwd, one CTA per channel tile")
     return ap.parse_args()
 
 
@@ -86,7 +86,7 @@ def decay_ex2_per_step(w) -> int:
 _COMMON_SOURCES = ("device_common.cuh", "fwd_params.h", "internal.h", "fwd_configs.h", "selscan_api.cu")
 KERNEL_SOURCES = {
     "ss_fwd_lane_kernel": _COMMON_SOURCES + ("ss_fwd_lane.cuh", "fwd_lane_impl.cuh", "fwd_launch_common.cuh",
-                                             "fwd_lane_f32.cu", "fwd_lane_bf16.cu"),
+                                             "fwd_lane_f32.cu", "fwd_lane_bf16.cu", "ss_fwd_carry.cu"),
     "ss_fwd_seg_kernel": _COMMON_SOURCES + ("ss_fwd_seg.cuh", "fwd_seg.cu", "fwd_launch_common.cuh"),
     "ss_step_kernel": _COMMON_SOURCES + ("ss_step.cu",),
 }
@@ -266,7 +266,7 @@ def run_ours(args, w, rank, world, local_rank):
     if decode:
         step, tensors, outs = make_decode_call(w, torch, ss, dev)
     else:
-        step, tensors, y, last = make_fwd_call(w, torch, ss, dev, workspace=not args.no_workspace)
+        step, tensors, y, last = make_fwd_call(w, torch, ss, dev, workspace=args.workspace)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -305,7 +305,7 @@ def run_ours(args, w, rank, world, local_rank):
         plan.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int32, ctypes.c_int, ctypes.c_char_p, ctypes.c_int]
         buf = ctypes.create_string_buffer(128)
         launches = plan(w.batch, w.L, w.Dm, w.N, ss.SS_BF16 if w.io == "bf16" else ss.SS_F32,
-                        0 if args.no_workspace else 1, buf, 128)
+                        1 if args.workspace else 0, buf, 128)
         kernel = buf.value.decode()
 
     # end-to-end through the public API: pinned host inputs -> device -> ss_fwd -> host output
@@ -329,7 +329,7 @@ def run_e2e(args, w, torch, ss, dev, t, y, last, barrier):
         for k in keys:
             t[k].copy_(host[k], non_blocking=True)
         ss.ss_fwd(t["u"], t["delta_raw"], t["delta_bias"], t["A_log"], t["B"], t["C"], t["D"], t["z"],
-                  y=y, last_state=last, workspace=not args.no_workspace)
+                  y=y, last_state=last, workspace=args.workspace)
         y_host.copy_(y, non_blocking=True)
         last_host.copy_(last, non_blocking=True)
 
