@@ -36,6 +36,8 @@ def _configure(lib):
     lib.oracle_ss_fwd_chunked.restype = ctypes.c_int
     lib.oracle_ss_step.argtypes = [f64p] + [f32p] * 8 + [f64p, f64p, i64, i64, i64]
     lib.oracle_ss_step.restype = ctypes.c_int
+    lib.oracle_conv1d.argtypes = [f32p, f32p, f32p, f64p, f64p, f64p, i64, i64, i64, i64, ctypes.c_int]
+    lib.oracle_conv1d.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
     return lib
@@ -170,3 +172,31 @@ def ss_step(state, x, delta_raw, delta_bias, A_log, B, C, D, z):
     if st != 0:
         raise RuntimeError(f"oracle_ss_step failed with status {st}")
     return y, st64, mag
+
+
+def conv1d(x, w, bias=None, window=None, act=True):
+    """Causal depthwise conv1d in fp64.  x [batch, L, Dm] (float32 values); w [Dm, K];
+    bias [Dm] or None; window [batch, Dm, K-1] (the samples before t = 0, oldest first; None:
+    zeros); act: apply silu.  Returns (out [batch, L, Dm], window_out [batch, Dm, K-1])."""
+    x = _f32(x, name="x")
+    if x.ndim != 3:
+        raise ValueError("x must be [batch, L, Dm]")
+    batch, L, Dm = x.shape
+    w = _f32(w, name="w")
+    if w.ndim != 2 or w.shape[0] != Dm:
+        raise ValueError(f"w must be [Dm, K], got {w.shape}")
+    K = w.shape[1]
+    bias = _f32(bias, (Dm,), "bias")
+    win = None
+    if window is not None:
+        win = np.ascontiguousarray(np.asarray(window, dtype=np.float64))
+        if win.shape != (batch, Dm, K - 1):
+            raise ValueError(f"window: expected shape {(batch, Dm, K - 1)}, got {win.shape}")
+    out = np.empty((batch, L, Dm), np.float64)
+    wout = np.empty((batch, Dm, K - 1), np.float64)
+    st = _load().oracle_conv1d(_ptr(x, ctypes.c_float), _ptr(w, ctypes.c_float), _ptr(bias, ctypes.c_float),
+                               _ptr(win, ctypes.c_double), _ptr(out, ctypes.c_double), _ptr(wout, ctypes.c_double),
+                               batch, L, Dm, K, int(bool(act)))
+    if st != 0:
+        raise RuntimeError(f"oracle_conv1d failed with status {st}")
+    return out, wout

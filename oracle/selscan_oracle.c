@@ -230,6 +230,49 @@ int oracle_ss_step(double* state, const float* x, const float* delta_raw,
     return ORACLE_OK;
 }
 
+/*
+ * Causal depthwise convolution over the sequence, the stage before the scan in a Mamba block
+ * ([M] "MambaBlock = in_proj -> conv1d -> SiLU -> ..."; [S] MetalCausalConv1d: depthwise,
+ * kernel 4, three zero samples on the causal left edge, output length L), with the sliding
+ * window that [M] "O(L) インクリメンタルデコード" carries across calls:
+ *   pre[b,t,d] = bias[d] + sum_{k=0}^{K-1} w[d,k] * e[t + k],   e = window ++ x[b,:,d]
+ *   out[b,t,d] = silu(pre) when act != 0, else pre
+ * The window win_in[b,d,0..K-2] holds the K-1 samples before t = 0, oldest first (NULL: zeros,
+ * i.e. the zero left padding).  win_out[b,d,:] receives the last K-1 samples of e, the window
+ * a following call continues from.  Layouts: x [batch, L, Dm]; w [Dm, K]; bias [Dm] or NULL;
+ * windows [batch, Dm, K-1]; out [batch, L, Dm].  Arithmetic in double.
+ */
+int oracle_conv1d(const float* x, const float* w, const float* bias, const double* win_in,
+                  double* out, double* win_out, int64_t batch, int64_t L, int64_t Dm, int64_t K, int act)
+{
+    if (batch < 0 || L < 0 || Dm < 0 || K < 1) return ORACLE_EINVAL;
+    if ((L > 0 && (!x || !out)) || !w) return ORACLE_EINVAL;
+    int status = ORACLE_OK;
+
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t row = 0; row < batch * Dm; ++row) {
+        const int64_t b = row / Dm, d = row % Dm;
+        double* e = (double*)malloc((size_t)(L + K - 1) * sizeof(double));
+        if (!e) {
+#pragma omp atomic write
+            status = ORACLE_ENOMEM;
+            continue;
+        }
+        for (int64_t k = 0; k < K - 1; ++k) e[k] = win_in ? win_in[row * (K - 1) + k] : 0.0;
+        for (int64_t t = 0; t < L; ++t) e[K - 1 + t] = (double)x[(b * L + t) * Dm + d];
+        const double bd = bias ? (double)bias[d] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            double acc = bd;
+            for (int64_t k = 0; k < K; ++k) acc += (double)w[d * K + k] * e[t + k];
+            out[(b * L + t) * Dm + d] = act ? oracle_silu(acc) : acc;
+        }
+        if (win_out)
+            for (int64_t k = 0; k < K - 1; ++k) win_out[row * (K - 1) + k] = e[L + k];
+        free(e);
+    }
+    return status;
+}
+
 /* Threads the OpenMP runtime will use (1 when built without OpenMP). */
 int oracle_num_threads(void)
 {

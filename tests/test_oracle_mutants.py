@@ -45,6 +45,18 @@ MUTANTS = [
     ("h0_scaled", "for (int64_t n = 0; n < N; ++n) h[n] = h0[row * N + n];",
      "for (int64_t n = 0; n < N; ++n) h[n] = 0.5 * h0[row * N + n];"),
     ("h0_not_in_chunked_carry", "double carry = h0 ? h0[row * N + n] : 0.0;", "double carry = 0.0;"),
+    ("conv_kernel_flipped", "for (int64_t k = 0; k < K; ++k) acc += (double)w[d * K + k] * e[t + k];",
+     "for (int64_t k = 0; k < K; ++k) acc += (double)w[d * K + (K - 1 - k)] * e[t + k];"),
+    ("conv_window_off_by_one", "for (int64_t k = 0; k < K; ++k) acc += (double)w[d * K + k] * e[t + k];",
+     "for (int64_t k = 0; k < K; ++k) acc += (double)w[d * K + k] * (t + k + 1 < L + K - 1 ? e[t + k + 1] : 0.0);"),
+    ("conv_window_ignored", "for (int64_t k = 0; k < K - 1; ++k) e[k] = win_in ? win_in[row * (K - 1) + k] : 0.0;",
+     "for (int64_t k = 0; k < K - 1; ++k) e[k] = 0.0 * (win_in ? win_in[row * (K - 1) + k] : 0.0);"),
+    ("conv_bias_dropped", "const double bd = bias ? (double)bias[d] : 0.0;",
+     "const double bd = bias ? 0.0 * (double)bias[d] : 0.0;"),
+    ("conv_act_before_bias", "out[(b * L + t) * Dm + d] = act ? oracle_silu(acc) : acc;",
+     "out[(b * L + t) * Dm + d] = act ? oracle_silu(acc - bd) + bd : acc;"),
+    ("conv_window_out_stale", "for (int64_t k = 0; k < K - 1; ++k) win_out[row * (K - 1) + k] = e[L + k];",
+     "for (int64_t k = 0; k < K - 1; ++k) win_out[row * (K - 1) + k] = e[k];"),
     ("step_bias_dropped",
      "oracle_softplus((double)delta_raw[row] + (delta_bias ? (double)delta_bias[d] : 0.0))",
      "oracle_softplus((double)delta_raw[row])"),
@@ -62,6 +74,7 @@ def _load_by_path(name, path, search=None):
 @pytest.fixture(scope="module")
 def harness():
     pins = _load_by_path("_oracle_pins_for_mutants", os.path.join(ROOT, "tests", "test_oracle_pins.py"))
+    conv = _load_by_path("_oracle_conv_pins_for_mutants", os.path.join(ROOT, "tests", "test_oracle_conv1d.py"))
     mod = _load_by_path("_oracle_mutant_pkg", os.path.join(ROOT, "oracle", "__init__.py"),
                         [os.path.join(ROOT, "oracle")])
     battery = [
@@ -83,6 +96,13 @@ def harness():
         lambda m: pins.test_h0_split_composition(m, 17),
         pins.test_h0_chunked_equals_sequential,
         pins.test_h0_decode_iterated_equals_forward,
+        conv.test_conv1d_matches_numpy_correlate,
+        conv.test_conv1d_impulse_response,
+        conv.test_conv1d_constant_input_and_left_edge,
+        lambda m: conv.test_conv1d_split_composition(m, 11),
+        lambda m: conv.test_conv1d_split_composition(m, 2),
+        conv.test_conv1d_window_shift_for_short_calls,
+        conv.test_conv1d_silu,
     ]
     return mod, battery
 
