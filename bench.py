@@ -37,7 +37,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="mamba130m",
-                    choices=["mamba130m", "long32k", "mamba2p8b_bf16", "decode1p4b", "tiny"])
+                    choices=["mamba130m", "long32k", "mamba2p8b_bf16", "decode1p4b", "tiny", "conv1d_130m"],
+                    help="conv1d_130m times the causal conv1d + SiLU on the 130m layer's conv input "
+                         "(its own metric, outputs/s)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -382,12 +384,71 @@ def workload_config(w, extra=None, variant=None):
     return c
 
 
+def bench_conv1d(args, local_rank):
+    """The causal conv1d + SiLU (ss_conv1d) on the conv input of the 130m-shaped layer (batch 8,
+    L 2048, Dm 1536, fp32), window in and out: one launch per step."""
+    import torch
+    import selective_state_space_scan_gb300 as ss
+    from selective_state_space_scan_gb300 import synth
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    batch, L, Dm = 8, 2048, 1536
+    g = synth.rng_for(1, 9)
+    x = torch.from_numpy(g.standard_normal((batch, L, Dm), dtype=np.float32)).to(dev)
+    wgt = torch.from_numpy((0.5 * g.standard_normal((Dm, 4), dtype=np.float32)).astype(np.float32)).to(dev)
+    bias = torch.from_numpy((0.1 * g.standard_normal(Dm, dtype=np.float32)).astype(np.float32)).to(dev)
+    win = torch.zeros((batch, Dm, 3), device=dev)
+    out = torch.empty_like(x)
+
+    def step():
+        ss.ss_conv1d(x, wgt, bias, out=out, window_in=win, window_out=win, silu=True)
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    units = batch * L * Dm
+    alg = 2 * units * 4 + Dm * 5 * 4 + 2 * batch * Dm * 3 * 4
+    hbm_peak, peak_kind = peaks()
+    achieved = alg / (launch_ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "causal conv1d + SiLU outputs/s (B·L·D), 1×GB300", "value": units * args.steps / (total_ms / 1e3),
+        "unit": "outputs/s", "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "conv1d_130m: batch=8 L=2048 Dm=1536 kernel=4 io=f32 silu window",
+                   "l2": "no flush: working set 201 MB > 129 MB L2"},
+        "gpu_launches": args.steps, "clocks": clk.summary(),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": None, "kernel": "ss_conv1d_kernel", "launch_ms": launch_ms,
+                     "alg_bytes_per_launch": alg}}))
+    return 0
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     from selective_state_space_scan_gb300 import synth
+    if args.workload == "conv1d_130m":
+        if args.impl == "reference" or world > 1:
+            if rank == 0:
+                print(json.dumps({"impl": args.impl, "unavailable": "conv1d_130m is measured on one GPU, ours only"}))
+            return 0
+        return bench_conv1d(args, local_rank)
     w = synth.config(args.workload)
 
     if args.impl == "reference":

@@ -180,6 +180,46 @@ ss_status ss_fwd_static(const void* u, const void* delta_raw, const float* delta
                         const void* z, void* y, float* last_state, int64_t batch, int64_t L,
                         int64_t Dm, int64_t N, const ss_fwd_strides* strides, void* stream);
 
+/* Kernel width of the causal convolution (the Mamba blocks of the pages use 4). */
+#define SS_CONV_WIDTH 4
+
+/*
+ * Element strides of the convolution's [batch, L, Dm] tensors (channel stride 1).  NULL means
+ * io_dtype = SS_F32 and both contiguous.
+ */
+typedef struct {
+    int32_t io_dtype;                       /* x and out: SS_F32 or SS_BF16 */
+    int64_t x_b, x_l;                       /* x   [batch, L, Dm] */
+    int64_t out_b, out_l;                   /* out [batch, L, Dm] */
+} ss_conv_strides;
+
+/*
+ * Causal depthwise convolution over the sequence, with optional SiLU: the stage before the
+ * scan in a Mamba block ("mamba-metal: Apple Silicon で Mamba を動かす", MambaBlock = in_proj ->
+ * conv1d -> SiLU -> ...; SpeechLens docs/kernel-optimization.md, MetalCausalConv1d: depthwise,
+ * kernel 4, three zero samples on the causal left edge, output length L), with the sliding
+ * window that the blog's section "O(L) インクリメンタルデコード" carries across calls:
+ *
+ *   out[b,t,d] = act( bias[d] + Σ_{k=0..3} weight[d,k] · e[t + k] ),   e = window_in[b,d,:] ++ x[b,:,d]
+ *   window_out[b,d,:] = the last three samples of e
+ *
+ * act is SiLU when silu != 0, the identity otherwise.  The newest sample meets weight[d,3].
+ *   x            [batch, L, Dm] io_dtype
+ *   weight       [Dm, 4] fp32 contiguous (a [Dm, 1, 4] depthwise Conv1d weight)
+ *   bias         [Dm] fp32 or NULL (= 0)
+ *   out          [batch, L, Dm] io_dtype; must not overlap any input or window
+ *   window_in    [batch, Dm, 3] fp32 contiguous or NULL (= the zero left padding): the three
+ *                samples before t = 0, oldest first
+ *   window_out   [batch, Dm, 3] fp32 contiguous or NULL; may be window_in itself (updated in
+ *                place: chunked prefill and decode, L = 1, keep one window buffer)
+ *   batch <= 65535, L, Dm >= 0; batch == 0 or Dm == 0 is a no-op; L == 0 copies window_in (or
+ *   zeros) to window_out.
+ * Errors as ss_fwd.  Returns SS_OK once the work is enqueued.
+ */
+ss_status ss_conv1d(const void* x, const float* weight, const float* bias, void* out,
+                    const float* window_in, float* window_out, int64_t batch, int64_t L,
+                    int64_t Dm, int32_t silu, const ss_conv_strides* strides, void* stream);
+
 /*
  * Element strides of the decode tensors.  x, delta_raw, z, y are [batch, Dm] with channel
  * stride 1; B, C are [batch, N] with state stride 1; the state is [batch, Dm, N] with

@@ -12,8 +12,8 @@ from typing import Optional
 
 from . import _build
 
-__all__ = ["ss_fwd", "ss_step", "ss_fwd_workspace_size", "SelscanError", "lib", "device_error", "version",
-           "status_string", "SS_F32", "SS_BF16", "FwdStrides", "StepStrides"]
+__all__ = ["ss_fwd", "ss_step", "ss_conv1d", "ss_fwd_workspace_size", "SelscanError", "lib", "device_error",
+           "version", "status_string", "SS_F32", "SS_BF16", "FwdStrides", "StepStrides", "ConvStrides"]
 
 SS_F32, SS_BF16 = 0, 1
 _STATUS = {0: "SS_OK", 1: "SS_ERR_INVALID_ARG", 2: "SS_ERR_UNSUPPORTED", 3: "SS_ERR_MISALIGNED",
@@ -29,6 +29,10 @@ class SelscanError(RuntimeError):
 class FwdStrides(ctypes.Structure):
     _fields_ = [("io_dtype", ctypes.c_int32)] + [(n, ctypes.c_int64) for n in (
         "u_b", "u_l", "delta_b", "delta_l", "z_b", "z_l", "y_b", "y_l", "B_b", "B_l", "C_b", "C_l")]
+
+
+class ConvStrides(ctypes.Structure):
+    _fields_ = [("io_dtype", ctypes.c_int32)] + [(n, ctypes.c_int64) for n in ("x_b", "x_l", "out_b", "out_l")]
 
 
 class StepStrides(ctypes.Structure):
@@ -56,6 +60,8 @@ def lib() -> ctypes.CDLL:
         L.ss_fwd_workspace_size.restype = ctypes.c_size_t
         L.ss_step.argtypes = [vp] * 10 + [i64] * 3 + [ctypes.POINTER(StepStrides), vp]
         L.ss_step.restype = ctypes.c_int
+        L.ss_conv1d.argtypes = [vp] * 6 + [i64] * 3 + [ctypes.c_int32, ctypes.POINTER(ConvStrides), vp]
+        L.ss_conv1d.restype = ctypes.c_int
         L.ss_status_string.argtypes = [ctypes.c_int]
         L.ss_status_string.restype = ctypes.c_char_p
         L.ss_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
@@ -204,3 +210,24 @@ def ss_step(state, x, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None
     if st != 0:
         raise SelscanError(st, "ss_step")
     return y
+
+
+def ss_conv1d(x, weight, bias=None, out=None, window_in=None, window_out=None, silu=True, stream=None):
+    """Causal depthwise conv1d (kernel 4) + optional SiLU through the C ABI.
+
+    x [batch, L, Dm] float32 or bfloat16 (channel stride 1); weight [Dm, 4] float32; bias [Dm];
+    window_in / window_out [batch, Dm, 3] float32 (the samples before t = 0, oldest first; the
+    same tensor updates it in place).  ``out`` is allocated like x when None.  Returns out."""
+    import torch
+    batch, L, Dm = x.shape
+    io = _io_code(x.dtype)
+    if out is None:
+        out = torch.empty((batch, L, Dm), dtype=x.dtype, device=x.device)
+    for name, t in (("x", x), ("out", out)):
+        _check_inner(t, name)
+    s = ConvStrides(io, x.stride(0), x.stride(1), out.stride(0), out.stride(1))
+    st = lib().ss_conv1d(_ptr(x), _ptr(weight), _ptr(bias), _ptr(out), _ptr(window_in), _ptr(window_out),
+                         batch, L, Dm, int(bool(silu)), ctypes.byref(s), _stream_handle(stream))
+    if st != 0:
+        raise SelscanError(st, "ss_conv1d")
+    return out

@@ -180,14 +180,14 @@ __device__ __forceinline__ void lane_issue_tma(uint8_t* st, uint64_t* bar, const
     const uint32_t bytes = (has_z ? 3u : 2u) * Cfg::TILE_X + (WITH_C ? 2u : 1u) * Cfg::TILE_N;
     mbar_expect_tx(bar, bytes);
     const int t0 = chunk * Cfg::T;
-    // one [T][W] box per stream (rows of W channels, hardware swizzle), read once: evict first;
-    // one [T][NS] box for B and C, which every channel tile of the batch row reads: keep in L2
-    const uint64_t once = l2_evict_first(), kept = l2_evict_last();
-    tma_load_3d_hint(st + Cfg::OFF_U, &m.u, bar, d0, t0, b, once);
-    tma_load_3d_hint(st + Cfg::OFF_D, &m.delta, bar, d0, t0, b, once);
-    if (has_z) tma_load_3d_hint(st + Cfg::OFF_Z, &m.z, bar, d0, t0, b, once);
-    tma_load_3d_hint(st + Cfg::OFF_B, &m.B, bar, 0, t0, b, kept);
-    if (WITH_C) tma_load_3d_hint(st + Cfg::OFF_C, &m.C, bar, 0, t0, b, kept);
+    // one [T][W] box per stream (rows of W channels, hardware swizzle), one [T][NS] box for B, C.
+    // (L2 eviction hints were measured: evict-first on the streams re-fetched lines that a
+    // neighbouring tile still needed, evict-last on B/C changed nothing; none are used.)
+    tma_load_3d(st + Cfg::OFF_U, &m.u, bar, d0, t0, b);
+    tma_load_3d(st + Cfg::OFF_D, &m.delta, bar, d0, t0, b);
+    if (has_z) tma_load_3d(st + Cfg::OFF_Z, &m.z, bar, d0, t0, b);
+    tma_load_3d(st + Cfg::OFF_B, &m.B, bar, 0, t0, b);
+    if (WITH_C) tma_load_3d(st + Cfg::OFF_C, &m.C, bar, 0, t0, b);
 }
 
 // Wait (thread 0 only) until another CTA has published with this call's epoch; gives up
