@@ -236,7 +236,12 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int j = lane / CPW;            // state slice of this lane / step within a group
-    const int c = lane % CPW;            // channel within the warp
+    const int c = lane % CPW;            // channel slot within the warp
+    // Channel of this lane within the tile.  fp32: a warp's channels are the 16-byte chunks
+    // w, w + WARPS, w + 2·WARPS, ... of the tile row (4 channels each), so that the LPC rows
+    // one load touches land on different banks of the swizzled tile; bf16 (8 channels per chunk)
+    // is conflict-free with consecutive channels.
+    const int cw = Cfg::ES == 4 ? 4 * (warp + Cfg::WARPS * (c >> 2)) + (c & 3) : warp * CPW + c;
     const int nchunks = p.nchunks;
     const bool has_z = p.z != nullptr;
     const int64_t L = p.L;
@@ -251,7 +256,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     uint32_t cx[NCX];
 #pragma unroll
     for (int q = 0; q < NCX; ++q)
-        cx[q] = swz<Cfg::RB>(static_cast<uint32_t>((q * LPC + j) * Cfg::RB + (warp * CPW + c) * Cfg::ES));
+        cx[q] = swz<Cfg::RB>(static_cast<uint32_t>((q * LPC + j) * Cfg::RB + cw * Cfg::ES));
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -309,7 +314,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             tile = work.t2; c0 = work.c2; cnt = work.n2;      // tail, or a time-split segment
         }
         b = tile / p.tiles_per_batch;
-        d = (tile % p.tiles_per_batch) * Cfg::W + warp * CPW + c;
+        d = (tile % p.tiles_per_batch) * Cfg::W + cw;
         d_ok = d < p.Dm;
         bias_w = (p.bias && d_ok) ? p.bias[d] : 0.f;
         D_w = (p.Dv && d_ok) ? p.Dv[d] : 0.f;
@@ -339,7 +344,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                 if (tid == 0) wait_published(p.ws_flag + blockIdx.x - 1, p.epoch, p.err);
                 __syncthreads();
                 const float* ws = p.ws_state + (static_cast<int64_t>(blockIdx.x - 1) * Cfg::W +
-                                                 warp * CPW + c) * NS + n0;
+                                                 cw) * NS + n0;
 #pragma unroll
                 for (int qq = 0; qq < QPL; ++qq) {
                     const float4 v = __ldcg(reinterpret_cast<const float4*>(ws + 4 * qq));
@@ -574,7 +579,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                 }
             }
         } else if (work.n0 > 0 && piece == 0) {
-            float* dst = p.ws_state + (static_cast<int64_t>(blockIdx.x) * Cfg::W + warp * CPW + c) * NS + n0;
+            float* dst = p.ws_state + (static_cast<int64_t>(blockIdx.x) * Cfg::W + cw) * NS + n0;
 #pragma unroll
             for (int qq = 0; qq < QPL; ++qq)
                 __stcg(reinterpret_cast<float4*>(dst + 4 * qq),
