@@ -36,6 +36,8 @@ def _configure(lib):
     lib.oracle_ss_fwd_chunked.restype = ctypes.c_int
     lib.oracle_ss_step.argtypes = [f64p] + [f32p] * 8 + [f64p, f64p, i64, i64, i64]
     lib.oracle_ss_step.restype = ctypes.c_int
+    lib.oracle_ss_bwd.argtypes = [f32p] * 8 + [f64p, f32p, f64p] + [f64p] * 9 + [i64] * 4
+    lib.oracle_ss_bwd.restype = ctypes.c_int
     lib.oracle_conv1d.argtypes = [f32p, f32p, f32p, f64p, f64p, f64p, i64, i64, i64, i64, ctypes.c_int]
     lib.oracle_conv1d.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
@@ -200,3 +202,29 @@ def conv1d(x, w, bias=None, window=None, act=True):
     if st != 0:
         raise RuntimeError(f"oracle_conv1d failed with status {st}")
     return out, wout
+
+
+def ss_bwd(u, delta_raw, delta_bias, A_log, B, C, D, z, dy, h0=None, dlast=None):
+    """Gradients of the forward scan in fp64 for upstream gradients dy [batch, L, Dm] (of y)
+    and dlast [batch, Dm, N] (of last_state, or None).  Returns a dict with du, ddelta_raw, dz
+    [batch, L, Dm]; dB, dC [batch, L, N]; dA_log [Dm, N]; dD, ddelta_bias [Dm]; dh0 [batch, Dm, N]."""
+    u = _f32(u, name="u")
+    batch, L, Dm = u.shape
+    A_log = _f32(A_log, name="A_log")
+    N = A_log.shape[1]
+    args = [u, _f32(delta_raw, (batch, L, Dm)), _f32(delta_bias, (Dm,)), A_log, _f32(B, (batch, L, N)),
+            _f32(C, (batch, L, N)), _f32(D, (Dm,)), _f32(z, (batch, L, Dm))]
+    h0 = _h0(h0, batch, Dm, N)
+    dy = _f32(dy, (batch, L, Dm), "dy")
+    dl = None if dlast is None else _h0(dlast, batch, Dm, N)
+    out = {k: np.zeros(sh, np.float64) for k, sh in (
+        ("du", (batch, L, Dm)), ("ddelta_raw", (batch, L, Dm)), ("dz", (batch, L, Dm)), ("dB", (batch, L, N)),
+        ("dC", (batch, L, N)), ("dA_log", (Dm, N)), ("dD", (Dm,)), ("ddelta_bias", (Dm,)), ("dh0", (batch, Dm, N)))}
+    st = _load().oracle_ss_bwd(*[_ptr(a, ctypes.c_float) for a in args], _ptr(h0, ctypes.c_double),
+                               _ptr(dy, ctypes.c_float), _ptr(dl, ctypes.c_double),
+                               *[_ptr(out[k], ctypes.c_double) for k in ("du", "ddelta_raw", "dz", "dB", "dC",
+                                                                         "dA_log", "dD", "ddelta_bias", "dh0")],
+                               batch, L, Dm, N)
+    if st != 0:
+        raise RuntimeError(f"oracle_ss_bwd failed with status {st}")
+    return out

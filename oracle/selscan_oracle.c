@@ -231,6 +231,126 @@ int oracle_ss_step(double* state, const float* x, const float* delta_raw,
 }
 
 /*
+ * Gradients of the forward scan (oracle_ss_fwd_rows with h0) for an upstream gradient dy of y
+ * and dlast of last_state.  The pages implement no backward pass; this is the derivative of
+ * the forward definition, written as the reverse (adjoint) recurrence of the same scan:
+ *   g_t = silu(z_t) (1 without z),  yhat_t = sum_n C_t,n h_t,n + D u_t,  dyh_t = dy_t g_t
+ *   dz_t = dy_t yhat_t silu'(z_t),  silu'(z) = s (1 + z (1 - s)),  s = sigmoid(z)
+ *   lam_t,n = C_t,n dyh_t + a_{t+1},n lam_{t+1},n   (t = L-1 .. 0; dlast_n joins at t = L-1)
+ *   dC_t,n += dyh_t h_t,n          dB_t,n += lam_t,n Delta_t u_t      (summed over channels)
+ *   du_t = D dyh_t + sum_n lam_t,n Delta_t B_t,n
+ *   dDelta_t = sum_n lam_t,n (A_n a_t,n h_{t-1},n + B_t,n u_t),  ddelta_raw_t = dDelta_t sigmoid(r_t)
+ *   dA_n += sum_t lam_t,n Delta_t a_t,n h_{t-1},n,  dA_log = dA A,   dD += sum_t dyh_t u_t
+ *   ddelta_bias += sum_t ddelta_raw_t,   dh0_n = a_0,n lam_0,n
+ * with r_t = delta_raw + bias, Delta = softplus(r), A_n = -exp(A_log), a_t,n = exp(Delta_t A_n).
+ * Inputs as oracle_ss_fwd_rows (h0 double, NULL = zeros); dy [batch, L, Dm] float; dlast
+ * [batch, Dm, N] double or NULL.  Outputs (double, all written): du, ddelta_raw, dz
+ * [batch, L, Dm]; dB, dC [batch, L, N]; dA_log [Dm, N]; dD, ddelta_bias [Dm]; dh0 [batch, Dm, N].
+ * Parallel over batch rows (each owns its dB, dC); per-channel sums are combined after.
+ */
+int oracle_ss_bwd(const float* u, const float* delta_raw, const float* delta_bias,
+                  const float* A_log, const float* B, const float* C, const float* D,
+                  const float* z, const double* h0, const float* dy, const double* dlast,
+                  double* du, double* ddelta_raw, double* dz, double* dB, double* dC,
+                  double* dA_log, double* dD, double* ddelta_bias, double* dh0,
+                  int64_t batch, int64_t L, int64_t Dm, int64_t N)
+{
+    if (batch < 0 || L < 0 || Dm < 0 || N < 1) return ORACLE_EINVAL;
+    if (!u || !delta_raw || !A_log || !B || !C || !dy) return ORACLE_EINVAL;
+    if (!du || !ddelta_raw || !dz || !dB || !dC || !dA_log || !dD || !ddelta_bias || !dh0) return ORACLE_EINVAL;
+    /* per-batch-row partial sums of the per-channel gradients */
+    double* pA = (double*)calloc((size_t)(batch > 0 ? batch : 1) * Dm * N, sizeof(double));
+    double* pD = (double*)calloc((size_t)(batch > 0 ? batch : 1) * Dm, sizeof(double));
+    double* pb = (double*)calloc((size_t)(batch > 0 ? batch : 1) * Dm, sizeof(double));
+    if (!pA || !pD || !pb) {
+        free(pA); free(pD); free(pb);
+        return ORACLE_ENOMEM;
+    }
+    for (int64_t i = 0; i < batch * L * N; ++i) dB[i] = dC[i] = 0.0;
+    int status = ORACLE_OK;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t b = 0; b < batch; ++b) {
+        double* hs = (double*)malloc((size_t)(L + 1) * N * sizeof(double));   /* h_{t-1} for t = 0..L */
+        double* A = (double*)malloc((size_t)N * sizeof(double));
+        double* lam = (double*)malloc((size_t)N * sizeof(double));
+        if (!hs || !A || !lam) {
+            free(hs); free(A); free(lam);
+#pragma omp atomic write
+            status = ORACLE_ENOMEM;
+            continue;
+        }
+        for (int64_t d = 0; d < Dm; ++d) {
+            const int64_t row = b * Dm + d;
+            for (int64_t n = 0; n < N; ++n) A[n] = -exp((double)A_log[d * N + n]);
+            const double bias = delta_bias ? (double)delta_bias[d] : 0.0;
+            const double Dd = D ? (double)D[d] : 0.0;
+            /* forward: keep every state (hs row t+1 holds h_t, row 0 holds h_{-1}) */
+            for (int64_t n = 0; n < N; ++n) hs[n] = h0 ? h0[row * N + n] : 0.0;
+            for (int64_t t = 0; t < L; ++t) {
+                const int64_t io = (b * L + t) * Dm + d, ib = (b * L + t) * N;
+                const double delta = oracle_softplus((double)delta_raw[io] + bias);
+                for (int64_t n = 0; n < N; ++n)
+                    hs[(t + 1) * N + n] = exp(delta * A[n]) * hs[t * N + n] + delta * (double)B[ib + n] * (double)u[io];
+            }
+            /* reverse */
+            for (int64_t n = 0; n < N; ++n) lam[n] = dlast ? dlast[row * N + n] : 0.0;   /* a_{t+1} lam_{t+1} */
+            for (int64_t t = L - 1; t >= 0; --t) {
+                const int64_t io = (b * L + t) * Dm + d, ib = (b * L + t) * N;
+                const double ut = (double)u[io];
+                const double r = (double)delta_raw[io] + bias;
+                const double delta = oracle_softplus(r);
+                const double sig_r = 1.0 / (1.0 + exp(-r));
+                double yhat = Dd * ut;
+                for (int64_t n = 0; n < N; ++n) yhat += (double)C[ib + n] * hs[(t + 1) * N + n];
+                double g = 1.0, dg = 0.0;
+                if (z) {
+                    const double zt = (double)z[io], s = 1.0 / (1.0 + exp(-zt));
+                    g = zt * s;
+                    dg = s * (1.0 + zt * (1.0 - s));
+                }
+                const double dyh = (double)dy[io] * g;
+                dz[io] = z ? (double)dy[io] * yhat * dg : 0.0;
+                double dut = Dd * dyh, ddel = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    const double l = (double)C[ib + n] * dyh + lam[n];
+                    const double a = exp(delta * A[n]);
+                    const double hp = hs[t * N + n];
+                    dC[ib + n] += dyh * hs[(t + 1) * N + n];
+                    dB[ib + n] += l * delta * ut;
+                    dut += l * delta * (double)B[ib + n];
+                    ddel += l * (A[n] * a * hp + (double)B[ib + n] * ut);
+                    pA[row * N + n] += l * delta * a * hp;
+                    lam[n] = a * l;
+                }
+                du[io] = dut;
+                ddelta_raw[io] = ddel * sig_r;
+                pD[row] += dyh * ut;
+                pb[row] += ddel * sig_r;
+            }
+            for (int64_t n = 0; n < N; ++n) dh0[row * N + n] = lam[n];
+        }
+        free(hs); free(A); free(lam);
+    }
+    for (int64_t d = 0; d < Dm; ++d) {
+        double sD = 0.0, sb = 0.0;
+        for (int64_t b = 0; b < batch; ++b) {
+            sD += pD[b * Dm + d];
+            sb += pb[b * Dm + d];
+        }
+        dD[d] = sD;
+        ddelta_bias[d] = sb;
+        for (int64_t n = 0; n < N; ++n) {
+            double sA = 0.0;
+            for (int64_t b = 0; b < batch; ++b) sA += pA[(b * Dm + d) * N + n];
+            dA_log[d * N + n] = sA * (-exp((double)A_log[d * N + n]));
+        }
+    }
+    free(pA); free(pD); free(pb);
+    return status;
+}
+
+/*
  * Causal depthwise convolution over the sequence, the stage before the scan in a Mamba block
  * ([M] "MambaBlock = in_proj -> conv1d -> SiLU -> ..."; [S] MetalCausalConv1d: depthwise,
  * kernel 4, three zero samples on the causal left edge, output length L), with the sliding

@@ -57,6 +57,15 @@ MUTANTS = [
      "out[(b * L + t) * Dm + d] = act ? oracle_silu(acc - bd) + bd : acc;"),
     ("conv_window_out_stale", "for (int64_t k = 0; k < K - 1; ++k) win_out[row * (K - 1) + k] = e[L + k];",
      "for (int64_t k = 0; k < K - 1; ++k) win_out[row * (K - 1) + k] = e[k];"),
+    ("bwd_adjoint_without_decay", "lam[n] = a * l;", "lam[n] = l;"),
+    ("bwd_dDelta_decay_sign", "ddel += l * (A[n] * a * hp + (double)B[ib + n] * ut);",
+     "ddel += l * (-A[n] * a * hp + (double)B[ib + n] * ut);"),
+    ("bwd_softplus_derivative_dropped", "ddelta_raw[io] = ddel * sig_r;", "ddelta_raw[io] = ddel;"),
+    ("bwd_du_without_skip", "double dut = Dd * dyh, ddel = 0.0;", "double dut = 0.0 * dyh, ddel = 0.0;"),
+    ("bwd_dz_without_yhat", "dz[io] = z ? (double)dy[io] * yhat * dg : 0.0;", "dz[io] = z ? (double)dy[io] * dg : 0.0;"),
+    ("bwd_dA_log_chain_dropped", "dA_log[d * N + n] = sA * (-exp((double)A_log[d * N + n]));",
+     "dA_log[d * N + n] = sA;"),
+    ("bwd_dC_previous_state", "dC[ib + n] += dyh * hs[(t + 1) * N + n];", "dC[ib + n] += dyh * hs[t * N + n];"),
     ("step_bias_dropped",
      "oracle_softplus((double)delta_raw[row] + (delta_bias ? (double)delta_bias[d] : 0.0))",
      "oracle_softplus((double)delta_raw[row])"),
@@ -75,6 +84,7 @@ def _load_by_path(name, path, search=None):
 def harness():
     pins = _load_by_path("_oracle_pins_for_mutants", os.path.join(ROOT, "tests", "test_oracle_pins.py"))
     conv = _load_by_path("_oracle_conv_pins_for_mutants", os.path.join(ROOT, "tests", "test_oracle_conv1d.py"))
+    bwd = _load_by_path("_oracle_bwd_pins_for_mutants", os.path.join(ROOT, "tests", "test_oracle_bwd.py"))
     mod = _load_by_path("_oracle_mutant_pkg", os.path.join(ROOT, "oracle", "__init__.py"),
                         [os.path.join(ROOT, "oracle")])
     battery = [
@@ -103,6 +113,9 @@ def harness():
         lambda m: conv.test_conv1d_split_composition(m, 2),
         conv.test_conv1d_window_shift_for_short_calls,
         conv.test_conv1d_silu,
+        lambda m: bwd.test_bwd_matches_finite_differences(m, True),
+        lambda m: bwd.test_bwd_matches_finite_differences(m, False),
+        bwd.test_bwd_A_to_zero_closed_form,
     ]
     return mod, battery
 
