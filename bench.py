@@ -37,9 +37,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="mamba130m",
-                    choices=["mamba130m", "long32k", "mamba2p8b_bf16", "decode1p4b", "tiny", "conv1d_130m"],
+                    choices=["mamba130m", "long32k", "mamba2p8b_bf16", "decode1p4b", "tiny", "conv1d_130m",
+                             "bwd_130m"],
                     help="conv1d_130m times the causal conv1d + SiLU on the 130m layer's conv input "
-                         "(its own metric, outputs/s)")
+                         "(its own metric, outputs/s); bwd_130m the backward scan of the 130m layer")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -437,18 +438,72 @@ def bench_conv1d(args, local_rank):
     return 0
 
 
+def bench_bwd(args, local_rank):
+    """The backward scan (ss_bwd) of the 130m-shaped layer (batch 8, L 2048, Dm 1536, N 16,
+    fp32): gradients of every input for a random dy; one launch (plus the zeroing of the sums)
+    per step."""
+    import torch
+    import selective_state_space_scan_gb300 as ss
+    from selective_state_space_scan_gb300 import synth
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = synth.config("mamba130m")
+    a = w.arrays
+    t = {k: (None if v is None else torch.from_numpy(v).to(dev)) for k, v in a.items()}
+    dy = torch.from_numpy(synth.rng_for(1, 12).standard_normal((w.batch, w.L, w.Dm), dtype=np.float32)).to(dev)
+
+    def step():
+        ss.ss_bwd(dy, t["u"], t["delta_raw"], t["delta_bias"], t["A_log"], t["B"], t["C"], t["D"], t["z"])
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    launch_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ev)
+    units = updates_per_step(w)
+    s = w.io_bytes()
+    # must move: read u, delta_raw, z, dy and B, C; write du, ddelta_raw, dz and dB, dC; params
+    alg = w.batch * w.L * (7 * w.Dm * s + 4 * w.N * 4) + w.Dm * (w.N + 2) * 4 * 2
+    hbm_peak, peak_kind = peaks()
+    achieved = alg / (launch_ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "selective-scan backward state-updates/s (B·L·D·N), 1×GB300",
+        "value": units * args.steps / (total_ms / 1e3), "unit": "state-updates/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "bwd_130m: batch=8 L=2048 Dm=1536 N=16 io=f32, all input gradients",
+                   "l2": "no flush: working set > 129 MB L2"},
+        "gpu_launches": args.steps, "clocks": clk.summary(),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": None, "kernel": "ss_bwd_kernel", "launch_ms": launch_ms,
+                     "alg_bytes_per_launch": alg}}))
+    return 0
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     from selective_state_space_scan_gb300 import synth
-    if args.workload == "conv1d_130m":
+    if args.workload in ("conv1d_130m", "bwd_130m"):
         if args.impl == "reference" or world > 1:
             if rank == 0:
-                print(json.dumps({"impl": args.impl, "unavailable": "conv1d_130m is measured on one GPU, ours only"}))
+                print(json.dumps({"impl": args.impl,
+                                  "unavailable": f"{args.workload} is measured on one GPU, ours only"}))
             return 0
-        return bench_conv1d(args, local_rank)
+        return bench_conv1d(args, local_rank) if args.workload == "conv1d_130m" else bench_bwd(args, local_rank)
     w = synth.config(args.workload)
 
     if args.impl == "reference":

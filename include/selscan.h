@@ -180,6 +180,41 @@ ss_status ss_fwd_static(const void* u, const void* delta_raw, const float* delta
                         const void* z, void* y, float* last_state, int64_t batch, int64_t L,
                         int64_t Dm, int64_t N, const ss_fwd_strides* strides, void* stream);
 
+/*
+ * Backward pass: the gradients of ss_fwd_h0's outputs (y and last_state) with respect to every
+ * input, for training.  The pages implement no backward pass ("mamba-metal: Apple Silicon で
+ * Mamba を動かす", section "残り課題", lists the backward kernel for training as still to do); this
+ * is the derivative of the forward definition above, evaluated as the reverse (adjoint) recurrence
+ * of the same scan:
+ *   dŷ_t = dy_t·silu(z_t),  dz_t = dy_t·ŷ_t·silu'(z_t),  λ_t = C_t dŷ_t + exp(Δ_{t+1}A) λ_{t+1}
+ *   (dlast joins at t = L-1); dC_t = Σ_d dŷ_t h_t, dB_t = Σ_d λ_t Δ_t u_t, du_t = D dŷ_t +
+ *   Σ_n λ_t Δ_t B_t, ddelta_raw_t = sigmoid(r_t) Σ_n λ_t (A exp(Δ_t A) h_{t-1} + B_t u_t),
+ *   dA_log = A Σ_{b,t} λ_t Δ_t exp(Δ_t A) h_{t-1}, dD = Σ dŷ_t u_t, ddelta_bias = Σ ddelta_raw,
+ *   dh0 = exp(Δ_0 A) λ_0,  with r = delta_raw + delta_bias.
+ *   Inputs: those of ss_fwd_h0 (same strides struct; h0 NULL = zeros); dy [batch, L, Dm] io_dtype
+ *   contiguous (the gradient of y); dlast [batch, Dm, N] fp32 or NULL (of last_state).
+ *   Outputs (caller-owned, written or zeroed by the call):
+ *     du, ddelta_raw, dz   [batch, L, Dm] io_dtype contiguous (dz NULL when z is NULL)
+ *     dB, dC               [batch, L, N] fp32 contiguous (sums over channels)
+ *     dA_log               [Dm, N] fp32
+ *     dD, ddelta_bias      [Dm] fp32 or NULL (not computed)
+ *     dh0                  [batch, Dm, N] fp32 or NULL
+ *   Outputs must not overlap each other or any input.  The sums (dB, dC, dA_log, dD,
+ *   ddelta_bias) are accumulated with atomic adds, so their rounding varies from run to run.
+ *   workspace          device memory, 256-byte aligned, ss_bwd_workspace_size(...) bytes (the
+ *                      state at every 64-step chunk start); contents need no initialisation.
+ * Errors as ss_fwd.  Returns SS_OK once the work is enqueued.
+ */
+ss_status ss_bwd(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
+                 const void* B, const void* C, const float* D, const void* z, const float* h0,
+                 const void* dy, const float* dlast, void* du, void* ddelta_raw, void* dz,
+                 float* dB, float* dC, float* dA_log, float* dD, float* ddelta_bias, float* dh0,
+                 int64_t batch, int64_t L, int64_t Dm, int64_t N, const ss_fwd_strides* strides,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes ss_bwd needs for these sizes (0: sizes invalid or empty). */
+size_t ss_bwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N);
+
 /* Kernel width of the causal convolution (the Mamba blocks of the pages use 4). */
 #define SS_CONV_WIDTH 4
 

@@ -12,7 +12,7 @@ from typing import Optional
 
 from . import _build
 
-__all__ = ["ss_fwd", "ss_step", "ss_conv1d", "ss_fwd_workspace_size", "SelscanError", "lib", "device_error",
+__all__ = ["ss_fwd", "ss_step", "ss_conv1d", "ss_bwd", "ss_fwd_workspace_size", "SelscanError", "lib", "device_error",
            "version", "status_string", "SS_F32", "SS_BF16", "FwdStrides", "StepStrides", "ConvStrides"]
 
 SS_F32, SS_BF16 = 0, 1
@@ -62,6 +62,10 @@ def lib() -> ctypes.CDLL:
         L.ss_step.restype = ctypes.c_int
         L.ss_conv1d.argtypes = [vp] * 6 + [i64] * 3 + [ctypes.c_int32, ctypes.POINTER(ConvStrides), vp]
         L.ss_conv1d.restype = ctypes.c_int
+        L.ss_bwd.argtypes = [vp] * 20 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp, ctypes.c_size_t, vp]
+        L.ss_bwd.restype = ctypes.c_int
+        L.ss_bwd_workspace_size.argtypes = [i64] * 4
+        L.ss_bwd_workspace_size.restype = ctypes.c_size_t
         L.ss_status_string.argtypes = [ctypes.c_int]
         L.ss_status_string.restype = ctypes.c_char_p
         L.ss_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
@@ -119,12 +123,13 @@ _WORKSPACES = {}
 _WS_SIZES = {}
 
 
-def workspace_for(device, stream_handle, nbytes: int):
+def workspace_for(device, stream_handle, nbytes: int, purpose: str = "fwd"):
     """A zero-filled, 256-byte aligned device buffer of at least nbytes, cached per (device,
-    stream) and grown when needed; calls on one stream are ordered, so they never overlap on
-    the GPU while sharing it."""
+    stream, purpose) and grown when needed; calls on one stream are ordered, so they never
+    overlap on the GPU while sharing it.  The forward schedules' hand-over flags and the
+    backward's checkpoints live in separate buffers (the flags must never see checkpoint bits)."""
     import torch
-    key = (str(device), stream_handle)
+    key = (str(device), stream_handle, purpose)
     ws = _WORKSPACES.get(key)
     if ws is None or ws.numel() < nbytes:
         ws = torch.zeros(max(nbytes, 1), dtype=torch.uint8, device=device)
@@ -231,3 +236,39 @@ def ss_conv1d(x, weight, bias=None, out=None, window_in=None, window_out=None, s
     if st != 0:
         raise SelscanError(st, "ss_conv1d")
     return out
+
+
+def ss_bwd(dy, u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, h0=None, dlast=None, stream=None):
+    """Gradients of ss_fwd (from h0) through the C ABI.  dy [batch, L, Dm] (gradient of y, io
+    dtype); dlast [batch, Dm, N] float32 (of last_state) or None.  Returns a dict: du,
+    ddelta_raw, dz (None without z) [batch, L, Dm] io dtype; dB, dC [batch, L, N], dA_log [Dm, N],
+    dD, ddelta_bias [Dm], dh0 [batch, Dm, N] float32.  The workspace (chunk checkpoints) comes
+    from the per-(device, stream) cache."""
+    import torch
+    batch, L, Dm = u.shape
+    N = A_log.shape[1]
+    io = _io_code(u.dtype)
+    for name, t in (("u", u), ("delta_raw", delta_raw), ("z", z), ("B", B), ("C", C)):
+        _check_inner(t, name)
+    dy = dy.contiguous()
+    f32 = dict(dtype=torch.float32, device=u.device)
+    g = dict(du=torch.empty((batch, L, Dm), dtype=u.dtype, device=u.device),
+             ddelta_raw=torch.empty((batch, L, Dm), dtype=u.dtype, device=u.device),
+             dz=torch.empty((batch, L, Dm), dtype=u.dtype, device=u.device) if z is not None else None,
+             dB=torch.empty((batch, L, N), **f32), dC=torch.empty((batch, L, N), **f32),
+             dA_log=torch.empty((Dm, N), **f32), dD=torch.empty((Dm,), **f32),
+             ddelta_bias=torch.empty((Dm,), **f32), dh0=torch.empty((batch, Dm, N), **f32))
+    s = FwdStrides(io, u.stride(0), u.stride(1), delta_raw.stride(0), delta_raw.stride(1),
+                   z.stride(0) if z is not None else 0, z.stride(1) if z is not None else 0,
+                   0, 0, B.stride(0), B.stride(1), C.stride(0), C.stride(1))
+    sh = _stream_handle(stream)
+    nbytes = int(lib().ss_bwd_workspace_size(batch, L, Dm, N))
+    ws = workspace_for(u.device, sh, nbytes, purpose="bwd") if nbytes else None
+    st = lib().ss_bwd(_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                      _ptr(h0), _ptr(dy), _ptr(dlast), _ptr(g["du"]), _ptr(g["ddelta_raw"]), _ptr(g["dz"]),
+                      _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dA_log"]), _ptr(g["dD"]), _ptr(g["ddelta_bias"]),
+                      _ptr(g["dh0"]), batch, L, Dm, N, ctypes.byref(s), None if ws is None else ws.data_ptr(),
+                      0 if ws is None else ws.numel(), sh)
+    if st != 0:
+        raise SelscanError(st, "ss_bwd")
+    return g

@@ -1,0 +1,479 @@
+// Backward pass of the selective scan: the gradients of ss_fwd's outputs (y, last_state) with
+// respect to every input.  The pages implement no backward pass (the blog below lists the
+// backward kernel for training under "残り課題"); this is the derivative of the forward
+// definition ("mamba-metal: Apple Silicon で Mamba を動かす", section "Selective
+// scan の本質": h_t = Ā_t h_{t-1} + B̄_t u_t, y_t = C_t h_t, with softplus on Δ, the D skip and
+// the z gate of the blog's walkthrough of the official CUDA kernel, section "1チャンク内の処理
+// フロー"), evaluated as the reverse (adjoint) recurrence of the same scan:
+//   dŷ_t = dy_t g_t (g = silu(z)),  dz_t = dy_t ŷ_t silu'(z_t)
+//   λ_t = C_t dŷ_t + a_{t+1} λ_{t+1}          (dlast joins at t = L-1)
+//   dC_t += dŷ_t h_t,  dB_t += λ_t Δ_t u_t    (summed over the channels of a batch row)
+//   du_t = D dŷ_t + Σ_n λ_t Δ_t B_t,   dΔ_t = Σ_n λ_t (A a_t h_{t-1} + B_t u_t),  dr_t = dΔ_t σ(r_t)
+//   dA += λ_t Δ_t a_t h_{t-1} (then · A for A_log),  dD += dŷ_t u_t,  dbias += dr_t,  dh0 = a_0 λ_0
+//
+// Layout: the forward kernel's lanes (a channel's states split over NS/4 lanes of 4 states, a
+// CTA = 32 channels of one batch row).  The reverse recurrence needs h_{t-1} at every step:
+//   pass 1 folds the sequence forward and stores the state at every chunk start (workspace);
+//   pass 2 walks the chunks backwards; inside a chunk it refolds from the checkpoint to get the
+//   state at each sub-chunk start, then for each sub-chunk (last first) refolds its kBS states
+//   into registers and runs the adjoint backwards over them.
+// The per-(step, channel) quantities (Δ, σ(r), dŷ, dy·silu'(z), u) and the chunk's B, C are
+// staged in shared memory; dB, dC (sums over the CTA's channels) are reduced over a warp's
+// channel lanes by shuffles, over the warps with shared atomics, and reach global memory with
+// one atomic per (step, state) per CTA; dA_log, dD and dbias are summed over batch rows with
+// global atomics.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/selscan.h"
+#include "device_common.cuh"
+#include "host_util.h"
+
+namespace selscan {
+namespace {
+
+constexpr int kBT = 64;    // steps per chunk (one checkpoint per chunk)
+constexpr int kBS = 16;    // steps per sub-chunk (their states are held in registers)
+constexpr int kBW = 32;    // channels per CTA
+
+struct BwdParams {
+    const void* u;
+    const void* delta;
+    const void* z;
+    const void* Bm;
+    const void* Cm;
+    const float* bias;
+    const float* A_log;
+    const float* Dv;
+    const float* h0;
+    const void* dy;        // [batch, L, Dm] contiguous
+    const float* dlast;    // [batch, Dm, N] or nullptr
+    void* du;              // [batch, L, Dm] contiguous
+    void* ddelta;
+    void* dz;
+    float* dB;             // [batch, L, N] contiguous (zeroed by the host)
+    float* dC;
+    float* dA_log;         // [Dm, N] (zeroed)
+    float* dD;             // [Dm] or nullptr (zeroed)
+    float* dbias;          // [Dm] or nullptr (zeroed)
+    float* dh0;            // [batch, Dm, N] or nullptr
+    float* ckpt;           // [tiles][nchunks][kBW][NS]
+    int64_t u_b, u_l, d_b, d_l, z_b, z_l, B_b, B_l, C_b, C_l;
+    int batch, L, Dm, N, nchunks, tiles_per_batch;
+};
+
+template <typename TIO, int NS_>
+struct BwdCfg {
+    static constexpr int NS = NS_;
+    static constexpr int LPC = NS / 4;           // lanes per channel, four states each
+    static constexpr int CPW = 32 / LPC;         // channels per warp
+    static constexpr int WARPS = kBW / CPW;
+    static constexpr int THREADS = 32 * WARPS;
+    static constexpr int X = kBT * kBW;          // one [T][W] array (floats)
+    static constexpr int OFF_U = 0, OFF_DEL = X, OFF_SIG = 2 * X, OFF_DYH = 3 * X, OFF_DYG = 4 * X;
+    static constexpr int OFF_B = 5 * X;
+    static constexpr int OFF_C = OFF_B + kBT * NS;
+    static constexpr int OFF_DB = OFF_C + kBT * NS;
+    static constexpr int OFF_DC = OFF_DB + kBT * NS;
+    static constexpr int OFF_HB = OFF_DC + kBT * NS;     // [kBT / kBS][kBW][NS] sub-chunk start states
+    static constexpr int SMEM = (OFF_HB + (kBT / kBS) * kBW * NS) * 4;
+};
+
+__device__ __forceinline__ float sigmoid_f(float x) { return rcp_approx(1.f + ex2(-x * kLog2e)); }
+
+// Stage chunk `chunk` of the tile in shared memory.  full = false (pass 1): u, Δ, B only.
+template <class Cfg, typename TIO>
+__device__ void bwd_fill(float* sm, const BwdParams& p, int b, int d0, int chunk, bool full) {
+    const int64_t t0 = static_cast<int64_t>(chunk) * kBT;
+    const TIO* u = static_cast<const TIO*>(p.u);
+    const TIO* dl = static_cast<const TIO*>(p.delta);
+    const TIO* zz = static_cast<const TIO*>(p.z);
+    const TIO* dy = static_cast<const TIO*>(p.dy);
+    for (int i = threadIdx.x; i < kBT * kBW; i += Cfg::THREADS) {
+        const int r = i / kBW, c = i % kBW;
+        const int64_t t = t0 + r;
+        const int d = d0 + c;
+        float uu = 0.f, del = 0.f, sig = 0.f, dyh = 0.f, dyg = 0.f;
+        if (t < p.L && d < p.Dm) {
+            uu = to_f32<TIO>(u[b * p.u_b + t * p.u_l + d]);
+            const float rr = to_f32<TIO>(dl[b * p.d_b + t * p.d_l + d]) + (p.bias ? p.bias[d] : 0.f);
+            del = softplus(rr);
+            if (full) {
+                sig = sigmoid_f(rr);
+                const float dyv = to_f32<TIO>(dy[(static_cast<int64_t>(b) * p.L + t) * p.Dm + d]);
+                float g = 1.f, dg = 0.f;
+                if (zz) {
+                    const float zv = to_f32<TIO>(zz[b * p.z_b + t * p.z_l + d]);
+                    const float s = sigmoid_f(zv);
+                    g = zv * s;
+                    dg = s * fmaf(zv, 1.f - s, 1.f);
+                }
+                dyh = dyv * g;
+                dyg = dyv * dg;
+            }
+        }
+        sm[Cfg::OFF_U + i] = uu;
+        sm[Cfg::OFF_DEL + i] = del;
+        if (full) {
+            sm[Cfg::OFF_SIG + i] = sig;
+            sm[Cfg::OFF_DYH + i] = dyh;
+            sm[Cfg::OFF_DYG + i] = dyg;
+        }
+    }
+    const TIO* Bm = static_cast<const TIO*>(p.Bm);
+    const TIO* Cm = static_cast<const TIO*>(p.Cm);
+    for (int i = threadIdx.x; i < kBT * Cfg::NS; i += Cfg::THREADS) {
+        const int r = i / Cfg::NS, n = i % Cfg::NS;
+        const int64_t t = t0 + r;
+        const bool in = t < p.L && n < p.N;
+        sm[Cfg::OFF_B + i] = in ? to_f32<TIO>(Bm[b * p.B_b + t * p.B_l + n]) : 0.f;
+        if (full) {
+            sm[Cfg::OFF_C + i] = in ? to_f32<TIO>(Cm[b * p.C_b + t * p.C_l + n]) : 0.f;
+            sm[Cfg::OFF_DB + i] = 0.f;
+            sm[Cfg::OFF_DC + i] = 0.f;
+        }
+    }
+}
+
+// Sum over the LPC lanes of a channel (lanes c + CPW·j), every lane receiving the total.
+template <int CPW>
+__device__ __forceinline__ float channel_sum(float v) {
+#pragma unroll
+    for (int off = CPW; off < 32; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// Sum over the CPW channel lanes of a warp (lanes c + CPW·j, c = lane % CPW) of each of a
+// lane's 8 values v[k] (dB of its 4 states, then dC of them), scattered: three halving rounds
+// over the channel bits 2, 1, 0 leave value k = c & 7 in lane c; wider warps (CPW > 8) finish
+// with plain add rounds, after which the lanes with c < 8 hold the sums.  Returns that value.
+template <int CPW>
+__device__ __forceinline__ float channel_reduce_scatter(const float (&v)[8], int c) {
+    const bool b2 = (c & 4) != 0, b1 = (c & 2) != 0, b0 = (c & 1) != 0;
+    float w4[4], w2[2];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float keep = b2 ? v[4 + k] : v[k], send = b2 ? v[k] : v[4 + k];
+        w4[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const float keep = b1 ? w4[2 + k] : w4[k], send = b1 ? w4[k] : w4[2 + k];
+        w2[k] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    const float keep = b0 ? w2[1] : w2[0], send = b0 ? w2[0] : w2[1];
+    float r = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+#pragma unroll
+    for (int off = 8; off < CPW; off <<= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+    return r;
+}
+
+template <typename TIO, int NS>
+__global__ void __launch_bounds__(BwdCfg<TIO, NS>::THREADS) ss_bwd_kernel(const BwdParams p) {
+    using Cfg = BwdCfg<TIO, NS>;
+    constexpr int CPW = Cfg::CPW;
+    constexpr int NSUB = kBT / kBS;
+    extern __shared__ __align__(16) float sm[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int j = lane / CPW, c = lane % CPW;
+    const int cw = warp * CPW + c;               // channel within the tile
+    const int tile = blockIdx.x;
+    const int b = tile / p.tiles_per_batch;
+    const int d0 = (tile % p.tiles_per_batch) * kBW;
+    const int d = d0 + cw;
+    const bool d_ok = d < p.Dm;
+    const int n0 = j * 4;
+    float An[4], A2[4];                          // A = -exp(A_log) and A·log2(e)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int n = n0 + q;
+        An[q] = (d_ok && n < p.N) ? -expf(p.A_log[static_cast<int64_t>(d) * p.N + n]) : 0.f;
+        A2[q] = An[q] * kLog2e;
+    }
+    const float Dd = (d_ok && p.Dv) ? p.Dv[d] : 0.f;
+    float* ck = p.ckpt + static_cast<int64_t>(tile) * p.nchunks * kBW * NS;
+    const int64_t row = static_cast<int64_t>(b) * p.Dm + d;
+
+    auto fold = [&](float (&h)[4], int r) {      // one step of the forward fold (chunk row r)
+        const float del = sm[Cfg::OFF_DEL + r * kBW + cw];
+        const float du = del * sm[Cfg::OFF_U + r * kBW + cw];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) h[q] = fmaf(ex2(del * A2[q]), h[q], du * sm[Cfg::OFF_B + r * NS + n0 + q]);
+    };
+
+    // ---- pass 1: forward, the state at every chunk start
+    float h[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) h[q] = (p.h0 && d_ok && n0 + q < p.N) ? p.h0[row * p.N + n0 + q] : 0.f;
+    for (int ch = 0; ch < p.nchunks; ++ch) {
+        *reinterpret_cast<float4*>(ck + (static_cast<int64_t>(ch) * kBW + cw) * NS + n0) =
+            make_float4(h[0], h[1], h[2], h[3]);
+        __syncthreads();                         // the previous chunk's shared reads are done
+        bwd_fill<Cfg, TIO>(sm, p, b, d0, ch, false);
+        __syncthreads();
+        for (int r = 0; r < kBT; ++r) fold(h, r);
+    }
+
+    // ---- pass 2: reverse
+    float mu[4];                                 // a_{t+1} λ_{t+1}: what step t receives
+#pragma unroll
+    for (int q = 0; q < 4; ++q) mu[q] = (p.dlast && d_ok && n0 + q < p.N) ? p.dlast[row * p.N + n0 + q] : 0.f;
+    float dA[4] = {0.f, 0.f, 0.f, 0.f}, dDacc = 0.f, dbacc = 0.f;
+    TIO* g_du = static_cast<TIO*>(p.du);
+    TIO* g_dd = static_cast<TIO*>(p.ddelta);
+    TIO* g_dz = static_cast<TIO*>(p.dz);
+    for (int ch = p.nchunks - 1; ch >= 0; --ch) {
+        __syncthreads();
+        bwd_fill<Cfg, TIO>(sm, p, b, d0, ch, true);
+        __syncthreads();
+        // the state before each sub-chunk, kept in this lane's slots of shared memory
+        float* hbs = sm + Cfg::OFF_HB + cw * NS + n0;    // + k·kBW·NS for sub-chunk k
+        {
+            const float4 v = *reinterpret_cast<const float4*>(ck + (static_cast<int64_t>(ch) * kBW + cw) * NS + n0);
+            h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
+        }
+#pragma unroll 1
+        for (int k = 0; k < NSUB; ++k) {
+            *reinterpret_cast<float4*>(hbs + k * kBW * NS) = make_float4(h[0], h[1], h[2], h[3]);
+            if (k + 1 < NSUB)
+                for (int r = k * kBS; r < (k + 1) * kBS; ++r) fold(h, r);
+        }
+#pragma unroll 1
+        for (int k = NSUB - 1; k >= 0; --k) {
+            float H[kBS][4], yh[kBS], hb0[4];
+            {
+                const float4 v = *reinterpret_cast<const float4*>(hbs + k * kBW * NS);
+                hb0[0] = v.x; hb0[1] = v.y; hb0[2] = v.z; hb0[3] = v.w;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) h[q] = hb0[q];
+#pragma unroll
+            for (int i = 0; i < kBS; ++i) {
+                const int r = k * kBS + i;
+                fold(h, r);
+                float yp = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    H[i][q] = h[q];
+                    yp = fmaf(sm[Cfg::OFF_C + r * NS + n0 + q], h[q], yp);
+                }
+                yh[i] = fmaf(Dd, sm[Cfg::OFF_U + r * kBW + cw], channel_sum<CPW>(yp));
+            }
+#pragma unroll
+            for (int i = kBS - 1; i >= 0; --i) {
+                const int r = k * kBS + i;
+                const int64_t t = static_cast<int64_t>(ch) * kBT + r;
+                const float del = sm[Cfg::OFF_DEL + r * kBW + cw];
+                const float ut = sm[Cfg::OFF_U + r * kBW + cw];
+                const float dyh = sm[Cfg::OFF_DYH + r * kBW + cw];
+                const float dut_in = del * ut;
+                float dup = 0.f, ddp = 0.f, bc[8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float Bq = sm[Cfg::OFF_B + r * NS + n0 + q];
+                    const float l = fmaf(sm[Cfg::OFF_C + r * NS + n0 + q], dyh, mu[q]);
+                    const float a = ex2(del * A2[q]);
+                    const float hp = i > 0 ? H[i - 1][q] : hb0[q];
+                    bc[q] = l * dut_in;                  // dB of state n0 + q
+                    bc[4 + q] = dyh * H[i][q];           // dC
+                    dup = fmaf(l * del, Bq, dup);
+                    ddp = fmaf(l, fmaf(An[q] * a, hp, Bq * ut), ddp);
+                    dA[q] = fmaf(l * del * a, hp, dA[q]);
+                    mu[q] = a * l;
+                }
+                {
+                    // the tile's sums over channels: reduce over the warp's channel lanes,
+                    // then one shared atomic per lane (the warps of the tile add up there)
+                    const float sum = channel_reduce_scatter<CPW>(bc, c);
+                    if (c < 8) {
+                        const int kk = c & 7;
+                        atomicAdd(&sm[(kk < 4 ? Cfg::OFF_DB : Cfg::OFF_DC) + r * NS + n0 + (kk & 3)], sum);
+                    }
+                }
+                dup = channel_sum<CPW>(dup);
+                ddp = channel_sum<CPW>(ddp);
+                if (j == 0 && d_ok && t < p.L) {
+                    const float ddel = ddp * sm[Cfg::OFF_SIG + r * kBW + cw];
+                    const int64_t o = (static_cast<int64_t>(b) * p.L + t) * p.Dm + d;
+                    g_du[o] = from_f32<TIO>(fmaf(Dd, dyh, dup));
+                    g_dd[o] = from_f32<TIO>(ddel);
+                    if (p.z) g_dz[o] = from_f32<TIO>(sm[Cfg::OFF_DYG + r * kBW + cw] * yh[i]);
+                    dDacc = fmaf(dyh, ut, dDacc);
+                    dbacc += ddel;
+                }
+            }
+        }
+        __syncthreads();                         // every shared atomic of the chunk is done
+        for (int i = tid; i < kBT * NS; i += Cfg::THREADS) {
+            const int r = i / NS, n = i % NS;
+            const int64_t t = static_cast<int64_t>(ch) * kBT + r;
+            if (t < p.L && n < p.N) {
+                const int64_t o = (static_cast<int64_t>(b) * p.L + t) * p.N + n;
+                atomicAdd(p.dB + o, sm[Cfg::OFF_DB + i]);
+                atomicAdd(p.dC + o, sm[Cfg::OFF_DC + i]);
+            }
+        }
+    }
+    if (d_ok) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int n = n0 + q;
+            if (n < p.N) {
+                if (p.dh0) p.dh0[row * p.N + n] = mu[q];
+                atomicAdd(p.dA_log + static_cast<int64_t>(d) * p.N + n, dA[q] * An[q]);
+            }
+        }
+        if (j == 0) {
+            if (p.dD) atomicAdd(p.dD + d, dDacc);
+            if (p.dbias) atomicAdd(p.dbias + d, dbacc);
+        }
+    }
+}
+
+template <typename TIO, int NS>
+cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
+    using Cfg = BwdCfg<TIO, NS>;
+    cudaError_t e = cudaFuncSetAttribute(ss_bwd_kernel<TIO, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>(p.batch) * static_cast<unsigned>(p.tiles_per_batch);
+    ss_bwd_kernel<TIO, NS><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename TIO>
+cudaError_t launch_bwd(const BwdParams& p, int ns, cudaStream_t stream) {
+    if (ns == 4) return launch_bwd_t<TIO, 4>(p, stream);
+    if (ns == 8) return launch_bwd_t<TIO, 8>(p, stream);
+    return launch_bwd_t<TIO, 16>(p, stream);
+}
+
+int bwd_ns(int64_t N) { return N <= 4 ? 4 : N <= 8 ? 8 : 16; }
+
+size_t bwd_ws_bytes(int64_t batch, int64_t L, int64_t Dm, int64_t N) {
+    const int64_t tiles = batch * ((Dm + kBW - 1) / kBW);
+    const int64_t nch = (L + kBT - 1) / kBT;
+    return static_cast<size_t>(tiles) * nch * kBW * bwd_ns(N) * 4;
+}
+
+}  // namespace
+}  // namespace selscan
+
+using namespace selscan;
+using namespace selscan::host;
+
+extern "C" size_t ss_bwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N) {
+    if (batch <= 0 || L <= 0 || Dm <= 0 || N < 1 || N > 16) return 0;
+    return bwd_ws_bytes(batch, L, Dm, N);
+}
+
+extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
+                            const void* B, const void* C, const float* D, const void* z, const float* h0,
+                            const void* dy, const float* dlast, void* du, void* ddelta_raw, void* dz,
+                            float* dB, float* dC, float* dA_log, float* dD, float* ddelta_bias, float* dh0,
+                            int64_t batch, int64_t L, int64_t Dm, int64_t N, const ss_fwd_strides* strides,
+                            void* workspace, size_t workspace_bytes, void* stream_ptr) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    if (batch < 0 || L < 0 || Dm < 0) return SS_ERR_INVALID_ARG;
+    if (N < 1 || N > 16) return SS_ERR_UNSUPPORTED;
+    ss_fwd_strides s;
+    if (strides) {
+        s = *strides;
+    } else {
+        std::memset(&s, 0, sizeof(s));
+        s.io_dtype = SS_F32;
+        s.u_b = s.delta_b = s.z_b = s.y_b = L * Dm;
+        s.u_l = s.delta_l = s.z_l = s.y_l = Dm;
+        s.B_b = s.C_b = L * N;
+        s.B_l = s.C_l = N;
+    }
+    if (s.io_dtype != SS_F32 && s.io_dtype != SS_BF16) return SS_ERR_INVALID_ARG;
+    const bool bf16 = s.io_dtype == SS_BF16;
+    const int64_t es = bf16 ? 2 : 4;
+    if (batch == 0 || Dm == 0) return SS_OK;
+    if (!A_log || !dA_log) return SS_ERR_INVALID_ARG;
+    if (L > INT32_MAX || Dm > INT32_MAX || batch > INT32_MAX) return SS_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+    // the sums are accumulated: clear them (also the whole answer when L == 0)
+    auto clear = [&](float* q, int64_t n) { return q ? cudaMemsetAsync(q, 0, sizeof(float) * n, stream) : cudaSuccess; };
+    if (L == 0) {
+        const void* small[] = {A_log, dA_log, dD, ddelta_bias, dh0, dlast};
+        for (const void* q : small) {
+            if (q && !is_aligned(q, 4)) return SS_ERR_MISALIGNED;
+            if (q && !dev_ptr(q, dev)) return SS_ERR_INVALID_ARG;
+        }
+        if (clear(dA_log, Dm * N) != cudaSuccess || clear(dD, Dm) != cudaSuccess ||
+            clear(ddelta_bias, Dm) != cudaSuccess)
+            return SS_ERR_CUDA;
+        if (dh0) {   // no steps: the gradient of h0 is dlast
+            if (dlast) return cudaMemcpyAsync(dh0, dlast, sizeof(float) * batch * Dm * N, cudaMemcpyDeviceToDevice,
+                                              stream) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+            return clear(dh0, batch * Dm * N) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+        }
+        return SS_OK;
+    }
+    if (!u || !delta_raw || !B || !C || !dy || !du || !ddelta_raw || !dB || !dC) return SS_ERR_INVALID_ARG;
+    if (z && !dz) return SS_ERR_INVALID_ARG;
+    const int64_t st[] = {s.u_b, s.u_l, s.delta_b, s.delta_l, s.B_b, s.B_l, s.C_b, s.C_l,
+                          z ? s.z_b : 0, z ? s.z_l : 0};
+    for (int64_t v : st)
+        if (v < 0) return SS_ERR_INVALID_ARG;
+    if ((s.u_l < Dm || s.delta_l < Dm || (z && s.z_l < Dm) || s.B_l < N || s.C_l < N) && L > 1)
+        return SS_ERR_INVALID_ARG;
+    const void* io_ptrs[] = {u, delta_raw, B, C, z, dy, du, ddelta_raw, dz};
+    for (const void* q : io_ptrs)
+        if (q && !is_aligned(q, es)) return SS_ERR_MISALIGNED;
+    const void* f_ptrs[] = {A_log, D, delta_bias, h0, dlast, dB, dC, dA_log, dD, ddelta_bias, dh0};
+    for (const void* q : f_ptrs)
+        if (q && !is_aligned(q, 4)) return SS_ERR_MISALIGNED;
+    const void* all[] = {u, delta_raw, B, C, z, dy, du, ddelta_raw, dz, A_log, D, delta_bias, h0, dlast,
+                         dB, dC, dA_log, dD, ddelta_bias, dh0};
+    for (const void* q : all)
+        if (q && !dev_ptr(q, dev)) return SS_ERR_INVALID_ARG;
+    // outputs: pairwise disjoint and disjoint from every input
+    const Range outs[] = {range3(du, batch, L, Dm, L * Dm, Dm, es), range3(ddelta_raw, batch, L, Dm, L * Dm, Dm, es),
+                          range3(dz, batch, L, Dm, L * Dm, Dm, es), range3(dB, batch, L, N, L * N, N, 4),
+                          range3(dC, batch, L, N, L * N, N, 4), range3(dA_log, 1, Dm, N, 0, N, 4),
+                          range3(dD, 1, 1, Dm, 0, 0, 4), range3(ddelta_bias, 1, 1, Dm, 0, 0, 4),
+                          range3(dh0, batch, Dm, N, Dm * N, N, 4)};
+    const Range ins[] = {range3(u, batch, L, Dm, s.u_b, s.u_l, es), range3(delta_raw, batch, L, Dm, s.delta_b, s.delta_l, es),
+                         range3(z, batch, L, Dm, s.z_b, s.z_l, es), range3(B, batch, L, N, s.B_b, s.B_l, es),
+                         range3(C, batch, L, N, s.C_b, s.C_l, es), range3(dy, batch, L, Dm, L * Dm, Dm, es),
+                         range3(A_log, 1, Dm, N, 0, N, 4), range3(D, 1, 1, Dm, 0, 0, 4),
+                         range3(delta_bias, 1, 1, Dm, 0, 0, 4), range3(h0, batch, Dm, N, Dm * N, N, 4),
+                         range3(dlast, batch, Dm, N, Dm * N, N, 4)};
+    const int nouts = sizeof(outs) / sizeof(outs[0]);
+    for (int i = 0; i < nouts; ++i) {
+        for (const Range& r : ins)
+            if (meet(outs[i], r)) return SS_ERR_INVALID_ARG;
+        for (int k = i + 1; k < nouts; ++k)
+            if (meet(outs[i], outs[k])) return SS_ERR_INVALID_ARG;
+    }
+    const size_t need = bwd_ws_bytes(batch, L, Dm, N);
+    if (!workspace || workspace_bytes < need) return SS_ERR_INVALID_ARG;
+    if (!is_aligned(workspace, 256)) return SS_ERR_MISALIGNED;
+    if (!dev_ptr(workspace, dev)) return SS_ERR_INVALID_ARG;
+    if (clear(dB, batch * L * N) != cudaSuccess || clear(dC, batch * L * N) != cudaSuccess ||
+        clear(dA_log, Dm * N) != cudaSuccess || clear(dD, Dm) != cudaSuccess ||
+        clear(ddelta_bias, Dm) != cudaSuccess)
+        return SS_ERR_CUDA;
+
+    BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.u = u; p.delta = delta_raw; p.z = z; p.Bm = B; p.Cm = C; p.bias = delta_bias; p.A_log = A_log; p.Dv = D;
+    p.h0 = h0; p.dy = dy; p.dlast = dlast; p.du = du; p.ddelta = ddelta_raw; p.dz = dz; p.dB = dB; p.dC = dC;
+    p.dA_log = dA_log; p.dD = dD; p.dbias = ddelta_bias; p.dh0 = dh0;
+    p.ckpt = static_cast<float*>(workspace);
+    p.u_b = s.u_b; p.u_l = s.u_l; p.d_b = s.delta_b; p.d_l = s.delta_l; p.z_b = s.z_b; p.z_l = s.z_l;
+    p.B_b = s.B_b; p.B_l = s.B_l; p.C_b = s.C_b; p.C_l = s.C_l;
+    p.batch = static_cast<int>(batch); p.L = static_cast<int>(L); p.Dm = static_cast<int>(Dm);
+    p.N = static_cast<int>(N);
+    p.nchunks = static_cast<int>((L + kBT - 1) / kBT);
+    p.tiles_per_batch = static_cast<int>((Dm + kBW - 1) / kBW);
+    if (static_cast<int64_t>(p.batch) * p.tiles_per_batch > INT32_MAX) return SS_ERR_UNSUPPORTED;
+    const int ns = bwd_ns(N);
+    const cudaError_t e = bf16 ? launch_bwd<__nv_bfloat16>(p, ns, stream) : launch_bwd<float>(p, ns, stream);
+    return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}

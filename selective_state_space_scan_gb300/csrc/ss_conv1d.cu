@@ -21,6 +21,7 @@
 
 #include "../../include/selscan.h"
 #include "device_common.cuh"
+#include "host_util.h"
 
 namespace selscan {
 namespace {
@@ -191,34 +192,11 @@ __global__ void ss_conv1d_window_copy(const float* win_in, float* win_out, int64
     if (i < n) win_out[i] = win_in ? win_in[i] : 0.f;
 }
 
-bool dev_ptr(const void* q, int dev) {
-    cudaPointerAttributes a;
-    if (cudaPointerGetAttributes(&a, q) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    if (a.type == cudaMemoryTypeManaged) return true;
-    return a.type == cudaMemoryTypeDevice && a.device == dev;
-}
-
-bool is_aligned(const void* q, size_t a) { return reinterpret_cast<uintptr_t>(q) % a == 0; }
-
-struct Range {
-    uintptr_t lo = 0, hi = 0;
-};
-Range range3(const void* q, int64_t n0, int64_t n1, int64_t n2, int64_t s0, int64_t s1, int64_t es) {
-    Range r;
-    if (!q || n0 <= 0 || n1 <= 0 || n2 <= 0) return r;
-    r.lo = reinterpret_cast<uintptr_t>(q);
-    r.hi = r.lo + static_cast<uintptr_t>(((n0 - 1) * s0 + (n1 - 1) * s1 + n2) * es);
-    return r;
-}
-bool meet(const Range& a, const Range& b) { return a.hi > a.lo && b.hi > b.lo && a.lo < b.hi && b.lo < a.hi; }
-
 }  // namespace
 }  // namespace selscan
 
 using namespace selscan;
+using namespace selscan::host;
 
 extern "C" ss_status ss_conv1d(const void* x, const float* weight, const float* bias, void* out,
                                const float* window_in, float* window_out, int64_t batch, int64_t L,

@@ -1,0 +1,161 @@
+"""Parity of the CUDA backward scan (ss_bwd, through the C ABI) with the fp64 oracle's
+gradients.  Elementwise gradients (du, ddelta_raw, dz, dh0) and the sums over channels or
+batch rows (dB, dC, dA_log, dD, ddelta_bias, accumulated with atomics) have separate gates."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import selective_state_space_scan_gb300 as ss
+from selective_state_space_scan_gb300 import synth
+
+from helpers import BF16_REL_L2, f32dev, rel_l2, to_dev, to_host
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+GRAD_REL_L2 = 1e-5       # fp32, elementwise gradients
+SUM_REL_L2 = 1e-4        # fp32 sums over channels / batch rows (atomic order varies)
+BF16_SUM_REL_L2 = 1e-3
+
+ELEMENTWISE = ("du", "ddelta_raw", "dz", "dh0")
+SUMS = ("dB", "dC", "dA_log", "dD", "ddelta_bias")
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    torch.cuda.synchronize()
+
+
+def problem(batch, L, Dm, N, io="f32", seed=0, gate=True, with_h0=True, with_dlast=True, **kw):
+    w = synth.fwd_inputs(batch, L, Dm, N, io=io, seed=seed, **kw)
+    a = w.arrays
+    if not gate:
+        a["z"] = None
+    g = synth.rng_for(seed, 12)
+    dy = g.standard_normal((batch, L, Dm), dtype=np.float32)
+    if io == "bf16":
+        dy = synth.round_bf16(dy)
+    h0 = synth.initial_state(batch, Dm, N, seed=seed) if with_h0 else None
+    dlast = g.standard_normal((batch, Dm, N), dtype=np.float32) if with_dlast else None
+    return w, a, dy, h0, dlast
+
+
+def run(w, a, dy, h0, dlast):
+    io = w.io
+    t = dict(u=to_dev(a["u"], io), delta_raw=to_dev(a["delta_raw"], io), z=to_dev(a["z"], io),
+             B=to_dev(a["B"], io), C=to_dev(a["C"], io))
+    g = ss.ss_bwd(to_dev(dy, io), t["u"], t["delta_raw"], f32dev(a["delta_bias"]), f32dev(a["A_log"]), t["B"],
+                  t["C"], f32dev(a["D"]), t["z"], h0=f32dev(h0), dlast=f32dev(dlast))
+    torch.cuda.synchronize()
+    return {k: (None if v is None else to_host(v)) for k, v in g.items()}
+
+
+def reference(a, dy, h0, dlast):
+    return oracle.ss_bwd(a["u"], a["delta_raw"], a["delta_bias"], a["A_log"], a["B"], a["C"], a["D"], a["z"], dy,
+                         h0=None if h0 is None else h0.astype(np.float64),
+                         dlast=None if dlast is None else dlast.astype(np.float64))
+
+
+def check(w, a, dy, h0, dlast, what=""):
+    got = run(w, a, dy, h0, dlast)
+    ref = reference(a, dy, h0, dlast)
+    for k in ELEMENTWISE + SUMS:
+        if k == "dz" and a["z"] is None:
+            assert got["dz"] is None
+            continue
+        if k == "dD" and a["D"] is None:
+            continue
+        assert np.all(np.isfinite(got[k])), f"{what} {k}: non-finite"
+        e = rel_l2(got[k], ref[k])
+        if w.io == "bf16":
+            tol = BF16_REL_L2 if k in ("du", "ddelta_raw", "dz") else BF16_SUM_REL_L2
+        else:
+            tol = GRAD_REL_L2 if k in ELEMENTWISE else SUM_REL_L2
+        assert e <= tol, f"{what} {k}: rel-L2 {e:.3e} > {tol}"
+    return got, ref
+
+
+@pytest.mark.parametrize("L", [1, 5, 63, 64, 65, 200])
+def test_bwd_lengths(L):
+    check(*problem(2, L, 40, 16, seed=L), what=f"L={L}")
+
+
+@pytest.mark.parametrize("N", [1, 3, 4, 5, 8, 12, 16])
+def test_bwd_state_counts(N):
+    check(*problem(2, 130, 72, N, seed=20 + N), what=f"N={N}")
+
+
+@pytest.mark.parametrize("Dm", [1, 31, 33, 100])
+def test_bwd_channel_counts(Dm):
+    check(*problem(3, 97, Dm, 16, seed=40 + Dm), what=f"Dm={Dm}")
+
+
+@pytest.mark.parametrize("opts", ["no_gate", "no_h0", "no_dlast", "plain"])
+def test_bwd_optional_inputs(opts):
+    kw = dict(gate=opts not in ("no_gate", "plain"), with_h0=opts not in ("no_h0", "plain"),
+              with_dlast=opts not in ("no_dlast", "plain"))
+    check(*problem(2, 150, 48, 16, seed=50, **kw), what=opts)
+
+
+def test_bwd_bf16():
+    check(*problem(2, 300, 64, 16, io="bf16", seed=60), what="bf16")
+
+
+def test_bwd_long_sequence():
+    check(*problem(2, 2048, 256, 16, seed=61), what="L=2048")
+
+
+def test_bwd_full_size_130m():
+    """The 130m-shaped layer (batch 8, L 2048, Dm 1536, N 16), gradients of every input."""
+    w = synth.config("mamba130m")
+    g = synth.rng_for(62, 12)
+    dy = g.standard_normal((w.batch, w.L, w.Dm), dtype=np.float32)
+    check(w, w.arrays, dy, None, None, what="130m")
+
+
+def test_bwd_matches_forward_difference_on_gpu():
+    """The GPU gradient of sum(dy * y) in a random direction v of u matches the directional
+    difference of two GPU forward passes (step 1e-3, central), a check that does not go
+    through the oracle."""
+    w, a, dy, _, _ = problem(2, 300, 64, 16, seed=63, with_h0=False, with_dlast=False)
+    got = run(w, a, dy, None, None)
+    v = synth.rng_for(64, 12).standard_normal(a["u"].shape).astype(np.float32)
+    eps = 1e-3
+
+    def J(u):
+        t = {k: f32dev(a[k]) for k in ("delta_raw", "z", "B", "C", "A_log", "D", "delta_bias")}
+        y = ss.ss_fwd(f32dev(u), t["delta_raw"], t["delta_bias"], t["A_log"], t["B"], t["C"], t["D"], t["z"])
+        torch.cuda.synchronize()
+        return float(np.sum(to_host(y) * dy.astype(np.float64)))
+    fd = (J(a["u"] + eps * v) - J(a["u"] - eps * v)) / (2 * eps)
+    an = float(np.sum(got["du"] * v))
+    assert abs(fd - an) <= 1e-3 * abs(an) + 1e-3, (fd, an)
+
+
+def test_bwd_rejects_small_workspace_and_overlap():
+    w, a, dy, h0, dlast = problem(1, 64, 32, 16, seed=65)
+    lib = ss.lib()
+    t = {k: f32dev(v) for k, v in a.items() if v is not None}
+    dyd = f32dev(dy)
+    out = {k: torch.empty(sh, device="cuda") for k, sh in (("du", (1, 64, 32)), ("dd", (1, 64, 32)), ("dz", (1, 64, 32)),
+                                                          ("dB", (1, 64, 16)), ("dC", (1, 64, 16)), ("dA", (32, 16)))}
+    s = ss.FwdStrides(ss.SS_F32, 64 * 32, 32, 64 * 32, 32, 64 * 32, 32, 0, 0, 64 * 16, 16, 64 * 16, 16)
+    need = lib.ss_bwd_workspace_size(1, 64, 32, 16)
+    ws = torch.zeros(need + 256, dtype=torch.uint8, device="cuda")
+
+    def call(du_ptr, nbytes):
+        return lib.ss_bwd(t["u"].data_ptr(), t["delta_raw"].data_ptr(), t["delta_bias"].data_ptr(),
+                          t["A_log"].data_ptr(), t["B"].data_ptr(), t["C"].data_ptr(), t["D"].data_ptr(),
+                          t["z"].data_ptr(), None, dyd.data_ptr(), None, du_ptr, out["dd"].data_ptr(),
+                          out["dz"].data_ptr(), out["dB"].data_ptr(), out["dC"].data_ptr(), out["dA"].data_ptr(),
+                          None, None, None, 1, 64, 32, 16, ctypes.byref(s), ws.data_ptr(), nbytes, None)
+    assert call(out["du"].data_ptr(), need - 4) == 1          # workspace too small
+    assert call(t["u"].data_ptr(), need) == 1                 # du over an input
+    assert call(out["dd"].data_ptr(), need) == 1              # du over ddelta_raw
+    assert call(out["du"].data_ptr(), need) == 0
+    torch.cuda.synchronize()
