@@ -202,7 +202,7 @@ ss_status ss_fwd_static(const void* u, const void* delta_raw, const float* delta
  *   Outputs must not overlap each other or any input.  The sums (dB, dC, dA_log, dD,
  *   ddelta_bias) are accumulated with atomic adds, so their rounding varies from run to run.
  *   workspace          device memory, 256-byte aligned, ss_bwd_workspace_size(...) bytes (the
- *                      state at every 64-step chunk start); contents need no initialisation.
+ *                      state at every 16th step); contents need no initialisation.
  * Errors as ss_fwd.  Returns SS_OK once the work is enqueued.
  */
 ss_status ss_bwd(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,

@@ -13,10 +13,10 @@
 //
 // Layout: the forward kernel's lanes (a channel's states split over NS/4 lanes of 4 states, a
 // CTA = 32 channels of one batch row).  The reverse recurrence needs h_{t-1} at every step:
-//   pass 1 folds the sequence forward and stores the state at every chunk start (workspace);
-//   pass 2 walks the chunks backwards; inside a chunk it refolds from the checkpoint to get the
-//   state at each sub-chunk start, then for each sub-chunk (last first) refolds its kBS states
-//   into registers and runs the adjoint backwards over them.
+//   pass 1 folds the sequence forward and stores the state at every kBS-step sub-chunk start
+//   (workspace);
+//   pass 2 walks the chunks backwards; for each sub-chunk (last first) it refolds the sub-chunk's
+//   kBS states into registers from its checkpoint and runs the adjoint backwards over them.
 // The per-(step, channel) quantities (Δ, σ(r), dŷ, dy·silu'(z), u) and the chunk's B, C are
 // staged in shared memory; dB, dC (sums over the CTA's channels) are reduced over a warp's
 // channel lanes by shuffles, over the warps with shared atomics, and reach global memory with
@@ -59,7 +59,7 @@ struct BwdParams {
     float* dD;             // [Dm] or nullptr (zeroed)
     float* dbias;          // [Dm] or nullptr (zeroed)
     float* dh0;            // [batch, Dm, N] or nullptr
-    float* ckpt;           // [tiles][nchunks][kBW][NS]
+    float* ckpt;           // [tiles][nchunks][kBT / kBS][kBW][NS]: the state at every sub-chunk start
     int64_t u_b, u_l, d_b, d_l, z_b, z_l, B_b, B_l, C_b, C_l;
     int batch, L, Dm, N, nchunks, tiles_per_batch;
 };
@@ -77,8 +77,7 @@ struct BwdCfg {
     static constexpr int OFF_C = OFF_B + kBT * NS;
     static constexpr int OFF_DB = OFF_C + kBT * NS;
     static constexpr int OFF_DC = OFF_DB + kBT * NS;
-    static constexpr int OFF_HB = OFF_DC + kBT * NS;     // [kBT / kBS][kBW][NS] sub-chunk start states
-    static constexpr int SMEM = (OFF_HB + (kBT / kBS) * kBW * NS) * 4;
+    static constexpr int SMEM = (OFF_DC + kBT * NS) * 4;
 };
 
 __device__ __forceinline__ float sigmoid_f(float x) { return rcp_approx(1.f + ex2(-x * kLog2e)); }
@@ -91,6 +90,7 @@ __device__ void bwd_fill(float* sm, const BwdParams& p, int b, int d0, int chunk
     const TIO* dl = static_cast<const TIO*>(p.delta);
     const TIO* zz = static_cast<const TIO*>(p.z);
     const TIO* dy = static_cast<const TIO*>(p.dy);
+#pragma unroll 4
     for (int i = threadIdx.x; i < kBT * kBW; i += Cfg::THREADS) {
         const int r = i / kBW, c = i % kBW;
         const int64_t t = t0 + r;
@@ -124,6 +124,7 @@ __device__ void bwd_fill(float* sm, const BwdParams& p, int b, int d0, int chunk
     }
     const TIO* Bm = static_cast<const TIO*>(p.Bm);
     const TIO* Cm = static_cast<const TIO*>(p.Cm);
+#pragma unroll 4
     for (int i = threadIdx.x; i < kBT * Cfg::NS; i += Cfg::THREADS) {
         const int r = i / Cfg::NS, n = i % Cfg::NS;
         const int64_t t = t0 + r;
@@ -193,7 +194,10 @@ __global__ void __launch_bounds__(BwdCfg<TIO, NS>::THREADS) ss_bwd_kernel(const 
         A2[q] = An[q] * kLog2e;
     }
     const float Dd = (d_ok && p.Dv) ? p.Dv[d] : 0.f;
-    float* ck = p.ckpt + static_cast<int64_t>(tile) * p.nchunks * kBW * NS;
+    float* ck = p.ckpt + static_cast<int64_t>(tile) * p.nchunks * NSUB * kBW * NS;
+    auto ckpt_at = [&](int ch, int k) {          // this lane's checkpoint slot: sub-chunk k of chunk ch
+        return ck + ((static_cast<int64_t>(ch) * NSUB + k) * kBW + cw) * NS + n0;
+    };
     const int64_t row = static_cast<int64_t>(b) * p.Dm + d;
 
     auto fold = [&](float (&h)[4], int r) {      // one step of the forward fold (chunk row r)
@@ -203,17 +207,19 @@ __global__ void __launch_bounds__(BwdCfg<TIO, NS>::THREADS) ss_bwd_kernel(const 
         for (int q = 0; q < 4; ++q) h[q] = fmaf(ex2(del * A2[q]), h[q], du * sm[Cfg::OFF_B + r * NS + n0 + q]);
     };
 
-    // ---- pass 1: forward, the state at every chunk start
+    // ---- pass 1: forward, the state at every sub-chunk start
     float h[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) h[q] = (p.h0 && d_ok && n0 + q < p.N) ? p.h0[row * p.N + n0 + q] : 0.f;
     for (int ch = 0; ch < p.nchunks; ++ch) {
-        *reinterpret_cast<float4*>(ck + (static_cast<int64_t>(ch) * kBW + cw) * NS + n0) =
-            make_float4(h[0], h[1], h[2], h[3]);
         __syncthreads();                         // the previous chunk's shared reads are done
         bwd_fill<Cfg, TIO>(sm, p, b, d0, ch, false);
         __syncthreads();
-        for (int r = 0; r < kBT; ++r) fold(h, r);
+#pragma unroll 1
+        for (int k = 0; k < NSUB; ++k) {
+            __stcg(reinterpret_cast<float4*>(ckpt_at(ch, k)), make_float4(h[0], h[1], h[2], h[3]));
+            for (int r = k * kBS; r < (k + 1) * kBS; ++r) fold(h, r);
+        }
     }
 
     // ---- pass 2: reverse
@@ -228,23 +234,11 @@ __global__ void __launch_bounds__(BwdCfg<TIO, NS>::THREADS) ss_bwd_kernel(const 
         __syncthreads();
         bwd_fill<Cfg, TIO>(sm, p, b, d0, ch, true);
         __syncthreads();
-        // the state before each sub-chunk, kept in this lane's slots of shared memory
-        float* hbs = sm + Cfg::OFF_HB + cw * NS + n0;    // + k·kBW·NS for sub-chunk k
-        {
-            const float4 v = *reinterpret_cast<const float4*>(ck + (static_cast<int64_t>(ch) * kBW + cw) * NS + n0);
-            h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
-        }
-#pragma unroll 1
-        for (int k = 0; k < NSUB; ++k) {
-            *reinterpret_cast<float4*>(hbs + k * kBW * NS) = make_float4(h[0], h[1], h[2], h[3]);
-            if (k + 1 < NSUB)
-                for (int r = k * kBS; r < (k + 1) * kBS; ++r) fold(h, r);
-        }
 #pragma unroll 1
         for (int k = NSUB - 1; k >= 0; --k) {
             float H[kBS][4], yh[kBS], hb0[4];
             {
-                const float4 v = *reinterpret_cast<const float4*>(hbs + k * kBW * NS);
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(ckpt_at(ch, k)));
                 hb0[0] = v.x; hb0[1] = v.y; hb0[2] = v.z; hb0[3] = v.w;
             }
 #pragma unroll
@@ -354,7 +348,7 @@ int bwd_ns(int64_t N) { return N <= 4 ? 4 : N <= 8 ? 8 : 16; }
 size_t bwd_ws_bytes(int64_t batch, int64_t L, int64_t Dm, int64_t N) {
     const int64_t tiles = batch * ((Dm + kBW - 1) / kBW);
     const int64_t nch = (L + kBT - 1) / kBT;
-    return static_cast<size_t>(tiles) * nch * kBW * bwd_ns(N) * 4;
+    return static_cast<size_t>(tiles) * nch * (kBT / kBS) * kBW * bwd_ns(N) * 4;
 }
 
 }  // namespace
