@@ -92,6 +92,8 @@ KERNEL_SOURCES = {
                                              "fwd_lane_f32.cu", "fwd_lane_bf16.cu", "ss_fwd_carry.cu"),
     "ss_fwd_seg_kernel": _COMMON_SOURCES + ("ss_fwd_seg.cuh", "fwd_seg.cu", "fwd_launch_common.cuh"),
     "ss_step_kernel": _COMMON_SOURCES + ("ss_step.cu",),
+    "ss_conv1d_kernel": ("device_common.cuh", "host_util.h", "ss_conv1d.cu"),
+    "ss_bwd_kernel": ("device_common.cuh", "host_util.h", "ss_bwd.cu"),
 }
 
 
@@ -433,7 +435,8 @@ def bench_conv1d(args, local_rank):
         "gpu_launches": args.steps, "clocks": clk.summary(),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                     "traffic": None, "kernel": "ss_conv1d_kernel", "launch_ms": launch_ms,
+                     "traffic": measured_traffic("conv1d_130m", "ss_conv1d_kernel"), "kernel": "ss_conv1d_kernel",
+                     "launch_ms": launch_ms,
                      "alg_bytes_per_launch": alg}}))
     return 0
 
@@ -486,7 +489,8 @@ def bench_bwd(args, local_rank):
         "gpu_launches": args.steps, "clocks": clk.summary(),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                     "traffic": None, "kernel": "ss_bwd_kernel", "launch_ms": launch_ms,
+                     "traffic": measured_traffic("bwd_130m", "ss_bwd_kernel"), "kernel": "ss_bwd_kernel",
+                     "launch_ms": launch_ms,
                      "alg_bytes_per_launch": alg}}))
     return 0
 
