@@ -47,4 +47,13 @@ cudaError_t launch_step(const StepParams& p, bool bf16, bool vec, cudaStream_t s
 // s-1)·slot s-1 + the end state pass A left in slot s, for s = 1 .. p.nseg - 1.
 cudaError_t launch_fwd_carry(const FwdParams& p, cudaStream_t stream);
 
+// Unswizzled 3-D TMA descriptor over a [batch, rows, cols] tensor (cols contiguous, element
+// strides row_stride and batch_stride) with a [1, box_rows, box_cols] box; elements past the
+// ends read as zero.  False when the tensor's alignment or strides rule TMA out.
+bool make_tile_map(CUtensorMap* m, const void* base, bool bf16, int64_t cols, int64_t rows, int64_t batch,
+                   int64_t row_stride, int64_t batch_stride, int box_cols, int box_rows);
+
+// The current device's error word (kErr* bits), or nullptr if its address cannot be found.
+unsigned int* device_error_word();
+
 }  // namespace selscan

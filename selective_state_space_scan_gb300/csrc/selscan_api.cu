@@ -168,6 +168,17 @@ bool tma_stride_ok(int64_t stride_elems, int64_t es) {
 }
 
 }  // namespace
+
+bool make_tile_map(CUtensorMap* m, const void* base, bool bf16, int64_t cols, int64_t rows, int64_t batch,
+                   int64_t row_stride, int64_t batch_stride, int box_cols, int box_rows) {
+    const int64_t es = bf16 ? 2 : 4;
+    return tma_stride_ok(row_stride, es) && (batch <= 1 || tma_stride_ok(batch_stride, es)) &&
+           reinterpret_cast<uintptr_t>(base) % 16 == 0 &&
+           make_map(m, base, bf16, cols, rows, batch, row_stride, batch_stride, box_cols, box_rows, false);
+}
+
+unsigned int* device_error_word() { return device_error_ptr(); }
+
 }  // namespace selscan
 
 using namespace selscan;

@@ -24,19 +24,24 @@
 // global atomics.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
 #include "../../include/selscan.h"
 #include "device_common.cuh"
 #include "host_util.h"
+#include "internal.h"
 
 namespace selscan {
 namespace {
 
-constexpr int kBT = 64;    // steps per chunk (one checkpoint per chunk)
+constexpr int kBT = 32;    // steps per chunk (the height of one staged tile)
 constexpr int kBS = 16;    // steps per sub-chunk (their states are held in registers)
 constexpr int kBW = 32;    // channels per CTA
+
+// Test hook: -1 automatic, 0 plain-load staging, 1 TMA staging (refused when it cannot be used).
+std::atomic<int> g_force_bwd_tma{-1};
 
 struct BwdParams {
     const void* u;
@@ -60,8 +65,14 @@ struct BwdParams {
     float* dbias;          // [Dm] or nullptr (zeroed)
     float* dh0;            // [batch, Dm, N] or nullptr
     float* ckpt;           // [tiles][nchunks][kBT / kBS][kBW][NS]: the state at every sub-chunk start
+    unsigned int* err;     // device error word
     int64_t u_b, u_l, d_b, d_l, z_b, z_l, B_b, B_l, C_b, C_l;
     int batch, L, Dm, N, nchunks, tiles_per_batch;
+};
+
+// TMA descriptors of the staged inputs: [T][W] boxes of u, δ, z, dy and [T][NS] boxes of B, C.
+struct BwdMaps {
+    CUtensorMap u, delta, z, dy, B, C;
 };
 
 template <typename TIO, int NS_>
@@ -71,70 +82,90 @@ struct BwdCfg {
     static constexpr int CPW = 32 / LPC;         // channels per warp
     static constexpr int WARPS = kBW / CPW;
     static constexpr int THREADS = 32 * WARPS;
-    static constexpr int X = kBT * kBW;          // one [T][W] array (floats)
+    static constexpr int ES = static_cast<int>(sizeof(TIO));
+    // staged input tiles, io dtype, as TMA writes them (bytes)
+    static constexpr int RAW_X = kBT * kBW * ES;
+    static constexpr int RAW_N = kBT * NS * ES;
+    static constexpr int R_U = 0, R_D = RAW_X, R_Z = 2 * RAW_X, R_Y = 3 * RAW_X, R_B = 4 * RAW_X,
+                         R_C = 4 * RAW_X + RAW_N;
+    static constexpr int RAW_BYTES = 4 * RAW_X + 2 * RAW_N;
+    // fp32 arrays the chunk is processed from (float offsets after the staged tiles)
+    static constexpr int X = kBT * kBW, XN = kBT * NS;
     static constexpr int OFF_U = 0, OFF_DEL = X, OFF_SIG = 2 * X, OFF_DYH = 3 * X, OFF_DYG = 4 * X;
-    static constexpr int OFF_B = 5 * X;
-    static constexpr int OFF_C = OFF_B + kBT * NS;
-    static constexpr int OFF_DB = OFF_C + kBT * NS;
-    static constexpr int OFF_DC = OFF_DB + kBT * NS;
-    static constexpr int SMEM = (OFF_DC + kBT * NS) * 4;
+    static constexpr int OFF_B = 5 * X, OFF_C = OFF_B + XN, OFF_DB = OFF_C + XN, OFF_DC = OFF_DB + XN;
+    static constexpr int BAR_OFF = RAW_BYTES + (OFF_DC + XN) * 4;
+    static constexpr int SMEM = BAR_OFF + 16;    // the mbarrier, then the abort flag
+    static_assert(RAW_X % 128 == 0 && RAW_N % 16 == 0, "TMA destinations stay 16-byte aligned");
 };
 
 __device__ __forceinline__ float sigmoid_f(float x) { return rcp_approx(1.f + ex2(-x * kLog2e)); }
 
-// Stage chunk `chunk` of the tile in shared memory.  full = false (pass 1): u, Δ, B only.
-template <class Cfg, typename TIO>
-__device__ void bwd_fill(float* sm, const BwdParams& p, int b, int d0, int chunk, bool full) {
-    const int64_t t0 = static_cast<int64_t>(chunk) * kBT;
-    const TIO* u = static_cast<const TIO*>(p.u);
-    const TIO* dl = static_cast<const TIO*>(p.delta);
-    const TIO* zz = static_cast<const TIO*>(p.z);
-    const TIO* dy = static_cast<const TIO*>(p.dy);
+// Build the chunk's fp32 arrays: Δ = softplus(δ + bias), u and B (and, full = pass 2, σ(δ + bias),
+// dŷ = dy·silu(z), dy·silu'(z), C).  Inputs come from the staged tiles (TMA) or straight from
+// global memory.  Steps past L and channels past Dm become zeros, which make those steps the
+// identity of both recurrences.
+template <class Cfg, typename TIO, bool TMA>
+__device__ __forceinline__ void bwd_prepare(float* sm, const uint8_t* raw, const BwdParams& p, int b, int d0,
+                                            int chunk, bool full, float bias_c) {
+    const int t0 = chunk * kBT;
+    const int c = threadIdx.x % kBW;             // fixed per thread (THREADS is a multiple of kBW)
+    const int d = d0 + c;
+    const TIO* gu = static_cast<const TIO*>(p.u);
+    const TIO* gd = static_cast<const TIO*>(p.delta);
+    const TIO* gz = static_cast<const TIO*>(p.z);
+    const TIO* gy = static_cast<const TIO*>(p.dy);
 #pragma unroll 4
     for (int i = threadIdx.x; i < kBT * kBW; i += Cfg::THREADS) {
-        const int r = i / kBW, c = i % kBW;
-        const int64_t t = t0 + r;
-        const int d = d0 + c;
-        float uu = 0.f, del = 0.f, sig = 0.f, dyh = 0.f, dyg = 0.f;
-        if (t < p.L && d < p.Dm) {
-            uu = to_f32<TIO>(u[b * p.u_b + t * p.u_l + d]);
-            const float rr = to_f32<TIO>(dl[b * p.d_b + t * p.d_l + d]) + (p.bias ? p.bias[d] : 0.f);
-            del = softplus(rr);
+        const int t = t0 + i / kBW;
+        const bool in = t < p.L && d < p.Dm;
+        float uu = 0.f, rr = 0.f, zv = 0.f, dyv = 0.f;
+        if constexpr (TMA) {
+            uu = to_f32<TIO>(reinterpret_cast<const TIO*>(raw + Cfg::R_U)[i]);
+            rr = to_f32<TIO>(reinterpret_cast<const TIO*>(raw + Cfg::R_D)[i]);
             if (full) {
-                sig = sigmoid_f(rr);
-                const float dyv = to_f32<TIO>(dy[(static_cast<int64_t>(b) * p.L + t) * p.Dm + d]);
-                float g = 1.f, dg = 0.f;
-                if (zz) {
-                    const float zv = to_f32<TIO>(zz[b * p.z_b + t * p.z_l + d]);
-                    const float s = sigmoid_f(zv);
-                    g = zv * s;
-                    dg = s * fmaf(zv, 1.f - s, 1.f);
-                }
-                dyh = dyv * g;
-                dyg = dyv * dg;
+                if (gz) zv = to_f32<TIO>(reinterpret_cast<const TIO*>(raw + Cfg::R_Z)[i]);
+                dyv = to_f32<TIO>(reinterpret_cast<const TIO*>(raw + Cfg::R_Y)[i]);
+            }
+        } else if (in) {
+            uu = to_f32<TIO>(gu[b * p.u_b + t * p.u_l + d]);
+            rr = to_f32<TIO>(gd[b * p.d_b + t * p.d_l + d]);
+            if (full) {
+                if (gz) zv = to_f32<TIO>(gz[b * p.z_b + t * p.z_l + d]);
+                dyv = to_f32<TIO>(gy[(static_cast<int64_t>(b) * p.L + t) * p.Dm + d]);
             }
         }
-        sm[Cfg::OFF_U + i] = uu;
-        sm[Cfg::OFF_DEL + i] = del;
+        rr += bias_c;
+        sm[Cfg::OFF_U + i] = in ? uu : 0.f;
+        sm[Cfg::OFF_DEL + i] = in ? softplus(rr) : 0.f;
         if (full) {
-            sm[Cfg::OFF_SIG + i] = sig;
-            sm[Cfg::OFF_DYH + i] = dyh;
-            sm[Cfg::OFF_DYG + i] = dyg;
+            float g = 1.f, dg = 0.f;
+            if (gz) {
+                const float s = sigmoid_f(zv);
+                g = zv * s;
+                dg = s * fmaf(zv, 1.f - s, 1.f);
+            }
+            sm[Cfg::OFF_SIG + i] = in ? sigmoid_f(rr) : 0.f;
+            sm[Cfg::OFF_DYH + i] = in ? dyv * g : 0.f;
+            sm[Cfg::OFF_DYG + i] = in ? dyv * dg : 0.f;
         }
     }
-    const TIO* Bm = static_cast<const TIO*>(p.Bm);
-    const TIO* Cm = static_cast<const TIO*>(p.Cm);
-#pragma unroll 4
+    const TIO* gB = static_cast<const TIO*>(p.Bm);
+    const TIO* gC = static_cast<const TIO*>(p.Cm);
+#pragma unroll 2
     for (int i = threadIdx.x; i < kBT * Cfg::NS; i += Cfg::THREADS) {
         const int r = i / Cfg::NS, n = i % Cfg::NS;
-        const int64_t t = t0 + r;
+        const int t = t0 + r;
         const bool in = t < p.L && n < p.N;
-        sm[Cfg::OFF_B + i] = in ? to_f32<TIO>(Bm[b * p.B_b + t * p.B_l + n]) : 0.f;
-        if (full) {
-            sm[Cfg::OFF_C + i] = in ? to_f32<TIO>(Cm[b * p.C_b + t * p.C_l + n]) : 0.f;
-            sm[Cfg::OFF_DB + i] = 0.f;
-            sm[Cfg::OFF_DC + i] = 0.f;
+        float bv = 0.f, cv = 0.f;
+        if constexpr (TMA) {
+            bv = to_f32<TIO>(reinterpret_cast<const TIO*>(raw + Cfg::R_B)[i]);
+            if (full) cv = to_f32<TIO>(reinterpret_cast<const TIO*>(raw + Cfg::R_C)[i]);
+        } else if (in) {
+            bv = to_f32<TIO>(gB[b * p.B_b + t * p.B_l + n]);
+            if (full) cv = to_f32<TIO>(gC[b * p.C_b + t * p.C_l + n]);
         }
+        sm[Cfg::OFF_B + i] = in ? bv : 0.f;
+        if (full) sm[Cfg::OFF_C + i] = in ? cv : 0.f;
     }
 }
 
@@ -171,12 +202,20 @@ __device__ __forceinline__ float channel_reduce_scatter(const float (&v)[8], int
     return r;
 }
 
-template <typename TIO, int NS>
-__global__ void __launch_bounds__(BwdCfg<TIO, NS>::THREADS) ss_bwd_kernel(const BwdParams p) {
+__device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
+__device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
+
+template <typename TIO, int NS, bool TMA>
+__global__ void __launch_bounds__(BwdCfg<TIO, NS>::THREADS)
+ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
     using Cfg = BwdCfg<TIO, NS>;
     constexpr int CPW = Cfg::CPW;
     constexpr int NSUB = kBT / kBS;
-    extern __shared__ __align__(16) float sm[];
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* raw = smem;
+    float* sm = reinterpret_cast<float*>(smem + Cfg::RAW_BYTES);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Cfg::BAR_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::BAR_OFF + 8);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int j = lane / CPW, c = lane % CPW;
     const int cw = warp * CPW + c;               // channel within the tile
@@ -186,12 +225,53 @@ __global__ void __launch_bounds__(BwdCfg<TIO, NS>::THREADS) ss_bwd_kernel(const 
     const int d = d0 + cw;
     const bool d_ok = d < p.Dm;
     const int n0 = j * 4;
-    float An[4], A2[4];                          // A = -exp(A_log) and A·log2(e)
+    const int dp = d0 + tid % kBW;               // the channel this thread prepares
+    const float bias_c = (p.bias && dp < p.Dm) ? p.bias[dp] : 0.f;
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        if constexpr (TMA) {
+            mbar_init(bar, 1);
+            mbar_fence_init();
+        }
+    }
+    for (int i = tid; i < 2 * Cfg::XN; i += Cfg::THREADS) sm[Cfg::OFF_DB + i] = 0.f;
+    __syncthreads();
+    // one TMA batch in flight at a time: the next chunk's tiles land while this chunk is processed
+    auto issue = [&](int chunk, bool full) {
+        const int t0 = chunk * kBT;
+        const bool hz = full && p.z != nullptr;
+        const uint32_t bytes = (full ? (hz ? 4u : 3u) : 2u) * Cfg::RAW_X + (full ? 2u : 1u) * Cfg::RAW_N;
+        mbar_expect_tx(bar, bytes);
+        tma_load_3d(raw + Cfg::R_U, &maps.u, bar, d0, t0, b);
+        tma_load_3d(raw + Cfg::R_D, &maps.delta, bar, d0, t0, b);
+        tma_load_3d(raw + Cfg::R_B, &maps.B, bar, 0, t0, b);
+        if (full) {
+            if (hz) tma_load_3d(raw + Cfg::R_Z, &maps.z, bar, d0, t0, b);
+            tma_load_3d(raw + Cfg::R_Y, &maps.dy, bar, d0, t0, b);
+            tma_load_3d(raw + Cfg::R_C, &maps.C, bar, 0, t0, b);
+        }
+    };
+    uint32_t phase = 0;
+    auto wait_staged = [&]() {
+        if constexpr (TMA) {
+            mbar_wait_bounded(bar, phase, abort_flag, p.err);
+            phase ^= 1u;
+        }
+    };
+    if (TMA && tid == 0) issue(0, false);
+
+    float2 A2[2], An[2];                         // A·log2(e) and A = -exp(A_log), state pairs
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int n = n0 + q;
-        An[q] = (d_ok && n < p.N) ? -expf(p.A_log[static_cast<int64_t>(d) * p.N + n]) : 0.f;
-        A2[q] = An[q] * kLog2e;
+    for (int q = 0; q < 2; ++q) {
+        float a[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int n = n0 + 2 * q + e;
+            a[e] = (d_ok && n < p.N) ? -expf(p.A_log[static_cast<int64_t>(d) * p.N + n]) : 0.f;
+        }
+        An[q] = f2(a[0], a[1]);
+        A2[q] = f2(a[0] * kLog2e, a[1] * kLog2e);
     }
     const float Dd = (d_ok && p.Dv) ? p.Dv[d] : 0.f;
     float* ck = p.ckpt + static_cast<int64_t>(tile) * p.nchunks * NSUB * kBW * NS;
@@ -200,98 +280,127 @@ __global__ void __launch_bounds__(BwdCfg<TIO, NS>::THREADS) ss_bwd_kernel(const 
     };
     const int64_t row = static_cast<int64_t>(b) * p.Dm + d;
 
-    auto fold = [&](float (&h)[4], int r) {      // one step of the forward fold (chunk row r)
+    auto fold = [&](float2 (&h)[2], int r) {     // one step of the forward recurrence (chunk row r)
         const float del = sm[Cfg::OFF_DEL + r * kBW + cw];
-        const float du = del * sm[Cfg::OFF_U + r * kBW + cw];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) h[q] = fmaf(ex2(del * A2[q]), h[q], du * sm[Cfg::OFF_B + r * NS + n0 + q]);
+        const float2 du = f2(del * sm[Cfg::OFF_U + r * kBW + cw]);
+        const float4 Bv = *reinterpret_cast<const float4*>(&sm[Cfg::OFF_B + r * NS + n0]);
+        const float2 e0 = mul2(f2(del), A2[0]), e1 = mul2(f2(del), A2[1]);
+        h[0] = fma2(f2(ex2(e0.x), ex2(e0.y)), h[0], mul2(du, f2(Bv.x, Bv.y)));
+        h[1] = fma2(f2(ex2(e1.x), ex2(e1.y)), h[1], mul2(du, f2(Bv.z, Bv.w)));
     };
 
     // ---- pass 1: forward, the state at every sub-chunk start
-    float h[4];
+    float2 h[2];
+    {
+        float v[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) h[q] = (p.h0 && d_ok && n0 + q < p.N) ? p.h0[row * p.N + n0 + q] : 0.f;
+        for (int q = 0; q < 4; ++q) v[q] = (p.h0 && d_ok && n0 + q < p.N) ? p.h0[row * p.N + n0 + q] : 0.f;
+        h[0] = f2(v[0], v[1]);
+        h[1] = f2(v[2], v[3]);
+    }
     for (int ch = 0; ch < p.nchunks; ++ch) {
-        __syncthreads();                         // the previous chunk's shared reads are done
-        bwd_fill<Cfg, TIO>(sm, p, b, d0, ch, false);
-        __syncthreads();
+        wait_staged();
+        bwd_prepare<Cfg, TIO, TMA>(sm, raw, p, b, d0, ch, false, bias_c);
+        __syncthreads();                         // staged tiles consumed; the chunk's arrays are ready
+        if (TMA && tid == 0 && !*abort_flag) {
+            if (ch + 1 < p.nchunks) issue(ch + 1, false);
+            else issue(p.nchunks - 1, true);     // pass 2 starts from the last chunk
+        }
 #pragma unroll 1
         for (int k = 0; k < NSUB; ++k) {
-            __stcg(reinterpret_cast<float4*>(ckpt_at(ch, k)), make_float4(h[0], h[1], h[2], h[3]));
+            __stcg(reinterpret_cast<float4*>(ckpt_at(ch, k)), make_float4(h[0].x, h[0].y, h[1].x, h[1].y));
+#pragma unroll 4
             for (int r = k * kBS; r < (k + 1) * kBS; ++r) fold(h, r);
         }
+        __syncthreads();                         // the chunk's arrays are no longer read
     }
 
     // ---- pass 2: reverse
-    float mu[4];                                 // a_{t+1} λ_{t+1}: what step t receives
+    float2 mu[2];                                // a_{t+1} λ_{t+1}: what step t receives
+    {
+        float v[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) mu[q] = (p.dlast && d_ok && n0 + q < p.N) ? p.dlast[row * p.N + n0 + q] : 0.f;
-    float dA[4] = {0.f, 0.f, 0.f, 0.f}, dDacc = 0.f, dbacc = 0.f;
+        for (int q = 0; q < 4; ++q) v[q] = (p.dlast && d_ok && n0 + q < p.N) ? p.dlast[row * p.N + n0 + q] : 0.f;
+        mu[0] = f2(v[0], v[1]);
+        mu[1] = f2(v[2], v[3]);
+    }
+    float2 dA[2] = {f2(0.f), f2(0.f)};
+    float dDacc = 0.f, dbacc = 0.f;
     TIO* g_du = static_cast<TIO*>(p.du);
     TIO* g_dd = static_cast<TIO*>(p.ddelta);
     TIO* g_dz = static_cast<TIO*>(p.dz);
     for (int ch = p.nchunks - 1; ch >= 0; --ch) {
+        wait_staged();
+        bwd_prepare<Cfg, TIO, TMA>(sm, raw, p, b, d0, ch, true, bias_c);
         __syncthreads();
-        bwd_fill<Cfg, TIO>(sm, p, b, d0, ch, true);
-        __syncthreads();
+        if (TMA && tid == 0 && ch > 0 && !*abort_flag) issue(ch - 1, true);
 #pragma unroll 1
         for (int k = NSUB - 1; k >= 0; --k) {
-            float H[kBS][4], yh[kBS], hb0[4];
+            float2 H[kBS][2], hb0[2];
+            float yh[kBS];
             {
                 const float4 v = __ldcg(reinterpret_cast<const float4*>(ckpt_at(ch, k)));
-                hb0[0] = v.x; hb0[1] = v.y; hb0[2] = v.z; hb0[3] = v.w;
+                hb0[0] = f2(v.x, v.y);
+                hb0[1] = f2(v.z, v.w);
             }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) h[q] = hb0[q];
+            h[0] = hb0[0];
+            h[1] = hb0[1];
+            // refold the sub-chunk's states from its checkpoint, with ŷ = Σ C h + D u
 #pragma unroll
             for (int i = 0; i < kBS; ++i) {
                 const int r = k * kBS + i;
                 fold(h, r);
-                float yp = 0.f;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    H[i][q] = h[q];
-                    yp = fmaf(sm[Cfg::OFF_C + r * NS + n0 + q], h[q], yp);
-                }
-                yh[i] = fmaf(Dd, sm[Cfg::OFF_U + r * kBW + cw], channel_sum<CPW>(yp));
+                H[i][0] = h[0];
+                H[i][1] = h[1];
+                const float4 Cv = *reinterpret_cast<const float4*>(&sm[Cfg::OFF_C + r * NS + n0]);
+                const float2 yp = fma2(h[1], f2(Cv.z, Cv.w), mul2(h[0], f2(Cv.x, Cv.y)));
+                yh[i] = fmaf(Dd, sm[Cfg::OFF_U + r * kBW + cw], channel_sum<CPW>(yp.x + yp.y));
             }
+            // the adjoint recurrence backwards over them
 #pragma unroll
             for (int i = kBS - 1; i >= 0; --i) {
                 const int r = k * kBS + i;
-                const int64_t t = static_cast<int64_t>(ch) * kBT + r;
+                const int t = ch * kBT + r;
                 const float del = sm[Cfg::OFF_DEL + r * kBW + cw];
                 const float ut = sm[Cfg::OFF_U + r * kBW + cw];
                 const float dyh = sm[Cfg::OFF_DYH + r * kBW + cw];
-                const float dut_in = del * ut;
-                float dup = 0.f, ddp = 0.f, bc[8];
+                const float4 Bv = *reinterpret_cast<const float4*>(&sm[Cfg::OFF_B + r * NS + n0]);
+                const float4 Cv = *reinterpret_cast<const float4*>(&sm[Cfg::OFF_C + r * NS + n0]);
+                const float2 B2[2] = {f2(Bv.x, Bv.y), f2(Bv.z, Bv.w)};
+                const float2 C2[2] = {f2(Cv.x, Cv.y), f2(Cv.z, Cv.w)};
+                const float2 dut = f2(del * ut);
+                float2 s1 = f2(0.f), slb = f2(0.f), bcB[2], bcC[2];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float Bq = sm[Cfg::OFF_B + r * NS + n0 + q];
-                    const float l = fmaf(sm[Cfg::OFF_C + r * NS + n0 + q], dyh, mu[q]);
-                    const float a = ex2(del * A2[q]);
-                    const float hp = i > 0 ? H[i - 1][q] : hb0[q];
-                    bc[q] = l * dut_in;                  // dB of state n0 + q
-                    bc[4 + q] = dyh * H[i][q];           // dC
-                    dup = fmaf(l * del, Bq, dup);
-                    ddp = fmaf(l, fmaf(An[q] * a, hp, Bq * ut), ddp);
-                    dA[q] = fmaf(l * del * a, hp, dA[q]);
-                    mu[q] = a * l;
+                for (int q = 0; q < 2; ++q) {
+                    const float2 l = fma2(C2[q], f2(dyh), mu[q]);          // λ_t
+                    const float2 e = mul2(f2(del), A2[q]);
+                    const float2 a = f2(ex2(e.x), ex2(e.y));             // a_t
+                    const float2 hp = i > 0 ? H[i - 1][q] : hb0[q];       // h_{t-1}
+                    mu[q] = mul2(a, l);
+                    const float2 w = mul2(mu[q], hp);                    // λ_t a_t h_{t-1}
+                    dA[q] = fma2(f2(del), w, dA[q]);
+                    s1 = fma2(An[q], w, s1);
+                    slb = fma2(l, B2[q], slb);
+                    bcB[q] = mul2(l, dut);                               // dB of the pair
+                    bcC[q] = mul2(f2(dyh), H[i][q]);                     // dC of the pair
                 }
                 {
                     // the tile's sums over channels: reduce over the warp's channel lanes,
                     // then one shared atomic per lane (the warps of the tile add up there)
+                    const float bc[8] = {bcB[0].x, bcB[0].y, bcB[1].x, bcB[1].y,
+                                         bcC[0].x, bcC[0].y, bcC[1].x, bcC[1].y};
                     const float sum = channel_reduce_scatter<CPW>(bc, c);
                     if (c < 8) {
                         const int kk = c & 7;
                         atomicAdd(&sm[(kk < 4 ? Cfg::OFF_DB : Cfg::OFF_DC) + r * NS + n0 + (kk & 3)], sum);
                     }
                 }
-                dup = channel_sum<CPW>(dup);
-                ddp = channel_sum<CPW>(ddp);
+                const float S1 = channel_sum<CPW>(s1.x + s1.y);          // Σ_n A λ a h_{t-1}
+                const float SLB = channel_sum<CPW>(slb.x + slb.y);       // Σ_n λ B
                 if (j == 0 && d_ok && t < p.L) {
-                    const float ddel = ddp * sm[Cfg::OFF_SIG + r * kBW + cw];
+                    const float ddel = fmaf(ut, SLB, S1) * sm[Cfg::OFF_SIG + r * kBW + cw];
                     const int64_t o = (static_cast<int64_t>(b) * p.L + t) * p.Dm + d;
-                    g_du[o] = from_f32<TIO>(fmaf(Dd, dyh, dup));
+                    g_du[o] = from_f32<TIO>(fmaf(Dd, dyh, del * SLB));
                     g_dd[o] = from_f32<TIO>(ddel);
                     if (p.z) g_dz[o] = from_f32<TIO>(sm[Cfg::OFF_DYG + r * kBW + cw] * yh[i]);
                     dDacc = fmaf(dyh, ut, dDacc);
@@ -299,24 +408,29 @@ __global__ void __launch_bounds__(BwdCfg<TIO, NS>::THREADS) ss_bwd_kernel(const 
                 }
             }
         }
-        __syncthreads();                         // every shared atomic of the chunk is done
-        for (int i = tid; i < kBT * NS; i += Cfg::THREADS) {
+        __syncthreads();                         // every shared atomic and read of the chunk is done
+        for (int i = tid; i < Cfg::XN; i += Cfg::THREADS) {
             const int r = i / NS, n = i % NS;
-            const int64_t t = static_cast<int64_t>(ch) * kBT + r;
+            const int t = ch * kBT + r;
+            const float vb = sm[Cfg::OFF_DB + i], vc = sm[Cfg::OFF_DC + i];
+            sm[Cfg::OFF_DB + i] = 0.f;
+            sm[Cfg::OFF_DC + i] = 0.f;
             if (t < p.L && n < p.N) {
                 const int64_t o = (static_cast<int64_t>(b) * p.L + t) * p.N + n;
-                atomicAdd(p.dB + o, sm[Cfg::OFF_DB + i]);
-                atomicAdd(p.dC + o, sm[Cfg::OFF_DC + i]);
+                atomicAdd(p.dB + o, vb);
+                atomicAdd(p.dC + o, vc);
             }
         }
     }
     if (d_ok) {
+        const float m4[4] = {mu[0].x, mu[0].y, mu[1].x, mu[1].y};
+        const float a4[4] = {dA[0].x * An[0].x, dA[0].y * An[0].y, dA[1].x * An[1].x, dA[1].y * An[1].y};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int n = n0 + q;
             if (n < p.N) {
-                if (p.dh0) p.dh0[row * p.N + n] = mu[q];
-                atomicAdd(p.dA_log + static_cast<int64_t>(d) * p.N + n, dA[q] * An[q]);
+                if (p.dh0) p.dh0[row * p.N + n] = m4[q];
+                atomicAdd(p.dA_log + static_cast<int64_t>(d) * p.N + n, a4[q]);
             }
         }
         if (j == 0) {
@@ -326,21 +440,27 @@ __global__ void __launch_bounds__(BwdCfg<TIO, NS>::THREADS) ss_bwd_kernel(const 
     }
 }
 
-template <typename TIO, int NS>
-cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
+template <typename TIO, int NS, bool TMA>
+cudaError_t launch_bwd_t(const BwdParams& p, const BwdMaps& m, cudaStream_t stream) {
     using Cfg = BwdCfg<TIO, NS>;
-    cudaError_t e = cudaFuncSetAttribute(ss_bwd_kernel<TIO, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(ss_bwd_kernel<TIO, NS, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::SMEM);
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(p.batch) * static_cast<unsigned>(p.tiles_per_batch);
-    ss_bwd_kernel<TIO, NS><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(p);
+    ss_bwd_kernel<TIO, NS, TMA><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(p, m);
     return cudaGetLastError();
 }
 
 template <typename TIO>
-cudaError_t launch_bwd(const BwdParams& p, int ns, cudaStream_t stream) {
-    if (ns == 4) return launch_bwd_t<TIO, 4>(p, stream);
-    if (ns == 8) return launch_bwd_t<TIO, 8>(p, stream);
-    return launch_bwd_t<TIO, 16>(p, stream);
+cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, int ns, bool tma, cudaStream_t stream) {
+    if (tma) {
+        if (ns == 4) return launch_bwd_t<TIO, 4, true>(p, m, stream);
+        if (ns == 8) return launch_bwd_t<TIO, 8, true>(p, m, stream);
+        return launch_bwd_t<TIO, 16, true>(p, m, stream);
+    }
+    if (ns == 4) return launch_bwd_t<TIO, 4, false>(p, m, stream);
+    if (ns == 8) return launch_bwd_t<TIO, 8, false>(p, m, stream);
+    return launch_bwd_t<TIO, 16, false>(p, m, stream);
 }
 
 int bwd_ns(int64_t N) { return N <= 4 ? 4 : N <= 8 ? 8 : 16; }
@@ -467,7 +587,27 @@ extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* d
     p.nchunks = static_cast<int>((L + kBT - 1) / kBT);
     p.tiles_per_batch = static_cast<int>((Dm + kBW - 1) / kBW);
     if (static_cast<int64_t>(p.batch) * p.tiles_per_batch > INT32_MAX) return SS_ERR_UNSUPPORTED;
+    p.err = device_error_word();
+    // staged by TMA when every tensor allows it, else by plain loads
     const int ns = bwd_ns(N);
-    const cudaError_t e = bf16 ? launch_bwd<__nv_bfloat16>(p, ns, stream) : launch_bwd<float>(p, ns, stream);
+    const int ft = g_force_bwd_tma.load();
+    BwdMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    bool tma = ft != 0 && (ns * es) % 16 == 0;
+    if (tma) {
+        tma = make_tile_map(&maps.u, u, bf16, Dm, L, batch, s.u_l, s.u_b, kBW, kBT) &&
+              make_tile_map(&maps.delta, delta_raw, bf16, Dm, L, batch, s.delta_l, s.delta_b, kBW, kBT) &&
+              (!z || make_tile_map(&maps.z, z, bf16, Dm, L, batch, s.z_l, s.z_b, kBW, kBT)) &&
+              make_tile_map(&maps.dy, dy, bf16, Dm, L, batch, Dm, L * Dm, kBW, kBT) &&
+              make_tile_map(&maps.B, B, bf16, N, L, batch, s.B_l, s.B_b, ns, kBT) &&
+              make_tile_map(&maps.C, C, bf16, N, L, batch, s.C_l, s.C_b, ns, kBT);
+    }
+    if (ft == 1 && !tma) return SS_ERR_UNSUPPORTED;
+    const cudaError_t e = bf16 ? launch_bwd<__nv_bfloat16>(p, maps, ns, tma, stream)
+                               : launch_bwd<float>(p, maps, ns, tma, stream);
     return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
+
+// Internal test hook (not in the public header): -1 automatic, 0 plain-load staging, 1 TMA
+// staging (SS_ERR_UNSUPPORTED where the tensors rule it out).  Returns the previous setting.
+extern "C" int ss__force_bwd_tma(int v) { return g_force_bwd_tma.exchange(v < 0 ? -1 : v > 0 ? 1 : 0); }

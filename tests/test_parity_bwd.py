@@ -80,19 +80,80 @@ def check(w, a, dy, h0, dlast, what=""):
     return got, ref
 
 
-@pytest.mark.parametrize("L", [1, 5, 63, 64, 65, 200])
-def test_bwd_lengths(L):
-    check(*problem(2, L, 40, 16, seed=L), what=f"L={L}")
+class staging:
+    """Pin how ss_bwd stages its tiles: -1 automatic, 0 plain loads, 1 TMA."""
+
+    def __init__(self, v):
+        self.v = v
+
+    def __enter__(self):
+        lib = ss.lib()
+        lib.ss__force_bwd_tma.argtypes = [ctypes.c_int]
+        self.prev = lib.ss__force_bwd_tma(self.v)
+
+    def __exit__(self, *a):
+        ss.lib().ss__force_bwd_tma(self.prev)
 
 
+STAGINGS = pytest.mark.parametrize("stage", [-1, 0], ids=["auto", "plain"])
+
+
+@STAGINGS
+@pytest.mark.parametrize("L", [1, 5, 31, 32, 33, 63, 64, 65, 200])
+def test_bwd_lengths(L, stage):
+    with staging(stage):
+        check(*problem(2, L, 40, 16, seed=L), what=f"L={L}")
+
+
+@STAGINGS
 @pytest.mark.parametrize("N", [1, 3, 4, 5, 8, 12, 16])
-def test_bwd_state_counts(N):
-    check(*problem(2, 130, 72, N, seed=20 + N), what=f"N={N}")
+def test_bwd_state_counts(N, stage):
+    with staging(stage):
+        check(*problem(2, 130, 72, N, seed=20 + N), what=f"N={N}")
 
 
+@STAGINGS
 @pytest.mark.parametrize("Dm", [1, 31, 33, 100])
-def test_bwd_channel_counts(Dm):
-    check(*problem(3, 97, Dm, 16, seed=40 + Dm), what=f"Dm={Dm}")
+def test_bwd_channel_counts(Dm, stage):
+    with staging(stage):
+        check(*problem(3, 97, Dm, 16, seed=40 + Dm), what=f"Dm={Dm}")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bwd_tma_staging_taken(io):
+    """Contiguous inputs with 16-byte rows are staged by TMA (forcing it is accepted), and
+    both stagings give the same gradients up to the atomics' summation order."""
+    w, a, dy, h0, dlast = problem(2, 200, 64, 16, io=io, seed=70)
+    with staging(1):
+        g1 = run(w, a, dy, h0, dlast)
+    with staging(0):
+        g0 = run(w, a, dy, h0, dlast)
+    for k in ("du", "ddelta_raw", "dz", "dh0"):
+        np.testing.assert_array_equal(g1[k], g0[k], err_msg=k)
+    for k in SUMS:
+        assert rel_l2(g1[k], g0[k]) <= 1e-6, k
+
+
+def test_bwd_strided_inputs_fall_back_to_plain_staging():
+    """u, δ, z as views with a row pitch of Dm + 1 floats (not a multiple of 16 bytes): TMA is
+    refused when forced, and the automatic choice stages them with plain loads."""
+    w, a, dy, h0, dlast = problem(2, 150, 48, 16, seed=71)
+    wide = {k: np.zeros((2, 150, 49), np.float32) for k in ("u", "delta_raw", "z")}
+    t = {}
+    for k in wide:
+        wide[k][..., :48] = a[k]
+        t[k] = torch.from_numpy(wide[k]).cuda()[..., :48]
+    args = (f32dev(dy), t["u"], t["delta_raw"], f32dev(a["delta_bias"]), f32dev(a["A_log"]), f32dev(a["B"]),
+            f32dev(a["C"]), f32dev(a["D"]), t["z"])
+    with staging(1):
+        with pytest.raises(ss.SelscanError):
+            ss.ss_bwd(*args, h0=f32dev(h0), dlast=f32dev(dlast))
+    g = ss.ss_bwd(*args, h0=f32dev(h0), dlast=f32dev(dlast))
+    torch.cuda.synchronize()
+    ref = reference(a, dy, h0, dlast)
+    for k in ELEMENTWISE + SUMS:
+        e = rel_l2(to_host(g[k]), ref[k])
+        assert e <= (GRAD_REL_L2 if k in ELEMENTWISE else SUM_REL_L2), (k, e)
 
 
 @pytest.mark.parametrize("opts", ["no_gate", "no_h0", "no_dlast", "plain"])
@@ -102,8 +163,11 @@ def test_bwd_optional_inputs(opts):
     check(*problem(2, 150, 48, 16, seed=50, **kw), what=opts)
 
 
-def test_bwd_bf16():
-    check(*problem(2, 300, 64, 16, io="bf16", seed=60), what="bf16")
+@STAGINGS
+@pytest.mark.parametrize("N", [4, 16])
+def test_bwd_bf16(N, stage):
+    with staging(stage):
+        check(*problem(2, 300, 64, N, io="bf16", seed=60 + N), what="bf16")
 
 
 def test_bwd_long_sequence():
