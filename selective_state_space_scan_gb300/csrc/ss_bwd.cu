@@ -70,9 +70,10 @@ struct BwdParams {
     int batch, L, Dm, N, nchunks, tiles_per_batch;
 };
 
-// TMA descriptors of the staged inputs: [T][W] boxes of u, δ, z, dy and [T][NS] boxes of B, C.
+// TMA descriptors: [T][W] boxes of u, δ, z, dy (loaded) and du, dδ, dz (stored); [T][NS] boxes
+// of B, C (loaded).
 struct BwdMaps {
-    CUtensorMap u, delta, z, dy, B, C;
+    CUtensorMap u, delta, z, dy, B, C, du, ddelta, dz;
 };
 
 template <typename TIO, int NS_>
@@ -89,13 +90,18 @@ struct BwdCfg {
     static constexpr int R_U = 0, R_D = RAW_X, R_Z = 2 * RAW_X, R_Y = 3 * RAW_X, R_B = 4 * RAW_X,
                          R_C = 4 * RAW_X + RAW_N;
     static constexpr int RAW_BYTES = 4 * RAW_X + 2 * RAW_N;
-    // fp32 arrays the chunk is processed from (float offsets after the staged tiles)
+    // the chunk's du, dδ, dz tiles, io dtype, as a TMA store reads them (bytes after the staged tiles)
+    static constexpr int O_DU = RAW_BYTES, O_DD = O_DU + RAW_X, O_DZ = O_DD + RAW_X;
+    static constexpr int DER_BYTE = O_DZ + RAW_X;
+    // fp32 arrays the chunk is processed from (float offsets from DER_BYTE); the chunk's dB and
+    // dC sums interleaved per step ([T][2][NS]), so that one step's shared atomics of a warp hit
+    // 2·NS consecutive words
     static constexpr int X = kBT * kBW, XN = kBT * NS;
     static constexpr int OFF_U = 0, OFF_DEL = X, OFF_SIG = 2 * X, OFF_DYH = 3 * X, OFF_DYG = 4 * X;
-    static constexpr int OFF_B = 5 * X, OFF_C = OFF_B + XN, OFF_DB = OFF_C + XN, OFF_DC = OFF_DB + XN;
-    static constexpr int BAR_OFF = RAW_BYTES + (OFF_DC + XN) * 4;
+    static constexpr int OFF_B = 5 * X, OFF_C = OFF_B + XN, OFF_BC = OFF_C + XN;
+    static constexpr int BAR_OFF = DER_BYTE + (OFF_BC + 2 * XN) * 4;
     static constexpr int SMEM = BAR_OFF + 16;    // the mbarrier, then the abort flag
-    static_assert(RAW_X % 128 == 0 && RAW_N % 16 == 0, "TMA destinations stay 16-byte aligned");
+    static_assert(RAW_X % 128 == 0 && RAW_N % 128 == 0, "TMA tiles stay 128-byte aligned");
 };
 
 __device__ __forceinline__ float sigmoid_f(float x) { return rcp_approx(1.f + ex2(-x * kLog2e)); }
@@ -184,19 +190,19 @@ __device__ __forceinline__ float channel_sum(float v) {
 template <int CPW>
 __device__ __forceinline__ float channel_reduce_scatter(const float (&v)[8], int c) {
     const bool b2 = (c & 4) != 0, b1 = (c & 2) != 0, b0 = (c & 1) != 0;
-    float w4[4], w2[2];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float keep = b2 ? v[4 + k] : v[k], send = b2 ? v[k] : v[4 + k];
-        w4[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
+    float2 w4[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-        const float keep = b1 ? w4[2 + k] : w4[k], send = b1 ? w4[k] : w4[2 + k];
-        w2[k] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        const int lo = 2 * k, hi = 4 + 2 * k;
+        const float2 keep = b2 ? make_float2(v[hi], v[hi + 1]) : make_float2(v[lo], v[lo + 1]);
+        const float2 send = b2 ? make_float2(v[lo], v[lo + 1]) : make_float2(v[hi], v[hi + 1]);
+        w4[k] = __fadd2_rn(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 4),
+                                             __shfl_xor_sync(0xffffffffu, send.y, 4)));
     }
-    const float keep = b0 ? w2[1] : w2[0], send = b0 ? w2[0] : w2[1];
-    float r = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+    const float2 keep = b1 ? w4[1] : w4[0], send = b1 ? w4[0] : w4[1];
+    const float2 w2 = __fadd2_rn(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 2),
+                                                   __shfl_xor_sync(0xffffffffu, send.y, 2)));
+    float r = (b0 ? w2.y : w2.x) + __shfl_xor_sync(0xffffffffu, b0 ? w2.x : w2.y, 1);
 #pragma unroll
     for (int off = 8; off < CPW; off <<= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
     return r;
@@ -213,7 +219,10 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
     constexpr int NSUB = kBT / kBS;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* raw = smem;
-    float* sm = reinterpret_cast<float*>(smem + Cfg::RAW_BYTES);
+    float* sm = reinterpret_cast<float*>(smem + Cfg::DER_BYTE);
+    TIO* o_du = reinterpret_cast<TIO*>(smem + Cfg::O_DU);
+    TIO* o_dd = reinterpret_cast<TIO*>(smem + Cfg::O_DD);
+    TIO* o_dz = reinterpret_cast<TIO*>(smem + Cfg::O_DZ);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Cfg::BAR_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::BAR_OFF + 8);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -235,7 +244,7 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
             mbar_fence_init();
         }
     }
-    for (int i = tid; i < 2 * Cfg::XN; i += Cfg::THREADS) sm[Cfg::OFF_DB + i] = 0.f;
+    for (int i = tid; i < 2 * Cfg::XN; i += Cfg::THREADS) sm[Cfg::OFF_BC + i] = 0.f;
     __syncthreads();
     // one TMA batch in flight at a time: the next chunk's tiles land while this chunk is processed
     auto issue = [&](int chunk, bool full) {
@@ -332,6 +341,7 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
     for (int ch = p.nchunks - 1; ch >= 0; --ch) {
         wait_staged();
         bwd_prepare<Cfg, TIO, TMA>(sm, raw, p, b, d0, ch, true, bias_c);
+        if (TMA && tid == 0) tma_store_wait_read();   // the previous chunk's gradient tiles are read out
         __syncthreads();
         if (TMA && tid == 0 && ch > 0 && !*abort_flag) issue(ch - 1, true);
 #pragma unroll 1
@@ -392,29 +402,46 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
                     const float sum = channel_reduce_scatter<CPW>(bc, c);
                     if (c < 8) {
                         const int kk = c & 7;
-                        atomicAdd(&sm[(kk < 4 ? Cfg::OFF_DB : Cfg::OFF_DC) + r * NS + n0 + (kk & 3)], sum);
+                        atomicAdd(&sm[Cfg::OFF_BC + r * 2 * NS + (kk < 4 ? 0 : NS) + n0 + (kk & 3)], sum);
                     }
                 }
                 const float S1 = channel_sum<CPW>(s1.x + s1.y);          // Σ_n A λ a h_{t-1}
                 const float SLB = channel_sum<CPW>(slb.x + slb.y);       // Σ_n λ B
-                if (j == 0 && d_ok && t < p.L) {
-                    const float ddel = fmaf(ut, SLB, S1) * sm[Cfg::OFF_SIG + r * kBW + cw];
+                // (steps past L and channels past Dm contribute zeros to the sums)
+                const float ddel = fmaf(ut, SLB, S1) * sm[Cfg::OFF_SIG + r * kBW + cw];
+                const float duv = fmaf(Dd, dyh, del * SLB);
+                const float dzv = p.z ? sm[Cfg::OFF_DYG + r * kBW + cw] * yh[i] : 0.f;
+                dDacc = fmaf(dyh, ut, dDacc);
+                dbacc += ddel;
+                if constexpr (TMA) {
+                    // into the chunk's gradient tiles (the channel's LPC lanes write the same value)
+                    o_du[r * kBW + cw] = from_f32<TIO>(duv);
+                    o_dd[r * kBW + cw] = from_f32<TIO>(ddel);
+                    if (p.z) o_dz[r * kBW + cw] = from_f32<TIO>(dzv);
+                } else if (j == 0 && d_ok && t < p.L) {
                     const int64_t o = (static_cast<int64_t>(b) * p.L + t) * p.Dm + d;
-                    g_du[o] = from_f32<TIO>(fmaf(Dd, dyh, del * SLB));
+                    g_du[o] = from_f32<TIO>(duv);
                     g_dd[o] = from_f32<TIO>(ddel);
-                    if (p.z) g_dz[o] = from_f32<TIO>(sm[Cfg::OFF_DYG + r * kBW + cw] * yh[i]);
-                    dDacc = fmaf(dyh, ut, dDacc);
-                    dbacc += ddel;
+                    if (p.z) g_dz[o] = from_f32<TIO>(dzv);
                 }
             }
         }
+        if constexpr (TMA) tma_store_fence();    // the gradient tiles' writes, before the TMA store
         __syncthreads();                         // every shared atomic and read of the chunk is done
+        if (TMA && tid == 0) {
+            const int t0 = ch * kBT;
+            tma_store_3d(&maps.du, o_du, d0, t0, b);
+            tma_store_3d(&maps.ddelta, o_dd, d0, t0, b);
+            if (p.z) tma_store_3d(&maps.dz, o_dz, d0, t0, b);
+            tma_store_commit();
+        }
         for (int i = tid; i < Cfg::XN; i += Cfg::THREADS) {
             const int r = i / NS, n = i % NS;
             const int t = ch * kBT + r;
-            const float vb = sm[Cfg::OFF_DB + i], vc = sm[Cfg::OFF_DC + i];
-            sm[Cfg::OFF_DB + i] = 0.f;
-            sm[Cfg::OFF_DC + i] = 0.f;
+            float* bc = &sm[Cfg::OFF_BC + r * 2 * NS + n];
+            const float vb = bc[0], vc = bc[NS];
+            bc[0] = 0.f;
+            bc[NS] = 0.f;
             if (t < p.L && n < p.N) {
                 const int64_t o = (static_cast<int64_t>(b) * p.L + t) * p.N + n;
                 atomicAdd(p.dB + o, vb);
@@ -422,6 +449,7 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
             }
         }
     }
+    if (TMA && tid == 0) tma_store_wait_all();
     if (d_ok) {
         const float m4[4] = {mu[0].x, mu[0].y, mu[1].x, mu[1].y};
         const float a4[4] = {dA[0].x * An[0].x, dA[0].y * An[0].y, dA[1].x * An[1].x, dA[1].y * An[1].y};
@@ -600,7 +628,10 @@ extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* d
               (!z || make_tile_map(&maps.z, z, bf16, Dm, L, batch, s.z_l, s.z_b, kBW, kBT)) &&
               make_tile_map(&maps.dy, dy, bf16, Dm, L, batch, Dm, L * Dm, kBW, kBT) &&
               make_tile_map(&maps.B, B, bf16, N, L, batch, s.B_l, s.B_b, ns, kBT) &&
-              make_tile_map(&maps.C, C, bf16, N, L, batch, s.C_l, s.C_b, ns, kBT);
+              make_tile_map(&maps.C, C, bf16, N, L, batch, s.C_l, s.C_b, ns, kBT) &&
+              make_tile_map(&maps.du, du, bf16, Dm, L, batch, Dm, L * Dm, kBW, kBT) &&
+              make_tile_map(&maps.ddelta, ddelta_raw, bf16, Dm, L, batch, Dm, L * Dm, kBW, kBT) &&
+              (!z || make_tile_map(&maps.dz, dz, bf16, Dm, L, batch, Dm, L * Dm, kBW, kBT));
     }
     if (ft == 1 && !tma) return SS_ERR_UNSUPPORTED;
     const cudaError_t e = bf16 ? launch_bwd<__nv_bfloat16>(p, maps, ns, tma, stream)
