@@ -479,6 +479,10 @@ def bench_bwd(args, local_rank):
     alg = w.batch * w.L * (7 * w.Dm * s + 4 * w.N * 4) + w.Dm * (w.N + 2) * 4 * 2
     hbm_peak, peak_kind = peaks()
     achieved = alg / (launch_ms / 1e3) / 1e9
+    # the SFU floor: two exp2 per state update (the forward recurrence and the adjoint one) at
+    # the ex2 rate; below the HBM floor, so the bound is HBM
+    sfu_peak = GB300_SMS * SFU_EX2_PER_CLK_PER_SM * GB300_MAX_SM_MHZ * 1e6
+    t_hbm, t_sfu = alg / (hbm_peak * 1e9), 2 * units / sfu_peak
     print(json.dumps({
         "metric": "selective-scan backward state-updates/s (B·L·D·N), 1×GB300",
         "value": units * args.steps / (total_ms / 1e3), "unit": "state-updates/s", "n_gpus": 1,
@@ -490,7 +494,7 @@ def bench_bwd(args, local_rank):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": measured_traffic("bwd_130m", "ss_bwd_kernel"), "kernel": "ss_bwd_kernel",
-                     "launch_ms": launch_ms,
+                     "launch_ms": launch_ms, "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6,
                      "alg_bytes_per_launch": alg}}))
     return 0
 
