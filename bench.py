@@ -38,9 +38,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="mamba130m",
                     choices=["mamba130m", "long32k", "mamba2p8b_bf16", "decode1p4b", "tiny", "conv1d_130m",
-                             "bwd_130m"],
+                             "bwd_130m", "lti_130m"],
                     help="conv1d_130m times the causal conv1d + SiLU on the 130m layer's conv input "
-                         "(its own metric, outputs/s); bwd_130m the backward scan of the 130m layer")
+                         "(its own metric, outputs/s); bwd_130m the backward scan of the 130m layer; "
+                         "lti_130m the forward with B and C constant over the steps")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -387,6 +388,73 @@ def workload_config(w, extra=None, variant=None):
     return c
 
 
+def time_step_fn(step, args, local_rank):
+    """W warm-up calls of `step`, then K timed ones bracketed by CUDA events on the current
+    stream, clocks sampled throughout.  Returns (total ms, mean per-call ms, clock summary)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    return start.elapsed_time(end), statistics.mean(a.elapsed_time(b) for a, b in ev), clk.summary()
+
+
+def bench_lti(args, local_rank):
+    """ss_fwd on the 130m-shaped layer (batch 8, L 2048, Dm 1536, N 16, fp32) with B and C
+    constant over the steps of each batch row (step stride 0, the LTI case): the kernel holds
+    them in registers.  One launch per step."""
+    import torch
+    import selective_state_space_scan_gb300 as ss
+    from selective_state_space_scan_gb300 import synth
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = synth.config("mamba130m")
+    a = w.arrays
+    t = {k: (None if v is None else torch.from_numpy(v).to(dev)) for k, v in a.items()}
+    Bm = t["B"][:, :1].expand(-1, w.L, -1)
+    Cm = t["C"][:, :1].expand(-1, w.L, -1)
+    y = torch.empty_like(t["u"])
+    last = torch.empty((w.batch, w.Dm, w.N), device=dev)
+
+    def step():
+        ss.ss_fwd(t["u"], t["delta_raw"], t["delta_bias"], t["A_log"], Bm, Cm, t["D"], t["z"], y=y, last_state=last)
+    total_ms, launch_ms, clocks = time_step_fn(step, args, local_rank)
+    err = ss.device_error(clear=True)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} after the timed region")
+    units = updates_per_step(w)
+    # read u, delta_raw, z and write y; one B and C row per batch row; params; last_state
+    alg = w.batch * w.L * 4 * w.Dm * 4 + 2 * w.batch * w.N * 4 + w.Dm * (w.N + 2) * 4 + w.batch * w.Dm * w.N * 4
+    hbm_peak, peak_kind = peaks()
+    sfu_peak = GB300_SMS * SFU_EX2_PER_CLK_PER_SM * GB300_MAX_SM_MHZ * 1e6
+    achieved = alg / (launch_ms / 1e3) / 1e9
+    kernel = "ss_fwd_lane_kernel(lpc=4,lti)"
+    print(json.dumps({
+        "metric": "selective-scan state-updates/s (B·L·D·N), time-invariant B/C, 1×GB300",
+        "value": units * args.steps / (total_ms / 1e3), "unit": "state-updates/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "lti_130m: batch=8 L=2048 Dm=1536 N=16 io=f32, B and C at step stride 0",
+                   "l2": "no flush: working set 403 MB > 129 MB L2"},
+        "gpu_launches": args.steps, "clocks": clocks,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": measured_traffic("lti_130m", kernel), "kernel": kernel, "launch_ms": launch_ms,
+                     "alg_bytes_per_launch": alg, "t_hbm_us": alg / (hbm_peak * 1e9) * 1e6,
+                     "t_sfu_us": units / sfu_peak * 1e6}}))
+    return 0
+
+
 def bench_conv1d(args, local_rank):
     """The causal conv1d + SiLU (ss_conv1d) on the conv input of the 130m-shaped layer (batch 8,
     L 2048, Dm 1536, fp32), window in and out: one launch per step."""
@@ -405,22 +473,7 @@ def bench_conv1d(args, local_rank):
 
     def step():
         ss.ss_conv1d(x, wgt, bias, out=out, window_in=win, window_out=win, silu=True)
-    stream = torch.cuda.current_stream()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank) as clk:
-        for _ in range(max(args.warmup, 3)):
-            step()
-        torch.cuda.synchronize()
-        start.record(stream)
-        for i in range(args.steps):
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
-        end.record(stream)
-        torch.cuda.synchronize()
-    total_ms = start.elapsed_time(end)
-    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    total_ms, launch_ms, clocks = time_step_fn(step, args, local_rank)
     units = batch * L * Dm
     alg = 2 * units * 4 + Dm * 5 * 4 + 2 * batch * Dm * 3 * 4
     hbm_peak, peak_kind = peaks()
@@ -432,7 +485,7 @@ def bench_conv1d(args, local_rank):
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": "conv1d_130m: batch=8 L=2048 Dm=1536 kernel=4 io=f32 silu window",
                    "l2": "no flush: working set 201 MB > 129 MB L2"},
-        "gpu_launches": args.steps, "clocks": clk.summary(),
+        "gpu_launches": args.steps, "clocks": clocks,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": measured_traffic("conv1d_130m", "ss_conv1d_kernel"), "kernel": "ss_conv1d_kernel",
@@ -457,22 +510,7 @@ def bench_bwd(args, local_rank):
 
     def step():
         ss.ss_bwd(dy, t["u"], t["delta_raw"], t["delta_bias"], t["A_log"], t["B"], t["C"], t["D"], t["z"])
-    stream = torch.cuda.current_stream()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank) as clk:
-        for _ in range(max(args.warmup, 3)):
-            step()
-        torch.cuda.synchronize()
-        start.record(stream)
-        for i in range(args.steps):
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
-        end.record(stream)
-        torch.cuda.synchronize()
-    total_ms = start.elapsed_time(end)
-    launch_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ev)
+    total_ms, launch_ms, clocks = time_step_fn(step, args, local_rank)
     units = updates_per_step(w)
     s = w.io_bytes()
     # must move: read u, delta_raw, z, dy and B, C; write du, ddelta_raw, dz and dB, dC; params
@@ -490,7 +528,7 @@ def bench_bwd(args, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "bwd_130m: batch=8 L=2048 Dm=1536 N=16 io=f32, all input gradients",
                    "l2": "no flush: working set > 129 MB L2"},
-        "gpu_launches": args.steps, "clocks": clk.summary(),
+        "gpu_launches": args.steps, "clocks": clocks,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": measured_traffic("bwd_130m", "ss_bwd_kernel"), "kernel": "ss_bwd_kernel",
@@ -505,13 +543,14 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     from selective_state_space_scan_gb300 import synth
-    if args.workload in ("conv1d_130m", "bwd_130m"):
+    if args.workload in ("conv1d_130m", "bwd_130m", "lti_130m"):
         if args.impl == "reference" or world > 1:
             if rank == 0:
                 print(json.dumps({"impl": args.impl,
                                   "unavailable": f"{args.workload} is measured on one GPU, ours only"}))
             return 0
-        return bench_conv1d(args, local_rank) if args.workload == "conv1d_130m" else bench_bwd(args, local_rank)
+        fn = {"conv1d_130m": bench_conv1d, "bwd_130m": bench_bwd, "lti_130m": bench_lti}[args.workload]
+        return fn(args, local_rank)
     w = synth.config(args.workload)
 
     if args.impl == "reference":

@@ -60,6 +60,11 @@ typedef enum { SS_F32 = 0, SS_BF16 = 1 } ss_dtype;
  * delta_raw, z, y and the state axis of B, C have stride 1.  A NULL strides pointer
  * means: io_dtype = SS_F32 and every tensor contiguous
  * (x_b = L·Dm, x_l = Dm for [batch, L, Dm]; B_b = L·N, B_l = N for [batch, L, N]).
+ * Steps of B and C are at least N elements apart, or B_l = C_l = 0: B and C constant over the
+ * steps of a batch row, the linear time-invariant case that the blog's walkthrough of the
+ * official CUDA kernel (section "主要な最適化テクニック", the kIsVariableB/C branch) specialises.
+ * The forward pass then holds each state's B and C in registers instead of staging tiles of
+ * them (only one of the two at stride 0 is served by the generic fill).
  */
 typedef struct {
     int32_t io_dtype;                       /* ss_dtype */

@@ -6,16 +6,20 @@
 
 namespace selscan {
 
-template <typename TIO, int NS, int LPC, bool BAL, bool TMA, bool SO = false>
+template <typename TIO, int NS, int LPC, bool BAL, bool TMA, bool SO = false, bool LTI = false>
 cudaError_t launch_lane_cfg(const FwdParams& p, const FwdMaps& m, cudaStream_t stream, int* max_grid) {
     using Cfg = LaneCfg<TIO, NS, LPC, lane_w(LPC, BAL), kLaneT, kLaneStages, lane_minb(LPC)>;
     constexpr int smem = TMA ? Cfg::SMEM_BYTES : Cfg::SMEM_BYTES - (Cfg::STAGES - 1) * Cfg::STAGE_BYTES;
     static_assert(smem <= 227 * 1024, "shared memory budget exceeded");
-    return launch_with_smem<Cfg, TMA>(ss_fwd_lane_kernel<Cfg, TMA, SO>, p, m, stream, smem, BAL, max_grid);
+    return launch_with_smem<Cfg, TMA>(ss_fwd_lane_kernel<Cfg, TMA, SO, LTI>, p, m, stream, smem, BAL, max_grid);
 }
 
 template <typename TIO, int NS, int LPC>
 cudaError_t launch_lane_v(const FwdVariant& v, const FwdParams& p, const FwdMaps& m, cudaStream_t s, int* mg) {
+    if (v.lti) {
+        if (!v.tma || v.balanced || v.state_only) return cudaErrorInvalidValue;   // per-tile, TMA-fed only
+        return launch_lane_cfg<TIO, NS, LPC, false, true, false, true>(p, m, s, mg);
+    }
     if (v.state_only) {
         if (!v.tma || v.balanced) return cudaErrorInvalidValue;   // pass A is TMA-fed only
         return launch_lane_cfg<TIO, NS, LPC, false, true, true>(p, m, s, mg);

@@ -21,6 +21,7 @@ struct FwdVariant {
     bool tma;
     bool balanced;   // lane family: equal (tile, chunk) ranges per CTA (needs a workspace, TMA)
     bool state_only; // lane family, TMA: pass A of the time-split schedule (end states only)
+    bool lti;        // lane family, TMA, per tile: B and C constant over the steps (held in registers)
 };
 
 struct FwdGeom {

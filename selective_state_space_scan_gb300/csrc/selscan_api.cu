@@ -160,6 +160,7 @@ FwdVariant choose_fwd_variant(int64_t batch, int64_t Dm, int64_t N) {
     v.tma = true;
     v.balanced = false;
     v.state_only = false;
+    v.lti = false;
     return v;
 }
 
@@ -355,7 +356,9 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     if (s.u_l < Dm || s.delta_l < Dm || s.y_l < Dm || (z && s.z_l < Dm)) {
         if (L > 1) return SS_ERR_INVALID_ARG;
     }
-    if ((s.B_l < N || s.C_l < N) && L > 1) return SS_ERR_INVALID_ARG;
+    // B, C: rows at least N apart, or step stride 0 (time-invariant, the LTI case)
+    if (((s.B_l < N && s.B_l != 0) || (s.C_l < N && s.C_l != 0)) && L > 1) return SS_ERR_INVALID_ARG;
+    const bool lti = L > 1 && s.B_l == 0 && s.C_l == 0;
     if (L > INT32_MAX || Dm > INT32_MAX || batch > INT32_MAX) return SS_ERR_UNSUPPORTED;
     // alignment to the element type
     const void* io_ptrs[] = {u, delta_raw, B, C, y, z};
@@ -398,27 +401,29 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         v.lpc = fl;
     }
     // TMA fill: B/C rows exactly ns wide and a multiple of 16 bytes, 16-byte aligned bases
-    // and row/batch strides.
-    bool tma = (N == v.ns) && (N * es) % 16 == 0;
-    const void* tma_ptrs[] = {u, delta_raw, B, C, z};
+    // and row/batch strides.  Time-invariant B/C (LTI) on the lane family: u/Δ/z by TMA, B and
+    // C held in registers (no B/C tiles); elsewhere LTI takes the plain-load fill.
+    bool tma = lti ? v.family == kFamLane : (N == v.ns) && (N * es) % 16 == 0;
+    const void* tma_ptrs[] = {u, delta_raw, lti ? nullptr : B, lti ? nullptr : C, z};
     for (const void* q : tma_ptrs)
         if (q && !aligned(q, 16)) tma = false;
-    const int64_t tma_strides[] = {s.u_l, s.delta_l, s.B_l, s.C_l, z ? s.z_l : s.u_l};
+    const int64_t tma_strides[] = {s.u_l, s.delta_l, lti ? s.u_l : s.B_l, lti ? s.u_l : s.C_l, z ? s.z_l : s.u_l};
     for (int64_t v2 : tma_strides)
         if (!tma_stride_ok(v2, es)) tma = false;
     if (batch > 1) {
-        const int64_t bstr[] = {s.u_b, s.delta_b, s.B_b, s.C_b, z ? s.z_b : s.u_b};
+        const int64_t bstr[] = {s.u_b, s.delta_b, lti ? s.u_b : s.B_b, lti ? s.u_b : s.C_b, z ? s.z_b : s.u_b};
         for (int64_t v2 : bstr)
             if (!tma_stride_ok(v2, es)) tma = false;
     }
     if (ft == 0) tma = false;
+    v.lti = lti && tma;
 
     // Time-split schedule (needs a workspace and TMA): when the channel tiles alone cannot
     // fill the GPU, cut the sequence into segments that run side by side (pass A: end states
     // from zero; carry pass; pass C: the fold from each segment's carried start).
     const int fs = g_force_nseg.load();
     SplitPlan plan;
-    if (workspace && tma && fs != 0 && (fs >= 2 || (v.family == kFamSeg && ff < 0))) {
+    if (workspace && tma && !lti && fs != 0 && (fs >= 2 || (v.family == kFamSeg && ff < 0))) {
         FwdVariant vs = v;
         vs.family = kFamLane;
         if (fl <= 0) vs.lpc = vs.ns / 4;
@@ -441,7 +446,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     // rejects is served by the plain-load fill.
     // The schedule fixes the tile width (and so the box width): decide it first.  With a
     // workspace, TMA-fed lane kernels that do not take the time split run the balanced one.
-    v.balanced = plan.nseg < 2 && workspace != nullptr && v.family == kFamLane && tma &&
+    v.balanced = plan.nseg < 2 && workspace != nullptr && v.family == kFamLane && tma && !v.lti &&
                  g_force_balanced.load() != 0;
     FwdMaps maps;
     std::memset(&maps, 0, sizeof(maps));
@@ -452,11 +457,12 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         tma = make_map(&maps.u, u, bf16, Dm, L, batch, s.u_l, s.u_b, bw, bh, true) &&
               make_map(&maps.delta, delta_raw, bf16, Dm, L, batch, s.delta_l, s.delta_b, bw, bh, true) &&
               (!z || make_map(&maps.z, z, bf16, Dm, L, batch, s.z_l, s.z_b, bw, bh, true)) &&
-              make_map(&maps.B, B, bf16, N, L, batch, s.B_l, s.B_b, v.ns, bh, swbc) &&
-              make_map(&maps.C, C, bf16, N, L, batch, s.C_l, s.C_b, v.ns, bh, swbc);
+              (v.lti || (make_map(&maps.B, B, bf16, N, L, batch, s.B_l, s.B_b, v.ns, bh, swbc) &&
+                         make_map(&maps.C, C, bf16, N, L, batch, s.C_l, s.C_b, v.ns, bh, swbc)));
     }
     if (ft == 1 && !tma) return SS_ERR_UNSUPPORTED;
     v.tma = tma;
+    if (!tma) v.lti = false;
     if (!tma) {                     // descriptors refused: the plain-load fill, per-tile schedule
         plan = SplitPlan();
         v.balanced = false;

@@ -562,7 +562,9 @@ extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* d
                           z ? s.z_b : 0, z ? s.z_l : 0};
     for (int64_t v : st)
         if (v < 0) return SS_ERR_INVALID_ARG;
-    if ((s.u_l < Dm || s.delta_l < Dm || (z && s.z_l < Dm) || s.B_l < N || s.C_l < N) && L > 1)
+    // B, C rows at least N apart, or step stride 0 (time-invariant; dB, dC still come per step)
+    if ((s.u_l < Dm || s.delta_l < Dm || (z && s.z_l < Dm) || (s.B_l < N && s.B_l != 0) ||
+         (s.C_l < N && s.C_l != 0)) && L > 1)
         return SS_ERR_INVALID_ARG;
     const void* io_ptrs[] = {u, delta_raw, B, C, z, dy, du, ddelta_raw, dz};
     for (const void* q : io_ptrs)

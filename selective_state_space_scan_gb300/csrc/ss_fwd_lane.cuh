@@ -173,11 +173,12 @@ __device__ void lane_fill_generic(uint8_t* st, const FwdParams& p, int b, int d0
     }
 }
 
-// WITH_C = false (pass A of the time split) skips the C tile; has_z = false the z tile.
-template <class Cfg, bool WITH_C>
+// WITH_C = false (pass A of the time split) skips the C tile; has_z = false the z tile; LTI
+// (time-invariant B and C, held in registers) both B/C tiles.
+template <class Cfg, bool WITH_C, bool LTI = false>
 __device__ __forceinline__ void lane_issue_tma(uint8_t* st, uint64_t* bar, const FwdMaps& m,
                                                bool has_z, int b, int d0, int chunk) {
-    const uint32_t bytes = (has_z ? 3u : 2u) * Cfg::TILE_X + (WITH_C ? 2u : 1u) * Cfg::TILE_N;
+    const uint32_t bytes = (has_z ? 3u : 2u) * Cfg::TILE_X + (LTI ? 0u : (WITH_C ? 2u : 1u) * Cfg::TILE_N);
     mbar_expect_tx(bar, bytes);
     const int t0 = chunk * Cfg::T;
     // one [T][W] box per stream (rows of W channels, hardware swizzle), one [T][NS] box for B, C.
@@ -186,8 +187,10 @@ __device__ __forceinline__ void lane_issue_tma(uint8_t* st, uint64_t* bar, const
     tma_load_3d(st + Cfg::OFF_U, &m.u, bar, d0, t0, b);
     tma_load_3d(st + Cfg::OFF_D, &m.delta, bar, d0, t0, b);
     if (has_z) tma_load_3d(st + Cfg::OFF_Z, &m.z, bar, d0, t0, b);
-    tma_load_3d(st + Cfg::OFF_B, &m.B, bar, 0, t0, b);
-    if (WITH_C) tma_load_3d(st + Cfg::OFF_C, &m.C, bar, 0, t0, b);
+    if (!LTI) {
+        tma_load_3d(st + Cfg::OFF_B, &m.B, bar, 0, t0, b);
+        if (WITH_C) tma_load_3d(st + Cfg::OFF_C, &m.C, bar, 0, t0, b);
+    }
 }
 
 // Wait (thread 0 only) until another CTA has published with this call's epoch; gives up
@@ -211,7 +214,9 @@ __device__ __forceinline__ void wait_published(const unsigned int* flag, unsigne
 
 // STATE_ONLY: pass A of the time-split schedule.  The same fold from a zero state, without
 // C, y or the z gate: it writes the segment's end state and its Σ Δ.
-template <class Cfg, bool USE_TMA, bool STATE_ONLY = false>
+// LTI: B and C do not vary with the step (the linear time-invariant case, step stride 0): each
+// lane holds its states' B and C in registers and no B/C tiles are staged.
+template <class Cfg, bool USE_TMA, bool STATE_ONLY = false, bool LTI = false>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
 ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     using TIO = typename Cfg::TIO;
@@ -267,15 +272,17 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             tma_prefetch_desc(&maps.u);
             tma_prefetch_desc(&maps.delta);
             if (has_z) tma_prefetch_desc(&maps.z);
-            tma_prefetch_desc(&maps.B);
-            tma_prefetch_desc(&maps.C);
+            if (!LTI) {
+                tma_prefetch_desc(&maps.B);
+                tma_prefetch_desc(&maps.C);
+            }
         }
     }
     __syncthreads();
     auto issue = [&](int k, uint8_t* st, uint64_t* bar) {
         int tl, chk;
         work.unit(k, nchunks, tl, chk);
-        lane_issue_tma<Cfg, !STATE_ONLY>(st, bar, maps, has_z, tl / p.tiles_per_batch,
+        lane_issue_tma<Cfg, !STATE_ONLY, LTI>(st, bar, maps, has_z, tl / p.tiles_per_batch,
                             (tl % p.tiles_per_batch) * Cfg::W, chk);
     };
     if (USE_TMA && tid == 0) {
@@ -290,10 +297,12 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     float2 A2[QPL][2];                   // A'[n] = -exp(A_log[d,n])·log2(e), hoisted out of the scan
     float2 h[QPL][2];                    // this lane's slice of the state
     float dsum = 0.f;                    // STATE_ONLY: Σ Δ over this lane's steps
+    float4 bL[QPL], cL[QPL];             // LTI: this lane's B and C
 #pragma unroll
     for (int qq = 0; qq < QPL; ++qq) {
         A2[qq][0] = A2[qq][1] = make_float2(0.f, 0.f);
         h[qq][0] = h[qq][1] = make_float2(0.f, 0.f);
+        bL[qq] = cL[qq] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
     // The work is a list of pieces, each chunks [c0, c0 + cnt) of one tile, in the order the
@@ -329,6 +338,19 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             A2[qq][0] = make_float2(v[0], v[1]);
             A2[qq][1] = make_float2(v[2], v[3]);
             h[qq][0] = h[qq][1] = make_float2(0.f, 0.f);
+            if constexpr (LTI) {
+                const TIO* Bb = static_cast<const TIO*>(p.Bm) + b * p.B_b;
+                const TIO* Cb = static_cast<const TIO*>(p.Cm) + b * p.C_b;
+                float w[8];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int n = n0 + 4 * qq + q4;
+                    w[q4] = n < p.N ? to_f32<TIO>(Bb[n]) : 0.f;
+                    w[4 + q4] = n < p.N ? to_f32<TIO>(Cb[n]) : 0.f;
+                }
+                bL[qq] = make_float4(w[0], w[1], w[2], w[3]);
+                cL[qq] = make_float4(w[4], w[5], w[6], w[7]);
+            }
         }
         dsum = 0.f;
         if constexpr (!STATE_ONLY) {
@@ -387,7 +409,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             };
             const float* tB;
             const float* tC;
-            if constexpr (Cfg::CONVERT_BC) {
+            if constexpr (Cfg::CONVERT_BC && !LTI) {
                 const TIO* rb = reinterpret_cast<const TIO*>(st + Cfg::OFF_B);
                 const TIO* rc = reinterpret_cast<const TIO*>(st + Cfg::OFF_C);
                 for (int i = tid; i < T * NS; i += Cfg::THREADS) {
@@ -446,7 +468,8 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                             const int row = (g0 + g) * LPC + kk;
 #pragma unroll
                             for (int qq = 0; qq < QPL; ++qq) {
-                                const float4 B4 = *reinterpret_cast<const float4*>(tB + row * NS + n0 + 4 * qq);
+                                const float4 B4 = LTI ? bL[qq]
+                                                      : *reinterpret_cast<const float4*>(tB + row * NS + n0 + 4 * qq);
                                 a[kk][qq][0] = ex2x2(mul2(dl2, A2[qq][0]));
                                 a[kk][qq][1] = ex2x2(mul2(dl2, A2[qq][1]));
                                 bb[kk][qq][0] = mul2(du2, make_float2(B4.x, B4.y));
@@ -474,7 +497,9 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
 #pragma unroll
                             for (int qq = 0; qq < QPL; ++qq) {
                                 float4 C4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                                if constexpr (!STATE_ONLY)
+                                if constexpr (LTI)
+                                    C4 = cL[qq];
+                                else if constexpr (!STATE_ONLY)
                                     C4 = *reinterpret_cast<const float4*>(tC + row * NS + n0 + 4 * qq);
                                 h[qq][0] = fma2(ac[kk][qq][0], h[qq][0], bc[kk][qq][0]);
                                 h[qq][1] = fma2(ac[kk][qq][1], h[qq][1], bc[kk][qq][1]);
@@ -532,7 +557,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                     }
                 }
             }
-            if (USE_TMA && !Cfg::CONVERT_BC) {
+            if (USE_TMA && !(Cfg::CONVERT_BC && !LTI)) {
                 // Release the stage without a block-wide barrier: the warp that finishes it last
                 // refills it, so warps that are ahead run on into the stages already loaded.
                 __syncwarp();

@@ -112,6 +112,32 @@ def test_unrolled_sum_form(oracle_mod):
     np.testing.assert_allclose(last, h[:, -1], rtol=1e-11, atol=1e-12)
 
 
+def test_lti_scan_is_a_causal_convolution(oracle_mod):
+    """B and C constant over the steps (the LTI case) and Δ constant over the steps make the
+    scan a linear time-invariant system: y_t = silu(z_t)·Σ_k K_k u_{t-k}, with the impulse
+    response K_0 = Σ_n C_n Δ B_n + D and K_k = Σ_n C_n a_n^k Δ B_n, a_n = exp(Δ A_n).  The
+    convolution is numpy.convolve, independent of the oracle's recurrence."""
+    batch, L, Dm, N = 2, 40, 3, 5
+    a = _rand_inputs(13, batch=batch, L=L, Dm=Dm, N=N)
+    g = np.random.default_rng(131)
+    a["delta_raw"] = np.broadcast_to(g.standard_normal((1, 1, Dm)).astype(np.float32), (batch, L, Dm)).copy()
+    a["B"] = np.broadcast_to(a["B"][:, :1], (batch, L, N)).copy()
+    a["C"] = np.broadcast_to(a["C"][:, :1], (batch, L, N)).copy()
+    y, _, _ = _call(oracle_mod, a)
+    for b in range(batch):
+        for d in range(Dm):
+            dlt = _softplus_np(float(a["delta_raw"][0, 0, d]) + float(a["delta_bias"][d]))
+            A = -np.exp(a["A_log"][d].astype(np.float64))
+            Bn = a["B"][b, 0].astype(np.float64)
+            Cn = a["C"][b, 0].astype(np.float64)
+            k = np.arange(L)[:, None]
+            K = (Cn * dlt * Bn * np.exp(dlt * A) ** k).sum(axis=1)
+            K[0] += float(a["D"][d])
+            yhat = np.convolve(a["u"][b, :, d].astype(np.float64), K)[:L]
+            z = a["z"][b, :, d].astype(np.float64)
+            np.testing.assert_allclose(y[b, :, d], yhat * z * expit(z), rtol=1e-11, atol=1e-12)
+
+
 def test_skip_only_when_B_or_C_is_zero(oracle_mod):
     a = _rand_inputs(3, batch=2, L=17, Dm=4, N=4)
     z = a["z"].astype(np.float64)
