@@ -32,6 +32,9 @@ def _configure(lib):
     lib.oracle_silu.restype = ctypes.c_double
     lib.oracle_ss_fwd_rows.argtypes = [f32p] * 8 + [f64p, i64p, i64, f64p, f64p, f64p, i64, i64, i64, i64]
     lib.oracle_ss_fwd_rows.restype = ctypes.c_int
+    lib.oracle_ss_fwd_dtproj_rows.argtypes = [f32p] * 3 + [i64] + [f32p] * 6 + [f64p, i64p, i64, f64p, f64p, f64p,
+                                                                               i64, i64, i64, i64]
+    lib.oracle_ss_fwd_dtproj_rows.restype = ctypes.c_int
     lib.oracle_ss_fwd_chunked.argtypes = [f32p] * 8 + [f64p, f64p, f64p, i64, i64, i64, i64, i64]
     lib.oracle_ss_fwd_chunked.restype = ctypes.c_int
     lib.oracle_ss_step.argtypes = [f64p] + [f32p] * 8 + [f64p, f64p, i64, i64, i64]
@@ -132,6 +135,42 @@ def ss_fwd(u, delta_raw, delta_bias, A_log, B, C, D, z, rows=None, h0=None):
         raise RuntimeError(f"oracle_ss_fwd_rows failed with status {st}")
     if rows is not None:
         return y, last, mag
+    y = y.reshape(batch, Dm, L).transpose(0, 2, 1)
+    mag = mag.reshape(batch, Dm, L).transpose(0, 2, 1)
+    return np.ascontiguousarray(y), last.reshape(batch, Dm, N), np.ascontiguousarray(mag)
+
+
+def ss_fwd_dtproj(u, dt_low, W_dt, delta_bias, A_log, B, C, D, z, h0=None):
+    """Sequential fp64 forward scan whose pre-softplus time step is the low-rank projection
+    delta_raw[b,t,d] = sum_k W_dt[d,k] dt_low[b,t,k], summed in fp64 inside the oracle.
+    dt_low [batch, L, R], W_dt [Dm, R]; the rest and the returns as ss_fwd(rows=None)."""
+    u = _f32(u, name="u")
+    if u.ndim != 3:
+        raise ValueError("u must be [batch, L, Dm]")
+    batch, L, Dm = u.shape
+    W_dt = _f32(W_dt, name="W_dt")
+    R = W_dt.shape[1]
+    dt_low = _f32(dt_low, (batch, L, R), "dt_low")
+    A_log = _f32(A_log, name="A_log")
+    N = A_log.shape[1]
+    z = _f32(z, (batch, L, Dm), "z")
+    B = _f32(B, (batch, L, N), "B")
+    C = _f32(C, (batch, L, N), "C")
+    D = _f32(D, (Dm,), "D")
+    delta_bias = _f32(delta_bias, (Dm,), "delta_bias")
+    h0 = _h0(h0, batch, Dm, N)
+    nrows = batch * Dm
+    y = np.empty((nrows, L), np.float64)
+    mag = np.empty((nrows, L), np.float64)
+    last = np.empty((nrows, N), np.float64)
+    st = _load().oracle_ss_fwd_dtproj_rows(
+        _ptr(u, ctypes.c_float), _ptr(dt_low, ctypes.c_float), _ptr(W_dt, ctypes.c_float), R,
+        _ptr(delta_bias, ctypes.c_float), _ptr(A_log, ctypes.c_float), _ptr(B, ctypes.c_float),
+        _ptr(C, ctypes.c_float), _ptr(D, ctypes.c_float), _ptr(z, ctypes.c_float), _ptr(h0, ctypes.c_double),
+        None, nrows, _ptr(y, ctypes.c_double), _ptr(mag, ctypes.c_double), _ptr(last, ctypes.c_double),
+        batch, L, Dm, N)
+    if st != 0:
+        raise RuntimeError(f"oracle_ss_fwd_dtproj_rows failed with status {st}")
     y = y.reshape(batch, Dm, L).transpose(0, 2, 1)
     mag = mag.reshape(batch, Dm, L).transpose(0, 2, 1)
     return np.ascontiguousarray(y), last.reshape(batch, Dm, N), np.ascontiguousarray(mag)

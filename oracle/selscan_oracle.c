@@ -66,15 +66,18 @@ double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
  *   h_t[n]  = exp(Δ_t · A_n) · h_{t-1}[n] + Δ_t · B[b,t,n] · u[b,t,d],  A_n = -exp(A_log[d,n])
  *   ŷ_t     = Σ_n C[b,t,n] · h_t[n] + D[d] · u[b,t,d]
  *   y[b,t,d]= ŷ_t · silu(z[b,t,d])   (ŷ_t when z is NULL)
+ * The pre-softplus time step comes from delta_raw, or (delta_raw NULL) from the low-rank
+ * projection dt_low [batch, L, R] · W_dt[Dm, R]^T summed in fp64 (see oracle_ss_fwd_dtproj_rows).
  */
-int oracle_ss_fwd_rows(const float* u, const float* delta_raw, const float* delta_bias,
-                       const float* A_log, const float* B, const float* C, const float* D,
-                       const float* z, const double* h0, const int64_t* rows, int64_t nrows,
-                       double* y_rows, double* mag_rows, double* last_rows,
-                       int64_t batch, int64_t L, int64_t Dm, int64_t N)
+static int fwd_rows(const float* u, const float* delta_raw, const float* dt_low, const float* W_dt, int64_t R,
+                    const float* delta_bias, const float* A_log, const float* B, const float* C,
+                    const float* D, const float* z, const double* h0, const int64_t* rows, int64_t nrows,
+                    double* y_rows, double* mag_rows, double* last_rows,
+                    int64_t batch, int64_t L, int64_t Dm, int64_t N)
 {
     if (batch < 0 || L < 0 || Dm < 0 || N < 1) return ORACLE_EINVAL;
-    if (!u || !delta_raw || !A_log || !B || !C) return ORACLE_EINVAL;
+    if (!u || !A_log || !B || !C) return ORACLE_EINVAL;
+    if (!delta_raw && (!dt_low || !W_dt || R < 1)) return ORACLE_EINVAL;
     if (rows == NULL) nrows = batch * Dm;
     int status = ORACLE_OK;
 
@@ -106,7 +109,13 @@ int oracle_ss_fwd_rows(const float* u, const float* delta_raw, const float* delt
             const int64_t io = (b * L + t) * Dm + d;   /* [b, t, d] */
             const int64_t ib = (b * L + t) * N;        /* [b, t, 0] */
             const double ut = (double)u[io];
-            const double delta = oracle_softplus((double)delta_raw[io] + bias);
+            double draw = 0.0;
+            if (delta_raw) {
+                draw = (double)delta_raw[io];
+            } else {
+                for (int64_t k = 0; k < R; ++k) draw += (double)W_dt[d * R + k] * (double)dt_low[(b * L + t) * R + k];
+            }
+            const double delta = oracle_softplus(draw + bias);
             double acc = 0.0, acc_abs = 0.0;
             for (int64_t n = 0; n < N; ++n) {
                 h[n] = exp(delta * A[n]) * h[n] + delta * (double)B[ib + n] * ut;
@@ -125,6 +134,35 @@ int oracle_ss_fwd_rows(const float* u, const float* delta_raw, const float* delt
         free(A);
     }
     return status;
+}
+
+int oracle_ss_fwd_rows(const float* u, const float* delta_raw, const float* delta_bias,
+                       const float* A_log, const float* B, const float* C, const float* D,
+                       const float* z, const double* h0, const int64_t* rows, int64_t nrows,
+                       double* y_rows, double* mag_rows, double* last_rows,
+                       int64_t batch, int64_t L, int64_t Dm, int64_t N)
+{
+    if (!delta_raw) return ORACLE_EINVAL;
+    return fwd_rows(u, delta_raw, NULL, NULL, 0, delta_bias, A_log, B, C, D, z, h0, rows, nrows,
+                    y_rows, mag_rows, last_rows, batch, L, Dm, N);
+}
+
+/*
+ * The forward scan with the time step's low-rank projection folded in: delta_raw[b,t,d] =
+ * Σ_k W_dt[d,k] · dt_low[b,t,k] (k < R), summed in fp64, replaces the delta_raw input.  The
+ * projection is the one SpeechLens kernel-optimization.md folds into its scan kernel (the
+ * "dtProj–scan fusion" experiment: the rank-R delta projection computed inside the kernel
+ * instead of materialising the [B, L, D] time steps).  dt_low [batch, L, R], W_dt [Dm, R].
+ */
+int oracle_ss_fwd_dtproj_rows(const float* u, const float* dt_low, const float* W_dt, int64_t R,
+                              const float* delta_bias, const float* A_log, const float* B, const float* C,
+                              const float* D, const float* z, const double* h0, const int64_t* rows,
+                              int64_t nrows, double* y_rows, double* mag_rows, double* last_rows,
+                              int64_t batch, int64_t L, int64_t Dm, int64_t N)
+{
+    if (!dt_low || !W_dt || R < 1) return ORACLE_EINVAL;
+    return fwd_rows(u, NULL, dt_low, W_dt, R, delta_bias, A_log, B, C, D, z, h0, rows, nrows,
+                    y_rows, mag_rows, last_rows, batch, L, Dm, N);
 }
 
 /*

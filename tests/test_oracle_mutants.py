@@ -66,6 +66,9 @@ MUTANTS = [
     ("bwd_dA_log_chain_dropped", "dA_log[d * N + n] = sA * (-exp((double)A_log[d * N + n]));",
      "dA_log[d * N + n] = sA;"),
     ("bwd_dC_previous_state", "dC[ib + n] += dyh * hs[(t + 1) * N + n];", "dC[ib + n] += dyh * hs[t * N + n];"),
+    ("dtproj_W_transposed", "draw += (double)W_dt[d * R + k] * (double)dt_low[(b * L + t) * R + k];",
+     "draw += (double)W_dt[k * Dm + d] * (double)dt_low[(b * L + t) * R + k];"),
+    ("dtproj_rank_term_dropped", "for (int64_t k = 0; k < R; ++k) draw +=", "for (int64_t k = 1; k < R; ++k) draw +="),
     ("step_bias_dropped",
      "oracle_softplus((double)delta_raw[row] + (delta_bias ? (double)delta_bias[d] : 0.0))",
      "oracle_softplus((double)delta_raw[row])"),
@@ -85,6 +88,7 @@ def harness():
     pins = _load_by_path("_oracle_pins_for_mutants", os.path.join(ROOT, "tests", "test_oracle_pins.py"))
     conv = _load_by_path("_oracle_conv_pins_for_mutants", os.path.join(ROOT, "tests", "test_oracle_conv1d.py"))
     bwd = _load_by_path("_oracle_bwd_pins_for_mutants", os.path.join(ROOT, "tests", "test_oracle_bwd.py"))
+    dtp = _load_by_path("_oracle_dtproj_pins_for_mutants", os.path.join(ROOT, "tests", "test_oracle_dtproj.py"))
     mod = _load_by_path("_oracle_mutant_pkg", os.path.join(ROOT, "oracle", "__init__.py"),
                         [os.path.join(ROOT, "oracle")])
     battery = [
@@ -116,6 +120,8 @@ def harness():
         lambda m: bwd.test_bwd_matches_finite_differences(m, True),
         lambda m: bwd.test_bwd_matches_finite_differences(m, False),
         bwd.test_bwd_A_to_zero_closed_form,
+        dtp.test_dtproj_exact_projection_matches_plain_forward,
+        lambda m: dtp.test_dtproj_general_projection_to_fp32_rounding(m, 4),
     ]
     return mod, battery
 
