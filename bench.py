@@ -38,10 +38,11 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="mamba130m",
                     choices=["mamba130m", "long32k", "mamba2p8b_bf16", "decode1p4b", "tiny", "conv1d_130m",
-                             "bwd_130m", "lti_130m"],
+                             "bwd_130m", "lti_130m", "dtproj_130m"],
                     help="conv1d_130m times the causal conv1d + SiLU on the 130m layer's conv input "
                          "(its own metric, outputs/s); bwd_130m the backward scan of the 130m layer; "
-                         "lti_130m the forward with B and C constant over the steps")
+                         "lti_130m the forward with B and C constant over the steps; dtproj_130m the forward "
+                         "with the rank-48 time-step projection folded in")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -90,7 +91,7 @@ def decay_ex2_per_step(w) -> int:
 _COMMON_SOURCES = ("device_common.cuh", "fwd_params.h", "internal.h", "fwd_configs.h", "selscan_api.cu")
 KERNEL_SOURCES = {
     "ss_fwd_lane_kernel": _COMMON_SOURCES + ("ss_fwd_lane.cuh", "fwd_lane_impl.cuh", "fwd_launch_common.cuh",
-                                             "fwd_lane_f32.cu", "fwd_lane_bf16.cu", "ss_fwd_carry.cu"),
+                                             "fwd_lane_f32.cu", "fwd_lane_bf16.cu", "ss_fwd_carry.cu", "fwd_lane_dtp.cu"),
     "ss_fwd_seg_kernel": _COMMON_SOURCES + ("ss_fwd_seg.cuh", "fwd_seg.cu", "fwd_launch_common.cuh"),
     "ss_step_kernel": _COMMON_SOURCES + ("ss_step.cu",),
     "ss_conv1d_kernel": ("device_common.cuh", "host_util.h", "ss_conv1d.cu"),
@@ -455,6 +456,57 @@ def bench_lti(args, local_rank):
     return 0
 
 
+def bench_dtproj(args, local_rank):
+    """ss_fwd_dtproj on the 130m-shaped layer (batch 8, L 2048, Dm 1536, N 16, fp32) with the
+    time-step projection of rank 48 (Mamba-130m's dt_rank, ceil(768 / 16)) folded in: the kernel
+    reads dt_low [8, 2048, 48] and W_dt [1536, 48] instead of delta_raw.  One launch per step."""
+    import torch
+    import selective_state_space_scan_gb300 as ss
+    from selective_state_space_scan_gb300 import synth
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = synth.config("mamba130m")
+    a = w.arrays
+    R = 48
+    g = synth.rng_for(1, 13)
+    t = {k: (None if v is None else torch.from_numpy(v).to(dev)) for k, v in a.items()}
+    dt_low = torch.from_numpy((0.5 * g.standard_normal((w.batch, w.L, R))).astype(np.float32)).to(dev)
+    W_dt = torch.from_numpy((g.standard_normal((w.Dm, R)) / np.sqrt(R)).astype(np.float32)).to(dev)
+    y = torch.empty_like(t["u"])
+    last = torch.empty((w.batch, w.Dm, w.N), device=dev)
+
+    def step():
+        ss.ss_fwd_dtproj(t["u"], dt_low, W_dt, t["delta_bias"], t["A_log"], t["B"], t["C"], t["D"], t["z"], y=y,
+                         last_state=last)
+    total_ms, launch_ms, clocks = time_step_fn(step, args, local_rank)
+    err = ss.device_error(clear=True)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} after the timed region")
+    units = updates_per_step(w)
+    # read u, z and write y; dt_low; B, C; params (W_dt, A_log, D, bias); last_state
+    alg = (w.batch * w.L * (3 * w.Dm + R + 2 * w.N) * 4 + w.Dm * (R + w.N + 2) * 4 + w.batch * w.Dm * w.N * 4)
+    hbm_peak, peak_kind = peaks()
+    sfu_peak = GB300_SMS * SFU_EX2_PER_CLK_PER_SM * GB300_MAX_SM_MHZ * 1e6
+    fma_peak = GB300_SMS * 128 * GB300_MAX_SM_MHZ * 1e6          # fp32 FMA lanes per second
+    achieved = alg / (launch_ms / 1e3) / 1e9
+    kernel = "ss_fwd_lane_kernel(lpc=4,dtproj)"
+    print(json.dumps({
+        "metric": "selective-scan state-updates/s (B·L·D·N), dt_proj folded in, 1×GB300",
+        "value": units * args.steps / (total_ms / 1e3), "unit": "state-updates/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "dtproj_130m: batch=8 L=2048 Dm=1536 N=16 dt_rank=48 io=f32",
+                   "l2": "no flush: working set 310 MB > 129 MB L2"},
+        "gpu_launches": args.steps, "clocks": clocks,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": measured_traffic("dtproj_130m", kernel), "kernel": kernel, "launch_ms": launch_ms,
+                     "alg_bytes_per_launch": alg, "t_hbm_us": alg / (hbm_peak * 1e9) * 1e6,
+                     "t_sfu_us": units / sfu_peak * 1e6,
+                     "t_fma_us": w.batch * w.L * w.Dm * R / fma_peak * 1e6}}))
+    return 0
+
+
 def bench_conv1d(args, local_rank):
     """The causal conv1d + SiLU (ss_conv1d) on the conv input of the 130m-shaped layer (batch 8,
     L 2048, Dm 1536, fp32), window in and out: one launch per step."""
@@ -543,13 +595,14 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     from selective_state_space_scan_gb300 import synth
-    if args.workload in ("conv1d_130m", "bwd_130m", "lti_130m"):
+    if args.workload in ("conv1d_130m", "bwd_130m", "lti_130m", "dtproj_130m"):
         if args.impl == "reference" or world > 1:
             if rank == 0:
                 print(json.dumps({"impl": args.impl,
                                   "unavailable": f"{args.workload} is measured on one GPU, ours only"}))
             return 0
-        fn = {"conv1d_130m": bench_conv1d, "bwd_130m": bench_bwd, "lti_130m": bench_lti}[args.workload]
+        fn = {"conv1d_130m": bench_conv1d, "bwd_130m": bench_bwd, "lti_130m": bench_lti,
+              "dtproj_130m": bench_dtproj}[args.workload]
         return fn(args, local_rank)
     w = synth.config(args.workload)
 

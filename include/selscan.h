@@ -157,6 +157,28 @@ ss_status ss_fwd_h0(const void* u, const void* delta_raw, const float* delta_bia
                     int64_t L, int64_t Dm, int64_t N, const ss_fwd_strides* strides,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Forward pass with the low-rank time-step projection folded in: the pre-softplus time step is
+ *   delta_raw[b,t,d] = Σ_k W_dt[d,k] · dt_low[b,t,k]   (k < dt_rank)
+ * computed inside the scan instead of being read as a [batch, L, Dm] tensor.  This is the
+ * "dtProj–scan fusion" of SpeechLens kernel-optimization.md (the rank-R delta projection
+ * folded into the scan kernel; rejected there on Apple GPUs as slower at high sample rates).
+ *   dt_low           [batch, L, dt_rank] fp32, strides strides->delta_b / delta_l (rows at
+ *                    least dt_rank apart); 16-byte aligned base and row stride a multiple of
+ *                    16 bytes
+ *   W_dt             [Dm, dt_rank] fp32 contiguous, 16-byte aligned
+ *   dt_rank          4..64, a multiple of 4 (else SS_ERR_UNSUPPORTED)
+ *   h0               as ss_fwd_h0 (NULL = zeros)
+ * Other arguments as ss_fwd (delta_raw replaced).  fp32 I/O only, and every tensor must allow
+ * TMA-fed tiles (16-byte aligned bases and strides, B/C rows of exactly 4, 8 or 16 states):
+ * otherwise SS_ERR_UNSUPPORTED, with no fallback.  One CTA per 32-channel tile, 48-step chunks.
+ */
+ss_status ss_fwd_dtproj(const void* u, const void* dt_low, const float* W_dt, int64_t dt_rank,
+                        const float* delta_bias, const float* A_log, const void* B, const void* C,
+                        const float* D, const void* z, void* y, float* last_state, const float* h0,
+                        int64_t batch, int64_t L, int64_t Dm, int64_t N, const ss_fwd_strides* strides,
+                        void* stream);
+
 /* Size of the fixed device array ss_fwd_static uses as its workspace (1 MiB). */
 #define SS_STATIC_WORKSPACE_BYTES ((size_t)1 << 20)
 

@@ -12,7 +12,7 @@ from typing import Optional
 
 from . import _build
 
-__all__ = ["ss_fwd", "ss_step", "ss_conv1d", "ss_bwd", "ss_fwd_workspace_size", "SelscanError", "lib", "device_error",
+__all__ = ["ss_fwd", "ss_fwd_dtproj", "ss_step", "ss_conv1d", "ss_bwd", "ss_fwd_workspace_size", "SelscanError", "lib", "device_error",
            "version", "status_string", "SS_F32", "SS_BF16", "FwdStrides", "StepStrides", "ConvStrides"]
 
 SS_F32, SS_BF16 = 0, 1
@@ -56,6 +56,8 @@ def lib() -> ctypes.CDLL:
         L.ss_fwd_ws.restype = ctypes.c_int
         L.ss_fwd_h0.argtypes = [vp] * 11 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp, ctypes.c_size_t, vp]
         L.ss_fwd_h0.restype = ctypes.c_int
+        L.ss_fwd_dtproj.argtypes = [vp] * 3 + [i64] + [vp] * 9 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp]
+        L.ss_fwd_dtproj.restype = ctypes.c_int
         L.ss_fwd_workspace_size.argtypes = [i64] * 4 + [ctypes.c_int32]
         L.ss_fwd_workspace_size.restype = ctypes.c_size_t
         L.ss_step.argtypes = [vp] * 10 + [i64] * 3 + [ctypes.POINTER(StepStrides), vp]
@@ -193,6 +195,34 @@ def ss_fwd(u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, last_s
         where = "ss_fwd"
     if st != 0:
         raise SelscanError(st, where)
+    return y
+
+
+def ss_fwd_dtproj(u, dt_low, W_dt, delta_bias, A_log, B, C, D=None, z=None, y=None, last_state=None,
+                  h0=None, stream=None):
+    """Forward pass with the low-rank time-step projection folded in (ss_fwd_dtproj):
+    delta_raw[b,t,d] = sum_k W_dt[d,k] dt_low[b,t,k] is computed inside the kernel.
+    dt_low [batch, L, R] float32 (last axis stride 1), W_dt [Dm, R] float32 contiguous; the rest
+    as ss_fwd (float32 I/O).  Returns y."""
+    import torch
+    batch, L, Dm = u.shape
+    N = A_log.shape[1]
+    R = W_dt.shape[1]
+    io = _io_code(u.dtype)
+    if y is None:
+        y = torch.empty((batch, L, Dm), dtype=u.dtype, device=u.device)
+    for name, t in (("u", u), ("dt_low", dt_low), ("z", z), ("y", y), ("B", B), ("C", C)):
+        _check_inner(t, name)
+    if not W_dt.is_contiguous() or W_dt.dtype != torch.float32:
+        raise ValueError("W_dt must be a contiguous float32 [Dm, R] tensor")
+    s = FwdStrides(io, u.stride(0), u.stride(1), dt_low.stride(0), dt_low.stride(1),
+                   z.stride(0) if z is not None else 0, z.stride(1) if z is not None else 0,
+                   y.stride(0), y.stride(1), B.stride(0), B.stride(1), C.stride(0), C.stride(1))
+    st = lib().ss_fwd_dtproj(_ptr(u), _ptr(dt_low), _ptr(W_dt), R, _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C),
+                             _ptr(D), _ptr(z), _ptr(y), _ptr(last_state), _ptr(h0), batch, L, Dm, N,
+                             ctypes.byref(s), _stream_handle(stream))
+    if st != 0:
+        raise SelscanError(st, "ss_fwd_dtproj")
     return y
 
 

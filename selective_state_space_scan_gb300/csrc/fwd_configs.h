@@ -25,6 +25,13 @@ constexpr int lane_minb(int lpc) { return lpc == 4 ? SS_LANE_MINB4 : lpc == 2 ? 
 // Tile width: 32 channels for one CTA per tile; 16 for the balanced schedule, which needs at
 // least as many tiles as resident CTAs (a lane family tile is whole warps of 32/lpc channels).
 constexpr int lane_w(int lpc, bool balanced) { return balanced && lpc > 1 ? 16 : 32; }
+// With the low-rank time-step projection folded in: 48-step chunks (the staged dt_low tile
+// replaces the Δ tile and is wider), ranks up to 64, rows padded to an odd number of 16-byte
+// chunks (at most 68 floats).
+constexpr int kLaneTD = 48;
+constexpr int kDtRankMax = 64;
+constexpr int kDtPitchMax = 68;
+constexpr int dt_pitch(int rank) { return (rank / 4) % 2 == 1 ? rank : rank + 4; }
 
 // Segment-lane family (time-parallel; few channels, long sequences): 8 channels per CTA,
 // each warp holds 4 time segments of those 8 channels, 8 warps.  K = 7 steps per thread

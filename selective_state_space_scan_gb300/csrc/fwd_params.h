@@ -46,6 +46,11 @@ struct FwdParams {
     int nseg;            // segments per tile in the schedule
     float* seg_slots;    // [nseg][batch·Dm·N]
     float* seg_dsum;     // [nseg - 1][batch·Dm]
+    // Low-rank time-step projection folded in (dt_rank > 0): `delta` points to dt_low
+    // [batch, L, dt_rank] (strides d_b, d_l) and delta_raw[b,t,d] = Σ_k W_dt[d,k] dt_low[b,t,k].
+    const float* W_dt;   // [Dm, dt_rank] contiguous
+    int dt_rank;
+    int dt_pitch;        // floats per staged dt_low row (dt_rank rounded up so that rows fall on different banks)
 };
 
 // TMA descriptors for the five streamed tensors (unused by the plain-load variant).

@@ -22,6 +22,7 @@ struct FwdVariant {
     bool balanced;   // lane family: equal (tile, chunk) ranges per CTA (needs a workspace, TMA)
     bool state_only; // lane family, TMA: pass A of the time-split schedule (end states only)
     bool lti;        // lane family, TMA, per tile: B and C constant over the steps (held in registers)
+    bool dtp;        // lane family, TMA, per tile: the low-rank time-step projection folded in
 };
 
 struct FwdGeom {
@@ -32,6 +33,7 @@ struct FwdGeom {
 
 inline FwdGeom fwd_geometry(const FwdVariant& v) {
     if (v.family == kFamSeg) return FwdGeom{8 * kSegG, 8 * kSegG, 4 * kSegQ * kSegK};
+    if (v.dtp) return FwdGeom{32, 32, kLaneTD};
     return FwdGeom{lane_w(v.lpc, v.balanced), lane_w(v.lpc, v.balanced), kLaneT};
 }
 
@@ -44,6 +46,8 @@ cudaError_t launch_fwd_lane_bf16(const FwdVariant& v, const FwdParams& p, const 
 cudaError_t launch_fwd_seg(const FwdVariant& v, bool bf16, const FwdParams& p, const FwdMaps& m,
                            cudaStream_t stream);
 cudaError_t launch_step(const StepParams& p, bool bf16, bool vec, cudaStream_t stream);
+// The lane kernel with the low-rank time-step projection folded in (fp32, per tile, TMA).
+cudaError_t launch_fwd_lane_dtp(const FwdVariant& v, const FwdParams& p, const FwdMaps& m, cudaStream_t stream);
 // Time-split carry pass: slot 0 of p.seg_slots = h0 (or zeros); slot s = exp(A·ΣΔ of segment
 // s-1)·slot s-1 + the end state pass A left in slot s, for s = 1 .. p.nseg - 1.
 cudaError_t launch_fwd_carry(const FwdParams& p, cudaStream_t stream);

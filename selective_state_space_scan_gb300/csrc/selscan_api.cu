@@ -161,6 +161,7 @@ FwdVariant choose_fwd_variant(int64_t batch, int64_t Dm, int64_t N) {
     v.balanced = false;
     v.state_only = false;
     v.lti = false;
+    v.dtp = false;
     return v;
 }
 
@@ -309,10 +310,15 @@ cudaError_t lane_max_grid(const FwdVariant& v, bool bf16, int* out) {
 ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
                    const void* B, const void* C, const float* D, const void* z, void* y,
                    float* last_state, const float* h0, int64_t batch, int64_t L, int64_t Dm, int64_t N,
-                   const ss_fwd_strides* strides, void* workspace, size_t ws_bytes, void* stream_ptr) {
+                   const ss_fwd_strides* strides, void* workspace, size_t ws_bytes, void* stream_ptr,
+                   const float* W_dt = nullptr, int64_t R = 0) {
+    // W_dt != nullptr: the low-rank time-step projection is folded in; `delta_raw` is then dt_low
+    // [batch, L, R] (strides delta_b, delta_l) and delta_raw[b,t,d] = Σ_k W_dt[d,k] dt_low[b,t,k].
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    const bool dtp = W_dt != nullptr;
     if (batch < 0 || L < 0 || Dm < 0) return SS_ERR_INVALID_ARG;
     if (N < 1 || N > 16) return SS_ERR_UNSUPPORTED;
+    if (dtp && (R < 4 || R > kDtRankMax || R % 4 != 0)) return SS_ERR_UNSUPPORTED;
     ss_fwd_strides s;
     if (strides) {
         s = *strides;
@@ -327,9 +333,11 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     if (s.io_dtype != SS_F32 && s.io_dtype != SS_BF16) return SS_ERR_INVALID_ARG;
     const bool bf16 = s.io_dtype == SS_BF16;
     const int64_t es = bf16 ? 2 : 4;
+    if (dtp && bf16) return SS_ERR_UNSUPPORTED;
     if (batch == 0 || Dm == 0) return SS_OK;
     if (!A_log) return SS_ERR_INVALID_ARG;
     if (h0 && !aligned(h0, 4)) return SS_ERR_MISALIGNED;
+    const int64_t dcols = dtp ? R : Dm;   // columns of the time-step input
     const Span sh = span3(h0, batch, Dm, N, Dm * N, N, 4);
     const Span sl = span3(last_state, batch, Dm, N, Dm * N, N, 4);
     // h0 may be last_state itself (continue in place) but not overlap it otherwise
@@ -353,12 +361,12 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
                           z ? s.z_b : 0, z ? s.z_l : 0};
     for (int64_t v : st)
         if (v < 0) return SS_ERR_INVALID_ARG;
-    if (s.u_l < Dm || s.delta_l < Dm || s.y_l < Dm || (z && s.z_l < Dm)) {
+    if (s.u_l < Dm || s.delta_l < dcols || s.y_l < Dm || (z && s.z_l < Dm)) {
         if (L > 1) return SS_ERR_INVALID_ARG;
     }
     // B, C: rows at least N apart, or step stride 0 (time-invariant, the LTI case)
     if (((s.B_l < N && s.B_l != 0) || (s.C_l < N && s.C_l != 0)) && L > 1) return SS_ERR_INVALID_ARG;
-    const bool lti = L > 1 && s.B_l == 0 && s.C_l == 0;
+    const bool lti = L > 1 && s.B_l == 0 && s.C_l == 0 && !dtp;
     if (L > INT32_MAX || Dm > INT32_MAX || batch > INT32_MAX) return SS_ERR_UNSUPPORTED;
     // alignment to the element type
     const void* io_ptrs[] = {u, delta_raw, B, C, y, z};
@@ -367,17 +375,19 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     const void* f_ptrs[] = {A_log, D, delta_bias, last_state, h0};
     for (const void* p : f_ptrs)
         if (p && !aligned(p, 4)) return SS_ERR_MISALIGNED;
+    if (dtp && !aligned(W_dt, 16)) return SS_ERR_MISALIGNED;
     // device memory of the current device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
-    const void* all_ptrs[] = {u, delta_raw, B, C, y, z, A_log, D, delta_bias, last_state, h0};
+    const void* all_ptrs[] = {u, delta_raw, B, C, y, z, A_log, D, delta_bias, last_state, h0, W_dt};
     for (const void* p : all_ptrs)
         if (p && !is_device_pointer(p, dev)) return SS_ERR_INVALID_ARG;
     // outputs must not overlap inputs
     const Span sy = span3(y, batch, L, Dm, s.y_b, s.y_l, es);
     if (overlap(sy, sh)) return SS_ERR_INVALID_ARG;
     const Span ins[] = {span3(u, batch, L, Dm, s.u_b, s.u_l, es),
-                        span3(delta_raw, batch, L, Dm, s.delta_b, s.delta_l, es),
+                        span3(delta_raw, batch, L, dcols, s.delta_b, s.delta_l, es),
+                        span3(W_dt, 1, Dm, R, 0, R, 4),
                         span3(z, batch, L, Dm, s.z_b, s.z_l, es),
                         span3(B, batch, L, N, s.B_b, s.B_l, es),
                         span3(C, batch, L, N, s.C_b, s.C_l, es),
@@ -396,6 +406,11 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     const int max_lpc = v.ns / 4;
     const int ff = g_force_family.load(), fl = g_force_lpc.load(), ft = g_force_tma.load();
     if (ff >= 0) v.family = ff;
+    if (dtp) {                           // lane family only, as many lanes per channel as allowed
+        if (v.family != kFamLane) v.lpc = max_lpc;
+        v.family = kFamLane;
+        v.dtp = true;
+    }
     if (fl > 0) {
         if (fl > max_lpc) return SS_ERR_UNSUPPORTED;
         v.lpc = fl;
@@ -423,7 +438,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     // from zero; carry pass; pass C: the fold from each segment's carried start).
     const int fs = g_force_nseg.load();
     SplitPlan plan;
-    if (workspace && tma && !lti && fs != 0 && (fs >= 2 || (v.family == kFamSeg && ff < 0))) {
+    if (workspace && tma && !lti && !dtp && fs != 0 && (fs >= 2 || (v.family == kFamSeg && ff < 0))) {
         FwdVariant vs = v;
         vs.family = kFamLane;
         if (fl <= 0) vs.lpc = vs.ns / 4;
@@ -446,7 +461,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     // rejects is served by the plain-load fill.
     // The schedule fixes the tile width (and so the box width): decide it first.  With a
     // workspace, TMA-fed lane kernels that do not take the time split run the balanced one.
-    v.balanced = plan.nseg < 2 && workspace != nullptr && v.family == kFamLane && tma && !v.lti &&
+    v.balanced = plan.nseg < 2 && workspace != nullptr && v.family == kFamLane && tma && !v.lti && !dtp &&
                  g_force_balanced.load() != 0;
     FwdMaps maps;
     std::memset(&maps, 0, sizeof(maps));
@@ -455,12 +470,14 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         const bool swbc = v.family == kFamSeg;
         const int bw = g0.box_channels, bh = g0.chunk_steps;
         tma = make_map(&maps.u, u, bf16, Dm, L, batch, s.u_l, s.u_b, bw, bh, true) &&
-              make_map(&maps.delta, delta_raw, bf16, Dm, L, batch, s.delta_l, s.delta_b, bw, bh, true) &&
+              (dtp ? make_map(&maps.delta, delta_raw, false, R, L, batch, s.delta_l, s.delta_b,
+                              dt_pitch(static_cast<int>(R)), bh, false)
+                   : make_map(&maps.delta, delta_raw, bf16, Dm, L, batch, s.delta_l, s.delta_b, bw, bh, true)) &&
               (!z || make_map(&maps.z, z, bf16, Dm, L, batch, s.z_l, s.z_b, bw, bh, true)) &&
               (v.lti || (make_map(&maps.B, B, bf16, N, L, batch, s.B_l, s.B_b, v.ns, bh, swbc) &&
                          make_map(&maps.C, C, bf16, N, L, batch, s.C_l, s.C_b, v.ns, bh, swbc)));
     }
-    if (ft == 1 && !tma) return SS_ERR_UNSUPPORTED;
+    if ((ft == 1 || dtp) && !tma) return SS_ERR_UNSUPPORTED;   // the folded projection is TMA-fed only
     v.tma = tma;
     if (!tma) v.lti = false;
     if (!tma) {                     // descriptors refused: the plain-load fill, per-tile schedule
@@ -490,6 +507,12 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     p.box_channels = tma ? geo.box_channels : 0;
     p.err = device_error_ptr();
     if (!p.err) return SS_ERR_CUDA;
+    if (dtp) {
+        p.W_dt = W_dt;
+        p.dt_rank = static_cast<int>(R);
+        p.dt_pitch = dt_pitch(static_cast<int>(R));
+        return cuda_status(launch_fwd_lane_dtp(v, p, maps, stream));
+    }
     if (v.balanced) {
         // grid: every CTA resident at once (cooperative launch), never more CTAs than tiles
         int max_grid = 0;
@@ -552,6 +575,15 @@ ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias, 
                  const ss_fwd_strides* strides, void* stream) {
     return fwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, y, last_state, nullptr, batch, L, Dm, N,
                     strides, nullptr, 0, stream);
+}
+
+ss_status ss_fwd_dtproj(const void* u, const void* dt_low, const float* W_dt, int64_t dt_rank,
+                        const float* delta_bias, const float* A_log, const void* B, const void* C, const float* D,
+                        const void* z, void* y, float* last_state, const float* h0, int64_t batch, int64_t L,
+                        int64_t Dm, int64_t N, const ss_fwd_strides* strides, void* stream) {
+    if (!W_dt || !dt_low) return SS_ERR_INVALID_ARG;
+    return fwd_impl(u, dt_low, delta_bias, A_log, B, C, D, z, y, last_state, h0, batch, L, Dm, N, strides,
+                    nullptr, 0, stream, W_dt, dt_rank);
 }
 
 ss_status ss_fwd_ws(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,

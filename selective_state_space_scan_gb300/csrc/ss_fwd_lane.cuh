@@ -45,7 +45,9 @@
 
 namespace selscan {
 
-template <typename TIO_, int NS_, int LPC_, int W_, int T_, int STAGES_, int MINB_>
+// DTR > 0: the low-rank time-step projection is folded in; the Δ tile's place holds a
+// [T][DTR-float-pitch] dt_low tile instead.
+template <typename TIO_, int NS_, int LPC_, int W_, int T_, int STAGES_, int MINB_, int DTR_ = 0>
 struct LaneCfg {
     using TIO = TIO_;
     static constexpr int NS = NS_;            // states handled (4, 8 or 16; N <= NS)
@@ -54,6 +56,7 @@ struct LaneCfg {
     static constexpr int T = T_;              // steps per chunk
     static constexpr int STAGES = STAGES_;
     static constexpr int MINB = MINB_;
+    static constexpr int DTR = DTR_;          // dt_low row pitch bound (floats); 0: Δ tile
     static constexpr int CPW = 32 / LPC;      // channels per warp
     static constexpr int WARPS = W / CPW;     // warps per CTA
     static constexpr int THREADS = 32 * WARPS;
@@ -66,22 +69,25 @@ struct LaneCfg {
     static constexpr int RB = W * ES;                         // bytes of one tile row (W channels)
     static constexpr int TILE_X = T * RB;                     // one tensor's [T][W] tile, swizzled
     static constexpr int TILE_N = T * NS * ES;
+    static constexpr int TILE_D = DTR > 0 ? up1024(T * DTR * 4) : TILE_X;
     static constexpr int OFF_U = 0;
     static constexpr int OFF_D = TILE_X;
-    static constexpr int OFF_Z = 2 * TILE_X;
-    static constexpr int OFF_B = 3 * TILE_X;
+    static constexpr int OFF_Z = OFF_D + TILE_D;
+    static constexpr int OFF_B = OFF_Z + TILE_X;
     static constexpr int OFF_C = OFF_B + up128(TILE_N);
     static constexpr int STAGE_BYTES = up1024(OFF_C + up128(TILE_N));   // keeps every tile 1 KB aligned
     static constexpr int AUX_BC = 0;                                       // fp32 B,C [2][T][NS]
     static constexpr int AUX_FLAG = AUX_BC + (CONVERT_BC ? 2 * T * NS * 4 : 0);
     static constexpr int AUX_DONE = AUX_FLAG + 16;                        // per-stage warp counters
     static constexpr int AUX_BAR = AUX_DONE + ((STAGES * 4 + 15) / 16) * 16;
-    static constexpr int AUX_BYTES = AUX_BAR + STAGES * 8;
+    static constexpr int AUX_W = AUX_BAR + ((STAGES * 8 + 15) / 16) * 16;   // DTR > 0: W_dt rows [W][DTR]
+    static constexpr int AUX_BYTES = AUX_W + (DTR > 0 ? W * DTR * 4 : 0);
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + AUX_BYTES;
     static_assert(RB == 128 || RB == 64 || RB == 32, "a tile row must be one TMA swizzle span");
     static_assert(NS % (4 * LPC) == 0, "each lane must hold whole state quads");
     static_assert(W % CPW == 0 && WARPS >= 1, "a tile is whole warps");
     static_assert(T % LPC == 0 && T <= 256, "chunk must be whole groups and one TMA box");
+    static_assert(DTR == 0 || ES == 4, "the folded projection is built for fp32 I/O");
 };
 
 // A CTA's work in processing order: up to three runs of (tile, chunk) units.
@@ -175,17 +181,20 @@ __device__ void lane_fill_generic(uint8_t* st, const FwdParams& p, int b, int d0
 
 // WITH_C = false (pass A of the time split) skips the C tile; has_z = false the z tile; LTI
 // (time-invariant B and C, held in registers) both B/C tiles.
+// With the projection folded in (Cfg::DTR > 0) the Δ box is the chunk's [T][dt_pitch] dt_low
+// rows (shared by all channels, x = 0).
 template <class Cfg, bool WITH_C, bool LTI = false>
 __device__ __forceinline__ void lane_issue_tma(uint8_t* st, uint64_t* bar, const FwdMaps& m,
-                                               bool has_z, int b, int d0, int chunk) {
-    const uint32_t bytes = (has_z ? 3u : 2u) * Cfg::TILE_X + (LTI ? 0u : (WITH_C ? 2u : 1u) * Cfg::TILE_N);
+                                               bool has_z, int b, int d0, int chunk, int dt_pitch) {
+    const uint32_t d_bytes = Cfg::DTR > 0 ? static_cast<uint32_t>(Cfg::T * dt_pitch * 4) : Cfg::TILE_X;
+    const uint32_t bytes = (has_z ? 2u : 1u) * Cfg::TILE_X + d_bytes + (LTI ? 0u : (WITH_C ? 2u : 1u) * Cfg::TILE_N);
     mbar_expect_tx(bar, bytes);
     const int t0 = chunk * Cfg::T;
     // one [T][W] box per stream (rows of W channels, hardware swizzle), one [T][NS] box for B, C.
     // (L2 eviction hints were measured: evict-first on the streams re-fetched lines that a
     // neighbouring tile still needed, evict-last on B/C changed nothing; none are used.)
     tma_load_3d(st + Cfg::OFF_U, &m.u, bar, d0, t0, b);
-    tma_load_3d(st + Cfg::OFF_D, &m.delta, bar, d0, t0, b);
+    tma_load_3d(st + Cfg::OFF_D, &m.delta, bar, Cfg::DTR > 0 ? 0 : d0, t0, b);
     if (has_z) tma_load_3d(st + Cfg::OFF_Z, &m.z, bar, d0, t0, b);
     if (!LTI) {
         tma_load_3d(st + Cfg::OFF_B, &m.B, bar, 0, t0, b);
@@ -283,7 +292,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
         int tl, chk;
         work.unit(k, nchunks, tl, chk);
         lane_issue_tma<Cfg, !STATE_ONLY, LTI>(st, bar, maps, has_z, tl / p.tiles_per_batch,
-                            (tl % p.tiles_per_batch) * Cfg::W, chk);
+                            (tl % p.tiles_per_batch) * Cfg::W, chk, p.dt_pitch);
     };
     if (USE_TMA && tid == 0) {
         const int pre = total < STAGES ? total : STAGES;
@@ -353,6 +362,16 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             }
         }
         dsum = 0.f;
+        if constexpr (Cfg::DTR > 0) {
+            // the tile's W_dt rows, [W][dt_pitch] (zeros past Dm); one piece per CTA on this path
+            float* sW = reinterpret_cast<float*>(aux + Cfg::AUX_W);
+            const int d0 = (tile % p.tiles_per_batch) * Cfg::W;
+            for (int i = tid; i < Cfg::W * p.dt_rank; i += Cfg::THREADS) {
+                const int r = i / p.dt_rank, k = i % p.dt_rank;
+                sW[r * p.dt_pitch + k] = d0 + r < p.Dm ? p.W_dt[static_cast<int64_t>(d0 + r) * p.dt_rank + k] : 0.f;
+            }
+            __syncthreads();
+        }
         if constexpr (!STATE_ONLY) {
             const float* src = nullptr;    // the state before this unit's first chunk
             if (p.seg_launch > 0) {
@@ -436,11 +455,39 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                 // Phase 1: Δ and Δ·u of the steps this lane prepares (step g·LPC + j of each group;
                 // zero past L, i.e. identity pairs).  G independent softplus chains.
                 float dd[G], du[G];
+                if constexpr (Cfg::DTR > 0) {
+                    // delta_raw = Σ_k W_dt[d,k] · dt_low[t,k] for this lane's G steps, four ranks at a
+                    // time: the W row from the tile's shared copy, the dt_low rows broadcast from
+                    // the staged tile; packed pairs carry the even- and odd-rank partial sums
+                    const float* trow = reinterpret_cast<const float*>(td) + (g0 * LPC + j) * p.dt_pitch;
+                    const float4* wrow = reinterpret_cast<const float4*>(
+                        reinterpret_cast<const float*>(aux + Cfg::AUX_W) + cw * p.dt_pitch);
+                    float2 xr[G];
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float x = softplus(at(td, g0, g) + bias_w);
-                    dd[g] = x;
-                    du[g] = x * at(tu, g0, g);
+                    for (int g = 0; g < G; ++g) xr[g] = make_float2(0.f, 0.f);
+#pragma unroll 2
+                    for (int k4 = 0; k4 < p.dt_rank / 4; ++k4) {
+                        const float4 w4 = wrow[k4];
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            const float4 x4 = *reinterpret_cast<const float4*>(trow + g * LPC * p.dt_pitch + 4 * k4);
+                            xr[g] = fma2(make_float2(w4.x, w4.y), make_float2(x4.x, x4.y), xr[g]);
+                            xr[g] = fma2(make_float2(w4.z, w4.w), make_float2(x4.z, x4.w), xr[g]);
+                        }
+                    }
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float x = softplus((xr[g].x + xr[g].y) + bias_w);
+                        dd[g] = x;
+                        du[g] = x * at(tu, g0, g);
+                    }
+                } else {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float x = softplus(at(td, g0, g) + bias_w);
+                        dd[g] = x;
+                        du[g] = x * at(tu, g0, g);
+                    }
                 }
                 if (!whole) {
 #pragma unroll
