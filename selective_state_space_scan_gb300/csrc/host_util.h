@@ -1,4 +1,4 @@
-// Host-side argument checks shared by the entry points of ss_conv1d.cu and ss_bwd.cu.
+// Host-side argument checks shared by every entry point (selscan_api.cu, ss_conv1d.cu, ss_bwd.cu).
 #pragma once
 
 #include <cuda_runtime.h>

@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "../../include/selscan.h"
+#include "host_util.h"
 #include "internal.h"
 
 namespace selscan {
@@ -88,33 +89,14 @@ void* static_workspace_ptr() {
     return p;
 }
 
-bool is_device_pointer(const void* p, int dev) {
-    cudaPointerAttributes a;
-    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    if (a.type == cudaMemoryTypeManaged) return true;
-    return a.type == cudaMemoryTypeDevice && a.device == dev;
+// Argument checks shared with the other entry points (host_util.h).
+using host::Range;
+inline bool is_device_pointer(const void* p, int dev) { return host::dev_ptr(p, dev); }
+inline bool aligned(const void* p, size_t a) { return host::is_aligned(p, a); }
+inline Range span3(const void* p, int64_t n0, int64_t n1, int64_t n2, int64_t s0, int64_t s1, int64_t es) {
+    return host::range3(p, n0, n1, n2, s0, s1, es);
 }
-
-bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// Byte range touched by a [n0, n1, n2] tensor with element strides (s0, s1, 1).
-struct Span {
-    uintptr_t lo = 0, hi = 0;
-    bool empty() const { return hi <= lo; }
-};
-Span span3(const void* p, int64_t n0, int64_t n1, int64_t n2, int64_t s0, int64_t s1, int64_t es) {
-    Span s;
-    if (!p || n0 <= 0 || n1 <= 0 || n2 <= 0) return s;
-    s.lo = reinterpret_cast<uintptr_t>(p);
-    s.hi = s.lo + static_cast<uintptr_t>(((n0 - 1) * s0 + (n1 - 1) * s1 + n2) * es);
-    return s;
-}
-bool overlap(const Span& a, const Span& b) {
-    return !a.empty() && !b.empty() && a.lo < b.hi && b.lo < a.hi;
-}
+inline bool overlap(const Range& a, const Range& b) { return host::meet(a, b); }
 
 ss_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SS_OK : SS_ERR_CUDA; }
 
@@ -338,8 +320,8 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     if (!A_log) return SS_ERR_INVALID_ARG;
     if (h0 && !aligned(h0, 4)) return SS_ERR_MISALIGNED;
     const int64_t dcols = dtp ? R : Dm;   // columns of the time-step input
-    const Span sh = span3(h0, batch, Dm, N, Dm * N, N, 4);
-    const Span sl = span3(last_state, batch, Dm, N, Dm * N, N, 4);
+    const Range sh = span3(h0, batch, Dm, N, Dm * N, N, 4);
+    const Range sl = span3(last_state, batch, Dm, N, Dm * N, N, 4);
     // h0 may be last_state itself (continue in place) but not overlap it otherwise
     if (h0 && static_cast<const void*>(h0) != static_cast<const void*>(last_state) && overlap(sh, sl))
         return SS_ERR_INVALID_ARG;
@@ -383,9 +365,9 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     for (const void* p : all_ptrs)
         if (p && !is_device_pointer(p, dev)) return SS_ERR_INVALID_ARG;
     // outputs must not overlap inputs
-    const Span sy = span3(y, batch, L, Dm, s.y_b, s.y_l, es);
+    const Range sy = span3(y, batch, L, Dm, s.y_b, s.y_l, es);
     if (overlap(sy, sh)) return SS_ERR_INVALID_ARG;
-    const Span ins[] = {span3(u, batch, L, Dm, s.u_b, s.u_l, es),
+    const Range ins[] = {span3(u, batch, L, Dm, s.u_b, s.u_l, es),
                         span3(delta_raw, batch, L, dcols, s.delta_b, s.delta_l, es),
                         span3(W_dt, 1, Dm, R, 0, R, 4),
                         span3(z, batch, L, Dm, s.z_b, s.z_l, es),
@@ -394,7 +376,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
                         span3(A_log, 1, Dm, N, 0, N, 4),
                         span3(D, 1, 1, Dm, 0, 0, 4),
                         span3(delta_bias, 1, 1, Dm, 0, 0, 4)};
-    for (const Span& in : ins)
+    for (const Range& in : ins)
         if (overlap(sy, in) || overlap(sl, in)) return SS_ERR_INVALID_ARG;
     if (overlap(sy, sl)) return SS_ERR_INVALID_ARG;
 
@@ -745,9 +727,9 @@ ss_status ss_step(float* state, const void* x, const void* delta_raw, const floa
     const void* all_ptrs[] = {state, x, delta_raw, B, C, y, z, A_log, D, delta_bias};
     for (const void* p : all_ptrs)
         if (p && !is_device_pointer(p, dev)) return SS_ERR_INVALID_ARG;
-    const Span sy = span3(y, 1, batch, Dm, 0, s.y_b, es);
-    const Span sst = span3(state, batch, Dm, N, s.state_b, s.state_d, 4);
-    const Span ins[] = {span3(x, 1, batch, Dm, 0, s.x_b, es),
+    const Range sy = span3(y, 1, batch, Dm, 0, s.y_b, es);
+    const Range sst = span3(state, batch, Dm, N, s.state_b, s.state_d, 4);
+    const Range ins[] = {span3(x, 1, batch, Dm, 0, s.x_b, es),
                         span3(delta_raw, 1, batch, Dm, 0, s.delta_b, es),
                         span3(z, 1, batch, Dm, 0, s.z_b, es),
                         span3(B, 1, batch, N, 0, s.B_b, es),
@@ -755,7 +737,7 @@ ss_status ss_step(float* state, const void* x, const void* delta_raw, const floa
                         span3(A_log, 1, Dm, N, 0, N, 4),
                         span3(D, 1, 1, Dm, 0, 0, 4),
                         span3(delta_bias, 1, 1, Dm, 0, 0, 4)};
-    for (const Span& in : ins)
+    for (const Range& in : ins)
         if (overlap(sy, in) || overlap(sst, in)) return SS_ERR_INVALID_ARG;
     if (overlap(sy, sst)) return SS_ERR_INVALID_ARG;
 
