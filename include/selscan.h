@@ -179,6 +179,34 @@ ss_status ss_fwd_dtproj(const void* u, const void* dt_low, const float* W_dt, in
                         int64_t batch, int64_t L, int64_t Dm, int64_t N, const ss_fwd_strides* strides,
                         void* stream);
 
+/*
+ * Forward pass on host-resident tensors: ss_fwd's result with the copies to and from the device
+ * inside the call.  The batch rows are processed in groups (at least four when the batch allows)
+ * through two device staging slots on three internal streams, so that the copy in of one group,
+ * the scan of another and the copy back of a third overlap.  No counterpart in the pages: it
+ * serves callers whose tensors live in host memory.
+ *   u, delta_raw, z, y   [batch, L, Dm] io_dtype, contiguous, HOST memory (pinned memory lets the
+ *                        copies run asynchronously; pageable memory works but serialises them)
+ *   B, C                 [batch, L, N] io_dtype, contiguous, host memory
+ *   A_log [Dm, N], D, delta_bias [Dm] (NULL allowed as for ss_fwd), last_state [batch, Dm, N]
+ *                        (or NULL): fp32, contiguous, host memory
+ *   workspace            device memory, 256-byte aligned, at least
+ *                        ss_fwd_host_workspace_size(...) bytes (staging only; no contents carried
+ *                        between calls)
+ *   stream               the work starts after everything enqueued on it, and it waits for the
+ *                        last copy back: y and last_state are valid on the host once the stream is
+ *                        synchronised.  L == 0 synchronises the stream and zeroes last_state.
+ * Device pointers where host memory is expected, overlapping outputs or a small workspace return
+ * SS_ERR_INVALID_ARG; errors of the scan itself are ss_fwd's.
+ */
+ss_status ss_fwd_host(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
+                      const void* B, const void* C, const float* D, const void* z, void* y,
+                      float* last_state, int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dtype,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Device workspace bytes ss_fwd_host needs (0: sizes invalid or empty). */
+size_t ss_fwd_host_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dtype);
+
 /* Size of the fixed device array ss_fwd_static uses as its workspace (1 MiB). */
 #define SS_STATIC_WORKSPACE_BYTES ((size_t)1 << 20)
 

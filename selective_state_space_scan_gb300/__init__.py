@@ -12,7 +12,7 @@ from typing import Optional
 
 from . import _build
 
-__all__ = ["ss_fwd", "ss_fwd_dtproj", "ss_step", "ss_conv1d", "ss_bwd", "ss_fwd_workspace_size", "SelscanError", "lib", "device_error",
+__all__ = ["ss_fwd", "ss_fwd_dtproj", "ss_fwd_host", "ss_step", "ss_conv1d", "ss_bwd", "ss_fwd_workspace_size", "SelscanError", "lib", "device_error",
            "version", "status_string", "SS_F32", "SS_BF16", "FwdStrides", "StepStrides", "ConvStrides"]
 
 SS_F32, SS_BF16 = 0, 1
@@ -58,6 +58,10 @@ def lib() -> ctypes.CDLL:
         L.ss_fwd_h0.restype = ctypes.c_int
         L.ss_fwd_dtproj.argtypes = [vp] * 3 + [i64] + [vp] * 9 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp]
         L.ss_fwd_dtproj.restype = ctypes.c_int
+        L.ss_fwd_host.argtypes = [vp] * 10 + [i64] * 4 + [ctypes.c_int32, vp, ctypes.c_size_t, vp]
+        L.ss_fwd_host.restype = ctypes.c_int
+        L.ss_fwd_host_workspace_size.argtypes = [i64] * 4 + [ctypes.c_int32]
+        L.ss_fwd_host_workspace_size.restype = ctypes.c_size_t
         L.ss_fwd_workspace_size.argtypes = [i64] * 4 + [ctypes.c_int32]
         L.ss_fwd_workspace_size.restype = ctypes.c_size_t
         L.ss_step.argtypes = [vp] * 10 + [i64] * 3 + [ctypes.POINTER(StepStrides), vp]
@@ -223,6 +227,35 @@ def ss_fwd_dtproj(u, dt_low, W_dt, delta_bias, A_log, B, C, D=None, z=None, y=No
                              ctypes.byref(s), _stream_handle(stream))
     if st != 0:
         raise SelscanError(st, "ss_fwd_dtproj")
+    return y
+
+
+def ss_fwd_host(u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, last_state=None, stream=None,
+                device=None):
+    """Forward pass on host (CPU) tensors (ss_fwd_host): copies in, scan and copies back happen
+    inside the call, overlapped over groups of batch rows.  All tensors are contiguous CPU tensors
+    (pinned memory for asynchronous copies); ``y`` and ``last_state`` (optional) are written and
+    valid once the stream is synchronised.  The device staging workspace is cached per (device,
+    stream).  Returns y."""
+    import torch
+    batch, L, Dm = u.shape
+    N = A_log.shape[1]
+    io = _io_code(u.dtype)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if y is None:
+        y = torch.empty((batch, L, Dm), dtype=u.dtype, pin_memory=True)
+    for name, t in (("u", u), ("delta_raw", delta_raw), ("z", z), ("B", B), ("C", C), ("y", y), ("A_log", A_log),
+                    ("D", D), ("delta_bias", delta_bias), ("last_state", last_state)):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+    sh = _stream_handle(stream)
+    nbytes = int(lib().ss_fwd_host_workspace_size(batch, L, Dm, N, io))
+    ws = workspace_for(dev, sh, nbytes, purpose="host") if nbytes else None
+    st = lib().ss_fwd_host(_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D),
+                           _ptr(z), _ptr(y), _ptr(last_state), batch, L, Dm, N, io,
+                           None if ws is None else ws.data_ptr(), 0 if ws is None else ws.numel(), sh)
+    if st != 0:
+        raise SelscanError(st, "ss_fwd_host")
     return y
 
 
