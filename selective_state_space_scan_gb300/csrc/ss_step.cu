@@ -18,6 +18,10 @@
 
 namespace selscan {
 
+// Threads per block: small blocks (2 warps) measured 5% faster per layer than 256-thread ones
+// (11.1 against 11.7 us on the 48-layer decode), 32 or 512 slower.
+constexpr int kStepThreads = 64;
+
 template <typename TIO> struct Vec4;
 template <> struct Vec4<float> {
     using T = float4;
@@ -46,8 +50,8 @@ __device__ __forceinline__ float step_quad(float4& hv, const float4& av, const f
 }
 
 template <typename TIO, int LPR, int RPT, bool VEC>
-__global__ void __launch_bounds__(256) ss_step_kernel(const StepParams p) {
-    constexpr int ROWS_PASS = 256 / LPR;             // rows one pass of the block covers
+__global__ void __launch_bounds__(kStepThreads) ss_step_kernel(const StepParams p) {
+    constexpr int ROWS_PASS = kStepThreads / LPR;    // rows one pass of the block covers
     const int blocks_per_b = static_cast<int>((static_cast<int64_t>(p.Dm) + ROWS_PASS * RPT - 1) / (ROWS_PASS * RPT));
     const int b = static_cast<int>(blockIdx.x) / blocks_per_b;
     const int blk = static_cast<int>(blockIdx.x) - b * blocks_per_b;
@@ -144,15 +148,15 @@ __global__ void __launch_bounds__(256) ss_step_kernel(const StepParams p) {
 template <typename TIO, int LPR>
 static cudaError_t launch_step_t(const StepParams& p, bool vec, cudaStream_t stream) {
     constexpr int RPT = 2;
-    constexpr int rows_block = (256 / LPR) * RPT;
+    constexpr int rows_block = (kStepThreads / LPR) * RPT;
     const int64_t blocks = (static_cast<int64_t>(p.Dm) + rows_block - 1) / rows_block * p.batch;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
     const dim3 grid(static_cast<unsigned>(blocks));
     if (vec)
-        ss_step_kernel<TIO, LPR, RPT, true><<<grid, 256, 0, stream>>>(p);
+        ss_step_kernel<TIO, LPR, RPT, true><<<grid, kStepThreads, 0, stream>>>(p);
     else
-        ss_step_kernel<TIO, LPR, RPT, false><<<grid, 256, 0, stream>>>(p);
+        ss_step_kernel<TIO, LPR, RPT, false><<<grid, kStepThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
