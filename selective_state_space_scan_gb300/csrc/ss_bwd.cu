@@ -1,7 +1,7 @@
 // Backward pass of the selective scan: the gradients of ss_fwd's outputs (y, last_state) with
-// respect to every input.  The pages implement no backward pass (the blog below lists the
-// backward kernel for training under "残り課題"); this is the derivative of the forward
-// definition ("mamba-metal: Apple Silicon で Mamba を動かす", section "Selective
+// respect to every input.  No backward pass is implemented on the pages ("mamba-metal: Apple
+// Silicon で Mamba を動かす" lists the backward kernel for training under "残り課題"); this is
+// the derivative of the forward definition (same blog, section "Selective
 // scan の本質": h_t = Ā_t h_{t-1} + B̄_t u_t, y_t = C_t h_t, with softplus on Δ, the D skip and
 // the z gate of the blog's walkthrough of the official CUDA kernel, section "1チャンク内の処理
 // フロー"), evaluated as the reverse (adjoint) recurrence of the same scan:
