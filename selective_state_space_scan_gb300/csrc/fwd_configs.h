@@ -12,11 +12,7 @@ namespace selscan {
 #ifndef SS_LANE_STAGES
 #define SS_LANE_STAGES 2
 #endif
-#ifndef SS_LANE_UNROLL
-#define SS_LANE_UNROLL 2
-#endif
 constexpr int kLaneT = SS_LANE_T;
-constexpr int kLaneUnroll = SS_LANE_UNROLL;   // step groups unrolled together
 constexpr int kLaneStages = SS_LANE_STAGES;
 #ifndef SS_LANE_MINB4
 #define SS_LANE_MINB4 3
