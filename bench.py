@@ -38,9 +38,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="mamba130m",
                     choices=["mamba130m", "long32k", "mamba2p8b_bf16", "decode1p4b", "tiny", "conv1d_130m",
-                             "bwd_130m", "lti_130m", "dtproj_130m"],
+                             "bwd_130m", "bwd_long32k", "lti_130m", "dtproj_130m"],
                     help="conv1d_130m times the causal conv1d + SiLU on the 130m layer's conv input "
-                         "(its own metric, outputs/s); bwd_130m the backward scan of the 130m layer; "
+                         "(its own metric, outputs/s); bwd_130m / bwd_long32k the backward scan of the 130m / "
+                         "long-sequence layer; "
                          "lti_130m the forward with B and C constant over the steps; dtproj_130m the forward "
                          "with the rank-48 time-step projection folded in")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -546,15 +547,16 @@ def bench_conv1d(args, local_rank):
 
 
 def bench_bwd(args, local_rank):
-    """The backward scan (ss_bwd) of the 130m-shaped layer (batch 8, L 2048, Dm 1536, N 16,
-    fp32): gradients of every input for a random dy; one launch (plus the zeroing of the sums)
-    per step."""
+    """The backward scan (ss_bwd): gradients of every input for a random dy, on the 130m-shaped
+    layer (bwd_130m: batch 8, L 2048, Dm 1536, N 16, fp32; one launch per step) or the
+    long-sequence one (bwd_long32k: batch 1, L 32768; the time split, four launches per step)."""
     import torch
     import selective_state_space_scan_gb300 as ss
     from selective_state_space_scan_gb300 import synth
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = synth.config("mamba130m")
+    split = args.workload == "bwd_long32k"      # 48 channel tiles: the automatic time split
+    w = synth.config("long32k" if split else "mamba130m")
     a = w.arrays
     t = {k: (None if v is None else torch.from_numpy(v).to(dev)) for k, v in a.items()}
     dy = torch.from_numpy(synth.rng_for(1, 12).standard_normal((w.batch, w.L, w.Dm), dtype=np.float32)).to(dev)
@@ -577,14 +579,15 @@ def bench_bwd(args, local_rank):
         "value": units * args.steps / (total_ms / 1e3), "unit": "state-updates/s", "n_gpus": 1,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "bwd_130m: batch=8 L=2048 Dm=1536 N=16 io=f32, all input gradients",
+        "config": {"workload": f"{args.workload}: batch={w.batch} L={w.L} Dm={w.Dm} N={w.N} io=f32, "
+                               "all input gradients" + (", time split" if split else ""),
                    "l2": "no flush: working set > 129 MB L2"},
-        "gpu_launches": args.steps, "clocks": clocks,
+        "gpu_launches": args.steps * (4 if split else 1), "clocks": clocks,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                     "traffic": measured_traffic("bwd_130m", "ss_bwd_kernel"), "kernel": "ss_bwd_kernel",
-                     "launch_ms": launch_ms, "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6,
-                     "alg_bytes_per_launch": alg}}))
+                     "traffic": measured_traffic(args.workload, "ss_bwd_kernel"), "kernel": "ss_bwd_kernel",
+                     "launch_ms": launch_ms, "launch_ms_is": "per step" if split else "per launch",
+                     "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6, "alg_bytes_per_launch": alg}}))
     return 0
 
 
@@ -594,13 +597,13 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     from selective_state_space_scan_gb300 import synth
-    if args.workload in ("conv1d_130m", "bwd_130m", "lti_130m", "dtproj_130m"):
+    if args.workload in ("conv1d_130m", "bwd_130m", "bwd_long32k", "lti_130m", "dtproj_130m"):
         if args.impl == "reference" or world > 1:
             if rank == 0:
                 print(json.dumps({"impl": args.impl,
                                   "unavailable": f"{args.workload} is measured on one GPU, ours only"}))
             return 0
-        fn = {"conv1d_130m": bench_conv1d, "bwd_130m": bench_bwd, "lti_130m": bench_lti,
+        fn = {"conv1d_130m": bench_conv1d, "bwd_130m": bench_bwd, "bwd_long32k": bench_bwd, "lti_130m": bench_lti,
               "dtproj_130m": bench_dtproj}[args.workload]
         return fn(args, local_rank)
     w = synth.config(args.workload)

@@ -42,6 +42,8 @@ constexpr int kBW = 32;    // channels per CTA
 
 // Test hook: -1 automatic, 0 plain-load staging, 1 TMA staging (refused when it cannot be used).
 std::atomic<int> g_force_bwd_tma{-1};
+// Test hook: -1 automatic time split, 0 never, n >= 2 always with up to n segments.
+std::atomic<int> g_force_bwd_nseg{-1};
 
 struct BwdParams {
     const void* u;
@@ -66,6 +68,16 @@ struct BwdParams {
     float* dh0;            // [batch, Dm, N] or nullptr
     float* ckpt;           // [tiles][nchunks][kBT / kBS][kBW][NS]: the state at every sub-chunk start
     unsigned int* err;     // device error word
+    // Time split (nseg > 1): CTA x takes segment x % nseg (chunks [seg·seg_chunks, ...)) of tile
+    // x / nseg.  The local launch folds each segment from zero (end state into h_slots[seg + 1],
+    // Σ Δ into dsum[seg]) and sweeps its adjoint from zero (the λ it hands to the segment on its
+    // left into m_slots[seg - 1]); the carry passes turn the slots into each segment's entering
+    // state (h_slots[seg]) and entering adjoint (m_slots[seg]); the main launch runs both passes
+    // per segment from them.
+    int nseg, seg_chunks;
+    float* h_slots;        // [nseg][batch·Dm·N]
+    float* m_slots;        // [nseg][batch·Dm·N]
+    float* dsum;           // [nseg][batch·Dm]
     int64_t u_b, u_l, d_b, d_l, z_b, z_l, B_b, B_l, C_b, C_l;
     int batch, L, Dm, N, nchunks, tiles_per_batch;
 };
@@ -211,7 +223,9 @@ __device__ __forceinline__ float channel_reduce_scatter(const float (&v)[8], int
 __device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
 __device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
 
-template <typename TIO, int NS, bool TMA>
+// LOCAL: the local launch of the time split (see BwdParams); otherwise both passes over this
+// CTA's chunks from its entering state and adjoint (the whole sequence when nseg == 1).
+template <typename TIO, int NS, bool TMA, bool LOCAL = false>
 __global__ void __launch_bounds__(BwdCfg<TIO, NS>::THREADS)
 ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
     using Cfg = BwdCfg<TIO, NS>;
@@ -228,7 +242,10 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int j = lane / CPW, c = lane % CPW;
     const int cw = warp * CPW + c;               // channel within the tile
-    const int tile = blockIdx.x;
+    const int tile = static_cast<int>(blockIdx.x) / p.nseg;
+    const int seg = static_cast<int>(blockIdx.x) - tile * p.nseg;
+    const int c0 = seg * p.seg_chunks;                  // this CTA's chunks [c0, c1)
+    const int c1 = min(p.nchunks, c0 + p.seg_chunks);
     const int b = tile / p.tiles_per_batch;
     const int d0 = (tile % p.tiles_per_batch) * kBW;
     const int d = d0 + cw;
@@ -268,7 +285,7 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
             phase ^= 1u;
         }
     };
-    if (TMA && tid == 0) issue(0, false);
+    if (TMA && tid == 0) issue(c0, false);
 
     float2 A2[2], An[2];                         // A·log2(e) and A = -exp(A_log), state pairs
 #pragma unroll
@@ -288,6 +305,7 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
         return ck + ((static_cast<int64_t>(ch) * NSUB + k) * kBW + cw) * NS + n0;
     };
     const int64_t row = static_cast<int64_t>(b) * p.Dm + d;
+    const int64_t count = static_cast<int64_t>(p.batch) * p.Dm * p.N;   // elements of one slot
 
     auto fold = [&](float2 (&h)[2], int r) {     // one step of the forward recurrence (chunk row r)
         const float del = sm[Cfg::OFF_DEL + r * kBW + cw];
@@ -298,52 +316,94 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
         h[1] = fma2(f2(ex2(e1.x), ex2(e1.y)), h[1], mul2(du, f2(Bv.z, Bv.w)));
     };
 
-    // ---- pass 1: forward, the state at every sub-chunk start
-    float2 h[2];
-    {
+    // this lane's four values of a [batch, Dm, N] state (zeros for none, or past Dm / N)
+    auto load_quad = [&](const float* src, float2 (&q2)[2]) {
         float v[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = (p.h0 && d_ok && n0 + q < p.N) ? p.h0[row * p.N + n0 + q] : 0.f;
-        h[0] = f2(v[0], v[1]);
-        h[1] = f2(v[2], v[3]);
-    }
-    for (int ch = 0; ch < p.nchunks; ++ch) {
+        for (int q = 0; q < 4; ++q) v[q] = (src && d_ok && n0 + q < p.N) ? src[row * p.N + n0 + q] : 0.f;
+        q2[0] = f2(v[0], v[1]);
+        q2[1] = f2(v[2], v[3]);
+    };
+    auto store_quad = [&](float* dst, const float2 (&q2)[2]) {
+        const float v[4] = {q2[0].x, q2[0].y, q2[1].x, q2[1].y};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (d_ok && n0 + q < p.N) dst[row * p.N + n0 + q] = v[q];
+    };
+
+    // ---- pass 1: forward, the state at every sub-chunk start (local launch: from zero, with Σ Δ)
+    float2 h[2];
+    float dsum = 0.f;
+    if (LOCAL)
+        h[0] = h[1] = f2(0.f);
+    else
+        load_quad(seg == 0 ? p.h0 : p.h_slots + seg * count, h);
+    for (int ch = c0; ch < c1; ++ch) {
         wait_staged();
         bwd_prepare<Cfg, TIO, TMA>(sm, raw, p, b, d0, ch, false, bias_c);
         __syncthreads();                         // staged tiles consumed; the chunk's arrays are ready
         if (TMA && tid == 0 && !*abort_flag) {
-            if (ch + 1 < p.nchunks) issue(ch + 1, false);
-            else issue(p.nchunks - 1, true);     // pass 2 starts from the last chunk
+            if (ch + 1 < c1) issue(ch + 1, false);
+            else issue(c1 - 1, true);            // pass 2 starts from the last chunk
         }
 #pragma unroll 1
         for (int k = 0; k < NSUB; ++k) {
-            __stcg(reinterpret_cast<float4*>(ckpt_at(ch, k)), make_float4(h[0].x, h[0].y, h[1].x, h[1].y));
+            if constexpr (!LOCAL)
+                __stcg(reinterpret_cast<float4*>(ckpt_at(ch, k)), make_float4(h[0].x, h[0].y, h[1].x, h[1].y));
 #pragma unroll 4
-            for (int r = k * kBS; r < (k + 1) * kBS; ++r) fold(h, r);
+            for (int r = k * kBS; r < (k + 1) * kBS; ++r) {
+                if constexpr (LOCAL) dsum += sm[Cfg::OFF_DEL + r * kBW + cw];
+                fold(h, r);
+            }
         }
         __syncthreads();                         // the chunk's arrays are no longer read
+    }
+    if constexpr (LOCAL) {
+        if (seg + 1 < p.nseg) store_quad(p.h_slots + (seg + 1) * count, h);
+        if (j == 0 && d_ok) p.dsum[seg * static_cast<int64_t>(p.batch) * p.Dm + row] = dsum;
     }
 
     // ---- pass 2: reverse
     float2 mu[2];                                // a_{t+1} λ_{t+1}: what step t receives
-    {
-        float v[4];
+    if (LOCAL)
+        mu[0] = mu[1] = f2(0.f);
+    else
+        load_quad(seg + 1 == p.nseg ? p.dlast : p.m_slots + seg * count, mu);
+    if constexpr (LOCAL) {
+        // the adjoint alone, λ = C·dŷ + μ, μ ← a·λ, from zero at the segment's end
+        for (int ch = c1 - 1; ch >= c0; --ch) {
+            wait_staged();
+            bwd_prepare<Cfg, TIO, TMA>(sm, raw, p, b, d0, ch, true, bias_c);
+            __syncthreads();
+            if (TMA && tid == 0 && ch > c0 && !*abort_flag) issue(ch - 1, true);
+#pragma unroll 4
+            for (int r = kBT - 1; r >= 0; --r) {
+                const float del = sm[Cfg::OFF_DEL + r * kBW + cw];
+                const float dyh = sm[Cfg::OFF_DYH + r * kBW + cw];
+                const float4 Cv = *reinterpret_cast<const float4*>(&sm[Cfg::OFF_C + r * NS + n0]);
+                const float2 C2[2] = {f2(Cv.x, Cv.y), f2(Cv.z, Cv.w)};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = (p.dlast && d_ok && n0 + q < p.N) ? p.dlast[row * p.N + n0 + q] : 0.f;
-        mu[0] = f2(v[0], v[1]);
-        mu[1] = f2(v[2], v[3]);
+                for (int q = 0; q < 2; ++q) {
+                    const float2 e = mul2(f2(del), A2[q]);
+                    mu[q] = mul2(f2(ex2(e.x), ex2(e.y)), fma2(C2[q], f2(dyh), mu[q]));
+                }
+            }
+            __syncthreads();
+        }
+        if (seg > 0) store_quad(p.m_slots + (seg - 1) * count, mu);
+        return;
     }
     float2 dA[2] = {f2(0.f), f2(0.f)};
     float dDacc = 0.f, dbacc = 0.f;
     TIO* g_du = static_cast<TIO*>(p.du);
     TIO* g_dd = static_cast<TIO*>(p.ddelta);
     TIO* g_dz = static_cast<TIO*>(p.dz);
-    for (int ch = p.nchunks - 1; ch >= 0; --ch) {
+    for (int ch = c1 - 1; ch >= c0; --ch) {
         wait_staged();
         bwd_prepare<Cfg, TIO, TMA>(sm, raw, p, b, d0, ch, true, bias_c);
         if (TMA && tid == 0) tma_store_wait_read();   // the previous chunk's gradient tiles are read out
         __syncthreads();
-        if (TMA && tid == 0 && ch > 0 && !*abort_flag) issue(ch - 1, true);
+        if (TMA && tid == 0 && ch > c0 && !*abort_flag) issue(ch - 1, true);
 #pragma unroll 1
         for (int k = NSUB - 1; k >= 0; --k) {
             float2 H[kBS][2], hb0[2];
@@ -457,7 +517,7 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
         for (int q = 0; q < 4; ++q) {
             const int n = n0 + q;
             if (n < p.N) {
-                if (p.dh0) p.dh0[row * p.N + n] = m4[q];
+                if (p.dh0 && seg == 0) p.dh0[row * p.N + n] = m4[q];
                 atomicAdd(p.dA_log + static_cast<int64_t>(d) * p.N + n, a4[q]);
             }
         }
@@ -468,35 +528,105 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
     }
 }
 
-template <typename TIO, int NS, bool TMA>
+template <typename TIO, int NS, bool TMA, bool LOCAL>
 cudaError_t launch_bwd_t(const BwdParams& p, const BwdMaps& m, cudaStream_t stream) {
     using Cfg = BwdCfg<TIO, NS>;
-    cudaError_t e = cudaFuncSetAttribute(ss_bwd_kernel<TIO, NS, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(ss_bwd_kernel<TIO, NS, TMA, LOCAL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
     if (e != cudaSuccess) return e;
-    const unsigned grid = static_cast<unsigned>(p.batch) * static_cast<unsigned>(p.tiles_per_batch);
-    ss_bwd_kernel<TIO, NS, TMA><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(p, m);
+    const unsigned grid = static_cast<unsigned>(p.batch) * static_cast<unsigned>(p.tiles_per_batch) *
+                          static_cast<unsigned>(p.nseg);
+    ss_bwd_kernel<TIO, NS, TMA, LOCAL><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(p, m);
     return cudaGetLastError();
 }
 
-template <typename TIO>
+template <typename TIO, bool LOCAL>
 cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, int ns, bool tma, cudaStream_t stream) {
     if (tma) {
-        if (ns == 4) return launch_bwd_t<TIO, 4, true>(p, m, stream);
-        if (ns == 8) return launch_bwd_t<TIO, 8, true>(p, m, stream);
-        return launch_bwd_t<TIO, 16, true>(p, m, stream);
+        if (ns == 4) return launch_bwd_t<TIO, 4, true, LOCAL>(p, m, stream);
+        if (ns == 8) return launch_bwd_t<TIO, 8, true, LOCAL>(p, m, stream);
+        return launch_bwd_t<TIO, 16, true, LOCAL>(p, m, stream);
     }
-    if (ns == 4) return launch_bwd_t<TIO, 4, false>(p, m, stream);
-    if (ns == 8) return launch_bwd_t<TIO, 8, false>(p, m, stream);
-    return launch_bwd_t<TIO, 16, false>(p, m, stream);
+    if (ns == 4) return launch_bwd_t<TIO, 4, false, LOCAL>(p, m, stream);
+    if (ns == 8) return launch_bwd_t<TIO, 8, false, LOCAL>(p, m, stream);
+    return launch_bwd_t<TIO, 16, false, LOCAL>(p, m, stream);
+}
+
+// Adjoint carry of the time split: slot s ends as the adjoint entering segment s from the right,
+//   M_{nseg-1} = dlast,   M_s = exp(A ΣΔ_{s+1}) M_{s+1} + local_{s+1},
+// where the local launch left local_{s+1} (the adjoint segment s + 1 hands on when swept from
+// zero) in slot s; the mirror image of the forward carry (ss_fwd_carry.cu), right to left.
+__global__ void __launch_bounds__(256)
+ss_bwd_carry_kernel(const float* __restrict__ A_log, const float* __restrict__ dlast, float* __restrict__ slots,
+                    const float* __restrict__ dsum, int64_t rows, int Dm, int N, int nseg) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t count = rows * N;
+    if (i >= count) return;
+    const int64_t row = i / N;
+    const int n = static_cast<int>(i - row * N);
+    const int d = static_cast<int>(row % Dm);
+    const float a2 = -expf(A_log[static_cast<int64_t>(d) * N + n]) * kLog2e;
+    float m = dlast ? dlast[i] : 0.f;
+    slots[static_cast<int64_t>(nseg - 1) * count + i] = m;
+    for (int s = nseg - 2; s >= 0; --s) {
+        const float decay = ex2(a2 * dsum[static_cast<int64_t>(s + 1) * rows + row]);
+        float* slot = slots + static_cast<int64_t>(s) * count + i;
+        m = fmaf(decay, m, *slot);
+        *slot = m;
+    }
 }
 
 int bwd_ns(int64_t N) { return N <= 4 ? 4 : N <= 8 ? 8 : 16; }
 
-size_t bwd_ws_bytes(int64_t batch, int64_t L, int64_t Dm, int64_t N) {
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+// CTAs of the backward kernel (fp32, 16 states, TMA: the representative instantiation) that the
+// current device holds at once; 0 if it cannot be queried.
+int64_t bwd_resident_ctas() {
+    using Cfg = BwdCfg<float, 16>;
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(ss_bwd_kernel<float, 16, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::SMEM) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ss_bwd_kernel<float, 16, true, false>, Cfg::THREADS,
+                                                      Cfg::SMEM) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return static_cast<int64_t>(sms) * per_sm;
+}
+
+// Schedule and workspace: one CTA per tile, or (when the tiles alone cannot fill the GPU, or
+// when forced) the time split into nseg segments of seg_chunks chunks, as many as fill it once
+// (at most one per chunk and 64).
+struct BwdPlan {
+    int nseg = 1, seg_chunks = 0;
+    size_t ckpt = 0, slots = 0, dsum = 0, total = 0;
+};
+
+BwdPlan bwd_plan(int64_t batch, int64_t L, int64_t Dm, int64_t N) {
+    BwdPlan pl;
     const int64_t tiles = batch * ((Dm + kBW - 1) / kBW);
     const int64_t nch = (L + kBT - 1) / kBT;
-    return static_cast<size_t>(tiles) * nch * (kBT / kBS) * kBW * bwd_ns(N) * 4;
+    const int forced = g_force_bwd_nseg.load();
+    int64_t want = 1;
+    if (forced >= 2) {
+        want = forced;
+    } else if (forced < 0) {
+        const int64_t resident = bwd_resident_ctas();
+        if (tiles > 0 && resident >= 2 * tiles) want = resident / tiles;
+    }
+    want = std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(want, nch), 64));
+    pl.seg_chunks = static_cast<int>((nch + want - 1) / want);
+    pl.nseg = static_cast<int>((nch + pl.seg_chunks - 1) / pl.seg_chunks);
+    pl.ckpt = up256(static_cast<size_t>(tiles) * nch * (kBT / kBS) * kBW * bwd_ns(N) * 4);
+    if (pl.nseg > 1) {
+        pl.slots = up256(static_cast<size_t>(pl.nseg) * batch * Dm * N * 4);
+        pl.dsum = up256(static_cast<size_t>(pl.nseg) * batch * Dm * 4);
+    }
+    pl.total = pl.ckpt + 2 * pl.slots + pl.dsum;
+    return pl;
 }
 
 }  // namespace
@@ -507,7 +637,8 @@ using namespace selscan::host;
 
 extern "C" size_t ss_bwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N) {
     if (batch <= 0 || L <= 0 || Dm <= 0 || N < 1 || N > 16) return 0;
-    return bwd_ws_bytes(batch, L, Dm, N);
+    if (L > INT32_MAX || Dm > INT32_MAX || batch > INT32_MAX) return 0;
+    return bwd_plan(batch, L, Dm, N).total;
 }
 
 extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
@@ -595,8 +726,8 @@ extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* d
         for (int k = i + 1; k < nouts; ++k)
             if (meet(outs[i], outs[k])) return SS_ERR_INVALID_ARG;
     }
-    const size_t need = bwd_ws_bytes(batch, L, Dm, N);
-    if (!workspace || workspace_bytes < need) return SS_ERR_INVALID_ARG;
+    const BwdPlan plan = bwd_plan(batch, L, Dm, N);
+    if (!workspace || workspace_bytes < plan.total) return SS_ERR_INVALID_ARG;
     if (!is_aligned(workspace, 256)) return SS_ERR_MISALIGNED;
     if (!dev_ptr(workspace, dev)) return SS_ERR_INVALID_ARG;
     if (clear(dB, batch * L * N) != cudaSuccess || clear(dC, batch * L * N) != cudaSuccess ||
@@ -616,7 +747,15 @@ extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* d
     p.N = static_cast<int>(N);
     p.nchunks = static_cast<int>((L + kBT - 1) / kBT);
     p.tiles_per_batch = static_cast<int>((Dm + kBW - 1) / kBW);
-    if (static_cast<int64_t>(p.batch) * p.tiles_per_batch > INT32_MAX) return SS_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(p.batch) * p.tiles_per_batch * plan.nseg > INT32_MAX) return SS_ERR_UNSUPPORTED;
+    p.nseg = plan.nseg;
+    p.seg_chunks = plan.nseg > 1 ? plan.seg_chunks : p.nchunks;
+    if (plan.nseg > 1) {
+        char* ws = static_cast<char*>(workspace);
+        p.h_slots = reinterpret_cast<float*>(ws + plan.ckpt);
+        p.m_slots = reinterpret_cast<float*>(ws + plan.ckpt + plan.slots);
+        p.dsum = reinterpret_cast<float*>(ws + plan.ckpt + 2 * plan.slots);
+    }
     p.err = device_error_word();
     // staged by TMA when every tensor allows it, else by plain loads
     const int ns = bwd_ns(N);
@@ -636,10 +775,30 @@ extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* d
               (!z || make_tile_map(&maps.dz, dz, bf16, Dm, L, batch, Dm, L * Dm, kBW, kBT));
     }
     if (ft == 1 && !tma) return SS_ERR_UNSUPPORTED;
-    const cudaError_t e = bf16 ? launch_bwd<__nv_bfloat16>(p, maps, ns, tma, stream)
-                               : launch_bwd<float>(p, maps, ns, tma, stream);
+    cudaError_t e = cudaSuccess;
+    if (plan.nseg > 1) {
+        // local sweeps of every segment, then the two carries
+        e = bf16 ? launch_bwd<__nv_bfloat16, true>(p, maps, ns, tma, stream)
+                 : launch_bwd<float, true>(p, maps, ns, tma, stream);
+        if (e != cudaSuccess) return SS_ERR_CUDA;
+        FwdParams fp;
+        std::memset(&fp, 0, sizeof(fp));
+        fp.A_log = A_log; fp.h0 = h0; fp.seg_slots = p.h_slots; fp.seg_dsum = p.dsum;
+        fp.batch = p.batch; fp.Dm = p.Dm; fp.N = p.N; fp.nseg = p.nseg;
+        if (launch_fwd_carry(fp, stream) != cudaSuccess) return SS_ERR_CUDA;
+        const int64_t count = batch * Dm * N;
+        ss_bwd_carry_kernel<<<static_cast<unsigned>((count + 255) / 256), 256, 0, stream>>>(
+            A_log, dlast, p.m_slots, p.dsum, batch * Dm, p.Dm, p.N, p.nseg);
+        if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+    }
+    e = bf16 ? launch_bwd<__nv_bfloat16, false>(p, maps, ns, tma, stream)
+             : launch_bwd<float, false>(p, maps, ns, tma, stream);
     return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
+
+// Internal test hook (not in the public header): -1 automatic time split, 0 (or 1) never,
+// n >= 2 always with up to n segments.  Returns the previous setting.
+extern "C" int ss__force_bwd_nseg(int n) { return g_force_bwd_nseg.exchange(n < 0 ? -1 : n <= 1 ? 0 : n); }
 
 // Internal test hook (not in the public header): -1 automatic, 0 plain-load staging, 1 TMA
 // staging (SS_ERR_UNSUPPORTED where the tensors rule it out).  Returns the previous setting.

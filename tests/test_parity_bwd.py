@@ -98,10 +98,29 @@ class staging:
 STAGINGS = pytest.mark.parametrize("stage", [-1, 0], ids=["auto", "plain"])
 
 
+class splitting:
+    """Pin the backward's time split: -1 automatic, 0 never, n >= 2 up to n segments."""
+
+    def __init__(self, n):
+        self.n = n
+
+    def __enter__(self):
+        lib = ss.lib()
+        lib.ss__force_bwd_nseg.argtypes = [ctypes.c_int]
+        self.prev = lib.ss__force_bwd_nseg(self.n)
+
+    def __exit__(self, *a):
+        ss.lib().ss__force_bwd_nseg(self.prev)
+
+
+SPLITS = pytest.mark.parametrize("nseg", [0, 3, -1], ids=["one-pass", "split3", "auto"])
+
+
+@SPLITS
 @STAGINGS
 @pytest.mark.parametrize("L", [1, 5, 31, 32, 33, 63, 64, 65, 200])
-def test_bwd_lengths(L, stage):
-    with staging(stage):
+def test_bwd_lengths(L, stage, nseg):
+    with staging(stage), splitting(nseg):
         check(*problem(2, L, 40, 16, seed=L), what=f"L={L}")
 
 
@@ -156,11 +175,28 @@ def test_bwd_strided_inputs_fall_back_to_plain_staging():
         assert e <= (GRAD_REL_L2 if k in ELEMENTWISE else SUM_REL_L2), (k, e)
 
 
+@SPLITS
 @pytest.mark.parametrize("opts", ["no_gate", "no_h0", "no_dlast", "plain"])
-def test_bwd_optional_inputs(opts):
+def test_bwd_optional_inputs(opts, nseg):
     kw = dict(gate=opts not in ("no_gate", "plain"), with_h0=opts not in ("no_h0", "plain"),
               with_dlast=opts not in ("no_dlast", "plain"))
-    check(*problem(2, 150, 48, 16, seed=50, **kw), what=opts)
+    with splitting(nseg):
+        check(*problem(2, 150, 48, 16, seed=50, **kw), what=opts)
+
+
+@pytest.mark.parametrize("nseg", [2, 5, 8, 64])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bwd_time_split_segment_counts(nseg, io):
+    """Forced segment counts (up to one per 32-step chunk) on a few-tile problem with h0 and
+    dlast, against the oracle and against the one-pass schedule."""
+    args = problem(1, 1000, 64, 16, io=io, seed=200 + nseg)
+    with splitting(nseg):
+        got, _ = check(*args, what=f"split {nseg} {io}")
+    with splitting(0):
+        one = run(*args)
+    tol = 1e-5 if io == "f32" else 5e-3
+    for k in ("du", "ddelta_raw", "dz", "dh0"):
+        assert rel_l2(got[k], one[k]) <= tol, k
 
 
 @STAGINGS
@@ -170,8 +206,29 @@ def test_bwd_bf16(N, stage):
         check(*problem(2, 300, 64, N, io="bf16", seed=60 + N), what="bf16")
 
 
-def test_bwd_long_sequence():
-    check(*problem(2, 2048, 256, 16, seed=61), what="L=2048")
+@pytest.mark.parametrize("nseg", [0, -1], ids=["one-pass", "auto"])
+def test_bwd_long_sequence(nseg):
+    with splitting(nseg):
+        check(*problem(2, 2048, 256, 16, seed=61), what="L=2048")
+
+
+def test_bwd_long32k_shape_sampled():
+    """The long-sequence shape (batch 1, L 32768, Dm 1536, N 16) on the automatic time split:
+    dh0 and dA_log against the oracle on a channel slice (the oracle runs the sliced problem,
+    which the slice's gradients depend on alone), the elementwise gradients on that slice too."""
+    w = synth.config("long32k")
+    a = w.arrays
+    dy = synth.rng_for(63, 12).standard_normal((1, w.L, w.Dm), dtype=np.float32)
+    got = run(w, a, dy, None, None)
+    sl = slice(0, 64)
+    sub = {k: (None if v is None else (v[..., sl] if v.ndim == 3 and v.shape[-1] == w.Dm else
+                                       v[sl] if v.shape[0] == w.Dm else v)) for k, v in a.items()}
+    ref = oracle.ss_bwd(sub["u"], sub["delta_raw"], sub["delta_bias"], sub["A_log"], sub["B"], sub["C"], sub["D"],
+                        sub["z"], dy[..., sl])
+    for k in ("du", "ddelta_raw", "dz"):
+        assert rel_l2(got[k][..., sl], ref[k]) <= GRAD_REL_L2, k
+    for k in ("dA_log", "dD", "ddelta_bias"):
+        assert rel_l2(got[k][sl], ref[k]) <= SUM_REL_L2, k
 
 
 def test_bwd_full_size_130m():
