@@ -375,6 +375,20 @@ def oracle_time(w, min_seconds=10.0, max_passes=50):
     return units / elapsed, passes, elapsed, oracle.num_threads()
 
 
+def oracle_sample_baseline(fn, units_per_pass, unit, sample, min_seconds=10.0, max_passes=50):
+    """The oracle timed on a bounded sample of a workload: fn() is one pass over the sample,
+    repeated until min_seconds; returns the cpu_baseline object."""
+    import oracle
+    passes, elapsed = 0, 0.0
+    while passes < 1 or (elapsed < min_seconds and passes < max_passes):
+        t0 = time.perf_counter()
+        fn()
+        elapsed += time.perf_counter() - t0
+        passes += 1
+    return {"value": units_per_pass * passes / elapsed, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{passes} pass(es) of {sample}, {elapsed:.1f} s of fp64 oracle time"}
+
+
 def workload_config(w, extra=None, variant=None):
     c = {"workload": f"{w.name}: batch={w.batch} L={w.L} Dm={w.Dm} N={w.N} io={w.io}",
          "batch": w.batch, "L": w.L, "Dm": w.Dm, "N": w.N, "io": w.io, "seed": w.seed,
@@ -440,7 +454,7 @@ def bench_lti(args, local_rank):
     sfu_peak = GB300_SMS * SFU_EX2_PER_CLK_PER_SM * GB300_MAX_SM_MHZ * 1e6
     achieved = alg / (launch_ms / 1e3) / 1e9
     kernel = "ss_fwd_lane_kernel(lpc=4,lti)"
-    print(json.dumps({
+    out = {
         "metric": "selective-scan state-updates/s (B·L·D·N), time-invariant B/C, 1×GB300",
         "value": units * args.steps / (total_ms / 1e3), "unit": "state-updates/s", "n_gpus": 1,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
@@ -452,7 +466,17 @@ def bench_lti(args, local_rank):
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": measured_traffic("lti_130m", kernel), "kernel": kernel, "launch_ms": launch_ms,
                      "alg_bytes_per_launch": alg, "t_hbm_us": alg / (hbm_peak * 1e9) * 1e6,
-                     "t_sfu_us": units / sfu_peak * 1e6}}))
+                     "t_sfu_us": units / sfu_peak * 1e6}}
+    if not args.no_cpu_baseline:
+        import oracle
+        rows = np.arange(w.Dm)                       # batch row 0, every channel
+        Bl = np.broadcast_to(a["B"][:, :1], a["B"].shape).copy()
+        Cl = np.broadcast_to(a["C"][:, :1], a["C"].shape).copy()
+        out["cpu_baseline"] = oracle_sample_baseline(
+            lambda: oracle.ss_fwd(a["u"], a["delta_raw"], a["delta_bias"], a["A_log"], Bl, Cl, a["D"], a["z"],
+                                  rows=rows),
+            w.Dm * w.L * w.N, "state-updates/s", "batch row 0 of the lti_130m workload (all channels)")
+    print(json.dumps(out))
     return 0
 
 
@@ -490,7 +514,7 @@ def bench_dtproj(args, local_rank):
     fma_peak = GB300_SMS * 128 * GB300_MAX_SM_MHZ * 1e6          # fp32 FMA lanes per second
     achieved = alg / (launch_ms / 1e3) / 1e9
     kernel = "ss_fwd_lane_kernel(lpc=4,dtproj)"
-    print(json.dumps({
+    out = {
         "metric": "selective-scan state-updates/s (B·L·D·N), dt_proj folded in, 1×GB300",
         "value": units * args.steps / (total_ms / 1e3), "unit": "state-updates/s", "n_gpus": 1,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
@@ -503,7 +527,16 @@ def bench_dtproj(args, local_rank):
                      "traffic": measured_traffic("dtproj_130m", kernel), "kernel": kernel, "launch_ms": launch_ms,
                      "alg_bytes_per_launch": alg, "t_hbm_us": alg / (hbm_peak * 1e9) * 1e6,
                      "t_sfu_us": units / sfu_peak * 1e6,
-                     "t_fma_us": w.batch * w.L * w.Dm * R / fma_peak * 1e6}}))
+                     "t_fma_us": w.batch * w.L * w.Dm * R / fma_peak * 1e6}}
+    if not args.no_cpu_baseline:
+        import oracle
+        dl, Wn = dt_low[:1].cpu().numpy(), W_dt.cpu().numpy()
+        one = {k: (None if v is None else (v[:1] if v.ndim == 3 else v)) for k, v in a.items()}
+        out["cpu_baseline"] = oracle_sample_baseline(
+            lambda: oracle.ss_fwd_dtproj(one["u"], dl, Wn, one["delta_bias"], one["A_log"], one["B"], one["C"],
+                                         one["D"], one["z"]),
+            w.Dm * w.L * w.N, "state-updates/s", "batch row 0 of the dtproj_130m workload (all channels)")
+    print(json.dumps(out))
     return 0
 
 
@@ -530,7 +563,7 @@ def bench_conv1d(args, local_rank):
     alg = 2 * units * 4 + Dm * 5 * 4 + 2 * batch * Dm * 3 * 4
     hbm_peak, peak_kind = peaks()
     achieved = alg / (launch_ms / 1e3) / 1e9
-    print(json.dumps({
+    out = {
         "metric": "causal conv1d + SiLU outputs/s (B·L·D), 1×GB300", "value": units * args.steps / (total_ms / 1e3),
         "unit": "outputs/s", "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -542,7 +575,14 @@ def bench_conv1d(args, local_rank):
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": measured_traffic("conv1d_130m", "ss_conv1d_kernel"), "kernel": "ss_conv1d_kernel",
                      "launch_ms": launch_ms,
-                     "alg_bytes_per_launch": alg}}))
+                     "alg_bytes_per_launch": alg}}
+    if not args.no_cpu_baseline:
+        import oracle
+        xn, wn, bn = x.cpu().numpy(), wgt.cpu().numpy(), bias.cpu().numpy()
+        out["cpu_baseline"] = oracle_sample_baseline(
+            lambda: oracle.conv1d(xn, wn, bn, window=np.zeros((batch, Dm, 3)), act=True),
+            units, "outputs/s", "the whole conv1d_130m workload")
+    print(json.dumps(out))
     return 0
 
 
@@ -574,7 +614,7 @@ def bench_bwd(args, local_rank):
     # the ex2 rate; below the HBM floor, so the bound is HBM
     sfu_peak = GB300_SMS * SFU_EX2_PER_CLK_PER_SM * GB300_MAX_SM_MHZ * 1e6
     t_hbm, t_sfu = alg / (hbm_peak * 1e9), 2 * units / sfu_peak
-    print(json.dumps({
+    out = {
         "metric": "selective-scan backward state-updates/s (B·L·D·N), 1×GB300",
         "value": units * args.steps / (total_ms / 1e3), "unit": "state-updates/s", "n_gpus": 1,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
@@ -587,7 +627,22 @@ def bench_bwd(args, local_rank):
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": measured_traffic(args.workload, "ss_bwd_kernel"), "kernel": "ss_bwd_kernel",
                      "launch_ms": launch_ms, "launch_ms_is": "per step" if split else "per launch",
-                     "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6, "alg_bytes_per_launch": alg}}))
+                     "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6, "alg_bytes_per_launch": alg}}
+    if not args.no_cpu_baseline:
+        import oracle
+        one = {k: (None if v is None else (v[:1] if v.ndim == 3 else v)) for k, v in a.items()}
+        dyn = dy[:1].cpu().numpy()
+        if split:                                    # a 64-channel slice of the long row
+            one = {k: (None if v is None else (v[..., :64] if v.ndim == 3 and v.shape[-1] == w.Dm else
+                                               v[:64] if v.shape[0] == w.Dm else v)) for k, v in one.items()}
+            dyn = dyn[..., :64]
+        nch = dyn.shape[-1]
+        out["cpu_baseline"] = oracle_sample_baseline(
+            lambda: oracle.ss_bwd(one["u"], one["delta_raw"], one["delta_bias"], one["A_log"], one["B"], one["C"],
+                                  one["D"], one["z"], dyn),
+            nch * w.L * w.N, "state-updates/s",
+            f"batch row 0 of the {args.workload} workload ({nch} channels)", min_seconds=5.0)
+    print(json.dumps(out))
     return 0
 
 
