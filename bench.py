@@ -153,6 +153,19 @@ def updates_per_step(w) -> int:
     return w.state_updates
 
 
+def warm_up(step, args, torch, min_seconds=0.5):
+    """At least W (>= 3) untimed steps, continued until the GPU has run them for min_seconds, so
+    that the clock sampler (every 100 ms) sees the GPU under this load right up to the timed
+    region, which follows without a gap."""
+    n, t0 = 0, time.perf_counter()
+    while n < max(args.warmup, 3) or time.perf_counter() - t0 < min_seconds:
+        step()
+        n += 1
+        if n % 16 == 0:
+            torch.cuda.synchronize()
+    return n
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -163,6 +176,7 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.path = None
+        self.warmup_steps = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -202,7 +216,8 @@ class ClockSampler:
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         loaded = [v for v in sm if mx and v >= 0.5 * max(mx)] or sm
         return {"sm_mhz": statistics.median(loaded) if loaded else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "warmup_steps_run": self.warmup_steps}
 
 
 # ---------------------------------------------------------------------------- our arm
@@ -290,8 +305,7 @@ def run_ours(args, w, rank, world, local_rank):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clk:
         # warm-up right before the timed region (no idle gap for the clocks to drop in)
-        for _ in range(max(args.warmup, 3)):
-            step()
+        clk.warmup_steps = warm_up(step, args, torch)
         barrier()
         start.record(stream)
         for i in range(args.steps):
@@ -411,8 +425,7 @@ def time_step_fn(step, args, local_rank):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clk:
-        for _ in range(max(args.warmup, 3)):
-            step()
+        clk.warmup_steps = warm_up(step, args, torch)
         torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
