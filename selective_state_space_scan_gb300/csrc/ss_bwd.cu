@@ -118,13 +118,19 @@ struct BwdCfg {
 
 __device__ __forceinline__ float sigmoid_f(float x) { return rcp_approx(1.f + ex2(-x * kLog2e)); }
 
-// Build the chunk's fp32 arrays: Δ = softplus(δ + bias), u and B (and, full = pass 2, σ(δ + bias),
-// dŷ = dy·silu(z), dy·silu'(z), C).  Inputs come from the staged tiles (TMA) or straight from
-// global memory.  Steps past L and channels past Dm become zeros, which make those steps the
-// identity of both recurrences.
-template <class Cfg, typename TIO, bool TMA>
+// What a chunk's staging holds: the forward fold's inputs (u, δ, B), everything the reverse pass
+// uses (u, δ, z, dy, B, C), or the adjoint sweep's alone (δ, z, dy, C: the time split's local launch).
+enum StageKind { kStFwd = 0, kStFull = 1, kStLam = 2 };
+
+// Build the chunk's fp32 arrays: Δ = softplus(δ + bias) always; u and B unless KIND is kStLam;
+// σ(δ + bias) and dy·silu'(z) for kStFull; dŷ = dy·silu(z) and C unless KIND is kStFwd.  Inputs come
+// from the staged tiles (TMA) or straight from global memory.  Steps past L and channels past Dm
+// become zeros, which make those steps the identity of both recurrences.
+template <class Cfg, typename TIO, bool TMA, int KIND>
 __device__ __forceinline__ void bwd_prepare(float* sm, const uint8_t* raw, const BwdParams& p, int b, int d0,
-                                            int chunk, bool full, float bias_c) {
+                                            int chunk, float bias_c) {
+    constexpr bool full = KIND != kStFwd;        // the reverse pass's inputs (dŷ, C)
+    constexpr bool with_u = KIND != kStLam;      // u and B
     const int t0 = chunk * kBT;
     const int c = threadIdx.x % kBW;             // fixed per thread (THREADS is a multiple of kBW)
     const int d = d0 + c;
@@ -138,14 +144,14 @@ __device__ __forceinline__ void bwd_prepare(float* sm, const uint8_t* raw, const
         const bool in = t < p.L && d < p.Dm;
         float uu = 0.f, rr = 0.f, zv = 0.f, dyv = 0.f;
         if constexpr (TMA) {
-            uu = to_f32<TIO>(reinterpret_cast<const TIO*>(raw + Cfg::R_U)[i]);
+            if (with_u) uu = to_f32<TIO>(reinterpret_cast<const TIO*>(raw + Cfg::R_U)[i]);
             rr = to_f32<TIO>(reinterpret_cast<const TIO*>(raw + Cfg::R_D)[i]);
             if (full) {
                 if (gz) zv = to_f32<TIO>(reinterpret_cast<const TIO*>(raw + Cfg::R_Z)[i]);
                 dyv = to_f32<TIO>(reinterpret_cast<const TIO*>(raw + Cfg::R_Y)[i]);
             }
         } else if (in) {
-            uu = to_f32<TIO>(gu[b * p.u_b + t * p.u_l + d]);
+            if (with_u) uu = to_f32<TIO>(gu[b * p.u_b + t * p.u_l + d]);
             rr = to_f32<TIO>(gd[b * p.d_b + t * p.d_l + d]);
             if (full) {
                 if (gz) zv = to_f32<TIO>(gz[b * p.z_b + t * p.z_l + d]);
@@ -153,7 +159,7 @@ __device__ __forceinline__ void bwd_prepare(float* sm, const uint8_t* raw, const
             }
         }
         rr += bias_c;
-        sm[Cfg::OFF_U + i] = in ? uu : 0.f;
+        if (with_u) sm[Cfg::OFF_U + i] = in ? uu : 0.f;
         sm[Cfg::OFF_DEL + i] = in ? softplus(rr) : 0.f;
         if (full) {
             float g = 1.f, dg = 0.f;
@@ -162,9 +168,11 @@ __device__ __forceinline__ void bwd_prepare(float* sm, const uint8_t* raw, const
                 g = zv * s;
                 dg = s * fmaf(zv, 1.f - s, 1.f);
             }
-            sm[Cfg::OFF_SIG + i] = in ? sigmoid_f(rr) : 0.f;
             sm[Cfg::OFF_DYH + i] = in ? dyv * g : 0.f;
-            sm[Cfg::OFF_DYG + i] = in ? dyv * dg : 0.f;
+            if (KIND == kStFull) {
+                sm[Cfg::OFF_SIG + i] = in ? sigmoid_f(rr) : 0.f;
+                sm[Cfg::OFF_DYG + i] = in ? dyv * dg : 0.f;
+            }
         }
     }
     const TIO* gB = static_cast<const TIO*>(p.Bm);
@@ -176,13 +184,13 @@ __device__ __forceinline__ void bwd_prepare(float* sm, const uint8_t* raw, const
         const bool in = t < p.L && n < p.N;
         float bv = 0.f, cv = 0.f;
         if constexpr (TMA) {
-            bv = to_f32<TIO>(reinterpret_cast<const TIO*>(raw + Cfg::R_B)[i]);
+            if (with_u) bv = to_f32<TIO>(reinterpret_cast<const TIO*>(raw + Cfg::R_B)[i]);
             if (full) cv = to_f32<TIO>(reinterpret_cast<const TIO*>(raw + Cfg::R_C)[i]);
         } else if (in) {
-            bv = to_f32<TIO>(gB[b * p.B_b + t * p.B_l + n]);
+            if (with_u) bv = to_f32<TIO>(gB[b * p.B_b + t * p.B_l + n]);
             if (full) cv = to_f32<TIO>(gC[b * p.C_b + t * p.C_l + n]);
         }
-        sm[Cfg::OFF_B + i] = in ? bv : 0.f;
+        if (with_u) sm[Cfg::OFF_B + i] = in ? bv : 0.f;
         if (full) sm[Cfg::OFF_C + i] = in ? cv : 0.f;
     }
 }
@@ -264,14 +272,18 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
     for (int i = tid; i < 2 * Cfg::XN; i += Cfg::THREADS) sm[Cfg::OFF_BC + i] = 0.f;
     __syncthreads();
     // one TMA batch in flight at a time: the next chunk's tiles land while this chunk is processed
-    auto issue = [&](int chunk, bool full) {
+    auto issue = [&](int chunk, int kind) {     // a StageKind
         const int t0 = chunk * kBT;
+        const bool full = kind != kStFwd, with_u = kind != kStLam;
         const bool hz = full && p.z != nullptr;
-        const uint32_t bytes = (full ? (hz ? 4u : 3u) : 2u) * Cfg::RAW_X + (full ? 2u : 1u) * Cfg::RAW_N;
-        mbar_expect_tx(bar, bytes);
-        tma_load_3d(raw + Cfg::R_U, &maps.u, bar, d0, t0, b);
+        const uint32_t nx = 1u + (with_u ? 1u : 0u) + (full ? 1u : 0u) + (hz ? 1u : 0u);
+        const uint32_t nn = (with_u ? 1u : 0u) + (full ? 1u : 0u);
+        mbar_expect_tx(bar, nx * Cfg::RAW_X + nn * Cfg::RAW_N);
         tma_load_3d(raw + Cfg::R_D, &maps.delta, bar, d0, t0, b);
-        tma_load_3d(raw + Cfg::R_B, &maps.B, bar, 0, t0, b);
+        if (with_u) {
+            tma_load_3d(raw + Cfg::R_U, &maps.u, bar, d0, t0, b);
+            tma_load_3d(raw + Cfg::R_B, &maps.B, bar, 0, t0, b);
+        }
         if (full) {
             if (hz) tma_load_3d(raw + Cfg::R_Z, &maps.z, bar, d0, t0, b);
             tma_load_3d(raw + Cfg::R_Y, &maps.dy, bar, d0, t0, b);
@@ -285,7 +297,7 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
             phase ^= 1u;
         }
     };
-    if (TMA && tid == 0) issue(c0, false);
+    if (TMA && tid == 0) issue(c0, kStFwd);
 
     float2 A2[2], An[2];                         // A·log2(e) and A = -exp(A_log), state pairs
 #pragma unroll
@@ -340,11 +352,11 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
         load_quad(seg == 0 ? p.h0 : p.h_slots + seg * count, h);
     for (int ch = c0; ch < c1; ++ch) {
         wait_staged();
-        bwd_prepare<Cfg, TIO, TMA>(sm, raw, p, b, d0, ch, false, bias_c);
+        bwd_prepare<Cfg, TIO, TMA, kStFwd>(sm, raw, p, b, d0, ch, bias_c);
         __syncthreads();                         // staged tiles consumed; the chunk's arrays are ready
         if (TMA && tid == 0 && !*abort_flag) {
-            if (ch + 1 < c1) issue(ch + 1, false);
-            else issue(c1 - 1, true);            // pass 2 starts from the last chunk
+            if (ch + 1 < c1) issue(ch + 1, kStFwd);
+            else issue(c1 - 1, LOCAL ? kStLam : kStFull);   // pass 2 starts from the last chunk
         }
 #pragma unroll 1
         for (int k = 0; k < NSUB; ++k) {
@@ -373,9 +385,9 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
         // the adjoint alone, λ = C·dŷ + μ, μ ← a·λ, from zero at the segment's end
         for (int ch = c1 - 1; ch >= c0; --ch) {
             wait_staged();
-            bwd_prepare<Cfg, TIO, TMA>(sm, raw, p, b, d0, ch, true, bias_c);
+            bwd_prepare<Cfg, TIO, TMA, kStLam>(sm, raw, p, b, d0, ch, bias_c);
             __syncthreads();
-            if (TMA && tid == 0 && ch > c0 && !*abort_flag) issue(ch - 1, true);
+            if (TMA && tid == 0 && ch > c0 && !*abort_flag) issue(ch - 1, kStLam);
 #pragma unroll 4
             for (int r = kBT - 1; r >= 0; --r) {
                 const float del = sm[Cfg::OFF_DEL + r * kBW + cw];
@@ -400,10 +412,10 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
     TIO* g_dz = static_cast<TIO*>(p.dz);
     for (int ch = c1 - 1; ch >= c0; --ch) {
         wait_staged();
-        bwd_prepare<Cfg, TIO, TMA>(sm, raw, p, b, d0, ch, true, bias_c);
+        bwd_prepare<Cfg, TIO, TMA, kStFull>(sm, raw, p, b, d0, ch, bias_c);
         if (TMA && tid == 0) tma_store_wait_read();   // the previous chunk's gradient tiles are read out
         __syncthreads();
-        if (TMA && tid == 0 && ch > c0 && !*abort_flag) issue(ch - 1, true);
+        if (TMA && tid == 0 && ch > c0 && !*abort_flag) issue(ch - 1, kStFull);
 #pragma unroll 1
         for (int k = NSUB - 1; k >= 0; --k) {
             float2 H[kBS][2], hb0[2];
