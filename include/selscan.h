@@ -257,7 +257,14 @@ ss_status ss_fwd_static(const void* u, const void* delta_raw, const float* delta
  *   Outputs must not overlap each other or any input.  The sums (dB, dC, dA_log, dD,
  *   ddelta_bias) are accumulated with atomic adds, so their rounding varies from run to run.
  *   workspace          device memory, 256-byte aligned, ss_bwd_workspace_size(...) bytes (the
- *                      state at every 16th step); contents need no initialisation.
+ *                      state at every 16th step and, for few channel tiles, the time split's
+ *                      per-segment entering states, adjoints and Σ Δ); contents need no
+ *                      initialisation.  Calls that share it must not overlap on the device.
+ * Schedule: one CTA per 32-channel tile over the whole sequence, or, when the tiles alone cannot
+ * fill the GPU (e.g. one long sequence), the sequence cut into segments that run side by side:
+ * each segment is folded and its adjoint swept from zero, the entering states are composed left
+ * to right and the entering adjoints right to left (the carry of the blog's section "チャンク間
+ * running prefix", both ways), then every segment runs both passes from them.  Four launches.
  * Errors as ss_fwd.  Returns SS_OK once the work is enqueued.
  */
 ss_status ss_bwd(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
@@ -267,7 +274,8 @@ ss_status ss_bwd(const void* u, const void* delta_raw, const float* delta_bias, 
                  int64_t batch, int64_t L, int64_t Dm, int64_t N, const ss_fwd_strides* strides,
                  void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes ss_bwd needs for these sizes (0: sizes invalid or empty). */
+/* Workspace bytes ss_bwd needs for these sizes on the current device (0: sizes invalid or
+ * empty); the time split's share depends on how many CTAs the device holds at once. */
 size_t ss_bwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N);
 
 /* Kernel width of the causal convolution (the Mamba blocks of the pages use 4). */
