@@ -181,7 +181,7 @@ ss_status ss_fwd_dtproj(const void* u, const void* dt_low, const float* W_dt, in
 
 /*
  * Forward pass on host-resident tensors: ss_fwd's result with the copies to and from the device
- * inside the call.  The batch rows are processed in groups (at least four when the batch allows)
+ * inside the call.  The batch rows are processed in groups (up to eight, one row each when the batch allows)
  * through two device staging slots on three internal streams, so that the copy in of one group,
  * the scan of another and the copy back of a third overlap.  No counterpart in the pages: it
  * serves callers whose tensors live in host memory.

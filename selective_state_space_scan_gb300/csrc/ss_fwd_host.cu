@@ -23,7 +23,7 @@ namespace selscan {
 namespace {
 
 constexpr int kSlots = 2;          // device staging slots (double buffering)
-constexpr int kMinGroups = 4;      // at least this many row groups when the batch allows it
+constexpr int kGroups = 8;         // row groups of ceil(batch / kGroups) rows (8 measured 2% faster than 4)
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -39,7 +39,7 @@ struct HostPlan {
 
 HostPlan host_plan(int64_t batch, int64_t L, int64_t Dm, int64_t N, int64_t es) {
     HostPlan h;
-    h.rows = std::max<int64_t>(1, (batch + kMinGroups - 1) / kMinGroups);
+    h.rows = std::max<int64_t>(1, (batch + kGroups - 1) / kGroups);
     h.groups = (batch + h.rows - 1) / h.rows;
     h.x_bytes = static_cast<size_t>(L * Dm * es);
     h.bc_bytes = static_cast<size_t>(L * N * es);

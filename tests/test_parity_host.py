@@ -57,7 +57,7 @@ def check(w, a, what, **kw):
 
 @pytest.mark.parametrize("batch", [1, 3, 5, 8, 9])
 def test_host_batch_groups(batch):
-    """Row groups of ceil(batch / 4): one group, ragged last groups, more groups than slots."""
+    """Row groups of ceil(batch / 8) rows: one group, ragged last groups, more groups than slots."""
     w = synth.fwd_inputs(batch, 300, 96, 16, seed=170 + batch)
     check(w, w.arrays, f"batch={batch}")
 
