@@ -679,16 +679,21 @@ extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* d
     if (batch == 0 || Dm == 0) return SS_OK;
     if (!A_log || !dA_log) return SS_ERR_INVALID_ARG;
     if (L > INT32_MAX || Dm > INT32_MAX || batch > INT32_MAX) return SS_ERR_UNSUPPORTED;
+    // alignment to the element type, checked before anything touches a device
+    const void* io_ptrs[] = {u, delta_raw, B, C, z, dy, du, ddelta_raw, dz};
+    for (const void* q : io_ptrs)
+        if (q && !is_aligned(q, es)) return SS_ERR_MISALIGNED;
+    const void* f_ptrs[] = {A_log, D, delta_bias, h0, dlast, dB, dC, dA_log, dD, ddelta_bias, dh0};
+    for (const void* q : f_ptrs)
+        if (q && !is_aligned(q, 4)) return SS_ERR_MISALIGNED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
     // the sums are accumulated: clear them (also the whole answer when L == 0)
     auto clear = [&](float* q, int64_t n) { return q ? cudaMemsetAsync(q, 0, sizeof(float) * n, stream) : cudaSuccess; };
     if (L == 0) {
         const void* small[] = {A_log, dA_log, dD, ddelta_bias, dh0, dlast};
-        for (const void* q : small) {
-            if (q && !is_aligned(q, 4)) return SS_ERR_MISALIGNED;
+        for (const void* q : small)
             if (q && !dev_ptr(q, dev)) return SS_ERR_INVALID_ARG;
-        }
         if (clear(dA_log, Dm * N) != cudaSuccess || clear(dD, Dm) != cudaSuccess ||
             clear(ddelta_bias, Dm) != cudaSuccess)
             return SS_ERR_CUDA;
@@ -709,12 +714,6 @@ extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* d
     if ((s.u_l < Dm || s.delta_l < Dm || (z && s.z_l < Dm) || (s.B_l < N && s.B_l != 0) ||
          (s.C_l < N && s.C_l != 0)) && L > 1)
         return SS_ERR_INVALID_ARG;
-    const void* io_ptrs[] = {u, delta_raw, B, C, z, dy, du, ddelta_raw, dz};
-    for (const void* q : io_ptrs)
-        if (q && !is_aligned(q, es)) return SS_ERR_MISALIGNED;
-    const void* f_ptrs[] = {A_log, D, delta_bias, h0, dlast, dB, dC, dA_log, dD, ddelta_bias, dh0};
-    for (const void* q : f_ptrs)
-        if (q && !is_aligned(q, 4)) return SS_ERR_MISALIGNED;
     const void* all[] = {u, delta_raw, B, C, z, dy, du, ddelta_raw, dz, A_log, D, delta_bias, h0, dlast,
                          dB, dC, dA_log, dD, ddelta_bias, dh0};
     for (const void* q : all)

@@ -79,3 +79,49 @@ def test_step_rejects_bad_arguments_on_host():
     assert call(batch=0) == 0
     assert call(state=None) == 1 and call(y=None) == 1
     assert call(state=FAKE + 2) == 3
+
+
+def test_conv1d_rejects_bad_arguments_on_host():
+    lib = ss.lib()
+    call = lambda **kw: lib.ss_conv1d(kw.get("x", FAKE), kw.get("w", FAKE), None, kw.get("out", FAKE), None, None,
+                                      kw.get("batch", 2), kw.get("L", 8), kw.get("Dm", 8), 1, kw.get("strides"), None)
+    assert call(batch=-1) == 1 and call(L=-1) == 1
+    assert call(batch=0) == 0 and call(Dm=0) == 0
+    assert call(w=None) == 1
+    s = ss.ConvStrides(9, 64, 8, 64, 8)
+    assert call(strides=ctypes.byref(s)) == 1              # unknown io dtype
+
+
+def test_bwd_rejects_bad_arguments_on_host():
+    lib = ss.lib()
+    assert lib.ss_bwd_workspace_size(0, 8, 8, 16) == 0 and lib.ss_bwd_workspace_size(1, 8, 8, 17) == 0
+
+    def call(**kw):
+        p = [FAKE] * 20
+        p[2] = p[6] = p[7] = p[8] = p[10] = p[13] = p[17] = p[18] = p[19] = None   # optional ones absent
+        for i, v in kw.get("ptrs", {}).items():
+            p[i] = v
+        return lib.ss_bwd(*p, kw.get("batch", 1), kw.get("L", 8), kw.get("Dm", 8), kw.get("N", 16), None, FAKE,
+                          1 << 20, None)
+    assert call(N=0) == 2 and call(N=17) == 2
+    assert call(batch=-1) == 1
+    assert call(batch=0) == 0
+    assert call(ptrs={3: None}) == 1                       # A_log
+    assert call(ptrs={11: FAKE + 2}) == 3                  # du not 4-byte aligned
+
+
+def test_dtproj_and_host_calls_reject_bad_arguments_on_host():
+    lib = ss.lib()
+    dt = lambda R, **kw: lib.ss_fwd_dtproj(FAKE, FAKE, FAKE, R, None, FAKE, FAKE, FAKE, None, None, FAKE, None, None,
+                                           kw.get("batch", 1), 8, 8, 16, kw.get("strides"), None)
+    assert dt(6) == 2 and dt(0) == 2 and dt(68) == 2       # rank not a multiple of 4 in 4..64
+    assert dt(8, batch=-1) == 1
+    s = ss.FwdStrides(ss.SS_BF16, 64, 8, 64, 8, 0, 0, 64, 8, 128, 16, 128, 16)
+    assert dt(8, strides=ctypes.byref(s)) == 2              # bf16 I/O
+    assert lib.ss_fwd_host_workspace_size(8, 2048, 1536, 16, ss.SS_F32) > 0
+    assert lib.ss_fwd_host_workspace_size(8, 2048, 1536, 16, 5) == 0
+    host = lambda **kw: lib.ss_fwd_host(FAKE, FAKE, None, FAKE, FAKE, FAKE, None, None, FAKE, None,
+                                        kw.get("batch", 1), 8, 8, kw.get("N", 16), kw.get("io", ss.SS_F32), FAKE,
+                                        1 << 20, None)
+    assert host(N=0) == 2 and host(io=3) == 1 and host(batch=-1) == 1
+    assert host(batch=0) == 0
