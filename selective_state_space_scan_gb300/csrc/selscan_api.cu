@@ -147,6 +147,17 @@ FwdVariant choose_fwd_variant(int64_t batch, int64_t Dm, int64_t N) {
     return v;
 }
 
+// Lanes per channel for the one-CTA-per-tile schedule: more warps pay there (the 2.8b-shaped
+// bf16 layer ran 993 us at 4 lanes against 1027 us at 2), so LPC doubles until about 16 warps
+// per SM (2432) rather than 8.  The balanced schedule keeps choose_fwd_variant's choice (at 4
+// lanes it measured 995 against 947 us).
+int per_tile_lpc(int64_t batch, int64_t Dm, int ns) {
+    const int64_t tiles32 = batch * ((Dm + 31) / 32);
+    int lpc = 1;
+    while (lpc < ns / 4 && tiles32 * lpc < 2432) lpc *= 2;
+    return lpc;
+}
+
 bool tma_stride_ok(int64_t stride_elems, int64_t es) {
     return stride_elems > 0 && (stride_elems * es) % 16 == 0 && stride_elems * es < (int64_t(1) << 40);
 }
@@ -200,7 +211,10 @@ const char* ss__fwd_kernel_name(int64_t batch, int64_t Dm, int64_t N) {
     if (N < 1 || N > 16) return "unsupported";
     FwdVariant v = choose_fwd_variant(batch, Dm, N);
     if (g_force_family.load() >= 0) v.family = g_force_family.load();
-    if (g_force_lpc.load() > 0) v.lpc = g_force_lpc.load();
+    if (g_force_lpc.load() > 0)
+        v.lpc = g_force_lpc.load();
+    else if (v.family == kFamLane)
+        v.lpc = per_tile_lpc(batch, Dm, v.ns);
     if (v.family == kFamSeg) return "ss_fwd_seg_kernel";
     return v.lpc == 1 ? "ss_fwd_lane_kernel(lpc=1)" : v.lpc == 2 ? "ss_fwd_lane_kernel(lpc=2)"
                                                                : "ss_fwd_lane_kernel(lpc=4)";
@@ -445,6 +459,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     // workspace, TMA-fed lane kernels that do not take the time split run the balanced one.
     v.balanced = plan.nseg < 2 && workspace != nullptr && v.family == kFamLane && tma && !v.lti && !dtp &&
                  g_force_balanced.load() != 0;
+    if (!v.balanced && plan.nseg < 2 && v.family == kFamLane && fl <= 0) v.lpc = per_tile_lpc(batch, Dm, v.ns);
     FwdMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     if (tma) {
@@ -663,6 +678,7 @@ int ss__fwd_plan(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dty
         return 1;
     }
     const bool bal = with_ws && g_force_balanced.load() != 0;
+    if (!bal && !fl) v.lpc = per_tile_lpc(batch, Dm, v.ns);
     std::snprintf(buf, sizeof(buf), "ss_fwd_lane_kernel(lpc=%d%s)", v.lpc, bal ? ",balanced" : "");
     put(buf);
     return 1;

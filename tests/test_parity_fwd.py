@@ -244,6 +244,17 @@ def test_rejects_host_pointer_and_aliasing():
 
 # ------------------------------------------------------------------ balanced schedule (ss_fwd_ws)
 
+def balanced_lpc(w):
+    """Lanes per channel of the balanced schedule for this workload (ss__fwd_plan's name)."""
+    import re
+    plan = ss.lib().ss__fwd_plan
+    plan.restype = ctypes.c_int
+    plan.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int32, ctypes.c_int, ctypes.c_char_p, ctypes.c_int]
+    buf = ctypes.create_string_buffer(128)
+    plan(w.batch, w.L, w.Dm, w.N, ss.SS_BF16 if w.io == "bf16" else ss.SS_F32, 1, buf, 128)
+    return int(re.search(r"lpc=(\d)", buf.value.decode()).group(1))
+
+
 @pytest.mark.parametrize("shape", [
     ("mamba130m", None), ("mamba2p8b_bf16", None),
     ("custom", (6, 1000, 4096, 16, "f32")),      # ~2 tiles per CTA, ranges split tiles mid-way
@@ -252,13 +263,15 @@ def test_rejects_host_pointer_and_aliasing():
     ("custom", (16, 200, 512, 16, "f32")),       # fewer tiles than CTAs: one tile per CTA
 ], ids=["130m", "2.8b", "split", "ragged-bf16", "n8", "few-tiles"])
 def test_balanced_equals_per_tile(shape):
-    """The balanced schedule hands the state between CTAs exactly: bitwise equal results."""
+    """The balanced schedule hands the state between CTAs exactly: bitwise equal results to the
+    one-CTA-per-tile schedule at the same lanes per channel (which ss_fwd may choose differently)."""
     name, dims = shape
     w = synth.config(name) if dims is None else synth.fwd_inputs(*dims[:4], io=dims[4], seed=21)
     if dims is not None:
         assert ss.ss_fwd_workspace_size(*dims[:4], ss.SS_BF16 if dims[4] == "bf16" else ss.SS_F32) > 0
-    y1, l1 = run_gpu(w, workspace=False)
-    y2, l2 = run_gpu(w, workspace=True)
+    lpc = balanced_lpc(w)
+    y1, l1 = run_gpu(w, workspace=False, variant=(0, lpc, -1))
+    y2, l2 = run_gpu(w, workspace=True, variant=(0, lpc, -1))
     np.testing.assert_array_equal(y1, y2)
     np.testing.assert_array_equal(l1, l2)
     if dims is not None and dims[0] * dims[1] * dims[2] < 3e6:
