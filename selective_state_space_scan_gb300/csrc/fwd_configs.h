@@ -32,6 +32,6 @@ constexpr int dt_pitch(int rank) { return (rank / 4) % 2 == 1 ? rank : rank + 4;
 // Segment-lane family (time-parallel; few channels, long sequences): 8 channels per CTA,
 // each warp holds 4 time segments of those 8 channels, 8 warps.  K = 7 steps per thread
 // keeps the swizzled tile reads free of bank conflicts for 8-channel rows.
-constexpr int kSegG = 1, kSegQ = 8, kSegK = 7, kSegStages = 3;
+constexpr int kSegG = 1, kSegQ = 8, kSegK = 7, kSegStages = 2;
 
 }  // namespace selscan
