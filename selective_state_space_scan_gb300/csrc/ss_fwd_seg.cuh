@@ -62,9 +62,12 @@ struct FwdCfg {
     static constexpr int OFF_C = OFF_B + up1k(TILE_N);
     static constexpr int STAGE_BYTES = OFF_C + up1k(TILE_N);
     // auxiliary shared memory after the stages (floats)
-    static constexpr int AUX_A = 0;                       // A'[W][NS] = -exp(A_log)·log2(e)
-    static constexpr int AUX_CARRY = AUX_A + W * NS;      // carry[2][W][NS]
-    static constexpr int AUX_AGGA = AUX_CARRY + 2 * W * NS;   // aggA[2][Q][W][4]
+    // A' and the carry are read as one state quad per channel by the warp's 8 channel lanes: a
+    // channel pitch of an odd number of 16-byte units (NSP floats) puts them on different banks
+    static constexpr int NSP = (NS / 4) % 2 == 1 ? NS : NS + 4;
+    static constexpr int AUX_A = 0;                       // A'[W][NSP] = -exp(A_log)·log2(e)
+    static constexpr int AUX_CARRY = AUX_A + W * NSP;     // carry[2][W][NSP]
+    static constexpr int AUX_AGGA = AUX_CARRY + 2 * W * NSP;  // aggA[2][Q][W][4]
     static constexpr int AUX_AGGH = AUX_AGGA + 2 * Q * W * 4; // aggH[2][Q][W][4]
     static constexpr int AUX_FLOATS = AUX_AGGH + 2 * Q * W * 4;
     static constexpr int AUX_BYTES = AUX_FLOATS * 4 + 64 + STAGES * 8;   // + abort flag + mbarriers
@@ -228,11 +231,11 @@ ss_fwd_seg_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     for (int i = tid; i < W * NS; i += Cfg::THREADS) {
         const int ww = i / NS, n = i % NS;
         const int dd = d0 + ww;
-        sA[i] = (dd < p.Dm && n < p.N) ? -expf(p.A_log[static_cast<int64_t>(dd) * p.N + n]) * kLog2e
-                                       : 0.f;
+        sA[ww * Cfg::NSP + n] = (dd < p.Dm && n < p.N) ? -expf(p.A_log[static_cast<int64_t>(dd) * p.N + n]) * kLog2e
+                                                      : 0.f;
         // the state before the first chunk: h0, or zeros
-        carry[i] = (p.h0 && dd < p.Dm && n < p.N)
-                       ? p.h0[(static_cast<int64_t>(b) * p.Dm + dd) * p.N + n] : 0.f;
+        carry[ww * Cfg::NSP + n] = (p.h0 && dd < p.Dm && n < p.N)
+                                       ? p.h0[(static_cast<int64_t>(b) * p.Dm + dd) * p.N + n] : 0.f;
     }
     __syncthreads();
     if (USE_TMA && tid == 0) {
@@ -277,12 +280,12 @@ ss_fwd_seg_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
 #pragma unroll
         for (int i = 0; i < K; ++i) yacc[i] = 0.f;
 
-        const float* carry_in = carry + (c & 1) * W * NS;
-        float* carry_out = carry + ((c & 1) ^ 1) * W * NS;
+        const float* carry_in = carry + (c & 1) * W * Cfg::NSP;
+        float* carry_out = carry + ((c & 1) ^ 1) * W * Cfg::NSP;
 
 #pragma unroll 1
         for (int qd = 0; qd < NQ; ++qd) {
-            const float4 A4 = *reinterpret_cast<const float4*>(sA + w * NS + qd * 4);
+            const float4 A4 = *reinterpret_cast<const float4*>(sA + w * Cfg::NSP + qd * 4);
             float a[K][4], bb[K][4];
             float H[4] = {0.f, 0.f, 0.f, 0.f};
             // pass 1: pairs and the thread-local fold over K steps
@@ -329,7 +332,7 @@ ss_fwd_seg_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                 }
                 named_barrier(1 + g, Q * 32);
             }
-            float4 hin4 = *reinterpret_cast<const float4*>(carry_in + w * NS + qd * 4);
+            float4 hin4 = *reinterpret_cast<const float4*>(carry_in + w * Cfg::NSP + qd * 4);
             float hin[4] = {hin4.x, hin4.y, hin4.z, hin4.w};
             if constexpr (Q > 1) {
                 for (int qq = 0; qq < q; ++qq) {
@@ -341,7 +344,7 @@ ss_fwd_seg_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                 }
             }
             if (q == Q - 1 && s_lo == 3) {
-                *reinterpret_cast<float4*>(carry_out + w * NS + qd * 4) =
+                *reinterpret_cast<float4*>(carry_out + w * Cfg::NSP + qd * 4) =
                     make_float4(fmaf(Ag[0], hin[0], H[0]), fmaf(Ag[1], hin[1], H[1]),
                                 fmaf(Ag[2], hin[2], H[2]), fmaf(Ag[3], hin[3], H[3]));
             }
@@ -381,9 +384,9 @@ ss_fwd_seg_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     }
 
     if (p.last_state && d_ok) {
-        const float* fin = carry + (nchunks & 1) * W * NS;
+        const float* fin = carry + (nchunks & 1) * W * Cfg::NSP;
         for (int n = seg; n < p.N; n += Cfg::S)
-            p.last_state[(static_cast<int64_t>(b) * p.Dm + d) * p.N + n] = fin[w * NS + n];
+            p.last_state[(static_cast<int64_t>(b) * p.Dm + d) * p.N + n] = fin[w * Cfg::NSP + n];
     }
 }
 
