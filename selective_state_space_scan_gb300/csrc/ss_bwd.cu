@@ -80,6 +80,7 @@ struct BwdParams {
     float* dsum;           // [nseg][batch·Dm]
     int64_t u_b, u_l, d_b, d_l, z_b, z_l, B_b, B_l, C_b, C_l;
     int batch, L, Dm, N, nchunks, tiles_per_batch;
+    int bc_vec;            // N % 4 == 0 and dB, dC 16-byte aligned: vector reductions into them
 };
 
 // TMA descriptors: [T][W] boxes of u, δ, z, dy (loaded) and du, dδ, dz (stored); [T][NS] boxes
@@ -507,17 +508,29 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
             if (p.z) tma_store_3d(&maps.dz, o_dz, d0, t0, b);
             tma_store_commit();
         }
-        for (int i = tid; i < Cfg::XN; i += Cfg::THREADS) {
-            const int r = i / NS, n = i % NS;
+        // four states per thread: one 16-byte reduction each into dB and dC (scalar atomics
+        // when N is not a multiple of 4 or the sums are not 16-byte aligned)
+        for (int i = tid; i < Cfg::XN / 4; i += Cfg::THREADS) {
+            const int r = i / (NS / 4), n = (i % (NS / 4)) * 4;
             const int t = ch * kBT + r;
-            float* bc = &sm[Cfg::OFF_BC + r * 2 * NS + n];
-            const float vb = bc[0], vc = bc[NS];
-            bc[0] = 0.f;
-            bc[NS] = 0.f;
+            float4* bc = reinterpret_cast<float4*>(&sm[Cfg::OFF_BC + r * 2 * NS + n]);
+            const float4 vb = bc[0], vc = bc[NS / 4];
+            bc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            bc[NS / 4] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (t < p.L && n < p.N) {
                 const int64_t o = (static_cast<int64_t>(b) * p.L + t) * p.N + n;
-                atomicAdd(p.dB + o, vb);
-                atomicAdd(p.dC + o, vc);
+                if (p.bc_vec) {
+                    atomicAdd(reinterpret_cast<float4*>(p.dB + o), vb);
+                    atomicAdd(reinterpret_cast<float4*>(p.dC + o), vc);
+                } else {
+                    const float b4[4] = {vb.x, vb.y, vb.z, vb.w}, c4[4] = {vc.x, vc.y, vc.z, vc.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (n + q < p.N) {
+                            atomicAdd(p.dB + o + q, b4[q]);
+                            atomicAdd(p.dC + o + q, c4[q]);
+                        }
+                }
             }
         }
     }
@@ -758,6 +771,7 @@ extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* d
     p.N = static_cast<int>(N);
     p.nchunks = static_cast<int>((L + kBT - 1) / kBT);
     p.tiles_per_batch = static_cast<int>((Dm + kBW - 1) / kBW);
+    p.bc_vec = (N % 4 == 0 && is_aligned(dB, 16) && is_aligned(dC, 16)) ? 1 : 0;
     if (static_cast<int64_t>(p.batch) * p.tiles_per_batch * plan.nseg > INT32_MAX) return SS_ERR_UNSUPPORTED;
     p.nseg = plan.nseg;
     p.seg_chunks = plan.nseg > 1 ? plan.seg_chunks : p.nchunks;

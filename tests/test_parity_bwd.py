@@ -280,3 +280,34 @@ def test_bwd_rejects_small_workspace_and_overlap():
     assert call(out["dd"].data_ptr(), need) == 1              # du over ddelta_raw
     assert call(out["du"].data_ptr(), need) == 0
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("N", [16, 6])
+def test_bwd_sums_at_4_byte_offsets(N):
+    """dB and dC 4-byte but not 16-byte aligned (and N not a multiple of 4): the kernel's scalar
+    atomics instead of its 16-byte reductions give the same sums."""
+    batch, L, Dm = 2, 80, 40
+    w, a, dy, h0, dlast = problem(batch, L, Dm, N, seed=66, with_h0=False, with_dlast=False)
+    lib = ss.lib()
+    t = {k: f32dev(v) for k, v in a.items() if v is not None}
+    dyd = f32dev(dy)
+    x = (batch, L, Dm)
+    du, dd, dz = (torch.empty(x, device="cuda") for _ in range(3))
+    dA = torch.empty((Dm, N), device="cuda")
+    n = batch * L * N
+    bc = torch.full((2 * n + 8,), float("nan"), device="cuda")
+    dB, dC = bc[1:1 + n], bc[n + 5:2 * n + 5]             # element offsets 1 and n + 5: never 16-byte aligned
+    s = ss.FwdStrides(ss.SS_F32, L * Dm, Dm, L * Dm, Dm, L * Dm, Dm, 0, 0, L * N, N, L * N, N)
+    need = lib.ss_bwd_workspace_size(batch, L, Dm, N)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    st = lib.ss_bwd(t["u"].data_ptr(), t["delta_raw"].data_ptr(), t["delta_bias"].data_ptr(), t["A_log"].data_ptr(),
+                    t["B"].data_ptr(), t["C"].data_ptr(), t["D"].data_ptr(), t["z"].data_ptr(), None, dyd.data_ptr(),
+                    None, du.data_ptr(), dd.data_ptr(), dz.data_ptr(), dB.data_ptr(), dC.data_ptr(), dA.data_ptr(),
+                    None, None, None, batch, L, Dm, N, ctypes.byref(s), ws.data_ptr(), need, None)
+    assert st == 0
+    torch.cuda.synchronize()
+    ref = reference(a, dy, None, None)
+    assert rel_l2(to_host(dB).reshape(batch, L, N), ref["dB"]) <= SUM_REL_L2
+    assert rel_l2(to_host(dC).reshape(batch, L, N), ref["dC"]) <= SUM_REL_L2
+    assert rel_l2(to_host(du), ref["du"]) <= GRAD_REL_L2
+    assert torch.isnan(bc[0]) and torch.isnan(bc[n + 1:n + 5]).all() and torch.isnan(bc[2 * n + 5:]).all()
