@@ -7,7 +7,7 @@
  * benchmark use it.  It shares no code, header, table or helper with the CUDA
  * library.
  *
- * Sources (the web pages this build is specified from):
+ * Sources (the web pages the method is taken from):
  *   [M]  "mamba-metal: Apple Silicon で Mamba を動かす" (createcentury blog #4),
  *        section "Selective scan の本質" (h_t = Ā_t h_{t-1} + B̄_t u_t, y_t = C_tᵀ h_t,
  *        Ā_t = exp(Δ_t A)), section "チャンク間 running prefix" (carry combined from
@@ -21,7 +21,7 @@
  *        contract: A_log [D,N], B,C [B,L,N], delta_raw,u,z [B,L,D], D [D]; the kernel
  *        takes raw A_log and applies -exp(A_log); softplus log(1+exp(x)) on delta_raw).
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   - B̄ is the Euler form b = Δ·B·u ([K] writes the pair's second element as Δ B u).
  *   - delta_bias (per channel, NULL = 0) is added to delta_raw before softplus.
  *   - softplus(x) = max(x,0) + log1p(exp(-|x|)), the exact overflow-free form.
