@@ -176,7 +176,7 @@ __device__ __forceinline__ void issue_stage_tma(uint8_t* st, uint64_t* bar, cons
 }
 
 template <class Cfg, bool USE_TMA>
-__global__ void __launch_bounds__(Cfg::THREADS)
+__global__ void __launch_bounds__(Cfg::THREADS, 2)   // two CTAs per SM: the few-rows grid is one wave
 ss_fwd_seg_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     using TIO = typename Cfg::TIO;
     constexpr int W = Cfg::W, K = Cfg::K, Q = Cfg::Q, NS = Cfg::NS, NQ = Cfg::NQ, T = Cfg::T;
@@ -276,9 +276,10 @@ ss_fwd_seg_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             du[i] = dd * uu;
             sumd += dd;
         }
-        float yacc[K];
+        // C·h partial sums of each step, over even and odd states (packed fp32x2 arithmetic)
+        float2 yacc[K];
 #pragma unroll
-        for (int i = 0; i < K; ++i) yacc[i] = 0.f;
+        for (int i = 0; i < K; ++i) yacc[i] = make_float2(0.f, 0.f);
 
         const float* carry_in = carry + (c & 1) * W * Cfg::NSP;
         float* carry_out = carry + ((c & 1) ^ 1) * W * Cfg::NSP;
@@ -286,19 +287,24 @@ ss_fwd_seg_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
 #pragma unroll 1
         for (int qd = 0; qd < NQ; ++qd) {
             const float4 A4 = *reinterpret_cast<const float4*>(sA + w * Cfg::NSP + qd * 4);
-            float a[K][4], bb[K][4];
-            float H[4] = {0.f, 0.f, 0.f, 0.f};
+            const float2 A2[2] = {make_float2(A4.x, A4.y), make_float2(A4.z, A4.w)};
+            // the quad's states as two pairs: (a, b) of every step, and the local fold
+            float2 a[K][2], bb[K][2];
+            float2 H2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             // pass 1: pairs and the thread-local fold over K steps
 #pragma unroll
             for (int i = 0; i < K; ++i) {
                 const float4 Bq = ld_quad<TIO, Cfg::RBC>(tB, row0 + i, qd);
+                const float2 Bp[2] = {make_float2(Bq.x, Bq.y), make_float2(Bq.z, Bq.w)};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    a[i][j] = ex2(dl[i] * f4get(A4, j));
-                    bb[i][j] = du[i] * f4get(Bq, j);
-                    H[j] = fmaf(a[i][j], H[j], bb[i][j]);
+                for (int pr = 0; pr < 2; ++pr) {
+                    const float2 e = mul2(make_float2(dl[i], dl[i]), A2[pr]);
+                    a[i][pr] = make_float2(ex2(e.x), ex2(e.y));
+                    bb[i][pr] = mul2(make_float2(du[i], du[i]), Bp[pr]);
+                    H2[pr] = fma2(a[i][pr], H2[pr], bb[i][pr]);
                 }
             }
+            float H[4] = {H2[0].x, H2[0].y, H2[1].x, H2[1].y};
             float Ag[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) Ag[j] = ex2(sumd * f4get(A4, j));
@@ -349,16 +355,16 @@ ss_fwd_seg_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                                 fmaf(Ag[2], hin[2], H[2]), fmaf(Ag[3], hin[3], H[3]));
             }
             // pass 2: replay the K pairs from the exclusive prefix, accumulate C·h
-            float h[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) h[j] = fmaf(Ae[j], hin[j], He[j]);
+            float2 h[2] = {make_float2(fmaf(Ae[0], hin[0], He[0]), fmaf(Ae[1], hin[1], He[1])),
+                           make_float2(fmaf(Ae[2], hin[2], He[2]), fmaf(Ae[3], hin[3], He[3]))};
 #pragma unroll
             for (int i = 0; i < K; ++i) {
                 const float4 Cq = ld_quad<TIO, Cfg::RBC>(tC, row0 + i, qd);
+                const float2 Cp[2] = {make_float2(Cq.x, Cq.y), make_float2(Cq.z, Cq.w)};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    h[j] = fmaf(a[i][j], h[j], bb[i][j]);
-                    yacc[i] = fmaf(f4get(Cq, j), h[j], yacc[i]);
+                for (int pr = 0; pr < 2; ++pr) {
+                    h[pr] = fma2(a[i][pr], h[pr], bb[i][pr]);
+                    yacc[i] = fma2(Cp[pr], h[pr], yacc[i]);
                 }
             }
         }
@@ -372,7 +378,7 @@ ss_fwd_seg_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                 const int r = row0 + i;
                 const int64_t t = tbase + r;
                 if (t < p.L) {
-                    float v = fmaf(D_w, ld_elem<TIO, Cfg::RB>(tu, r, w), yacc[i]);
+                    float v = fmaf(D_w, ld_elem<TIO, Cfg::RB>(tu, r, w), yacc[i].x + yacc[i].y);
                     if (has_z) v *= silu(ld_elem<TIO, Cfg::RB>(tz, r, w));
                     y[b * p.y_b + t * p.y_l + d] = from_f32<TIO>(v);
                 }
