@@ -126,10 +126,13 @@ def measured_traffic(workload: str, kernel: str):
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        rec = json.load(f).get(workload)
-    if not rec or rec.get("kernel") != kernel or rec.get("source_hash") != kernel_source_hash(kernel):
-        return None
-    return rec.get("dram_bytes_per_launch")
+        tab = json.load(f)
+    # one record per workload, plus "workload:kernel" for another call of the same workload
+    for key in (workload, f"{workload}:{kernel}"):
+        rec = tab.get(key)
+        if rec and rec.get("kernel") == kernel and rec.get("source_hash") == kernel_source_hash(kernel):
+            return rec.get("dram_bytes_per_launch")
+    return None
 
 
 def max_over_ranks(value: float, dist=None, device=None) -> float:
