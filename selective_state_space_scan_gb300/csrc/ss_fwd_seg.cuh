@@ -18,7 +18,7 @@
 //     ([T rows × W channels]) and B, C tiles ([T × N], shared by all W channels) arrive
 //     by TMA into a STAGES-deep ring of shared-memory buffers, each stage completing on
 //     its own mbarrier; the tiles use the hardware swizzle, and the reads below apply
-//     the same XOR so that no bank is hit twice by a warp.
+//     the same XOR, which puts a warp's B/C quad reads on different banks.
 //   * A warp's 32 lanes are 8 channels × 4 time segments; the warps of a channel group g
 //     are Q consecutive groups of 4 segments.  Each thread runs K consecutive steps of
 //     one channel sequentially (pass 1, folding the (a,b) pairs into a segment
