@@ -1,5 +1,6 @@
 """Host-side pieces of bench.py that need no GPU: the multi-rank timing aggregation over a
-2-rank gloo group, the whole-job throughput and the algorithmic byte counts."""
+2-rank gloo group, the whole-job throughput, the algorithmic byte counts and the lookup of
+stored DRAM traffic."""
 import os
 import socket
 import sys
@@ -61,3 +62,31 @@ def test_algorithmic_bytes_match_the_formula():
     assert bench.alg_bytes(w) == 1_345_953_792
     w = synth.Workload("decode1p4b", 64, 1, 4096, 16, "f32", 4)
     assert bench.alg_bytes(w) == 48 * 38_035_456
+
+
+def test_measured_traffic_follows_the_sources(tmp_path, monkeypatch):
+    """Stored DRAM traffic is reported only for the kernel it was captured on and only while
+    the hash of that kernel's sources matches; a second call of a workload has its own
+    "workload:kernel" record."""
+    import json
+    csrc = tmp_path / "selective_state_space_scan_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in set(sum(bench.KERNEL_SOURCES.values(), ())):
+        (csrc / f).write_text("// " + f + "\n")
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    lane, seg = "ss_fwd_lane_kernel(lpc=4)", "ss_fwd_seg_kernel"
+    tab = {"wl": {"kernel": lane, "source_hash": bench.kernel_source_hash(lane), "dram_bytes_per_launch": 1.0},
+           "wl:" + seg: {"kernel": seg, "source_hash": bench.kernel_source_hash(seg), "dram_bytes_per_launch": 2.0}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(tab))
+    assert bench.measured_traffic("wl", lane) == 1.0
+    assert bench.measured_traffic("wl", seg) == 2.0
+    assert bench.measured_traffic("wl", "ss_step_kernel") is None
+    assert bench.measured_traffic("other", lane) is None
+    # a segment-kernel source changes: its record goes stale, the lane kernel's does not
+    (csrc / "ss_fwd_seg.cuh").write_text("// changed\n")
+    assert bench.measured_traffic("wl", seg) is None
+    assert bench.measured_traffic("wl", lane) == 1.0
+    # a source both kernels are built from changes: both go stale
+    (csrc / "fwd_configs.h").write_text("// changed\n")
+    assert bench.measured_traffic("wl", lane) is None
