@@ -129,16 +129,22 @@ _WORKSPACES = {}
 _WS_SIZES = {}
 
 
-def workspace_for(device, stream_handle, nbytes: int, purpose: str = "fwd"):
+def workspace_for(device, stream, nbytes: int, purpose: str = "fwd"):
     """A zero-filled, 256-byte aligned device buffer of at least nbytes, cached per (device,
     stream, purpose) and grown when needed; calls on one stream are ordered, so they never
     overlap on the GPU while sharing it.  The forward schedules' hand-over flags and the
-    backward's checkpoints live in separate buffers (the flags must never see checkpoint bits)."""
+    backward's checkpoints live in separate buffers (the flags must never see checkpoint bits).
+    ``stream`` is the torch stream the calls run on (None: the device's current stream).  The
+    buffer is allocated and zero-filled on that stream, so the fill is ordered before its first
+    use, and when a larger buffer replaces it the caching allocator hands the old memory only to
+    later work on the same stream."""
     import torch
-    key = (str(device), stream_handle, purpose)
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    key = (str(device), s.cuda_stream, purpose)
     ws = _WORKSPACES.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(nbytes, 1), dtype=torch.uint8, device=device)
+        with torch.cuda.stream(s):
+            ws = torch.zeros(max(nbytes, 1), dtype=torch.uint8, device=device)
         _WORKSPACES[key] = ws
     return ws
 
@@ -186,7 +192,7 @@ def ss_fwd(u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, last_s
     sh = _stream_handle(stream)
     ws_ptr, ws_len = None, 0
     if nbytes:
-        ws = workspace_for(u.device, sh, nbytes)
+        ws = workspace_for(u.device, stream, nbytes)
         ws_ptr, ws_len = ws.data_ptr(), ws.numel()
     if h0 is not None:
         st = lib().ss_fwd_h0(*head, _ptr(h0), *dims, ws_ptr, ws_len, sh)
@@ -250,7 +256,7 @@ def ss_fwd_host(u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, l
             raise ValueError(f"{name} must be a contiguous CPU tensor")
     sh = _stream_handle(stream)
     nbytes = int(lib().ss_fwd_host_workspace_size(batch, L, Dm, N, io))
-    ws = workspace_for(dev, sh, nbytes, purpose="host") if nbytes else None
+    ws = workspace_for(dev, stream, nbytes, purpose="host") if nbytes else None
     st = lib().ss_fwd_host(_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D),
                            _ptr(z), _ptr(y), _ptr(last_state), batch, L, Dm, N, io,
                            None if ws is None else ws.data_ptr(), 0 if ws is None else ws.numel(), sh)
@@ -326,7 +332,7 @@ def ss_bwd(dy, u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, h0=None, d
                    0, 0, B.stride(0), B.stride(1), C.stride(0), C.stride(1))
     sh = _stream_handle(stream)
     nbytes = int(lib().ss_bwd_workspace_size(batch, L, Dm, N))
-    ws = workspace_for(u.device, sh, nbytes, purpose="bwd") if nbytes else None
+    ws = workspace_for(u.device, stream, nbytes, purpose="bwd") if nbytes else None
     st = lib().ss_bwd(_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                       _ptr(h0), _ptr(dy), _ptr(dlast), _ptr(g["du"]), _ptr(g["ddelta_raw"]), _ptr(g["dz"]),
                       _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dA_log"]), _ptr(g["dD"]), _ptr(g["ddelta_bias"]),
