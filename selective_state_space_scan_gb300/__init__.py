@@ -241,8 +241,9 @@ def ss_fwd_host(u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, l
     """Forward pass on host (CPU) tensors (ss_fwd_host): copies in, scan and copies back happen
     inside the call, overlapped over groups of batch rows.  All tensors are contiguous CPU tensors
     (pinned memory for asynchronous copies); ``y`` and ``last_state`` (optional) are written and
-    valid once the stream is synchronised.  The device staging workspace is cached per (device,
-    stream).  Returns y."""
+    valid once the stream is synchronised.  The call runs on ``device`` (default: the current one;
+    ``stream`` must be on it).  The device staging workspace is cached per (device, stream).
+    Returns y."""
     import torch
     batch, L, Dm = u.shape
     N = A_log.shape[1]
@@ -254,12 +255,15 @@ def ss_fwd_host(u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, l
                     ("D", D), ("delta_bias", delta_bias), ("last_state", last_state)):
         if t is not None and (t.is_cuda or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous CPU tensor")
-    sh = _stream_handle(stream)
-    nbytes = int(lib().ss_fwd_host_workspace_size(batch, L, Dm, N, io))
-    ws = workspace_for(dev, stream, nbytes, purpose="host") if nbytes else None
-    st = lib().ss_fwd_host(_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D),
-                           _ptr(z), _ptr(y), _ptr(last_state), batch, L, Dm, N, io,
-                           None if ws is None else ws.data_ptr(), 0 if ws is None else ws.numel(), sh)
+    if stream is not None and stream.device != dev:
+        raise ValueError(f"stream is on {stream.device}, the call on {dev}")
+    with torch.cuda.device(dev):          # the library runs on the current device
+        sh = _stream_handle(stream)
+        nbytes = int(lib().ss_fwd_host_workspace_size(batch, L, Dm, N, io))
+        ws = workspace_for(dev, stream, nbytes, purpose="host") if nbytes else None
+        st = lib().ss_fwd_host(_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D),
+                               _ptr(z), _ptr(y), _ptr(last_state), batch, L, Dm, N, io,
+                               None if ws is None else ws.data_ptr(), 0 if ws is None else ws.numel(), sh)
     if st != 0:
         raise SelscanError(st, "ss_fwd_host")
     return y
