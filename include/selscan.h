@@ -85,7 +85,9 @@ typedef struct {
  *                                           by all channels of a batch row
  *   D             [Dm] fp32 or NULL (= 0)   skip weight
  *   z             [batch, L, Dm] io_dtype or NULL (no gate)
- *   y             [batch, L, Dm] io_dtype   output; must not overlap any input
+ *   y             [batch, L, Dm] io_dtype   output; must not overlap any input, and its strides
+ *                                           must give every element its own address (no
+ *                                           stride-0 or overlapping rows): SS_ERR_INVALID_ARG
  *   last_state    [batch, Dm, N] fp32 contiguous or NULL: h_{L-1}, the state that a
  *                                           following ss_step continues from
  *   batch, L, Dm  >= 0; batch == 0 or Dm == 0 is a no-op; L == 0 writes zeros to
@@ -305,7 +307,8 @@ typedef struct {
  *   x            [batch, L, Dm] io_dtype
  *   weight       [Dm, 4] fp32 contiguous (a [Dm, 1, 4] depthwise Conv1d weight)
  *   bias         [Dm] fp32 or NULL (= 0)
- *   out          [batch, L, Dm] io_dtype; must not overlap any input or window
+ *   out          [batch, L, Dm] io_dtype; must not overlap any input or window, every element at
+ *                its own address (as y of ss_fwd)
  *   window_in    [batch, Dm, 3] fp32 contiguous or NULL (= the zero left padding): the three
  *                samples before t = 0, oldest first
  *   window_out   [batch, Dm, 3] fp32 contiguous or NULL; may be window_in itself (updated in
@@ -335,7 +338,8 @@ typedef struct {
  *   state[b,d,n] <- exp(Δ·A[d,n])·state[b,d,n] + Δ·x[b,d]·B[b,n]   (in place, fp32)
  *   y[b,d] = (Σ_n C[b,n]·state[b,d,n] + D[d]·x[b,d]) · silu(z[b,d])
  * Arguments as for ss_fwd with L = 1 and the initial state given; y must not overlap any
- * input or the state.  batch == 0 or Dm == 0 is a no-op.
+ * input or the state, and y and the state must each give every element its own address.
+ * batch == 0 or Dm == 0 is a no-op.
  */
 ss_status ss_step(float* state, const void* x, const void* delta_raw, const float* delta_bias,
                   const float* A_log, const void* B, const void* C, const float* D,

@@ -362,6 +362,8 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     }
     // B, C: rows at least N apart, or step stride 0 (time-invariant, the LTI case)
     if (((s.B_l < N && s.B_l != 0) || (s.C_l < N && s.C_l != 0)) && L > 1) return SS_ERR_INVALID_ARG;
+    // every element of y its own word (inputs may share memory, the output may not)
+    if (!host::distinct3(batch, s.y_b, L, s.y_l, Dm)) return SS_ERR_INVALID_ARG;
     const bool lti = L > 1 && s.B_l == 0 && s.C_l == 0 && !dtp;
     if (L > INT32_MAX || Dm > INT32_MAX || batch > INT32_MAX) return SS_ERR_UNSUPPORTED;
     // alignment to the element type
@@ -730,6 +732,9 @@ ss_status ss_step(float* state, const void* x, const void* delta_raw, const floa
                       s.C_b < N))
         return SS_ERR_INVALID_ARG;
     if (Dm > 1 && s.state_d < N) return SS_ERR_INVALID_ARG;
+    // y and the state are written: every element its own word
+    if (!host::distinct3(1, 0, batch, s.y_b, Dm) || !host::distinct3(batch, s.state_b, Dm, s.state_d, N))
+        return SS_ERR_INVALID_ARG;
     if (batch * Dm * 4 > (int64_t(1) << 40) || Dm > INT32_MAX || batch > INT32_MAX)
         return SS_ERR_UNSUPPORTED;
     const void* io_ptrs[] = {x, delta_raw, B, C, y, z};

@@ -222,6 +222,7 @@ extern "C" ss_status ss_conv1d(const void* x, const float* weight, const float* 
     if (L > 0 && (!x || !out)) return SS_ERR_INVALID_ARG;
     if (s.x_b < 0 || s.x_l < 0 || s.out_b < 0 || s.out_l < 0) return SS_ERR_INVALID_ARG;
     if (L > 1 && (s.x_l < Dm || s.out_l < Dm)) return SS_ERR_INVALID_ARG;
+    if (L > 0 && !distinct3(batch, s.out_b, L, s.out_l, Dm)) return SS_ERR_INVALID_ARG;   // out: one word each
     const void* f_ptrs[] = {weight, bias, window_in, window_out};
     for (const void* q : f_ptrs)
         if (q && !is_aligned(q, 4)) return SS_ERR_MISALIGNED;

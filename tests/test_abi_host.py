@@ -125,3 +125,46 @@ def test_dtproj_and_host_calls_reject_bad_arguments_on_host():
                                         1 << 20, None)
     assert host(N=0) == 2 and host(io=3) == 1 and host(batch=-1) == 1
     assert host(batch=0) == 0
+
+
+def _no_gpu():
+    try:
+        import torch
+        return not torch.cuda.is_available()
+    except ImportError:
+        return True
+
+
+def test_outputs_whose_elements_share_words_are_rejected_on_host():
+    """y (forward), y and the state (decode) and out (conv1d) are written, so no two of their
+    elements may sit at one address; inputs may (a broadcast).  Rejected before any device
+    access; a layout that passes reaches the device checks (SS_ERR_CUDA without a GPU)."""
+    full = dict(u=FAKE, delta_raw=FAKE, A_log=FAKE, B=FAKE, C=FAKE, y=FAKE)
+    # batch 2, L 8, Dm 8: (y_b, y_l)
+    for y_b, y_l in ((0, 8), (32, 8), (8, 8)):               # broadcast rows, rows running into each other
+        s = ss.FwdStrides(ss.SS_F32, 64, 8, 64, 8, 0, 0, y_b, y_l, 128, 16, 128, 16)
+        assert _fwd(**full, batch=2, strides=ctypes.byref(s)) == 1, (y_b, y_l)
+    s = ss.FwdStrides(ss.SS_F32, 0, 8, 0, 8, 0, 0, 64, 8, 0, 16, 0, 16)   # inputs broadcast over batch: allowed
+    ok = [_fwd(**full, batch=2, strides=ctypes.byref(s))]
+    for y_b, y_l in ((64, 8), (8, 16), (1000, 9)):           # contiguous, batch rows interleaved, padded
+        s = ss.FwdStrides(ss.SS_F32, 64, 8, 64, 8, 0, 0, y_b, y_l, 128, 16, 128, 16)
+        ok.append(_fwd(**full, batch=2, strides=ctypes.byref(s)))
+    if _no_gpu():                                              # (with a GPU the fake pointers fail the device check)
+        assert ok == [4] * len(ok), ok                         # past the layout checks, stopped at the device
+    lib = ss.lib()
+
+    def step(**kw):
+        st = ss.StepStrides(ss.SS_F32, 8, 8, 0, kw.get("y_b", 8), 16, 16, kw.get("state_b", 128), kw.get("state_d", 16))
+        return lib.ss_step(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, None, FAKE, 2, 8, 16, ctypes.byref(st), None)
+    assert step(state_b=0) == 1                                # both rows on one state
+    assert step(state_b=112) == 1                              # row 1 starts inside row 0
+    assert step(y_b=4) == 1
+    if _no_gpu():
+        assert step() == 4 and step(state_b=16, state_d=32) == 4   # contiguous; rows interleaved
+
+    def conv(out_b, out_l):
+        cs = ss.ConvStrides(ss.SS_F32, 64, 8, out_b, out_l)
+        return lib.ss_conv1d(FAKE, FAKE, None, FAKE, None, None, 2, 8, 8, 1, ctypes.byref(cs), None)
+    assert conv(0, 8) == 1 and conv(40, 8) == 1
+    if _no_gpu():
+        assert conv(64, 8) == 4
