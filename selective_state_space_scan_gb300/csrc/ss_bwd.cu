@@ -20,8 +20,9 @@
 // The per-(step, channel) quantities (Δ, σ(r), dŷ, dy·silu'(z), u) and the chunk's B, C are
 // staged in shared memory; dB, dC (sums over the CTA's channels) are reduced over a warp's
 // channel lanes by shuffles, over the warps with shared atomics, and reach global memory with
-// one atomic per (step, state) per CTA; dA_log, dD and dbias are summed over batch rows with
-// global atomics.
+// one 16-byte reduction per (step, four states) per CTA (scalar atomics when N is not a
+// multiple of 4 or the sums are not 16-byte aligned); dA_log, dD and dbias are summed over
+// batch rows with global atomics.
 #include <cuda_runtime.h>
 
 #include <atomic>
