@@ -90,3 +90,32 @@ def test_measured_traffic_follows_the_sources(tmp_path, monkeypatch):
     # a source both kernels are built from changes: both go stale
     (csrc / "fwd_configs.h").write_text("// changed\n")
     assert bench.measured_traffic("wl", lane) is None
+
+
+def _bench(args, env_extra):
+    import json
+    import subprocess
+    env = dict(os.environ, **env_extra)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, capture_output=True, text=True,
+                       env=env, cwd=ROOT, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    return [json.loads(l) for l in lines]
+
+
+def test_reference_arm_runs_the_oracle_on_the_host():
+    """bench.py --impl reference: the oracle timed on the host cores, one JSON line on rank 0
+    carrying the contract's keys, nothing from any other rank."""
+    args = ["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3"]
+    out = _bench(args, {"RANK": "0", "WORLD_SIZE": "1", "LOCAL_RANK": "0"})
+    assert len(out) == 1
+    d = out[0]
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 3 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"] and d["e2e"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"].startswith("tiny")
+    assert _bench(args, {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
