@@ -83,3 +83,52 @@ def test_bwd_A_to_zero_closed_form(oracle_mod):
     np.testing.assert_allclose(grads["du"], du, rtol=1e-12, atol=1e-13)
     dB = np.einsum("bsd,bsdn->bsn", dlt * a["u"], rev)
     np.testing.assert_allclose(grads["dB"], dB, rtol=1e-12, atol=1e-13)
+
+
+def test_bwd_matches_the_derivative_of_the_unrolled_sum(oracle_mod):
+    """Without the gate, the forward is the double sum h_t = Σ_{s≤t} e^{A(S_t − S_s)} Δ_s B_s u_s
+    (S_t = Σ_{r≤t} Δ_r), y_t = Σ_n C_t h_t + D u_t.  Differentiating J = Σ dy·y + Σ dlast·h_{L−1}
+    term by term, with G_t = dy_t C_t (+ dlast at t = L−1) and E_ts = e^{A(S_t − S_s)}:
+      ∂J/∂u_s = D dy_s + Σ_n Δ_s B_s Σ_{t≥s} G_t E_ts          ∂J/∂B_s = Σ_d Δ_s u_s Σ_{t≥s} G_t E_ts
+      ∂J/∂C_t = Σ_d dy_t h_t                                    ∂J/∂A  = Σ_t G_t Σ_{s≤t} (S_t − S_s) E_ts Δ_s B_s u_s
+      ∂J/∂Δ_r = Σ_n Σ_{t≥r} G_t (B_r u_r E_tr + A Σ_{s<r} E_ts Δ_s B_s u_s)
+    then dA_log = A·∂J/∂A, ∂J/∂δ_r = σ(δ_r + bias)·∂J/∂Δ_r, dbias = Σ ∂J/∂δ, dD = Σ dy·u.
+    An independent derivation of the oracle's adjoint recurrence, with real decays."""
+    batch, L, Dm, N = 2, 11, 3, 4
+    a, _, dy, dlast = _problem(5, batch=batch, L=L, Dm=Dm, N=N, gate=False)
+    g = oracle_mod.ss_bwd(a["u"], a["delta_raw"], a["delta_bias"], a["A_log"], a["B"], a["C"], a["D"], None, dy,
+                          dlast=dlast)
+    f = lambda k: a[k].astype(np.float64)
+    u, dr, Bm, Cm, D, bias = f("u"), f("delta_raw"), f("B"), f("C"), f("D"), f("delta_bias")
+    A = -np.exp(f("A_log"))
+    dyy = dy.astype(np.float64)
+    want = {k: np.zeros_like(v) for k, v in (("du", u), ("ddelta_raw", u), ("dB", Bm), ("dC", Cm))}
+    dA = np.zeros((Dm, N))
+    for b in range(batch):
+        for d in range(Dm):
+            x = dr[b, :, d] + bias[d]
+            dlt = np.logaddexp(0.0, x)
+            S = np.cumsum(dlt)
+            dDel = np.zeros(L)
+            for n in range(N):
+                E = np.exp(A[d, n] * (S[:, None] - S[None, :]))          # E[t, s]
+                G = dyy[b, :, d] * Cm[b, :, n]
+                G[-1] += dlast[b, d, n]
+                w = dlt * Bm[b, :, n] * u[b, :, d]                      # Δ_s B_s u_s
+                h = np.array([np.sum(E[t, :t + 1] * w[:t + 1]) for t in range(L)])
+                back = np.array([np.sum(G[s:] * E[s:, s]) for s in range(L)])   # Σ_{t≥s} G_t E_ts
+                want["du"][b, :, d] += dlt * Bm[b, :, n] * back
+                want["dB"][b, :, n] += dlt * u[b, :, d] * back
+                want["dC"][b, :, n] += dyy[b, :, d] * h
+                dA[d, n] += sum(G[t] * np.sum((S[t] - S[:t + 1]) * E[t, :t + 1] * w[:t + 1]) for t in range(L))
+                for r in range(L):
+                    inner = np.array([np.sum(E[t, :r] * w[:r]) for t in range(r, L)])
+                    dDel[r] += np.sum(G[r:] * (Bm[b, r, n] * u[b, r, d] * E[r:, r] + A[d, n] * inner))
+            want["du"][b, :, d] += D[d] * dyy[b, :, d]
+            want["ddelta_raw"][b, :, d] = dDel / (1.0 + np.exp(-x))
+    for k in ("du", "ddelta_raw", "dB", "dC"):
+        np.testing.assert_allclose(g[k], want[k], rtol=1e-11, atol=1e-12 * np.max(np.abs(want[k])), err_msg=k)
+    np.testing.assert_allclose(g["dA_log"], dA * A, rtol=1e-11, atol=1e-12 * np.max(np.abs(dA)))
+    np.testing.assert_allclose(g["dD"], np.sum(dyy * u, axis=(0, 1)), rtol=1e-12)
+    np.testing.assert_allclose(g["ddelta_bias"], want["ddelta_raw"].sum(axis=(0, 1)), rtol=1e-11,
+                               atol=1e-12 * np.max(np.abs(want["ddelta_raw"])))

@@ -120,6 +120,7 @@ def harness():
         lambda m: bwd.test_bwd_matches_finite_differences(m, True),
         lambda m: bwd.test_bwd_matches_finite_differences(m, False),
         bwd.test_bwd_A_to_zero_closed_form,
+        bwd.test_bwd_matches_the_derivative_of_the_unrolled_sum,
         dtp.test_dtproj_exact_projection_matches_plain_forward,
         lambda m: dtp.test_dtproj_general_projection_to_fp32_rounding(m, 4),
     ]
