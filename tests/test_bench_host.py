@@ -1,6 +1,6 @@
 """Host-side pieces of bench.py that need no GPU: the multi-rank timing aggregation over a
-2-rank gloo group, the whole-job throughput, the algorithmic byte counts and the lookup of
-stored DRAM traffic."""
+2-rank gloo group, the whole-job throughput, the algorithmic byte counts, the lookup of
+stored DRAM traffic, the clocks summary and the oracle reference arm."""
 import os
 import socket
 import sys
@@ -119,3 +119,28 @@ def test_reference_arm_runs_the_oracle_on_the_host():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"].startswith("tiny")
     assert _bench(args, {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
+
+
+def test_clock_summary_reads_nvidia_smi_rows(tmp_path):
+    """The clocks object from nvidia-smi's CSV rows: median SM clock over the loaded samples,
+    the maximum clock, and each throttle reason seen Active in any sample."""
+    rows = ["0, 1965, 2070, 410.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+            "0, 2070, 2070, 900.1, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+            "0, 2055, 2070, 890.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+            "0, 345, 2070, 120.0, 0x0000000000000001, Not Active, Not Active, Not Active, Not Active",   # idle
+            "garbage line"]
+    path = tmp_path / "clocks.csv"
+    path.write_text("\n".join(rows) + "\n")
+    c = bench.ClockSampler(0)
+    c.path = str(path)
+    c.warmup_steps = 12
+    s = c.summary()
+    assert s["sm_mhz"] == 2055.0 and s["sm_max_mhz"] == 2070.0        # idle sample left out of the median
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 4 and s["warmup_steps_run"] == 12
+    path.write_text(rows[0].replace("Not Active, Not Active, Not Active, Not Active",
+                                    "Active, Not Active, Active, Not Active") + "\n")
+    c.path = str(path)
+    assert c.summary()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    c.path = str(tmp_path / "empty.csv")
+    (tmp_path / "empty.csv").write_text("")
+    assert c.summary()["reasons"] == ["unavailable"]
