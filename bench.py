@@ -36,7 +36,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mamba130m",
+    ap.add_argument("--workload", default="mamba2p8b_bf16",
                     choices=["mamba130m", "long32k", "mamba2p8b_bf16", "decode1p4b", "tiny", "conv1d_130m",
                              "bwd_130m", "bwd_long32k", "lti_130m", "dtproj_130m"],
                     help="conv1d_130m times the causal conv1d + SiLU on the 130m layer's conv input "
@@ -45,14 +45,19 @@ def parse():
                          "lti_130m the forward with B and C constant over the steps; dtproj_130m the forward "
                          "with the rank-48 time-step projection folded in")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--probe", action="store_true",
+                    help="print the measured results per clock per SM of ex2, rcp, lg2, tanh, FFMA and FFMA2 "
+                         "(the library's pipe probe) and exit")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--variant", default=None,
                     help="pin the forward kernel as family,q,tma (family 0 channel-lane / 1 segment-lane; "
                          "q warps per CTA 1|2|4 or 0 auto; tma 1|0|-1 auto); default: the library's choice")
-    ap.add_argument("--workspace", action="store_true",
-                    help="call the forward pass with a workspace (ss_fwd_ws: the balanced or the time-split "
-                         "schedule); default: ss_fwd, one CTA per channel tile")
+    ap.add_argument("--workspace", action="store_true", default=True,
+                    help="(default) call the forward pass with the binding's cached workspace (ss_fwd_ws: the "
+                         "balanced or the time-split schedule)")
+    ap.add_argument("--no-workspace", dest="workspace", action="store_false",
+                    help="call the plain ss_fwd instead (one CTA per channel tile, no workspace)")
     return ap.parse_args()
 
 
@@ -77,9 +82,73 @@ def alg_bytes(w) -> int:
     return w.batch * w.L * (4 * w.Dm + 2 * w.N) * s + w.Dm * (w.N + 2) * 4 + w.batch * w.Dm * w.N * 4
 
 
-SFU_EX2_PER_CLK_PER_SM = 32      # MUFU ex2 results per SM per clock on GB300 (measured 31.6)
-GB300_SMS = 152
-GB300_MAX_SM_MHZ = 2070.0
+PROBE_KINDS = {"ex2": 0, "rcp": 1, "lg2": 2, "tanh": 3, "ffma": 4, "ffma2": 5}
+
+
+def max_sm_mhz(clocks=None) -> tuple:
+    """The SM clock the arithmetic peaks are quoted at: nvidia-smi's clocks.max.sm sampled during
+    the run, else the one MEASURED_PEAKS.json recorded."""
+    if clocks and clocks.get("sm_max_mhz"):
+        return float(clocks["sm_max_mhz"]), "nvidia-smi clocks.max.sm"
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("sm_max_mhz"):
+            return float(d["sm_max_mhz"]), "MEASURED_PEAKS.json sm_max_mhz"
+    raise RuntimeError("no SM clock: nvidia-smi gave none and MEASURED_PEAKS.json is absent")
+
+
+class PipePeaks:
+    """Arithmetic peaks of this GPU: the library's pipe probe (ss__pipe_probe: one CTA per SM,
+    independent chains, SM cycle counter) gives results per clock per SM for ex2 and fp32 FMA;
+    the SM count comes from the device properties and the clock from max_sm_mhz()."""
+
+    def __init__(self, ss, torch, dev):
+        import ctypes
+        fn = ss.lib().ss__pipe_probe
+        fn.restype = ctypes.c_int
+        fn.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
+        self.sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        self.per_clk = {}
+        for name in ("ex2", "ffma"):
+            r = ctypes.c_double(0.0)
+            if fn(PROBE_KINDS[name], 4096, ctypes.byref(r)) != 0:
+                raise RuntimeError(f"pipe probe {name} failed")
+            self.per_clk[name] = r.value
+
+    def ex2_per_s(self, clocks=None) -> float:
+        return self.sms * self.per_clk["ex2"] * max_sm_mhz(clocks)[0] * 1e6
+
+    def ffma_per_s(self, clocks=None) -> float:
+        return self.sms * self.per_clk["ffma"] * max_sm_mhz(clocks)[0] * 1e6
+
+    def source(self, clocks=None) -> str:
+        mhz, src = max_sm_mhz(clocks)
+        return (f"{self.sms} SMs (device properties) x {self.per_clk['ex2']:.2f} ex2/clk/SM (ss__pipe_probe, "
+                f"measured in this run) x {mhz:.0f} MHz ({src})")
+
+
+def run_probe(args, local_rank):
+    """--probe: results per clock per SM of every probed pipe operation, one JSON line."""
+    import ctypes
+    import torch
+    import selective_state_space_scan_gb300 as ss
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    fn = ss.lib().ss__pipe_probe
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
+    rates = {}
+    for name, kind in PROBE_KINDS.items():
+        r = ctypes.c_double(0.0)
+        if fn(kind, 4096, ctypes.byref(r)) != 0:
+            raise RuntimeError(f"pipe probe {name} failed")
+        rates[name] = round(r.value, 3)
+    props = torch.cuda.get_device_properties(dev)
+    print(json.dumps({"probe": "pipe results per clock per SM (ffma2: fp32 FMAs)", "per_clk_per_sm": rates,
+                      "sms": props.multi_processor_count, "gpu": props.name}))
+    return 0
 
 
 def decay_ex2_per_step(w) -> int:
@@ -282,6 +351,7 @@ def run_ours(args, w, rank, world, local_rank):
     import selective_state_space_scan_gb300 as ss
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    peaks_live = PipePeaks(ss, torch, dev)
     if args.variant:
         fam, q, tma = (int(x) for x in args.variant.split(","))
         hook = ss.lib().ss__force_fwd_variant
@@ -338,7 +408,7 @@ def run_ours(args, w, rank, world, local_rank):
     if not args.no_e2e and not decode:
         e2e = run_e2e(args, w, torch, ss, dev, tensors, y, last, barrier)
     return dict(total_ms=total_ms, per_launch_ms=per_launch_ms, clocks=clk.summary(), e2e=e2e,
-                kernel=kernel, launches=launches)
+                kernel=kernel, launches=launches, peaks=peaks_live)
 
 
 def run_e2e(args, w, torch, ss, dev, t, y, last, barrier):
@@ -449,6 +519,7 @@ def bench_lti(args, local_rank):
     from selective_state_space_scan_gb300 import synth
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    pk = PipePeaks(ss, torch, dev)
     w = synth.config("mamba130m")
     a = w.arrays
     t = {k: (None if v is None else torch.from_numpy(v).to(dev)) for k, v in a.items()}
@@ -467,7 +538,7 @@ def bench_lti(args, local_rank):
     # read u, delta_raw, z and write y; one B and C row per batch row; params; last_state
     alg = w.batch * w.L * 4 * w.Dm * 4 + 2 * w.batch * w.N * 4 + w.Dm * (w.N + 2) * 4 + w.batch * w.Dm * w.N * 4
     hbm_peak, peak_kind = peaks()
-    sfu_peak = GB300_SMS * SFU_EX2_PER_CLK_PER_SM * GB300_MAX_SM_MHZ * 1e6
+    sfu_peak = pk.ex2_per_s(clocks)
     achieved = alg / (launch_ms / 1e3) / 1e9
     kernel = "ss_fwd_lane_kernel(lpc=4,lti)"
     out = {
@@ -505,6 +576,7 @@ def bench_dtproj(args, local_rank):
     from selective_state_space_scan_gb300 import synth
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    pk = PipePeaks(ss, torch, dev)
     w = synth.config("mamba130m")
     a = w.arrays
     R = 48
@@ -526,8 +598,8 @@ def bench_dtproj(args, local_rank):
     # read u, z and write y; dt_low; B, C; params (W_dt, A_log, D, bias); last_state
     alg = (w.batch * w.L * (3 * w.Dm + R + 2 * w.N) * 4 + w.Dm * (R + w.N + 2) * 4 + w.batch * w.Dm * w.N * 4)
     hbm_peak, peak_kind = peaks()
-    sfu_peak = GB300_SMS * SFU_EX2_PER_CLK_PER_SM * GB300_MAX_SM_MHZ * 1e6
-    fma_peak = GB300_SMS * 128 * GB300_MAX_SM_MHZ * 1e6          # fp32 FMA lanes per second
+    sfu_peak = pk.ex2_per_s(clocks)
+    fma_peak = pk.ffma_per_s(clocks)                               # fp32 FMAs per second
     achieved = alg / (launch_ms / 1e3) / 1e9
     kernel = "ss_fwd_lane_kernel(lpc=4,dtproj)"
     out = {
@@ -611,6 +683,7 @@ def bench_bwd(args, local_rank):
     from selective_state_space_scan_gb300 import synth
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    pk = PipePeaks(ss, torch, dev)
     split = args.workload == "bwd_long32k"      # 48 channel tiles: the automatic time split
     w = synth.config("long32k" if split else "mamba130m")
     a = w.arrays
@@ -628,7 +701,7 @@ def bench_bwd(args, local_rank):
     achieved = alg / (launch_ms / 1e3) / 1e9
     # the SFU floor: two exp2 per state update (the forward recurrence and the adjoint one) at
     # the ex2 rate; below the HBM floor, so the bound is HBM
-    sfu_peak = GB300_SMS * SFU_EX2_PER_CLK_PER_SM * GB300_MAX_SM_MHZ * 1e6
+    sfu_peak = pk.ex2_per_s(clocks)
     t_hbm, t_sfu = alg / (hbm_peak * 1e9), 2 * units / sfu_peak
     out = {
         "metric": "selective-scan backward state-updates/s (B·L·D·N), 1×GB300",
@@ -668,6 +741,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     from selective_state_space_scan_gb300 import synth
+    if args.probe:
+        return run_probe(args, local_rank) if rank == 0 else 0
     if args.workload in ("conv1d_130m", "bwd_130m", "bwd_long32k", "lti_130m", "dtproj_130m"):
         if args.impl == "reference" or world > 1:
             if rank == 0:
@@ -696,7 +771,7 @@ def main():
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "io_dtype": w.io,
             "data": "synthetic", "config": workload_config(w),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
@@ -719,7 +794,7 @@ def main():
     hbm_peak, peak_kind = peaks()
     # Roofline of the dominant kernel: the slower of moving the algorithmic bytes at the
     # measured HBM copy bandwidth and issuing one exp2 per state update at the SFU rate.
-    sfu_peak = GB300_SMS * SFU_EX2_PER_CLK_PER_SM * GB300_MAX_SM_MHZ * 1e6     # ex2 / s
+    sfu_peak = res["peaks"].ex2_per_s(res["clocks"])     # ex2 / s
     ex2_launch = decay_ex2_per_step(w) / (DECODE_LAYERS if w.name.startswith("decode") else 1)
     t_hbm = bytes_launch / (hbm_peak * 1e9)
     t_sfu = ex2_launch / sfu_peak
@@ -731,14 +806,14 @@ def main():
         achieved = ex2_launch / (launch_ms / 1e3) / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": sfu_peak / 1e12, "unit": "Tex2/s",
                 "frac": achieved * 1e12 / sfu_peak,
-                "peak_source": "152 SMs x 32 MUFU ex2/clk x 2070 MHz (ex2 rate measured at 31.6/clk/SM)"}
+                "peak_source": res["peaks"].source(res["clocks"])}
     roof.update({"traffic": measured_traffic(w.name, res["kernel"]), "kernel": res["kernel"],
                  "launch_ms": launch_ms, "alg_bytes_per_launch": bytes_launch,
                  "decay_ex2_per_launch": ex2_launch, "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6})
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": w.io, "data": "synthetic",
         "config": workload_config(w, variant=args.variant), "hbm_gbs": alg_bytes(w) / (ms_step / 1e3) / 1e9,
         "gpu_launches": args.steps * res["launches"],
         "clocks": res["clocks"], "roofline": roof,

@@ -78,6 +78,14 @@ typedef struct {
 
 /*
  * Selective-scan forward pass (prefill / layer scan).
+ * Defined by: the recurrence and its left-to-right carry of "mamba-metal: Apple Silicon で
+ * Mamba を動かす" (sections "Selective scan の本質" and "チャンク間 running prefix"); the
+ * per-chunk steps, i.e. softplus on Δ, the D·u skip, out += h·C per state and the z·sigmoid(z)
+ * gate, of the same blog's walkthrough of the official CUDA forward kernel (section
+ * "1チャンク内の処理フロー"); the tensor contract of SpeechLens docs/kernel-optimization.md
+ * (MetalSelectiveScan: [B, L, D] streams, B and C [B, L, N] shared by every channel, raw A_log
+ * turned into -exp(A_log) inside the kernel).  last_state is the prefill-to-decode hand-off of
+ * the blog's section "O(L) インクリメンタルデコード".
  *   u, delta_raw  [batch, L, Dm] io_dtype   input activation, pre-softplus time step
  *   delta_bias    [Dm] fp32 or NULL (= 0)   added to delta_raw before softplus
  *   A_log         [Dm, N] fp32 contiguous    A = -exp(A_log), computed in-kernel
@@ -160,6 +168,44 @@ ss_status ss_fwd_h0(const void* u, const void* delta_raw, const float* delta_bia
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Summary of one segment of a sequence, for sequence parallelism: the state the segment's steps
+ * leave when folded from a zero state, and the sum of their Δ.  Over a segment the pairs
+ * (a_t, b_t) compose to (Π a_t, h_end) with Π a_t = exp(A · Σ Δ_t), so a segment is summed up by
+ * (h_end, Σ Δ): the aggregate that "mamba-metal: Apple Silicon で Mamba を動かす" (section
+ * "チャンク間 running prefix") carries from one chunk to the next, here between parts of a
+ * sequence held by different processes.  ss_carry_compose combines the summaries left to right
+ * into each segment's entering state; ss_fwd_h0 then runs each segment from it.
+ *   u, delta_raw, delta_bias, A_log, B   as for ss_fwd (C, D, z are not needed); the strides
+ *                struct's z, y and C fields are ignored
+ *   h_end        [batch, Dm, N] fp32 contiguous: h_{L-1} folded from h_{-1} = 0
+ *   dsum         [batch, Dm] fp32 contiguous: Σ_t softplus(delta_raw[b,t,d] + delta_bias[d])
+ *   L == 0       both outputs zero.
+ * Schedule: one CTA per 32-channel tile over the segment (the state-only fold of ss_fwd_ws's
+ * time split); the tiles must be TMA-fed (16-byte aligned bases and row strides, B rows of
+ * exactly 4, 8 or 16 states), otherwise SS_ERR_UNSUPPORTED (no fallback).  Outputs must not
+ * overlap the inputs or each other.  Errors as ss_fwd.
+ */
+ss_status ss_fwd_summary(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
+                         const void* B, float* h_end, float* dsum, int64_t batch, int64_t L, int64_t Dm, int64_t N,
+                         const ss_fwd_strides* strides, void* stream);
+
+/*
+ * Left-to-right composition of segment summaries into entering states (the carry of
+ * "mamba-metal: Apple Silicon で Mamba を動かす", section "チャンク間 running prefix", across
+ * segments):
+ *   H_0 = h0 (zeros if NULL),   H_s = exp(A · dsum[s-1]) · H_{s-1} + slots[s]   (s = 1 .. nseg-1)
+ * with A = -exp(A_log), per (b, d, n).
+ *   slots   [nseg][batch, Dm, N] fp32 contiguous, in/out: on entry slot s (s >= 1) is the h_end of
+ *           segment s-1 (ss_fwd_summary), slot 0 is ignored unless it is h0 itself; on exit slot s
+ *           is H_s, the state entering segment s
+ *   dsum    [nseg-1][batch, Dm] fp32 contiguous: the dsum of segments 0 .. nseg-2 (NULL if nseg == 1)
+ *   h0      [batch, Dm, N] fp32 or NULL; may be slot 0 itself, must not overlap another slot
+ *   nseg >= 1.  One thread per (b, d, n) walks the segments in order.  Errors as ss_fwd.
+ */
+ss_status ss_carry_compose(float* slots, const float* dsum, const float* h0, const float* A_log, int64_t nseg,
+                           int64_t batch, int64_t Dm, int64_t N, void* stream);
+
+/*
  * Forward pass with the low-rank time-step projection folded in: the pre-softplus time step is
  *   delta_raw[b,t,d] = Σ_k W_dt[d,k] · dt_low[b,t,k]   (k < dt_rank)
  * computed inside the scan instead of being read as a [batch, L, Dm] tensor.  This is the
@@ -219,16 +265,22 @@ size_t ss_fwd_host_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t 
  * or a plugin interface that passes the library tensors and a stream but no allocation hook.
  * The pages this library follows have no counterpart of this call; it is a packaging of
  * ss_fwd_ws.
- *   Arguments and results are those of ss_fwd: bitwise equal to it on the balanced schedule,
- *   equal up to rounding on the time-split one (see ss_fwd_ws).
+ *   Arguments and results are those of ss_fwd_ws on the same sizes: it runs the schedule
+ *   ss_fwd_ws picks (balanced or time-split), so its results are bitwise equal to ss_fwd_ws's,
+ *   and equal to ss_fwd's up to rounding (ss_fwd may split a channel's states over a different
+ *   number of lanes, which sums the C·h terms in another order).
  *   Workspace: a fixed SS_STATIC_WORKSPACE_BYTES array built into the library's device code;
  *   each device that loads the library holds it until the process exits.  The call allocates
  *   nothing (no cudaMalloc/cudaFree, no allocating library routine).
- *   Sizes whose ss_fwd_workspace_size exceeds SS_STATIC_WORKSPACE_BYTES return
- *   SS_ERR_UNSUPPORTED (use ss_fwd_ws with your own workspace).  Sizes that need no workspace
+ *   Sizes that need more than SS_STATIC_WORKSPACE_BYTES return SS_ERR_UNSUPPORTED (use
+ *   ss_fwd_ws with your own workspace).  For the balanced schedule that is its
+ *   ss_fwd_workspace_size; the time-split schedule takes as many segments as fit in the array
+ *   (at least two), as ss_fwd_ws does with a smaller workspace.  Sizes that need no workspace
  *   run as ss_fwd.
- *   The first call on each device looks up the array's device address (cudaGetSymbolAddress,
- *   with that device current) and caches it; make that first call before any stream capture.
+ *   The first call on each device (each CUDA context) looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that first call before
+ *   any stream capture.  The cache is keyed by the current context, so a context torn down and
+ *   created again (cudaDeviceReset) is looked up afresh.
  *   Every call on a device shares the array: calls that overlap on the GPU (e.g. on two
  *   streams) race and give wrong results.  Nothing in it needs clearing between calls.
  */
@@ -333,7 +385,10 @@ typedef struct {
 } ss_step_strides;
 
 /*
- * Single-token decode update (the O(1)-per-token step):
+ * Single-token decode update (the O(1)-per-token step of "mamba-metal: Apple Silicon で Mamba
+ * を動かす", section "O(L) インクリメンタルデコード": the recurrent state is kept and advanced
+ * one token at a time instead of re-scanning the prefix; the update itself is the recurrence of
+ * section "Selective scan の本質" at one step, with the softplus, skip and gate of ss_fwd):
  *   Δ = softplus(delta_raw[b,d] + delta_bias[d]);
  *   state[b,d,n] <- exp(Δ·A[d,n])·state[b,d,n] + Δ·x[b,d]·B[b,n]   (in place, fp32)
  *   y[b,d] = (Σ_n C[b,n]·state[b,d,n] + D[d]·x[b,d]) · silu(z[b,d])
@@ -345,6 +400,45 @@ ss_status ss_step(float* state, const void* x, const void* delta_raw, const floa
                   const float* A_log, const void* B, const void* C, const float* D,
                   const void* z, void* y, int64_t batch, int64_t Dm, int64_t N,
                   const ss_step_strides* strides, void* stream);
+
+/*
+ * The buffers of one layer for ss_step_layers: the pointer arguments of one ss_step call, same
+ * meaning, types and layout.
+ */
+typedef struct {
+    float* state;
+    const void* x;
+    const void* delta_raw;
+    const float* delta_bias;
+    const float* A_log;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    void* y;
+} ss_step_layer;
+
+/* Most layers one ss_step_layers call takes. */
+#define SS_STEP_MAX_LAYERS 128
+
+/*
+ * The decode update of many layers in one launch: for each layer l, exactly what
+ * ss_step(layers[l].state, layers[l].x, ..., layers[l].y, batch, Dm, N, strides, stream) does
+ * ("mamba-metal: Apple Silicon で Mamba を動かす", section "O(L) インクリメンタルデコード": each
+ * layer keeps and advances its own recurrent state).  The layers run at the same time, so this
+ * serves layers whose inputs are all ready, e.g. independent models or the states of a stack
+ * stepped together; a model whose layer l+1 reads layer l's y calls ss_step per layer.
+ *   layers       HOST array of n_layers descriptors (read during the call; the pointers in it are
+ *                device memory as for ss_step); the table travels in the kernel's parameters,
+ *                so the call allocates nothing
+ *   n_layers     0..SS_STEP_MAX_LAYERS (0 is a no-op; more returns SS_ERR_UNSUPPORTED)
+ *   batch, Dm, N, strides   shared by every layer, as for ss_step
+ * Each layer is validated as ss_step validates its arguments; in addition no layer's y or state
+ * may overlap another layer's buffers (SS_ERR_INVALID_ARG).  Results are bitwise equal to the
+ * n_layers ss_step calls.  Returns SS_OK once the work is enqueued.
+ */
+ss_status ss_step_layers(const ss_step_layer* layers, int64_t n_layers, int64_t batch, int64_t Dm, int64_t N,
+                         const ss_step_strides* strides, void* stream);
 
 /* Static, human-readable name of a status code. */
 const char* ss_status_string(ss_status status);

@@ -12,7 +12,7 @@ from typing import Optional
 
 from . import _build
 
-__all__ = ["ss_fwd", "ss_fwd_dtproj", "ss_fwd_host", "ss_step", "ss_conv1d", "ss_bwd", "ss_fwd_workspace_size", "SelscanError", "lib", "device_error",
+__all__ = ["ss_fwd", "ss_fwd_dtproj", "ss_fwd_host", "ss_step", "ss_step_layers", "ss_fwd_summary", "ss_carry_compose", "ss_conv1d", "ss_bwd", "ss_fwd_workspace_size", "SelscanError", "lib", "device_error",
            "version", "status_string", "SS_F32", "SS_BF16", "FwdStrides", "StepStrides", "ConvStrides"]
 
 SS_F32, SS_BF16 = 0, 1
@@ -66,6 +66,12 @@ def lib() -> ctypes.CDLL:
         L.ss_fwd_workspace_size.restype = ctypes.c_size_t
         L.ss_step.argtypes = [vp] * 10 + [i64] * 3 + [ctypes.POINTER(StepStrides), vp]
         L.ss_step.restype = ctypes.c_int
+        L.ss_step_layers.argtypes = [ctypes.POINTER(StepLayer), i64, i64, i64, i64, ctypes.POINTER(StepStrides), vp]
+        L.ss_step_layers.restype = ctypes.c_int
+        L.ss_fwd_summary.argtypes = [vp] * 7 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp]
+        L.ss_fwd_summary.restype = ctypes.c_int
+        L.ss_carry_compose.argtypes = [vp] * 4 + [i64] * 4 + [vp]
+        L.ss_carry_compose.restype = ctypes.c_int
         L.ss_conv1d.argtypes = [vp] * 6 + [i64] * 3 + [ctypes.c_int32, ctypes.POINTER(ConvStrides), vp]
         L.ss_conv1d.restype = ctypes.c_int
         L.ss_bwd.argtypes = [vp] * 20 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp, ctypes.c_size_t, vp]
@@ -288,6 +294,81 @@ def ss_step(state, x, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None
     if st != 0:
         raise SelscanError(st, "ss_step")
     return y
+
+
+def ss_fwd_summary(u, delta_raw, delta_bias, A_log, B, h_end=None, dsum=None, stream=None):
+    """Summary of one sequence segment through the C ABI (ss_fwd_summary): returns (h_end
+    [batch, Dm, N], dsum [batch, Dm]), the state the segment leaves from a zero start and the
+    sum of its Δ (float32, allocated when None)."""
+    import torch
+    batch, L, Dm = u.shape
+    N = A_log.shape[1]
+    io = _io_code(u.dtype)
+    if h_end is None:
+        h_end = torch.empty((batch, Dm, N), dtype=torch.float32, device=u.device)
+    if dsum is None:
+        dsum = torch.empty((batch, Dm), dtype=torch.float32, device=u.device)
+    for name, t in (("u", u), ("delta_raw", delta_raw), ("B", B)):
+        _check_inner(t, name)
+    s = FwdStrides(io, u.stride(0), u.stride(1), delta_raw.stride(0), delta_raw.stride(1), 0, 0, 0, 0,
+                   B.stride(0), B.stride(1), B.stride(0), B.stride(1))
+    st = lib().ss_fwd_summary(_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(h_end),
+                              _ptr(dsum), batch, L, Dm, N, ctypes.byref(s), _stream_handle(stream))
+    if st != 0:
+        raise SelscanError(st, "ss_fwd_summary")
+    return h_end, dsum
+
+
+def ss_carry_compose(slots, dsum, A_log, h0=None, stream=None):
+    """Left-to-right composition of segment summaries in place (ss_carry_compose): slots
+    [nseg, batch, Dm, N] float32 holds the segments' h_end in slots 1.. on entry and each
+    segment's entering state on exit; dsum [nseg - 1, batch, Dm]; h0 the state before segment 0
+    (None: zeros).  Returns slots."""
+    nseg, batch, Dm, N = slots.shape
+    st = lib().ss_carry_compose(_ptr(slots), _ptr(dsum) if nseg > 1 else None, _ptr(h0), _ptr(A_log), nseg, batch,
+                                Dm, N, _stream_handle(stream))
+    if st != 0:
+        raise SelscanError(st, "ss_carry_compose")
+    return slots
+
+
+class StepLayer(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("state", "x", "delta_raw", "delta_bias", "A_log", "B", "C", "D",
+                                               "z", "y")]
+
+
+def ss_step_layers(layers, stream=None):
+    """Many layers' decode steps in one launch through the C ABI (ss_step_layers).  ``layers`` is
+    a list of dicts with the tensors of one ss_step call each (keys state, x, delta_raw,
+    delta_bias, A_log, B, C and optionally D, z, y); every layer has the same sizes and strides.
+    Updates each state in place and returns the list of y tensors (allocated like x when a
+    layer gives none)."""
+    import torch
+    if not layers:
+        return []
+    first = layers[0]
+    batch, Dm, N = first["state"].shape
+    io = _io_code(first["x"].dtype)
+    table = (StepLayer * len(layers))()
+    ys = []
+    for i, L in enumerate(layers):
+        y = L.get("y")
+        if y is None:
+            y = torch.empty((batch, Dm), dtype=L["x"].dtype, device=L["x"].device)
+        ys.append(y)
+        for name in ("x", "delta_raw", "z", "B", "C", "state"):
+            _check_inner(L.get(name), name)
+        _check_inner(y, "y")
+        table[i] = StepLayer(*[_ptr(L.get(k)) for k in ("state", "x", "delta_raw", "delta_bias", "A_log", "B", "C",
+                                                        "D", "z")], _ptr(y))
+    x, dr, z, B, C, state = (first["x"], first["delta_raw"], first.get("z"), first["B"], first["C"],
+                             first["state"])
+    s = StepStrides(io, x.stride(0), dr.stride(0), z.stride(0) if z is not None else 0, ys[0].stride(0),
+                    B.stride(0), C.stride(0), state.stride(0), state.stride(1))
+    st = lib().ss_step_layers(table, len(layers), batch, Dm, N, ctypes.byref(s), _stream_handle(stream))
+    if st != 0:
+        raise SelscanError(st, "ss_step_layers")
+    return ys
 
 
 def ss_conv1d(x, weight, bias=None, out=None, window_in=None, window_out=None, silu=True, stream=None):

@@ -64,7 +64,30 @@ __device__ __forceinline__ float silu(float z) {
 // Packed fp32 pairs (one instruction for two lanes of arithmetic on sm_100+).
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 __device__ __forceinline__ float2 ex2x2(float2 v) { return make_float2(ex2(v.x), ex2(v.y)); }
+__device__ __forceinline__ float2 rcp2(float2 v) { return make_float2(rcp_approx(v.x), rcp_approx(v.y)); }
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+
+// softplus of two independent values (two steps of one channel): the same arithmetic as
+// softplus(), with the polynomial and the surrounding products on packed pairs, so one
+// instruction serves both (the SFU operations stay one per value).
+__device__ __forceinline__ float2 softplus2(float2 x) {
+    const float2 e = make_float2(ex2(-fabsf(x.x) * kLog2e), ex2(-fabsf(x.y) * kLog2e));
+    const float2 m = mul2(e, rcp2(add2(splat2(2.f), e)));
+    const float2 w = mul2(m, m);
+    float2 p = fma2(w, splat2(kLog1pP4), splat2(kLog1pP3));
+    p = fma2(w, p, splat2(kLog1pP2));
+    p = fma2(w, p, splat2(kLog1pP1));
+    p = fma2(w, p, splat2(kLog1pP0));
+    return fma2(m, p, make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)));
+}
+
+// silu of two independent values, as silu() with packed products.
+__device__ __forceinline__ float2 silu2(float2 z) {
+    const float2 e = ex2x2(mul2(z, splat2(-kLog2e)));
+    return mul2(z, rcp2(add2(splat2(1.f), e)));
+}
 
 template <typename T> __device__ __forceinline__ float to_f32(T v);
 template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }

@@ -17,10 +17,17 @@ constexpr int kLaneStages = SS_LANE_STAGES;
 #ifndef SS_LANE_MINB4
 #define SS_LANE_MINB4 3
 #endif
-constexpr int lane_minb(int lpc) { return lpc == 4 ? SS_LANE_MINB4 : lpc == 2 ? 6 : 8; }
-// Tile width: 32 channels for one CTA per tile; 16 for the balanced schedule, which needs at
-// least as many tiles as resident CTAs (a lane family tile is whole warps of 32/lpc channels).
-constexpr int lane_w(int lpc, bool balanced) { return balanced && lpc > 1 ? 16 : 32; }
+// Resident CTAs per SM the register budget is sized for: about 12 warps per SM with 2 or 4 lanes
+// per channel, 8 with one (a CTA of a w-channel tile is w·lpc/32 warps).
+constexpr int lane_minb(int lpc, int w) {
+    return (lpc == 4 ? 4 * SS_LANE_MINB4 : lpc == 2 ? 12 : 8) / (w * lpc / 32 > 0 ? w * lpc / 32 : 1);
+}
+// Tile width: 32 channels for one CTA per tile.  The balanced schedule needs at least as many
+// tiles as SMs times resident CTAs, so its fp32 tiles are 16 channels (64-byte rows); its bf16
+// tiles stay at 32 (64-byte rows too: narrower rows would have each 64-byte DRAM access read by
+// two CTAs at different times, which measured 1.8x the stream bytes in DRAM traffic).  A lane
+// family tile is whole warps of 32/lpc channels.
+constexpr int lane_w(int lpc, bool balanced, int es) { return balanced && lpc > 1 && es == 4 ? 16 : 32; }
 // With the low-rank time-step projection folded in: 48-step chunks (the staged dt_low tile
 // replaces the Δ tile and is wider), ranks up to 64, rows padded to an odd number of 16-byte
 // chunks (at most 68 floats).

@@ -8,7 +8,7 @@ namespace {
 
 template <int NS, int LPC>
 cudaError_t launch_dtp(const FwdParams& p, const FwdMaps& m, cudaStream_t stream) {
-    using Cfg = LaneCfg<float, NS, LPC, 32, kLaneTD, kLaneStages, lane_minb(LPC), kDtPitchMax>;
+    using Cfg = LaneCfg<float, NS, LPC, 32, kLaneTD, kLaneStages, lane_minb(LPC, 32), kDtPitchMax>;
     static_assert(Cfg::SMEM_BYTES <= 227 * 1024, "shared memory budget exceeded");
     return launch_with_smem<Cfg, true>(ss_fwd_lane_kernel<Cfg, true, false, false>, p, m, stream, Cfg::SMEM_BYTES);
 }

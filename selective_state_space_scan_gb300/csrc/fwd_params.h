@@ -46,6 +46,8 @@ struct FwdParams {
     int nseg;            // segments per tile in the schedule
     float* seg_slots;    // [nseg][batch·Dm·N]
     float* seg_dsum;     // [nseg - 1][batch·Dm]
+    int seg_out0;        // pass A writes segment s's end state to slot s + seg_out0 (1 in the time
+                         // split; 0 for a segment summary, whose slot 0 is the output)
     // Low-rank time-step projection folded in (dt_rank > 0): `delta` points to dt_low
     // [batch, L, dt_rank] (strides d_b, d_l) and delta_raw[b,t,d] = Σ_k W_dt[d,k] dt_low[b,t,k].
     const float* W_dt;   // [Dm, dt_rank] contiguous
@@ -72,6 +74,27 @@ struct StepParams {
     void* y;             // [batch, Dm]
     int64_t x_b, d_b, z_b, y_b, B_b, C_b, s_b, s_d;
     int batch, Dm, N;
+};
+
+// Decode step over many layers in one launch: the layers share sizes and strides (`common`,
+// whose pointers are unused) and each has its own buffers.
+constexpr int kStepMaxLayers = 128;
+struct StepLayerPtrs {
+    float* state;
+    const void* x;
+    const void* delta;
+    const void* z;
+    const void* Bm;
+    const void* Cm;
+    const float* bias;
+    const float* A_log;
+    const float* Dv;
+    void* y;
+};
+struct StepLayersParams {
+    StepParams common;
+    int n_layers;
+    StepLayerPtrs layer[kStepMaxLayers];
 };
 
 }  // namespace selscan

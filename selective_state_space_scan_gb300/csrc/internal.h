@@ -23,6 +23,8 @@ struct FwdVariant {
     bool state_only; // lane family, TMA: pass A of the time-split schedule (end states only)
     bool lti;        // lane family, TMA, per tile: B and C constant over the steps (held in registers)
     bool dtp;        // lane family, TMA, per tile: the low-rank time-step projection folded in
+    int es = 4;      // bytes per I/O element (4 fp32, 2 bf16)
+    int chunk = 0;   // test override of the steps per chunk (16, 32 or 256; 0: the kernels' own)
 };
 
 struct FwdGeom {
@@ -34,7 +36,7 @@ struct FwdGeom {
 inline FwdGeom fwd_geometry(const FwdVariant& v) {
     if (v.family == kFamSeg) return FwdGeom{8 * kSegG, 8 * kSegG, 4 * kSegQ * kSegK};
     if (v.dtp) return FwdGeom{32, 32, kLaneTD};
-    return FwdGeom{lane_w(v.lpc, v.balanced), lane_w(v.lpc, v.balanced), kLaneT};
+    return FwdGeom{lane_w(v.lpc, v.balanced, v.es), lane_w(v.lpc, v.balanced, v.es), v.chunk > 0 ? v.chunk : kLaneT};
 }
 
 // Launch (grid = p.grid CTAs; cooperative when v.balanced).  With `max_grid` non-null, launch
@@ -46,8 +48,13 @@ cudaError_t launch_fwd_lane_bf16(const FwdVariant& v, const FwdParams& p, const 
 cudaError_t launch_fwd_seg(const FwdVariant& v, bool bf16, const FwdParams& p, const FwdMaps& m,
                            cudaStream_t stream);
 cudaError_t launch_step(const StepParams& p, bool bf16, bool vec, cudaStream_t stream);
+cudaError_t launch_step_layers(const StepLayersParams& q, bool bf16, bool vec, cudaStream_t stream);
 // The lane kernel with the low-rank time-step projection folded in (fp32, per tile, TMA).
 cudaError_t launch_fwd_lane_dtp(const FwdVariant& v, const FwdParams& p, const FwdMaps& m, cudaStream_t stream);
+// Test instantiations at other chunk lengths (fwd_lane_chunks.cu): whether v (with v.chunk set)
+// is one of them, and its launch.
+bool chunk_override_ok(const FwdVariant& v);
+cudaError_t launch_fwd_lane_chunked(const FwdVariant& v, const FwdParams& p, const FwdMaps& m, cudaStream_t stream);
 // Time-split carry pass: slot 0 of p.seg_slots = h0 (or zeros); slot s = exp(A·ΣΔ of segment
 // s-1)·slot s-1 + the end state pass A left in slot s, for s = 1 .. p.nseg - 1.
 cudaError_t launch_fwd_carry(const FwdParams& p, cudaStream_t stream);
@@ -60,5 +67,8 @@ bool make_tile_map(CUtensorMap* m, const void* base, bool bf16, int64_t cols, in
 
 // The current device's error word (kErr* bits), or nullptr if its address cannot be found.
 unsigned int* device_error_word();
+
+// The calling thread's current CUDA context (nullptr if there is none or it cannot be had).
+CUcontext current_context();
 
 }  // namespace selscan

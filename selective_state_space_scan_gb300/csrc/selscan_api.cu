@@ -10,6 +10,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/selscan.h"
 #include "host_util.h"
@@ -40,6 +41,9 @@ std::atomic<int> g_force_balanced{1};
 // Test hook on the time-split schedule: -1 automatic (with a workspace, for shapes with too
 // few channel tiles to fill the GPU), 0 never, n >= 2 always with up to n segments.
 std::atomic<int> g_force_nseg{-1};
+// Test hook: steps per chunk of the lane kernel (0: its own 64; 16, 32 or 256: the test
+// instantiations of one configuration, per tile, which take no workspace schedule).
+std::atomic<int> g_force_chunk{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -55,38 +59,61 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-unsigned int* device_error_ptr() {
+}  // namespace
+
+// The calling thread's current CUDA context, through the runtime's driver entry point (the
+// library does not link libcuda); nullptr if it cannot be had.
+CUcontext current_context() {
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    });
+    CUcontext c = nullptr;
+    if (fn) fn(&c);
+    return c;
+}
+
+namespace {
+
+// Device address of a __device__ symbol, looked up with the device current and cached per device
+// and context: in host code the symbol's name is only a host-side handle, and a context that is
+// torn down and created again (cudaDeviceReset) loads the module afresh, at a new address.
+// nullptr if the lookup fails.
+template <class Sym>
+void* symbol_address(const Sym& sym, std::mutex& mu, CUcontext (&ctx)[64], void* (&addr)[64]) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-    static std::atomic<unsigned int*> cache[64] = {};
-    if (dev < 0 || dev >= 64) return nullptr;
-    unsigned int* p = cache[dev].load();
-    if (!p) {
-        void* a = nullptr;
-        if (cudaGetSymbolAddress(&a, g_device_error) != cudaSuccess) return nullptr;
-        p = static_cast<unsigned int*>(a);
-        cache[dev].store(p);
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    const CUcontext cur = current_context();
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] && cur && ctx[dev] == cur) return addr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, sym) != cudaSuccess) {   // creates the context if there is none yet
+        cudaGetLastError();
+        return nullptr;
     }
+    ctx[dev] = current_context();
+    addr[dev] = p;
     return p;
 }
 
-// Device address of g_static_ws on the current device.  In host code the symbol's name is only
-// a host-side handle, so the address is looked up once per device (with that device current)
-// and cached; a failed lookup returns nullptr.
+unsigned int* device_error_ptr() {
+    static std::mutex mu;
+    static CUcontext ctx[64] = {};
+    static void* addr[64] = {};
+    return static_cast<unsigned int*>(symbol_address(g_device_error, mu, ctx, addr));
+}
+
+// Device address of g_static_ws on the current device and context.
 void* static_workspace_ptr() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-    static std::atomic<void*> cache[64] = {};
-    if (dev < 0 || dev >= 64) return nullptr;
-    void* p = cache[dev].load();
-    if (!p) {
-        if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess) {
-            cudaGetLastError();
-            return nullptr;
-        }
-        cache[dev].store(p);
-    }
-    return p;
+    static std::mutex mu;
+    static CUcontext ctx[64] = {};
+    static void* addr[64] = {};
+    return symbol_address(g_static_ws, mu, ctx, addr);
 }
 
 // Argument checks shared with the other entry points (host_util.h).
@@ -220,6 +247,13 @@ const char* ss__fwd_kernel_name(int64_t batch, int64_t Dm, int64_t N) {
                                                                : "ss_fwd_lane_kernel(lpc=4)";
 }
 
+// Internal test hook (see g_force_chunk): 0 restores the kernels' own chunk length; returns the
+// previous setting, or -1 for a length without a test instantiation.
+int ss__force_chunk_steps(int steps) {
+    if (steps != 0 && steps != 16 && steps != 32 && steps != 256) return -1;
+    return g_force_chunk.exchange(steps);
+}
+
 // Internal test hook: 0 keeps ss_fwd_ws on the one-CTA-per-tile schedule; 1 (default) lets it
 // use the balanced schedule.
 int ss__force_balanced(int on) { return g_force_balanced.exchange(on ? 1 : 0); }
@@ -292,6 +326,19 @@ SplitPlan split_plan(int64_t tiles_total, int nchunks, int64_t rows, int64_t N, 
     pl.bytes = bytes(nseg);
     pl.off_dsum = split_slot_bytes(nseg, rows, N);
     return pl;
+}
+
+// Grid of the balanced schedule: a whole number of CTAs per SM when there are at least as many
+// tiles as SMs, so that every SM gets the same share of the work; never more CTAs than tiles
+// (a range must not lie inside one tile) or than fit on the GPU at once (cooperative launch).
+int64_t balanced_grid(int64_t tiles_total, int max_grid) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) {
+        const int64_t k = std::min<int64_t>(max_grid / sms, tiles_total / sms);
+        if (k >= 1) return k * sms;
+    }
+    return std::min<int64_t>(tiles_total, max_grid);
 }
 
 cudaError_t lane_max_grid(const FwdVariant& v, bool bf16, int* out) {
@@ -401,9 +448,12 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     // the GPU.  With few rows even LPC = 4 is not enough (a long sequence at batch 1) and the
     // segment-lane family, which runs time segments in parallel through the scan, takes over.
     FwdVariant v = choose_fwd_variant(batch, Dm, N);
+    v.es = static_cast<int>(es);
     const int max_lpc = v.ns / 4;
     const int ff = g_force_family.load(), fl = g_force_lpc.load(), ft = g_force_tma.load();
+    const int fc = dtp ? 0 : g_force_chunk.load();
     if (ff >= 0) v.family = ff;
+    if (fc > 0) v.chunk = fc;
     if (dtp) {                           // lane family only, as many lanes per channel as allowed
         if (v.family != kFamLane) v.lpc = max_lpc;
         v.family = kFamLane;
@@ -436,7 +486,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     // from zero; carry pass; pass C: the fold from each segment's carried start).
     const int fs = g_force_nseg.load();
     SplitPlan plan;
-    if (workspace && tma && !lti && !dtp && fs != 0 && (fs >= 2 || (v.family == kFamSeg && ff < 0))) {
+    if (workspace && tma && !lti && !dtp && fc == 0 && fs != 0 && (fs >= 2 || (v.family == kFamSeg && ff < 0))) {
         FwdVariant vs = v;
         vs.family = kFamLane;
         if (fl <= 0) vs.lpc = vs.ns / 4;
@@ -445,7 +495,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         vs.state_only = false;
         int max_grid = 0;
         if (lane_max_grid(vs, bf16, &max_grid) != cudaSuccess || max_grid <= 0) return SS_ERR_CUDA;
-        const int64_t tiles_ts = batch * ((Dm + lane_w(vs.lpc, false) - 1) / lane_w(vs.lpc, false));
+        const int64_t tiles_ts = batch * ((Dm + lane_w(vs.lpc, false, 4) - 1) / lane_w(vs.lpc, false, 4));
         const int64_t nch = (L + kLaneT - 1) / kLaneT;
         if (nch <= INT32_MAX && tiles_ts * 64 <= INT32_MAX) {
             plan = split_plan(tiles_ts, static_cast<int>(nch), batch * Dm, N, max_grid, ws_bytes, fs);
@@ -460,7 +510,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     // The schedule fixes the tile width (and so the box width): decide it first.  With a
     // workspace, TMA-fed lane kernels that do not take the time split run the balanced one.
     v.balanced = plan.nseg < 2 && workspace != nullptr && v.family == kFamLane && tma && !v.lti && !dtp &&
-                 g_force_balanced.load() != 0;
+                 fc == 0 && g_force_balanced.load() != 0;
     if (!v.balanced && plan.nseg < 2 && v.family == kFamLane && fl <= 0) v.lpc = per_tile_lpc(batch, Dm, v.ns);
     FwdMaps maps;
     std::memset(&maps, 0, sizeof(maps));
@@ -516,7 +566,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         // grid: every CTA resident at once (cooperative launch), never more CTAs than tiles
         int max_grid = 0;
         if (lane_max_grid(v, bf16, &max_grid) != cudaSuccess || max_grid <= 0) return SS_ERR_CUDA;
-        const int64_t grid = std::min<int64_t>(batch * tiles, max_grid);
+        const int64_t grid = balanced_grid(batch * tiles, max_grid);
         if (balanced_ws_bytes(static_cast<int>(grid), geo.tile_channels, v.ns) > ws_bytes)
             return SS_ERR_INVALID_ARG;
         if (!aligned(workspace, 256)) return SS_ERR_MISALIGNED;
@@ -536,6 +586,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         p.seg_chunks = plan.seg_chunks;
         p.seg_slots = static_cast<float*>(workspace);
         p.seg_dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.off_dsum);
+        p.seg_out0 = 1;                   // slot 0 holds h0; segment s ends in slot s + 1
         auto lane = [&](const FwdVariant& vv, const FwdParams& pp) {
             return bf16 ? launch_fwd_lane_bf16(vv, pp, maps, stream) : launch_fwd_lane_f32(vv, pp, maps, stream);
         };
@@ -556,6 +607,10 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         return cuda_status(lane(v, pc));
     }
     cudaError_t e;
+    if (v.chunk > 0) {
+        if (!chunk_override_ok(v)) return SS_ERR_UNSUPPORTED;
+        return cuda_status(launch_fwd_lane_chunked(v, p, maps, stream));
+    }
     if (v.family == kFamSeg)
         e = launch_fwd_seg(v, bf16, p, maps, stream);
     else
@@ -601,10 +656,19 @@ ss_status ss_fwd_h0(const void* u, const void* delta_raw, const float* delta_bia
                     strides, workspace, workspace_bytes, stream);
 }
 
-size_t ss_fwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dtype) {
+}  // extern "C"
+
+namespace selscan {
+namespace {
+
+// Workspace bytes of the schedule ss_fwd_ws picks for these sizes (0: none needed, or invalid
+// sizes).  *split tells whether it is the time split, which also runs on less (fewer segments).
+size_t fwd_ws_need(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dtype, bool* split) {
+    *split = false;
     if (batch <= 0 || L <= 0 || Dm <= 0 || N < 1 || N > 16) return 0;
     if (io_dtype != SS_F32 && io_dtype != SS_BF16) return 0;
     FwdVariant v = choose_fwd_variant(batch, Dm, N);
+    v.es = io_dtype == SS_BF16 ? 2 : 4;
     const int ff = g_force_family.load(), fs = g_force_nseg.load();
     if (ff >= 0) v.family = ff;
     const int fl = g_force_lpc.load() > 0 && g_force_lpc.load() <= v.ns / 4 ? g_force_lpc.load() : 0;
@@ -616,11 +680,12 @@ size_t ss_fwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N, in
         v.tma = true;
         int max_grid = 0;
         if (lane_max_grid(v, io_dtype == SS_BF16, &max_grid) != cudaSuccess || max_grid <= 0) return 0;
-        const int64_t tiles_ts = batch * ((Dm + lane_w(v.lpc, false) - 1) / lane_w(v.lpc, false));
+        const int64_t tiles_ts = batch * ((Dm + lane_w(v.lpc, false, 4) - 1) / lane_w(v.lpc, false, 4));
         const int64_t nch = (L + kLaneT - 1) / kLaneT;
         if (nch > INT32_MAX) return 0;
         const SplitPlan pl = split_plan(tiles_ts, static_cast<int>(nch), batch * Dm, N, max_grid,
                                         static_cast<size_t>(-1), fs);
+        *split = pl.nseg >= 2;
         return pl.nseg >= 2 ? pl.bytes : 0;
     }
     if (v.family != kFamLane) return 0;
@@ -630,8 +695,154 @@ size_t ss_fwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N, in
     const int64_t tiles = batch * ((Dm + geo.tile_channels - 1) / geo.tile_channels);
     int max_grid = 0;
     if (lane_max_grid(v, io_dtype == SS_BF16, &max_grid) != cudaSuccess || max_grid <= 0) return 0;
-    const int64_t grid = std::min<int64_t>(tiles, max_grid);
+    const int64_t grid = balanced_grid(tiles, max_grid);
     return balanced_ws_bytes(static_cast<int>(grid), geo.tile_channels, v.ns);
+}
+
+}  // namespace
+}  // namespace selscan
+
+extern "C" {
+
+ss_status ss_fwd_summary(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
+                         const void* B, float* h_end, float* dsum, int64_t batch, int64_t L, int64_t Dm, int64_t N,
+                         const ss_fwd_strides* strides, void* stream_ptr) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    if (batch < 0 || L < 0 || Dm < 0) return SS_ERR_INVALID_ARG;
+    if (N < 1 || N > 16) return SS_ERR_UNSUPPORTED;
+    ss_fwd_strides s;
+    if (strides) {
+        s = *strides;
+    } else {
+        std::memset(&s, 0, sizeof(s));
+        s.io_dtype = SS_F32;
+        s.u_b = s.delta_b = s.z_b = s.y_b = L * Dm;
+        s.u_l = s.delta_l = s.z_l = s.y_l = Dm;
+        s.B_b = s.C_b = L * N;
+        s.B_l = s.C_l = N;
+    }
+    if (s.io_dtype != SS_F32 && s.io_dtype != SS_BF16) return SS_ERR_INVALID_ARG;
+    const bool bf16 = s.io_dtype == SS_BF16;
+    const int64_t es = bf16 ? 2 : 4;
+    if (batch == 0 || Dm == 0) return SS_OK;
+    if (!A_log || !h_end || !dsum) return SS_ERR_INVALID_ARG;
+    if (!aligned(h_end, 4) || !aligned(dsum, 4) || !aligned(A_log, 4)) return SS_ERR_MISALIGNED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+    if (!is_device_pointer(h_end, dev) || !is_device_pointer(dsum, dev) || !is_device_pointer(A_log, dev))
+        return SS_ERR_INVALID_ARG;
+    const Range sh = span3(h_end, batch, Dm, N, Dm * N, N, 4);
+    const Range sd = span3(dsum, 1, batch, Dm, 0, Dm, 4);
+    if (overlap(sh, sd)) return SS_ERR_INVALID_ARG;
+    if (L == 0) {   // no steps: the end state from zero is zero, and so is the sum of Δ
+        if (cudaMemsetAsync(h_end, 0, sizeof(float) * batch * Dm * N, stream) != cudaSuccess) return SS_ERR_CUDA;
+        return cuda_status(cudaMemsetAsync(dsum, 0, sizeof(float) * batch * Dm, stream));
+    }
+    if (!u || !delta_raw || !B) return SS_ERR_INVALID_ARG;
+    const int64_t st[] = {s.u_b, s.u_l, s.delta_b, s.delta_l, s.B_b, s.B_l};
+    for (int64_t v : st)
+        if (v < 0) return SS_ERR_INVALID_ARG;
+    if ((s.u_l < Dm || s.delta_l < Dm || s.B_l < N) && L > 1) return SS_ERR_INVALID_ARG;
+    if (L > INT32_MAX || Dm > INT32_MAX || batch > INT32_MAX) return SS_ERR_UNSUPPORTED;
+    const void* io_ptrs[] = {u, delta_raw, B};
+    for (const void* q : io_ptrs)
+        if (!aligned(q, es)) return SS_ERR_MISALIGNED;
+    if (delta_bias && !aligned(delta_bias, 4)) return SS_ERR_MISALIGNED;
+    const void* ptrs[] = {u, delta_raw, B, delta_bias};
+    for (const void* q : ptrs)
+        if (q && !is_device_pointer(q, dev)) return SS_ERR_INVALID_ARG;
+    const Range ins[] = {span3(u, batch, L, Dm, s.u_b, s.u_l, es), span3(delta_raw, batch, L, Dm, s.delta_b, s.delta_l, es),
+                        span3(B, batch, L, N, s.B_b, s.B_l, es), span3(A_log, 1, Dm, N, 0, N, 4),
+                        span3(delta_bias, 1, 1, Dm, 0, 0, 4)};
+    for (const Range& in : ins)
+        if (overlap(sh, in) || overlap(sd, in)) return SS_ERR_INVALID_ARG;
+
+    // The state-only fold (the time split's first pass) over the whole sequence as one segment:
+    // one CTA per 32-channel tile, TMA-fed tiles of u, Δ and B (C and z are not read).
+    FwdVariant v = choose_fwd_variant(batch, Dm, N);
+    v.es = static_cast<int>(es);
+    v.family = kFamLane;
+    v.lpc = v.ns / 4;
+    v.tma = true;
+    v.state_only = true;
+    v.balanced = false;
+    bool tma = N == v.ns && (N * es) % 16 == 0 && aligned(u, 16) && aligned(delta_raw, 16) && aligned(B, 16) &&
+               tma_stride_ok(s.u_l, es) && tma_stride_ok(s.delta_l, es) && tma_stride_ok(s.B_l, es);
+    if (batch > 1)
+        tma = tma && tma_stride_ok(s.u_b, es) && tma_stride_ok(s.delta_b, es) && tma_stride_ok(s.B_b, es);
+    const FwdGeom geo = fwd_geometry(v);
+    FwdMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    tma = tma && make_map(&maps.u, u, bf16, Dm, L, batch, s.u_l, s.u_b, geo.box_channels, geo.chunk_steps, true) &&
+          make_map(&maps.delta, delta_raw, bf16, Dm, L, batch, s.delta_l, s.delta_b, geo.box_channels,
+                   geo.chunk_steps, true) &&
+          make_map(&maps.B, B, bf16, N, L, batch, s.B_l, s.B_b, v.ns, geo.chunk_steps, false);
+    if (!tma) return SS_ERR_UNSUPPORTED;   // the state-only fold is TMA-fed only; no fallback
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.u = u; p.delta = delta_raw; p.Bm = B; p.bias = delta_bias; p.A_log = A_log;
+    p.u_b = s.u_b; p.u_l = s.u_l; p.d_b = s.delta_b; p.d_l = s.delta_l; p.B_b = s.B_b; p.B_l = s.B_l;
+    const int64_t tiles = (Dm + geo.tile_channels - 1) / geo.tile_channels;
+    if (batch * tiles > INT32_MAX) return SS_ERR_UNSUPPORTED;
+    p.batch = static_cast<int>(batch);
+    p.L = static_cast<int>(L);
+    p.Dm = static_cast<int>(Dm);
+    p.N = static_cast<int>(N);
+    p.nchunks = static_cast<int>((L + geo.chunk_steps - 1) / geo.chunk_steps);
+    p.tiles_per_batch = static_cast<int>(tiles);
+    p.chunk_steps = geo.chunk_steps;
+    p.tile_channels = geo.tile_channels;
+    p.box_channels = geo.box_channels;
+    p.err = device_error_ptr();
+    if (!p.err) return SS_ERR_CUDA;
+    p.seg_launch = 1;
+    p.seg_chunks = p.nchunks;
+    p.nseg = 1;
+    p.seg_slots = h_end;
+    p.seg_dsum = dsum;
+    p.seg_out0 = 0;
+    p.grid = static_cast<int>(batch * tiles);
+    return cuda_status(bf16 ? launch_fwd_lane_bf16(v, p, maps, stream) : launch_fwd_lane_f32(v, p, maps, stream));
+}
+
+ss_status ss_carry_compose(float* slots, const float* dsum, const float* h0, const float* A_log, int64_t nseg,
+                           int64_t batch, int64_t Dm, int64_t N, void* stream_ptr) {
+    if (nseg < 1 || batch < 0 || Dm < 0) return SS_ERR_INVALID_ARG;
+    if (N < 1 || N > 16) return SS_ERR_UNSUPPORTED;
+    if (batch == 0 || Dm == 0) return SS_OK;
+    if (!slots || !A_log || (nseg > 1 && !dsum)) return SS_ERR_INVALID_ARG;
+    if (batch * Dm * N * nseg > (int64_t(1) << 40) || Dm > INT32_MAX || nseg > INT32_MAX) return SS_ERR_UNSUPPORTED;
+    const void* f_ptrs[] = {slots, dsum, h0, A_log};
+    for (const void* q : f_ptrs)
+        if (q && !aligned(q, 4)) return SS_ERR_MISALIGNED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+    for (const void* q : f_ptrs)
+        if (q && !is_device_pointer(q, dev)) return SS_ERR_INVALID_ARG;
+    const int64_t rows = batch * Dm;
+    const Range ss_ = span3(slots, 1, nseg, rows * N, 0, rows * N, 4);
+    const Range ins[] = {span3(nseg > 1 ? dsum : nullptr, 1, nseg - 1, rows, 0, rows, 4),
+                        span3(A_log, 1, Dm, N, 0, N, 4)};
+    for (const Range& in : ins)
+        if (overlap(ss_, in)) return SS_ERR_INVALID_ARG;
+    // h0 may be slot 0 itself; it must not overlap any other slot
+    if (h0 && h0 != slots && overlap(ss_, span3(h0, 1, 1, rows * N, 0, 0, 4))) return SS_ERR_INVALID_ARG;
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.A_log = A_log;
+    p.h0 = h0;
+    p.seg_slots = slots;
+    p.seg_dsum = const_cast<float*>(dsum);
+    p.batch = static_cast<int>(batch);
+    p.Dm = static_cast<int>(Dm);
+    p.N = static_cast<int>(N);
+    p.nseg = static_cast<int>(nseg);
+    return cuda_status(launch_fwd_carry(p, static_cast<cudaStream_t>(stream_ptr)));
+}
+
+size_t ss_fwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dtype) {
+    bool split = false;
+    return fwd_ws_need(batch, L, Dm, N, io_dtype, &split);
 }
 
 // Internal reporting hook (not part of the public header): the schedule a forward call with
@@ -651,6 +862,7 @@ int ss__fwd_plan(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dty
         return 0;
     }
     FwdVariant v = choose_fwd_variant(batch, Dm, N);
+    v.es = io_dtype == SS_BF16 ? 2 : 4;
     const int ff = g_force_family.load(), fs = g_force_nseg.load();
     if (ff >= 0) v.family = ff;
     const int fl = g_force_lpc.load() > 0 && g_force_lpc.load() <= v.ns / 4 ? g_force_lpc.load() : 0;
@@ -662,7 +874,7 @@ int ss__fwd_plan(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dty
         if (!fl) vs.lpc = vs.ns / 4;
         int max_grid = 0;
         if (lane_max_grid(vs, io_dtype == SS_BF16, &max_grid) == cudaSuccess && max_grid > 0) {
-            const int64_t tiles = batch * ((Dm + lane_w(vs.lpc, false) - 1) / lane_w(vs.lpc, false));
+            const int64_t tiles = batch * ((Dm + lane_w(vs.lpc, false, 4) - 1) / lane_w(vs.lpc, false, 4));
             const int64_t nch = (L + kLaneT - 1) / kLaneT;
             if (nch <= INT32_MAX) {
                 const SplitPlan pl = split_plan(tiles, static_cast<int>(nch), batch * Dm, N, max_grid,
@@ -691,8 +903,11 @@ ss_status ss_fwd_static(const void* u, const void* delta_raw, const float* delta
                         const void* z, void* y, float* last_state, int64_t batch, int64_t L,
                         int64_t Dm, int64_t N, const ss_fwd_strides* strides, void* stream) {
     const int32_t io = strides ? strides->io_dtype : SS_F32;
-    const size_t need = (batch > 0 && L > 0 && Dm > 0) ? ss_fwd_workspace_size(batch, L, Dm, N, io) : 0;
-    if (need > SS_STATIC_WORKSPACE_BYTES) return SS_ERR_UNSUPPORTED;   // beyond the fixed array
+    bool split = false;
+    const size_t need = (batch > 0 && L > 0 && Dm > 0) ? fwd_ws_need(batch, L, Dm, N, io, &split) : 0;
+    // beyond the fixed array: the balanced schedule cannot shrink; the time split takes as many
+    // segments as the array holds (fwd_impl's plan), or none below two
+    if (need > SS_STATIC_WORKSPACE_BYTES && !split) return SS_ERR_UNSUPPORTED;
     void* ws = nullptr;
     if (need > 0) {
         ws = static_workspace_ptr();
@@ -702,13 +917,29 @@ ss_status ss_fwd_static(const void* u, const void* delta_raw, const float* delta
                     strides, ws, ws ? SS_STATIC_WORKSPACE_BYTES : 0, stream);
 }
 
-ss_status ss_step(float* state, const void* x, const void* delta_raw, const float* delta_bias,
-                  const float* A_log, const void* B, const void* C, const float* D, const void* z,
-                  void* y, int64_t batch, int64_t Dm, int64_t N, const ss_step_strides* strides,
-                  void* stream_ptr) {
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-    if (batch < 0 || Dm < 0) return SS_ERR_INVALID_ARG;
-    if (N < 1 || N > 16) return SS_ERR_UNSUPPORTED;
+}  // extern "C"
+
+namespace selscan {
+namespace {
+
+// Validated decode-step arguments of one layer.
+struct StepCheck {
+    ss_status status = SS_OK;
+    bool empty = false;      // batch == 0 or Dm == 0: nothing to do
+    bool bf16 = false;
+    bool vec = false;        // the vector (state quad) path applies
+    StepParams p{};
+    Range out_y, out_state;  // the bytes the step writes
+    Range in[8];             // the bytes it reads
+};
+
+StepCheck step_check(float* state, const void* x, const void* delta_raw, const float* delta_bias,
+                     const float* A_log, const void* B, const void* C, const float* D, const void* z,
+                     void* y, int64_t batch, int64_t Dm, int64_t N, const ss_step_strides* strides) {
+    StepCheck r;
+    auto fail = [&](ss_status e) { r.status = e; return r; };
+    if (batch < 0 || Dm < 0) return fail(SS_ERR_INVALID_ARG);
+    if (N < 1 || N > 16) return fail(SS_ERR_UNSUPPORTED);
     ss_step_strides s;
     if (strides) {
         s = *strides;
@@ -720,36 +951,40 @@ ss_status ss_step(float* state, const void* x, const void* delta_raw, const floa
         s.state_b = Dm * N;
         s.state_d = N;
     }
-    if (s.io_dtype != SS_F32 && s.io_dtype != SS_BF16) return SS_ERR_INVALID_ARG;
+    if (s.io_dtype != SS_F32 && s.io_dtype != SS_BF16) return fail(SS_ERR_INVALID_ARG);
     const bool bf16 = s.io_dtype == SS_BF16;
+    r.bf16 = bf16;
     const int64_t es = bf16 ? 2 : 4;
-    if (batch == 0 || Dm == 0) return SS_OK;
-    if (!state || !x || !delta_raw || !A_log || !B || !C || !y) return SS_ERR_INVALID_ARG;
+    if (batch == 0 || Dm == 0) {
+        r.empty = true;
+        return r;
+    }
+    if (!state || !x || !delta_raw || !A_log || !B || !C || !y) return fail(SS_ERR_INVALID_ARG);
     const int64_t st[] = {s.x_b, s.delta_b, s.y_b, s.B_b, s.C_b, s.state_b, s.state_d, z ? s.z_b : 0};
     for (int64_t v : st)
-        if (v < 0) return SS_ERR_INVALID_ARG;
+        if (v < 0) return fail(SS_ERR_INVALID_ARG);
     if (batch > 1 && (s.x_b < Dm || s.delta_b < Dm || s.y_b < Dm || (z && s.z_b < Dm) || s.B_b < N ||
                       s.C_b < N))
-        return SS_ERR_INVALID_ARG;
-    if (Dm > 1 && s.state_d < N) return SS_ERR_INVALID_ARG;
+        return fail(SS_ERR_INVALID_ARG);
+    if (Dm > 1 && s.state_d < N) return fail(SS_ERR_INVALID_ARG);
     // y and the state are written: every element its own word
     if (!host::distinct3(1, 0, batch, s.y_b, Dm) || !host::distinct3(batch, s.state_b, Dm, s.state_d, N))
-        return SS_ERR_INVALID_ARG;
+        return fail(SS_ERR_INVALID_ARG);
     if (batch * Dm * 4 > (int64_t(1) << 40) || Dm > INT32_MAX || batch > INT32_MAX)
-        return SS_ERR_UNSUPPORTED;
+        return fail(SS_ERR_UNSUPPORTED);
     const void* io_ptrs[] = {x, delta_raw, B, C, y, z};
-    for (const void* p : io_ptrs)
-        if (p && !aligned(p, es)) return SS_ERR_MISALIGNED;
+    for (const void* q : io_ptrs)
+        if (q && !aligned(q, es)) return fail(SS_ERR_MISALIGNED);
     const void* f_ptrs[] = {state, A_log, D, delta_bias};
-    for (const void* p : f_ptrs)
-        if (p && !aligned(p, 4)) return SS_ERR_MISALIGNED;
+    for (const void* q : f_ptrs)
+        if (q && !aligned(q, 4)) return fail(SS_ERR_MISALIGNED);
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(SS_ERR_CUDA);
     const void* all_ptrs[] = {state, x, delta_raw, B, C, y, z, A_log, D, delta_bias};
-    for (const void* p : all_ptrs)
-        if (p && !is_device_pointer(p, dev)) return SS_ERR_INVALID_ARG;
-    const Range sy = span3(y, 1, batch, Dm, 0, s.y_b, es);
-    const Range sst = span3(state, batch, Dm, N, s.state_b, s.state_d, 4);
+    for (const void* q : all_ptrs)
+        if (q && !is_device_pointer(q, dev)) return fail(SS_ERR_INVALID_ARG);
+    r.out_y = span3(y, 1, batch, Dm, 0, s.y_b, es);
+    r.out_state = span3(state, batch, Dm, N, s.state_b, s.state_d, 4);
     const Range ins[] = {span3(x, 1, batch, Dm, 0, s.x_b, es),
                         span3(delta_raw, 1, batch, Dm, 0, s.delta_b, es),
                         span3(z, 1, batch, Dm, 0, s.z_b, es),
@@ -758,11 +993,13 @@ ss_status ss_step(float* state, const void* x, const void* delta_raw, const floa
                         span3(A_log, 1, Dm, N, 0, N, 4),
                         span3(D, 1, 1, Dm, 0, 0, 4),
                         span3(delta_bias, 1, 1, Dm, 0, 0, 4)};
-    for (const Range& in : ins)
-        if (overlap(sy, in) || overlap(sst, in)) return SS_ERR_INVALID_ARG;
-    if (overlap(sy, sst)) return SS_ERR_INVALID_ARG;
+    for (int i = 0; i < 8; ++i) {
+        r.in[i] = ins[i];
+        if (overlap(r.out_y, ins[i]) || overlap(r.out_state, ins[i])) return fail(SS_ERR_INVALID_ARG);
+    }
+    if (overlap(r.out_y, r.out_state)) return fail(SS_ERR_INVALID_ARG);
 
-    StepParams p;
+    StepParams& p = r.p;
     p.state = state; p.x = x; p.delta = delta_raw; p.z = z; p.Bm = B; p.Cm = C;
     p.bias = delta_bias; p.A_log = A_log; p.Dv = D; p.y = y;
     p.x_b = s.x_b; p.d_b = s.delta_b; p.z_b = s.z_b; p.y_b = s.y_b;
@@ -771,11 +1008,65 @@ ss_status ss_step(float* state, const void* x, const void* delta_raw, const floa
     p.Dm = static_cast<int>(Dm);
     p.N = static_cast<int>(N);
     // vector path: whole state quads, 16-byte aligned state and A_log rows, B/C quads aligned
-    const bool vec = (N % 4 == 0) && aligned(state, 16) && aligned(A_log, 16) &&
-                     (s.state_d % 4 == 0 || Dm == 1) && (s.state_b % 4 == 0 || batch == 1) &&
-                     aligned(B, 4 * es) && aligned(C, 4 * es) && (s.B_b % 4 == 0 || batch == 1) &&
-                     (s.C_b % 4 == 0 || batch == 1);
-    return cuda_status(launch_step(p, bf16, vec, stream));
+    r.vec = (N % 4 == 0) && aligned(state, 16) && aligned(A_log, 16) &&
+            (s.state_d % 4 == 0 || Dm == 1) && (s.state_b % 4 == 0 || batch == 1) &&
+            aligned(B, 4 * es) && aligned(C, 4 * es) && (s.B_b % 4 == 0 || batch == 1) &&
+            (s.C_b % 4 == 0 || batch == 1);
+    return r;
+}
+
+}  // namespace
+}  // namespace selscan
+
+extern "C" {
+
+ss_status ss_step(float* state, const void* x, const void* delta_raw, const float* delta_bias,
+                  const float* A_log, const void* B, const void* C, const float* D, const void* z,
+                  void* y, int64_t batch, int64_t Dm, int64_t N, const ss_step_strides* strides,
+                  void* stream_ptr) {
+    const StepCheck c = step_check(state, x, delta_raw, delta_bias, A_log, B, C, D, z, y, batch, Dm, N, strides);
+    if (c.status != SS_OK || c.empty) return c.status;
+    return cuda_status(launch_step(c.p, c.bf16, c.vec, static_cast<cudaStream_t>(stream_ptr)));
+}
+
+ss_status ss_step_layers(const ss_step_layer* layers, int64_t n_layers, int64_t batch, int64_t Dm, int64_t N,
+                         const ss_step_strides* strides, void* stream_ptr) {
+    if (n_layers < 0) return SS_ERR_INVALID_ARG;
+    if (n_layers > kStepMaxLayers) return SS_ERR_UNSUPPORTED;
+    if (n_layers == 0) return SS_OK;
+    if (!layers) return SS_ERR_INVALID_ARG;
+    static_assert(sizeof(StepLayersParams) <= 32000, "kernel parameter block too large");
+    StepLayersParams q;
+    std::memset(&q, 0, sizeof(q));
+    q.n_layers = static_cast<int>(n_layers);
+    std::vector<StepCheck> cs;
+    cs.reserve(static_cast<size_t>(n_layers));
+    bool vec = true;
+    for (int64_t l = 0; l < n_layers; ++l) {
+        const ss_step_layer& L = layers[l];
+        cs.push_back(step_check(L.state, L.x, L.delta_raw, L.delta_bias, L.A_log, L.B, L.C, L.D, L.z, L.y, batch,
+                                Dm, N, strides));
+        const StepCheck& c = cs.back();
+        if (c.status != SS_OK) return c.status;
+        if (c.empty) return SS_OK;          // sizes are shared: every layer is empty
+        vec = vec && c.vec;
+        if (l == 0) q.common = c.p;
+        StepLayerPtrs& P = q.layer[l];
+        P.state = L.state; P.x = L.x; P.delta = L.delta_raw; P.z = L.z; P.Bm = L.B; P.Cm = L.C;
+        P.bias = L.delta_bias; P.A_log = L.A_log; P.Dv = L.D; P.y = L.y;
+    }
+    // the layers run at the same time: what one writes must not meet what another reads or writes
+    for (int64_t a = 0; a < n_layers; ++a)
+        for (int64_t b = 0; b < n_layers; ++b) {
+            if (a == b) continue;
+            const StepCheck& A = cs[static_cast<size_t>(a)];
+            const StepCheck& Bc = cs[static_cast<size_t>(b)];
+            if (overlap(A.out_y, Bc.out_y) || overlap(A.out_y, Bc.out_state) || overlap(A.out_state, Bc.out_state))
+                return SS_ERR_INVALID_ARG;
+            for (const Range& in : Bc.in)
+                if (overlap(A.out_y, in) || overlap(A.out_state, in)) return SS_ERR_INVALID_ARG;
+        }
+    return cuda_status(launch_step_layers(q, cs[0].bf16, vec, static_cast<cudaStream_t>(stream_ptr)));
 }
 
 }  // extern "C"

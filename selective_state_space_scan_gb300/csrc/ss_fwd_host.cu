@@ -5,9 +5,11 @@
 // 130m-shaped layer.)
 // Every step of the scan itself is ss_fwd (selscan_api.cu) on the device copies.
 //
-// Streams and events are created per call and released at its end (the driver defers their
-// destruction until the enqueued work completes), so concurrent calls share nothing but the
-// device.  Ordering: the work starts after everything already enqueued on the caller's stream,
+// The three streams and their events are created once per device (per CUDA context, on its
+// first call) and kept for the life of the process.  Calls on one device enqueue their work one
+// at a time (a mutex held while enqueueing, not while the GPU runs it), so a call's waits always
+// see its own event records; the GPU work of concurrent calls is then ordered on the shared
+// streams.  Ordering: the work starts after everything already enqueued on the caller's stream,
 // and the caller's stream waits for the last copy back, so synchronising it makes y and
 // last_state valid on the host.
 #include <cuda_runtime.h>
@@ -15,9 +17,11 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/selscan.h"
 #include "host_util.h"
+#include "internal.h"
 
 namespace selscan {
 namespace {
@@ -59,7 +63,7 @@ bool host_ptr(const void* q) {
     return a.type == cudaMemoryTypeHost || a.type == cudaMemoryTypeUnregistered;
 }
 
-// Streams and events of one call, released when it returns.
+// Streams and events of the copy / scan / copy-back pipeline of one device.
 struct Pipeline {
     cudaStream_t s_in = nullptr, s_c = nullptr, s_out = nullptr;
     cudaEvent_t start = nullptr, params = nullptr;
@@ -79,6 +83,15 @@ struct Pipeline {
         for (cudaStream_t s : {s_in, s_c, s_out}) if (s) cudaStreamDestroy(s);
     }
 };
+
+// One pipeline per device, made on the device's first call in a context and remade when the
+// context changes (the old handles belonged to a context that is gone and are not touched).
+struct PipelineSlot {
+    std::mutex mu;
+    CUcontext ctx = nullptr;
+    Pipeline* pl = nullptr;
+};
+PipelineSlot g_pipelines[64];
 
 }  // namespace
 }  // namespace selscan
@@ -156,8 +169,20 @@ extern "C" ss_status ss_fwd_host(const void* u, const void* delta_raw, const flo
         slot[i].last = reinterpret_cast<float*>(base + 4 * xs + 2 * bs);
     }
 
-    Pipeline pl;
-    if (!pl.ok) return SS_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return SS_ERR_UNSUPPORTED;
+    PipelineSlot& slot_of_dev = g_pipelines[dev];
+    std::lock_guard<std::mutex> lock(slot_of_dev.mu);
+    const CUcontext cur = current_context();
+    if (!slot_of_dev.pl || slot_of_dev.ctx != cur) {
+        Pipeline* fresh = new Pipeline();
+        if (!fresh->ok) {
+            delete fresh;
+            return SS_ERR_CUDA;
+        }
+        slot_of_dev.pl = fresh;
+        slot_of_dev.ctx = current_context();
+    }
+    Pipeline& pl = *slot_of_dev.pl;
     auto chk = [](cudaError_t e) { return e == cudaSuccess; };
     auto h2d_on = [&](cudaStream_t q, void* dst, const void* src, size_t n) {
         return chk(cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, q));

@@ -429,11 +429,17 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             const float* tB;
             const float* tC;
             if constexpr (Cfg::CONVERT_BC && !LTI) {
-                const TIO* rb = reinterpret_cast<const TIO*>(st + Cfg::OFF_B);
-                const TIO* rc = reinterpret_cast<const TIO*>(st + Cfg::OFF_C);
-                for (int i = tid; i < T * NS; i += Cfg::THREADS) {
-                    bcf[i] = to_f32<TIO>(rb[i]);
-                    if constexpr (!STATE_ONLY) bcf[T * NS + i] = to_f32<TIO>(rc[i]);
+                // widen four bf16 at a time (a bf16 is the high half of its fp32)
+                const uint2* rb = reinterpret_cast<const uint2*>(st + Cfg::OFF_B);
+                const uint2* rc = reinterpret_cast<const uint2*>(st + Cfg::OFF_C);
+                float4* wb = reinterpret_cast<float4*>(bcf);
+                auto widen = [](uint2 v) {
+                    return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                                       __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+                };
+                for (int i = tid; i < T * NS / 4; i += Cfg::THREADS) {
+                    wb[i] = widen(rb[i]);
+                    if constexpr (!STATE_ONLY) wb[T * NS / 4 + i] = widen(rc[i]);
                 }
                 __syncthreads();
                 tB = bcf;
@@ -450,11 +456,13 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             constexpr int G = GT <= 16 ? GT : GT % 16 == 0 ? 16 : GT % 12 == 0 ? 12 : 8;
             static_assert(GT % G == 0, "chunk must be whole sub-blocks");
             static_assert(G % NCX == 0, "sub-blocks start on a swizzle row class");
+            static_assert(G % 2 == 0, "phases 1 and 3 take the steps in pairs");
 #pragma unroll 1
             for (int g0 = 0; g0 < GT; g0 += G) {
                 // Phase 1: Δ and Δ·u of the steps this lane prepares (step g·LPC + j of each group;
                 // zero past L, i.e. identity pairs).  G independent softplus chains.
-                float dd[G], du[G];
+                // u of this lane's steps, read once here and kept for phase 3's D·u skip
+                float dd[G], du[G], uv[G];
                 if constexpr (Cfg::DTR > 0) {
                     // delta_raw = Σ_k W_dt[d,k] · dt_low[t,k] for this lane's G steps, four ranks at a
                     // time: the W row from the tile's shared copy, the dt_low rows broadcast from
@@ -476,17 +484,27 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                         }
                     }
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const float x = softplus((xr[g].x + xr[g].y) + bias_w);
-                        dd[g] = x;
-                        du[g] = x * at(tu, g0, g);
+                    for (int g = 0; g < G; g += 2) {
+                        const float2 x = add2(make_float2(xr[g].x + xr[g].y, xr[g + 1].x + xr[g + 1].y),
+                                              splat2(bias_w));
+                        const float2 dl = softplus2(x);
+                        uv[g] = at(tu, g0, g);
+                        uv[g + 1] = at(tu, g0, g + 1);
+                        const float2 uu = mul2(dl, make_float2(uv[g], uv[g + 1]));
+                        dd[g] = dl.x; dd[g + 1] = dl.y;
+                        du[g] = uu.x; du[g + 1] = uu.y;
                     }
                 } else {
+                    // two steps per pass: the polynomial and the products on packed pairs
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const float x = softplus(at(td, g0, g) + bias_w);
-                        dd[g] = x;
-                        du[g] = x * at(tu, g0, g);
+                    for (int g = 0; g < G; g += 2) {
+                        const float2 x = add2(make_float2(at(td, g0, g), at(td, g0, g + 1)), splat2(bias_w));
+                        const float2 dl = softplus2(x);
+                        uv[g] = at(tu, g0, g);
+                        uv[g + 1] = at(tu, g0, g + 1);
+                        const float2 uu = mul2(dl, make_float2(uv[g], uv[g + 1]));
+                        dd[g] = dl.x; dd[g + 1] = dl.y;
+                        du[g] = uu.x; du[g + 1] = uu.y;
                     }
                 }
                 if (!whole) {
@@ -512,11 +530,11 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                             const float dk = LPC == 1 ? dd[g] : __shfl_sync(0xffffffffu, dd[g], kk * CPW + c);
                             const float uk = LPC == 1 ? du[g] : __shfl_sync(0xffffffffu, du[g], kk * CPW + c);
                             const float2 dl2 = make_float2(dk, dk), du2 = make_float2(uk, uk);
-                            const int row = (g0 + g) * LPC + kk;
+                            const float* rowB = tB + ((g0 + g) * LPC + kk) * NS + n0;
 #pragma unroll
                             for (int qq = 0; qq < QPL; ++qq) {
                                 const float4 B4 = LTI ? bL[qq]
-                                                      : *reinterpret_cast<const float4*>(tB + row * NS + n0 + 4 * qq);
+                                                      : *reinterpret_cast<const float4*>(rowB + 4 * qq);
                                 a[kk][qq][0] = ex2x2(mul2(dl2, A2[qq][0]));
                                 a[kk][qq][1] = ex2x2(mul2(dl2, A2[qq][1]));
                                 bb[kk][qq][0] = mul2(du2, make_float2(B4.x, B4.y));
@@ -539,7 +557,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                         float yp[LPC];
 #pragma unroll
                         for (int kk = 0; kk < LPC; ++kk) {
-                            const int row = (g0 + g) * LPC + kk;
+                            const float* rowC = tC + ((g0 + g) * LPC + kk) * NS + n0;
                             float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                             for (int qq = 0; qq < QPL; ++qq) {
@@ -547,7 +565,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                                 if constexpr (LTI)
                                     C4 = cL[qq];
                                 else if constexpr (!STATE_ONLY)
-                                    C4 = *reinterpret_cast<const float4*>(tC + row * NS + n0 + 4 * qq);
+                                    C4 = *reinterpret_cast<const float4*>(rowC + 4 * qq);
                                 h[qq][0] = fma2(ac[kk][qq][0], h[qq][0], bc[kk][qq][0]);
                                 h[qq][1] = fma2(ac[kk][qq][1], h[qq][1], bc[kk][qq][1]);
                                 if constexpr (!STATE_ONLY) {
@@ -570,7 +588,8 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                             // butterfly reduce-scatter over the four slices (lanes c + CPW·s): first
                             // across slice bit 1 (each side keeps two steps), then across bit 0.  Only
                             // shuffles, no shared-memory round trip or warp barrier, so the next
-                            // group's loads are free to start early.
+                            // group's loads are free to start early.  (The fold itself must visit the
+                            // steps in time order, so the slots cannot be renumbered per lane.)
                             const bool b1 = (j & 2) != 0, b0 = (j & 1) != 0;
                             const float s0 = b1 ? yp[0] : yp[2], s1 = b1 ? yp[1] : yp[3];
                             const float k0 = b1 ? yp[2] : yp[0], k1 = b1 ? yp[3] : yp[1];
@@ -588,15 +607,18 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                     const int nst = whole ? G : (rem <= 0 ? 0 : rem >= int64_t(G) * LPC ? G : static_cast<int>((rem + LPC - 1) / LPC));
                     if (has_z && nst == G) {
 #pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            const float v = fmaf(D_w, at(tu, g0, g), yv[g]) * silu(at(tz, g0, g));
-                            *reinterpret_cast<TIO*>(yrow + g * LPC * ystride) = from_f32<TIO>(v);
+                        for (int g = 0; g < G; g += 2) {
+                            const float2 v = mul2(fma2(splat2(D_w), make_float2(uv[g], uv[g + 1]),
+                                                       make_float2(yv[g], yv[g + 1])),
+                                                  silu2(make_float2(at(tz, g0, g), at(tz, g0, g + 1))));
+                            *reinterpret_cast<TIO*>(yrow + g * LPC * ystride) = from_f32<TIO>(v.x);
+                            *reinterpret_cast<TIO*>(yrow + (g + 1) * LPC * ystride) = from_f32<TIO>(v.y);
                         }
                     } else {
 #pragma unroll
                         for (int g = 0; g < G; ++g) {
                             if (g < nst) {
-                                float v = fmaf(D_w, at(tu, g0, g), yv[g]);
+                                float v = fmaf(D_w, uv[g], yv[g]);
                                 if (has_z) v *= silu(at(tz, g0, g));
                                 *reinterpret_cast<TIO*>(yrow + g * LPC * ystride) = from_f32<TIO>(v);
                             }
@@ -626,7 +648,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
         if constexpr (STATE_ONLY) {
             const int sg = c0 / p.seg_chunks;
             if (d_ok) {
-                float* dst = p.seg_slots + ((static_cast<int64_t>(sg + 1) * p.batch + b) * p.Dm + d) * p.N;
+                float* dst = p.seg_slots + ((static_cast<int64_t>(sg + p.seg_out0) * p.batch + b) * p.Dm + d) * p.N;
 #pragma unroll
                 for (int qq = 0; qq < QPL; ++qq) {
                     const float v[4] = {h[qq][0].x, h[qq][0].y, h[qq][1].x, h[qq][1].y};

@@ -49,12 +49,12 @@ __device__ __forceinline__ float step_quad(float4& hv, const float4& av, const f
     return fmaf(Cv.x, h0, fmaf(Cv.y, h1, fmaf(Cv.z, h2, Cv.w * h3)));
 }
 
+// The work of block `block` of one layer's step (blocks_per_b row blocks per batch row).
 template <typename TIO, int LPR, int RPT, bool VEC>
-__global__ void __launch_bounds__(kStepThreads) ss_step_kernel(const StepParams p) {
+__device__ __forceinline__ void step_block(const StepParams& p, int block, int blocks_per_b) {
     constexpr int ROWS_PASS = kStepThreads / LPR;    // rows one pass of the block covers
-    const int blocks_per_b = static_cast<int>((static_cast<int64_t>(p.Dm) + ROWS_PASS * RPT - 1) / (ROWS_PASS * RPT));
-    const int b = static_cast<int>(blockIdx.x) / blocks_per_b;
-    const int blk = static_cast<int>(blockIdx.x) - b * blocks_per_b;
+    const int b = block / blocks_per_b;
+    const int blk = block - b * blocks_per_b;
     const int qd = threadIdx.x % LPR;
     const int d0 = blk * (ROWS_PASS * RPT) + threadIdx.x / LPR;
     const TIO* x = static_cast<const TIO*>(p.x) + static_cast<int64_t>(b) * p.x_b;
@@ -145,6 +145,56 @@ __global__ void __launch_bounds__(kStepThreads) ss_step_kernel(const StepParams 
     }
 }
 
+template <int LPR, int RPT>
+__device__ __forceinline__ int step_blocks_per_b(int Dm) {
+    constexpr int rows_block = (kStepThreads / LPR) * RPT;
+    return static_cast<int>((static_cast<int64_t>(Dm) + rows_block - 1) / rows_block);
+}
+
+template <typename TIO, int LPR, int RPT, bool VEC>
+__global__ void __launch_bounds__(kStepThreads) ss_step_kernel(const StepParams p) {
+    step_block<TIO, LPR, RPT, VEC>(p, static_cast<int>(blockIdx.x), step_blocks_per_b<LPR, RPT>(p.Dm));
+}
+
+// Many layers' steps in one launch: block x works on layer x / blocks_per_layer.  The layers
+// share sizes and strides; their pointers come from the parameter block.
+template <typename TIO, int LPR, int RPT, bool VEC>
+__global__ void __launch_bounds__(kStepThreads) ss_step_layers_kernel(const __grid_constant__ StepLayersParams q) {
+    const int per_b = step_blocks_per_b<LPR, RPT>(q.common.Dm);
+    const int per_layer = per_b * q.common.batch;
+    const int layer = static_cast<int>(blockIdx.x) / per_layer;
+    if (layer >= q.n_layers) return;
+    StepParams p = q.common;
+    const StepLayerPtrs& L = q.layer[layer];
+    p.state = L.state; p.x = L.x; p.delta = L.delta; p.z = L.z; p.Bm = L.Bm; p.Cm = L.Cm;
+    p.bias = L.bias; p.A_log = L.A_log; p.Dv = L.Dv; p.y = L.y;
+    step_block<TIO, LPR, RPT, VEC>(p, static_cast<int>(blockIdx.x) - layer * per_layer, per_b);
+}
+
+template <typename TIO, int LPR>
+static cudaError_t launch_step_layers_t(const StepLayersParams& q, bool vec, cudaStream_t stream) {
+    constexpr int RPT = 2;
+    constexpr int rows_block = (kStepThreads / LPR) * RPT;
+    const int64_t blocks = (static_cast<int64_t>(q.common.Dm) + rows_block - 1) / rows_block * q.common.batch *
+                           q.n_layers;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
+    const dim3 grid(static_cast<unsigned>(blocks));
+    if (vec)
+        ss_step_layers_kernel<TIO, LPR, RPT, true><<<grid, kStepThreads, 0, stream>>>(q);
+    else
+        ss_step_layers_kernel<TIO, LPR, RPT, false><<<grid, kStepThreads, 0, stream>>>(q);
+    return cudaGetLastError();
+}
+
+template <typename TIO>
+static cudaError_t launch_step_layers_dtype(const StepLayersParams& q, bool vec, cudaStream_t stream) {
+    const int quads = (q.common.N + 3) / 4;
+    if (quads <= 1) return launch_step_layers_t<TIO, 1>(q, vec, stream);
+    if (quads <= 2) return launch_step_layers_t<TIO, 2>(q, vec, stream);
+    return launch_step_layers_t<TIO, 4>(q, vec, stream);
+}
+
 template <typename TIO, int LPR>
 static cudaError_t launch_step_t(const StepParams& p, bool vec, cudaStream_t stream) {
     constexpr int RPT = 2;
@@ -171,6 +221,11 @@ static cudaError_t launch_step_dtype(const StepParams& p, bool vec, cudaStream_t
 cudaError_t launch_step(const StepParams& p, bool bf16, bool vec, cudaStream_t stream) {
     return bf16 ? launch_step_dtype<__nv_bfloat16>(p, vec, stream)
                 : launch_step_dtype<float>(p, vec, stream);
+}
+
+cudaError_t launch_step_layers(const StepLayersParams& q, bool bf16, bool vec, cudaStream_t stream) {
+    return bf16 ? launch_step_layers_dtype<__nv_bfloat16>(q, vec, stream)
+                : launch_step_layers_dtype<float>(q, vec, stream);
 }
 
 }  // namespace selscan

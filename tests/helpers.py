@@ -29,9 +29,26 @@ def max_rel(got, ref, mag):
     return float(r.max()) if r.size else 0.0
 
 
+def plain_max_rel(got, ref):
+    """max_i |e_i| / max_i |y_ref,i|: the largest error against the output's scale (recorded
+    beside the condition-aware max_rel, which divides each error by its own term sizes)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    scale = float(np.abs(ref).max()) if ref.size else 0.0
+    err = float(np.abs(got - ref).max()) if ref.size else 0.0
+    return err / scale if scale > 0 else err
+
+
+# Every assert_fwd_close call appends (what, io, rel-L2, max-rel, plain max-rel) here; conftest
+# prints the worst of each at the end of the session.
+RECORDED = []
+
+
 def assert_fwd_close(io, y, ref_y, mag, last=None, ref_last=None, what=""):
     assert np.all(np.isfinite(y)), f"{what}: non-finite output"
     e2 = rel_l2(y, ref_y)
+    RECORDED.append((what, io, e2, max_rel(y, ref_y, mag) if io == "f32" else float("nan"),
+                     plain_max_rel(y, ref_y)))
     if io == "bf16":
         assert e2 <= BF16_REL_L2, f"{what}: y rel-L2 {e2:.3e} > {BF16_REL_L2}"
     else:

@@ -127,3 +127,56 @@ def test_prefill_then_decode_equals_forward():
                                                             "B", "C", "D", "z")))
     assert_fwd_close("f32", to_host(torch.stack(ys, 1)), ry[:, k:], mag[:, k:], to_host(state), rlast,
                      what="prefill+decode")
+
+
+def _layer_tensors(w, state_dev=None):
+    a = w.arrays
+    io = w.io
+    return {"state": f32dev(a["state"]) if state_dev is None else state_dev, "x": to_dev(a["x"], io),
+            "delta_raw": to_dev(a["delta_raw"], io), "delta_bias": f32dev(a["delta_bias"]),
+            "A_log": f32dev(a["A_log"]), "B": to_dev(a["B"], io), "C": to_dev(a["C"], io), "D": f32dev(a["D"]),
+            "z": to_dev(a["z"], io)}
+
+
+def test_step_layers_decode_workload_48_layers():
+    """All 48 layers of the decode workload in one ss_step_layers launch: every layer's y and
+    updated state against the oracle, and bit for bit against 48 ss_step calls."""
+    ws = [synth.step_inputs(64, 4096, 16, seed=4, layer=layer) for layer in range(48)]
+    batched = [_layer_tensors(w) for w in ws]
+    ys = ss.ss_step_layers(batched)
+    torch.cuda.synchronize()
+    for w, L, y in zip(ws, batched, ys):
+        ry, rst, mag = oracle_step(w)
+        assert_fwd_close("f32", to_host(y), ry, mag, to_host(L["state"]), rst, what=f"layers {w.name}")
+        y1, st1 = gpu_step(w)
+        np.testing.assert_array_equal(to_host(y), y1)
+        np.testing.assert_array_equal(to_host(L["state"]), to_host(st1))
+
+
+@pytest.mark.parametrize("N", [4, 5, 16])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_step_layers_shapes(N, io):
+    """A few layers of ragged sizes (the vector path at N = 4, 16; the scalar one at N = 5)."""
+    ws = [synth.step_inputs(3, 77, N, io=io, seed=60 + N + k, with_bias=True) for k in range(5)]
+    batched = [_layer_tensors(w) for w in ws]
+    ys = ss.ss_step_layers(batched)
+    torch.cuda.synchronize()
+    for w, L, y in zip(ws, batched, ys):
+        ry, rst, mag = oracle_step(w)
+        assert_fwd_close(io, to_host(y), ry, mag, to_host(L["state"]), rst, what=f"layers N={N} {io}")
+
+
+def test_step_layers_rejects_shared_outputs_and_too_many_layers():
+    w = synth.step_inputs(2, 32, 16, seed=70)
+    a, b = _layer_tensors(w), _layer_tensors(w)
+    b["state"] = a["state"]                     # two layers writing one state
+    with pytest.raises(ss.SelscanError):
+        ss.ss_step_layers([a, b])
+    c = _layer_tensors(w)
+    c["x"] = a["state"].view(-1)[: 2 * 32].view(2, 32)   # a layer reading another's state
+    with pytest.raises(ss.SelscanError):
+        ss.ss_step_layers([a, c])
+    many = [_layer_tensors(w) for _ in range(129)]
+    with pytest.raises(ss.SelscanError):
+        ss.ss_step_layers(many)
+    assert ss.ss_step_layers([]) == []

@@ -2,8 +2,8 @@
 
 Some callers cannot call cudaMalloc, or must not: a host whose allocator owns all device
 memory, a runtime that forbids allocation once started, or a plugin interface with no
-allocation hook.  For them ss_fwd_static runs the balanced schedule of ss_fwd_ws on a fixed
-workspace built into the library's device code, and allocates nothing.
+allocation hook.  For them ss_fwd_static runs ss_fwd_ws's schedule (balanced, or the time split)
+on a fixed workspace built into the library's device code, and allocates nothing.
 
 This file is collected last so that a run that stops at the first failure has already run
 every other test; it passes both on its own in a fresh process and after the others.
@@ -13,10 +13,11 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 import selective_state_space_scan_gb300 as ss
 from selective_state_space_scan_gb300 import synth
 
-from helpers import BF16_REL_L2, FP32_REL_L2, rel_l2, to_dev, f32dev, to_host
+from helpers import BF16_REL_L2, FP32_REL_L2, assert_fwd_close, rel_l2, to_dev, f32dev, to_host
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -40,47 +41,96 @@ def _static_fn():
     return f
 
 
-def _call(w, use_static):
-    """One forward pass through the C ABI: ss_fwd_static or the existing ss_fwd."""
+def _plan(w, with_ws=True):
+    """Name of the schedule the library picks for w's sizes (a workspace-taking call)."""
+    f = ss.lib().ss__fwd_plan
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int32, ctypes.c_int, ctypes.c_char_p, ctypes.c_int]
+    buf = ctypes.create_string_buffer(128)
+    f(w.batch, w.L, w.Dm, w.N, ss.SS_BF16 if w.io == "bf16" else ss.SS_F32, 1 if with_ws else 0, buf, 128)
+    return buf.value.decode()
+
+
+def _call(w, kind, ws_bytes=None):
+    """One forward pass through the C ABI: kind "static" (ss_fwd_static), "ws" (ss_fwd_ws with a
+    caller-allocated workspace of ws_bytes, default the size query's) or "plain" (ss_fwd)."""
     a = w.arrays
     t = dict(u=to_dev(a["u"], w.io), delta_raw=to_dev(a["delta_raw"], w.io), z=to_dev(a["z"], w.io),
              B=to_dev(a["B"], w.io), C=to_dev(a["C"], w.io), A_log=f32dev(a["A_log"]), D=f32dev(a["D"]),
              bias=f32dev(a["delta_bias"]))
-    y = torch.empty_like(t["u"])
-    last = torch.empty((w.batch, w.Dm, w.N), device="cuda")
+    y = torch.full_like(t["u"], float("nan"))
+    last = torch.full((w.batch, w.Dm, w.N), float("nan"), device="cuda")
     u, dr, z, B, C = t["u"], t["delta_raw"], t["z"], t["B"], t["C"]
     s = ss.FwdStrides(ss.SS_BF16 if w.io == "bf16" else ss.SS_F32, u.stride(0), u.stride(1),
                       dr.stride(0), dr.stride(1), z.stride(0), z.stride(1), y.stride(0), y.stride(1),
                       B.stride(0), B.stride(1), C.stride(0), C.stride(1))
     args = (u.data_ptr(), dr.data_ptr(), t["bias"].data_ptr(), t["A_log"].data_ptr(), B.data_ptr(),
             C.data_ptr(), t["D"].data_ptr(), z.data_ptr(), y.data_ptr(), last.data_ptr(),
-            w.batch, w.L, w.Dm, w.N, ctypes.byref(s), torch.cuda.current_stream().cuda_stream)
-    st = _static_fn()(*args) if use_static else ss.lib().ss_fwd(*args)
+            w.batch, w.L, w.Dm, w.N, ctypes.byref(s))
+    stream = torch.cuda.current_stream().cuda_stream
+    if kind == "static":
+        st = _static_fn()(*args, stream)
+    elif kind == "ws":
+        io = ss.SS_BF16 if w.io == "bf16" else ss.SS_F32
+        n = ws_bytes if ws_bytes is not None else ss.lib().ss_fwd_workspace_size(w.batch, w.L, w.Dm, w.N, io)
+        ws = torch.zeros(max(int(n), 256), dtype=torch.uint8, device="cuda")
+        st = ss.lib().ss_fwd_ws(*args, ws.data_ptr(), int(n), stream)
+    else:
+        st = ss.lib().ss_fwd(*args, stream)
     torch.cuda.synchronize()
     assert st == 0, ss.status_string(st)
     return to_host(y), to_host(last)
 
 
-@pytest.mark.parametrize("name", ["mamba130m", "split", "bf16"])
-def test_static_workspace_matches_ss_fwd_twice(name):
-    """Two calls in a row (the second reuses the array the first left behind) agree with
-    ss_fwd within the parity tolerance."""
-    if name == "split":
-        w = synth.fwd_inputs(6, 1000, 4096, 16, seed=31)       # ranges split tiles between CTAs
-    elif name == "bf16":
-        w = synth.fwd_inputs(8, 700, 1536, 16, io="bf16", seed=32)
-    else:
-        w = synth.config(name)
+def _oracle_rows(w, rows):
+    a = w.arrays
+    y, last, mag = oracle.ss_fwd(a["u"], a["delta_raw"], a["delta_bias"], a["A_log"], a["B"], a["C"], a["D"],
+                                 a["z"], rows=rows)
+    return y, last, mag
+
+
+CASES = {
+    # the 130m-shaped layer: balanced schedule, fp32
+    "mamba130m": lambda: synth.config("mamba130m"),
+    # ranges that split channel tiles between CTAs (hand-overs through the array)
+    "split": lambda: synth.fwd_inputs(6, 1000, 4096, 16, seed=31),
+    # bf16 I/O, balanced schedule
+    "bf16": lambda: synth.fwd_inputs(8, 700, 1536, 16, io="bf16", seed=32),
+    # one long row: the time split, its segment slots and Σ Δ in the array
+    "timesplit": lambda: synth.fwd_inputs(1, 8192, 1536, 16, seed=33),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_static_workspace_matches_ss_fwd_ws_twice(name):
+    """Two calls in a row (the second runs on what the first left in the array) give exactly
+    ss_fwd_ws's result on the same sizes (the same schedule), agree with the fp64 oracle on
+    sampled rows within the parity tolerance, and with ss_fwd within it too."""
+    w = CASES[name]()
     io = ss.SS_BF16 if w.io == "bf16" else ss.SS_F32
     need = ss.lib().ss_fwd_workspace_size(w.batch, w.L, w.Dm, w.N, io)
-    assert 0 < need <= SS_STATIC_WORKSPACE_BYTES                # the static path is really used
-    y_ref, last_ref = _call(w, use_static=False)
+    plan = _plan(w)
+    if name == "timesplit":
+        assert "time-split" in plan, plan
+        assert need > 0                                         # the static path holds its segments
+    else:
+        assert "balanced" in plan, plan
+        assert 0 < need <= SS_STATIC_WORKSPACE_BYTES            # the static path is really used
+    y_ws, last_ws = _call(w, "ws", ws_bytes=min(need, SS_STATIC_WORKSPACE_BYTES))
+    y_plain, last_plain = _call(w, "plain")
+    rng = np.random.default_rng(7)
+    rows = np.sort(rng.choice(w.batch * w.Dm, size=min(24, w.batch * w.Dm), replace=False))
+    y_or, last_or, mag = _oracle_rows(w, rows)
     tol = BF16_REL_L2 if w.io == "bf16" else FP32_REL_L2
     for _ in range(2):
-        y, last = _call(w, use_static=True)
+        y, last = _call(w, "static")
         assert np.all(np.isfinite(y))
-        assert rel_l2(y, y_ref) <= tol
-        assert rel_l2(last, last_ref) <= FP32_REL_L2
+        np.testing.assert_array_equal(y, y_ws)                  # the same schedule, bit for bit
+        np.testing.assert_array_equal(last, last_ws)
+        assert rel_l2(y, y_plain) <= tol
+        assert rel_l2(last, last_plain) <= FP32_REL_L2
+        b, d = rows // w.Dm, rows % w.Dm
+        assert_fwd_close(w.io, y[b, :, d], y_or, mag, last[b, d, :], last_or, what=f"static {name}")
 
 
 def test_static_workspace_rejects_sizes_beyond_its_maximum():
