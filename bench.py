@@ -5,7 +5,8 @@
 One step = one pass of the whole hot path over one batch of synthetic input:
   forward workloads: one ss_fwd over the whole [batch, L, Dm] problem (softplus, the scan,
                      D skip, z gate and last_state, all in one kernel launch);
-  decode workload:   ss_step for each of 48 layers' distinct states, replayed as one CUDA graph.
+  decode workload:   the decode update of 48 layers' distinct states: one ss_step_layers launch
+                     (or, with --decode-per-layer, 48 ss_step launches), replayed as a CUDA graph.
 Prints one JSON line.  Inputs live in HBM before the timed region; every workload's working
 set is larger than the 129 MB L2, so no flush is needed between steps.  Under torchrun each
 rank runs its own copy of the workload (independent problems, no collective): weak scaling.
@@ -56,6 +57,9 @@ def parse():
     ap.add_argument("--workspace", action="store_true", default=True,
                     help="(default) call the forward pass with the binding's cached workspace (ss_fwd_ws: the "
                          "balanced or the time-split schedule)")
+    ap.add_argument("--decode-per-layer", action="store_true",
+                    help="decode workload: time 48 ss_step launches (one per layer) instead of one "
+                         "ss_step_layers launch over all 48")
     ap.add_argument("--no-workspace", dest="workspace", action="store_false",
                     help="call the plain ss_fwd instead (one CTA per channel tile, no workspace)")
     return ap.parse_args()
@@ -161,9 +165,11 @@ def decay_ex2_per_step(w) -> int:
 _COMMON_SOURCES = ("device_common.cuh", "fwd_params.h", "internal.h", "fwd_configs.h", "selscan_api.cu")
 KERNEL_SOURCES = {
     "ss_fwd_lane_kernel": _COMMON_SOURCES + ("ss_fwd_lane.cuh", "fwd_lane_impl.cuh", "fwd_launch_common.cuh",
-                                             "fwd_lane_f32.cu", "fwd_lane_bf16.cu", "ss_fwd_carry.cu", "fwd_lane_dtp.cu"),
+                                             "fwd_lane_f32.cu", "fwd_lane_bf16.cu", "fwd_lane_bf16w.cu",
+                                             "ss_fwd_widen.cu", "ss_fwd_carry.cu", "fwd_lane_dtp.cu"),
     "ss_fwd_seg_kernel": _COMMON_SOURCES + ("ss_fwd_seg.cuh", "fwd_seg.cu", "fwd_launch_common.cuh"),
     "ss_step_kernel": _COMMON_SOURCES + ("ss_step.cu",),
+    "ss_step_layers_kernel": _COMMON_SOURCES + ("ss_step.cu",),
     "ss_conv1d_kernel": ("device_common.cuh", "host_util.h", "ss_conv1d.cu"),
     "ss_bwd_kernel": ("device_common.cuh", "host_util.h", "ss_bwd.cu"),
 }
@@ -318,7 +324,7 @@ def make_fwd_call(w, torch, ss, dev, workspace=False):
     return step, t, y, last
 
 
-def make_decode_call(w0, torch, ss, dev):
+def make_decode_call(w0, torch, ss, dev, per_layer=False):
     from selective_state_space_scan_gb300 import synth
     layers = []
     for layer in range(DECODE_LAYERS):
@@ -328,9 +334,12 @@ def make_decode_call(w0, torch, ss, dev):
     ys = [torch.empty((w0.batch, w0.Dm), device=dev) for _ in layers]
 
     def eager():
-        for L, y in zip(layers, ys):
-            ss.ss_step(L["state"], L["x"], L["delta_raw"], L["delta_bias"], L["A_log"], L["B"], L["C"],
-                       L["D"], L["z"], y=y)
+        if per_layer:
+            for L, y in zip(layers, ys):
+                ss.ss_step(L["state"], L["x"], L["delta_raw"], L["delta_bias"], L["A_log"], L["B"], L["C"],
+                           L["D"], L["z"], y=y)
+        else:
+            ss.ss_step_layers([dict(L, y=y) for L, y in zip(layers, ys)])
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -360,7 +369,7 @@ def run_ours(args, w, rank, world, local_rank):
             raise ValueError(f"bad --variant {args.variant}")
     decode = w.name.startswith("decode")
     if decode:
-        step, tensors, outs = make_decode_call(w, torch, ss, dev)
+        step, tensors, outs = make_decode_call(w, torch, ss, dev, per_layer=args.decode_per_layer)
     else:
         step, tensors, y, last = make_fwd_call(w, torch, ss, dev, workspace=args.workspace)
     dist = None
@@ -393,7 +402,8 @@ def run_ours(args, w, rank, world, local_rank):
     if err:
         raise RuntimeError(f"device error word {err:#x} after the timed region")
     if decode:
-        kernel, launches = "ss_step_kernel", DECODE_LAYERS
+        kernel, launches = (("ss_step_kernel", DECODE_LAYERS) if args.decode_per_layer
+                            else ("ss_step_layers_kernel", 1))
     else:
         plan = ss.lib().ss__fwd_plan
         plan.restype = ctypes.c_int
@@ -476,15 +486,18 @@ def oracle_sample_baseline(fn, units_per_pass, unit, sample, min_seconds=10.0, m
             "sample": f"{passes} pass(es) of {sample}, {elapsed:.1f} s of fp64 oracle time"}
 
 
-def workload_config(w, extra=None, variant=None):
+def workload_config(w, extra=None, variant=None, decode_per_layer=False, call=None):
     c = {"workload": f"{w.name}: batch={w.batch} L={w.L} Dm={w.Dm} N={w.N} io={w.io}",
          "batch": w.batch, "L": w.L, "Dm": w.Dm, "N": w.N, "io": w.io, "seed": w.seed,
          "l2": "no flush: working set {:.0f} MB > 129 MB L2".format(alg_bytes(w) / 1e6)}
     if w.name.startswith("decode"):
         c["layers"] = DECODE_LAYERS
-        c["graph"] = "48 ss_step launches captured in one CUDA graph per step"
+        c["graph"] = ("48 ss_step launches" if decode_per_layer else "one ss_step_layers launch over "
+                      "the 48 layers") + " captured in one CUDA graph per step"
     if variant:
         c["kernel_variant"] = variant
+    if call:
+        c["call"] = call
     if extra:
         c.update(extra)
     return c
@@ -786,16 +799,17 @@ def main():
     ms_step = res["total_ms"] / args.steps
     value = job_throughput(units, world, res["total_ms"], args.steps)
     launch_ms = statistics.mean(res["per_launch_ms"])
-    if w.name.startswith("decode"):
-        launch_ms = launch_ms / DECODE_LAYERS    # per ss_step kernel
-        bytes_launch = alg_bytes(w) / DECODE_LAYERS
-    else:
-        bytes_launch = alg_bytes(w)
+    # decode: the step is per_step_launches equal launches (one per layer, or one for all layers);
+    # forward: the step's launches run the scan once (time split: three passes; bf16 with a
+    # workspace: the B/C widening first), so the whole step is timed as the scan's launch
+    per_step_launches = res["launches"] if w.name.startswith("decode") else 1
+    launch_ms = launch_ms / per_step_launches
+    bytes_launch = alg_bytes(w) / per_step_launches if w.name.startswith("decode") else alg_bytes(w)
     hbm_peak, peak_kind = peaks()
     # Roofline of the dominant kernel: the slower of moving the algorithmic bytes at the
     # measured HBM copy bandwidth and issuing one exp2 per state update at the SFU rate.
     sfu_peak = res["peaks"].ex2_per_s(res["clocks"])     # ex2 / s
-    ex2_launch = decay_ex2_per_step(w) / (DECODE_LAYERS if w.name.startswith("decode") else 1)
+    ex2_launch = decay_ex2_per_step(w) / (per_step_launches if w.name.startswith("decode") else 1)
     t_hbm = bytes_launch / (hbm_peak * 1e9)
     t_sfu = ex2_launch / sfu_peak
     if t_hbm >= t_sfu:
@@ -807,6 +821,9 @@ def main():
         roof = {"bound": "alu", "achieved": achieved, "peak": sfu_peak / 1e12, "unit": "Tex2/s",
                 "frac": achieved * 1e12 / sfu_peak,
                 "peak_source": res["peaks"].source(res["clocks"])}
+    if not w.name.startswith("decode") and res["launches"] > 1:
+        roof["launch_ms_is"] = ("per step: " + str(res["launches"]) + " launches (the time split's passes and/or "
+                                "the widening of bf16 B and C to fp32, about 1 us, before the scan)")
     roof.update({"traffic": measured_traffic(w.name, res["kernel"]), "kernel": res["kernel"],
                  "launch_ms": launch_ms, "alg_bytes_per_launch": bytes_launch,
                  "decay_ex2_per_launch": ex2_launch, "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6})
@@ -814,7 +831,11 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": w.io, "data": "synthetic",
-        "config": workload_config(w, variant=args.variant), "hbm_gbs": alg_bytes(w) / (ms_step / 1e3) / 1e9,
+        "config": workload_config(
+            w, variant=args.variant, decode_per_layer=args.decode_per_layer,
+            call=None if w.name.startswith("decode") else
+            ("ss_fwd with the binding's cached workspace (C ABI ss_fwd_ws)" if args.workspace else "ss_fwd (C ABI)")),
+        "hbm_gbs": alg_bytes(w) / (ms_step / 1e3) / 1e9,
         "gpu_launches": args.steps * res["launches"],
         "clocks": res["clocks"], "roofline": roof,
     }

@@ -83,6 +83,26 @@ __device__ __forceinline__ float2 softplus2(float2 x) {
     return fma2(m, p, make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)));
 }
 
+// log2(x) on the SFU (lg2.approx.ftz).
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+constexpr float kLn2 = 0.6931471805599453f;
+
+// softplus of two values for bf16 outputs: log(1 + e^x) = max(x, 0) + ln 2 · log2(1 + e^{-|x|})
+// with the SFU's log2, 5 instructions a value against softplus2's 8.  Its relative error is
+// about 2e-5 at x ~ -5 (the rounding of 1 + e^{-|x|} and lg2.approx's absolute error, over a
+// result of ~e^x), two orders below bf16's own 2^-9 rounding of the output.
+__device__ __forceinline__ float2 softplus2_lg2(float2 x) {
+    const float2 e = make_float2(ex2(-fabsf(x.x) * kLog2e), ex2(-fabsf(x.y) * kLog2e));
+    const float2 s = add2(splat2(1.f), e);
+    return fma2(make_float2(lg2_approx(s.x), lg2_approx(s.y)), splat2(kLn2),
+                make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)));
+}
+
 // silu of two independent values, as silu() with packed products.
 __device__ __forceinline__ float2 silu2(float2 z) {
     const float2 e = ex2x2(mul2(z, splat2(-kLog2e)));

@@ -13,6 +13,15 @@ namespace selscan {
 #define SS_LANE_STAGES 2
 #endif
 constexpr int kLaneT = SS_LANE_T;
+// Lane kernel options (compile-time, for measurement): the (Δ, Δ·u) hand-over at 2 lanes per
+// channel through shared memory instead of shuffles (fp32); softplus through the SFU's log2 for
+// bf16 (742 -> 723 us on the 2.8b-shaped layer).
+#ifndef SS_DX_SMEM
+#define SS_DX_SMEM 1
+#endif
+#ifndef SS_BF16_LG2_SOFTPLUS
+#define SS_BF16_LG2_SOFTPLUS 1
+#endif
 constexpr int kLaneStages = SS_LANE_STAGES;
 #ifndef SS_LANE_MINB4
 #define SS_LANE_MINB4 3

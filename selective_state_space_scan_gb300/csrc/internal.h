@@ -25,6 +25,7 @@ struct FwdVariant {
     bool dtp;        // lane family, TMA, per tile: the low-rank time-step projection folded in
     int es = 4;      // bytes per I/O element (4 fp32, 2 bf16)
     int chunk = 0;   // test override of the steps per chunk (16, 32 or 256; 0: the kernels' own)
+    bool bcf32 = false;  // bf16 streams with B and C staged as fp32 (a widened copy in the workspace)
 };
 
 struct FwdGeom {
@@ -45,6 +46,13 @@ cudaError_t launch_fwd_lane_f32(const FwdVariant& v, const FwdParams& p, const F
                                 cudaStream_t stream, int* max_grid = nullptr);
 cudaError_t launch_fwd_lane_bf16(const FwdVariant& v, const FwdParams& p, const FwdMaps& m,
                                  cudaStream_t stream, int* max_grid = nullptr);
+// The bf16 lane kernels with widened (fp32) B/C tiles, 16 states (v.bcf32).
+cudaError_t launch_fwd_lane_bf16w(const FwdVariant& v, const FwdParams& p, const FwdMaps& m,
+                                  cudaStream_t stream, int* max_grid = nullptr);
+// bf16 B and C [batch, L, N] (strides in elements) widened to fp32 [batch, L, N] contiguous; N a
+// multiple of 4, rows 8-byte aligned.
+cudaError_t launch_widen_bc(const void* B, const void* C, int64_t B_b, int64_t B_l, int64_t C_b, int64_t C_l,
+                            float* Bf, float* Cf, int64_t batch, int64_t L, int N, cudaStream_t stream);
 cudaError_t launch_fwd_seg(const FwdVariant& v, bool bf16, const FwdParams& p, const FwdMaps& m,
                            cudaStream_t stream);
 cudaError_t launch_step(const StepParams& p, bool bf16, bool vec, cudaStream_t stream);

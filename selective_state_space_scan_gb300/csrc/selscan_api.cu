@@ -346,9 +346,20 @@ cudaError_t lane_max_grid(const FwdVariant& v, bool bf16, int* out) {
     std::memset(&dummy, 0, sizeof(dummy));
     FwdMaps maps;
     std::memset(&maps, 0, sizeof(maps));
-    return bf16 ? launch_fwd_lane_bf16(v, dummy, maps, nullptr, out)
-                : launch_fwd_lane_f32(v, dummy, maps, nullptr, out);
+    return v.bcf32 ? launch_fwd_lane_bf16w(v, dummy, maps, nullptr, out)
+         : bf16     ? launch_fwd_lane_bf16(v, dummy, maps, nullptr, out)
+                    : launch_fwd_lane_f32(v, dummy, maps, nullptr, out);
 }
+
+size_t fwd_ws_need(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dtype, bool* split,
+                   bool with_widen = true);
+
+// Bytes of one widened (fp32) copy of bf16 B or C, and whether the workspace schedules widen them
+// (bf16 I/O with 16 states).
+size_t widen_copy_bytes(int64_t batch, int64_t L, int64_t N) {
+    return align_up(sizeof(float) * static_cast<size_t>(batch) * static_cast<size_t>(L) * static_cast<size_t>(N), 256);
+}
+bool widens_bc(int32_t io_dtype, int64_t N) { return io_dtype == SS_BF16 && N == 16; }
 
 ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
                    const void* B, const void* C, const float* D, const void* z, void* y,
@@ -481,6 +492,23 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     if (ft == 0) tma = false;
     v.lti = lti && tma;
 
+    // bf16 B and C are widened once into the front of the workspace when it holds the full size
+    // the size query asks for; the workspace schedules then stage fp32 B/C tiles and need no
+    // per-chunk widening (nor its block barriers) inside the scan.
+    float* Bw = nullptr;
+    float* Cw = nullptr;
+    if (widens_bc(s.io_dtype, N) && tma && !lti && !dtp && fc == 0 && workspace) {
+        bool need_split = false;
+        const size_t one = widen_copy_bytes(batch, L, N);
+        const size_t need = fwd_ws_need(batch, L, Dm, N, SS_BF16, &need_split);
+        if (need >= 2 * one && ws_bytes >= need) {
+            Bw = static_cast<float*>(workspace);
+            Cw = reinterpret_cast<float*>(static_cast<char*>(workspace) + one);
+            workspace = static_cast<char*>(workspace) + 2 * one;
+            ws_bytes -= 2 * one;
+        }
+    }
+
     // Time-split schedule (needs a workspace and TMA): when the channel tiles alone cannot
     // fill the GPU, cut the sequence into segments that run side by side (pass A: end states
     // from zero; carry pass; pass C: the fold from each segment's carried start).
@@ -534,6 +562,18 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         v.balanced = false;
     }
     const bool split = plan.nseg >= 2;
+    v.bcf32 = Bw && tma && v.family == kFamLane && (v.balanced || split);
+    if (v.bcf32) {
+        const int bh = fwd_geometry(v).chunk_steps;
+        if (!make_map(&maps.B, Bw, false, N, L, batch, N, L * N, v.ns, bh, false) ||
+            !make_map(&maps.C, Cw, false, N, L, batch, N, L * N, v.ns, bh, false))
+            return SS_ERR_CUDA;
+    }
+    // enqueued once every check of the schedule has passed, right before the scan
+    auto widen = [&]() -> cudaError_t {
+        return v.bcf32 ? launch_widen_bc(B, C, s.B_b, s.B_l, s.C_b, s.C_l, Bw, Cw, batch, L, static_cast<int>(N), stream)
+                       : cudaSuccess;
+    };
 
     FwdParams p;
     std::memset(&p, 0, sizeof(p));
@@ -576,6 +616,8 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         p.ws_state = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                               align_up(static_cast<size_t>(grid) * 4, 256));
         p.epoch = next_epoch();
+        const cudaError_t we = widen();
+        if (we != cudaSuccess) return cuda_status(we);
     }
     if (split) {
         if (plan.bytes > ws_bytes) return SS_ERR_INVALID_ARG;
@@ -588,8 +630,12 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         p.seg_dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.off_dsum);
         p.seg_out0 = 1;                   // slot 0 holds h0; segment s ends in slot s + 1
         auto lane = [&](const FwdVariant& vv, const FwdParams& pp) {
-            return bf16 ? launch_fwd_lane_bf16(vv, pp, maps, stream) : launch_fwd_lane_f32(vv, pp, maps, stream);
+            return vv.bcf32 ? launch_fwd_lane_bf16w(vv, pp, maps, stream)
+                 : bf16     ? launch_fwd_lane_bf16(vv, pp, maps, stream)
+                            : launch_fwd_lane_f32(vv, pp, maps, stream);
         };
+        cudaError_t e = widen();
+        if (e != cudaSuccess) return cuda_status(e);
         FwdParams pa = p;                 // pass A: segments 0 .. nseg-2 from zero
         pa.seg_launch = plan.nseg - 1;
         pa.grid = static_cast<int>(tiles_total * pa.seg_launch);
@@ -598,7 +644,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         pa.z = nullptr;                   // pass A reads neither z nor C
         FwdVariant va = v;
         va.state_only = true;
-        cudaError_t e = lane(va, pa);
+        e = lane(va, pa);
         if (e != cudaSuccess) return cuda_status(e);
         if ((e = launch_fwd_carry(p, stream)) != cudaSuccess) return cuda_status(e);
         FwdParams pc = p;                 // pass C: every segment from its carried start
@@ -613,6 +659,8 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     }
     if (v.family == kFamSeg)
         e = launch_fwd_seg(v, bf16, p, maps, stream);
+    else if (v.bcf32)
+        e = launch_fwd_lane_bf16w(v, p, maps, stream);
     else
         e = bf16 ? launch_fwd_lane_bf16(v, p, maps, stream) : launch_fwd_lane_f32(v, p, maps, stream);
     return cuda_status(e);
@@ -663,8 +711,11 @@ namespace {
 
 // Workspace bytes of the schedule ss_fwd_ws picks for these sizes (0: none needed, or invalid
 // sizes).  *split tells whether it is the time split, which also runs on less (fewer segments).
-size_t fwd_ws_need(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dtype, bool* split) {
+// with_widen: count the widened fp32 copies of bf16 B and C that a full-size workspace carries.
+size_t fwd_ws_need(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dtype, bool* split,
+                   bool with_widen) {
     *split = false;
+    const size_t widen = with_widen && widens_bc(io_dtype, N) ? 2 * widen_copy_bytes(batch, L, N) : 0;
     if (batch <= 0 || L <= 0 || Dm <= 0 || N < 1 || N > 16) return 0;
     if (io_dtype != SS_F32 && io_dtype != SS_BF16) return 0;
     FwdVariant v = choose_fwd_variant(batch, Dm, N);
@@ -686,17 +737,18 @@ size_t fwd_ws_need(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_d
         const SplitPlan pl = split_plan(tiles_ts, static_cast<int>(nch), batch * Dm, N, max_grid,
                                         static_cast<size_t>(-1), fs);
         *split = pl.nseg >= 2;
-        return pl.nseg >= 2 ? pl.bytes : 0;
+        return pl.nseg >= 2 ? pl.bytes + widen : 0;
     }
     if (v.family != kFamLane) return 0;
     v.balanced = true;
     v.tma = true;
+    v.bcf32 = widen > 0;
     const FwdGeom geo = fwd_geometry(v);
     const int64_t tiles = batch * ((Dm + geo.tile_channels - 1) / geo.tile_channels);
     int max_grid = 0;
     if (lane_max_grid(v, io_dtype == SS_BF16, &max_grid) != cudaSuccess || max_grid <= 0) return 0;
     const int64_t grid = balanced_grid(tiles, max_grid);
-    return balanced_ws_bytes(static_cast<int>(grid), geo.tile_channels, v.ns);
+    return balanced_ws_bytes(static_cast<int>(grid), geo.tile_channels, v.ns) + widen;
 }
 
 }  // namespace
@@ -880,9 +932,11 @@ int ss__fwd_plan(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dty
                 const SplitPlan pl = split_plan(tiles, static_cast<int>(nch), batch * Dm, N, max_grid,
                                                 static_cast<size_t>(-1), fs);
                 if (pl.nseg >= 2) {
-                    std::snprintf(buf, sizeof(buf), "ss_fwd_lane_kernel(lpc=%d,time-split,nseg=%d)", vs.lpc, pl.nseg);
+                    const bool wide = widens_bc(io_dtype, N);
+                    std::snprintf(buf, sizeof(buf), "ss_fwd_lane_kernel(lpc=%d,time-split,nseg=%d%s)", vs.lpc, pl.nseg,
+                                  wide ? ",fp32 B/C" : "");
                     put(buf);
-                    return 3;
+                    return wide ? 4 : 3;      // (widening,) pass A, carry, pass C
                 }
             }
         }
@@ -893,9 +947,11 @@ int ss__fwd_plan(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dty
     }
     const bool bal = with_ws && g_force_balanced.load() != 0;
     if (!bal && !fl) v.lpc = per_tile_lpc(batch, Dm, v.ns);
-    std::snprintf(buf, sizeof(buf), "ss_fwd_lane_kernel(lpc=%d%s)", v.lpc, bal ? ",balanced" : "");
+    const bool wide = bal && widens_bc(io_dtype, N);
+    std::snprintf(buf, sizeof(buf), "ss_fwd_lane_kernel(lpc=%d%s%s)", v.lpc, bal ? ",balanced" : "",
+                  wide ? ",fp32 B/C" : "");
     put(buf);
-    return 1;
+    return wide ? 2 : 1;                  // (the B/C widening pass,) the scan
 }
 
 ss_status ss_fwd_static(const void* u, const void* delta_raw, const float* delta_bias,
@@ -904,7 +960,8 @@ ss_status ss_fwd_static(const void* u, const void* delta_raw, const float* delta
                         int64_t Dm, int64_t N, const ss_fwd_strides* strides, void* stream) {
     const int32_t io = strides ? strides->io_dtype : SS_F32;
     bool split = false;
-    const size_t need = (batch > 0 && L > 0 && Dm > 0) ? fwd_ws_need(batch, L, Dm, N, io, &split) : 0;
+    // the fixed array carries no widened B/C copies: the schedules' own bytes only
+    const size_t need = (batch > 0 && L > 0 && Dm > 0) ? fwd_ws_need(batch, L, Dm, N, io, &split, false) : 0;
     // beyond the fixed array: the balanced schedule cannot shrink; the time split takes as many
     // segments as the array holds (fwd_impl's plan), or none below two
     if (need > SS_STATIC_WORKSPACE_BYTES && !split) return SS_ERR_UNSUPPORTED;

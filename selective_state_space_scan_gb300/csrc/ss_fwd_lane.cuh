@@ -47,7 +47,9 @@ namespace selscan {
 
 // DTR > 0: the low-rank time-step projection is folded in; the Δ tile's place holds a
 // [T][DTR-float-pitch] dt_low tile instead.
-template <typename TIO_, int NS_, int LPC_, int W_, int T_, int STAGES_, int MINB_, int DTR_ = 0>
+// BCF32: B and C arrive as fp32 tiles (a widened copy of bf16 B, C that the workspace schedules
+// make before the scan), so bf16 streams need no per-chunk widening in shared memory.
+template <typename TIO_, int NS_, int LPC_, int W_, int T_, int STAGES_, int MINB_, int DTR_ = 0, bool BCF32_ = false>
 struct LaneCfg {
     using TIO = TIO_;
     static constexpr int NS = NS_;            // states handled (4, 8 or 16; N <= NS)
@@ -63,12 +65,14 @@ struct LaneCfg {
     static constexpr int SPL = NS / LPC;      // states per lane
     static constexpr int QPL = SPL / 4;       // state quads per lane
     static constexpr int ES = sizeof(TIO);
-    static constexpr bool CONVERT_BC = ES == 2;
+    static constexpr bool BCF32 = BCF32_;
+    static constexpr int ES_BC = BCF32_ ? 4 : ES;             // bytes per staged B/C element
+    static constexpr bool CONVERT_BC = ES_BC == 2;
     static constexpr int up128(int x) { return (x + 127) / 128 * 128; }
     static constexpr int up1024(int x) { return (x + 1023) / 1024 * 1024; }
     static constexpr int RB = W * ES;                         // bytes of one tile row (W channels)
     static constexpr int TILE_X = T * RB;                     // one tensor's [T][W] tile, swizzled
-    static constexpr int TILE_N = T * NS * ES;
+    static constexpr int TILE_N = T * NS * ES_BC;
     static constexpr int TILE_D = DTR > 0 ? up1024(T * DTR * 4) : TILE_X;
     static constexpr int OFF_U = 0;
     static constexpr int OFF_D = TILE_X;
@@ -81,13 +85,25 @@ struct LaneCfg {
     static constexpr int AUX_DONE = AUX_FLAG + 16;                        // per-stage warp counters
     static constexpr int AUX_BAR = AUX_DONE + ((STAGES * 4 + 15) / 16) * 16;
     static constexpr int AUX_W = AUX_BAR + ((STAGES * 8 + 15) / 16) * 16;   // DTR > 0: W_dt rows [W][DTR]
-    static constexpr int AUX_BYTES = AUX_W + (DTR > 0 ? W * DTR * 4 : 0);
+    // Step groups per sub-block (register budget): at most 16, a divisor of the chunk's groups.
+    static constexpr int GT = T / LPC;
+    static constexpr int G = GT <= 16 ? GT : GT % 16 == 0 ? 16 : GT % 12 == 0 ? 12 : 8;
+    // DXS: the prepared (Δ, Δ·u) of a sub-block go through shared memory, [CPW][G·LPC + 2] float2
+    // per warp (rows padded so that a warp's 16-byte reads of its channels spread over the banks),
+    // read back two steps per 16-byte load, instead of two shuffles per step.  fp32 only: at 2
+    // lanes per channel it measured 153 against 170 us on the 130m-shaped layer, while on the
+    // 2.8b-shaped bf16 layer the shuffles were faster (694 against 724 us).
+    static constexpr bool DXS = LPC == 2 && ES == 4 && SS_DX_SMEM;
+    static constexpr int DX_PITCH = G * LPC + 2;                          // float2 per channel row
+    static constexpr int AUX_DX = AUX_W + (DTR > 0 ? W * DTR * 4 : 0);
+    static constexpr int AUX_BYTES = AUX_DX + (DXS ? WARPS * CPW * DX_PITCH * 8 : 0);
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + AUX_BYTES;
     static_assert(RB == 128 || RB == 64 || RB == 32, "a tile row must be one TMA swizzle span");
     static_assert(NS % (4 * LPC) == 0, "each lane must hold whole state quads");
     static_assert(W % CPW == 0 && WARPS >= 1, "a tile is whole warps");
     static_assert(T % LPC == 0 && T <= 256, "chunk must be whole groups and one TMA box");
     static_assert(DTR == 0 || ES == 4, "the folded projection is built for fp32 I/O");
+    static_assert(!BCF32_ || (ES == 2 && DTR == 0), "widened B/C tiles serve bf16 streams");
 };
 
 // A CTA's work in processing order: up to three runs of (tile, chunk) units.
@@ -228,6 +244,7 @@ __device__ __forceinline__ void wait_published(const unsigned int* flag, unsigne
 template <class Cfg, bool USE_TMA, bool STATE_ONLY = false, bool LTI = false>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
 ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
+    static_assert(!Cfg::BCF32 || (USE_TMA && !LTI), "widened B/C tiles come by TMA");
     using TIO = typename Cfg::TIO;
     constexpr int LPC = Cfg::LPC, CPW = Cfg::CPW, NS = Cfg::NS, QPL = Cfg::QPL, T = Cfg::T;
     constexpr int STAGES = USE_TMA ? Cfg::STAGES : 1;
@@ -451,9 +468,8 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             const int64_t tbase = static_cast<int64_t>(ch) * T;
             const int64_t left = L - tbase;                     // steps of this chunk before L
             const bool whole = left >= T;
-            constexpr int GT = T / LPC;                         // step groups in the chunk
-            // groups per sub-block (register budget): at most 16, a divisor of GT
-            constexpr int G = GT <= 16 ? GT : GT % 16 == 0 ? 16 : GT % 12 == 0 ? 12 : 8;
+            constexpr int GT = Cfg::GT;                         // step groups in the chunk
+            constexpr int G = Cfg::G;                           // groups per sub-block
             static_assert(GT % G == 0, "chunk must be whole sub-blocks");
             static_assert(G % NCX == 0, "sub-blocks start on a swizzle row class");
             static_assert(G % 2 == 0, "phases 1 and 3 take the steps in pairs");
@@ -495,11 +511,12 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                         du[g] = uu.x; du[g + 1] = uu.y;
                     }
                 } else {
-                    // two steps per pass: the polynomial and the products on packed pairs
+                    // two steps per pass: the polynomial and the products on packed pairs (bf16
+                    // outputs: the SFU's log2, whose error is far below the output's rounding)
 #pragma unroll
                     for (int g = 0; g < G; g += 2) {
                         const float2 x = add2(make_float2(at(td, g0, g), at(td, g0, g + 1)), splat2(bias_w));
-                        const float2 dl = softplus2(x);
+                        const float2 dl = (Cfg::ES == 2 && SS_BF16_LG2_SOFTPLUS) ? softplus2_lg2(x) : softplus2(x);
                         uv[g] = at(tu, g0, g);
                         uv[g + 1] = at(tu, g0, g + 1);
                         const float2 uu = mul2(dl, make_float2(uv[g], uv[g + 1]));
@@ -516,6 +533,15 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
 #pragma unroll
                     for (int g = 0; g < G; ++g) dsum += dd[g];
                 }
+                float2* dxrow = nullptr;
+                if constexpr (Cfg::DXS) {
+                    // this warp's rows; the previous sub-block's reads are done once every lane is here
+                    dxrow = reinterpret_cast<float2*>(aux + Cfg::AUX_DX) + (warp * CPW + c) * Cfg::DX_PITCH;
+                    __syncwarp();
+#pragma unroll
+                    for (int g = 0; g < G; ++g) dxrow[g * LPC + j] = make_float2(dd[g], du[g]);
+                    __syncwarp();
+                }
                 // Phase 2: the sequential fold.  Step g·LPC + k takes its Δ, Δ·u from lane (c, k);
                 // the C·h partial sums of the channel's LPC lanes are reduce-scattered so that lane
                 // (c, j) ends with the sum of step g·LPC + j.
@@ -525,10 +551,21 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                     // B load, SFU) before group g's recurrence runs, so their latency overlaps it.
                     float2 an[LPC][QPL][2], bn[LPC][QPL][2];
                     auto prep = [&](int g, float2 (&a)[LPC][QPL][2], float2 (&bb)[LPC][QPL][2]) {
+                        float4 dxq = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if constexpr (Cfg::DXS) dxq = *reinterpret_cast<const float4*>(dxrow + g * LPC);
 #pragma unroll
                         for (int kk = 0; kk < LPC; ++kk) {
-                            const float dk = LPC == 1 ? dd[g] : __shfl_sync(0xffffffffu, dd[g], kk * CPW + c);
-                            const float uk = LPC == 1 ? du[g] : __shfl_sync(0xffffffffu, du[g], kk * CPW + c);
+                            float dk, uk;
+                            if constexpr (LPC == 1) {
+                                dk = dd[g];
+                                uk = du[g];
+                            } else if constexpr (Cfg::DXS) {
+                                dk = kk == 0 ? dxq.x : dxq.z;
+                                uk = kk == 0 ? dxq.y : dxq.w;
+                            } else {
+                                dk = __shfl_sync(0xffffffffu, dd[g], kk * CPW + c);
+                                uk = __shfl_sync(0xffffffffu, du[g], kk * CPW + c);
+                            }
                             const float2 dl2 = make_float2(dk, dk), du2 = make_float2(uk, uk);
                             const float* rowB = tB + ((g0 + g) * LPC + kk) * NS + n0;
 #pragma unroll

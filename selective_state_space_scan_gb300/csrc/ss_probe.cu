@@ -23,11 +23,6 @@ constexpr int kProbeThreads = 512;
 constexpr int kProbeChains = 8;
 constexpr int kProbeSmem = 150 * 1024;    // more than half an SM's shared memory: one CTA per SM
 
-__device__ __forceinline__ float lg2_approx(float x) {
-    float y;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 __device__ __forceinline__ float tanh_approx(float x) {
     float y;
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
