@@ -22,6 +22,14 @@ namespace selscan {
 // (11.1 against 11.7 us on the 48-layer decode), 32 or 512 slower.
 constexpr int kStepThreads = 64;
 
+// Resident blocks per SM the decode kernels' registers are sized for: the step is bound by the
+// state loads in flight, so occupancy pays.  At 24 blocks (at most 42 registers) the 48-layer
+// launch measured 391 us against 455 us unbounded (56 registers, 52% occupancy) and 420 us at 32
+// blocks (32 registers, with spills).
+#ifndef SS_STEPL_MINB
+#define SS_STEPL_MINB 24
+#endif
+
 template <typename TIO> struct Vec4;
 template <> struct Vec4<float> {
     using T = float4;
@@ -153,16 +161,12 @@ __device__ __forceinline__ int step_blocks_per_b(int Dm) {
 }
 
 template <typename TIO, int LPR, int RPT, bool VEC>
-__global__ void __launch_bounds__(kStepThreads) ss_step_kernel(const StepParams p) {
+__global__ void __launch_bounds__(kStepThreads, SS_STEPL_MINB) ss_step_kernel(const StepParams p) {
     step_block<TIO, LPR, RPT, VEC>(p, static_cast<int>(blockIdx.x), step_blocks_per_b<LPR, RPT>(p.Dm));
 }
 
 // Many layers' steps in one launch: block x works on layer x / blocks_per_layer.  The layers
 // share sizes and strides; their pointers come from the parameter block.
-// Resident blocks per SM the many-layer kernel's registers are sized for (bytes in flight).
-#ifndef SS_STEPL_MINB
-#define SS_STEPL_MINB 1
-#endif
 
 template <typename TIO, int LPR, int RPT, bool VEC, int THREADS>
 __global__ void __launch_bounds__(THREADS, SS_STEPL_MINB) ss_step_layers_kernel(const __grid_constant__ StepLayersParams q) {
