@@ -26,6 +26,7 @@ struct FwdVariant {
     int es = 4;      // bytes per I/O element (4 fp32, 2 bf16)
     int chunk = 0;   // test override of the steps per chunk (16, 32 or 256; 0: the kernels' own)
     bool bcf32 = false;  // bf16 streams with B and C staged as fp32 (a widened copy in the workspace)
+    int cluster = 0;     // > 0: the single-launch time split, segments per cluster
 };
 
 struct FwdGeom {
@@ -59,6 +60,11 @@ cudaError_t launch_step(const StepParams& p, bool bf16, bool vec, cudaStream_t s
 cudaError_t launch_step_layers(const StepLayersParams& q, bool bf16, bool vec, cudaStream_t stream);
 // The lane kernel with the low-rank time-step projection folded in (fp32, per tile, TMA).
 cudaError_t launch_fwd_lane_dtp(const FwdVariant& v, const FwdParams& p, const FwdMaps& m, cudaStream_t stream);
+// The single-launch time split (fwd_lane_cluster.cu): p.grid = tiles × cluster CTAs in clusters of
+// `cluster` (2..8) consecutive CTAs, p.seg_launch = cluster.  With `fit` non-null, launch nothing
+// and return in fit[0] how many such clusters can be resident at once and in fit[1] the CTAs per SM.
+cudaError_t launch_fwd_lane_cluster(bool bf16, const FwdParams& p, const FwdMaps& m, cudaStream_t stream, int cluster,
+                                    int* fit = nullptr);
 // Test instantiations at other chunk lengths (fwd_lane_chunks.cu): whether v (with v.chunk set)
 // is one of them, and its launch.
 bool chunk_override_ok(const FwdVariant& v);

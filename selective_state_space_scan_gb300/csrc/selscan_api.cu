@@ -32,7 +32,8 @@ namespace {
 constexpr int kVersion = 100;   // 0.1.0
 
 // Test hook overriding the automatic choice of forward kernel: family (-1 auto, 0 state-split
-// lane, 1 segment-lane), lanes per channel of the lane family (0 auto, 1, 2 or 4) and tile fill
+// lane, 1 segment-lane, 2 the lane family's single-launch cluster split where it applies: no
+// workspace, TMA-fed, 16 states), lanes per channel of the lane family (0 auto, 1, 2 or 4) and tile fill
 // (-1 auto, 0 plain loads, 1 TMA; a forced choice the arguments cannot use is
 // SS_ERR_UNSUPPORTED).
 std::atomic<int> g_force_family{-1}, g_force_lpc{0}, g_force_tma{-1};
@@ -237,7 +238,7 @@ ss_status ss_device_error(uint32_t* bits, int clear) {
 const char* ss__fwd_kernel_name(int64_t batch, int64_t Dm, int64_t N) {
     if (N < 1 || N > 16) return "unsupported";
     FwdVariant v = choose_fwd_variant(batch, Dm, N);
-    if (g_force_family.load() >= 0) v.family = g_force_family.load();
+    if (g_force_family.load() >= 0) v.family = g_force_family.load() == 2 ? kFamSeg : g_force_family.load();
     if (g_force_lpc.load() > 0)
         v.lpc = g_force_lpc.load();
     else if (v.family == kFamLane)
@@ -263,7 +264,7 @@ int ss__force_nseg(int n) { return g_force_nseg.exchange(n < 0 ? -1 : n == 1 ? 0
 
 // Internal test hook (not part of the public header); see g_force_family.
 int ss__force_fwd_variant(int family, int lpc, int tma) {
-    if (family < -1 || family > 1 || (lpc != 0 && lpc != 1 && lpc != 2 && lpc != 4) || tma < -1 || tma > 1)
+    if (family < -1 || family > 2 || (lpc != 0 && lpc != 1 && lpc != 2 && lpc != 4) || tma < -1 || tma > 1)
         return -1;
     g_force_family.store(family);
     g_force_lpc.store(lpc);
@@ -360,6 +361,37 @@ size_t widen_copy_bytes(int64_t batch, int64_t L, int64_t N) {
     return align_up(sizeof(float) * static_cast<size_t>(batch) * static_cast<size_t>(L) * static_cast<size_t>(N), 256);
 }
 bool widens_bc(int32_t io_dtype, int64_t N) { return io_dtype == SS_BF16 && N == 16; }
+
+// Segments per cluster of the single-launch time split for these sizes (as many as fill the GPU
+// once, at most 8, none empty; 0: it does not fit), and the chunks per segment.
+int cluster_plan(bool bf16, int64_t batch, int64_t L, int64_t Dm, int* seg_chunks) {
+    const int64_t nch = (L + kLaneT - 1) / kLaneT;
+    const int64_t tiles_c = batch * ((Dm + 31) / 32);
+    int dev = 0, sms = 0, fit[2] = {0, 0};
+    FwdParams probe;
+    std::memset(&probe, 0, sizeof(probe));
+    FwdMaps none;
+    std::memset(&none, 0, sizeof(none));
+    int result = 0;
+    if (tiles_c > 0 && cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        launch_fwd_lane_cluster(bf16, probe, none, nullptr, 8, fit) == cudaSuccess && fit[1] > 0) {
+        int64_t cs = std::min<int64_t>(std::min<int64_t>(static_cast<int64_t>(fit[1]) * sms / tiles_c, 8), nch);
+        if (cs >= 2) {
+            const int64_t seg = (nch + cs - 1) / cs;
+            cs = (nch + seg - 1) / seg;
+            int fit_cs[2] = {0, 0};
+            if (cs >= 2 && seg <= INT32_MAX &&
+                launch_fwd_lane_cluster(bf16, probe, none, nullptr, static_cast<int>(cs), fit_cs) == cudaSuccess &&
+                fit_cs[0] > 0) {
+                *seg_chunks = static_cast<int>(seg);
+                result = static_cast<int>(cs);
+            }
+        }
+    }
+    cudaGetLastError();
+    return result;
+}
 
 ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
                    const void* B, const void* C, const float* D, const void* z, void* y,
@@ -463,7 +495,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     const int max_lpc = v.ns / 4;
     const int ff = g_force_family.load(), fl = g_force_lpc.load(), ft = g_force_tma.load();
     const int fc = dtp ? 0 : g_force_chunk.load();
-    if (ff >= 0) v.family = ff;
+    if (ff >= 0) v.family = ff == 2 ? kFamSeg : ff;   // 2: the cluster split where it applies, else segment
     if (fc > 0) v.chunk = fc;
     if (dtp) {                           // lane family only, as many lanes per channel as allowed
         if (v.family != kFamLane) v.lpc = max_lpc;
@@ -542,6 +574,21 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     if (!v.balanced && plan.nseg < 2 && v.family == kFamLane && fl <= 0) v.lpc = per_tile_lpc(batch, Dm, v.ns);
     FwdMaps maps;
     std::memset(&maps, 0, sizeof(maps));
+
+    // Single-launch time split (no workspace): when the channel tiles alone cannot fill the GPU
+    // (the segment family's case; family 2 forces it), CTAs that fold the time segments of one
+    // tile form a cluster and exchange their segments' summaries through distributed shared
+    // memory, so the split needs neither a workspace nor a second launch.
+    int cluster_seg_chunks = 0;
+    if (!workspace && tma && !lti && !dtp && fc == 0 && v.ns == 16 && v.family == kFamSeg && (ff < 0 || ff == 2) &&
+        (fl <= 0 || fl == 4)) {
+        const int cs = cluster_plan(bf16, batch, L, Dm, &cluster_seg_chunks);
+        if (cs >= 2) {
+            v.family = kFamLane;
+            v.lpc = 4;
+            v.cluster = cs;
+        }
+    }
     if (tma) {
         const FwdGeom g0 = fwd_geometry(v);
         const bool swbc = v.family == kFamSeg;
@@ -653,6 +700,13 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         return cuda_status(lane(v, pc));
     }
     cudaError_t e;
+    if (v.cluster > 0) {
+        p.seg_launch = v.cluster;
+        p.seg_chunks = cluster_seg_chunks;
+        p.nseg = v.cluster;
+        p.grid = static_cast<int>(batch * tiles * v.cluster);
+        return cuda_status(launch_fwd_lane_cluster(bf16, p, maps, stream, v.cluster));
+    }
     if (v.chunk > 0) {
         if (!chunk_override_ok(v)) return SS_ERR_UNSUPPORTED;
         return cuda_status(launch_fwd_lane_chunked(v, p, maps, stream));
@@ -721,7 +775,7 @@ size_t fwd_ws_need(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_d
     FwdVariant v = choose_fwd_variant(batch, Dm, N);
     v.es = io_dtype == SS_BF16 ? 2 : 4;
     const int ff = g_force_family.load(), fs = g_force_nseg.load();
-    if (ff >= 0) v.family = ff;
+    if (ff >= 0) v.family = ff == 2 ? kFamSeg : ff;
     const int fl = g_force_lpc.load() > 0 && g_force_lpc.load() <= v.ns / 4 ? g_force_lpc.load() : 0;
     if (fl) v.lpc = fl;
     if (fs != 0 && (fs >= 2 || (v.family == kFamSeg && ff < 0))) {
@@ -916,7 +970,7 @@ int ss__fwd_plan(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dty
     FwdVariant v = choose_fwd_variant(batch, Dm, N);
     v.es = io_dtype == SS_BF16 ? 2 : 4;
     const int ff = g_force_family.load(), fs = g_force_nseg.load();
-    if (ff >= 0) v.family = ff;
+    if (ff >= 0) v.family = ff == 2 ? kFamSeg : ff;
     const int fl = g_force_lpc.load() > 0 && g_force_lpc.load() <= v.ns / 4 ? g_force_lpc.load() : 0;
     if (fl) v.lpc = fl;
     char buf[96];
@@ -942,7 +996,15 @@ int ss__fwd_plan(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dty
         }
     }
     if (v.family == kFamSeg) {
-        put("ss_fwd_seg_kernel");
+        int seg = 0;
+        const int cs = !with_ws && N == 16 && (fl <= 0 || fl == 4) ? cluster_plan(io_dtype == SS_BF16, batch, L, Dm, &seg)
+                                                                    : 0;
+        if (cs >= 2) {
+            std::snprintf(buf, sizeof(buf), "ss_fwd_lane_kernel(lpc=4,cluster split,nseg=%d)", cs);
+            put(buf);
+        } else {
+            put("ss_fwd_seg_kernel");
+        }
         return 1;
     }
     const bool bal = with_ws && g_force_balanced.load() != 0;

@@ -40,6 +40,8 @@
 // state and Σ Δ; pass C from the segment's start state that the carry kernel composed.
 #pragma once
 
+#include <type_traits>
+
 #include "device_common.cuh"
 #include "fwd_params.h"
 
@@ -49,7 +51,10 @@ namespace selscan {
 // [T][DTR-float-pitch] dt_low tile instead.
 // BCF32: B and C arrive as fp32 tiles (a widened copy of bf16 B, C that the workspace schedules
 // make before the scan), so bf16 streams need no per-chunk widening in shared memory.
-template <typename TIO_, int NS_, int LPC_, int W_, int T_, int STAGES_, int MINB_, int DTR_ = 0, bool BCF32_ = false>
+// XCH: room for this CTA's segment summary (end state [W][NS] and Σ Δ [W]) that the CTAs of a
+// cluster read from each other (the single-launch time split).
+template <typename TIO_, int NS_, int LPC_, int W_, int T_, int STAGES_, int MINB_, int DTR_ = 0, bool BCF32_ = false,
+          bool XCH_ = false>
 struct LaneCfg {
     using TIO = TIO_;
     static constexpr int NS = NS_;            // states handled (4, 8 or 16; N <= NS)
@@ -96,7 +101,8 @@ struct LaneCfg {
     static constexpr bool DXS = LPC == 2 && ES == 4 && SS_DX_SMEM;
     static constexpr int DX_PITCH = G * LPC + 2;                          // float2 per channel row
     static constexpr int AUX_DX = AUX_W + (DTR > 0 ? W * DTR * 4 : 0);
-    static constexpr int AUX_BYTES = AUX_DX + (DXS ? WARPS * CPW * DX_PITCH * 8 : 0);
+    static constexpr int AUX_XCH = AUX_DX + (DXS ? WARPS * CPW * DX_PITCH * 8 : 0);
+    static constexpr int AUX_BYTES = AUX_XCH + (XCH_ ? W * NS * 4 + W * 4 : 0);
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + AUX_BYTES;
     static_assert(RB == 128 || RB == 64 || RB == 32, "a tile row must be one TMA swizzle span");
     static_assert(NS % (4 * LPC) == 0, "each lane must hold whole state quads");
@@ -241,10 +247,17 @@ __device__ __forceinline__ void wait_published(const unsigned int* flag, unsigne
 // C, y or the z gate: it writes the segment's end state and its Σ Δ.
 // LTI: B and C do not vary with the step (the linear time-invariant case, step stride 0): each
 // lane holds its states' B and C in registers and no B/C tiles are staged.
-template <class Cfg, bool USE_TMA, bool STATE_ONLY = false, bool LTI = false>
+// CLUSTER: the single-launch time split.  The grid is tiles × p.seg_launch CTAs in clusters of
+// p.seg_launch; CTA rank r of a cluster folds segment r of the cluster's tile twice: first from a
+// zero state keeping only its end state and Σ Δ (as STATE_ONLY), which it leaves in its shared
+// memory; after a cluster barrier it reads the summaries of ranks 0 .. r-1 from their shared
+// memory and composes the state entering its segment, H_0 = h0, H_{s+1} = 2^(A'·ΣΔ_s)·H_s + end_s;
+// then it folds the segment again from that state with every output.
+template <class Cfg, bool USE_TMA, bool STATE_ONLY = false, bool LTI = false, bool CLUSTER = false>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
 ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     static_assert(!Cfg::BCF32 || (USE_TMA && !LTI), "widened B/C tiles come by TMA");
+    static_assert(!CLUSTER || (USE_TMA && !STATE_ONLY && !LTI && Cfg::DTR == 0), "the cluster split is TMA-fed");
     using TIO = typename Cfg::TIO;
     constexpr int LPC = Cfg::LPC, CPW = Cfg::CPW, NS = Cfg::NS, QPL = Cfg::QPL, T = Cfg::T;
     constexpr int STAGES = USE_TMA ? Cfg::STAGES : 1;
@@ -279,7 +292,8 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     const int n0 = j * Cfg::SPL;         // first state of this lane's slice
     const int64_t ystride = p.y_l * static_cast<int64_t>(sizeof(TIO));   // bytes between steps of y
     const LaneWork work = lane_work(p, p.batch * p.tiles_per_batch);
-    const int total = work.total();
+    // CLUSTER: the segment's chunks are staged twice (the summary fold, then the full fold)
+    const int total = CLUSTER ? 2 * work.total() : work.total();
     // Byte offset of this lane's element in a swizzled [T][W] tile, for rows j + q·LPC (row
     // offset included).  A sub-block's rows g·LPC + j fall in NCX classes mod 8, and the
     // swizzle depends on the row only mod 8.
@@ -307,6 +321,19 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     __syncthreads();
     auto issue = [&](int k, uint8_t* st, uint64_t* bar) {
         int tl, chk;
+        if constexpr (CLUSTER) {
+            // units 0 .. n-1: the summary fold (u, Δ, B only); n .. 2n-1: the full fold
+            const int n = work.n2;
+            tl = work.t2;
+            chk = work.c2 + (k < n ? k : k - n);
+            if (k < n)
+                lane_issue_tma<Cfg, false, LTI>(st, bar, maps, false, tl / p.tiles_per_batch,
+                                                (tl % p.tiles_per_batch) * Cfg::W, chk, p.dt_pitch);
+            else
+                lane_issue_tma<Cfg, true, LTI>(st, bar, maps, has_z, tl / p.tiles_per_batch,
+                                               (tl % p.tiles_per_batch) * Cfg::W, chk, p.dt_pitch);
+            return;
+        }
         work.unit(k, nchunks, tl, chk);
         lane_issue_tma<Cfg, !STATE_ONLY, LTI>(st, bar, maps, has_z, tl / p.tiles_per_batch,
                             (tl % p.tiles_per_batch) * Cfg::W, chk, p.dt_pitch);
@@ -338,7 +365,11 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     const int whole_tiles = work.n1 / nchunks;
     const int npieces = (work.n0 > 0 ? 1 : 0) + whole_tiles + (work.n2 > 0 ? 1 : 0);
     int k = 0;
-    for (int piece = 0; piece < npieces; ++piece) {
+    // One piece; SO: the state-only fold (pass A of the time split, or the summary fold of the
+    // cluster split), known at compile time.
+    auto run_piece = [&](auto so_tag, int piece) {
+        constexpr bool SO = decltype(so_tag)::value;
+        constexpr bool KEEP_H = CLUSTER && !SO;     // the cluster's full fold starts from the composed state
         int tile, c0, cnt;
         const int q = piece - (work.n0 > 0 ? 1 : 0);
         if (q < 0) {
@@ -363,7 +394,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             }
             A2[qq][0] = make_float2(v[0], v[1]);
             A2[qq][1] = make_float2(v[2], v[3]);
-            h[qq][0] = h[qq][1] = make_float2(0.f, 0.f);
+            if constexpr (!KEEP_H) h[qq][0] = h[qq][1] = make_float2(0.f, 0.f);
             if constexpr (LTI) {
                 const TIO* Bb = static_cast<const TIO*>(p.Bm) + b * p.B_b;
                 const TIO* Cb = static_cast<const TIO*>(p.Cm) + b * p.C_b;
@@ -389,7 +420,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             }
             __syncthreads();
         }
-        if constexpr (!STATE_ONLY) {
+        if constexpr (!SO && !CLUSTER) {
             const float* src = nullptr;    // the state before this unit's first chunk
             if (p.seg_launch > 0) {
                 // time-split pass C: the carry the carry kernel left for this segment
@@ -456,7 +487,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                 };
                 for (int i = tid; i < T * NS / 4; i += Cfg::THREADS) {
                     wb[i] = widen(rb[i]);
-                    if constexpr (!STATE_ONLY) wb[T * NS / 4 + i] = widen(rc[i]);
+                    if constexpr (!SO) wb[T * NS / 4 + i] = widen(rc[i]);
                 }
                 __syncthreads();
                 tB = bcf;
@@ -529,7 +560,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                     for (int g = 0; g < G; ++g)
                         if ((g0 + g) * LPC + j >= left) dd[g] = du[g] = 0.f;
                 }
-                if constexpr (STATE_ONLY) {
+                if constexpr (SO) {
 #pragma unroll
                     for (int g = 0; g < G; ++g) dsum += dd[g];
                 }
@@ -601,18 +632,18 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                                 float4 C4 = make_float4(0.f, 0.f, 0.f, 0.f);
                                 if constexpr (LTI)
                                     C4 = cL[qq];
-                                else if constexpr (!STATE_ONLY)
+                                else if constexpr (!SO)
                                     C4 = *reinterpret_cast<const float4*>(rowC + 4 * qq);
                                 h[qq][0] = fma2(ac[kk][qq][0], h[qq][0], bc[kk][qq][0]);
                                 h[qq][1] = fma2(ac[kk][qq][1], h[qq][1], bc[kk][qq][1]);
-                                if constexpr (!STATE_ONLY) {
+                                if constexpr (!SO) {
                                     acc = fma2(make_float2(C4.x, C4.y), h[qq][0], acc);
                                     acc = fma2(make_float2(C4.z, C4.w), h[qq][1], acc);
                                 }
                             }
                             yp[kk] = acc.x + acc.y;
                         }
-                        if constexpr (STATE_ONLY) {
+                        if constexpr (SO) {
                             (void)yp;
                         } else if constexpr (LPC == 1) {
                             yv[g] = yp[0];
@@ -638,7 +669,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                     }
                 }
                 // Phase 3: D skip, z gate, store (G independent chains).
-                if (!STATE_ONLY && d_ok) {
+                if (!SO && d_ok) {
                     char* yrow = reinterpret_cast<char*>(static_cast<TIO*>(p.y) + b * p.y_b + (tbase + g0 * LPC + j) * p.y_l + d);
                     const int64_t rem = left - g0 * LPC - j;          // steps of this lane's column before L
                     const int nst = whole ? G : (rem <= 0 ? 0 : rem >= int64_t(G) * LPC ? G : static_cast<int>((rem + LPC - 1) / LPC));
@@ -682,7 +713,11 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
 
         // End of the piece: the sequence's final state, or (head of a tile another CTA
         // finishes) the state to hand over; for pass A, the segment's end state and Σ Δ.
-        if constexpr (STATE_ONLY) {
+        if constexpr (SO && CLUSTER) {
+            // the summary stays on chip: the end state in h, the channel's Σ Δ (over its lanes) in dsum
+            if constexpr (LPC >= 2) dsum += __shfl_xor_sync(0xffffffffu, dsum, CPW);
+            if constexpr (LPC >= 4) dsum += __shfl_xor_sync(0xffffffffu, dsum, 2 * CPW);
+        } else if constexpr (SO) {
             const int sg = c0 / p.seg_chunks;
             if (d_ok) {
                 float* dst = p.seg_slots + ((static_cast<int64_t>(sg + p.seg_out0) * p.batch + b) * p.Dm + d) * p.N;
@@ -722,6 +757,54 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                              : "memory");
             }
         }
+    };
+
+    if constexpr (CLUSTER) {
+        // this CTA's segment: the summary fold, the exchange, the full fold (one piece; an empty
+        // segment folds nothing and passes the state through)
+        if (npieces > 0) run_piece(std::true_type{}, 0);
+        float* xh = reinterpret_cast<float*>(aux + Cfg::AUX_XCH);   // [W][NS] end state from zero
+        float* xd = xh + Cfg::W * NS;                                // [W] Σ Δ
+#pragma unroll
+        for (int qq = 0; qq < QPL; ++qq)
+            *reinterpret_cast<float4*>(xh + cw * NS + n0 + 4 * qq) =
+                make_float4(h[qq][0].x, h[qq][0].y, h[qq][1].x, h[qq][1].y);
+        if (j == 0) xd[cw] = dsum;
+        cluster_sync_all();                 // every summary of the cluster written
+        const uint32_t rank = cluster_ctarank();
+        float2 H[QPL][2];
+#pragma unroll
+        for (int qq = 0; qq < QPL; ++qq) H[qq][0] = H[qq][1] = make_float2(0.f, 0.f);
+        if (p.h0 && d_ok) {
+            const float* src = p.h0 + (static_cast<int64_t>(b) * p.Dm + d) * p.N;
+#pragma unroll
+            for (int qq = 0; qq < QPL; ++qq) {
+                float v[4];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) v[q4] = n0 + 4 * qq + q4 < p.N ? __ldcg(src + n0 + 4 * qq + q4) : 0.f;
+                H[qq][0] = make_float2(v[0], v[1]);
+                H[qq][1] = make_float2(v[2], v[3]);
+            }
+        }
+        for (uint32_t r = 0; r < rank; ++r) {
+            const float ds = ld_peer_f32(peer_smem_addr(xd + cw, r));
+            const float2 ds2 = make_float2(ds, ds);
+#pragma unroll
+            for (int qq = 0; qq < QPL; ++qq) {
+                const float4 e = ld_peer_f32x4(peer_smem_addr(xh + cw * NS + n0 + 4 * qq, r));
+                H[qq][0] = fma2(ex2x2(mul2(ds2, A2[qq][0])), H[qq][0], make_float2(e.x, e.y));
+                H[qq][1] = fma2(ex2x2(mul2(ds2, A2[qq][1])), H[qq][1], make_float2(e.z, e.w));
+            }
+        }
+        cluster_sync_all();                 // no CTA leaves while a peer may still read its summary
+#pragma unroll
+        for (int qq = 0; qq < QPL; ++qq) {
+            h[qq][0] = H[qq][0];
+            h[qq][1] = H[qq][1];
+        }
+        if (npieces > 0) run_piece(std::false_type{}, 0);
+    } else {
+        for (int piece = 0; piece < npieces; ++piece) run_piece(std::integral_constant<bool, STATE_ONLY>{}, piece);
     }
 }
 
