@@ -61,6 +61,17 @@ __device__ __forceinline__ float silu(float z) {
     return z * rcp_approx(1.f + ex2(-z * kLog2e));
 }
 
+// A run of steps of the recurrence acts on the state as the affine map h -> a·h + b, kept as the
+// pair (a, b).  Running `earlier` and then `later` is again such a map, with
+// a = a_later·a_earlier and b = a_later·b_earlier + b_later: the associative operator the scans
+// combine with ("mamba-metal: Apple Silicon で Mamba を動かす", section "Selective scan の本質").
+struct AffinePair {
+    float a, b;
+};
+__device__ __forceinline__ AffinePair compose(AffinePair later, AffinePair earlier) {
+    return AffinePair{later.a * earlier.a, fmaf(later.a, earlier.b, later.b)};
+}
+
 // Packed fp32 pairs (one instruction for two lanes of arithmetic on sm_100+).
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }

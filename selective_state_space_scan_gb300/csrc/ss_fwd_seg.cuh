@@ -308,16 +308,19 @@ ss_fwd_seg_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             float Ag[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) Ag[j] = ex2(sumd * f4get(A4, j));
-            // intra-warp (a,b) scan over the 4 segments of this warp (lanes 8 apart)
+            // Inclusive scan of the segment maps across this warp's 4 segments (lanes 8 apart): in
+            // two doubling rounds each lane composes its map with the one `off` segments earlier,
+            // so that it ends with the map of every segment up to its own.
 #pragma unroll
             for (int off = 8; off <= 16; off <<= 1) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float Ap = __shfl_up_sync(0xffffffffu, Ag[j], off);
-                    const float Hp = __shfl_up_sync(0xffffffffu, H[j], off);
+                    const AffinePair earlier{__shfl_up_sync(0xffffffffu, Ag[j], off),
+                                             __shfl_up_sync(0xffffffffu, H[j], off)};
                     if (lane >= off) {
-                        H[j] = fmaf(Ag[j], Hp, H[j]);   // b first, with the old a
-                        Ag[j] *= Ap;
+                        const AffinePair upto = compose(AffinePair{Ag[j], H[j]}, earlier);
+                        Ag[j] = upto.a;
+                        H[j] = upto.b;
                     }
                 }
             }

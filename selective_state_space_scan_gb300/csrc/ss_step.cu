@@ -22,10 +22,11 @@ namespace selscan {
 // (11.1 against 11.7 us on the 48-layer decode), 32 or 512 slower.
 constexpr int kStepThreads = 64;
 
-// Resident blocks per SM the decode kernels' registers are sized for: the step is bound by the
-// state loads in flight, so occupancy pays.  At 24 blocks (at most 42 registers) the 48-layer
+// Resident blocks per SM the many-layer kernel's registers are sized for: the step is bound by
+// the state loads in flight, so occupancy pays.  At 24 blocks (at most 42 registers) the 48-layer
 // launch measured 391 us against 455 us unbounded (56 registers, 52% occupancy) and 420 us at 32
-// blocks (32 registers, with spills).
+// blocks (32 registers, with spills).  The single-layer kernel stays unbounded: its short
+// launches measured 10.8 us a layer unbounded against 12.4 us at 24 blocks.
 #ifndef SS_STEPL_MINB
 #define SS_STEPL_MINB 24
 #endif
@@ -161,7 +162,7 @@ __device__ __forceinline__ int step_blocks_per_b(int Dm) {
 }
 
 template <typename TIO, int LPR, int RPT, bool VEC>
-__global__ void __launch_bounds__(kStepThreads, SS_STEPL_MINB) ss_step_kernel(const StepParams p) {
+__global__ void __launch_bounds__(kStepThreads) ss_step_kernel(const StepParams p) {
     step_block<TIO, LPR, RPT, VEC>(p, static_cast<int>(blockIdx.x), step_blocks_per_b<LPR, RPT>(p.Dm));
 }
 
