@@ -13,6 +13,12 @@ namespace selscan {
 #define SS_LANE_STAGES 2
 #endif
 constexpr int kLaneT = SS_LANE_T;
+// Sub-blocks of a chunk unrolled together (1: a loop over the sub-blocks; 2 measured 842 against
+// 677 us on the 2.8b-shaped layer).
+#ifndef SS_UNROLL_SUB
+#define SS_UNROLL_SUB 1
+#endif
+constexpr int kLaneUnrollSub = SS_UNROLL_SUB;
 // Lane kernel options (compile-time, for measurement): the (Δ, Δ·u) hand-over at 2 lanes per
 // channel through shared memory instead of shuffles (fp32); softplus through the SFU's log2 for
 // bf16 (742 -> 723 us on the 2.8b-shaped layer).

@@ -92,7 +92,11 @@ struct LaneCfg {
     static constexpr int AUX_W = AUX_BAR + ((STAGES * 8 + 15) / 16) * 16;   // DTR > 0: W_dt rows [W][DTR]
     // Step groups per sub-block (register budget): at most 16, a divisor of the chunk's groups.
     static constexpr int GT = T / LPC;
-    static constexpr int G = GT <= 16 ? GT : GT % 16 == 0 ? 16 : GT % 12 == 0 ? 12 : 8;
+// (At most 16 groups: at 8 the 2.8b-shaped layer measured 717 against 677 us.)
+#ifndef SS_LANE_GMAX
+#define SS_LANE_GMAX 16
+#endif
+    static constexpr int G = GT <= SS_LANE_GMAX ? GT : GT % SS_LANE_GMAX == 0 ? SS_LANE_GMAX : GT % 12 == 0 ? 12 : 8;
     // DXS: the prepared (Δ, Δ·u) of a sub-block go through shared memory, [CPW][G·LPC + 2] float2
     // per warp (rows padded so that a warp's 16-byte reads of its channels spread over the banks),
     // read back two steps per 16-byte load, instead of two shuffles per step.  fp32 only: at 2
@@ -504,7 +508,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             static_assert(GT % G == 0, "chunk must be whole sub-blocks");
             static_assert(G % NCX == 0, "sub-blocks start on a swizzle row class");
             static_assert(G % 2 == 0, "phases 1 and 3 take the steps in pairs");
-#pragma unroll 1
+#pragma unroll (kLaneUnrollSub)
             for (int g0 = 0; g0 < GT; g0 += G) {
                 // Phase 1: Δ and Δ·u of the steps this lane prepares (step g·LPC + j of each group;
                 // zero past L, i.e. identity pairs).  G independent softplus chains.
