@@ -19,6 +19,12 @@ constexpr int kLaneT = SS_LANE_T;
 #define SS_UNROLL_SUB 1
 #endif
 constexpr int kLaneUnrollSub = SS_UNROLL_SUB;
+// The reduce-scatter of a step group's C·h partial sums issued after the next group's
+// arithmetic (1) or right after its own (0).
+#ifndef SS_DEFER_REDUCE
+#define SS_DEFER_REDUCE 1
+#endif
+constexpr bool kLaneDeferReduce = SS_DEFER_REDUCE != 0;
 // Lane kernel options (compile-time, for measurement): the (Δ, Δ·u) hand-over at 2 lanes per
 // channel through shared memory instead of shuffles (fp32); softplus through the SFU's log2 for
 // bf16 (742 -> 723 us on the 2.8b-shaped layer).

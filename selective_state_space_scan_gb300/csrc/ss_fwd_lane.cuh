@@ -614,6 +614,33 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                             }
                         }
                     };
+                    // The channel's LPC partial sums of one step group, reduce-scattered so that lane
+                    // (c, j) ends with step j's sum.  LPC = 2: one exchange.  LPC = 4: a butterfly over
+                    // the four slices (lanes c + CPW·s), first across slice bit 1 (each side keeps two
+                    // steps), then across bit 0.  Only shuffles, no shared-memory round trip or warp
+                    // barrier.  (The fold must visit the steps in time order, so the slots cannot be
+                    // renumbered per lane to spare the selects.)
+                    auto reduce_scatter = [&](const float (&v)[LPC]) -> float {
+                        if constexpr (LPC == 2) {
+                            const bool hi = j & 1;
+                            const float send = hi ? v[0] : v[1];
+                            const float keep = hi ? v[1] : v[0];
+                            return keep + __shfl_xor_sync(0xffffffffu, send, CPW);
+                        } else if constexpr (LPC == 4) {
+                            const bool b1 = (j & 2) != 0, b0 = (j & 1) != 0;
+                            const float s0 = b1 ? v[0] : v[2], s1 = b1 ? v[1] : v[3];
+                            const float k0 = b1 ? v[2] : v[0], k1 = b1 ? v[3] : v[1];
+                            const float t0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 2 * CPW);
+                            const float t1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 2 * CPW);
+                            const float sd = b0 ? t0 : t1, kp = b0 ? t1 : t0;
+                            return kp + __shfl_xor_sync(0xffffffffu, sd, CPW);
+                        } else {
+                            return v[0];
+                        }
+                    };
+                    float ypp[LPC];                 // the previous group's partial sums (deferred reduce)
+#pragma unroll
+                    for (int kk = 0; kk < LPC; ++kk) ypp[kk] = 0.f;
                     prep(0, an, bn);
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
@@ -651,24 +678,15 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                             (void)yp;
                         } else if constexpr (LPC == 1) {
                             yv[g] = yp[0];
-                        } else if constexpr (LPC == 2) {
-                            const bool hi = j & 1;
-                            const float send = hi ? yp[0] : yp[1];
-                            const float keep = hi ? yp[1] : yp[0];
-                            yv[g] = keep + __shfl_xor_sync(0xffffffffu, send, CPW);
+                        } else if constexpr (kLaneDeferReduce) {
+                            // reduce the previous group's partial sums now, after this group's
+                            // arithmetic, so that the shuffles' latency overlaps it
+                            if (g > 0) yv[g - 1] = reduce_scatter(ypp);
+#pragma unroll
+                            for (int kk = 0; kk < LPC; ++kk) ypp[kk] = yp[kk];
+                            if (g + 1 == G) yv[g] = reduce_scatter(ypp);
                         } else {
-                            // butterfly reduce-scatter over the four slices (lanes c + CPW·s): first
-                            // across slice bit 1 (each side keeps two steps), then across bit 0.  Only
-                            // shuffles, no shared-memory round trip or warp barrier, so the next
-                            // group's loads are free to start early.  (The fold itself must visit the
-                            // steps in time order, so the slots cannot be renumbered per lane.)
-                            const bool b1 = (j & 2) != 0, b0 = (j & 1) != 0;
-                            const float s0 = b1 ? yp[0] : yp[2], s1 = b1 ? yp[1] : yp[3];
-                            const float k0 = b1 ? yp[2] : yp[0], k1 = b1 ? yp[3] : yp[1];
-                            const float t0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 2 * CPW);
-                            const float t1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 2 * CPW);
-                            const float sd = b0 ? t0 : t1, kp = b0 ? t1 : t0;
-                            yv[g] = kp + __shfl_xor_sync(0xffffffffu, sd, CPW);
+                            yv[g] = reduce_scatter(yp);
                         }
                     }
                 }
