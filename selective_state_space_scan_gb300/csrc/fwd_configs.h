@@ -25,6 +25,7 @@ constexpr int kLaneUnrollSub = SS_UNROLL_SUB;
 #define SS_DEFER_REDUCE 1
 #endif
 constexpr bool kLaneDeferReduce = SS_DEFER_REDUCE != 0;
+
 // Lane kernel options (compile-time, for measurement): the (Δ, Δ·u) hand-over at 2 lanes per
 // channel through shared memory instead of shuffles (fp32); softplus through the SFU's log2 for
 // bf16 (742 -> 723 us on the 2.8b-shaped layer).
@@ -43,6 +44,10 @@ constexpr int kLaneStages = SS_LANE_STAGES;
 constexpr int lane_minb(int lpc, int w) {
     return (lpc == 4 ? 4 * SS_LANE_MINB4 : lpc == 2 ? 12 : 8) / (w * lpc / 32 > 0 ? w * lpc / 32 : 1);
 }
+// bf16 streams with fp32 B/C tiles (the workspace schedules): shared memory holds five CTAs of a
+// 32-channel tile per SM, and a 2-lane CTA sized for four per SM gets 176 registers per thread,
+// which still lets five reside (126 before: 674 -> 667 us on the 2.8b-shaped layer).
+constexpr int lane_minb_bcf32(int lpc, int w) { return lpc == 2 && w == 32 ? 4 : lane_minb(lpc, w); }
 // Tile width: 32 channels for one CTA per tile.  The balanced schedule needs at least as many
 // tiles as SMs times resident CTAs, so its fp32 tiles are 16 channels (64-byte rows); its bf16
 // tiles stay at 32 (64-byte rows too: narrower rows would have each 64-byte DRAM access read by

@@ -9,7 +9,7 @@ namespace selscan {
 template <typename TIO, int NS, int LPC, bool BAL, bool TMA, bool SO = false, bool LTI = false, bool BCF = false>
 cudaError_t launch_lane_cfg(const FwdParams& p, const FwdMaps& m, cudaStream_t stream, int* max_grid) {
     constexpr int W = lane_w(LPC, BAL, static_cast<int>(sizeof(TIO)));
-    using Cfg = LaneCfg<TIO, NS, LPC, W, kLaneT, kLaneStages, lane_minb(LPC, W), 0, BCF>;
+    using Cfg = LaneCfg<TIO, NS, LPC, W, kLaneT, kLaneStages, BCF ? lane_minb_bcf32(LPC, W) : lane_minb(LPC, W), 0, BCF>;
     constexpr int smem = TMA ? Cfg::SMEM_BYTES : Cfg::SMEM_BYTES - (Cfg::STAGES - 1) * Cfg::STAGE_BYTES;
     static_assert(smem <= 227 * 1024, "shared memory budget exceeded");
     return launch_with_smem<Cfg, TMA>(ss_fwd_lane_kernel<Cfg, TMA, SO, LTI>, p, m, stream, smem, BAL, max_grid);

@@ -583,24 +583,30 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                 float yv[G];
                 {
                     // The decays a = 2^(Δ·A') and inputs b = Δu·B of group g + 1 are formed (shuffle,
-                    // B load, SFU) before group g's recurrence runs, so their latency overlaps it.
+                    // B load, SFU) while group g's recurrence runs, so their latency overlaps it; the
+                    // source interleaves them state pair by state pair (two decays on the SFU beside
+                    // two FMA-pipe updates; about 1% faster than issuing them as one block first).
                     float2 an[LPC][QPL][2], bn[LPC][QPL][2];
+                    // Δ and Δ·u of step kk of group g (dxq: the group's pairs when DXS)
+                    auto step_in = [&](int g, int kk, const float4& dxq, float& dk, float& uk) {
+                        if constexpr (LPC == 1) {
+                            dk = dd[g];
+                            uk = du[g];
+                        } else if constexpr (Cfg::DXS) {
+                            dk = kk == 0 ? dxq.x : dxq.z;
+                            uk = kk == 0 ? dxq.y : dxq.w;
+                        } else {
+                            dk = __shfl_sync(0xffffffffu, dd[g], kk * CPW + c);
+                            uk = __shfl_sync(0xffffffffu, du[g], kk * CPW + c);
+                        }
+                    };
                     auto prep = [&](int g, float2 (&a)[LPC][QPL][2], float2 (&bb)[LPC][QPL][2]) {
                         float4 dxq = make_float4(0.f, 0.f, 0.f, 0.f);
                         if constexpr (Cfg::DXS) dxq = *reinterpret_cast<const float4*>(dxrow + g * LPC);
 #pragma unroll
                         for (int kk = 0; kk < LPC; ++kk) {
                             float dk, uk;
-                            if constexpr (LPC == 1) {
-                                dk = dd[g];
-                                uk = du[g];
-                            } else if constexpr (Cfg::DXS) {
-                                dk = kk == 0 ? dxq.x : dxq.z;
-                                uk = kk == 0 ? dxq.y : dxq.w;
-                            } else {
-                                dk = __shfl_sync(0xffffffffu, dd[g], kk * CPW + c);
-                                uk = __shfl_sync(0xffffffffu, du[g], kk * CPW + c);
-                            }
+                            step_in(g, kk, dxq, dk, uk);
                             const float2 dl2 = make_float2(dk, dk), du2 = make_float2(uk, uk);
                             const float* rowB = tB + ((g0 + g) * LPC + kk) * NS + n0;
 #pragma unroll
@@ -652,10 +658,39 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                                 ac[kk][qq][0] = an[kk][qq][0]; ac[kk][qq][1] = an[kk][qq][1];
                                 bc[kk][qq][0] = bn[kk][qq][0]; bc[kk][qq][1] = bn[kk][qq][1];
                             }
-                        if (g + 1 < G) prep(g + 1, an, bn);
                         float yp[LPC];
+                        if constexpr (LPC == 1) {
+                            // one step per group: the next group's inputs as one block first
+                            // (interleaving them costs this register-heavy layout spills)
+                            if (g + 1 < G) prep(g + 1, an, bn);
+                            const float* rowC = tC + (g0 + g) * NS + n0;
+                            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int qq = 0; qq < QPL; ++qq) {
+                                float4 C4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                                if constexpr (LTI)
+                                    C4 = cL[qq];
+                                else if constexpr (!SO)
+                                    C4 = *reinterpret_cast<const float4*>(rowC + 4 * qq);
+                                h[qq][0] = fma2(ac[0][qq][0], h[qq][0], bc[0][qq][0]);
+                                h[qq][1] = fma2(ac[0][qq][1], h[qq][1], bc[0][qq][1]);
+                                if constexpr (!SO) {
+                                    acc = fma2(make_float2(C4.x, C4.y), h[qq][0], acc);
+                                    acc = fma2(make_float2(C4.z, C4.w), h[qq][1], acc);
+                                }
+                            }
+                            yp[0] = acc.x + acc.y;
+                        } else {
+                        const bool more = g + 1 < G;
+                        const int gn = more ? g + 1 : g;
+                        float4 dxq = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if constexpr (Cfg::DXS) dxq = *reinterpret_cast<const float4*>(dxrow + gn * LPC);
 #pragma unroll
                         for (int kk = 0; kk < LPC; ++kk) {
+                            float dk = 0.f, uk = 0.f;
+                            if (more) step_in(gn, kk, dxq, dk, uk);
+                            const float2 dl2 = make_float2(dk, dk), du2 = make_float2(uk, uk);
+                            const float* rowB = tB + ((g0 + gn) * LPC + kk) * NS + n0;
                             const float* rowC = tC + ((g0 + g) * LPC + kk) * NS + n0;
                             float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
@@ -665,14 +700,21 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                                     C4 = cL[qq];
                                 else if constexpr (!SO)
                                     C4 = *reinterpret_cast<const float4*>(rowC + 4 * qq);
+                                float4 B4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                                if (more) B4 = LTI ? bL[qq] : *reinterpret_cast<const float4*>(rowB + 4 * qq);
+                                if (more) an[kk][qq][0] = ex2x2(mul2(dl2, A2[qq][0]));
                                 h[qq][0] = fma2(ac[kk][qq][0], h[qq][0], bc[kk][qq][0]);
+                                if constexpr (!SO) acc = fma2(make_float2(C4.x, C4.y), h[qq][0], acc);
+                                if (more) an[kk][qq][1] = ex2x2(mul2(dl2, A2[qq][1]));
                                 h[qq][1] = fma2(ac[kk][qq][1], h[qq][1], bc[kk][qq][1]);
-                                if constexpr (!SO) {
-                                    acc = fma2(make_float2(C4.x, C4.y), h[qq][0], acc);
-                                    acc = fma2(make_float2(C4.z, C4.w), h[qq][1], acc);
+                                if constexpr (!SO) acc = fma2(make_float2(C4.z, C4.w), h[qq][1], acc);
+                                if (more) {
+                                    bn[kk][qq][0] = mul2(du2, make_float2(B4.x, B4.y));
+                                    bn[kk][qq][1] = mul2(du2, make_float2(B4.z, B4.w));
                                 }
                             }
                             yp[kk] = acc.x + acc.y;
+                        }
                         }
                         if constexpr (SO) {
                             (void)yp;
