@@ -105,7 +105,8 @@ def max_sm_mhz(clocks=None) -> tuple:
 
 class PipePeaks:
     """Arithmetic peaks of this GPU: the library's pipe probe (ss__pipe_probe: one CTA per SM,
-    independent chains, SM cycle counter) gives results per clock per SM for ex2 and fp32 FMA;
+    independent chains, SM cycle counter) gives results per clock per SM for ex2, rcp, lg2 and
+    fp32 FMA;
     the SM count comes from the device properties and the clock from max_sm_mhz()."""
 
     def __init__(self, ss, torch, dev):
@@ -115,14 +116,17 @@ class PipePeaks:
         fn.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
         self.sms = torch.cuda.get_device_properties(dev).multi_processor_count
         self.per_clk = {}
-        for name in ("ex2", "ffma"):
+        for name in ("ex2", "rcp", "lg2", "ffma"):
             r = ctypes.c_double(0.0)
             if fn(PROBE_KINDS[name], 4096, ctypes.byref(r)) != 0:
                 raise RuntimeError(f"pipe probe {name} failed")
             self.per_clk[name] = r.value
 
     def ex2_per_s(self, clocks=None) -> float:
-        return self.sms * self.per_clk["ex2"] * max_sm_mhz(clocks)[0] * 1e6
+        return self.per_s("ex2", clocks)
+
+    def per_s(self, op: str, clocks=None) -> float:
+        return self.sms * self.per_clk[op] * max_sm_mhz(clocks)[0] * 1e6
 
     def ffma_per_s(self, clocks=None) -> float:
         return self.sms * self.per_clk["ffma"] * max_sm_mhz(clocks)[0] * 1e6
@@ -160,6 +164,14 @@ def decay_ex2_per_step(w) -> int:
     return updates_per_step(w)
 
 
+def transcendentals_per_step(w) -> dict:
+    """The method's full count of transcendentals: per (b, t, d) the N decays, softplus as
+    exp and log (log1p(e^x)) and the gate's sigmoid as exp and reciprocal, i.e.
+    B·L·Dm·(N+2) exp2, B·L·Dm log2 and B·L·Dm reciprocals."""
+    rows = updates_per_step(w) // w.N
+    return {"ex2": rows * (w.N + 2), "lg2": rows, "rcp": rows}
+
+
 # Sources each timed kernel's code and launch configuration come from: a traffic figure
 # measured on other sources is stale.
 _COMMON_SOURCES = ("device_common.cuh", "fwd_params.h", "internal.h", "fwd_configs.h", "selscan_api.cu")
@@ -170,6 +182,7 @@ KERNEL_SOURCES = {
     "ss_fwd_seg_kernel": _COMMON_SOURCES + ("ss_fwd_seg.cuh", "fwd_seg.cu", "fwd_launch_common.cuh"),
     "ss_step_kernel": _COMMON_SOURCES + ("ss_step.cu",),
     "ss_step_layers_kernel": _COMMON_SOURCES + ("ss_step.cu",),
+    "ss_step_layers_staged_kernel": _COMMON_SOURCES + ("ss_step.cu",),
     "ss_conv1d_kernel": ("device_common.cuh", "host_util.h", "ss_conv1d.cu"),
     "ss_bwd_kernel": ("device_common.cuh", "host_util.h", "ss_bwd.cu"),
 }
@@ -402,8 +415,12 @@ def run_ours(args, w, rank, world, local_rank):
     if err:
         raise RuntimeError(f"device error word {err:#x} after the timed region")
     if decode:
-        kernel, launches = (("ss_step_kernel", DECODE_LAYERS) if args.decode_per_layer
-                            else ("ss_step_layers_kernel", 1))
+        # the library reports which decode kernel the last call launched: the staged one wherever
+        # the buffers allow it (per layer too, as a table of one layer), else the per-block ones
+        staged = ss.lib().ss__last_step_path() == 1
+        kernel = ("ss_step_layers_staged_kernel" if staged else
+                  "ss_step_kernel" if args.decode_per_layer else "ss_step_layers_kernel")
+        launches = DECODE_LAYERS if args.decode_per_layer else 1
     else:
         plan = ss.lib().ss__fwd_plan
         plan.restype = ctypes.c_int
@@ -824,6 +841,12 @@ def main():
     if not w.name.startswith("decode") and res["launches"] > 1:
         roof["launch_ms_is"] = ("per step: " + str(res["launches"]) + " launches (the time split's passes and/or "
                                 "the widening of bf16 B and C to fp32, about 1 us, before the scan)")
+    per = per_step_launches if w.name.startswith("decode") else 1
+    tr = {k: v / per for k, v in transcendentals_per_step(w).items()}
+    # every transcendental at the probe's measured rate of its own operation (rcp and lg2 run at
+    # half the ex2 rate): the SFU time of the whole op mix, against t_sfu's decays alone
+    t_sfu_all = sum(tr[k] / res["peaks"].per_s(k, res["clocks"]) for k in tr)
+    roof.update({"transcendentals_per_launch": tr, "t_sfu_all_us": t_sfu_all * 1e6})
     roof.update({"traffic": measured_traffic(w.name, res["kernel"]), "kernel": res["kernel"],
                  "launch_ms": launch_ms, "alg_bytes_per_launch": bytes_launch,
                  "decay_ex2_per_launch": ex2_launch, "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6})

@@ -93,6 +93,7 @@ struct StepLayerPtrs {
 };
 struct StepLayersParams {
     StepParams common;
+    unsigned int* err;   // device error word (the staged kernel's bounded waits)
     int n_layers;
     StepLayerPtrs layer[kStepMaxLayers];
 };

@@ -1158,6 +1158,7 @@ ss_status ss_step_layers(const ss_step_layer* layers, int64_t n_layers, int64_t 
     StepLayersParams q;
     std::memset(&q, 0, sizeof(q));
     q.n_layers = static_cast<int>(n_layers);
+    q.err = device_error_ptr();
     std::vector<StepCheck> cs;
     cs.reserve(static_cast<size_t>(n_layers));
     bool vec = true;

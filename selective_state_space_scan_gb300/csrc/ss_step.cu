@@ -12,6 +12,10 @@
 // 32-bit division per block, none per element.
 // exp(A_log) is taken on the SFU (2^(A_log·log2 e)); its relative error (~1e-7) moves the
 // decay exponent by as much, far below the fp32 tolerance.
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+
 #include "device_common.cuh"
 #include "fwd_params.h"
 #include "internal.h"
@@ -47,15 +51,26 @@ template <> struct Vec4<__nv_bfloat16> {
 
 // One row's decode update with the state already loaded (VEC path): returns this lane's C·h
 // partial sum and writes the new state back.
-__device__ __forceinline__ float step_quad(float4& hv, const float4& av, const float4& Bv,
-                                           const float4& Cv, float dlt, float dx) {
+// exp(A_log) of a quad (-A), on the SFU.
+__device__ __forceinline__ float4 exp_quad(const float4& av) {
+    return make_float4(ex2(av.x * kLog2e), ex2(av.y * kLog2e), ex2(av.z * kLog2e), ex2(av.w * kLog2e));
+}
+
+// The same with exp(A_log) already taken (ae = exp_quad(A_log quad)).
+__device__ __forceinline__ float step_quad_e(float4& hv, const float4& ae, const float4& Bv,
+                                             const float4& Cv, float dlt, float dx) {
     const float k = -dlt * kLog2e;
-    const float h0 = fmaf(ex2(k * ex2(av.x * kLog2e)), hv.x, dx * Bv.x);
-    const float h1 = fmaf(ex2(k * ex2(av.y * kLog2e)), hv.y, dx * Bv.y);
-    const float h2 = fmaf(ex2(k * ex2(av.z * kLog2e)), hv.z, dx * Bv.z);
-    const float h3 = fmaf(ex2(k * ex2(av.w * kLog2e)), hv.w, dx * Bv.w);
+    const float h0 = fmaf(ex2(k * ae.x), hv.x, dx * Bv.x);
+    const float h1 = fmaf(ex2(k * ae.y), hv.y, dx * Bv.y);
+    const float h2 = fmaf(ex2(k * ae.z), hv.z, dx * Bv.z);
+    const float h3 = fmaf(ex2(k * ae.w), hv.w, dx * Bv.w);
     hv = make_float4(h0, h1, h2, h3);
     return fmaf(Cv.x, h0, fmaf(Cv.y, h1, fmaf(Cv.z, h2, Cv.w * h3)));
+}
+
+__device__ __forceinline__ float step_quad(float4& hv, const float4& av, const float4& Bv,
+                                           const float4& Cv, float dlt, float dx) {
+    return step_quad_e(hv, exp_quad(av), Bv, Cv, dlt, dx);
 }
 
 
@@ -182,6 +197,153 @@ __global__ void __launch_bounds__(THREADS, SS_STEPL_MINB) ss_step_layers_kernel(
     step_block<TIO, LPR, RPT, VEC, THREADS>(p, static_cast<int>(blockIdx.x) - layer * per_layer, per_b);
 }
 
+// ---- Staged many-layer step (16 states, rows of whole 16-byte units) ----
+// The rows of all layers form one sequence of units of kSlRows rows, ordered (layer, row block,
+// batch row), split into equal contiguous ranges, one per warp of a persistent grid.  Each warp
+// streams its range through its own ring of kSlStages shared-memory stages: one lane issues a
+// unit's bulk copies (the state rows, x, Δ, z and the batch row's B and C) on the stage's
+// mbarrier kSlStages - 1 units ahead, so that several units of every warp are in flight while it
+// computes; the lanes then update the unit's rows in four passes of eight rows (four lanes of
+// four states a row, the arithmetic of step_quad) and write the state back with 16-byte stores.
+// Consecutive units of a warp share their row block, so exp(A_log), bias and D of the warp's
+// rows stay in registers across the batch rows (reloaded when the block changes), and a stage
+// holds only what changes with the batch row.  No block barrier: the warps run independently.
+constexpr int kSlRows = 32;
+#ifndef SS_STEPL_STAGES
+#define SS_STEPL_STAGES 4
+#endif
+constexpr int kSlStages = SS_STEPL_STAGES;
+#ifndef SS_STEPL_WARPS
+#define SS_STEPL_WARPS 4
+#endif
+constexpr int kSlWarps = SS_STEPL_WARPS;
+
+template <typename TIO>
+struct SlStage {
+    static constexpr int ES = static_cast<int>(sizeof(TIO));
+    static constexpr int H = 0;                              // [32][16] fp32 state rows
+    static constexpr int X = H + kSlRows * 16 * 4;           // [32] x
+    static constexpr int DL = X + kSlRows * ES;              // [32] delta_raw
+    static constexpr int Z = DL + kSlRows * ES;              // [32] z
+    static constexpr int BR = Z + kSlRows * ES;              // [16] B of the batch row
+    static constexpr int CR = BR + 16 * ES;                  // [16] C of the batch row
+    static constexpr int BYTES = (CR + 16 * ES + 127) / 128 * 128;
+    static constexpr int RING = kSlStages * BYTES;
+    static constexpr int SMEM = kSlWarps * RING + kSlWarps * kSlStages * 8 + kSlWarps * 4;
+    static_assert(X % 16 == 0 && DL % 16 == 0 && Z % 16 == 0 && BR % 16 == 0 && CR % 16 == 0,
+                  "bulk copy destinations are 16-byte aligned");
+};
+
+template <typename TIO>
+__global__ void __launch_bounds__(kSlWarps * 32) ss_step_layers_staged_kernel(const __grid_constant__ StepLayersParams q) {
+    using St = SlStage<TIO>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t* ring = smem + warp * St::RING;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSlWarps * St::RING) + warp * kSlStages;
+    volatile int* abort_flag =
+        reinterpret_cast<volatile int*>(smem + kSlWarps * St::RING + kSlWarps * kSlStages * 8) + warp;
+    const StepParams& c = q.common;
+    const int per_blk = c.batch;                             // units of one row block
+    const int64_t per_layer = static_cast<int64_t>(c.Dm / kSlRows) * per_blk;
+    const int64_t U = per_layer * q.n_layers;
+    const int64_t wid = static_cast<int64_t>(blockIdx.x) * kSlWarps + warp;
+    const int64_t nw = static_cast<int64_t>(gridDim.x) * kSlWarps;
+    const int64_t u0 = U * wid / nw, u1 = U * (wid + 1) / nw;
+    if (lane == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < kSlStages; ++s) mbar_init(&bars[s], 1);
+        mbar_fence_init();
+    }
+    __syncwarp();
+    auto where = [&](int64_t u, int& layer, int& b, int& d0) {
+        layer = static_cast<int>(u / per_layer);
+        const int64_t rem = u - layer * per_layer;
+        const int blk = static_cast<int>(rem / per_blk);
+        b = static_cast<int>(rem - static_cast<int64_t>(blk) * per_blk);
+        d0 = blk * kSlRows;
+    };
+    auto issue = [&](int64_t u, int s) {                     // lane 0
+        int layer, b, d0;
+        where(u, layer, b, d0);
+        const StepLayerPtrs& L = q.layer[layer];
+        uint8_t* st = ring + s * St::BYTES;
+        const uint32_t rows_x = kSlRows * St::ES;
+        const uint32_t bytes = kSlRows * 64u + 2u * rows_x + (L.z ? rows_x : 0u) + 2u * 16u * St::ES;
+        mbar_expect_tx(&bars[s], bytes);
+        bulk_load(st + St::H, L.state + static_cast<int64_t>(b) * c.s_b + static_cast<int64_t>(d0) * 16,
+                  kSlRows * 64, &bars[s]);
+        bulk_load(st + St::X, static_cast<const TIO*>(L.x) + static_cast<int64_t>(b) * c.x_b + d0, rows_x, &bars[s]);
+        bulk_load(st + St::DL, static_cast<const TIO*>(L.delta) + static_cast<int64_t>(b) * c.d_b + d0, rows_x,
+                  &bars[s]);
+        if (L.z)
+            bulk_load(st + St::Z, static_cast<const TIO*>(L.z) + static_cast<int64_t>(b) * c.z_b + d0, rows_x,
+                      &bars[s]);
+        bulk_load(st + St::BR, static_cast<const TIO*>(L.Bm) + static_cast<int64_t>(b) * c.B_b, 16 * St::ES, &bars[s]);
+        bulk_load(st + St::CR, static_cast<const TIO*>(L.Cm) + static_cast<int64_t>(b) * c.C_b, 16 * St::ES, &bars[s]);
+    };
+    if (lane == 0)
+        for (int k = 0; k < kSlStages && u0 + k < u1; ++k) issue(u0 + k, k);
+    constexpr int PASSES = kSlRows / 8;
+    const int qd = lane & 3, n0 = qd * 4;
+    int cur_layer = -1, cur_d0 = -1;
+    float4 ae[PASSES];                                       // exp(A_log) of this lane's quad of its rows
+    float bias_r[PASSES], D_r[PASSES];
+    int64_t k = 0;
+    for (int64_t u = u0; u < u1; ++u, ++k) {
+        const int s = static_cast<int>(k % kSlStages);
+        int layer, b, d0;
+        where(u, layer, b, d0);
+        const StepLayerPtrs& L = q.layer[layer];
+        if (layer != cur_layer || d0 != cur_d0) {            // a new row block: its parameters
+            cur_layer = layer;
+            cur_d0 = d0;
+#pragma unroll
+            for (int pass = 0; pass < PASSES; ++pass) {
+                const int d = d0 + pass * 8 + (lane >> 2);
+                ae[pass] = exp_quad(*reinterpret_cast<const float4*>(L.A_log + static_cast<int64_t>(d) * 16 + n0));
+                bias_r[pass] = L.bias ? L.bias[d] : 0.f;
+                D_r[pass] = L.Dv ? L.Dv[d] : 0.f;
+            }
+        }
+        // every lane waits (a bounded wait: one lane's timeout raises the warp's abort flag, so
+        // the others return too); the warp then leaves together or goes on together
+        const bool got = mbar_wait_bounded(&bars[s], static_cast<uint32_t>((k / kSlStages) & 1), abort_flag, q.err);
+        if (!__all_sync(0xffffffffu, got)) break;
+        const uint8_t* st = ring + s * St::BYTES;
+        const TIO* sx = reinterpret_cast<const TIO*>(st + St::X);
+        const TIO* sdl = reinterpret_cast<const TIO*>(st + St::DL);
+        const TIO* sz = reinterpret_cast<const TIO*>(st + St::Z);
+        const float4 Bv = Vec4<TIO>::get(*reinterpret_cast<const typename Vec4<TIO>::T*>(st + St::BR + n0 * St::ES));
+        const float4 Cv = Vec4<TIO>::get(*reinterpret_cast<const typename Vec4<TIO>::T*>(st + St::CR + n0 * St::ES));
+        float* hrow = L.state + static_cast<int64_t>(b) * c.s_b;
+        TIO* yrow = static_cast<TIO*>(L.y) + static_cast<int64_t>(b) * c.y_b;
+#pragma unroll
+        for (int pass = 0; pass < PASSES; ++pass) {
+            const int r = pass * 8 + (lane >> 2);
+            const int d = d0 + r;
+            float4 hv = *reinterpret_cast<const float4*>(st + St::H + r * 64 + qd * 16);
+            const float xv = to_f32<TIO>(sx[r]);
+            const float dv = to_f32<TIO>(sdl[r]) + bias_r[pass];
+            const float dlt = softplus(dv);
+            float partial = step_quad_e(hv, ae[pass], Bv, Cv, dlt, dlt * xv);
+            *reinterpret_cast<float4*>(hrow + static_cast<int64_t>(d) * 16 + n0) = hv;
+            partial += __shfl_xor_sync(0xffffffffu, partial, 1);
+            partial += __shfl_xor_sync(0xffffffffu, partial, 2);
+            if (qd == 0) {
+                float v = fmaf(D_r[pass], xv, partial);
+                if (L.z) v *= silu(to_f32<TIO>(sz[r]));
+                yrow[d] = from_f32<TIO>(v);
+            }
+        }
+        __syncwarp();                                        // every lane is done with stage s
+        if (lane == 0 && u + kSlStages < u1) {
+            tma_store_fence();                               // generic reads before the async refill
+            issue(u + kSlStages, s);
+        }
+    }
+}
+
 template <typename TIO, int LPR, int THREADS, int RPT>
 static cudaError_t launch_step_layers_s(const StepLayersParams& q, bool vec, cudaStream_t stream) {
     constexpr int rows_block = (THREADS / LPR) * RPT;
@@ -235,14 +397,94 @@ static cudaError_t launch_step_dtype(const StepParams& p, bool vec, cudaStream_t
     return launch_step_t<TIO, 4>(p, vec, stream);
 }
 
+
+
+// Test hook (ss_step and ss_step_layers): -1 automatic, 0 the per-block kernels, 1 the staged
+// kernel (refused when it cannot be used).
+static std::atomic<int> g_force_step_layers{-1};
+// Which kernel the last ss_step or ss_step_layers call launched (0 per-block, 1 staged), for the
+// benchmark's report.
+static std::atomic<int> g_last_step_path{-1};
+
+// Whether every layer's buffers suit the staged kernel: 16 states in rows of 64 bytes, row blocks
+// of whole units, and every bulk-copied range (state rows, x, Δ, z, B and C rows) starting on a
+// 16-byte boundary; A_log (16-byte rows), bias and D are read with plain loads.
+static bool step_layers_staged_ok(const StepLayersParams& q, bool bf16) {
+    const StepParams& c = q.common;
+    const int64_t es = bf16 ? 2 : 4;
+    if (c.N != 16 || c.s_d != 16 || c.Dm % kSlRows != 0) return false;
+    if ((c.s_b * 4) % 16 || (c.x_b * es) % 16 || (c.d_b * es) % 16 || (c.z_b * es) % 16 || (c.B_b * es) % 16 ||
+        (c.C_b * es) % 16)
+        return false;
+    auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    for (int l = 0; l < q.n_layers; ++l) {
+        const StepLayerPtrs& L = q.layer[l];
+        if (!al(L.state) || !al(L.A_log) || !al(L.x) || !al(L.delta) || (L.z && !al(L.z)) || !al(L.Bm) || !al(L.Cm))
+            return false;
+    }
+    return true;
+}
+
+template <typename TIO>
+static cudaError_t launch_step_layers_staged(const StepLayersParams& q, cudaStream_t stream) {
+    using St = SlStage<TIO>;
+    auto kern = ss_step_layers_staged_kernel<TIO>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, St::SMEM);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSlWarps * 32, St::SMEM)) != cudaSuccess)
+        return e;
+    const int64_t units = static_cast<int64_t>(q.n_layers) * q.common.batch * (q.common.Dm / kSlRows);
+    const int64_t blocks = std::min<int64_t>(static_cast<int64_t>(std::max(per_sm, 1)) * sms,
+                                             (units + kSlWarps - 1) / kSlWarps);
+    if (blocks <= 0) return cudaSuccess;
+    kern<<<static_cast<unsigned>(blocks), kSlWarps * 32, St::SMEM, stream>>>(q);
+    return cudaGetLastError();
+}
+
+// One layer's step: the staged kernel over a table of one layer where it applies.
 cudaError_t launch_step(const StepParams& p, bool bf16, bool vec, cudaStream_t stream) {
+    const int force = g_force_step_layers.load();
+    if (vec && force != 0) {
+        StepLayersParams q;
+        std::memset(&q, 0, sizeof(q));
+        q.common = p;
+        q.err = device_error_word();
+        q.n_layers = 1;
+        q.layer[0] = StepLayerPtrs{p.state, p.x, p.delta, p.z, p.Bm, p.Cm, p.bias, p.A_log, p.Dv, p.y};
+        if (step_layers_staged_ok(q, bf16)) {
+            g_last_step_path.store(1);
+            return bf16 ? launch_step_layers_staged<__nv_bfloat16>(q, stream) : launch_step_layers_staged<float>(q, stream);
+        }
+    }
+    if (force == 1) return cudaErrorInvalidValue;
+    g_last_step_path.store(0);
     return bf16 ? launch_step_dtype<__nv_bfloat16>(p, vec, stream)
                 : launch_step_dtype<float>(p, vec, stream);
 }
 
 cudaError_t launch_step_layers(const StepLayersParams& q, bool bf16, bool vec, cudaStream_t stream) {
+    const int force = g_force_step_layers.load();
+    const bool ok = vec && step_layers_staged_ok(q, bf16);
+    if (force == 1 && !ok) return cudaErrorInvalidValue;
+    if (ok && force != 0) {
+        g_last_step_path.store(1);
+        return bf16 ? launch_step_layers_staged<__nv_bfloat16>(q, stream) : launch_step_layers_staged<float>(q, stream);
+    }
+    g_last_step_path.store(0);
     return bf16 ? launch_step_layers_dtype<__nv_bfloat16>(q, vec, stream)
                 : launch_step_layers_dtype<float>(q, vec, stream);
 }
+
+}  // namespace selscan
+
+extern "C" int ss__force_step_layers_path(int v) {
+    return selscan::g_force_step_layers.exchange(v < 0 ? -1 : v > 0 ? 1 : 0);
+}
+extern "C" int ss__last_step_path() { return selscan::g_last_step_path.load(); }
+
+namespace selscan {
 
 }  // namespace selscan

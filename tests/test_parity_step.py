@@ -1,5 +1,7 @@
 """Parity of the CUDA decode step (through the C ABI) with the fp64 oracle, and the
 decode == scan identities between the two entry points."""
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -180,3 +182,84 @@ def test_step_layers_rejects_shared_outputs_and_too_many_layers():
     with pytest.raises(ss.SelscanError):
         ss.ss_step_layers(many)
     assert ss.ss_step_layers([]) == []
+
+
+def _force_layers_path(v):
+    f = ss.lib().ss__force_step_layers_path
+    f.argtypes = [ctypes.c_int]
+    f.restype = ctypes.c_int
+    return f(v)
+
+
+def _layers_run(ws, path):
+    """ss_step_layers over the layers of `ws` on a forced kernel (0 per-block, 1 staged)."""
+    batched = [_layer_tensors(w) for w in ws]
+    _force_layers_path(path)
+    try:
+        ys = ss.ss_step_layers(batched)
+        torch.cuda.synchronize()
+    finally:
+        _force_layers_path(-1)
+    return [to_host(y) for y in ys], [to_host(L["state"]) for L in batched]
+
+
+def test_step_layers_staged_equals_block_kernel_on_decode_workload():
+    """The staged kernel (each warp's contiguous range of 32-row units streamed through its own
+    ring of bulk-copied stages) computes every row with the per-block kernel's arithmetic: the
+    same y and states bit for bit on 12 layers of the decode workload, and the oracle's."""
+    ws = [synth.step_inputs(64, 4096, 16, seed=4, layer=layer) for layer in range(12)]
+    y1, s1 = _layers_run(ws, 1)
+    y0, s0 = _layers_run(ws, 0)
+    for w, a, b, sa, sb in zip(ws, y1, y0, s1, s0):
+        np.testing.assert_array_equal(a, b)
+        np.testing.assert_array_equal(sa, sb)
+    for w, y, st in list(zip(ws, y1, s1))[:3]:
+        ry, rst, mag = oracle_step(w)
+        assert_fwd_close("f32", y, ry, mag, st, rst, what=f"staged {w.name}")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("opts", [dict(with_z=True, with_bias=True), dict(with_z=False, with_bias=False)])
+def test_step_layers_staged_ranges_cross_layers_and_rows(io, opts):
+    """7 layers of batch 5 and 96 channels (three 32-row units a batch row, one unit a warp;
+    the decode-workload test above gives each warp a range of about 50 units across batch rows
+    and layers), with and without the gate and the bias, and without D on some layers."""
+    ws = [synth.step_inputs(5, 96, 16, io=io, seed=80 + k, **opts) for k in range(7)]
+    for k in (1, 4):
+        ws[k].arrays["D"] = None
+    y1, s1 = _layers_run(ws, 1)
+    for w, y, st in zip(ws, y1, s1):
+        ry, rst, mag = oracle_step(w)
+        assert_fwd_close(io, y, ry, mag, st, rst, what=f"staged ragged {io} {opts}")
+    y0, s0 = _layers_run(ws, 0)
+    for a, b, sa, sb in zip(y1, y0, s1, s0):
+        np.testing.assert_array_equal(a, b)
+        np.testing.assert_array_equal(sa, sb)
+
+
+def test_step_layers_staged_refused_where_it_cannot_run():
+    """Channels that are not whole 32-row units, or 8 states: the staged kernel is refused when
+    forced (no silent substitute), and the automatic choice runs the per-block kernel."""
+    for Dm, N in ((77, 16), (64, 8)):
+        ws = [synth.step_inputs(3, Dm, N, seed=90 + Dm, with_bias=True) for _ in range(2)]
+        with pytest.raises(ss.SelscanError):
+            _layers_run(ws, 1)
+        ys, sts = _layers_run(ws, -1)
+        for w, y, st in zip(ws, ys, sts):
+            ry, rst, mag = oracle_step(w)
+            assert_fwd_close("f32", y, ry, mag, st, rst, what=f"auto Dm={Dm} N={N}")
+
+
+def test_step_single_layer_staged_equals_block_kernel():
+    """ss_step on one layer of the decode workload takes the staged kernel too (a table of one
+    layer): bit for bit the per-block kernel's y and state."""
+    w = synth.step_inputs(64, 4096, 16, seed=4, layer=7)
+    out = {}
+    for path in (1, 0):
+        _force_layers_path(path)
+        try:
+            out[path] = gpu_step(w)
+        finally:
+            _force_layers_path(-1)
+    np.testing.assert_array_equal(out[1][0], out[0][0])
+    np.testing.assert_array_equal(to_host(out[1][1]), to_host(out[0][1]))
