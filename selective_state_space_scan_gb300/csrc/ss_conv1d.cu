@@ -9,13 +9,15 @@
 // The stage is a stream (4 multiply-adds per element against 8 bytes moved for fp32), so the
 // kernel is laid out for bandwidth: a thread owns 4 adjacent channels (one 16-byte fp32 or
 // 8-byte bf16 access per step, a warp covering 128 channels = 512 contiguous bytes) and a
-// segment of kSeg steps; the three samples before the segment come from x itself (or, for the
+// segment of seg steps (chosen per call so that the grid is whole waves of resident blocks); the three samples before the segment come from x itself (or, for the
 // first segment, from the window), and kUnroll steps of loads are issued before their
 // arithmetic.  The thread of a row's first segment is the only one that reads window_in and
 // the only one that writes window_out (taking the last three samples from x), so the window
 // may be updated in place.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -27,7 +29,11 @@ namespace selscan {
 namespace {
 
 constexpr int kConvK = SS_CONV_WIDTH;   // 4
-constexpr int kSeg = 32;                // steps per thread (measured 10% faster than 64 or 16)
+// Steps per thread: chosen per call (segment_steps) so that the grid fills whole waves of
+// resident blocks; at least kSegMin, so that the three samples re-read before each segment stay
+// a small part of its loads.
+constexpr int kSegMin = 16;
+constexpr int kSegMax = 128;
 constexpr int kUnroll = 8;              // steps whose loads are issued together
 constexpr int kThreads = 128;           // 512 channels per block
 
@@ -41,6 +47,7 @@ struct ConvParams {
     int64_t x_b, x_l, o_b, o_l;
     int batch, L, Dm;
     int silu;
+    int seg;                // steps per thread
 };
 
 template <typename TIO> struct Quad;
@@ -75,8 +82,8 @@ __global__ void __launch_bounds__(kThreads) ss_conv1d_kernel(const ConvParams p)
     const int seg = static_cast<int>(blockIdx.x) / nbd, b = blockIdx.y;
     const int d0 = ((static_cast<int>(blockIdx.x) - seg * nbd) * kThreads + threadIdx.x) * 4;
     if (d0 >= p.Dm) return;
-    const int t0 = seg * kSeg;
-    const int nt = min(kSeg, p.L - t0);
+    const int t0 = seg * p.seg;
+    const int nt = min(p.seg, p.L - t0);
     const TIO* x = static_cast<const TIO*>(p.x) + static_cast<int64_t>(b) * p.x_b;
     TIO* out = static_cast<TIO*>(p.out) + static_cast<int64_t>(b) * p.o_b;
     const int nc = min(4, p.Dm - d0);           // channels this thread owns (4 on the VEC path)
@@ -187,6 +194,27 @@ __global__ void __launch_bounds__(kThreads) ss_conv1d_kernel(const ConvParams p)
     }
 }
 
+// Steps per thread for a grid of batch x ceil(L / seg) x nbd blocks when `slots` blocks are
+// resident at once: the length whose whole waves take the least time, modelling a wave as
+// seg + 6 steps of one thread (the three re-read samples and the set-up).  On the 130m-shaped
+// input (8 x 2048 x 1536, 760 resident blocks) it picks 33 steps: 1512 blocks in two full waves
+// (38.8 us), where 32 steps gave 1536 blocks, two waves and 16 blocks more (42.9 us).
+int segment_steps(int64_t batch, int64_t L, int64_t nbd, int64_t slots) {
+    if (L <= kSegMin) return static_cast<int>(std::max<int64_t>(L, 1));
+    int best = kSegMin;
+    int64_t best_cost = -1;
+    for (int seg = kSegMin; seg <= kSegMax; ++seg) {
+        const int64_t blocks = batch * ((L + seg - 1) / seg) * nbd;
+        const int64_t waves = (blocks + slots - 1) / slots;
+        const int64_t cost = waves * (seg + 6);
+        if (best_cost < 0 || cost <= best_cost) {
+            best_cost = cost;
+            best = seg;
+        }
+    }
+    return best;
+}
+
 // Windows only (L == 0): window_out = window_in (or zeros).
 __global__ void ss_conv1d_window_copy(const float* win_in, float* win_out, int64_t n) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -198,6 +226,11 @@ __global__ void ss_conv1d_window_copy(const float* win_in, float* win_out, int64
 
 using namespace selscan;
 using namespace selscan::host;
+
+// Test hook: steps per thread, at least 3 (a later segment re-reads the three samples before it
+// from x); anything else restores the choice per call.  Returns the previous value.
+static std::atomic<int> g_force_conv_seg{0};
+extern "C" int ss__force_conv_segment(int steps) { return g_force_conv_seg.exchange(steps >= 3 ? steps : 0); }
 
 extern "C" ss_status ss_conv1d(const void* x, const float* weight, const float* bias, void* out,
                                const float* window_in, float* window_out, int64_t batch, int64_t L,
@@ -257,16 +290,18 @@ extern "C" ss_status ss_conv1d(const void* x, const float* weight, const float* 
     const int64_t va = 4 * es;   // quad access alignment
     const bool vec = Dm % 4 == 0 && is_aligned(x, va) && is_aligned(out, va) && (s.x_l * es) % va == 0 &&
                      (s.out_l * es) % va == 0 && (batch == 1 || ((s.x_b * es) % va == 0 && (s.out_b * es) % va == 0));
-    const int64_t segs = (L + kSeg - 1) / kSeg;
     const int64_t nbd = (Dm + 4 * kThreads - 1) / (4 * kThreads);
+    void (*kern)(ConvParams) = bf16 ? (vec ? ss_conv1d_kernel<__nv_bfloat16, true> : ss_conv1d_kernel<__nv_bfloat16, false>)
+                                    : (vec ? ss_conv1d_kernel<float, true> : ss_conv1d_kernel<float, false>);
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0) != cudaSuccess)
+        return SS_ERR_CUDA;
+    const int forced = g_force_conv_seg.load();
+    p.seg = forced > 0 ? forced : segment_steps(batch, L, nbd, static_cast<int64_t>(std::max(sms, 1)) * std::max(per_sm, 1));
+    const int64_t segs = (L + p.seg - 1) / p.seg;
     if (segs * nbd > INT32_MAX) return SS_ERR_UNSUPPORTED;
     const dim3 grid(static_cast<unsigned>(segs * nbd), static_cast<unsigned>(batch));   // x: (segment, channel block)
-    if (bf16) {
-        if (vec) ss_conv1d_kernel<__nv_bfloat16, true><<<grid, kThreads, 0, stream>>>(p);
-        else ss_conv1d_kernel<__nv_bfloat16, false><<<grid, kThreads, 0, stream>>>(p);
-    } else {
-        if (vec) ss_conv1d_kernel<float, true><<<grid, kThreads, 0, stream>>>(p);
-        else ss_conv1d_kernel<float, false><<<grid, kThreads, 0, stream>>>(p);
-    }
+    kern<<<grid, kThreads, 0, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }

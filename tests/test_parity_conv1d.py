@@ -164,3 +164,23 @@ def test_conv1d_rejects_overlap_and_misalignment():
     assert call(x.data_ptr() + 2, out.data_ptr()) == 3                  # misaligned x
     assert call(x.data_ptr(), out.data_ptr(), big.data_ptr(), big.data_ptr()) == 0       # in place
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("steps", [3, 7, 16, 41, 128, 300])
+def test_conv1d_segment_length_invariance(steps):
+    """The steps each thread takes (chosen per call to fill whole waves; forced here) change
+    nothing: the same outputs and window bit for bit, with and without the incoming window."""
+    f = ss.lib().ss__force_conv_segment
+    f.argtypes = [ctypes.c_int]
+    x, w, bias, win = inputs(20 + steps, 3, 1000, 608)
+    ref = run(x, w, bias, win, True)
+    f(steps)
+    try:
+        got = run(x, w, bias, win, True)
+        got0 = run(x, w, bias, None, False)
+    finally:
+        f(0)
+    np.testing.assert_array_equal(got[0], ref[0])
+    np.testing.assert_array_equal(got[1], ref[1])
+    check("f32", got[0], x, w, bias, win, True, f"segment {steps}", got[1])
+    check("f32", got0[0], x, w, bias, None, False, f"segment {steps} no window", got0[1])
