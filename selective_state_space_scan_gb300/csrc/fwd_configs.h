@@ -25,11 +25,7 @@ constexpr int kLaneUnrollSub = SS_UNROLL_SUB;
 #define SS_DEFER_REDUCE 1
 #endif
 constexpr bool kLaneDeferReduce = SS_DEFER_REDUCE != 0;
-// C·h partial sums in two accumulators (halving the dependent chain) or one.
-#ifndef SS_ACC2
-#define SS_ACC2 0
-#endif
-constexpr bool kLaneAcc2 = SS_ACC2 != 0;
+
 
 // Lane kernel options (compile-time, for measurement): the (Δ, Δ·u) hand-over at 2 lanes per
 // channel through shared memory instead of shuffles (fp32); softplus through the SFU's log2 for

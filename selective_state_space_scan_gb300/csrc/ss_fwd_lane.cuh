@@ -692,7 +692,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                             const float2 dl2 = make_float2(dk, dk), du2 = make_float2(uk, uk);
                             const float* rowB = tB + ((g0 + gn) * LPC + kk) * NS + n0;
                             const float* rowC = tC + ((g0 + g) * LPC + kk) * NS + n0;
-                            float2 acc = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+                            float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                             for (int qq = 0; qq < QPL; ++qq) {
                                 float4 C4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -707,18 +707,12 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                                 if constexpr (!SO) acc = fma2(make_float2(C4.x, C4.y), h[qq][0], acc);
                                 if (more) an[kk][qq][1] = ex2x2(mul2(dl2, A2[qq][1]));
                                 h[qq][1] = fma2(ac[kk][qq][1], h[qq][1], bc[kk][qq][1]);
-                                if constexpr (!SO) {
-                                    if constexpr (kLaneAcc2)
-                                        acc1 = fma2(make_float2(C4.z, C4.w), h[qq][1], acc1);
-                                    else
-                                        acc = fma2(make_float2(C4.z, C4.w), h[qq][1], acc);
-                                }
+                                if constexpr (!SO) acc = fma2(make_float2(C4.z, C4.w), h[qq][1], acc);
                                 if (more) {
                                     bn[kk][qq][0] = mul2(du2, make_float2(B4.x, B4.y));
                                     bn[kk][qq][1] = mul2(du2, make_float2(B4.z, B4.w));
                                 }
                             }
-                            if constexpr (kLaneAcc2) acc = add2(acc, acc1);
                             yp[kk] = acc.x + acc.y;
                         }
                         }
