@@ -26,7 +26,6 @@ constexpr int kLaneUnrollSub = SS_UNROLL_SUB;
 #endif
 constexpr bool kLaneDeferReduce = SS_DEFER_REDUCE != 0;
 
-
 // Lane kernel options (compile-time, for measurement): the (Δ, Δ·u) hand-over at 2 lanes per
 // channel through shared memory instead of shuffles (fp32); softplus through the SFU's log2 for
 // bf16 (742 -> 723 us on the 2.8b-shaped layer).
