@@ -229,10 +229,12 @@ ss_status ss_fwd_dtproj(const void* u, const void* dt_low, const float* W_dt, in
 
 /*
  * Forward pass on host-resident tensors: ss_fwd's result with the copies to and from the device
- * inside the call.  The batch rows are processed in groups (up to eight, one row each when the batch allows)
- * through two device staging slots on three internal streams, so that the copy in of one group,
- * the scan of another and the copy back of a third overlap.  No counterpart in the pages: it
- * serves callers whose tensors live in host memory.
+ * inside the call.  The work goes in units of a group of batch rows (up to eight groups, one row
+ * each when the batch allows) and a piece of the sequence (about 64 MB of inputs; each piece
+ * scanned from the state the previous piece of its rows left, as ss_fwd_h0 does), through two
+ * device staging slots on three internal streams, so that the copy in of one unit, the scan of
+ * another and the copy back of a third overlap.  The result equals one ss_fwd call up to
+ * rounding.  No counterpart in the pages: it serves callers whose tensors live in host memory.
  *   u, delta_raw, z, y   [batch, L, Dm] io_dtype, contiguous, HOST memory (pinned memory lets the
  *                        copies run asynchronously; pageable memory works but serialises them)
  *   B, C                 [batch, L, N] io_dtype, contiguous, host memory

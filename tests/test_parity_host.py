@@ -127,3 +127,20 @@ def test_host_rejects_device_pointers_and_small_workspace():
     assert call(h["u"].data_ptr(), need - 256) == 1           # workspace too small
     assert call(h["u"].data_ptr(), need) == 0
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("io,steps,batch", [("f32", 64, 9), ("bf16", 128, 3), ("f32", 1000, 2)])
+def test_host_sequence_pieces(io, steps, batch):
+    """The call cut into pieces of the sequence (forced here: 64 or 128 steps, against 300), each
+    piece scanned from the state the previous one left on the device; two-row groups (batch 9)
+    take strided copies.  With and without the gate and last_state."""
+    f = ss.lib().ss__force_host_steps
+    f.argtypes = [ctypes.c_int64]
+    f.restype = ctypes.c_int64
+    w = synth.fwd_inputs(batch, 300, 64, 16, io=io, seed=200 + steps + batch)
+    f(steps)
+    try:
+        check(w, w.arrays, f"pieces of {steps} steps {io}")
+        check(w, w.arrays, f"pieces of {steps} steps, no gate, no last_state", gate=False, with_last=False)
+    finally:
+        f(0)
