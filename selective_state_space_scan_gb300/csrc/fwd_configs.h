@@ -49,10 +49,12 @@ constexpr int lane_minb(int lpc, int w) {
 // which still lets five reside (126 before: 674 -> 667 us on the 2.8b-shaped layer).
 constexpr int lane_minb_bcf32(int lpc, int w) { return lpc == 2 && w == 32 ? 4 : lane_minb(lpc, w); }
 // Tile width: 32 channels for one CTA per tile.  The balanced schedule needs at least as many
-// tiles as SMs times resident CTAs, so its fp32 tiles are 16 channels (64-byte rows); its bf16
-// tiles stay at 32 (64-byte rows too: narrower rows would have each 64-byte DRAM access read by
-// two CTAs at different times, which measured 1.8x the stream bytes in DRAM traffic).  A lane
-// family tile is whole warps of 32/lpc channels.
+// tiles as SMs times resident CTAs, so its fp32 tiles are 16 channels (64-byte rows) unless the
+// 32-channel tiles alone give two CTAs per SM (FwdVariant::w32: the per-tile kernel itself, run
+// balanced; 133 against 148 us on the 130m-shaped layer); its bf16 tiles stay at 32 (64-byte rows
+// too: narrower rows would have each 64-byte DRAM access read by two CTAs at different times,
+// which measured 1.8x the stream bytes in DRAM traffic).  A lane family tile is whole warps of
+// 32/lpc channels.
 constexpr int lane_w(int lpc, bool balanced, int es) { return balanced && lpc > 1 && es == 4 ? 16 : 32; }
 // With the low-rank time-step projection folded in: 48-step chunks (the staged dt_low tile
 // replaces the Δ tile and is wider), ranks up to 64, rows padded to an odd number of 16-byte

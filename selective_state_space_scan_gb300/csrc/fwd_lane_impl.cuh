@@ -6,9 +6,11 @@
 
 namespace selscan {
 
-template <typename TIO, int NS, int LPC, bool BAL, bool TMA, bool SO = false, bool LTI = false, bool BCF = false>
+// WIDE: the balanced schedule on the per-tile kernel's 32-channel tiles (the same instantiation).
+template <typename TIO, int NS, int LPC, bool BAL, bool TMA, bool SO = false, bool LTI = false, bool BCF = false,
+          bool WIDE = false>
 cudaError_t launch_lane_cfg(const FwdParams& p, const FwdMaps& m, cudaStream_t stream, int* max_grid) {
-    constexpr int W = lane_w(LPC, BAL, static_cast<int>(sizeof(TIO)));
+    constexpr int W = WIDE ? 32 : lane_w(LPC, BAL, static_cast<int>(sizeof(TIO)));
     using Cfg = LaneCfg<TIO, NS, LPC, W, kLaneT, kLaneStages, BCF ? lane_minb_bcf32(LPC, W) : lane_minb(LPC, W), 0, BCF>;
     constexpr int smem = TMA ? Cfg::SMEM_BYTES : Cfg::SMEM_BYTES - (Cfg::STAGES - 1) * Cfg::STAGE_BYTES;
     static_assert(smem <= 227 * 1024, "shared memory budget exceeded");
@@ -27,6 +29,7 @@ cudaError_t launch_lane_v(const FwdVariant& v, const FwdParams& p, const FwdMaps
     }
     if (v.balanced) {
         if (!v.tma) return cudaErrorInvalidValue;   // the balanced schedule is TMA-fed only
+        if (v.w32) return launch_lane_cfg<TIO, NS, LPC, true, true, false, false, false, true>(p, m, s, mg);
         return launch_lane_cfg<TIO, NS, LPC, true, true>(p, m, s, mg);
     }
     return v.tma ? launch_lane_cfg<TIO, NS, LPC, false, true>(p, m, s, mg)

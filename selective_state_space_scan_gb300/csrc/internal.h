@@ -27,6 +27,7 @@ struct FwdVariant {
     int chunk = 0;   // test override of the steps per chunk (16, 32 or 256; 0: the kernels' own)
     bool bcf32 = false;  // bf16 streams with B and C staged as fp32 (a widened copy in the workspace)
     int cluster = 0;     // > 0: the single-launch time split, segments per cluster
+    bool w32 = false;    // balanced fp32 on 32-channel tiles (the per-tile kernel's own geometry)
 };
 
 struct FwdGeom {
@@ -38,7 +39,8 @@ struct FwdGeom {
 inline FwdGeom fwd_geometry(const FwdVariant& v) {
     if (v.family == kFamSeg) return FwdGeom{8 * kSegG, 8 * kSegG, 4 * kSegQ * kSegK};
     if (v.dtp) return FwdGeom{32, 32, kLaneTD};
-    return FwdGeom{lane_w(v.lpc, v.balanced, v.es), lane_w(v.lpc, v.balanced, v.es), v.chunk > 0 ? v.chunk : kLaneT};
+    const int w = v.w32 ? 32 : lane_w(v.lpc, v.balanced, v.es);
+    return FwdGeom{w, w, v.chunk > 0 ? v.chunk : kLaneT};
 }
 
 // Launch (grid = p.grid CTAs; cooperative when v.balanced).  With `max_grid` non-null, launch

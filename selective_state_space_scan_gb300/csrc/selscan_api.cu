@@ -342,6 +342,17 @@ int64_t balanced_grid(int64_t tiles_total, int max_grid) {
     return std::min<int64_t>(tiles_total, max_grid);
 }
 
+// fp32 balanced schedule on 32-channel tiles (the per-tile kernel, run balanced) when those tiles
+// alone give two CTAs per SM; else 16-channel tiles, twice as many.
+bool balanced_w32(int64_t batch, int64_t Dm, int es) {
+    if (es != 4) return false;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        return false;
+    return batch * ((Dm + 31) / 32) >= 2 * static_cast<int64_t>(sms);
+}
+
 cudaError_t lane_max_grid(const FwdVariant& v, bool bf16, int* out) {
     FwdParams dummy;
     std::memset(&dummy, 0, sizeof(dummy));
@@ -572,6 +583,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     v.balanced = plan.nseg < 2 && workspace != nullptr && v.family == kFamLane && tma && !v.lti && !dtp &&
                  fc == 0 && g_force_balanced.load() != 0;
     if (!v.balanced && plan.nseg < 2 && v.family == kFamLane && fl <= 0) v.lpc = per_tile_lpc(batch, Dm, v.ns);
+    v.w32 = v.balanced && balanced_w32(batch, Dm, v.es);
     FwdMaps maps;
     std::memset(&maps, 0, sizeof(maps));
 
@@ -607,6 +619,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     if (!tma) {                     // descriptors refused: the plain-load fill, per-tile schedule
         plan = SplitPlan();
         v.balanced = false;
+        v.w32 = false;
     }
     const bool split = plan.nseg >= 2;
     v.bcf32 = Bw && tma && v.family == kFamLane && (v.balanced || split);
@@ -797,6 +810,7 @@ size_t fwd_ws_need(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_d
     v.balanced = true;
     v.tma = true;
     v.bcf32 = widen > 0;
+    v.w32 = balanced_w32(batch, Dm, v.es);
     const FwdGeom geo = fwd_geometry(v);
     const int64_t tiles = batch * ((Dm + geo.tile_channels - 1) / geo.tile_channels);
     int max_grid = 0;
@@ -1010,8 +1024,9 @@ int ss__fwd_plan(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dty
     const bool bal = with_ws && g_force_balanced.load() != 0;
     if (!bal && !fl) v.lpc = per_tile_lpc(batch, Dm, v.ns);
     const bool wide = bal && widens_bc(io_dtype, N);
-    std::snprintf(buf, sizeof(buf), "ss_fwd_lane_kernel(lpc=%d%s%s)", v.lpc, bal ? ",balanced" : "",
-                  wide ? ",fp32 B/C" : "");
+    const bool w32 = bal && balanced_w32(batch, Dm, io_dtype == SS_BF16 ? 2 : 4);
+    std::snprintf(buf, sizeof(buf), "ss_fwd_lane_kernel(lpc=%d%s%s%s)", v.lpc, bal ? ",balanced" : "",
+                  w32 ? ",32-channel tiles" : "", wide ? ",fp32 B/C" : "");
     put(buf);
     return wide ? 2 : 1;                  // (the B/C widening pass,) the scan
 }

@@ -569,6 +569,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                     for (int g = 0; g < G; ++g) dsum += dd[g];
                 }
                 float2* dxrow = nullptr;
+                (void)dxrow;                                    // used by the DXS hand-over only
                 if constexpr (Cfg::DXS) {
                     // this warp's rows; the previous sub-block's reads are done once every lane is here
                     dxrow = reinterpret_cast<float2*>(aux + Cfg::AUX_DX) + (warp * CPW + c) * Cfg::DX_PITCH;
@@ -664,6 +665,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                             // (interleaving them costs this register-heavy layout spills)
                             if (g + 1 < G) prep(g + 1, an, bn);
                             const float* rowC = tC + (g0 + g) * NS + n0;
+                            (void)rowC;                         // unread when C is in registers or unused
                             float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                             for (int qq = 0; qq < QPL; ++qq) {
@@ -692,6 +694,7 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                             const float2 dl2 = make_float2(dk, dk), du2 = make_float2(uk, uk);
                             const float* rowB = tB + ((g0 + gn) * LPC + kk) * NS + n0;
                             const float* rowC = tC + ((g0 + g) * LPC + kk) * NS + n0;
+                            (void)rowC;
                             float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                             for (int qq = 0; qq < QPL; ++qq) {

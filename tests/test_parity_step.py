@@ -263,3 +263,13 @@ def test_step_single_layer_staged_equals_block_kernel():
             _force_layers_path(-1)
     np.testing.assert_array_equal(out[1][0], out[0][0])
     np.testing.assert_array_equal(to_host(out[1][1]), to_host(out[0][1]))
+
+
+def test_step_layers_at_the_layer_limit():
+    """128 layers (the most one call takes) of batch 3 and 64 channels through the staged kernel,
+    each against the oracle."""
+    ws = [synth.step_inputs(3, 64, 16, seed=300 + k, with_bias=bool(k % 2)) for k in range(128)]
+    ys, sts = _layers_run(ws, 1)
+    for w, y, st in zip(ws, ys, sts):
+        ry, rst, mag = oracle_step(w)
+        assert_fwd_close("f32", y, ry, mag, st, rst, what=f"128 layers {w.seed}")
