@@ -5,11 +5,14 @@
 //   y[b,d]     = (Σ_n C[b,n] h[b,d,n] + D[d] x[b,d]) · silu(z[b,d])
 // The state is updated in place.  The step is elementwise over (b,d) and HBM-bound on the
 // state read + write (16 states x 8 bytes per row against 16 bytes of x, Δ, z, y), so the
-// kernel is a stream: LPR lanes per (b,d) row, each lane owning four consecutive states (one
-// 16-byte load and store of h), RPT rows per thread with every load of all of them issued
-// before any arithmetic (bytes in flight hide HBM latency), the partial C·h sums reduced
-// across the row's lanes by shuffles.  Block x covers rows of batch row x / blocks_per_b: one
-// 32-bit division per block, none per element.
+// kernels are streams with LPR lanes per (b,d) row, each lane owning four consecutive states,
+// and the partial C·h sums reduced across the row's lanes by shuffles.  Two of them:
+//   - the staged kernel (16 states, aligned rows: the usual case; see the section below): each
+//     warp streams a contiguous range of 32-row units through its own ring of bulk-copied
+//     shared-memory stages, so the bytes in flight are bound by shared memory, not registers;
+//   - the per-block kernel (any N, strides or alignment): RPT rows per thread with every load of
+//     all of them issued before any arithmetic, one 16-byte load and store of h per lane; block
+//     x covers rows of batch row x / blocks_per_b (one 32-bit division per block).
 // exp(A_log) is taken on the SFU (2^(A_log·log2 e)); its relative error (~1e-7) moves the
 // decay exponent by as much, far below the fp32 tolerance.
 #include <algorithm>
@@ -26,10 +29,10 @@ namespace selscan {
 // (11.1 against 11.7 us on the 48-layer decode), 32 or 512 slower.
 constexpr int kStepThreads = 64;
 
-// Resident blocks per SM the many-layer kernel's registers are sized for: the step is bound by
-// the state loads in flight, so occupancy pays.  At 24 blocks (at most 42 registers) the 48-layer
-// launch measured 391 us against 455 us unbounded (56 registers, 52% occupancy) and 420 us at 32
-// blocks (32 registers, with spills).  The single-layer kernel stays unbounded: its short
+// Resident blocks per SM the per-block many-layer kernel's registers are sized for: it is bound
+// by the state loads in flight, so occupancy pays.  At 24 blocks (at most 42 registers) the
+// 48-layer launch measured 391 us against 455 us unbounded (56 registers, 52% occupancy) and
+// 420 us at 32 blocks (32 registers, with spills).  The single-layer kernel stays unbounded: its short
 // launches measured 10.8 us a layer unbounded against 12.4 us at 24 blocks.
 #ifndef SS_STEPL_MINB
 #define SS_STEPL_MINB 24
