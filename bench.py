@@ -51,6 +51,9 @@ def parse():
                          "(the library's pipe probe) and exit")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-bwd-ckpt", action="store_true",
+                    help="backward workloads: time ss_bwd with its own first pass instead of reading the "
+                         "forward's checkpoints (ss_fwd_ckpt + ss_bwd_ckpt)")
     ap.add_argument("--variant", default=None,
                     help="pin the forward kernel as family,q,tma (family 0 channel-lane / 1 segment-lane; "
                          "q warps per CTA 1|2|4 or 0 auto; tma 1|0|-1 auto); default: the library's choice")
@@ -720,8 +723,16 @@ def bench_bwd(args, local_rank):
     t = {k: (None if v is None else torch.from_numpy(v).to(dev)) for k, v in a.items()}
     dy = torch.from_numpy(synth.rng_for(1, 12).standard_normal((w.batch, w.L, w.Dm), dtype=np.float32)).to(dev)
 
+    # the training flow: the forward pass (ss_fwd_ckpt, outside the timed region) leaves the state
+    # at every 16th step, and the backward reads them instead of refolding the sequence first
+    # (ss_bwd_ckpt; the time split of the long row recomputes its own and ignores them)
+    ckpt = None
+    if not args.no_bwd_ckpt and w.N == 16:
+        _, ckpt = ss.ss_fwd_ckpt(t["u"], t["delta_raw"], t["delta_bias"], t["A_log"], t["B"], t["C"], t["D"], t["z"])
+        torch.cuda.synchronize()
+
     def step():
-        ss.ss_bwd(dy, t["u"], t["delta_raw"], t["delta_bias"], t["A_log"], t["B"], t["C"], t["D"], t["z"])
+        ss.ss_bwd(dy, t["u"], t["delta_raw"], t["delta_bias"], t["A_log"], t["B"], t["C"], t["D"], t["z"], ckpt=ckpt)
     total_ms, launch_ms, clocks = time_step_fn(step, args, local_rank)
     units = updates_per_step(w)
     s = w.io_bytes()
@@ -740,7 +751,11 @@ def bench_bwd(args, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{args.workload}: batch={w.batch} L={w.L} Dm={w.Dm} N={w.N} io=f32, "
                                "all input gradients" + (", time split" if split else ""),
-                   "l2": "no flush: working set > 129 MB L2"},
+                   "l2": "no flush: working set > 129 MB L2",
+                   "call": ("ss_bwd_ckpt: with the checkpoints ss_fwd_ckpt wrote (outside the timed region)"
+                            if ckpt is not None and not split else
+                            "ss_bwd (its own first pass)" if ckpt is None else
+                            "ss_bwd_ckpt (the time split recomputes its own states)")},
         "gpu_launches": args.steps * (4 if split else 1), "clocks": clocks,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",

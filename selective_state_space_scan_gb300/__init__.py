@@ -12,7 +12,7 @@ from typing import Optional
 
 from . import _build
 
-__all__ = ["ss_fwd", "ss_fwd_dtproj", "ss_fwd_host", "ss_step", "ss_step_layers", "ss_fwd_summary", "ss_carry_compose", "ss_conv1d", "ss_bwd", "ss_fwd_workspace_size", "SelscanError", "lib", "device_error",
+__all__ = ["ss_fwd", "ss_fwd_ckpt", "ss_fwd_dtproj", "ss_fwd_host", "ss_step", "ss_step_layers", "ss_fwd_summary", "ss_carry_compose", "ss_conv1d", "ss_bwd", "ss_fwd_workspace_size", "SelscanError", "lib", "device_error",
            "version", "status_string", "SS_F32", "SS_BF16", "FwdStrides", "StepStrides", "ConvStrides"]
 
 SS_F32, SS_BF16 = 0, 1
@@ -78,6 +78,12 @@ def lib() -> ctypes.CDLL:
         L.ss_bwd.restype = ctypes.c_int
         L.ss_bwd_workspace_size.argtypes = [i64] * 4
         L.ss_bwd_workspace_size.restype = ctypes.c_size_t
+        L.ss_bwd_ckpt.argtypes = [vp] * 21 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp, ctypes.c_size_t, vp]
+        L.ss_bwd_ckpt.restype = ctypes.c_int
+        L.ss_fwd_ckpt.argtypes = [vp] * 12 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp]
+        L.ss_fwd_ckpt.restype = ctypes.c_int
+        L.ss_fwd_ckpt_size.argtypes = [i64] * 4
+        L.ss_fwd_ckpt_size.restype = ctypes.c_size_t
         L.ss_status_string.argtypes = [ctypes.c_int]
         L.ss_status_string.restype = ctypes.c_char_p
         L.ss_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
@@ -392,12 +398,40 @@ def ss_conv1d(x, weight, bias=None, out=None, window_in=None, window_out=None, s
     return out
 
 
-def ss_bwd(dy, u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, h0=None, dlast=None, stream=None):
+def ss_fwd_ckpt(u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, last_state=None, h0=None,
+                ckpt=None, stream=None):
+    """Forward pass for training through the C ABI (ss_fwd_ckpt): y as ss_fwd, and the
+    checkpoints ss_bwd(..., ckpt=...) reads instead of a first pass of its own (16 states only).
+    Returns (y, ckpt); ckpt (float32, allocated when None) has ss_fwd_ckpt_size bytes."""
+    import torch
+    batch, L, Dm = u.shape
+    N = A_log.shape[1]
+    io = _io_code(u.dtype)
+    if y is None:
+        y = torch.empty((batch, L, Dm), dtype=u.dtype, device=u.device)
+    for name, t in (("u", u), ("delta_raw", delta_raw), ("z", z), ("y", y), ("B", B), ("C", C)):
+        _check_inner(t, name)
+    nbytes = int(lib().ss_fwd_ckpt_size(batch, L, Dm, N))
+    if ckpt is None:
+        ckpt = torch.empty((max(nbytes, 4) // 4,), dtype=torch.float32, device=u.device)
+    s = FwdStrides(io, u.stride(0), u.stride(1), delta_raw.stride(0), delta_raw.stride(1),
+                   z.stride(0) if z is not None else 0, z.stride(1) if z is not None else 0,
+                   y.stride(0), y.stride(1), B.stride(0), B.stride(1), C.stride(0), C.stride(1))
+    st = lib().ss_fwd_ckpt(_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D),
+                           _ptr(z), _ptr(y), _ptr(last_state), _ptr(h0), _ptr(ckpt), batch, L, Dm, N, ctypes.byref(s),
+                           _stream_handle(stream))
+    if st != 0:
+        raise SelscanError(st, "ss_fwd_ckpt")
+    return y, ckpt
+
+
+def ss_bwd(dy, u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, h0=None, dlast=None, stream=None, ckpt=None):
     """Gradients of ss_fwd (from h0) through the C ABI.  dy [batch, L, Dm] (gradient of y, io
     dtype); dlast [batch, Dm, N] float32 (of last_state) or None.  Returns a dict: du,
     ddelta_raw, dz (None without z) [batch, L, Dm] io dtype; dB, dC [batch, L, N], dA_log [Dm, N],
     dD, ddelta_bias [Dm], dh0 [batch, Dm, N] float32.  The workspace (chunk checkpoints) comes
-    from the per-(device, stream) cache."""
+    from the per-(device, stream) cache.  ckpt: the checkpoints ss_fwd_ckpt wrote on the same
+    inputs and h0 (ss_bwd_ckpt: no first pass), or None."""
     import torch
     batch, L, Dm = u.shape
     N = A_log.shape[1]
@@ -418,11 +452,16 @@ def ss_bwd(dy, u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, h0=None, d
     sh = _stream_handle(stream)
     nbytes = int(lib().ss_bwd_workspace_size(batch, L, Dm, N))
     ws = workspace_for(u.device, stream, nbytes, purpose="bwd") if nbytes else None
-    st = lib().ss_bwd(_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
-                      _ptr(h0), _ptr(dy), _ptr(dlast), _ptr(g["du"]), _ptr(g["ddelta_raw"]), _ptr(g["dz"]),
-                      _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dA_log"]), _ptr(g["dD"]), _ptr(g["ddelta_bias"]),
-                      _ptr(g["dh0"]), batch, L, Dm, N, ctypes.byref(s), None if ws is None else ws.data_ptr(),
-                      0 if ws is None else ws.numel(), sh)
+    head = (_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(h0))
+    tail = (_ptr(dy), _ptr(dlast), _ptr(g["du"]), _ptr(g["ddelta_raw"]), _ptr(g["dz"]), _ptr(g["dB"]), _ptr(g["dC"]),
+            _ptr(g["dA_log"]), _ptr(g["dD"]), _ptr(g["ddelta_bias"]), _ptr(g["dh0"]), batch, L, Dm, N, ctypes.byref(s),
+            None if ws is None else ws.data_ptr(), 0 if ws is None else ws.numel(), sh)
+    if ckpt is not None:
+        st = lib().ss_bwd_ckpt(*head, _ptr(ckpt), *tail)
+        where = "ss_bwd_ckpt"
+    else:
+        st = lib().ss_bwd(*head, *tail)
+        where = "ss_bwd"
     if st != 0:
-        raise SelscanError(st, "ss_bwd")
+        raise SelscanError(st, where)
     return g

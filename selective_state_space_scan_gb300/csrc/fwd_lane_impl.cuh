@@ -7,18 +7,29 @@
 namespace selscan {
 
 // WIDE: the balanced schedule on the per-tile kernel's 32-channel tiles (the same instantiation).
+// CKPT: the per-tile kernel that also writes the backward's checkpoints.
 template <typename TIO, int NS, int LPC, bool BAL, bool TMA, bool SO = false, bool LTI = false, bool BCF = false,
-          bool WIDE = false>
+          bool WIDE = false, bool CKPT = false>
 cudaError_t launch_lane_cfg(const FwdParams& p, const FwdMaps& m, cudaStream_t stream, int* max_grid) {
     constexpr int W = WIDE ? 32 : lane_w(LPC, BAL, static_cast<int>(sizeof(TIO)));
     using Cfg = LaneCfg<TIO, NS, LPC, W, kLaneT, kLaneStages, BCF ? lane_minb_bcf32(LPC, W) : lane_minb(LPC, W), 0, BCF>;
     constexpr int smem = TMA ? Cfg::SMEM_BYTES : Cfg::SMEM_BYTES - (Cfg::STAGES - 1) * Cfg::STAGE_BYTES;
     static_assert(smem <= 227 * 1024, "shared memory budget exceeded");
-    return launch_with_smem<Cfg, TMA>(ss_fwd_lane_kernel<Cfg, TMA, SO, LTI>, p, m, stream, smem, BAL, max_grid);
+    return launch_with_smem<Cfg, TMA>(ss_fwd_lane_kernel<Cfg, TMA, SO, LTI, false, CKPT>, p, m, stream, smem, BAL,
+                                      max_grid);
 }
 
 template <typename TIO, int NS, int LPC>
 cudaError_t launch_lane_v(const FwdVariant& v, const FwdParams& p, const FwdMaps& m, cudaStream_t s, int* mg) {
+    if (v.ckpt) {
+        // per tile, TMA-fed, 16 states at 4 lanes per channel only
+        if constexpr (NS == 16 && LPC == 4) {
+            if (!v.tma || v.balanced || v.state_only || v.lti) return cudaErrorInvalidValue;
+            return launch_lane_cfg<TIO, NS, LPC, false, true, false, false, false, false, true>(p, m, s, mg);
+        } else {
+            return cudaErrorInvalidValue;
+        }
+    }
     if (v.lti) {
         if (!v.tma || v.balanced || v.state_only) return cudaErrorInvalidValue;   // per-tile, TMA-fed only
         return launch_lane_cfg<TIO, NS, LPC, false, true, false, true>(p, m, s, mg);

@@ -36,6 +36,12 @@ struct FwdParams {
     int grid;            // CTAs in the launch (0: batch·tiles_per_batch)
     // Initial state h_{-1} [batch, Dm, N] contiguous (nullptr: zeros).
     const float* h0;
+    // Checkpoints for the backward pass (the CKPT kernel, one CTA per 32-channel tile, 16 states):
+    // the state entering every 16th step, [tiles][ckpt_chunks][2][32][16] fp32 with
+    // ckpt_chunks = ceil(L / 32) (the steps past L are identity steps: their entries hold the
+    // final state).
+    float* ckpt;
+    int ckpt_chunks;
     // Time-split schedule (seg_launch > 0): the sequence is cut into segments of seg_chunks
     // chunks; CTA x takes segment x % seg_launch of tile x / seg_launch.  Pass A (state-only
     // kernel) folds segments 0 .. nseg-2 from zero and writes each end state to slot s + 1

@@ -28,6 +28,7 @@ struct FwdVariant {
     bool bcf32 = false;  // bf16 streams with B and C staged as fp32 (a widened copy in the workspace)
     int cluster = 0;     // > 0: the single-launch time split, segments per cluster
     bool w32 = false;    // balanced fp32 on 32-channel tiles (the per-tile kernel's own geometry)
+    bool ckpt = false;   // per tile, LPC 4, 16 states: also write the backward's checkpoints
 };
 
 struct FwdGeom {

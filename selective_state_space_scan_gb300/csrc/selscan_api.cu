@@ -366,6 +366,13 @@ cudaError_t lane_max_grid(const FwdVariant& v, bool bf16, int* out) {
 size_t fwd_ws_need(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dtype, bool* split,
                    bool with_widen = true);
 
+// Bytes of the backward's checkpoints for these sizes (16 states): the state entering every 16th
+// step, [batch·ceil(Dm/32)][ceil(L/32)][2][32][16] fp32.
+size_t ckpt_bytes(int64_t batch, int64_t L, int64_t Dm) {
+    return sizeof(float) * static_cast<size_t>(batch) * static_cast<size_t>((Dm + 31) / 32) *
+           static_cast<size_t>((L + 31) / 32) * 2 * 32 * 16;
+}
+
 // Bytes of one widened (fp32) copy of bf16 B or C, and whether the workspace schedules widen them
 // (bf16 I/O with 16 states).
 size_t widen_copy_bytes(int64_t batch, int64_t L, int64_t N) {
@@ -408,7 +415,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
                    const void* B, const void* C, const float* D, const void* z, void* y,
                    float* last_state, const float* h0, int64_t batch, int64_t L, int64_t Dm, int64_t N,
                    const ss_fwd_strides* strides, void* workspace, size_t ws_bytes, void* stream_ptr,
-                   const float* W_dt = nullptr, int64_t R = 0) {
+                   const float* W_dt = nullptr, int64_t R = 0, float* ckpt = nullptr) {
     // W_dt != nullptr: the low-rank time-step projection is folded in; `delta_raw` is then dt_low
     // [batch, L, R] (strides delta_b, delta_l) and delta_raw[b,t,d] = Σ_k W_dt[d,k] dt_low[b,t,k].
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
@@ -416,6 +423,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     if (batch < 0 || L < 0 || Dm < 0) return SS_ERR_INVALID_ARG;
     if (N < 1 || N > 16) return SS_ERR_UNSUPPORTED;
     if (dtp && (R < 4 || R > kDtRankMax || R % 4 != 0)) return SS_ERR_UNSUPPORTED;
+    if (ckpt && (N != 16 || dtp || workspace)) return SS_ERR_UNSUPPORTED;   // checkpoints: 16 states, per tile
     ss_fwd_strides s;
     if (strides) {
         s = *strides;
@@ -475,10 +483,11 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     for (const void* p : f_ptrs)
         if (p && !aligned(p, 4)) return SS_ERR_MISALIGNED;
     if (dtp && !aligned(W_dt, 16)) return SS_ERR_MISALIGNED;
+    if (ckpt && !aligned(ckpt, 16)) return SS_ERR_MISALIGNED;
     // device memory of the current device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
-    const void* all_ptrs[] = {u, delta_raw, B, C, y, z, A_log, D, delta_bias, last_state, h0, W_dt};
+    const void* all_ptrs[] = {u, delta_raw, B, C, y, z, A_log, D, delta_bias, last_state, h0, W_dt, ckpt};
     for (const void* p : all_ptrs)
         if (p && !is_device_pointer(p, dev)) return SS_ERR_INVALID_ARG;
     // outputs must not overlap inputs
@@ -496,6 +505,13 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     for (const Range& in : ins)
         if (overlap(sy, in) || overlap(sl, in)) return SS_ERR_INVALID_ARG;
     if (overlap(sy, sl)) return SS_ERR_INVALID_ARG;
+    if (ckpt) {
+        // the checkpoints are an output too
+        const Range sc = span3(ckpt, 1, 1, static_cast<int64_t>(ckpt_bytes(batch, L, Dm) / 4), 0, 0, 4);
+        for (const Range& in : ins)
+            if (overlap(sc, in)) return SS_ERR_INVALID_ARG;
+        if (overlap(sc, sy) || overlap(sc, sl) || overlap(sc, sh)) return SS_ERR_INVALID_ARG;
+    }
 
     // Kernel choice.  The lane family folds each (channel, state) chain sequentially, its
     // parallelism being channels x LPC lanes; LPC grows until there are enough warps to fill
@@ -584,6 +600,15 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
                  fc == 0 && g_force_balanced.load() != 0;
     if (!v.balanced && plan.nseg < 2 && v.family == kFamLane && fl <= 0) v.lpc = per_tile_lpc(batch, Dm, v.ns);
     v.w32 = v.balanced && balanced_w32(batch, Dm, v.es);
+    if (ckpt) {
+        // the checkpoint-writing kernel: one CTA per tile, 4 lanes per channel, TMA-fed tiles
+        if (!tma || lti) return SS_ERR_UNSUPPORTED;
+        v.family = kFamLane;
+        v.lpc = 4;
+        v.balanced = false;
+        v.w32 = false;
+        v.ckpt = true;
+    }
     FwdMaps maps;
     std::memset(&maps, 0, sizeof(maps));
 
@@ -639,6 +664,8 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     std::memset(&p, 0, sizeof(p));
     p.u = u; p.delta = delta_raw; p.z = z; p.Bm = B; p.Cm = C;
     p.bias = delta_bias; p.A_log = A_log; p.Dv = D; p.y = y; p.last_state = last_state; p.h0 = h0;
+    p.ckpt = ckpt;
+    p.ckpt_chunks = static_cast<int>((L + 31) / 32);
     p.u_b = s.u_b; p.u_l = s.u_l; p.d_b = s.delta_b; p.d_l = s.delta_l;
     p.z_b = s.z_b; p.z_l = s.z_l; p.y_b = s.y_b; p.y_l = s.y_l;
     p.B_b = s.B_b; p.B_l = s.B_l; p.C_b = s.C_b; p.C_l = s.C_l;
@@ -769,6 +796,20 @@ ss_status ss_fwd_h0(const void* u, const void* delta_raw, const float* delta_bia
                     const ss_fwd_strides* strides, void* workspace, size_t workspace_bytes, void* stream) {
     return fwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, y, last_state, h0, batch, L, Dm, N,
                     strides, workspace, workspace_bytes, stream);
+}
+
+ss_status ss_fwd_ckpt(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
+                      const void* B, const void* C, const float* D, const void* z, void* y, float* last_state,
+                      const float* h0, float* ckpt, int64_t batch, int64_t L, int64_t Dm, int64_t N,
+                      const ss_fwd_strides* strides, void* stream) {
+    if (!ckpt && batch > 0 && L > 0 && Dm > 0) return SS_ERR_INVALID_ARG;
+    return fwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, y, last_state, h0, batch, L, Dm, N, strides,
+                    nullptr, 0, stream, nullptr, 0, ckpt);
+}
+
+size_t ss_fwd_ckpt_size(int64_t batch, int64_t L, int64_t Dm, int64_t N) {
+    if (batch <= 0 || L <= 0 || Dm <= 0 || N != 16) return 0;
+    return ckpt_bytes(batch, L, Dm);
 }
 
 }  // extern "C"

@@ -68,6 +68,7 @@ struct BwdParams {
     float* dbias;          // [Dm] or nullptr (zeroed)
     float* dh0;            // [batch, Dm, N] or nullptr
     float* ckpt;           // [tiles][nchunks][kBT / kBS][kBW][NS]: the state at every sub-chunk start
+    int ckpt_given;        // the checkpoints came from the forward pass (ss_fwd_ckpt): no pass 1
     unsigned int* err;     // device error word
     // Time split (nseg > 1): CTA x takes segment x % nseg (chunks [seg·seg_chunks, ...)) of tile
     // x / nseg.  The local launch folds each segment from zero (end state into h_slots[seg + 1],
@@ -299,7 +300,11 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
             phase ^= 1u;
         }
     };
-    if (TMA && tid == 0) issue(c0, kStFwd);
+    const bool pass1 = LOCAL || !p.ckpt_given;
+    if (TMA && tid == 0) {
+        if (pass1) issue(c0, kStFwd);
+        else issue(c1 - 1, kStFull);             // pass 2 starts from the last chunk
+    }
 
     float2 A2[2], An[2];                         // A·log2(e) and A = -exp(A_log), state pairs
 #pragma unroll
@@ -352,7 +357,7 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
         h[0] = h[1] = f2(0.f);
     else
         load_quad(seg == 0 ? p.h0 : p.h_slots + seg * count, h);
-    for (int ch = c0; ch < c1; ++ch) {
+    for (int ch = c0; pass1 && ch < c1; ++ch) {
         wait_staged();
         bwd_prepare<Cfg, TIO, TMA, kStFwd>(sm, raw, p, b, d0, ch, bias_c);
         __syncthreads();                         // staged tiles consumed; the chunk's arrays are ready
@@ -667,12 +672,13 @@ extern "C" size_t ss_bwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, in
     return bwd_plan(batch, L, Dm, N).total;
 }
 
-extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
-                            const void* B, const void* C, const float* D, const void* z, const float* h0,
-                            const void* dy, const float* dlast, void* du, void* ddelta_raw, void* dz,
-                            float* dB, float* dC, float* dA_log, float* dD, float* ddelta_bias, float* dh0,
-                            int64_t batch, int64_t L, int64_t Dm, int64_t N, const ss_fwd_strides* strides,
-                            void* workspace, size_t workspace_bytes, void* stream_ptr) {
+// ckpt_in: the forward's checkpoints (ss_fwd_ckpt), used when the backward runs unsplit.
+static ss_status bwd_impl(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
+                          const void* B, const void* C, const float* D, const void* z, const float* h0,
+                          const void* dy, const float* dlast, void* du, void* ddelta_raw, void* dz,
+                          float* dB, float* dC, float* dA_log, float* dD, float* ddelta_bias, float* dh0,
+                          int64_t batch, int64_t L, int64_t Dm, int64_t N, const ss_fwd_strides* strides,
+                          void* workspace, size_t workspace_bytes, void* stream_ptr, const float* ckpt_in) {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     if (batch < 0 || L < 0 || Dm < 0) return SS_ERR_INVALID_ARG;
     if (N < 1 || N > 16) return SS_ERR_UNSUPPORTED;
@@ -700,6 +706,8 @@ extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* d
     const void* f_ptrs[] = {A_log, D, delta_bias, h0, dlast, dB, dC, dA_log, dD, ddelta_bias, dh0};
     for (const void* q : f_ptrs)
         if (q && !is_aligned(q, 4)) return SS_ERR_MISALIGNED;
+    if (ckpt_in && (N != 16)) return SS_ERR_UNSUPPORTED;
+    if (ckpt_in && !is_aligned(ckpt_in, 16)) return SS_ERR_MISALIGNED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
     // the sums are accumulated: clear them (also the whole answer when L == 0)
@@ -729,7 +737,7 @@ extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* d
          (s.C_l < N && s.C_l != 0)) && L > 1)
         return SS_ERR_INVALID_ARG;
     const void* all[] = {u, delta_raw, B, C, z, dy, du, ddelta_raw, dz, A_log, D, delta_bias, h0, dlast,
-                         dB, dC, dA_log, dD, ddelta_bias, dh0};
+                         dB, dC, dA_log, dD, ddelta_bias, dh0, ckpt_in};
     for (const void* q : all)
         if (q && !dev_ptr(q, dev)) return SS_ERR_INVALID_ARG;
     // outputs: pairwise disjoint and disjoint from every input
@@ -743,7 +751,9 @@ extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* d
                          range3(C, batch, L, N, s.C_b, s.C_l, es), range3(dy, batch, L, Dm, L * Dm, Dm, es),
                          range3(A_log, 1, Dm, N, 0, N, 4), range3(D, 1, 1, Dm, 0, 0, 4),
                          range3(delta_bias, 1, 1, Dm, 0, 0, 4), range3(h0, batch, Dm, N, Dm * N, N, 4),
-                         range3(dlast, batch, Dm, N, Dm * N, N, 4)};
+                         range3(dlast, batch, Dm, N, Dm * N, N, 4),
+                         range3(ckpt_in, 1, 1, batch * ((Dm + kBW - 1) / kBW) * ((L + kBT - 1) / kBT) * 2 * kBW * 16,
+                                0, 0, 4)};
     const int nouts = sizeof(outs) / sizeof(outs[0]);
     for (int i = 0; i < nouts; ++i) {
         for (const Range& r : ins)
@@ -766,6 +776,10 @@ extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* d
     p.h0 = h0; p.dy = dy; p.dlast = dlast; p.du = du; p.ddelta = ddelta_raw; p.dz = dz; p.dB = dB; p.dC = dC;
     p.dA_log = dA_log; p.dD = dD; p.dbias = ddelta_bias; p.dh0 = dh0;
     p.ckpt = static_cast<float*>(workspace);
+    if (ckpt_in && plan.nseg == 1) {              // the forward's checkpoints: no pass 1
+        p.ckpt = const_cast<float*>(ckpt_in);
+        p.ckpt_given = 1;
+    }
     p.u_b = s.u_b; p.u_l = s.u_l; p.d_b = s.delta_b; p.d_l = s.delta_l; p.z_b = s.z_b; p.z_l = s.z_l;
     p.B_b = s.B_b; p.B_l = s.B_l; p.C_b = s.C_b; p.C_l = s.C_l;
     p.batch = static_cast<int>(batch); p.L = static_cast<int>(L); p.Dm = static_cast<int>(Dm);
@@ -824,6 +838,27 @@ extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* d
 
 // Internal test hook (not in the public header): -1 automatic time split, 0 (or 1) never,
 // n >= 2 always with up to n segments.  Returns the previous setting.
+extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
+                            const void* B, const void* C, const float* D, const void* z, const float* h0,
+                            const void* dy, const float* dlast, void* du, void* ddelta_raw, void* dz,
+                            float* dB, float* dC, float* dA_log, float* dD, float* ddelta_bias, float* dh0,
+                            int64_t batch, int64_t L, int64_t Dm, int64_t N, const ss_fwd_strides* strides,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+    return bwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, h0, dy, dlast, du, ddelta_raw, dz, dB, dC, dA_log,
+                    dD, ddelta_bias, dh0, batch, L, Dm, N, strides, workspace, workspace_bytes, stream, nullptr);
+}
+
+extern "C" ss_status ss_bwd_ckpt(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
+                                 const void* B, const void* C, const float* D, const void* z, const float* h0,
+                                 const float* ckpt, const void* dy, const float* dlast, void* du, void* ddelta_raw,
+                                 void* dz, float* dB, float* dC, float* dA_log, float* dD, float* ddelta_bias,
+                                 float* dh0, int64_t batch, int64_t L, int64_t Dm, int64_t N,
+                                 const ss_fwd_strides* strides, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!ckpt && batch > 0 && L > 0 && Dm > 0) return SS_ERR_INVALID_ARG;
+    return bwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, h0, dy, dlast, du, ddelta_raw, dz, dB, dC, dA_log,
+                    dD, ddelta_bias, dh0, batch, L, Dm, N, strides, workspace, workspace_bytes, stream, ckpt);
+}
+
 extern "C" int ss__force_bwd_nseg(int n) { return g_force_bwd_nseg.exchange(n < 0 ? -1 : n <= 1 ? 0 : n); }
 
 // Internal test hook (not in the public header): -1 automatic, 0 plain-load staging, 1 TMA

@@ -257,11 +257,15 @@ __device__ __forceinline__ void wait_published(const unsigned int* flag, unsigne
 // memory; after a cluster barrier it reads the summaries of ranks 0 .. r-1 from their shared
 // memory and composes the state entering its segment, H_0 = h0, H_{s+1} = 2^(A'·ΣΔ_s)·H_s + end_s;
 // then it folds the segment again from that state with every output.
-template <class Cfg, bool USE_TMA, bool STATE_ONLY = false, bool LTI = false, bool CLUSTER = false>
+// CKPT: also write the backward pass's checkpoints (FwdParams::ckpt), one CTA per 32-channel tile.
+template <class Cfg, bool USE_TMA, bool STATE_ONLY = false, bool LTI = false, bool CLUSTER = false, bool CKPT = false>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
 ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     static_assert(!Cfg::BCF32 || (USE_TMA && !LTI), "widened B/C tiles come by TMA");
     static_assert(!CLUSTER || (USE_TMA && !STATE_ONLY && !LTI && Cfg::DTR == 0), "the cluster split is TMA-fed");
+    static_assert(!CKPT || (Cfg::NS == 16 && Cfg::W == 32 && Cfg::LPC > 1 && Cfg::G * Cfg::LPC % 16 == 0 &&
+                            !STATE_ONLY && !CLUSTER && Cfg::DTR == 0),
+                  "checkpoints: 16 states, 32-channel tiles, sub-blocks of whole 16-step pieces");
     using TIO = typename Cfg::TIO;
     constexpr int LPC = Cfg::LPC, CPW = Cfg::CPW, NS = Cfg::NS, QPL = Cfg::QPL, T = Cfg::T;
     constexpr int STAGES = USE_TMA ? Cfg::STAGES : 1;
@@ -651,6 +655,20 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                     prep(0, an, bn);
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
+                        if constexpr (CKPT) {
+                            // the state entering step t of every 16: the backward's checkpoint
+                            if ((g * LPC) % 16 == 0) {
+                                const int64_t t = tbase + (g0 + g) * LPC;
+                                if (d_ok && t < static_cast<int64_t>(p.ckpt_chunks) * 32) {
+                                    float* dst = p.ckpt + (((static_cast<int64_t>(tile) * p.ckpt_chunks + t / 32) * 2 +
+                                                            (t / 16) % 2) * 32 + cw) * 16 + n0;
+#pragma unroll
+                                    for (int qq = 0; qq < QPL; ++qq)
+                                        __stcg(reinterpret_cast<float4*>(dst + 4 * qq),
+                                               make_float4(h[qq][0].x, h[qq][0].y, h[qq][1].x, h[qq][1].y));
+                                }
+                            }
+                        }
                         float2 ac[LPC][QPL][2], bc[LPC][QPL][2];
 #pragma unroll
                         for (int kk = 0; kk < LPC; ++kk)

@@ -311,3 +311,82 @@ def test_bwd_sums_at_4_byte_offsets(N):
     assert rel_l2(to_host(dC).reshape(batch, L, N), ref["dC"]) <= SUM_REL_L2
     assert rel_l2(to_host(du), ref["du"]) <= GRAD_REL_L2
     assert torch.isnan(bc[0]) and torch.isnan(bc[n + 1:n + 5]).all() and torch.isnan(bc[2 * n + 5:]).all()
+
+
+def run_with_ckpt(w, a, dy, h0, dlast):
+    """ss_fwd_ckpt (y checked against ss_fwd: the same arithmetic, bit for bit) then ss_bwd with its
+    checkpoints."""
+    io = w.io
+    t = dict(u=to_dev(a["u"], io), delta_raw=to_dev(a["delta_raw"], io), z=to_dev(a["z"], io),
+             B=to_dev(a["B"], io), C=to_dev(a["C"], io))
+    prm = dict(delta_bias=f32dev(a["delta_bias"]), A_log=f32dev(a["A_log"]), D=f32dev(a["D"]))
+    h0d = f32dev(h0)
+    last = torch.empty((w.batch, w.Dm, w.N), device="cuda")
+    y, ckpt = ss.ss_fwd_ckpt(t["u"], t["delta_raw"], prm["delta_bias"], prm["A_log"], t["B"], t["C"], prm["D"],
+                             t["z"], last_state=last, h0=h0d)
+    lib = ss.lib()
+    lib.ss__force_fwd_variant.argtypes = [ctypes.c_int] * 3
+    lib.ss__force_fwd_variant(0, 4, -1)           # ss_fwd on the same per-tile, 4-lane configuration
+    try:
+        last2 = torch.empty_like(last)
+        y2 = ss.ss_fwd(t["u"], t["delta_raw"], prm["delta_bias"], prm["A_log"], t["B"], t["C"], prm["D"], t["z"],
+                       last_state=last2, h0=h0d)
+        torch.cuda.synchronize()
+    finally:
+        lib.ss__force_fwd_variant(-1, 0, -1)
+    np.testing.assert_array_equal(to_host(y), to_host(y2))
+    np.testing.assert_array_equal(to_host(last), to_host(last2))
+    g = ss.ss_bwd(to_dev(dy, io), t["u"], t["delta_raw"], prm["delta_bias"], prm["A_log"], t["B"], t["C"], prm["D"],
+                  t["z"], h0=h0d, dlast=f32dev(dlast), ckpt=ckpt)
+    torch.cuda.synchronize()
+    return {k: (None if v is None else to_host(v)) for k, v in g.items()}
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("L", [1, 15, 16, 33, 64, 65, 200, 1000])
+def test_bwd_with_forward_checkpoints(io, L):
+    """The backward from the forward's checkpoints (no first pass of its own) against the oracle,
+    with h0 and dlast, on ragged lengths (entries past the last step hold the final state)."""
+    w, a, dy, h0, dlast = problem(2, L, 200, 16, io=io, seed=70 + L)
+    got = run_with_ckpt(w, a, dy, h0, dlast)
+    ref = reference(a, dy, h0, dlast)
+    for k in ELEMENTWISE + SUMS:
+        e = rel_l2(got[k], ref[k])
+        if io == "bf16":
+            tol = BF16_REL_L2 if k in ("du", "ddelta_raw", "dz") else BF16_SUM_REL_L2
+        else:
+            tol = GRAD_REL_L2 if k in ELEMENTWISE else SUM_REL_L2
+        assert e <= tol, f"ckpt L={L} {io} {k}: rel-L2 {e:.3e} > {tol}"
+
+
+def test_bwd_with_forward_checkpoints_130m_equals_plain_backward():
+    """The 130m-shaped layer: with the forward's checkpoints the elementwise gradients equal the
+    backward's own (its first pass folds the same steps with the same arithmetic), the sums up to
+    their atomic order; and the oracle's on sampled channels."""
+    w = synth.config("mamba130m")
+    a = w.arrays
+    dy = synth.rng_for(71, 12).standard_normal((w.batch, w.L, w.Dm), dtype=np.float32)
+    got = run_with_ckpt(w, a, dy, None, None)
+    plain = run(w, a, dy, None, None)
+    for k in ELEMENTWISE:
+        if got[k] is not None:
+            assert rel_l2(got[k], plain[k]) <= 1e-6, k
+    for k in SUMS:
+        assert rel_l2(got[k], plain[k]) <= 1e-5, k
+
+
+def test_fwd_ckpt_refusals_and_split_backward():
+    """N other than 16 is refused by both calls; a backward that takes the time split (one long
+    row) ignores the checkpoints and still gives the oracle's gradients."""
+    w5, a5, dy5, _, _ = problem(1, 40, 32, 8, seed=72, with_h0=False, with_dlast=False)
+    assert ss.lib().ss_fwd_ckpt_size(1, 40, 32, 8) == 0
+    with pytest.raises(ss.SelscanError):
+        ss.ss_fwd_ckpt(f32dev(a5["u"]), f32dev(a5["delta_raw"]), f32dev(a5["delta_bias"]), f32dev(a5["A_log"]),
+                       f32dev(a5["B"]), f32dev(a5["C"]), f32dev(a5["D"]), f32dev(a5["z"]),
+                       ckpt=torch.empty(1024, device="cuda"))
+    w, a, dy, h0, dlast = problem(1, 3000, 64, 16, seed=73)
+    with splitting(4):
+        got = run_with_ckpt(w, a, dy, h0, dlast)
+    ref = reference(a, dy, h0, dlast)
+    for k in ELEMENTWISE:
+        assert rel_l2(got[k], ref[k]) <= GRAD_REL_L2, k
