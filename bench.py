@@ -725,7 +725,7 @@ def bench_bwd(args, local_rank):
 
     # the training flow: the forward pass (ss_fwd_ckpt, outside the timed region) leaves the state
     # at every 16th step, and the backward reads them instead of refolding the sequence first
-    # (ss_bwd_ckpt; the time split of the long row recomputes its own and ignores them)
+    # (ss_bwd_ckpt; the long row's time split also takes its segments' entering states from them)
     ckpt = None
     if not args.no_bwd_ckpt and w.N == 16:
         _, ckpt = ss.ss_fwd_ckpt(t["u"], t["delta_raw"], t["delta_bias"], t["A_log"], t["B"], t["C"], t["D"], t["z"])
@@ -752,11 +752,10 @@ def bench_bwd(args, local_rank):
         "config": {"workload": f"{args.workload}: batch={w.batch} L={w.L} Dm={w.Dm} N={w.N} io=f32, "
                                "all input gradients" + (", time split" if split else ""),
                    "l2": "no flush: working set > 129 MB L2",
-                   "call": ("ss_bwd_ckpt: with the checkpoints ss_fwd_ckpt wrote (outside the timed region)"
-                            if ckpt is not None and not split else
-                            "ss_bwd (its own first pass)" if ckpt is None else
-                            "ss_bwd_ckpt (the time split recomputes its own states)")},
-        "gpu_launches": args.steps * (4 if split else 1), "clocks": clocks,
+                   "call": ("ss_bwd (its own first pass)" if ckpt is None else
+                            "ss_bwd_ckpt: with the checkpoints ss_fwd_ckpt wrote (outside the timed region)" +
+                            ("; the time split's local launch sweeps only the adjoint" if split else ""))},
+        "gpu_launches": args.steps * ((3 if ckpt is not None else 4) if split else 1), "clocks": clocks,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": measured_traffic(args.workload, "ss_bwd_kernel"), "kernel": "ss_bwd_kernel",

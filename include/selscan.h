@@ -336,8 +336,9 @@ size_t ss_bwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N);
 
 /*
  * Forward pass for training: ss_fwd_h0's results (no workspace: one CTA per 32-channel tile at 4
- * lanes per channel) and, besides, the checkpoints ss_bwd_ckpt reads instead of refolding the
- * sequence in a first pass of its own: the state entering every 16th step,
+ * lanes per channel, or, when the tiles alone cannot fill the GPU, ss_fwd's single-launch
+ * cluster split of the sequence) and, besides, the checkpoints ss_bwd_ckpt reads instead of
+ * refolding the sequence in a first pass of its own: the state entering every 16th step,
  *   ckpt   [batch·ceil(Dm/32)][ceil(L/32)][2][32][16] fp32, device memory, 16-byte aligned,
  *          ss_fwd_ckpt_size(...) bytes; entries past the last step hold the final state.
  * N must be 16 and every tensor must allow TMA-fed tiles (16-byte aligned bases and strides);
@@ -355,9 +356,10 @@ size_t ss_fwd_ckpt_size(int64_t batch, int64_t L, int64_t Dm, int64_t N);
 /*
  * ss_bwd with the forward's checkpoints (ss_fwd_ckpt on the same inputs and h0): the backward
  * then skips its own first pass (the forward fold that writes them), one pass over the inputs
- * fewer.  Used when the backward runs unsplit (the tiles fill the GPU); the time split recomputes
- * its own states and ignores them.  ckpt as ss_fwd_ckpt writes it (an input here: it must not
- * overlap an output); N must be 16.  Other arguments, errors and results as ss_bwd.
+ * fewer.  With the time split (few tiles) the checkpoints also hold every segment's entering
+ * state: the local launch sweeps only the adjoint and the forward carry is not run (three
+ * launches).  ckpt as ss_fwd_ckpt writes it (an input here: it must not overlap an output); N
+ * must be 16.  Other arguments, errors and results as ss_bwd.
  */
 ss_status ss_bwd_ckpt(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
                       const void* B, const void* C, const float* D, const void* z, const float* h0,

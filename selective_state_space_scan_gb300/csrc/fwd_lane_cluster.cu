@@ -1,19 +1,19 @@
 // The single-launch time split of the lane kernel (one CTA per (channel tile, time segment),
 // the segments of a tile forming one thread-block cluster that exchanges segment summaries
 // through distributed shared memory): fp32 and bf16 I/O, 16 states at 4 lanes per channel,
-// 32-channel tiles, TMA-fed.
+// 32-channel tiles, TMA-fed; with or without the backward's checkpoints.
 #include "fwd_launch_common.cuh"
 #include "ss_fwd_lane.cuh"
 
 namespace selscan {
 namespace {
 
-template <typename TIO>
+template <typename TIO, bool CKPT>
 cudaError_t launch_cluster_t(const FwdParams& p, const FwdMaps& m, cudaStream_t stream, int cluster,
                              int* fit) {
     using Cfg = LaneCfg<TIO, 16, 4, 32, kLaneT, kLaneStages, lane_minb(4, 32), 0, false, true>;
     static_assert(Cfg::SMEM_BYTES <= 227 * 1024, "shared memory budget exceeded");
-    auto kern = ss_fwd_lane_kernel<Cfg, true, false, false, true>;
+    auto kern = ss_fwd_lane_kernel<Cfg, true, false, false, true, CKPT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -47,8 +47,12 @@ cudaError_t launch_cluster_t(const FwdParams& p, const FwdMaps& m, cudaStream_t 
 cudaError_t launch_fwd_lane_cluster(bool bf16, const FwdParams& p, const FwdMaps& m, cudaStream_t stream, int cluster,
                                     int* fit) {
     if (cluster < 2 || cluster > 8) return cudaErrorInvalidValue;
-    return bf16 ? launch_cluster_t<__nv_bfloat16>(p, m, stream, cluster, fit)
-                : launch_cluster_t<float>(p, m, stream, cluster, fit);
+    // with FwdParams::ckpt: the instantiation that also writes the backward's checkpoints
+    if (p.ckpt)
+        return bf16 ? launch_cluster_t<__nv_bfloat16, true>(p, m, stream, cluster, fit)
+                    : launch_cluster_t<float, true>(p, m, stream, cluster, fit);
+    return bf16 ? launch_cluster_t<__nv_bfloat16, false>(p, m, stream, cluster, fit)
+                : launch_cluster_t<float, false>(p, m, stream, cluster, fit);
 }
 
 }  // namespace selscan

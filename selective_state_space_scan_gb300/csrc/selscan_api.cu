@@ -601,10 +601,13 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     if (!v.balanced && plan.nseg < 2 && v.family == kFamLane && fl <= 0) v.lpc = per_tile_lpc(batch, Dm, v.ns);
     v.w32 = v.balanced && balanced_w32(batch, Dm, v.es);
     if (ckpt) {
-        // the checkpoint-writing kernel: one CTA per tile, 4 lanes per channel, TMA-fed tiles
+        // the checkpoint-writing kernels (TMA-fed, 4 lanes per channel): the single-launch time split
+        // where it applies (below), else one CTA per tile
         if (!tma || lti) return SS_ERR_UNSUPPORTED;
-        v.family = kFamLane;
-        v.lpc = 4;
+        if (v.family != kFamSeg) {
+            v.family = kFamLane;
+            v.lpc = 4;
+        }
         v.balanced = false;
         v.w32 = false;
         v.ckpt = true;
@@ -625,6 +628,10 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
             v.lpc = 4;
             v.cluster = cs;
         }
+    }
+    if (ckpt && v.family == kFamSeg) {   // no cluster split for these sizes: one CTA per tile
+        v.family = kFamLane;
+        v.lpc = 4;
     }
     if (tma) {
         const FwdGeom g0 = fwd_geometry(v);

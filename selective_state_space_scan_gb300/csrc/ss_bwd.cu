@@ -300,10 +300,12 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
             phase ^= 1u;
         }
     };
-    const bool pass1 = LOCAL || !p.ckpt_given;
+    // with the forward's checkpoints there is no forward pass here (the time split's local launch
+    // then sums Δ during its adjoint sweep instead)
+    const bool pass1 = !p.ckpt_given;
     if (TMA && tid == 0) {
         if (pass1) issue(c0, kStFwd);
-        else issue(c1 - 1, kStFull);             // pass 2 starts from the last chunk
+        else issue(c1 - 1, LOCAL ? kStLam : kStFull);   // pass 2 starts from the last chunk
     }
 
     float2 A2[2], An[2];                         // A·log2(e) and A = -exp(A_log), state pairs
@@ -378,8 +380,10 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
         __syncthreads();                         // the chunk's arrays are no longer read
     }
     if constexpr (LOCAL) {
-        if (seg + 1 < p.nseg) store_quad(p.h_slots + (seg + 1) * count, h);
-        if (j == 0 && d_ok) p.dsum[seg * static_cast<int64_t>(p.batch) * p.Dm + row] = dsum;
+        if (pass1) {
+            if (seg + 1 < p.nseg) store_quad(p.h_slots + (seg + 1) * count, h);
+            if (j == 0 && d_ok) p.dsum[seg * static_cast<int64_t>(p.batch) * p.Dm + row] = dsum;
+        }
     }
 
     // ---- pass 2: reverse
@@ -401,6 +405,7 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
                 const float dyh = sm[Cfg::OFF_DYH + r * kBW + cw];
                 const float4 Cv = *reinterpret_cast<const float4*>(&sm[Cfg::OFF_C + r * NS + n0]);
                 const float2 C2[2] = {f2(Cv.x, Cv.y), f2(Cv.z, Cv.w)};
+                if (!pass1) dsum += del;
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const float2 e = mul2(f2(del), A2[q]);
@@ -410,6 +415,7 @@ ss_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
             __syncthreads();
         }
         if (seg > 0) store_quad(p.m_slots + (seg - 1) * count, mu);
+        if (!pass1 && j == 0 && d_ok) p.dsum[seg * static_cast<int64_t>(p.batch) * p.Dm + row] = dsum;
         return;
     }
     float2 dA[2] = {f2(0.f), f2(0.f)};
@@ -776,7 +782,7 @@ static ss_status bwd_impl(const void* u, const void* delta_raw, const float* del
     p.h0 = h0; p.dy = dy; p.dlast = dlast; p.du = du; p.ddelta = ddelta_raw; p.dz = dz; p.dB = dB; p.dC = dC;
     p.dA_log = dA_log; p.dD = dD; p.dbias = ddelta_bias; p.dh0 = dh0;
     p.ckpt = static_cast<float*>(workspace);
-    if (ckpt_in && plan.nseg == 1) {              // the forward's checkpoints: no pass 1
+    if (ckpt_in) {                                // the forward's checkpoints: no pass 1
         p.ckpt = const_cast<float*>(ckpt_in);
         p.ckpt_given = 1;
     }
@@ -821,11 +827,13 @@ static ss_status bwd_impl(const void* u, const void* delta_raw, const float* del
         e = bf16 ? launch_bwd<__nv_bfloat16, true>(p, maps, ns, tma, stream)
                  : launch_bwd<float, true>(p, maps, ns, tma, stream);
         if (e != cudaSuccess) return SS_ERR_CUDA;
-        FwdParams fp;
-        std::memset(&fp, 0, sizeof(fp));
-        fp.A_log = A_log; fp.h0 = h0; fp.seg_slots = p.h_slots; fp.seg_dsum = p.dsum;
-        fp.batch = p.batch; fp.Dm = p.Dm; fp.N = p.N; fp.nseg = p.nseg;
-        if (launch_fwd_carry(fp, stream) != cudaSuccess) return SS_ERR_CUDA;
+        if (!p.ckpt_given) {                     // (the checkpoints hold the entering states)
+            FwdParams fp;
+            std::memset(&fp, 0, sizeof(fp));
+            fp.A_log = A_log; fp.h0 = h0; fp.seg_slots = p.h_slots; fp.seg_dsum = p.dsum;
+            fp.batch = p.batch; fp.Dm = p.Dm; fp.N = p.N; fp.nseg = p.nseg;
+            if (launch_fwd_carry(fp, stream) != cudaSuccess) return SS_ERR_CUDA;
+        }
         const int64_t count = batch * Dm * N;
         ss_bwd_carry_kernel<<<static_cast<unsigned>((count + 255) / 256), 256, 0, stream>>>(
             A_log, dlast, p.m_slots, p.dsum, batch * Dm, p.Dm, p.N, p.nseg);
@@ -836,8 +844,6 @@ static ss_status bwd_impl(const void* u, const void* delta_raw, const float* del
     return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
-// Internal test hook (not in the public header): -1 automatic time split, 0 (or 1) never,
-// n >= 2 always with up to n segments.  Returns the previous setting.
 extern "C" ss_status ss_bwd(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
                             const void* B, const void* C, const float* D, const void* z, const float* h0,
                             const void* dy, const float* dlast, void* du, void* ddelta_raw, void* dz,
@@ -859,6 +865,8 @@ extern "C" ss_status ss_bwd_ckpt(const void* u, const void* delta_raw, const flo
                     dD, ddelta_bias, dh0, batch, L, Dm, N, strides, workspace, workspace_bytes, stream, ckpt);
 }
 
+// Internal test hook (not in the public header): -1 automatic time split, 0 (or 1) never,
+// n >= 2 always with up to n segments.  Returns the previous setting.
 extern "C" int ss__force_bwd_nseg(int n) { return g_force_bwd_nseg.exchange(n < 0 ? -1 : n <= 1 ? 0 : n); }
 
 // Internal test hook (not in the public header): -1 automatic, 0 plain-load staging, 1 TMA

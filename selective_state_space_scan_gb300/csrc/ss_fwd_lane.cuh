@@ -257,14 +257,15 @@ __device__ __forceinline__ void wait_published(const unsigned int* flag, unsigne
 // memory; after a cluster barrier it reads the summaries of ranks 0 .. r-1 from their shared
 // memory and composes the state entering its segment, H_0 = h0, H_{s+1} = 2^(A'·ΣΔ_s)·H_s + end_s;
 // then it folds the segment again from that state with every output.
-// CKPT: also write the backward pass's checkpoints (FwdParams::ckpt), one CTA per 32-channel tile.
+// CKPT: also write the backward pass's checkpoints (FwdParams::ckpt): one CTA per 32-channel tile,
+// or (CLUSTER) from the full fold of each time segment.
 template <class Cfg, bool USE_TMA, bool STATE_ONLY = false, bool LTI = false, bool CLUSTER = false, bool CKPT = false>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
 ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     static_assert(!Cfg::BCF32 || (USE_TMA && !LTI), "widened B/C tiles come by TMA");
     static_assert(!CLUSTER || (USE_TMA && !STATE_ONLY && !LTI && Cfg::DTR == 0), "the cluster split is TMA-fed");
     static_assert(!CKPT || (Cfg::NS == 16 && Cfg::W == 32 && Cfg::LPC > 1 && Cfg::G * Cfg::LPC % 16 == 0 &&
-                            !STATE_ONLY && !CLUSTER && Cfg::DTR == 0),
+                            !STATE_ONLY && Cfg::DTR == 0),
                   "checkpoints: 16 states, 32-channel tiles, sub-blocks of whole 16-step pieces");
     using TIO = typename Cfg::TIO;
     constexpr int LPC = Cfg::LPC, CPW = Cfg::CPW, NS = Cfg::NS, QPL = Cfg::QPL, T = Cfg::T;

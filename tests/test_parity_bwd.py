@@ -10,7 +10,7 @@ import oracle
 import selective_state_space_scan_gb300 as ss
 from selective_state_space_scan_gb300 import synth
 
-from helpers import BF16_REL_L2, f32dev, rel_l2, to_dev, to_host
+from helpers import BF16_REL_L2, assert_fwd_close, f32dev, rel_l2, to_dev, to_host
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -313,9 +313,9 @@ def test_bwd_sums_at_4_byte_offsets(N):
     assert torch.isnan(bc[0]) and torch.isnan(bc[n + 1:n + 5]).all() and torch.isnan(bc[2 * n + 5:]).all()
 
 
-def run_with_ckpt(w, a, dy, h0, dlast):
-    """ss_fwd_ckpt (y checked against ss_fwd: the same arithmetic, bit for bit) then ss_bwd with its
-    checkpoints."""
+def run_with_ckpt(w, a, dy, h0, dlast, rows=None):
+    """ss_fwd_ckpt (its y and last_state against the oracle's forward, on `rows` channels when
+    given) then ss_bwd with its checkpoints."""
     io = w.io
     t = dict(u=to_dev(a["u"], io), delta_raw=to_dev(a["delta_raw"], io), z=to_dev(a["z"], io),
              B=to_dev(a["B"], io), C=to_dev(a["C"], io))
@@ -324,18 +324,13 @@ def run_with_ckpt(w, a, dy, h0, dlast):
     last = torch.empty((w.batch, w.Dm, w.N), device="cuda")
     y, ckpt = ss.ss_fwd_ckpt(t["u"], t["delta_raw"], prm["delta_bias"], prm["A_log"], t["B"], t["C"], prm["D"],
                              t["z"], last_state=last, h0=h0d)
-    lib = ss.lib()
-    lib.ss__force_fwd_variant.argtypes = [ctypes.c_int] * 3
-    lib.ss__force_fwd_variant(0, 4, -1)           # ss_fwd on the same per-tile, 4-lane configuration
-    try:
-        last2 = torch.empty_like(last)
-        y2 = ss.ss_fwd(t["u"], t["delta_raw"], prm["delta_bias"], prm["A_log"], t["B"], t["C"], prm["D"], t["z"],
-                       last_state=last2, h0=h0d)
-        torch.cuda.synchronize()
-    finally:
-        lib.ss__force_fwd_variant(-1, 0, -1)
-    np.testing.assert_array_equal(to_host(y), to_host(y2))
-    np.testing.assert_array_equal(to_host(last), to_host(last2))
+    torch.cuda.synchronize()
+    ry, rl, mag = oracle.ss_fwd(a["u"], a["delta_raw"], a["delta_bias"], a["A_log"], a["B"], a["C"], a["D"], a["z"],
+                                h0=None if h0 is None else h0.astype(np.float64), rows=rows)
+    yh, lh = to_host(y), to_host(last)
+    if rows is not None:
+        yh, lh = yh[0][:, rows].T, lh[0][rows]
+    assert_fwd_close(io, yh, ry, mag, lh, rl, what=f"ss_fwd_ckpt {w.name}")
     g = ss.ss_bwd(to_dev(dy, io), t["u"], t["delta_raw"], prm["delta_bias"], prm["A_log"], t["B"], t["C"], prm["D"],
                   t["z"], h0=h0d, dlast=f32dev(dlast), ckpt=ckpt)
     torch.cuda.synchronize()
@@ -366,7 +361,7 @@ def test_bwd_with_forward_checkpoints_130m_equals_plain_backward():
     w = synth.config("mamba130m")
     a = w.arrays
     dy = synth.rng_for(71, 12).standard_normal((w.batch, w.L, w.Dm), dtype=np.float32)
-    got = run_with_ckpt(w, a, dy, None, None)
+    got = run_with_ckpt(w, a, dy, None, None, rows=np.sort(np.random.default_rng(7).choice(w.Dm, 16, replace=False)))
     plain = run(w, a, dy, None, None)
     for k in ELEMENTWISE:
         if got[k] is not None:
@@ -377,7 +372,8 @@ def test_bwd_with_forward_checkpoints_130m_equals_plain_backward():
 
 def test_fwd_ckpt_refusals_and_split_backward():
     """N other than 16 is refused by both calls; a backward that takes the time split (one long
-    row) ignores the checkpoints and still gives the oracle's gradients."""
+    row) takes its segments' entering states from the checkpoints (the local launch sweeps only
+    the adjoint, summing Δ as it goes) and gives the oracle's gradients."""
     w5, a5, dy5, _, _ = problem(1, 40, 32, 8, seed=72, with_h0=False, with_dlast=False)
     assert ss.lib().ss_fwd_ckpt_size(1, 40, 32, 8) == 0
     with pytest.raises(ss.SelscanError):
@@ -390,3 +386,23 @@ def test_fwd_ckpt_refusals_and_split_backward():
     ref = reference(a, dy, h0, dlast)
     for k in ELEMENTWISE:
         assert rel_l2(got[k], ref[k]) <= GRAD_REL_L2, k
+    for k in SUMS:
+        assert rel_l2(got[k], ref[k]) <= SUM_REL_L2, k
+
+
+@pytest.mark.parametrize("nseg", [2, 5])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bwd_split_with_forward_checkpoints(nseg, io):
+    """The time split from the forward's checkpoints at forced segment counts, ragged length,
+    with h0 and dlast, against the oracle."""
+    w, a, dy, h0, dlast = problem(2, 1500, 96, 16, io=io, seed=74 + nseg)
+    with splitting(nseg):
+        got = run_with_ckpt(w, a, dy, h0, dlast)
+    ref = reference(a, dy, h0, dlast)
+    for k in ELEMENTWISE + SUMS:
+        e = rel_l2(got[k], ref[k])
+        if io == "bf16":
+            tol = BF16_REL_L2 if k in ("du", "ddelta_raw", "dz") else BF16_SUM_REL_L2
+        else:
+            tol = GRAD_REL_L2 if k in ELEMENTWISE else SUM_REL_L2
+        assert e <= tol, f"split {nseg} {io} {k}: rel-L2 {e:.3e} > {tol}"
