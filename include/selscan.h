@@ -335,20 +335,23 @@ ss_status ss_bwd(const void* u, const void* delta_raw, const float* delta_bias, 
 size_t ss_bwd_workspace_size(int64_t batch, int64_t L, int64_t Dm, int64_t N);
 
 /*
- * Forward pass for training: ss_fwd_h0's results (no workspace: one CTA per 32-channel tile at 4
- * lanes per channel, or, when the tiles alone cannot fill the GPU, ss_fwd's single-launch
- * cluster split of the sequence) and, besides, the checkpoints ss_bwd_ckpt reads instead of
- * refolding the sequence in a first pass of its own: the state entering every 16th step,
+ * Forward pass for training: ss_fwd_h0's results and, besides, the checkpoints ss_bwd_ckpt reads
+ * instead of refolding the sequence in a first pass of its own.  Schedule: with a workspace
+ * (ss_fwd_workspace_size bytes) the balanced one of ss_fwd_ws where it applies (bf16 I/O, or fp32
+ * with at least two 32-channel tiles per SM); when the tiles alone cannot fill the GPU, ss_fwd's
+ * single-launch cluster split (no workspace used); else one CTA per 32-channel tile at 4 lanes
+ * per channel.  The checkpoints are the state entering every 16th step,
  *   ckpt   [batch·ceil(Dm/32)][ceil(L/32)][2][32][16] fp32, device memory, 16-byte aligned,
  *          ss_fwd_ckpt_size(...) bytes; entries past the last step hold the final state.
  * N must be 16 and every tensor must allow TMA-fed tiles (16-byte aligned bases and strides);
  * time-invariant B/C (step stride 0) are not taken: SS_ERR_UNSUPPORTED.  ckpt must not overlap
- * any other argument.  Other arguments, errors and results as ss_fwd_h0.
+ * any other argument; the workspace (NULL allowed) as for ss_fwd_ws.  Other arguments, errors and
+ * results as ss_fwd_h0.
  */
 ss_status ss_fwd_ckpt(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
                       const void* B, const void* C, const float* D, const void* z, void* y, float* last_state,
                       const float* h0, float* ckpt, int64_t batch, int64_t L, int64_t Dm, int64_t N,
-                      const ss_fwd_strides* strides, void* stream);
+                      const ss_fwd_strides* strides, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of ss_fwd_ckpt's checkpoints (0: sizes invalid, empty, or N other than 16). */
 size_t ss_fwd_ckpt_size(int64_t batch, int64_t L, int64_t Dm, int64_t N);

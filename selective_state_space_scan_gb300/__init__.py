@@ -80,7 +80,7 @@ def lib() -> ctypes.CDLL:
         L.ss_bwd_workspace_size.restype = ctypes.c_size_t
         L.ss_bwd_ckpt.argtypes = [vp] * 21 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp, ctypes.c_size_t, vp]
         L.ss_bwd_ckpt.restype = ctypes.c_int
-        L.ss_fwd_ckpt.argtypes = [vp] * 12 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp]
+        L.ss_fwd_ckpt.argtypes = [vp] * 12 + [i64] * 4 + [ctypes.POINTER(FwdStrides), vp, ctypes.c_size_t, vp]
         L.ss_fwd_ckpt.restype = ctypes.c_int
         L.ss_fwd_ckpt_size.argtypes = [i64] * 4
         L.ss_fwd_ckpt_size.restype = ctypes.c_size_t
@@ -399,9 +399,10 @@ def ss_conv1d(x, weight, bias=None, out=None, window_in=None, window_out=None, s
 
 
 def ss_fwd_ckpt(u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, last_state=None, h0=None,
-                ckpt=None, stream=None):
+                ckpt=None, stream=None, workspace=True):
     """Forward pass for training through the C ABI (ss_fwd_ckpt): y as ss_fwd, and the
     checkpoints ss_bwd(..., ckpt=...) reads instead of a first pass of its own (16 states only).
+    workspace=True passes the per-(device, stream) cached workspace (the balanced schedule).
     Returns (y, ckpt); ckpt (float32, allocated when None) has ss_fwd_ckpt_size bytes."""
     import torch
     batch, L, Dm = u.shape
@@ -417,9 +418,14 @@ def ss_fwd_ckpt(u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, l
     s = FwdStrides(io, u.stride(0), u.stride(1), delta_raw.stride(0), delta_raw.stride(1),
                    z.stride(0) if z is not None else 0, z.stride(1) if z is not None else 0,
                    y.stride(0), y.stride(1), B.stride(0), B.stride(1), C.stride(0), C.stride(1))
+    ws_ptr, ws_len = None, 0
+    wbytes = ss_fwd_workspace_size(batch, L, Dm, N, io) if workspace and batch * L * Dm > 0 else 0
+    if wbytes:
+        ws = workspace_for(u.device, stream, wbytes)
+        ws_ptr, ws_len = ws.data_ptr(), ws.numel()
     st = lib().ss_fwd_ckpt(_ptr(u), _ptr(delta_raw), _ptr(delta_bias), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D),
                            _ptr(z), _ptr(y), _ptr(last_state), _ptr(h0), _ptr(ckpt), batch, L, Dm, N, ctypes.byref(s),
-                           _stream_handle(stream))
+                           ws_ptr, ws_len, _stream_handle(stream))
     if st != 0:
         raise SelscanError(st, "ss_fwd_ckpt")
     return y, ckpt

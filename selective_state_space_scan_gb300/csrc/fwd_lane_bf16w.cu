@@ -9,6 +9,14 @@ template <int LPC>
 static cudaError_t launch_bf16w_lpc(const FwdVariant& v, const FwdParams& p, const FwdMaps& m, cudaStream_t s,
                                     int* mg) {
     using T = __nv_bfloat16;
+    if (v.ckpt) {       // the balanced schedule that also writes the backward's checkpoints
+        if constexpr (LPC == 2) {
+            if (!v.balanced || v.state_only) return cudaErrorInvalidValue;
+            return launch_lane_cfg<T, 16, LPC, true, true, false, false, true, false, true>(p, m, s, mg);
+        } else {
+            return cudaErrorInvalidValue;
+        }
+    }
     if (v.state_only) return launch_lane_cfg<T, 16, LPC, false, true, true, false, true>(p, m, s, mg);
     if (v.balanced) return launch_lane_cfg<T, 16, LPC, true, true, false, false, true>(p, m, s, mg);
     return launch_lane_cfg<T, 16, LPC, false, true, false, false, true>(p, m, s, mg);

@@ -22,9 +22,13 @@ cudaError_t launch_lane_cfg(const FwdParams& p, const FwdMaps& m, cudaStream_t s
 template <typename TIO, int NS, int LPC>
 cudaError_t launch_lane_v(const FwdVariant& v, const FwdParams& p, const FwdMaps& m, cudaStream_t s, int* mg) {
     if (v.ckpt) {
-        // per tile, TMA-fed, 16 states at 4 lanes per channel only
+        // TMA-fed, 16 states at 4 lanes per channel on 32-channel tiles: per tile, or balanced
         if constexpr (NS == 16 && LPC == 4) {
-            if (!v.tma || v.balanced || v.state_only || v.lti) return cudaErrorInvalidValue;
+            if (!v.tma || v.state_only || v.lti) return cudaErrorInvalidValue;
+            if (v.balanced) {
+                if (!v.w32) return cudaErrorInvalidValue;
+                return launch_lane_cfg<TIO, NS, LPC, true, true, false, false, false, true, true>(p, m, s, mg);
+            }
             return launch_lane_cfg<TIO, NS, LPC, false, true, false, false, false, false, true>(p, m, s, mg);
         } else {
             return cudaErrorInvalidValue;

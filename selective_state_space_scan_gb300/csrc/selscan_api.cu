@@ -423,7 +423,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     if (batch < 0 || L < 0 || Dm < 0) return SS_ERR_INVALID_ARG;
     if (N < 1 || N > 16) return SS_ERR_UNSUPPORTED;
     if (dtp && (R < 4 || R > kDtRankMax || R % 4 != 0)) return SS_ERR_UNSUPPORTED;
-    if (ckpt && (N != 16 || dtp || workspace)) return SS_ERR_UNSUPPORTED;   // checkpoints: 16 states, per tile
+    if (ckpt && (N != 16 || dtp)) return SS_ERR_UNSUPPORTED;   // checkpoints: 16 states
     ss_fwd_strides s;
     if (strides) {
         s = *strides;
@@ -573,7 +573,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     // from zero; carry pass; pass C: the fold from each segment's carried start).
     const int fs = g_force_nseg.load();
     SplitPlan plan;
-    if (workspace && tma && !lti && !dtp && fc == 0 && fs != 0 && (fs >= 2 || (v.family == kFamSeg && ff < 0))) {
+    if (workspace && !ckpt && tma && !lti && !dtp && fc == 0 && fs != 0 && (fs >= 2 || (v.family == kFamSeg && ff < 0))) {
         FwdVariant vs = v;
         vs.family = kFamLane;
         if (fl <= 0) vs.lpc = vs.ns / 4;
@@ -601,15 +601,19 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     if (!v.balanced && plan.nseg < 2 && v.family == kFamLane && fl <= 0) v.lpc = per_tile_lpc(batch, Dm, v.ns);
     v.w32 = v.balanced && balanced_w32(batch, Dm, v.es);
     if (ckpt) {
-        // the checkpoint-writing kernels (TMA-fed, 4 lanes per channel): the single-launch time split
-        // where it applies (below), else one CTA per tile
+        // the checkpoint-writing kernels (TMA-fed): the balanced schedule where a workspace allows it
+        // (bf16 with fp32 B/C tiles at 2 lanes per channel; fp32 on 32-channel tiles at 4), the
+        // single-launch time split for few tiles (below), else one CTA per tile at 4 lanes
         if (!tma || lti) return SS_ERR_UNSUPPORTED;
-        if (v.family != kFamSeg) {
-            v.family = kFamLane;
-            v.lpc = 4;
+        const bool bal_ok = v.balanced && ((bf16 && Bw && v.lpc == 2) || (!bf16 && v.w32 && v.lpc == 4));
+        if (!bal_ok) {
+            v.balanced = false;
+            v.w32 = false;
+            if (v.family != kFamSeg) {
+                v.family = kFamLane;
+                v.lpc = 4;
+            }
         }
-        v.balanced = false;
-        v.w32 = false;
         v.ckpt = true;
     }
     FwdMaps maps;
@@ -620,8 +624,8 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
     // tile form a cluster and exchange their segments' summaries through distributed shared
     // memory, so the split needs neither a workspace nor a second launch.
     int cluster_seg_chunks = 0;
-    if (!workspace && tma && !lti && !dtp && fc == 0 && v.ns == 16 && v.family == kFamSeg && (ff < 0 || ff == 2) &&
-        (fl <= 0 || fl == 4)) {
+    if ((!workspace || ckpt) && tma && !lti && !dtp && fc == 0 && v.ns == 16 && v.family == kFamSeg &&
+        (ff < 0 || ff == 2) && (fl <= 0 || fl == 4)) {
         const int cs = cluster_plan(bf16, batch, L, Dm, &cluster_seg_chunks);
         if (cs >= 2) {
             v.family = kFamLane;
@@ -808,10 +812,10 @@ ss_status ss_fwd_h0(const void* u, const void* delta_raw, const float* delta_bia
 ss_status ss_fwd_ckpt(const void* u, const void* delta_raw, const float* delta_bias, const float* A_log,
                       const void* B, const void* C, const float* D, const void* z, void* y, float* last_state,
                       const float* h0, float* ckpt, int64_t batch, int64_t L, int64_t Dm, int64_t N,
-                      const ss_fwd_strides* strides, void* stream) {
+                      const ss_fwd_strides* strides, void* workspace, size_t workspace_bytes, void* stream) {
     if (!ckpt && batch > 0 && L > 0 && Dm > 0) return SS_ERR_INVALID_ARG;
     return fwd_impl(u, delta_raw, delta_bias, A_log, B, C, D, z, y, last_state, h0, batch, L, Dm, N, strides,
-                    nullptr, 0, stream, nullptr, 0, ckpt);
+                    workspace, workspace_bytes, stream, nullptr, 0, ckpt);
 }
 
 size_t ss_fwd_ckpt_size(int64_t batch, int64_t L, int64_t Dm, int64_t N) {

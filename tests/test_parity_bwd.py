@@ -406,3 +406,33 @@ def test_bwd_split_with_forward_checkpoints(nseg, io):
         else:
             tol = GRAD_REL_L2 if k in ELEMENTWISE else SUM_REL_L2
         assert e <= tol, f"split {nseg} {io} {k}: rel-L2 {e:.3e} > {tol}"
+
+
+@pytest.mark.parametrize("io,batch", [("f32", 2), ("bf16", 4)])
+def test_bwd_ckpt_balanced_forward(io, batch):
+    """Enough tiles for ss_fwd_ckpt to take the balanced schedule with its workspace (fp32 on
+    32-channel tiles at 4 lanes, bf16 with fp32 B/C tiles at 2): y bit for bit ss_fwd's on the
+    same schedule, and the backward from its checkpoints against the oracle."""
+    w, a, dy, h0, dlast = problem(batch, 100, 4864, 16, io=io, seed=80 + batch)
+    t = dict(u=to_dev(a["u"], io), delta_raw=to_dev(a["delta_raw"], io), z=to_dev(a["z"], io),
+             B=to_dev(a["B"], io), C=to_dev(a["C"], io))
+    prm = dict(delta_bias=f32dev(a["delta_bias"]), A_log=f32dev(a["A_log"]), D=f32dev(a["D"]))
+    h0d = f32dev(h0)
+    y1 = ss.ss_fwd(t["u"], t["delta_raw"], prm["delta_bias"], prm["A_log"], t["B"], t["C"], prm["D"], t["z"],
+                   h0=h0d, workspace=True)
+    y2, ckpt = ss.ss_fwd_ckpt(t["u"], t["delta_raw"], prm["delta_bias"], prm["A_log"], t["B"], t["C"], prm["D"],
+                              t["z"], h0=h0d)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_host(y1), to_host(y2))
+    g = ss.ss_bwd(to_dev(dy, io), t["u"], t["delta_raw"], prm["delta_bias"], prm["A_log"], t["B"], t["C"], prm["D"],
+                  t["z"], h0=h0d, dlast=f32dev(dlast), ckpt=ckpt)
+    torch.cuda.synchronize()
+    got = {k: (None if v is None else to_host(v)) for k, v in g.items()}
+    ref = reference(a, dy, h0, dlast)
+    for k in ELEMENTWISE + SUMS:
+        e = rel_l2(got[k], ref[k])
+        if io == "bf16":
+            tol = BF16_REL_L2 if k in ("du", "ddelta_raw", "dz") else BF16_SUM_REL_L2
+        else:
+            tol = GRAD_REL_L2 if k in ELEMENTWISE else SUM_REL_L2
+        assert e <= tol, f"balanced ckpt {io} {k}: rel-L2 {e:.3e} > {tol}"
