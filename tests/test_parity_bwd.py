@@ -436,3 +436,35 @@ def test_bwd_ckpt_balanced_forward(io, batch):
         else:
             tol = GRAD_REL_L2 if k in ELEMENTWISE else SUM_REL_L2
         assert e <= tol, f"balanced ckpt {io} {k}: rel-L2 {e:.3e} > {tol}"
+
+
+def test_fwd_ckpt_argument_checks():
+    """ss_fwd_ckpt refuses time-invariant B/C and strides TMA cannot describe (no substitute
+    schedule), a missing or misaligned checkpoint buffer, and one that overlaps y."""
+    w, a, dy, h0, dlast = problem(2, 64, 64, 16, seed=90, with_h0=False, with_dlast=False)
+    t = {k: f32dev(v) for k, v in a.items() if v is not None}
+    need = ss.lib().ss_fwd_ckpt_size(2, 64, 64, 16)
+    assert need == 2 * 2 * 2 * 2 * 32 * 16 * 4
+    ck = torch.empty(need // 4 + 8, device="cuda")
+    call = lambda **kw: ss.ss_fwd_ckpt(kw.get("u", t["u"]), t["delta_raw"], t["delta_bias"], t["A_log"],
+                                       kw.get("B", t["B"]), kw.get("C", t["C"]), t["D"], t["z"], y=kw.get("y"),
+                                       ckpt=kw.get("ckpt", ck[: need // 4]), workspace=False)
+    call()
+    torch.cuda.synchronize()
+    with pytest.raises(ss.SelscanError):                      # B, C at step stride 0
+        call(B=t["B"][:, :1].expand(-1, 64, -1), C=t["C"][:, :1].expand(-1, 64, -1))
+    wide = torch.zeros((2, 64, 66), device="cuda")
+    wide[..., :64] = t["u"]
+    with pytest.raises(ss.SelscanError):                      # rows 264 bytes apart: no TMA
+        call(u=wide[..., :64])
+    with pytest.raises(ss.SelscanError):                      # 4 bytes off 16-byte alignment
+        call(ckpt=ck[1: 1 + need // 4])
+    yb = torch.empty(need // 4 + 2 * 64 * 64, device="cuda")
+    with pytest.raises(ss.SelscanError):                      # y over the checkpoints
+        call(y=yb[: 2 * 64 * 64].view(2, 64, 64), ckpt=yb[: need // 4])
+    lib = ss.lib()
+    s = ss.FwdStrides(ss.SS_F32, 64 * 64, 64, 64 * 64, 64, 64 * 64, 64, 64 * 64, 64, 64 * 16, 16, 64 * 16, 16)
+    y = torch.empty((2, 64, 64), device="cuda")
+    assert lib.ss_fwd_ckpt(t["u"].data_ptr(), t["delta_raw"].data_ptr(), None, t["A_log"].data_ptr(),
+                           t["B"].data_ptr(), t["C"].data_ptr(), None, None, y.data_ptr(), None, None, None,
+                           2, 64, 64, 16, ctypes.byref(s), None, 0, None) == 1    # no checkpoint buffer
