@@ -118,7 +118,10 @@ ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias,
  *     equal contiguous ranges, one per CTA the device can hold at once (a cooperative launch),
  *     so every SM gets the same amount of work; a range that starts inside a tile takes the
  *     state at its start from the CTA before it (the workspace holds one flag and one tile
- *     state per CTA).  Results are bitwise equal to ss_fwd's.
+ *     state per CTA).  Results are bitwise equal to the one-CTA-per-tile schedule's at the
+ *     same number of lanes per channel; ss_fwd may split a channel's states over more lanes
+ *     (it has fewer CTAs per SM to fill), which sums the C·h terms in another order, so the
+ *     two calls then agree up to rounding.
  *   - time-split (too few channel tiles, e.g. one long sequence): each sequence is cut into
  *     segments that run side by side.  A first pass folds every segment but the last from a
  *     zero state; a carry pass combines those end states left to right (the decay over a
