@@ -29,6 +29,7 @@ struct FwdVariant {
     int cluster = 0;     // > 0: the single-launch time split, segments per cluster
     bool w32 = false;    // balanced fp32 on 32-channel tiles (the per-tile kernel's own geometry)
     bool ckpt = false;   // per tile, LPC 4, 16 states: also write the backward's checkpoints
+    bool dx4 = false;    // balanced fp32 32-channel tiles at LPC 4: (Δ, Δ·u) through shared memory
 };
 
 struct FwdGeom {

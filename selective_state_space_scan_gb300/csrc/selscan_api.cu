@@ -353,6 +353,18 @@ bool balanced_w32(int64_t batch, int64_t Dm, int es) {
     return batch * ((Dm + 31) / 32) >= 2 * static_cast<int64_t>(sms);
 }
 
+// The balanced 32-channel fp32 schedule at 4 lanes per channel hands (Δ, Δ·u) over through shared
+// memory (the DX4 instantiation, two CTAs per SM) when the grid is two CTAs per SM anyway (fewer
+// than three tiles per SM); with more tiles the shuffle form keeps three CTAs per SM.
+bool balanced_dx4(const FwdVariant& v, int64_t batch, int64_t Dm) {
+    if (!v.w32 || v.lpc != 4 || v.es != 4 || v.ckpt) return false;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        return false;
+    return batch * ((Dm + 31) / 32) < 3 * static_cast<int64_t>(sms);
+}
+
 cudaError_t lane_max_grid(const FwdVariant& v, bool bf16, int* out) {
     FwdParams dummy;
     std::memset(&dummy, 0, sizeof(dummy));
@@ -600,6 +612,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
                  fc == 0 && g_force_balanced.load() != 0;
     if (!v.balanced && plan.nseg < 2 && v.family == kFamLane && fl <= 0) v.lpc = per_tile_lpc(batch, Dm, v.ns);
     v.w32 = v.balanced && balanced_w32(batch, Dm, v.es);
+    v.dx4 = !ckpt && balanced_dx4(v, batch, Dm);
     if (ckpt) {
         // the checkpoint-writing kernels (TMA-fed): the balanced schedule where a workspace allows it
         // (bf16 with fp32 B/C tiles at 2 lanes per channel; fp32 on 32-channel tiles at 4), the
@@ -656,6 +669,7 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         plan = SplitPlan();
         v.balanced = false;
         v.w32 = false;
+        v.dx4 = false;
     }
     const bool split = plan.nseg >= 2;
     v.bcf32 = Bw && tma && v.family == kFamLane && (v.balanced || split);
@@ -863,6 +877,7 @@ size_t fwd_ws_need(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_d
     v.tma = true;
     v.bcf32 = widen > 0;
     v.w32 = balanced_w32(batch, Dm, v.es);
+    v.dx4 = balanced_dx4(v, batch, Dm);
     const FwdGeom geo = fwd_geometry(v);
     const int64_t tiles = batch * ((Dm + geo.tile_channels - 1) / geo.tile_channels);
     int max_grid = 0;
@@ -1077,8 +1092,12 @@ int ss__fwd_plan(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dty
     if (!bal && !fl) v.lpc = per_tile_lpc(batch, Dm, v.ns);
     const bool wide = bal && widens_bc(io_dtype, N);
     const bool w32 = bal && balanced_w32(batch, Dm, io_dtype == SS_BF16 ? 2 : 4);
-    std::snprintf(buf, sizeof(buf), "ss_fwd_lane_kernel(lpc=%d%s%s%s)", v.lpc, bal ? ",balanced" : "",
-                  w32 ? ",32-channel tiles" : "", wide ? ",fp32 B/C" : "");
+    FwdVariant vd = v;
+    vd.w32 = w32;
+    vd.es = io_dtype == SS_BF16 ? 2 : 4;
+    const bool dx4 = balanced_dx4(vd, batch, Dm);
+    std::snprintf(buf, sizeof(buf), "ss_fwd_lane_kernel(lpc=%d%s%s%s%s)", v.lpc, bal ? ",balanced" : "",
+                  w32 ? ",32-channel tiles" : "", dx4 ? ",shared-memory hand-over" : "", wide ? ",fp32 B/C" : "");
     put(buf);
     return wide ? 2 : 1;                  // (the B/C widening pass,) the scan
 }

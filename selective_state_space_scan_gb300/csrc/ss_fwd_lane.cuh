@@ -53,8 +53,12 @@ namespace selscan {
 // make before the scan), so bf16 streams need no per-chunk widening in shared memory.
 // XCH: room for this CTA's segment summary (end state [W][NS] and Σ Δ [W]) that the CTAs of a
 // cluster read from each other (the single-launch time split).
+// DX4: at 4 lanes per channel (fp32), the prepared (Δ, Δ·u) go through shared memory as at 2
+// (see DXS); its rows take 16.5 KB a CTA, which leaves room for two CTAs per SM, so only the
+// balanced schedule on 32-channel tiles uses it, where the grid is two CTAs per SM anyway
+// (130m-shaped layer: 133.5 -> 129.7 us; one CTA per tile, which needs three per SM, 141 -> 168).
 template <typename TIO_, int NS_, int LPC_, int W_, int T_, int STAGES_, int MINB_, int DTR_ = 0, bool BCF32_ = false,
-          bool XCH_ = false>
+          bool XCH_ = false, bool DX4_ = false>
 struct LaneCfg {
     using TIO = TIO_;
     static constexpr int NS = NS_;            // states handled (4, 8 or 16; N <= NS)
@@ -102,7 +106,9 @@ struct LaneCfg {
     // read back two steps per 16-byte load, instead of two shuffles per step.  fp32 only: at 2
     // lanes per channel it measured 153 against 170 us on the 130m-shaped layer, while on the
     // 2.8b-shaped bf16 layer the shuffles were faster (694 against 724 us).
-    static constexpr bool DXS = LPC == 2 && ES == 4 && SS_DX_SMEM;
+    // (At 2 lanes with bf16 streams and fp32 B/C tiles it measured 701 against 667 us.)
+    static constexpr bool DXS = ES == 4 && ((LPC == 2 && SS_DX_SMEM) || (LPC == 4 && DX4_));
+    static constexpr int NDX = LPC > 1 ? LPC / 2 : 1;                     // 16-byte reads per group
     static constexpr int DX_PITCH = G * LPC + 2;                          // float2 per channel row
     static constexpr int AUX_DX = AUX_W + (DTR > 0 ? W * DTR * 4 : 0);
     static constexpr int AUX_XCH = AUX_DX + (DXS ? WARPS * CPW * DX_PITCH * 8 : 0);
@@ -114,6 +120,7 @@ struct LaneCfg {
     static_assert(T % LPC == 0 && T <= 256, "chunk must be whole groups and one TMA box");
     static_assert(DTR == 0 || ES == 4, "the folded projection is built for fp32 I/O");
     static_assert(!BCF32_ || (ES == 2 && DTR == 0), "widened B/C tiles serve bf16 streams");
+    static_assert(!DX4_ || (LPC == 4 && ES == 4), "the 4-lane shared-memory hand-over is built for fp32");
 };
 
 // A CTA's work in processing order: up to three runs of (tile, chunk) units.
@@ -594,21 +601,24 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                     // two FMA-pipe updates; about 1% faster than issuing them as one block first).
                     float2 an[LPC][QPL][2], bn[LPC][QPL][2];
                     // Δ and Δ·u of step kk of group g (dxq: the group's pairs when DXS)
-                    auto step_in = [&](int g, int kk, const float4& dxq, float& dk, float& uk) {
+                    auto step_in = [&](int g, int kk, const float4 (&dxq)[Cfg::NDX], float& dk, float& uk) {
                         if constexpr (LPC == 1) {
                             dk = dd[g];
                             uk = du[g];
                         } else if constexpr (Cfg::DXS) {
-                            dk = kk == 0 ? dxq.x : dxq.z;
-                            uk = kk == 0 ? dxq.y : dxq.w;
+                            dk = (kk & 1) == 0 ? dxq[kk >> 1].x : dxq[kk >> 1].z;
+                            uk = (kk & 1) == 0 ? dxq[kk >> 1].y : dxq[kk >> 1].w;
                         } else {
                             dk = __shfl_sync(0xffffffffu, dd[g], kk * CPW + c);
                             uk = __shfl_sync(0xffffffffu, du[g], kk * CPW + c);
                         }
                     };
                     auto prep = [&](int g, float2 (&a)[LPC][QPL][2], float2 (&bb)[LPC][QPL][2]) {
-                        float4 dxq = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if constexpr (Cfg::DXS) dxq = *reinterpret_cast<const float4*>(dxrow + g * LPC);
+                        float4 dxq[Cfg::NDX];
+#pragma unroll
+                        for (int x = 0; x < Cfg::NDX; ++x)
+                            dxq[x] = Cfg::DXS ? *reinterpret_cast<const float4*>(dxrow + g * LPC + 2 * x)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                         for (int kk = 0; kk < LPC; ++kk) {
                             float dk, uk;
@@ -704,8 +714,11 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                         } else {
                         const bool more = g + 1 < G;
                         const int gn = more ? g + 1 : g;
-                        float4 dxq = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if constexpr (Cfg::DXS) dxq = *reinterpret_cast<const float4*>(dxrow + gn * LPC);
+                        float4 dxq[Cfg::NDX];
+#pragma unroll
+                        for (int x = 0; x < Cfg::NDX; ++x)
+                            dxq[x] = Cfg::DXS ? *reinterpret_cast<const float4*>(dxrow + gn * LPC + 2 * x)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                         for (int kk = 0; kk < LPC; ++kk) {
                             float dk = 0.f, uk = 0.f;
