@@ -111,9 +111,13 @@ ss_status ss_fwd(const void* u, const void* delta_raw, const float* delta_bias,
 /*
  * Forward pass with a caller-provided workspace; same arguments and result as ss_fwd.
  *
- * ss_fwd runs one CTA per tile of channels over the whole sequence.  With a workspace, one of
- * two schedules of the same carry-across-chunks scan ("mamba-metal: Apple Silicon で Mamba を
- * 動かす", section "チャンク間 running prefix") runs instead:
+ * ss_fwd runs one CTA per tile of channels over the whole sequence; with more tiles than the GPU
+ * holds at once, clusters of CTAs instead split their tiles' chunks evenly, handing the state of
+ * a tile split between two CTAs over through the cluster's distributed shared memory (bitwise
+ * the same results), and with too few tiles to fill the GPU, the CTAs of a cluster fold the time
+ * segments of one tile (equal up to rounding).  With a workspace, one of two schedules of the
+ * same carry-across-chunks scan ("mamba-metal: Apple Silicon で Mamba を動かす", section
+ * "チャンク間 running prefix") runs instead:
  *   - balanced (enough channel tiles to fill the GPU): the (tile, chunk) work is split into
  *     equal contiguous ranges, one per CTA the device can hold at once (a cooperative launch),
  *     so every SM gets the same amount of work; a range that starts inside a tile takes the

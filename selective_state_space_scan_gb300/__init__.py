@@ -179,7 +179,9 @@ def ss_fwd(u, delta_raw, delta_bias, A_log, B, C, D=None, z=None, y=None, last_s
     ``last_state`` ([batch, Dm, N] float32, optional) are written.  Returns y.
     h0 ([batch, Dm, N] float32, optional) is the state before step 0 (ss_fwd_h0); it may be
     last_state itself.
-    workspace=False (default) runs one CTA per channel tile over the whole sequence (ss_fwd).
+    workspace=False (default) calls ss_fwd: one CTA per channel tile over the whole sequence, or,
+    with more tiles than the GPU holds at once, clusters of CTAs that split their tiles' work
+    evenly (the cluster-balanced schedule), or for few tiles the single-launch time split.
     workspace=True passes a workspace cached per (device, stream), which enables the balanced
     schedule (equal work per CTA) or, for few channel tiles, the time-split one (ss_fwd_ws).
     """

@@ -169,17 +169,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same with acquire at cluster scope, for a barrier that threads of other CTAs of the cluster
+// arrive on (their stores before arriving are visible once the phase is seen complete).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the barrier phase with the given parity.  Gives up after ~2^31 SM cycles
 // (about a second at GB300 clocks), records kErrWaitTimeout, and raises the block's
 // abort flag so that later waits return at once; the caller then finishes its loop
-// without blocking, so no thread is left waiting on a barrier.
+// without blocking, so no thread is left waiting on a barrier.  CLUSTER_SCOPE: arrivals come
+// from other CTAs of the cluster.
+template <bool CLUSTER_SCOPE = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort_flag,
                                                   unsigned int* err_word) {
+    auto try_wait = [&]() { return CLUSTER_SCOPE ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
     if (*abort_flag) return false;
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_wait()) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!try_wait()) {
         if (*abort_flag) return false;
         if (clock64() - t0 > (1ll << 31)) {
             *abort_flag = 1;
@@ -253,6 +269,17 @@ __device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
+}
+__device__ __forceinline__ void st_peer_f32x4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+// One arrival (release at cluster scope: this thread's earlier stores, to any CTA of the cluster,
+// become visible to a thread that then sees the phase complete) on an mbarrier in a peer's shared
+// memory, at the address peer_smem_addr gives.
+__device__ __forceinline__ void mbar_arrive_peer(uint32_t addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
 __device__ __forceinline__ float4 ld_peer_f32x4(uint32_t addr) {
     float4 v;

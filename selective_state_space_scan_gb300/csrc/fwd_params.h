@@ -34,6 +34,11 @@ struct FwdParams {
     unsigned int* ws_flag;   // [grid]
     unsigned int epoch;  // this call's nonzero tag
     int grid;            // CTAs in the launch (0: batch·tiles_per_batch)
+    // Cluster-balanced schedule (cbal > 0, no workspace): the grid is clusters of cbal CTAs; cluster
+    // q takes the whole tiles [T·q/Q, T·(q+1)/Q) of the T tiles (Q clusters) and splits their
+    // (tile, chunk) units into cbal equal contiguous ranges, one per CTA; a tile split between two
+    // CTAs of the cluster hands its state over through distributed shared memory.
+    int cbal;
     // Initial state h_{-1} [batch, Dm, N] contiguous (nullptr: zeros).
     const float* h0;
     // Checkpoints for the backward pass (the CKPT kernel, one CTA per 32-channel tile, 16 states):

@@ -30,6 +30,7 @@ struct FwdVariant {
     bool w32 = false;    // balanced fp32 on 32-channel tiles (the per-tile kernel's own geometry)
     bool ckpt = false;   // per tile, LPC 4, 16 states: also write the backward's checkpoints
     bool dx4 = false;    // balanced fp32 32-channel tiles at LPC 4: (Δ, Δ·u) through shared memory
+    int cbal = 0;        // > 0: the cluster-balanced schedule (no workspace), CTAs per cluster
 };
 
 struct FwdGeom {
@@ -69,6 +70,12 @@ cudaError_t launch_fwd_lane_dtp(const FwdVariant& v, const FwdParams& p, const F
 // and return in fit[0] how many such clusters can be resident at once and in fit[1] the CTAs per SM.
 cudaError_t launch_fwd_lane_cluster(bool bf16, const FwdParams& p, const FwdMaps& m, cudaStream_t stream, int cluster,
                                     int* fit = nullptr);
+// The cluster-balanced schedule (fwd_lane_cbal.cu): p.grid = Q × cluster CTAs in clusters of
+// `cluster` (2..8), p.cbal = cluster; bf16 at lpc 2 or fp32 at lpc 4; per_sm > 0 pads the shared
+// memory so that at most per_sm CTAs share an SM.  With `fit` non-null, launch nothing and return in
+// fit[0] how many such clusters can be resident at once and in fit[1] the CTAs per SM.
+cudaError_t launch_fwd_lane_cbal(bool bf16, int lpc, const FwdParams& p, const FwdMaps& m, cudaStream_t stream,
+                                 int cluster, int per_sm, int* fit = nullptr);
 // Test instantiations at other chunk lengths (fwd_lane_chunks.cu): whether v (with v.chunk set)
 // is one of them, and its launch.
 bool chunk_override_ok(const FwdVariant& v);

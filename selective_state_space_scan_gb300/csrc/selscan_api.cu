@@ -45,6 +45,10 @@ std::atomic<int> g_force_nseg{-1};
 // Test hook: steps per chunk of the lane kernel (0: its own 64; 16, 32 or 256: the test
 // instantiations of one configuration, per tile, which take no workspace schedule).
 std::atomic<int> g_force_chunk{0};
+// Test hook on the cluster-balanced schedule of ss_fwd without a workspace: -1 automatic (when one
+// CTA per tile would need more than one wave), 0 never, 2..8 always where it applies, with
+// clusters of that many CTAs.
+std::atomic<int> g_force_cbal{-1};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -262,6 +266,13 @@ int ss__force_balanced(int on) { return g_force_balanced.exchange(on ? 1 : 0); }
 // Internal test hook (see g_force_nseg); returns the previous setting.
 int ss__force_nseg(int n) { return g_force_nseg.exchange(n < 0 ? -1 : n == 1 ? 0 : n); }
 
+// Internal test hook (see g_force_cbal): -1 automatic, 0 never, 2..8 always with that cluster size;
+// returns the previous setting, or -2 for a value it does not take.
+int ss__force_cbal(int s) {
+    if (s < -1 || s == 1 || s > 8) return -2;
+    return g_force_cbal.exchange(s);
+}
+
 // Internal test hook (not part of the public header); see g_force_family.
 int ss__force_fwd_variant(int family, int lpc, int tma) {
     if (family < -1 || family > 2 || (lpc != 0 && lpc != 1 && lpc != 2 && lpc != 4) || tma < -1 || tma > 1)
@@ -356,6 +367,77 @@ bool balanced_w32(int64_t batch, int64_t Dm, int es) {
 // The balanced 32-channel fp32 schedule at 4 lanes per channel hands (Δ, Δ·u) over through shared
 // memory (the DX4 instantiation, two CTAs per SM) when the grid is two CTAs per SM anyway (fewer
 // than three tiles per SM); with more tiles the shuffle form keeps three CTAs per SM.
+cudaError_t lane_max_grid(const FwdVariant& v, bool bf16, int* out);
+
+// Cluster-balanced plan for tiles_total channel tiles of nch chunks: the cluster size S (8, 4 or
+// 2; force_s > 0: that one), the CTAs per SM K and the cluster count Q.  As in the balanced
+// schedule the grid is a whole number K of CTAs per SM (the CTAs an SM holds, at most tiles / SMs;
+// fewer tiles than SMs: one) with the shared memory padded so that no SM takes more; Q is at most
+// the clusters that then fit at once (a cluster stays within one GPC, so large clusters can leave
+// SMs idle) and at most tiles / S, so that every CTA's range spans at least one tile.  Of the sizes
+// that fit, the one with the fewest (tile, chunk) units on the busiest CTA,
+// ceil(ceil(tiles / Q) · nch / S).  False when none fits.
+bool cbal_plan(bool bf16, int lpc, int64_t tiles_total, int64_t nch, int force_s, int* S, int* K, int* Q) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        return false;
+    FwdParams dummy;
+    std::memset(&dummy, 0, sizeof(dummy));
+    FwdMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    int64_t best = -1;
+    for (int sz : {8, 4, 2}) {
+        if (force_s > 0 && sz != force_s) continue;
+        int fit[2] = {0, 0};
+        if (launch_fwd_lane_cbal(bf16, lpc, dummy, maps, nullptr, sz, 0, fit) != cudaSuccess || fit[1] <= 0) {
+            cudaGetLastError();
+            continue;
+        }
+        const int k = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(fit[1], tiles_total / sms)));
+        if (launch_fwd_lane_cbal(bf16, lpc, dummy, maps, nullptr, sz, k, fit) != cudaSuccess || fit[0] <= 0) {
+            cudaGetLastError();
+            continue;
+        }
+        const int64_t q = std::min<int64_t>(std::min<int64_t>(static_cast<int64_t>(k) * sms / sz, fit[0]),
+                                            tiles_total / sz);
+        if (q < 1) continue;
+        const int64_t cost = (((tiles_total + q - 1) / q) * nch + sz - 1) / sz;
+        if (best < 0 || cost < best) {
+            best = cost;
+            *S = sz;
+            *K = k;
+            *Q = static_cast<int>(q);
+        }
+    }
+    return best >= 0;
+}
+
+// Whether ss_fwd without a workspace takes the cluster-balanced schedule for a per-tile lane
+// variant v (TMA-fed, 16 states, one CTA per 32-channel tile): when the tiles are more than fit on
+// the GPU at once (g_force_cbal: never, or always with a given cluster size).  Sets the schedule's
+// lanes per channel (bf16 2, fp32 4; a forced lane count must be that one), S and Q.
+bool cbal_choice(const FwdVariant& v, bool bf16, int64_t batch, int64_t Dm, int64_t L, int forced_lpc, int* lpc,
+                 int* S, int* K, int* Q) {
+    const int fc = g_force_cbal.load();
+    if (fc == 0 || v.family != kFamLane || !v.tma || v.lti || v.dtp || v.ns != 16 || v.balanced || v.cluster > 0 ||
+        v.ckpt || v.chunk > 0)
+        return false;
+    const int want = bf16 ? 2 : 4;
+    if (forced_lpc > 0 && forced_lpc != want) return false;
+    const int64_t tiles_total = batch * ((Dm + 31) / 32);
+    const int64_t nch = (L + kLaneT - 1) / kLaneT;
+    if (nch > INT32_MAX || tiles_total > INT32_MAX) return false;
+    if (fc < 0) {
+        int cap = 0;
+        if (lane_max_grid(v, bf16, &cap) != cudaSuccess || cap <= 0) return false;
+        if (tiles_total <= cap) return false;   // one CTA per tile runs in one wave
+    }
+    if (!cbal_plan(bf16, want, tiles_total, nch, fc > 0 ? fc : 0, S, K, Q)) return false;
+    *lpc = want;
+    return true;
+}
+
 bool balanced_dx4(const FwdVariant& v, int64_t batch, int64_t Dm) {
     if (!v.w32 || v.lpc != 4 || v.es != 4 || v.ckpt) return false;
     int dev = 0, sms = 0;
@@ -672,6 +754,18 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         v.dx4 = false;
     }
     const bool split = plan.nseg >= 2;
+    // Cluster-balanced schedule: no workspace, and more channel tiles than one CTA per tile can
+    // run at once (a second wave would hold the rest).
+    int cbal_q = 0, cbal_k = 0;
+    if (!workspace && !split) {
+        int lpc_c = 0, s_c = 0, k_c = 0, q_c = 0;
+        if (cbal_choice(v, bf16, batch, Dm, L, fl, &lpc_c, &s_c, &k_c, &q_c)) {
+            v.lpc = lpc_c;
+            v.cbal = s_c;
+            cbal_k = k_c;
+            cbal_q = q_c;
+        }
+    }
     v.bcf32 = Bw && tma && v.family == kFamLane && (v.balanced || split);
     if (v.bcf32) {
         const int bh = fwd_geometry(v).chunk_steps;
@@ -771,6 +865,11 @@ ss_status fwd_impl(const void* u, const void* delta_raw, const float* delta_bias
         p.nseg = v.cluster;
         p.grid = static_cast<int>(batch * tiles * v.cluster);
         return cuda_status(launch_fwd_lane_cluster(bf16, p, maps, stream, v.cluster));
+    }
+    if (v.cbal > 0) {
+        p.cbal = v.cbal;
+        p.grid = cbal_q * v.cbal;
+        return cuda_status(launch_fwd_lane_cbal(bf16, v.lpc, p, maps, stream, v.cbal, cbal_k));
     }
     if (v.chunk > 0) {
         if (!chunk_override_ok(v)) return SS_ERR_UNSUPPORTED;
@@ -1090,6 +1189,17 @@ int ss__fwd_plan(int64_t batch, int64_t L, int64_t Dm, int64_t N, int32_t io_dty
     }
     const bool bal = with_ws && g_force_balanced.load() != 0;
     if (!bal && !fl) v.lpc = per_tile_lpc(batch, Dm, v.ns);
+    if (!with_ws && N == 16) {
+        FwdVariant vc = v;
+        vc.tma = true;
+        vc.es = io_dtype == SS_BF16 ? 2 : 4;
+        int lc = 0, sc = 0, kc = 0, qc = 0;
+        if (cbal_choice(vc, io_dtype == SS_BF16, batch, Dm, L, fl, &lc, &sc, &kc, &qc)) {
+            std::snprintf(buf, sizeof(buf), "ss_fwd_lane_kernel(lpc=%d,cluster-balanced,S=%d)", lc, sc);
+            put(buf);
+            return 1;
+        }
+    }
     const bool wide = bal && widens_bc(io_dtype, N);
     const bool w32 = bal && balanced_w32(batch, Dm, io_dtype == SS_BF16 ? 2 : 4);
     FwdVariant vd = v;

@@ -75,6 +75,7 @@ struct LaneCfg {
     static constexpr int QPL = SPL / 4;       // state quads per lane
     static constexpr int ES = sizeof(TIO);
     static constexpr bool BCF32 = BCF32_;
+    static constexpr bool XCH = XCH_;
     static constexpr int ES_BC = BCF32_ ? 4 : ES;             // bytes per staged B/C element
     static constexpr bool CONVERT_BC = ES_BC == 2;
     static constexpr int up128(int x) { return (x + 127) / 128 * 128; }
@@ -156,17 +157,27 @@ __device__ __forceinline__ LaneWork lane_work(const FwdParams& p, int tiles_tota
         w.n2 = cnt > 0 ? cnt : 0;
         return w;
     }
-    if (p.ws_flag == nullptr) {               // one whole tile per CTA
+    int64_t U, u0, u1, tbase = 0;
+    if (p.cbal > 0) {                         // cluster-balanced: this cluster's whole tiles, split S ways
+        const int S = p.cbal, Q = p.grid / p.cbal;
+        const int q = static_cast<int>(blockIdx.x) / S, r = static_cast<int>(cluster_ctarank());
+        tbase = static_cast<int64_t>(tiles_total) * q / Q;
+        U = (static_cast<int64_t>(tiles_total) * (q + 1) / Q - tbase) * nch;
+        u0 = U * r / S;
+        u1 = U * (r + 1) / S;
+    } else if (p.ws_flag == nullptr) {        // one whole tile per CTA
         w.t1 = blockIdx.x;
         w.n1 = nch;
         return w;
+    } else {
+        U = static_cast<int64_t>(tiles_total) * nch;
+        u0 = U * blockIdx.x / p.grid;
+        u1 = U * (blockIdx.x + 1) / p.grid;
     }
-    const int64_t U = static_cast<int64_t>(tiles_total) * nch;
-    const int64_t u0 = U * blockIdx.x / p.grid, u1 = U * (blockIdx.x + 1) / p.grid;
     if (u1 <= u0) return w;
-    const int tf = static_cast<int>(u0 / nch), cf = static_cast<int>(u0 % nch);
-    const int tl = static_cast<int>((u1 - 1) / nch), ce = static_cast<int>((u1 - 1) % nch) + 1;
-    if (tf == tl) {                           // the whole of one tile (the grid is <= tiles)
+    const int tf = static_cast<int>(tbase + u0 / nch), cf = static_cast<int>(u0 % nch);
+    const int tl = static_cast<int>(tbase + (u1 - 1) / nch), ce = static_cast<int>((u1 - 1) % nch) + 1;
+    if (tf == tl) {                           // the whole of one tile (a range spans at least one tile)
         w.t1 = tf;
         w.n1 = nch;
         return w;
@@ -266,11 +277,22 @@ __device__ __forceinline__ void wait_published(const unsigned int* flag, unsigne
 // then it folds the segment again from that state with every output.
 // CKPT: also write the backward pass's checkpoints (FwdParams::ckpt): one CTA per 32-channel tile,
 // or (CLUSTER) from the full fold of each time segment.
-template <class Cfg, bool USE_TMA, bool STATE_ONLY = false, bool LTI = false, bool CLUSTER = false, bool CKPT = false>
+// CBAL: the cluster-balanced schedule (FwdParams::cbal; no workspace).  The CTAs of a cluster split
+// its tiles' (tile, chunk) units into equal ranges as the balanced schedule does, and a tile split
+// between two of them is handed over through distributed shared memory: the CTA that folds the
+// head of the tile (its first piece) stores its final state into the exchange area of the next
+// CTA of the cluster and arrives on that CTA's hand-over mbarrier; the next CTA waits (bounded)
+// on it before the tail (its last piece).  Only neighbours wait for each other; cluster barriers
+// at the start (every hand-over mbarrier initialised) and the end (no CTA leaves while its
+// neighbour may still write to it) bracket the work.
+template <class Cfg, bool USE_TMA, bool STATE_ONLY = false, bool LTI = false, bool CLUSTER = false, bool CKPT = false,
+          bool CBAL = false>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
 ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
     static_assert(!Cfg::BCF32 || (USE_TMA && !LTI), "widened B/C tiles come by TMA");
     static_assert(!CLUSTER || (USE_TMA && !STATE_ONLY && !LTI && Cfg::DTR == 0), "the cluster split is TMA-fed");
+    static_assert(!CBAL || (USE_TMA && Cfg::XCH && !STATE_ONLY && !LTI && !CLUSTER && !CKPT && Cfg::DTR == 0),
+                  "the cluster-balanced schedule is TMA-fed and hands states over in the exchange area");
     static_assert(!CKPT || (Cfg::NS == 16 && Cfg::W == 32 && Cfg::LPC > 1 && Cfg::G * Cfg::LPC % 16 == 0 &&
                             !STATE_ONLY && Cfg::DTR == 0),
                   "checkpoints: 16 states, 32-channel tiles, sub-blocks of whole 16-step pieces");
@@ -324,6 +346,8 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
         for (int s = 0; s < STAGES; ++s) done[s] = 0;
         if (USE_TMA) {
             for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+            // the hand-over barrier: one arrival per thread of the previous CTA of the cluster
+            if (CBAL) mbar_init(reinterpret_cast<uint64_t*>(aux + Cfg::AUX_XCH + Cfg::W * NS * 4), Cfg::THREADS);
             mbar_fence_init();
             tma_prefetch_desc(&maps.u);
             tma_prefetch_desc(&maps.delta);
@@ -444,6 +468,18 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                       ((static_cast<int64_t>(c0 / p.seg_chunks) * p.batch + b) * p.Dm + d) * p.N;
             } else if (c0 == 0) {
                 if (p.h0) src = p.h0 + (static_cast<int64_t>(b) * p.Dm + d) * p.N;
+            } else if constexpr (CBAL) {
+                // the tail of a tile whose head the previous CTA of the cluster folded: its state,
+                // which that CTA stored into this CTA's exchange area before arriving
+                const float* xh = reinterpret_cast<const float*>(aux + Cfg::AUX_XCH);
+                mbar_wait_bounded<true>(reinterpret_cast<uint64_t*>(aux + Cfg::AUX_XCH + Cfg::W * NS * 4), 0u,
+                                        abort_flag, p.err);
+#pragma unroll
+                for (int qq = 0; qq < QPL; ++qq) {
+                    const float4 v = *reinterpret_cast<const float4*>(xh + cw * NS + n0 + 4 * qq);
+                    h[qq][0] = make_float2(v.x, v.y);
+                    h[qq][1] = make_float2(v.z, v.w);
+                }
             } else {
                 // balanced: the tail of a tile whose head the previous CTA folded
                 if (tid == 0) wait_published(p.ws_flag + blockIdx.x - 1, p.epoch, p.err);
@@ -843,6 +879,16 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
                         if (n0 + 4 * qq + q4 < p.N) out[n0 + 4 * qq + q4] = v[q4];
                 }
             }
+        } else if (CBAL && work.n0 > 0 && piece == 0) {
+            // the head of a tile the next CTA of the cluster finishes: the state into that CTA's
+            // exchange area, then one arrival per thread on its hand-over barrier
+            const float* xh = reinterpret_cast<const float*>(aux + Cfg::AUX_XCH);
+            const uint32_t next = cluster_ctarank() + 1;
+#pragma unroll
+            for (int qq = 0; qq < QPL; ++qq)
+                st_peer_f32x4(peer_smem_addr(xh + cw * NS + n0 + 4 * qq, next),
+                              make_float4(h[qq][0].x, h[qq][0].y, h[qq][1].x, h[qq][1].y));
+            mbar_arrive_peer(peer_smem_addr(aux + Cfg::AUX_XCH + Cfg::W * NS * 4, next));
         } else if (work.n0 > 0 && piece == 0) {
             float* dst = p.ws_state + (static_cast<int64_t>(blockIdx.x) * Cfg::W + cw) * NS + n0;
 #pragma unroll
@@ -902,6 +948,11 @@ ss_fwd_lane_kernel(const FwdParams p, const __grid_constant__ FwdMaps maps) {
             h[qq][1] = H[qq][1];
         }
         if (npieces > 0) run_piece(std::false_type{}, 0);
+    } else if constexpr (CBAL) {
+        // head (handed over at its end), whole tiles, tail (taken over at its start)
+        cluster_sync_all();                 // every CTA's hand-over barrier is initialised
+        for (int piece = 0; piece < npieces; ++piece) run_piece(std::false_type{}, piece);
+        cluster_sync_all();                 // no CTA leaves while its neighbour may still write to it
     } else {
         for (int piece = 0; piece < npieces; ++piece) run_piece(std::integral_constant<bool, STATE_ONLY>{}, piece);
     }

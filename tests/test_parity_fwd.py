@@ -279,6 +279,81 @@ def test_balanced_equals_per_tile(shape):
         assert_fwd_close(w.io, y2, ry, mag, l2, rlast, what="balanced")
 
 
+class ForceCbal:
+    """Pin the cluster-balanced schedule of ss_fwd without a workspace: -1 automatic, 0 never,
+    2..8 always where it applies, with that many CTAs per cluster."""
+    def __init__(self, s):
+        self.s = s
+
+    def __enter__(self):
+        f = ss.lib().ss__force_cbal
+        f.argtypes = [ctypes.c_int]
+        f.restype = ctypes.c_int
+        assert f(self.s) != -2
+
+    def __exit__(self, *exc):
+        ss.lib().ss__force_cbal(-1)
+
+
+def plan_name(w, with_ws):
+    plan = ss.lib().ss__fwd_plan
+    plan.restype = ctypes.c_int
+    plan.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int32, ctypes.c_int, ctypes.c_char_p, ctypes.c_int]
+    buf = ctypes.create_string_buffer(128)
+    plan(w.batch, w.L, w.Dm, w.N, ss.SS_BF16 if w.io == "bf16" else ss.SS_F32, 1 if with_ws else 0, buf, 128)
+    return buf.value.decode()
+
+
+@pytest.mark.parametrize("shape,S", [
+    (("mamba2p8b_bf16", None), -1),                  # automatic: more tiles than one wave holds
+    (("custom", (3, 515, 2000, 16, "bf16")), 8),     # ragged L and Dm, bf16 (2 lanes per channel)
+    (("custom", (3, 515, 2000, 16, "bf16")), 2),
+    (("custom", (6, 1000, 4096, 16, "f32")), 4),     # fp32 (4 lanes), tiles split mid-way
+    (("custom", (2, 130, 320, 16, "f32")), 8),       # 3 chunks a tile, ranges of 3 to 4 units
+], ids=["2.8b-auto", "ragged-bf16-S8", "ragged-bf16-S2", "f32-S4", "short-f32-S8"])
+def test_cluster_balanced_equals_per_tile(shape, S):
+    """ss_fwd without a workspace on the cluster-balanced schedule hands the state between the CTAs
+    of a cluster exactly: bitwise equal to one CTA per tile at the same lanes per channel."""
+    name, dims = shape
+    w = synth.config(name) if dims is None else synth.fwd_inputs(*dims[:4], io=dims[4], seed=24)
+    lpc = 2 if w.io == "bf16" else 4
+    with ForceCbal(0):
+        with ForceVariant(0, lpc, -1):
+            assert "cluster-balanced" not in plan_name(w, False)
+        y1, l1 = run_gpu(w, workspace=False, variant=(0, lpc, -1))
+    auto = S < 0                         # the library's own choice of schedule and lanes
+    with ForceCbal(S):
+        with ForceVariant(*((-1, 0, -1) if auto else (0, lpc, -1))):
+            assert f"lpc={lpc},cluster-balanced" in plan_name(w, False)
+        y2, l2 = run_gpu(w, workspace=False, variant=(-1, 0, -1) if auto else (0, lpc, -1))
+    np.testing.assert_array_equal(y1, y2)
+    np.testing.assert_array_equal(l1, l2)
+    if dims is not None and dims[0] * dims[1] * dims[2] < 3e6:
+        ry, rlast, mag = run_oracle(w)
+        assert_fwd_close(w.io, y2, ry, mag, l2, rlast, what="cluster-balanced")
+
+
+def test_cluster_balanced_with_h0():
+    """The initial state enters every tile's first chunk on the cluster-balanced schedule too."""
+    w = synth.fwd_inputs(2, 200, 352, 16, io="f32", seed=25)   # 22 tiles: clusters of 8 split 11
+    a = w.arrays
+    h0 = np.random.default_rng(25).standard_normal((w.batch, w.Dm, w.N)).astype(np.float32) * 0.5
+    outs = []
+    for s in (0, 8):
+        with ForceCbal(s), ForceVariant(0, 4, -1):
+            last = torch.full((w.batch, w.Dm, w.N), float("nan"), device="cuda")
+            y = ss.ss_fwd(to_dev(a["u"], "f32"), to_dev(a["delta_raw"], "f32"), f32dev(a["delta_bias"]),
+                          f32dev(a["A_log"]), to_dev(a["B"], "f32"), to_dev(a["C"], "f32"), f32dev(a["D"]),
+                          to_dev(a["z"], "f32"), last_state=last, workspace=False, h0=f32dev(h0))
+            torch.cuda.synchronize()
+            outs.append((to_host(y), to_host(last)))
+    np.testing.assert_array_equal(outs[0][0], outs[1][0])
+    np.testing.assert_array_equal(outs[0][1], outs[1][1])
+    ry, rlast, mag = oracle.ss_fwd(a["u"], a["delta_raw"], a["delta_bias"], a["A_log"], a["B"], a["C"], a["D"],
+                                   a["z"], h0=h0)
+    assert_fwd_close("f32", outs[1][0], ry, mag, outs[1][1], rlast, what="cluster-balanced h0")
+
+
 def test_balanced_repeated_calls_reuse_workspace():
     """Consecutive calls reuse one workspace: each call's epoch keeps stale hand-overs out."""
     w = synth.fwd_inputs(6, 1000, 4096, 16, seed=22)
