@@ -382,6 +382,28 @@ bool cbal_plan(bool bf16, int lpc, int64_t tiles_total, int64_t nch, int force_s
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         sms <= 0)
         return false;
+    // the occupancy queries cost some microseconds a call: plans are kept per device and shape
+    struct Entry {
+        int dev, lpc, force_s;
+        bool bf16;
+        int64_t tiles, nch;
+        int S, K, Q;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (const Entry& e : cache)
+            if (e.dev == dev && e.lpc == lpc && e.force_s == force_s && e.bf16 == bf16 && e.tiles == tiles_total &&
+                e.nch == nch) {
+                if (e.S <= 0) return false;
+                *S = e.S;
+                *K = e.K;
+                *Q = e.Q;
+                return true;
+            }
+    }
+    int bs = 0, bk = 0, bq = 0;
     FwdParams dummy;
     std::memset(&dummy, 0, sizeof(dummy));
     FwdMaps maps;
@@ -405,12 +427,21 @@ bool cbal_plan(bool bf16, int lpc, int64_t tiles_total, int64_t nch, int force_s
         const int64_t cost = (((tiles_total + q - 1) / q) * nch + sz - 1) / sz;
         if (best < 0 || cost < best) {
             best = cost;
-            *S = sz;
-            *K = k;
-            *Q = static_cast<int>(q);
+            bs = sz;
+            bk = k;
+            bq = static_cast<int>(q);
         }
     }
-    return best >= 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (cache.size() >= 64) cache.clear();
+        cache.push_back(Entry{dev, lpc, force_s, bf16, tiles_total, nch, best >= 0 ? bs : 0, bk, bq});
+    }
+    if (best < 0) return false;
+    *S = bs;
+    *K = bk;
+    *Q = bq;
+    return true;
 }
 
 // Whether ss_fwd without a workspace takes the cluster-balanced schedule for a per-tile lane
