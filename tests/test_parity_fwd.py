@@ -333,6 +333,26 @@ def test_cluster_balanced_equals_per_tile(shape, S):
         assert_fwd_close(w.io, y2, ry, mag, l2, rlast, what="cluster-balanced")
 
 
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("flags", ["no_z", "none"])
+def test_cluster_balanced_optional_inputs(io, flags):
+    """No gate (and no D or bias): the same hand-overs with the z tile left out, bitwise equal to one
+    CTA per tile and within tolerance of the oracle."""
+    kw = dict(with_z=False, with_D=flags != "none", with_bias=flags != "none")
+    w = synth.fwd_inputs(2, 150, 352, 16, io=io, seed=26, **kw)   # 22 tiles of 3 chunks
+    lpc = 2 if io == "bf16" else 4
+    with ForceCbal(0):
+        y1, l1 = run_gpu(w, workspace=False, variant=(0, lpc, -1))
+    with ForceCbal(4):
+        with ForceVariant(0, lpc, -1):
+            assert "cluster-balanced,S=4" in plan_name(w, False)
+        y2, l2 = run_gpu(w, workspace=False, variant=(0, lpc, -1))
+    np.testing.assert_array_equal(y1, y2)
+    np.testing.assert_array_equal(l1, l2)
+    ry, rlast, mag = run_oracle(w)
+    assert_fwd_close(io, y2, ry, mag, l2, rlast, what=f"cluster-balanced {flags}")
+
+
 def test_cluster_balanced_with_h0():
     """The initial state enters every tile's first chunk on the cluster-balanced schedule too."""
     w = synth.fwd_inputs(2, 200, 352, 16, io="f32", seed=25)   # 22 tiles: clusters of 8 split 11
